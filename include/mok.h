@@ -1,0 +1,230 @@
+/*
+ * mok.h — C ABI of libmok: a single-GPU (GB300, sm_103a) implementation of
+ * the deterministic routed-plus-shared SwiGLU mixture-of-experts layer that
+ * the Mixture-of-Kittens (MoK) pages describe.
+ *
+ * Sources (page title, section):
+ *   [MoKEd]  "Mixture-of-Kittens: a deterministic MoE megakernel for NVL72
+ *            racks" — "The two API layers and the schedule object": the
+ *            schedule is built once from the routing, before any kernel runs,
+ *            and the same object feeds forward and backward; a workspace holds
+ *            scratch.  "Tuning the five hyperparameters before production":
+ *            minibatch_size, schedule_capacity_multiplier, MXFP8 weights
+ *            prequantised by a separate mxfp8_quantize.  "Where MoK is the
+ *            wrong tool": top-k experts int64 [tokens, topk], router weights
+ *            float32, the router is outside the library.
+ *   [MoKDoc] "nemo_automodel.components.moe.mok_experts" — _MoKRuntime.forward
+ *            (x bf16 [tokens, hidden], router weights fp32 [tokens, topk],
+ *            top experts int64, shared gate/up [I_s, H], shared down [H, I_s],
+ *            routed gate/up [E, I, H], routed down [E, H, I], all contiguous
+ *            bf16; returns y bf16 [tokens, hidden] plus an opaque schedule and
+ *            context) and _MoKRuntime.backward (gradients for x, the router
+ *            weights, the three routed and the three shared weights).
+ *
+ * Conventions for every call:
+ *   - Every pointer is a DEVICE pointer unless stated otherwise; every buffer
+ *     is contiguous, row-major and 16-byte aligned.  bf16 values are passed as
+ *     uint16_t bit patterns.
+ *   - The library allocates nothing.  The caller owns every buffer; the
+ *     *_bytes() queries say how large each caller-provided region must be.
+ *   - Work is enqueued on `stream` (a cudaStream_t, NULL = legacy default
+ *     stream) and returns without synchronising.  Only mok_schedule_status()
+ *     and mok_ctx_status() synchronise.
+ *   - Host-visible argument errors return a status code and enqueue nothing.
+ *     Errors found on the device (an expert id out of range, a bounded wait
+ *     that gave up) are recorded in a device status word and read back with
+ *     mok_schedule_status() / mok_ctx_status(); kernels that follow a failed
+ *     schedule do no work.
+ *   - mok_last_error() returns a message for the last failing call of the
+ *     calling thread.
+ *   - Loading the library creates no CUDA context.
+ *   - Only sm_103a devices are supported (MOK_ERR_UNSUPPORTED otherwise).
+ */
+#ifndef MOK_H
+#define MOK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int mok_status_t;
+
+#define MOK_OK               0
+#define MOK_ERR_INVALID_ARG  1  /* bad size, NULL or misaligned pointer, short buffer */
+#define MOK_ERR_INDEX        2  /* an expert id outside [0, E) */
+#define MOK_ERR_CAPACITY     3  /* reserved: the capacity split never drops rows */
+#define MOK_ERR_UNSUPPORTED  4  /* not an sm_103a device, or a shape outside the kernels' contract */
+#define MOK_ERR_TIMEOUT      5  /* a bounded device-side wait gave up */
+#define MOK_ERR_CUDA         6  /* a CUDA runtime call failed */
+
+#define MOK_TILE_ROWS 128       /* each expert's row range is padded to this */
+#define MOK_MX_BLOCK  32        /* MXFP8: one E8M0 scale per 1x32 block along K */
+
+#define MOK_MODE_BF16       0   /* forward and backward in bf16, fp32 accumulate */
+#define MOK_MODE_MXFP8_FWD  1   /* forward GEMMs on MXFP8 operands, backward in bf16 */
+
+/* Debug flags (mok_config_t.debug_flags). */
+#define MOK_DEBUG_DROP_ACC_SIGNAL 1  /* the first forward GEMM withholds one
+                                        accumulator-ready signal, so a bounded
+                                        wait must expire and the context must
+                                        report MOK_ERR_TIMEOUT (tests only) */
+
+/* Per-call knobs ([MoKEd] "Tuning the five hyperparameters before
+ * production").  minibatch_size (0 = T) sets the order in which the
+ * persistent GEMMs visit work (waves of tokens); it never changes a result
+ * bit. */
+typedef struct {
+  int mode;            /* MOK_MODE_* */
+  int minibatch_size;  /* tokens per wave of the persistent pipeline; 0 = T */
+  int debug_flags;     /* MOK_DEBUG_*; 0 in production */
+  int reserved;        /* must be 0 */
+} mok_config_t;
+
+/* The dispatch/combine schedule ([MoKEd] "The two API layers and the
+ * schedule object").  All arrays live in the caller's schedule buffer.
+ * Flat routed row f = t*k + j.  Rows of expert e occupy schedule rows
+ * [row0[e], row0[e] + cnt[e]) in ascending f; each expert's range is padded
+ * to a multiple of 128 rows; padding rows and unused entries hold -1. */
+typedef struct {
+  int T, k, E;
+  int max_tiles;          /* floor((T*k + 127*E) / 128): bound on tiles */
+  int32_t* cnt;           /* [E]   rows per expert */
+  int32_t* row0;          /* [E+1] exclusive scan of the padded counts; row0[E] = P */
+  int32_t* row_src;       /* [max_tiles*128] schedule row -> f, or -1 */
+  int32_t* slot_row;      /* [T*k] f -> schedule row */
+  int32_t* tile_expert;   /* [max_tiles] expert of each 128-row tile, or -1 */
+  int32_t* tile_row0;     /* [max_tiles] first schedule row of the tile, or -1 */
+  int32_t* tile_rows;     /* [max_tiles] valid rows in the tile (1..128), or -1 */
+  int32_t* header;        /* [8] num_tiles, P, status, num_primary, 0... */
+  int32_t* scratch;       /* internal: per-chunk histograms */
+} mok_schedule_t;
+
+/* Layer weights, [MoKDoc] _MoKRuntime.forward layouts.  The shared expert is
+ * optional (I_s == 0 and NULL pointers).  In MOK_MODE_MXFP8_FWD the MXFP8
+ * copies (codes uint8 row-major like the bf16 tensor, scales uint8 E8M0
+ * [rows][K/32]) made by mok_mxfp8_quantize along each tensor's K axis
+ * (gate/up: H; down: I or I_s) are required as well; the backward always
+ * uses the bf16 tensors. */
+typedef struct {
+  int E, H, I, I_s;
+  const uint16_t* w_gate;    /* [E][I][H] */
+  const uint16_t* w_up;      /* [E][I][H] */
+  const uint16_t* w_down;    /* [E][H][I] */
+  const uint16_t* ws_gate;   /* [I_s][H] or NULL */
+  const uint16_t* ws_up;     /* [I_s][H] or NULL */
+  const uint16_t* ws_down;   /* [H][I_s] or NULL */
+  const uint8_t* mx_gate;  const uint8_t* mx_gate_sc;   /* [E][I][H], [E][I][H/32] */
+  const uint8_t* mx_up;    const uint8_t* mx_up_sc;     /* [E][I][H], [E][I][H/32] */
+  const uint8_t* mx_down;  const uint8_t* mx_down_sc;   /* [E][H][I], [E][H][I/32] */
+  const uint8_t* mxs_gate; const uint8_t* mxs_gate_sc;  /* [I_s][H], [I_s][H/32] */
+  const uint8_t* mxs_up;   const uint8_t* mxs_up_sc;    /* [I_s][H], [I_s][H/32] */
+  const uint8_t* mxs_down; const uint8_t* mxs_down_sc;  /* [H][I_s], [H][I_s/32] */
+} mok_weights_t;
+
+/* Forward context: activations saved for the backward plus forward scratch,
+ * all inside the caller's context buffer ([MoKDoc] _MoKRuntime.forward
+ * returns an opaque context that _MoKRuntime.backward consumes). */
+typedef struct {
+  int T, k, E, H, I, I_s, mode, max_tiles;
+  uint16_t* gu;       /* [max_tiles*128][2I] gate | up pre-activations per schedule row (saved) */
+  uint16_t* h;        /* [max_tiles*128][I]  SwiGLU output, bf16 mode (scratch) */
+  uint8_t*  hq;       /* [max_tiles*128][I]  SwiGLU output E4M3 codes, MXFP8 mode (scratch) */
+  uint8_t*  hq_sc;    /* [max_tiles*128][I/32] its E8M0 scales */
+  uint16_t* slots;    /* [T*k][H] router-weighted expert outputs (scratch) */
+  uint16_t* gu_s;     /* [T][2 I_s] shared gate | up (saved) */
+  uint16_t* h_s;      /* [T][I_s] shared SwiGLU output, bf16 mode (scratch) */
+  uint8_t*  hq_s;     /* [T][I_s] shared SwiGLU output codes, MXFP8 mode */
+  uint8_t*  hq_s_sc;  /* [T][I_s/32] */
+  uint16_t* shared_out; /* [T][H] shared expert output (scratch) */
+  uint8_t*  xq;       /* [T][H] x codes, MXFP8 mode (scratch) */
+  uint8_t*  xq_sc;    /* [T][H/32] */
+  int32_t*  status;   /* device status word: MOK_OK or the first device error */
+} mok_ctx_t;
+
+/* Weight gradients (bf16, same layouts as the weights; shared ones NULL when
+ * the layer has no shared expert). */
+typedef struct {
+  uint16_t* d_w_gate;   /* [E][I][H] */
+  uint16_t* d_w_up;     /* [E][I][H] */
+  uint16_t* d_w_down;   /* [E][H][I] */
+  uint16_t* d_ws_gate;  /* [I_s][H] or NULL */
+  uint16_t* d_ws_up;    /* [I_s][H] or NULL */
+  uint16_t* d_ws_down;  /* [H][I_s] or NULL */
+} mok_weight_grads_t;
+
+/* ---- version / errors --------------------------------------------------- */
+int mok_version(void);
+const char* mok_last_error(void);
+
+/* ---- schedule ([MoKEd] "The two API layers and the schedule object") ----
+ * Bytes of the device buffer mok_schedule() carves its arrays from. */
+size_t mok_schedule_bytes(int T, int k, int E);
+
+/* Build the schedule for top_experts (device int64 [T][k]) over E experts.
+ * capacity_multiplier (>= 0, finite) sets the per-expert tile budget
+ * ceil(ceil(c*T)/128) of the static work table ([MoKEd] "Tuning the five
+ * hyperparameters before production": the worst-case fraction of tokens on
+ * one expert); tiles beyond it go to an overflow list that follows the
+ * primary list.  It changes the order of the tile list only, never a row or a
+ * result.  `out` (host struct) receives pointers into `buf`.  An id outside
+ * [0, E) sets status MOK_ERR_INDEX in header[2] and num_tiles = 0.
+ * Limits: 1 <= k <= 64, 1 <= E <= 1024, T*k < 2^31. */
+mok_status_t mok_schedule(const int64_t* top_experts, int T, int k, int E,
+                          float capacity_multiplier, void* buf, size_t bytes,
+                          mok_schedule_t* out, void* stream);
+
+/* Synchronise `stream`'s work on the schedule and read its header.  Any of the
+ * host output pointers may be NULL. */
+mok_status_t mok_schedule_status(const mok_schedule_t* sched, int* status,
+                                 int* num_tiles, int* P);
+
+/* ---- MXFP8 quantiser ([MoKEd] "Tuning the five hyperparameters before
+ * production": weights are prequantised by a separate mxfp8_quantize) ----
+ * x bf16 [rows][K] -> codes E4M3 [rows][K], scales E8M0 [rows][K/32].  Per
+ * 1x32 block: s = smallest integer with amax <= 448 * 2^s (clamped to
+ * [-127, 127]; s = 0 for an all-zero block), scale code s + 127, element code
+ * = E4M3 round-to-nearest-even of v / 2^s with saturation; a value that
+ * rounds to zero keeps its sign.  Inputs must be finite.  K % 32 == 0. */
+mok_status_t mok_mxfp8_quantize(const uint16_t* x, int64_t rows, int K,
+                                uint8_t* codes, uint8_t* scales, void* stream);
+
+/* ---- forward ([MoKDoc] _MoKRuntime.forward) -----------------------------
+ * y[t] = S(x[t]) + sum_j w[t,j] * F_{e[t,j]}(x[t]),
+ * F_e(v) = W_down[e] (silu(W_gate[e] v) * (W_up[e] v)), S the same with the
+ * shared weights.  Deterministic: every output element is summed in a fixed
+ * order (shared term, then j ascending) with no floating-point atomics.
+ * Shape contract: H % 128 == 0, I % 128 == 0, I_s % 128 == 0, T >= 1.
+ * x bf16 [T][H]; router_w fp32 [T][k]; y bf16 [T][H].  The context buffer
+ * (mok_ctx_bytes) must stay alive and unmodified until mok_backward. */
+size_t mok_ctx_bytes(int T, int k, int E, int H, int I, int I_s, int mode);
+mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x,
+                         const float* router_w, const mok_schedule_t* sched,
+                         const mok_weights_t* w, uint16_t* y, void* ctx_buf,
+                         size_t ctx_bytes, mok_ctx_t* ctx, void* stream);
+
+/* Synchronise and read the context's device status word. */
+mok_status_t mok_ctx_status(const mok_ctx_t* ctx, int* status);
+
+/* ---- backward ([MoKDoc] _MoKRuntime.backward) ---------------------------
+ * Exact gradients of the forward given dy = dL/dy (bf16 [T][H]); in MXFP8
+ * mode the derivative treats the quantisers as the identity and is taken at
+ * the saved gate/up pre-activations.  x and router_w are the forward's
+ * inputs.  Outputs: dx bf16 [T][H], d_router_w fp32 [T][k] (= <dy[t],
+ * F_e(x[t])>), the six weight gradients.  Scratch comes from `ws`
+ * (mok_bwd_workspace_bytes).  Device errors land in ctx->status. */
+size_t mok_bwd_workspace_bytes(int T, int k, int E, int H, int I, int I_s);
+mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy,
+                          const uint16_t* x, const float* router_w,
+                          const mok_schedule_t* sched, const mok_ctx_t* ctx,
+                          const mok_weights_t* w, uint16_t* dx,
+                          float* d_router_w, const mok_weight_grads_t* grads,
+                          void* ws, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOK_H */

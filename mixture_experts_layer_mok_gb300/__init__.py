@@ -1,0 +1,212 @@
+"""MoK layer on GB300: Python binding of libmok (argument marshalling only).
+
+The calls mirror the C ABI in ``include/mok.h``:
+``schedule`` (built once from the routing), ``mxfp8_quantize`` (weights,
+ahead of time), ``forward`` -> (y, ctx), ``backward`` -> gradients.  PyTorch
+provides device memory and the stream; every step of the layer runs in the
+library's CUDA kernels.  The library is loaded on first use, never at import
+time, so importing this package creates no CUDA context.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib
+from ._lib import MokError  # noqa: F401
+
+__all__ = ["schedule", "mxfp8_quantize", "forward", "backward", "Schedule", "Weights", "Context",
+           "MokError", "quantize_weights"]
+
+
+def _ptr(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+def _need(t, dtype, shape, name):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name}: expected contiguous CUDA {dtype} {tuple(shape)}, got "
+                         f"{t.dtype} {tuple(t.shape)} on {t.device}")
+    return t
+
+
+@dataclass
+class Schedule:
+    """The dispatch/combine schedule; ``buf`` owns the device memory."""
+    T: int
+    k: int
+    E: int
+    buf: torch.Tensor
+    c: _lib.MokSchedule
+
+    def status(self):
+        st, nt, P = C.c_int32(), C.c_int32(), C.c_int32()
+        _lib.check(_lib.load().mok_schedule_status(C.byref(self.c), C.byref(st), C.byref(nt), C.byref(P)),
+                   "mok_schedule_status")
+        return st.value, nt.value, P.value
+
+    def arrays(self):
+        """Device int32 views of the schedule arrays (for inspection/tests)."""
+        base = self.buf.data_ptr()
+        mt = self.c.max_tiles
+        view = {}
+        for name, n in (("cnt", self.E), ("row0", self.E + 1), ("row_src", mt * 128),
+                        ("slot_row", self.T * self.k), ("tile_expert", mt), ("tile_row0", mt),
+                        ("tile_rows", mt), ("header", 8)):
+            off = getattr(self.c, name) - base
+            view[name] = self.buf[off: off + 4 * n].view(torch.int32)
+        return view
+
+
+@dataclass
+class Weights:
+    w_gate: torch.Tensor
+    w_up: torch.Tensor
+    w_down: torch.Tensor
+    ws_gate: torch.Tensor | None = None
+    ws_up: torch.Tensor | None = None
+    ws_down: torch.Tensor | None = None
+    mx: dict | None = None  # name -> (codes, scales) for MXFP8 mode
+
+    @property
+    def dims(self):
+        E, I, H = self.w_gate.shape
+        I_s = 0 if self.ws_gate is None else self.ws_gate.shape[0]
+        return E, H, I, I_s
+
+    def struct(self):
+        E, H, I, I_s = self.dims
+        _need(self.w_gate, torch.bfloat16, (E, I, H), "w_gate")
+        _need(self.w_up, torch.bfloat16, (E, I, H), "w_up")
+        _need(self.w_down, torch.bfloat16, (E, H, I), "w_down")
+        if I_s:
+            _need(self.ws_up, torch.bfloat16, (I_s, H), "ws_up")
+            _need(self.ws_down, torch.bfloat16, (H, I_s), "ws_down")
+        w = _lib.MokWeights(E=E, H=H, I=I, I_s=I_s)
+        w.w_gate, w.w_up, w.w_down = (t.data_ptr() for t in (self.w_gate, self.w_up, self.w_down))
+        if I_s:
+            w.ws_gate, w.ws_up, w.ws_down = (t.data_ptr() for t in (self.ws_gate, self.ws_up, self.ws_down))
+        if self.mx:
+            for name, (codes, scales) in self.mx.items():
+                setattr(w, "mx" + name, codes.data_ptr())
+                setattr(w, "mx" + name + "_sc", scales.data_ptr())
+        return w
+
+
+@dataclass
+class Context:
+    buf: torch.Tensor
+    c: _lib.MokCtx
+    mode: int
+
+    def status(self) -> int:
+        st = C.c_int32()
+        _lib.check(_lib.load().mok_ctx_status(C.byref(self.c), C.byref(st)), "mok_ctx_status")
+        return st.value
+
+
+def schedule(top_experts: torch.Tensor, E: int, capacity_multiplier: float = 0.5, stream=None) -> Schedule:
+    lib = _lib.load()
+    T, k = top_experts.shape
+    _need(top_experts, torch.int64, (T, k), "top_experts")
+    nbytes = lib.mok_schedule_bytes(T, k, E)
+    if nbytes == 0:
+        raise ValueError("invalid schedule shape")
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=top_experts.device)
+    c = _lib.MokSchedule()
+    _lib.check(lib.mok_schedule(_ptr(top_experts), T, k, E, float(capacity_multiplier), _ptr(buf), nbytes,
+                                C.byref(c), _stream(stream)), "mok_schedule")
+    return Schedule(T, k, E, buf, c)
+
+
+def mxfp8_quantize(x: torch.Tensor, stream=None):
+    """bf16 [..., K] -> (E4M3 codes uint8 [..., K], E8M0 scales uint8 [..., K/32])."""
+    lib = _lib.load()
+    if x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be contiguous CUDA bf16")
+    K = x.shape[-1]
+    rows = x.numel() // K if K else 0
+    codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    scales = torch.empty(tuple(x.shape[:-1]) + (K // 32,), dtype=torch.uint8, device=x.device)
+    _lib.check(lib.mok_mxfp8_quantize(_ptr(x), rows, K, _ptr(codes), _ptr(scales), _stream(stream)),
+               "mok_mxfp8_quantize")
+    return codes, scales
+
+
+def quantize_weights(w: Weights, stream=None) -> Weights:
+    """Prequantise every weight along its K axis for MXFP8 mode."""
+    mx = {"_gate": mxfp8_quantize(w.w_gate, stream), "_up": mxfp8_quantize(w.w_up, stream),
+          "_down": mxfp8_quantize(w.w_down, stream)}
+    if w.ws_gate is not None:
+        mx.update({"s_gate": mxfp8_quantize(w.ws_gate, stream), "s_up": mxfp8_quantize(w.ws_up, stream),
+                   "s_down": mxfp8_quantize(w.ws_down, stream)})
+    return Weights(w.w_gate, w.w_up, w.w_down, w.ws_gate, w.ws_up, w.ws_down, mx)
+
+
+def _config(mode, minibatch, debug):
+    return _lib.MokConfig(mode=mode, minibatch_size=minibatch, debug_flags=debug, reserved=0)
+
+
+def forward(x, router_w, sched: Schedule, weights: Weights, mode: str = "bf16", minibatch: int = 0,
+            debug: int = 0, out=None, ctx_buf=None, stream=None):
+    """y = layer(x); returns (y, Context).  ``mode`` is "bf16" or "mxfp8"."""
+    lib = _lib.load()
+    m = _lib.MOK_MODE_MXFP8_FWD if mode == "mxfp8" else _lib.MOK_MODE_BF16
+    E, H, I, I_s = weights.dims
+    T, k = sched.T, sched.k
+    _need(x, torch.bfloat16, (T, H), "x")
+    _need(router_w, torch.float32, (T, k), "router_w")
+    ws = weights.struct()
+    nbytes = lib.mok_ctx_bytes(T, k, E, H, I, I_s, m)
+    if nbytes == 0:
+        raise ValueError("shape outside the kernels' contract")
+    if ctx_buf is None or ctx_buf.numel() < nbytes:
+        ctx_buf = torch.empty(nbytes, dtype=torch.uint8, device=x.device)
+    y = out if out is not None else torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    c = _lib.MokCtx()
+    cfg = _config(m, minibatch, debug)
+    _lib.check(lib.mok_forward(C.byref(cfg), _ptr(x), _ptr(router_w), C.byref(sched.c), C.byref(ws), _ptr(y),
+                               _ptr(ctx_buf), ctx_buf.numel(), C.byref(c), _stream(stream)), "mok_forward")
+    return y, Context(ctx_buf, c, m)
+
+
+def backward(dy, x, router_w, sched: Schedule, ctx: Context, weights: Weights, minibatch: int = 0,
+             grads: dict | None = None, ws_buf=None, stream=None):
+    """Returns dict dx, d_router_w, d_w_gate, d_w_up, d_w_down (+ d_ws_* with a shared expert)."""
+    lib = _lib.load()
+    E, H, I, I_s = weights.dims
+    T, k = sched.T, sched.k
+    _need(dy, torch.bfloat16, (T, H), "dy")
+    _need(x, torch.bfloat16, (T, H), "x")
+    _need(router_w, torch.float32, (T, k), "router_w")
+    dev = dy.device
+    if grads is None:
+        grads = {"dx": torch.empty((T, H), dtype=torch.bfloat16, device=dev),
+                 "d_router_w": torch.empty((T, k), dtype=torch.float32, device=dev),
+                 "d_w_gate": torch.empty_like(weights.w_gate), "d_w_up": torch.empty_like(weights.w_up),
+                 "d_w_down": torch.empty_like(weights.w_down)}
+        if I_s:
+            grads.update(d_ws_gate=torch.empty_like(weights.ws_gate), d_ws_up=torch.empty_like(weights.ws_up),
+                         d_ws_down=torch.empty_like(weights.ws_down))
+    g = _lib.MokWeightGrads()
+    for name in ("d_w_gate", "d_w_up", "d_w_down", "d_ws_gate", "d_ws_up", "d_ws_down"):
+        if name in grads:
+            setattr(g, name, grads[name].data_ptr())
+    nbytes = lib.mok_bwd_workspace_bytes(T, k, E, H, I, I_s)
+    if ws_buf is None or ws_buf.numel() < nbytes:
+        ws_buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    cfg = _config(ctx.mode, minibatch, 0)
+    wsd = weights.struct()
+    _lib.check(lib.mok_backward(C.byref(cfg), _ptr(dy), _ptr(x), _ptr(router_w), C.byref(sched.c),
+                                C.byref(ctx.c), C.byref(wsd), _ptr(grads["dx"]), _ptr(grads["d_router_w"]),
+                                C.byref(g), _ptr(ws_buf), ws_buf.numel(), _stream(stream)), "mok_backward")
+    return grads

@@ -1,0 +1,649 @@
+// C ABI of libmok (declared in include/mok.h): argument checks, carving of the
+// caller's buffers, TMA descriptor encoding and the launch sequence of the
+// forward and backward passes.  No allocation happens here.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "../../include/mok.h"
+#include "gemm.cuh"
+#include "internal.h"
+
+using namespace mok;
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+mok_status_t fail(mok_status_t code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+#define MOK_CUDA(call)                                                                     \
+  do {                                                                                     \
+    cudaError_t e_ = (call);                                                               \
+    if (e_ != cudaSuccess)                                                                 \
+      return fail(MOK_ERR_CUDA, "%s failed: %s (%s:%d)", #call, cudaGetErrorString(e_),    \
+                  __FILE__, __LINE__);                                                     \
+  } while (0)
+
+// ---------------------------------------------------------------- device info
+struct DevInfo {
+  int checked = 0;
+  int ok = 0;
+  int num_sms = 0;
+};
+DevInfo g_dev[64];
+std::mutex g_dev_mu;
+
+mok_status_t device_info(int* num_sms) {
+  int dev = 0;
+  MOK_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return fail(MOK_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.checked) {
+    int major = 0, minor = 0, sms = 0;
+    MOK_CUDA(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev));
+    MOK_CUDA(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev));
+    MOK_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    d.ok = (major == 10 && minor == 3);
+    d.num_sms = sms;
+    d.checked = 1;
+  }
+  if (!d.ok) return fail(MOK_ERR_UNSUPPORTED, "libmok runs on sm_103 (GB300) devices only");
+  *num_sms = d.num_sms;
+  return MOK_OK;
+}
+
+// ---------------------------------------------------------------- TMA descriptors
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor [outer][inner] with a box of box_outer rows x 64 elements and
+// 128-byte swizzle; out-of-range elements read as zero.
+mok_status_t make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                      uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(MOK_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {64, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MOK_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for [%llu x %llu] box %u", (int)r,
+                (unsigned long long)outer, (unsigned long long)inner, box_outer);
+  return MOK_OK;
+}
+
+// ---------------------------------------------------------------- carving
+struct Carver {
+  uint8_t* base;
+  size_t off = 0;
+  explicit Carver(void* b) : base(static_cast<uint8_t*>(b)) {}
+  template <class T>
+  T* take(size_t count) {
+    off = (off + 255) & ~static_cast<size_t>(255);
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += count * sizeof(T);
+    return p;
+  }
+};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+long long max_tiles_of(int T, int k, int E) {
+  return (static_cast<long long>(T) * k + static_cast<long long>(kTileRows - 1) * E) / kTileRows;
+}
+
+struct SchedLayout {
+  int32_t *cnt, *row0, *row_src, *slot_row, *tile_expert, *tile_row0, *tile_rows, *header, *hist;
+};
+
+size_t carve_schedule(void* buf, int T, int k, int E, SchedLayout* L) {
+  const long long mt = max_tiles_of(T, k, E);
+  const long long n = static_cast<long long>(T) * k;
+  const long long nchunks = (n + kSchedChunk - 1) / kSchedChunk;
+  Carver c(buf);
+  L->cnt = c.take<int32_t>(E);
+  L->row0 = c.take<int32_t>(E + 1);
+  L->row_src = c.take<int32_t>(mt * kTileRows);
+  L->slot_row = c.take<int32_t>(n);
+  L->tile_expert = c.take<int32_t>(mt);
+  L->tile_row0 = c.take<int32_t>(mt);
+  L->tile_rows = c.take<int32_t>(mt);
+  L->header = c.take<int32_t>(8);
+  L->hist = c.take<int32_t>(nchunks * E);
+  return c.off + 256;
+}
+
+struct CtxExtra {  // forward scratch beyond the public context fields
+  uint16_t* h_deq;      // MXFP8 mode: bf16 expansion of h [max_rows][I]
+  uint16_t* hs_deq;     // [T][I_s]
+  uint16_t* x_deq;      // [T][H]
+  uint16_t* wg_deq;     // [E][I][H]
+  uint16_t* wu_deq;
+  uint16_t* wd_deq;     // [E][H][I]
+  uint16_t* wsg_deq;    // [I_s][H]
+  uint16_t* wsu_deq;
+  uint16_t* wsd_deq;    // [H][I_s]
+};
+
+size_t carve_ctx(void* buf, int T, int k, int E, int H, int I, int Is, int mode, mok_ctx_t* ctx,
+                 CtxExtra* X) {
+  const long long mr = max_tiles_of(T, k, E) * kTileRows;
+  const long long n = static_cast<long long>(T) * k;
+  const bool mx = (mode == MOK_MODE_MXFP8_FWD);
+  Carver c(buf);
+  memset(ctx, 0, sizeof(*ctx));
+  memset(X, 0, sizeof(*X));
+  ctx->T = T; ctx->k = k; ctx->E = E; ctx->H = H; ctx->I = I; ctx->I_s = Is; ctx->mode = mode;
+  ctx->max_tiles = static_cast<int>(max_tiles_of(T, k, E));
+  ctx->status = c.take<int32_t>(8);
+  ctx->gu = c.take<uint16_t>(mr * 2 * I);
+  ctx->slots = c.take<uint16_t>(n * H);
+  if (!mx) {
+    ctx->h = c.take<uint16_t>(mr * I);
+  } else {
+    ctx->hq = c.take<uint8_t>(mr * I);
+    ctx->hq_sc = c.take<uint8_t>(mr * I / 32);
+    ctx->xq = c.take<uint8_t>(static_cast<long long>(T) * H);
+    ctx->xq_sc = c.take<uint8_t>(static_cast<long long>(T) * H / 32);
+    X->h_deq = c.take<uint16_t>(mr * I);
+    X->x_deq = c.take<uint16_t>(static_cast<long long>(T) * H);
+    X->wg_deq = c.take<uint16_t>(static_cast<long long>(E) * I * H);
+    X->wu_deq = c.take<uint16_t>(static_cast<long long>(E) * I * H);
+    X->wd_deq = c.take<uint16_t>(static_cast<long long>(E) * H * I);
+  }
+  if (Is > 0) {
+    ctx->gu_s = c.take<uint16_t>(static_cast<long long>(T) * 2 * Is);
+    ctx->shared_out = c.take<uint16_t>(static_cast<long long>(T) * H);
+    if (!mx) {
+      ctx->h_s = c.take<uint16_t>(static_cast<long long>(T) * Is);
+    } else {
+      ctx->hq_s = c.take<uint8_t>(static_cast<long long>(T) * Is);
+      ctx->hq_s_sc = c.take<uint8_t>(static_cast<long long>(T) * Is / 32);
+      X->hs_deq = c.take<uint16_t>(static_cast<long long>(T) * Is);
+      X->wsg_deq = c.take<uint16_t>(static_cast<long long>(Is) * H);
+      X->wsu_deq = c.take<uint16_t>(static_cast<long long>(Is) * H);
+      X->wsd_deq = c.take<uint16_t>(static_cast<long long>(H) * Is);
+    }
+  }
+  return c.off + 256;
+}
+
+struct BwdLayout {
+  uint16_t *dgu, *hw, *dx_slots, *dgu_s, *hs, *dx_s;
+  float* dw_part;
+};
+
+int tile_n(int N) { return (N % 256 == 0) ? 256 : 128; }
+
+size_t carve_bwd(void* buf, int T, int k, int E, int H, int I, int Is, BwdLayout* L) {
+  const long long mr = max_tiles_of(T, k, E) * kTileRows;
+  const long long n = static_cast<long long>(T) * k;
+  Carver c(buf);
+  memset(L, 0, sizeof(*L));
+  L->dgu = c.take<uint16_t>(mr * 2 * I);
+  L->hw = c.take<uint16_t>(mr * I);
+  L->dw_part = c.take<float>(n * (I / tile_n(I)));
+  L->dx_slots = c.take<uint16_t>(n * H);
+  if (Is > 0) {
+    L->dgu_s = c.take<uint16_t>(static_cast<long long>(T) * 2 * Is);
+    L->hs = c.take<uint16_t>(static_cast<long long>(T) * Is);
+    L->dx_s = c.take<uint16_t>(static_cast<long long>(T) * H);
+  }
+  return c.off + 256;
+}
+
+mok_status_t check_shapes(int T, int k, int E, int H, int I, int Is) {
+  if (T < 1 || k < 1 || k > 64 || E < 1 || E > 1024)
+    return fail(MOK_ERR_INVALID_ARG, "need T >= 1, 1 <= k <= 64, 1 <= E <= 1024 (T=%d k=%d E=%d)", T, k, E);
+  if (static_cast<long long>(T) * k >= (1ll << 31) - 128ll * E)
+    return fail(MOK_ERR_INVALID_ARG, "T*k too large");
+  if (H < 128 || H % 128 || I < 128 || I % 128 || Is < 0 || Is % 128)
+    return fail(MOK_ERR_UNSUPPORTED, "need H, I (and I_s) multiples of 128 (H=%d I=%d I_s=%d)", H, I, Is);
+  return MOK_OK;
+}
+
+GemmParams base_params(const mok_schedule_t* s, int* status, int debug) {
+  GemmParams p;
+  memset(&p, 0, sizeof(p));
+  p.topk = s ? s->k : 1;
+  if (s) {
+    p.header = s->header;
+    p.tile_expert = s->tile_expert;
+    p.tile_row0 = s->tile_row0;
+    p.tile_rows = s->tile_rows;
+    p.row_src = s->row_src;
+    p.row0 = s->row0;
+    p.cnt = s->cnt;
+  }
+  p.status = status;
+  p.debug = debug;
+  p.E = 1;
+  return p;
+}
+
+__global__ void propagate_status_kernel(const int* header, int* status) {
+  if (header[2] != 0) atomicCAS(status, 0, header[2]);
+}
+
+}  // namespace
+
+// ===========================================================================
+extern "C" {
+
+int mok_version(void) { return 1; }
+
+const char* mok_last_error(void) { return g_err; }
+
+size_t mok_schedule_bytes(int T, int k, int E) {
+  if (T < 1 || k < 1 || E < 1) return 0;
+  SchedLayout L;
+  return carve_schedule(nullptr, T, k, E, &L);
+}
+
+mok_status_t mok_schedule(const int64_t* top_experts, int T, int k, int E, float capacity_multiplier,
+                          void* buf, size_t bytes, mok_schedule_t* out, void* stream) {
+  if (!top_experts || !buf || !out) return fail(MOK_ERR_INVALID_ARG, "NULL argument");
+  if (T < 1 || k < 1 || k > 64 || E < 1 || E > 1024)
+    return fail(MOK_ERR_INVALID_ARG, "need T >= 1, 1 <= k <= 64, 1 <= E <= 1024");
+  if (static_cast<long long>(T) * k >= (1ll << 31) - 128ll * E)
+    return fail(MOK_ERR_INVALID_ARG, "T*k too large");
+  if (!std::isfinite(capacity_multiplier) || capacity_multiplier < 0.f)
+    return fail(MOK_ERR_INVALID_ARG, "capacity_multiplier must be finite and >= 0");
+  if (!aligned16(top_experts) || !aligned16(buf)) return fail(MOK_ERR_INVALID_ARG, "misaligned pointer");
+  if (bytes < mok_schedule_bytes(T, k, E)) return fail(MOK_ERR_INVALID_ARG, "schedule buffer too small");
+  int sms = 0;
+  mok_status_t st = device_info(&sms);
+  if (st) return st;
+  SchedLayout L;
+  carve_schedule(buf, T, k, E, &L);
+  const long long mt = max_tiles_of(T, k, E);
+  // per-expert tile budget, decided in double precision
+  const double rows = std::ceil(static_cast<double>(capacity_multiplier) * static_cast<double>(T));
+  double capd = std::ceil(rows / kTileRows);
+  if (capd > static_cast<double>(mt)) capd = static_cast<double>(mt);
+  const int cap = static_cast<int>(capd);
+  MOK_CUDA(launch_schedule(top_experts, T, k, E, cap, static_cast<int>(mt), L.hist, L.cnt, L.row0,
+                           L.row_src, L.slot_row, L.tile_expert, L.tile_row0, L.tile_rows, L.header,
+                           static_cast<cudaStream_t>(stream)));
+  out->T = T; out->k = k; out->E = E; out->max_tiles = static_cast<int>(mt);
+  out->cnt = L.cnt; out->row0 = L.row0; out->row_src = L.row_src; out->slot_row = L.slot_row;
+  out->tile_expert = L.tile_expert; out->tile_row0 = L.tile_row0; out->tile_rows = L.tile_rows;
+  out->header = L.header; out->scratch = L.hist;
+  return MOK_OK;
+}
+
+mok_status_t mok_schedule_status(const mok_schedule_t* s, int* status, int* num_tiles, int* P) {
+  if (!s || !s->header) return fail(MOK_ERR_INVALID_ARG, "NULL schedule");
+  int h[8];
+  MOK_CUDA(cudaDeviceSynchronize());
+  MOK_CUDA(cudaMemcpy(h, s->header, sizeof(h), cudaMemcpyDeviceToHost));
+  if (status) *status = h[2];
+  if (num_tiles) *num_tiles = h[0];
+  if (P) *P = h[1];
+  return MOK_OK;
+}
+
+mok_status_t mok_mxfp8_quantize(const uint16_t* x, int64_t rows, int K, uint8_t* codes,
+                                uint8_t* scales, void* stream) {
+  if (rows < 0 || K <= 0 || K % 32) return fail(MOK_ERR_INVALID_ARG, "need rows >= 0 and K % 32 == 0");
+  if (rows == 0) return MOK_OK;
+  if (!x || !codes || !scales) return fail(MOK_ERR_INVALID_ARG, "NULL argument");
+  if (!aligned16(x) || !aligned16(codes)) return fail(MOK_ERR_INVALID_ARG, "misaligned pointer");
+  int sms = 0;
+  mok_status_t st = device_info(&sms);
+  if (st) return st;
+  MOK_CUDA(launch_mx_quantize(x, rows * (K / 32), codes, scales, sms, static_cast<cudaStream_t>(stream)));
+  return MOK_OK;
+}
+
+size_t mok_ctx_bytes(int T, int k, int E, int H, int I, int I_s, int mode) {
+  if (check_shapes(T, k, E, H, I, I_s) != MOK_OK) return 0;
+  mok_ctx_t c;
+  CtxExtra X;
+  return carve_ctx(nullptr, T, k, E, H, I, I_s, mode, &c, &X);
+}
+
+mok_status_t mok_ctx_status(const mok_ctx_t* ctx, int* status) {
+  if (!ctx || !ctx->status || !status) return fail(MOK_ERR_INVALID_ARG, "NULL argument");
+  MOK_CUDA(cudaDeviceSynchronize());
+  MOK_CUDA(cudaMemcpy(status, ctx->status, sizeof(int), cudaMemcpyDeviceToHost));
+  return MOK_OK;
+}
+
+mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x, const float* router_w,
+                         const mok_schedule_t* s, const mok_weights_t* w, uint16_t* y, void* ctx_buf,
+                         size_t ctx_bytes, mok_ctx_t* ctx, void* stream) {
+  if (!cfg || !x || !router_w || !s || !w || !y || !ctx_buf || !ctx)
+    return fail(MOK_ERR_INVALID_ARG, "NULL argument");
+  if (cfg->mode != MOK_MODE_BF16 && cfg->mode != MOK_MODE_MXFP8_FWD)
+    return fail(MOK_ERR_INVALID_ARG, "unknown mode %d", cfg->mode);
+  const int T = s->T, k = s->k, E = s->E, H = w->H, I = w->I, Is = w->I_s;
+  if (w->E != E) return fail(MOK_ERR_INVALID_ARG, "weights have E=%d, schedule E=%d", w->E, E);
+  mok_status_t st = check_shapes(T, k, E, H, I, Is);
+  if (st) return st;
+  if (!w->w_gate || !w->w_up || !w->w_down) return fail(MOK_ERR_INVALID_ARG, "NULL routed weight");
+  if (Is > 0 && (!w->ws_gate || !w->ws_up || !w->ws_down))
+    return fail(MOK_ERR_INVALID_ARG, "NULL shared weight");
+  const bool mx = cfg->mode == MOK_MODE_MXFP8_FWD;
+  if (mx && (!w->mx_gate || !w->mx_gate_sc || !w->mx_up || !w->mx_up_sc || !w->mx_down || !w->mx_down_sc ||
+             (Is > 0 && (!w->mxs_gate || !w->mxs_gate_sc || !w->mxs_up || !w->mxs_up_sc || !w->mxs_down ||
+                         !w->mxs_down_sc))))
+    return fail(MOK_ERR_INVALID_ARG, "MXFP8 mode needs the prequantised weights");
+  const void* ptrs[] = {x, router_w, y, ctx_buf, w->w_gate, w->w_up, w->w_down};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return fail(MOK_ERR_INVALID_ARG, "misaligned pointer");
+  if (ctx_bytes < mok_ctx_bytes(T, k, E, H, I, Is, cfg->mode))
+    return fail(MOK_ERR_INVALID_ARG, "context buffer too small");
+  int sms = 0;
+  st = device_info(&sms);
+  if (st) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  CtxExtra X;
+  carve_ctx(ctx_buf, T, k, E, H, I, Is, cfg->mode, ctx, &X);
+  MOK_CUDA(cudaMemsetAsync(ctx->status, 0, 8 * sizeof(int), cs));
+  propagate_status_kernel<<<1, 1, 0, cs>>>(s->header, ctx->status);
+  MOK_CUDA(cudaGetLastError());
+
+  const long long mr = static_cast<long long>(s->max_tiles) * kTileRows;
+  const uint16_t *xa = x, *wg = w->w_gate, *wu = w->w_up, *wd = w->w_down;
+  const uint16_t *wsg = w->ws_gate, *wsu = w->ws_up, *wsd = w->ws_down;
+  if (mx) {
+    // MXFP8 operands, expanded exactly to bf16 for the tensor-core GEMMs
+    MOK_CUDA(launch_mx_quantize(x, static_cast<long long>(T) * H / 32, ctx->xq, ctx->xq_sc, sms, cs));
+    MOK_CUDA(launch_mx_dequant(ctx->xq, ctx->xq_sc, static_cast<long long>(T) * H / 32, X.x_deq, sms, cs));
+    const long long nw = static_cast<long long>(E) * I * H / 32;
+    MOK_CUDA(launch_mx_dequant(w->mx_gate, w->mx_gate_sc, nw, X.wg_deq, sms, cs));
+    MOK_CUDA(launch_mx_dequant(w->mx_up, w->mx_up_sc, nw, X.wu_deq, sms, cs));
+    MOK_CUDA(launch_mx_dequant(w->mx_down, w->mx_down_sc, nw, X.wd_deq, sms, cs));
+    xa = X.x_deq; wg = X.wg_deq; wu = X.wu_deq; wd = X.wd_deq;
+    if (Is > 0) {
+      const long long ns = static_cast<long long>(Is) * H / 32;
+      MOK_CUDA(launch_mx_dequant(w->mxs_gate, w->mxs_gate_sc, ns, X.wsg_deq, sms, cs));
+      MOK_CUDA(launch_mx_dequant(w->mxs_up, w->mxs_up_sc, ns, X.wsu_deq, sms, cs));
+      MOK_CUDA(launch_mx_dequant(w->mxs_down, w->mxs_down_sc, ns, X.wsd_deq, sms, cs));
+      wsg = X.wsg_deq; wsu = X.wsu_deq; wsd = X.wsd_deq;
+    }
+  }
+
+  // ---- shared expert: gate/up + SwiGLU over all T tokens, then down
+  if (Is > 0) {
+    GemmMaps m;
+    if ((st = make_map(&m.a, xa, H, T, 128)) || (st = make_map(&m.b0, wsg, H, Is, 128)) ||
+        (st = make_map(&m.b1, wsu, H, Is, 128)))
+      return st;
+    GemmParams p = base_params(nullptr, ctx->status, 0);
+    p.rows = T; p.K = H; p.N = Is; p.n_tiles = Is / 128; p.b_rows_per_expert = 0;
+    p.out0 = ctx->gu_s;
+    const int items = ((T + 127) / 128) * p.n_tiles;
+    const int grid = items < sms ? items : sms;
+    if (!mx) {
+      p.out1 = ctx->h_s;
+      MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 256, EPI_SWIGLU>(m, p, grid, cs)));
+    } else {
+      p.out1 = ctx->hq_s; p.out2 = ctx->hq_s_sc;
+      MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 256, EPI_SWIGLU_MX>(m, p, grid, cs)));
+      MOK_CUDA(launch_mx_dequant(ctx->hq_s, ctx->hq_s_sc, static_cast<long long>(T) * Is / 32, X.hs_deq, sms, cs));
+    }
+    const uint16_t* hs = mx ? X.hs_deq : ctx->h_s;
+    GemmMaps m2;
+    if ((st = make_map(&m2.a, hs, Is, T, 128)) || (st = make_map(&m2.b0, wsd, Is, H, 128))) return st;
+    m2.b1 = m2.b0;
+    GemmParams q = base_params(nullptr, ctx->status, 0);
+    const int bn = tile_n(H);
+    q.rows = T; q.K = Is; q.N = H; q.n_tiles = H / bn; q.out0 = ctx->shared_out; q.ld = H;
+    const int items2 = ((T + 127) / 128) * q.n_tiles;
+    const int grid2 = items2 < sms ? items2 : sms;
+    if (bn == 256)
+      MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 256, EPI_STORE_ROWS>(m2, q, grid2, cs)));
+    else
+      MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 128, EPI_STORE_ROWS>(m2, q, grid2, cs)));
+  }
+
+  // ---- routed experts: gathered gate/up + SwiGLU, then down + scale + scatter
+  {
+    GemmMaps m;
+    if ((st = make_map(&m.a, xa, H, T, 1)) ||
+        (st = make_map(&m.b0, wg, H, static_cast<uint64_t>(E) * I, 128)) ||
+        (st = make_map(&m.b1, wu, H, static_cast<uint64_t>(E) * I, 128)))
+      return st;
+    GemmParams p = base_params(s, ctx->status, cfg->debug_flags);
+    p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / 128; p.b_rows_per_expert = I;
+    p.out0 = ctx->gu;
+    const long long items = static_cast<long long>(s->max_tiles) * p.n_tiles;
+    const int grid = items < sms ? static_cast<int>(items) : sms;
+    if (!mx) {
+      p.out1 = ctx->h;
+      MOK_CUDA((launch_gemm<SRC_K_GATHER, SRC_K_TILE, 256, EPI_SWIGLU>(m, p, grid, cs)));
+    } else {
+      p.out1 = ctx->hq; p.out2 = ctx->hq_sc;
+      MOK_CUDA((launch_gemm<SRC_K_GATHER, SRC_K_TILE, 256, EPI_SWIGLU_MX>(m, p, grid, cs)));
+      MOK_CUDA(launch_mx_dequant(ctx->hq, ctx->hq_sc, mr * I / 32, X.h_deq, sms, cs));
+    }
+    const uint16_t* hr = mx ? X.h_deq : ctx->h;
+    GemmMaps m2;
+    if ((st = make_map(&m2.a, hr, I, mr, 128)) ||
+        (st = make_map(&m2.b0, wd, I, static_cast<uint64_t>(E) * H, 128)))
+      return st;
+    m2.b1 = m2.b0;
+    GemmParams q = base_params(s, ctx->status, 0);
+    const int bn = tile_n(H);
+    q.grouped = 1; q.K = I; q.N = H; q.n_tiles = H / bn; q.b_rows_per_expert = H;
+    q.out0 = ctx->slots; q.ld = H; q.rw = router_w;
+    const long long items2 = static_cast<long long>(s->max_tiles) * q.n_tiles;
+    const int grid2 = items2 < sms ? static_cast<int>(items2) : sms;
+    if (bn == 256)
+      MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 256, EPI_SCALE_SCATTER>(m2, q, grid2, cs)));
+    else
+      MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 128, EPI_SCALE_SCATTER>(m2, q, grid2, cs)));
+  }
+
+  // ---- combine: y[t] = shared[t] + sum_j slots[t, j] in fixed order
+  MOK_CUDA(launch_combine(ctx->slots, Is > 0 ? ctx->shared_out : nullptr, T, k, H, y, sms, cs));
+  return MOK_OK;
+}
+
+size_t mok_bwd_workspace_bytes(int T, int k, int E, int H, int I, int I_s) {
+  if (check_shapes(T, k, E, H, I, I_s) != MOK_OK) return 0;
+  BwdLayout L;
+  return carve_bwd(nullptr, T, k, E, H, I, I_s, &L);
+}
+
+mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uint16_t* x,
+                          const float* router_w, const mok_schedule_t* s, const mok_ctx_t* ctx,
+                          const mok_weights_t* w, uint16_t* dx, float* d_router_w,
+                          const mok_weight_grads_t* g, void* ws, size_t ws_bytes, void* stream) {
+  if (!cfg || !dy || !x || !router_w || !s || !ctx || !w || !dx || !d_router_w || !g || !ws)
+    return fail(MOK_ERR_INVALID_ARG, "NULL argument");
+  const int T = s->T, k = s->k, E = s->E, H = w->H, I = w->I, Is = w->I_s;
+  mok_status_t st = check_shapes(T, k, E, H, I, Is);
+  if (st) return st;
+  if (ctx->T != T || ctx->k != k || ctx->E != E || ctx->H != H || ctx->I != I || ctx->I_s != Is)
+    return fail(MOK_ERR_INVALID_ARG, "context does not match the schedule / weights");
+  if (!g->d_w_gate || !g->d_w_up || !g->d_w_down) return fail(MOK_ERR_INVALID_ARG, "NULL routed grad");
+  if (Is > 0 && (!g->d_ws_gate || !g->d_ws_up || !g->d_ws_down || !w->ws_gate || !w->ws_up || !w->ws_down))
+    return fail(MOK_ERR_INVALID_ARG, "NULL shared weight or grad");
+  const void* ptrs[] = {dy, x, router_w, dx, d_router_w, ws, g->d_w_gate, g->d_w_up, g->d_w_down};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return fail(MOK_ERR_INVALID_ARG, "misaligned pointer");
+  if (ws_bytes < mok_bwd_workspace_bytes(T, k, E, H, I, Is))
+    return fail(MOK_ERR_INVALID_ARG, "backward workspace too small");
+  int sms = 0;
+  st = device_info(&sms);
+  if (st) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  BwdLayout L;
+  carve_bwd(ws, T, k, E, H, I, Is, &L);
+  const long long mr = static_cast<long long>(s->max_tiles) * kTileRows;
+
+  // ---- routed: down dgrad + SwiGLU backward + router-weight partials
+  const int bn1 = tile_n(I);
+  {
+    GemmMaps m;
+    if ((st = make_map(&m.a, dy, H, T, 1)) ||
+        (st = make_map(&m.b0, w->w_down, I, static_cast<uint64_t>(E) * H, 64)))
+      return st;
+    m.b1 = m.b0;
+    GemmParams p = base_params(s, ctx->status, 0);
+    p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / bn1; p.b_rows_per_expert = H;
+    p.aux0 = ctx->gu; p.out0 = L.dgu; p.out1 = L.hw; p.rw = router_w; p.dw_part = L.dw_part;
+    const long long items = static_cast<long long>(s->max_tiles) * p.n_tiles;
+    const int grid = items < sms ? static_cast<int>(items) : sms;
+    if (bn1 == 256)
+      MOK_CUDA((launch_gemm<SRC_K_GATHER, SRC_MN_TILE, 256, EPI_DOWN_BWD>(m, p, grid, cs)));
+    else
+      MOK_CUDA((launch_gemm<SRC_K_GATHER, SRC_MN_TILE, 128, EPI_DOWN_BWD>(m, p, grid, cs)));
+  }
+  // ---- routed: dW_down[e] = sum over e's rows of dy[t(r)]^T (w h)[r]
+  {
+    GemmMaps m;
+    if ((st = make_map(&m.a, dy, H, T, 1)) || (st = make_map(&m.b0, L.hw, I, mr, 64))) return st;
+    m.b1 = m.b0;
+    GemmParams p = base_params(s, ctx->status, 0);
+    const int bn = tile_n(I);
+    p.wgrad = 1; p.grouped = 1; p.E = E; p.m_tiles = H / 128; p.n_tiles = I / bn;
+    p.out0 = g->d_w_down; p.out1 = g->d_w_down; p.ld = I; p.split = H;
+    p.estride = static_cast<long long>(H) * I;
+    const long long items = static_cast<long long>(E) * p.m_tiles * p.n_tiles;
+    const int grid = items < sms ? static_cast<int>(items) : sms;
+    if (bn == 256)
+      MOK_CUDA((launch_gemm<SRC_MN_GATHER, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, grid, cs)));
+    else
+      MOK_CUDA((launch_gemm<SRC_MN_GATHER, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, grid, cs)));
+  }
+  // ---- routed: dW_gate|up[e] = sum over e's rows of (dG|dU)[r]^T x[t(r)]
+  {
+    GemmMaps m;
+    if ((st = make_map(&m.a, L.dgu, 2 * I, mr, 64)) || (st = make_map(&m.b0, x, H, T, 1))) return st;
+    m.b1 = m.b0;
+    GemmParams p = base_params(s, ctx->status, 0);
+    const int bn = tile_n(H);
+    p.wgrad = 1; p.grouped = 1; p.E = E; p.m_tiles = 2 * I / 128; p.n_tiles = H / bn;
+    p.out0 = g->d_w_gate; p.out1 = g->d_w_up; p.ld = H; p.split = I;
+    p.estride = static_cast<long long>(I) * H;
+    const long long items = static_cast<long long>(E) * p.m_tiles * p.n_tiles;
+    const int grid = items < sms ? static_cast<int>(items) : sms;
+    if (bn == 256)
+      MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_GATHER, 256, EPI_WGRAD>(m, p, grid, cs)));
+    else
+      MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_GATHER, 128, EPI_WGRAD>(m, p, grid, cs)));
+  }
+  // ---- routed: dx slots = dG W_gate[e] + dU W_up[e]
+  {
+    GemmMaps m;
+    if ((st = make_map(&m.a, L.dgu, 2 * I, mr, 128)) ||
+        (st = make_map(&m.b0, w->w_gate, H, static_cast<uint64_t>(E) * I, 64)) ||
+        (st = make_map(&m.b1, w->w_up, H, static_cast<uint64_t>(E) * I, 64)))
+      return st;
+    GemmParams p = base_params(s, ctx->status, 0);
+    const int bn = tile_n(H);
+    p.grouped = 1; p.K = 2 * I; p.N = H; p.n_tiles = H / bn; p.b_rows_per_expert = I; p.b_split = I;
+    p.out0 = L.dx_slots; p.ld = H;
+    const long long items = static_cast<long long>(s->max_tiles) * p.n_tiles;
+    const int grid = items < sms ? static_cast<int>(items) : sms;
+    if (bn == 256)
+      MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_MN_TILE, 256, EPI_SCATTER>(m, p, grid, cs)));
+    else
+      MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_MN_TILE, 128, EPI_SCATTER>(m, p, grid, cs)));
+  }
+  // ---- shared expert backward (dense rows, w = 1)
+  if (Is > 0) {
+    const int bns = tile_n(Is);
+    {
+      GemmMaps m;
+      if ((st = make_map(&m.a, dy, H, T, 128)) || (st = make_map(&m.b0, w->ws_down, Is, H, 64))) return st;
+      m.b1 = m.b0;
+      GemmParams p = base_params(nullptr, ctx->status, 0);
+      p.rows = T; p.K = H; p.N = Is; p.n_tiles = Is / bns; p.b_rows_per_expert = 0;
+      p.aux0 = ctx->gu_s; p.out0 = L.dgu_s; p.out1 = L.hs;
+      const int items = ((T + 127) / 128) * p.n_tiles;
+      const int grid = items < sms ? items : sms;
+      if (bns == 256)
+        MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_MN_TILE, 256, EPI_DOWN_BWD>(m, p, grid, cs)));
+      else
+        MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_MN_TILE, 128, EPI_DOWN_BWD>(m, p, grid, cs)));
+    }
+    {  // dW_s_down = dy^T h_s
+      GemmMaps m;
+      if ((st = make_map(&m.a, dy, H, T, 64)) || (st = make_map(&m.b0, L.hs, Is, T, 64))) return st;
+      m.b1 = m.b0;
+      GemmParams p = base_params(nullptr, ctx->status, 0);
+      p.wgrad = 1; p.rows = T; p.E = 1; p.m_tiles = H / 128; p.n_tiles = Is / bns;
+      p.out0 = g->d_ws_down; p.out1 = g->d_ws_down; p.ld = Is; p.split = H; p.estride = 0;
+      const int items = p.m_tiles * p.n_tiles;
+      const int grid = items < sms ? items : sms;
+      if (bns == 256)
+        MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, grid, cs)));
+      else
+        MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, grid, cs)));
+    }
+    {  // dW_s_gate|up = (dG_s|dU_s)^T x
+      GemmMaps m;
+      if ((st = make_map(&m.a, L.dgu_s, 2 * Is, T, 64)) || (st = make_map(&m.b0, x, H, T, 64))) return st;
+      m.b1 = m.b0;
+      GemmParams p = base_params(nullptr, ctx->status, 0);
+      const int bn = tile_n(H);
+      p.wgrad = 1; p.rows = T; p.E = 1; p.m_tiles = 2 * Is / 128; p.n_tiles = H / bn;
+      p.out0 = g->d_ws_gate; p.out1 = g->d_ws_up; p.ld = H; p.split = Is; p.estride = 0;
+      const int items = p.m_tiles * p.n_tiles;
+      const int grid = items < sms ? items : sms;
+      if (bn == 256)
+        MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, grid, cs)));
+      else
+        MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, grid, cs)));
+    }
+    {  // dx_s = dG_s W_s_gate + dU_s W_s_up
+      GemmMaps m;
+      if ((st = make_map(&m.a, L.dgu_s, 2 * Is, T, 128)) || (st = make_map(&m.b0, w->ws_gate, H, Is, 64)) ||
+          (st = make_map(&m.b1, w->ws_up, H, Is, 64)))
+        return st;
+      GemmParams p = base_params(nullptr, ctx->status, 0);
+      const int bn = tile_n(H);
+      p.rows = T; p.K = 2 * Is; p.N = H; p.n_tiles = H / bn; p.b_rows_per_expert = 0; p.b_split = Is;
+      p.out0 = L.dx_s; p.ld = H;
+      const int items = ((T + 127) / 128) * p.n_tiles;
+      const int grid = items < sms ? items : sms;
+      if (bn == 256)
+        MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_MN_TILE, 256, EPI_STORE_ROWS>(m, p, grid, cs)));
+      else
+        MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_MN_TILE, 128, EPI_STORE_ROWS>(m, p, grid, cs)));
+    }
+  }
+  // ---- fixed-order reductions: dx and the router-weight gradient
+  MOK_CUDA(launch_combine(L.dx_slots, Is > 0 ? L.dx_s : nullptr, T, k, H, dx, sms, cs));
+  MOK_CUDA(launch_dw_reduce(L.dw_part, T * k, I / bn1, d_router_w, cs));
+  return MOK_OK;
+}
+
+}  // extern "C"

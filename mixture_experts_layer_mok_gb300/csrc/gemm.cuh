@@ -1,0 +1,626 @@
+// Persistent grouped GEMM engine on tcgen05 / TMEM / TMA for sm_103a.
+//
+// One CTA per SM, 192 threads:
+//   warp 0      TMA producer: tile loads, and tile::gather4 loads that fetch
+//               the token rows of a schedule tile straight into shared memory
+//               (the on-chip form of MoK's dispatch exchange);
+//   warp 1      MMA issuer (one thread) and TMEM owner;
+//   warps 2..5  epilogue: TMEM -> registers -> fused elementwise -> HBM
+//               (SwiGLU, MXFP8 requantisation, router scaling, scatter to
+//               per-(token, k) slots, SwiGLU backward, router-weight grad).
+// Warp 0/1 (data movement) overlap with warps 2-5 (output) on a
+// double-buffered TMEM accumulator: the single-GPU analogue of MoK's split of
+// SMs into communication and compute roles ("Mixture-of-Kittens: a
+// deterministic MoE megakernel for NVL72 racks", "Tuning the five
+// hyperparameters before production": fwd/bwd_num_comm_sms).
+//
+// Work items are output tiles of 128 rows x BN columns; each is produced by
+// exactly one CTA with a fixed K order, so results do not depend on which CTA
+// takes which item or on the item order.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include "ptx.cuh"
+
+namespace mok {
+
+constexpr int kBM = 128;        // rows of an output tile (TMEM lanes)
+constexpr int kBK = 64;         // bf16 elements per 128-byte swizzled row
+constexpr int kThreads = 192;
+constexpr int kChunkBytes = 64 * 128;  // one MN-major chunk: 64 K-rows x 64 elements
+
+enum Src : int {
+  SRC_K_TILE = 0,     // K-major rows [p0, p0+128) of a 2-D tensor (box 64 x 128)
+  SRC_K_GATHER = 1,   // K-major: the 128 token rows of a schedule tile (box 64 x 1)
+  SRC_MN_TILE = 2,    // MN-major: K-rows [k, k+64) of a 2-D tensor (box 64 x 64)
+  SRC_MN_GATHER = 3,  // MN-major: 64 token rows of a schedule range (box 64 x 1)
+};
+
+enum Epi : int {
+  EPI_SWIGLU = 0,        // gate|up accumulators -> G, U (bf16), h = silu(G) U (bf16)
+  EPI_SWIGLU_MX = 1,     // same, h written as MXFP8 codes + E8M0 scales
+  EPI_SCALE_SCATTER = 2, // slot[f] = bf16(w[f] * acc) for the tile's routed rows
+  EPI_STORE_ROWS = 3,    // out[row] = bf16(acc) for dense rows
+  EPI_DOWN_BWD = 4,      // dH = w Z; SwiGLU backward; d_w partial = sum Z h; hw = w h
+  EPI_SCATTER = 5,       // out[f] = bf16(acc) for the tile's routed rows
+  EPI_WGRAD = 6,         // out[e][m][n] = bf16(acc), rows split over two tensors
+};
+
+struct GemmMaps {
+  CUtensorMap a;
+  CUtensorMap b0;
+  CUtensorMap b1;
+};
+
+struct GemmParams {
+  // ---- work decomposition
+  int wgrad;       // 0: output rows are layer rows; 1: per-expert weight gradient
+  int grouped;     // layer rows (or wgrad K-rows) come from the schedule
+  int rows;        // dense: number of layer rows (T)
+  int K;           // row GEMMs: contraction length (multiple of 64)
+  int n_tiles;     // output column tiles
+  int m_tiles;     // wgrad: output row tiles
+  int E;           // wgrad: experts (1 for a dense weight)
+  int topk;
+  const int* header;  // schedule header: [0] num_tiles, [2] status (grouped only)
+  const int* tile_expert;
+  const int* tile_row0;
+  const int* tile_rows;
+  const int* row_src;
+  const int* row0;
+  const int* cnt;
+  // ---- operand coordinates
+  int b_rows_per_expert;  // weight rows (K-major B) or K-rows (MN-major B) per expert
+  int b_split;            // MN-major B: K index where map b1 takes over (0 = never)
+  // ---- epilogue
+  int N;             // logical width used by the epilogue (I for SwiGLU, ...)
+  void* out0;
+  void* out1;
+  void* out2;
+  void* out3;
+  const void* aux0;  // EPI_DOWN_BWD: saved gate|up pre-activations
+  const float* rw;   // router weights [T*k] (grouped), NULL = 1
+  float* dw_part;    // EPI_DOWN_BWD grouped: [T*k][n_tiles]
+  long long ld;      // output row stride (elements)
+  int split;         // EPI_WGRAD: first output row that goes to out1
+  long long estride; // EPI_WGRAD: elements per expert in out0 / out1
+  int* status;       // device status word
+  int debug;         // MOK_DEBUG_* flags
+};
+
+struct Item {
+  int e, p0, rows, m0, nt, kbeg, nk;
+};
+
+__device__ __forceinline__ int num_items(const GemmParams& p) {
+  if (p.grouped && p.header[2] != 0) return 0;
+  if (!p.wgrad) {
+    const int mt = p.grouped ? p.header[0] : (p.rows + kBM - 1) / kBM;
+    return mt * p.n_tiles;
+  }
+  return p.E * p.m_tiles * p.n_tiles;
+}
+
+__device__ __forceinline__ Item get_item(const GemmParams& p, int idx) {
+  Item it;
+  if (!p.wgrad) {
+    const int mt = idx / p.n_tiles;
+    it.nt = idx - mt * p.n_tiles;
+    if (p.grouped) {
+      it.e = __ldg(p.tile_expert + mt);
+      it.p0 = __ldg(p.tile_row0 + mt);
+      it.rows = __ldg(p.tile_rows + mt);
+    } else {
+      it.e = 0;
+      it.p0 = mt * kBM;
+      it.rows = min(kBM, p.rows - it.p0);
+    }
+    it.m0 = it.p0;
+    it.kbeg = 0;
+    it.nk = p.K / kBK;
+  } else {
+    const int per_e = p.m_tiles * p.n_tiles;
+    it.e = idx / per_e;
+    const int r = idx - it.e * per_e;
+    const int mt = r / p.n_tiles;
+    it.nt = r - mt * p.n_tiles;
+    it.m0 = mt * kBM;
+    it.p0 = 0;
+    it.rows = 0;
+    if (p.grouped) {
+      it.kbeg = __ldg(p.row0 + it.e);
+      const int c = __ldg(p.cnt + it.e);
+      it.nk = (c + kBM - 1) / kBM * (kBM / kBK);
+    } else {
+      it.kbeg = 0;
+      it.nk = (p.rows + kBK - 1) / kBK;
+    }
+  }
+  return it;
+}
+
+// Token row of schedule row q (padding rows read token 0; their partner
+// operand row is zero, or the epilogue drops them).
+__device__ __forceinline__ int token_of(const GemmParams& p, int q) {
+  const int f = __ldg(p.row_src + q);
+  return f >= 0 ? f / p.topk : 0;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void store_bf16x32(void* dst, const float* v) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    d[q] = make_uint4(pack_bf16(v[8 * q + 0], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
+                      pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+}
+
+__device__ __forceinline__ void zero_bytes64(void* dst) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) d[q] = make_uint4(0, 0, 0, 0);
+}
+
+__device__ __forceinline__ void load_bf16x32(const void* src, float* v) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 w = __ldg(s + q);
+    uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[8 * q + 2 * i + 0] = __uint_as_float(ws[i] << 16);
+      v[8 * q + 2 * i + 1] = __uint_as_float(ws[i] & 0xFFFF0000u);
+    }
+  }
+}
+
+// E8M0 exponent of a block: smallest s with amax <= 448 * 2^s, clamped to
+// [-127, 127], 0 for amax == 0; decided from the fp32 exponent and mantissa.
+__device__ __forceinline__ int mx_scale_exponent(float amax) {
+  const uint32_t b = __float_as_uint(amax);
+  const int ef = static_cast<int>((b >> 23) & 0xFF);
+  if (b == 0) return 0;
+  if (ef == 0) return -127;  // fp32 subnormal: far below 448 * 2^-127
+  const int e = ef - 127;
+  int s = e - 8 + (((b & 0x7FFFFFu) > 0x600000u) ? 1 : 0);  // mantissa above 1.75
+  return max(-127, min(127, s));
+}
+
+// 32 values -> 32 E4M3 codes (RNE, satfinite) scaled by 2^-s; returns s + 127.
+__device__ __forceinline__ uint32_t mx_quantize32(const float* v, uint8_t* codes_out) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const int s = mx_scale_exponent(amax);
+  const float inv = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);  // 2^-s, s <= 126
+  uint32_t w[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const __nv_fp8x2_storage_t lo =
+        __nv_cvt_float2_to_fp8x2(make_float2(v[4 * q + 0] * inv, v[4 * q + 1] * inv),
+                                 __NV_SATFINITE, __NV_E4M3);
+    const __nv_fp8x2_storage_t hi =
+        __nv_cvt_float2_to_fp8x2(make_float2(v[4 * q + 2] * inv, v[4 * q + 3] * inv),
+                                 __NV_SATFINITE, __NV_E4M3);
+    w[q] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+  }
+  uint4* d = reinterpret_cast<uint4*>(codes_out);
+  d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  return static_cast<uint32_t>(s + 127);
+}
+
+template <int A_SRC, int B_SRC, int BN, int EPI>
+struct GemmCfg {
+  static constexpr bool kAMN = (A_SRC == SRC_MN_TILE || A_SRC == SRC_MN_GATHER);
+  static constexpr bool kBMN = (B_SRC == SRC_MN_TILE || B_SRC == SRC_MN_GATHER);
+  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = (BN == 256) ? 4 : 6;
+  static constexpr int kTmemCols = 2 * BN;  // two accumulator buffers
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+  static constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, kAMN, kBMN);
+  static_assert(BN == 128 || BN == 256, "tile N");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+};
+
+// Bounded wait that ignores the abort flag (used while draining in-flight work).
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) break;
+  }
+}
+
+template <int A_SRC, int B_SRC, int BN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
+  using C = GemmCfg<A_SRC, B_SRC, BN, EPI>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::kStages;
+  uint64_t* tfull = bars + 2 * C::kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&maps.a);
+    tma_prefetch_desc(&maps.b0);
+    tma_prefetch_desc(&maps.b1);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int nitems = num_items(p);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    int stage = 0;
+    uint32_t phase = 0;
+    long long fills = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; idx < nitems && ok; idx += gridDim.x) {
+      const Item it = get_item(p, idx);
+      const int bn_out = (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_MX) ? BN / 2 : BN;
+      const int n0 = it.nt * bn_out;
+      // token rows of a row tile (K-major gather): rows 4*lane .. 4*lane+3
+      int tok[4] = {0, 0, 0, 0};
+      if (A_SRC == SRC_K_GATHER) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = 4 * lane + i;
+          tok[i] = (r < it.rows) ? token_of(p, it.p0 + r) : 0;
+        }
+      }
+      // token rows of the first K-block (MN-major gather along K)
+      int ktok[4] = {0, 0, 0, 0};
+      const bool mn_gather = (A_SRC == SRC_MN_GATHER || B_SRC == SRC_MN_GATHER);
+      if (mn_gather && it.nk > 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ktok[i] = token_of(p, it.kbeg + 4 * (lane & 15) + i);
+      }
+      for (int kb = 0; kb < it.nk; ++kb) {
+        int cur[4] = {ktok[0], ktok[1], ktok[2], ktok[3]};
+        int w = (lane == 0) ? (mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status) ? 1 : 0) : 0;
+        w = __shfl_sync(0xffffffffu, w, 0);
+        if (!w) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+        __syncwarp();
+        uint8_t* sA = smem + stage * C::kStageBytes;
+        uint8_t* sB = sA + C::kABytes;
+        const int k0 = kb * kBK;
+        // ---- A operand
+        if (A_SRC == SRC_K_TILE) {
+          if (lane == 0) tma_load_2d(sA, &maps.a, &full[stage], k0, it.p0);
+        } else if (A_SRC == SRC_K_GATHER) {
+          tma_gather4(sA + lane * 512, &maps.a, &full[stage], k0, tok[0], tok[1], tok[2], tok[3]);
+        } else if (A_SRC == SRC_MN_TILE) {
+          if (lane < 2)
+            tma_load_2d(sA + lane * kChunkBytes, &maps.a, &full[stage], it.m0 + 64 * lane,
+                        it.kbeg + k0);
+        } else {  // SRC_MN_GATHER
+          const int c = lane >> 4, g = lane & 15;
+          tma_gather4(sA + c * kChunkBytes + g * 512, &maps.a, &full[stage], it.m0 + 64 * c, cur[0],
+                      cur[1], cur[2], cur[3]);
+        }
+        // ---- B operand
+        if (B_SRC == SRC_K_TILE) {
+          if (lane == 0) {
+            if (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_MX) {
+              const int r = it.e * p.b_rows_per_expert + n0;
+              tma_load_2d(sB, &maps.b0, &full[stage], k0, r);
+              tma_load_2d(sB + (BN / 2) * 128, &maps.b1, &full[stage], k0, r);
+            } else {
+#pragma unroll
+              for (int h = 0; h < BN / 128; ++h)
+                tma_load_2d(sB + h * 128 * 128, &maps.b0, &full[stage], k0,
+                            it.e * p.b_rows_per_expert + n0 + 128 * h);
+            }
+          }
+        } else if (B_SRC == SRC_MN_TILE) {
+          if (lane < BN / 64) {
+            int krow = k0;
+            const CUtensorMap* m = &maps.b0;
+            if (p.b_split > 0 && krow >= p.b_split) {
+              m = &maps.b1;
+              krow -= p.b_split;
+            }
+            const int kr = p.wgrad ? (it.kbeg + k0) : (it.e * p.b_rows_per_expert + krow);
+            tma_load_2d(sB + lane * kChunkBytes, m, &full[stage], n0 + 64 * lane, kr);
+          }
+        } else if (B_SRC == SRC_MN_GATHER) {
+          const int g = lane & 15;
+#pragma unroll
+          for (int cc = 0; cc < BN / 128; ++cc) {
+            const int c = (lane >> 4) + 2 * cc;
+            tma_gather4(sB + c * kChunkBytes + g * 512, &maps.b0, &full[stage], n0 + 64 * c,
+                        cur[0], cur[1], cur[2], cur[3]);
+          }
+        }
+        ++fills;
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+        // prefetch the next K-block's token rows (latency hidden by the next wait)
+        if (mn_gather && kb + 1 < it.nk) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            ktok[i] = token_of(p, it.kbeg + (kb + 1) * kBK + 4 * (lane & 15) + i);
+        }
+      }
+    }
+    if (!ok && lane == 0) {
+      // drain: wait until every load issued into a stage has landed
+      const long long n = fills < C::kStages ? fills : C::kStages;
+      int s = stage;
+      uint32_t ph = phase;
+      for (long long i = 0; i < n; ++i) {
+        if (--s < 0) {
+          s = C::kStages - 1;
+          ph ^= 1;
+        }
+        mbar_drain(&full[s], ph);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int abuf = 0;
+      uint32_t aphase = 0;
+      bool first = true;
+      for (int idx = blockIdx.x; idx < nitems; idx += gridDim.x) {
+        const Item it = get_item(p, idx);
+        if (it.nk == 0) continue;
+        if (!mbar_wait(&tempty[abuf], aphase ^ 1, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t acc = tmem_base + static_cast<uint32_t>(abuf * BN);
+        bool ok = true;
+        for (int kb = 0; kb < it.nk; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + stage * C::kStageBytes);
+          const uint32_t b0 = a0 + C::kABytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t ad = C::kAMN ? smem_desc_sw128(a0 + kk * 2048, kChunkBytes, 1024)
+                                        : smem_desc_sw128(a0 + kk * 32, 16, 1024);
+            const uint64_t bd = C::kBMN ? smem_desc_sw128(b0 + kk * 2048, kChunkBytes, 1024)
+                                        : smem_desc_sw128(b0 + kk * 32, 16, 1024);
+            umma_bf16(acc, ad, bd, C::kIdesc, (kb | kk) ? 1u : 0u);
+          }
+          umma_commit(&empty[stage]);
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        const bool drop = (p.debug & 1) && first && blockIdx.x == 0;
+        if (!drop) umma_commit(&tfull[abuf]);
+        first = false;
+        if (++abuf == 2) {
+          abuf = 0;
+          aphase ^= 1;
+        }
+      }
+      // every MMA issued by this thread must finish before TMEM is released
+      umma_commit(done);
+      mbar_drain(done, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;         // TMEM lane quarter this warp may access
+    const int r = q * 32 + lane;    // tile row of this thread
+    int abuf = 0;
+    uint32_t aphase = 0;
+    for (int idx = blockIdx.x; idx < nitems; idx += gridDim.x) {
+      const Item it = get_item(p, idx);
+      const int bn_out = (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_MX) ? BN / 2 : BN;
+      const int n0 = it.nt * bn_out;
+      if (it.nk == 0) {
+        // weight gradient of an expert with no rows: zeros
+        if (EPI == EPI_WGRAD) {
+          const int m = it.m0 + r;
+          uint16_t* dst = (m < p.split)
+                              ? static_cast<uint16_t*>(p.out0) + it.e * p.estride + m * p.ld
+                              : static_cast<uint16_t*>(p.out1) + it.e * p.estride + (m - p.split) * p.ld;
+          for (int c = 0; c < BN / 32; ++c) zero_bytes64(dst + n0 + c * 32);
+        }
+        continue;
+      }
+      int w = (lane == 0) ? (mbar_wait(&tfull[abuf], aphase, abort_flag, p.status) ? 1 : 0) : 0;
+      w = __shfl_sync(0xffffffffu, w, 0);
+      if (!w) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + static_cast<uint32_t>(abuf * BN) +
+                          (static_cast<uint32_t>(q * 32) << 16);
+
+      if constexpr (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_MX) {
+        // out0 = gu [rows][2N], out1 = h [rows][N] (bf16) or codes, out2 = scales
+        const int prow = it.p0 + r;
+        const bool valid = r < it.rows;
+        const bool inb = p.grouped ? true : valid;
+        uint16_t* gu = static_cast<uint16_t*>(p.out0) + static_cast<long long>(prow) * 2 * p.N;
+#pragma unroll 1
+        for (int c = 0; c < BN / 64; ++c) {
+          float g[32], u[32];
+          tmem_ld32(tb + c * 32, g);
+          tmem_ld32(tb + BN / 2 + c * 32, u);
+          if (inb) {
+            const int col = n0 + c * 32;
+            if (!valid) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) g[i] = u[i] = 0.f;
+            }
+            float hv[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float sg = 1.f / (1.f + __expf(-g[i]));
+              hv[i] = g[i] * sg * u[i];
+            }
+            store_bf16x32(gu + col, g);
+            store_bf16x32(gu + p.N + col, u);
+            if constexpr (EPI == EPI_SWIGLU) {
+              store_bf16x32(static_cast<uint16_t*>(p.out1) + static_cast<long long>(prow) * p.N + col, hv);
+            } else {
+              uint8_t* codes = static_cast<uint8_t*>(p.out1) + static_cast<long long>(prow) * p.N + col;
+              const uint32_t sc = mx_quantize32(hv, codes);
+              static_cast<uint8_t*>(p.out2)[static_cast<long long>(prow) * (p.N / 32) + col / 32] =
+                  static_cast<uint8_t>(sc);
+            }
+          }
+        }
+      } else if constexpr (EPI == EPI_SCALE_SCATTER || EPI == EPI_SCATTER) {
+        const int f = (r < it.rows) ? __ldg(p.row_src + it.p0 + r) : -1;
+        const float wt = (EPI == EPI_SCALE_SCATTER && f >= 0) ? __ldg(p.rw + f) : 1.f;
+        uint16_t* dst = static_cast<uint16_t*>(p.out0) + static_cast<long long>(f) * p.ld + n0;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(tb + c * 32, v);
+          if (f >= 0) {
+            if (EPI == EPI_SCALE_SCATTER) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] *= wt;
+            }
+            store_bf16x32(dst + c * 32, v);
+          }
+        }
+      } else if constexpr (EPI == EPI_STORE_ROWS) {
+        const int prow = it.p0 + r;
+        const bool valid = r < it.rows;
+        uint16_t* dst = static_cast<uint16_t*>(p.out0) + static_cast<long long>(prow) * p.ld + n0;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(tb + c * 32, v);
+          if (valid) store_bf16x32(dst + c * 32, v);
+        }
+      } else if constexpr (EPI == EPI_DOWN_BWD) {
+        // out0 = dgu [rows][2N], out1 = hw [rows][N]; aux0 = gu [rows][2N]
+        const int prow = it.p0 + r;
+        int f = -1;
+        bool valid, inb;
+        float wt = 1.f;
+        if (p.grouped) {
+          f = (r < it.rows) ? __ldg(p.row_src + prow) : -1;
+          valid = f >= 0;
+          inb = true;
+          if (valid) wt = __ldg(p.rw + f);
+        } else {
+          valid = r < it.rows;
+          inb = valid;
+        }
+        const uint16_t* gu = static_cast<const uint16_t*>(p.aux0) + static_cast<long long>(prow) * 2 * p.N;
+        uint16_t* dgu = static_cast<uint16_t*>(p.out0) + static_cast<long long>(prow) * 2 * p.N;
+        uint16_t* hw = static_cast<uint16_t*>(p.out1) + static_cast<long long>(prow) * p.N;
+        float dpart = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float z[32];
+          tmem_ld32(tb + c * 32, z);
+          if (inb) {
+            const int col = n0 + c * 32;
+            if (valid) {
+              float g[32], u[32];
+              load_bf16x32(gu + col, g);
+              load_bf16x32(gu + p.N + col, u);
+              float dg[32], du[32], hv[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const float sg = 1.f / (1.f + __expf(-g[i]));
+                const float sl = g[i] * sg;
+                const float h = sl * u[i];
+                dpart = fmaf(z[i], h, dpart);
+                const float dh = wt * z[i];
+                dg[i] = dh * u[i] * sg * (1.f + g[i] * (1.f - sg));
+                du[i] = dh * sl;
+                hv[i] = wt * h;
+              }
+              store_bf16x32(dgu + col, dg);
+              store_bf16x32(dgu + p.N + col, du);
+              store_bf16x32(hw + col, hv);
+            } else {
+              zero_bytes64(dgu + col);
+              zero_bytes64(dgu + p.N + col);
+              zero_bytes64(hw + col);
+            }
+          }
+        }
+        if (p.grouped && valid) p.dw_part[static_cast<long long>(f) * p.n_tiles + it.nt] = dpart;
+      } else if constexpr (EPI == EPI_WGRAD) {
+        const int m = it.m0 + r;
+        uint16_t* dst = (m < p.split)
+                            ? static_cast<uint16_t*>(p.out0) + it.e * p.estride + static_cast<long long>(m) * p.ld
+                            : static_cast<uint16_t*>(p.out1) + it.e * p.estride +
+                                  static_cast<long long>(m - p.split) * p.ld;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(tb + c * 32, v);
+          store_bf16x32(dst + n0 + c * 32, v);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[abuf]);
+      if (++abuf == 2) {
+        abuf = 0;
+        aphase ^= 1;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+}  // namespace mok

@@ -1,0 +1,33 @@
+// Internal launch interface shared by the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mok {
+
+constexpr int kTileRows = 128;     // rows per expert tile
+constexpr int kSchedChunk = 4096;  // routed rows per schedule block
+
+struct GemmMaps;
+struct GemmParams;
+
+cudaError_t launch_schedule(const int64_t* te, int T, int k, int E, int cap_tiles, int max_tiles,
+                            int* hist, int* cnt, int* row0, int* row_src, int* slot_row,
+                            int* tile_expert, int* tile_row0, int* tile_rows, int* header,
+                            cudaStream_t st);
+cudaError_t launch_mx_quantize(const uint16_t* x, long long nblocks, uint8_t* codes, uint8_t* scales,
+                               int num_sms, cudaStream_t st);
+cudaError_t launch_mx_dequant(const uint8_t* codes, const uint8_t* scales, long long nblocks,
+                              uint16_t* out, int num_sms, cudaStream_t st);
+cudaError_t launch_combine(const uint16_t* slots, const uint16_t* base, int T, int k, int H,
+                           uint16_t* out, int num_sms, cudaStream_t st);
+cudaError_t launch_dw_reduce(const float* part, int nf, int ntiles, float* dw, cudaStream_t st);
+
+// Grouped GEMM launch: instantiated for the operand sources / tile widths /
+// epilogues the layer uses (gemm_fwd.cu, gemm_bwd.cu).
+template <int A_SRC, int B_SRC, int BN, int EPI>
+cudaError_t launch_gemm(const GemmMaps& maps, const GemmParams& p, int grid, cudaStream_t st);
+
+}  // namespace mok

@@ -1,0 +1,330 @@
+// Schedule builder, MXFP8 quantiser, and the fixed-order combine kernels.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gemm.cuh"
+#include "internal.h"
+
+namespace mok {
+
+// ===========================================================================
+// Schedule ("Mixture-of-Kittens: a deterministic MoE megakernel for NVL72
+// racks", "The two API layers and the schedule object": routing decisions are
+// materialised into a dispatch/combine plan before any compute kernel runs).
+// Three launches: per-chunk histograms; one block scans them into per-expert
+// counts, padded row offsets and the tile list; per-chunk stable scatter.
+// ===========================================================================
+
+__global__ void sched_count_kernel(const int64_t* __restrict__ te, int n, int E,
+                                   int* __restrict__ hist, int* __restrict__ header) {
+  extern __shared__ int sh_cnt[];
+  for (int i = threadIdx.x; i < E; i += blockDim.x) sh_cnt[i] = 0;
+  __syncthreads();
+  const int base = blockIdx.x * kSchedChunk;
+  const int end = min(n, base + kSchedChunk);
+  bool bad = false;
+  for (int i = base + threadIdx.x; i < end; i += blockDim.x) {
+    const int64_t e = te[i];
+    if (e < 0 || e >= E)
+      bad = true;
+    else
+      atomicAdd(&sh_cnt[static_cast<int>(e)], 1);
+  }
+  if (bad) atomicCAS(&header[2], 0, 2 /* MOK_ERR_INDEX */);
+  __syncthreads();
+  for (int i = threadIdx.x; i < E; i += blockDim.x) hist[blockIdx.x * E + i] = sh_cnt[i];
+}
+
+// Exclusive scan over a 1024-thread block.
+__device__ int block_exclusive_scan(int v, int* tmp /* >= 32 ints */, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) tmp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = (lane < (int)(blockDim.x >> 5)) ? tmp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    tmp[lane] = w;  // inclusive warp totals
+  }
+  __syncthreads();
+  const int before = (warp > 0) ? tmp[warp - 1] : 0;
+  *total = tmp[(blockDim.x >> 5) - 1];
+  __syncthreads();
+  return before + x - v;
+}
+
+__global__ void __launch_bounds__(1024) sched_scan_kernel(int n, int E, int nchunks, int cap_tiles,
+                                                          int max_tiles, int* __restrict__ hist,
+                                                          int* __restrict__ cnt, int* __restrict__ row0,
+                                                          int* __restrict__ row_src,
+                                                          int* __restrict__ tile_expert,
+                                                          int* __restrict__ tile_row0,
+                                                          int* __restrict__ tile_rows,
+                                                          int* __restrict__ header) {
+  __shared__ int tmp[32];
+  const int e = threadIdx.x;  // E <= 1024: one thread per expert
+  const long long max_rows = static_cast<long long>(max_tiles) * kTileRows;
+  if (header[2] != 0) {
+    if (threadIdx.x == 0) {
+      header[0] = 0;
+      header[1] = 0;
+      header[3] = 0;
+    }
+    return;
+  }
+  int c = 0;
+  if (e < E) {
+    int run = 0;
+    for (int k = 0; k < nchunks; ++k) {
+      const int v = hist[k * E + e];
+      hist[k * E + e] = run;  // becomes the chunk's exclusive offset within expert e
+      run += v;
+    }
+    c = run;
+    cnt[e] = c;
+  }
+  int total_rows;
+  const int padded = (c + kTileRows - 1) / kTileRows * kTileRows;
+  const int r0 = block_exclusive_scan(padded, tmp, &total_rows);
+  if (e < E) row0[e] = r0;
+  if (e == 0) row0[E] = total_rows;
+  const int ntile = (c + kTileRows - 1) / kTileRows;
+  const int prim = min(ntile, cap_tiles);
+  int total_prim, total_ovf;
+  const int prim_off = block_exclusive_scan(prim, tmp, &total_prim);
+  const int ovf_off = block_exclusive_scan(ntile - prim, tmp, &total_ovf);
+  if (e < E) {
+    for (int i = 0; i < ntile; ++i) {
+      const int idx = (i < prim) ? prim_off + i : total_prim + ovf_off + (i - prim);
+      tile_expert[idx] = e;
+      tile_row0[idx] = r0 + i * kTileRows;
+      tile_rows[idx] = min(kTileRows, c - i * kTileRows);
+    }
+    for (int q = r0 + c; q < r0 + padded; ++q) row_src[q] = -1;
+  }
+  const int num_tiles = total_prim + total_ovf;
+  for (int i = num_tiles + threadIdx.x; i < max_tiles; i += blockDim.x) {
+    tile_expert[i] = -1;
+    tile_row0[i] = -1;
+    tile_rows[i] = -1;
+  }
+  for (long long q = total_rows + threadIdx.x; q < max_rows; q += blockDim.x) row_src[q] = -1;
+  if (threadIdx.x == 0) {
+    header[0] = num_tiles;
+    header[1] = total_rows;
+    header[3] = total_prim;
+  }
+}
+
+// Stable scatter: within a chunk, rows are placed in ascending flat index f.
+// Each round of 256 consecutive f: rank within the warp from match_any, plus
+// the counts of the same expert in lower warps of the round, plus the running
+// offset of the expert.
+__global__ void __launch_bounds__(256) sched_scatter_kernel(const int64_t* __restrict__ te, int n, int E,
+                                                            const int* __restrict__ hist,
+                                                            const int* __restrict__ row0,
+                                                            int* __restrict__ row_src,
+                                                            int* __restrict__ slot_row,
+                                                            const int* __restrict__ header) {
+  extern __shared__ int sh[];
+  int* run = sh;               // [E]
+  int* wcnt = sh + E;          // [8][E]
+  if (header[2] != 0) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < E; i += blockDim.x) run[i] = row0[i] + hist[blockIdx.x * E + i];
+  for (int i = threadIdx.x; i < 8 * E; i += blockDim.x) wcnt[i] = 0;
+  __syncthreads();
+  const int base = blockIdx.x * kSchedChunk;
+  const int end = min(n, base + kSchedChunk);
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int r = base; r < end; r += 256) {
+    const int f = r + threadIdx.x;
+    const bool valid = f < end;
+    const int e = valid ? static_cast<int>(te[f]) : -1;
+    const unsigned m = __match_any_sync(0xffffffffu, e);
+    const int leader = __ffs(m) - 1;
+    const int rank = __popc(m & lt_mask);
+    if (valid && lane == leader) wcnt[warp * E + e] = __popc(m);
+    __syncthreads();
+    if (valid) {
+      int before = 0;
+      for (int w = 0; w < warp; ++w) before += wcnt[w * E + e];
+      const int pos = run[e] + before + rank;
+      row_src[pos] = f;
+      slot_row[f] = pos;
+    }
+    __syncthreads();
+    if (valid && lane == leader) {
+      atomicAdd(&run[e], __popc(m));
+      wcnt[warp * E + e] = 0;
+    }
+    __syncthreads();
+  }
+}
+
+cudaError_t launch_schedule(const int64_t* te, int T, int k, int E, int cap_tiles, int max_tiles,
+                            int* hist, int* cnt, int* row0, int* row_src, int* slot_row,
+                            int* tile_expert, int* tile_row0, int* tile_rows, int* header,
+                            cudaStream_t st) {
+  const int n = T * k;
+  const int nchunks = (n + kSchedChunk - 1) / kSchedChunk;
+  cudaError_t err = cudaMemsetAsync(header, 0, 8 * sizeof(int), st);
+  if (err != cudaSuccess) return err;
+  sched_count_kernel<<<nchunks, 256, E * sizeof(int), st>>>(te, n, E, hist, header);
+  sched_scan_kernel<<<1, 1024, 0, st>>>(n, E, nchunks, cap_tiles, max_tiles, hist, cnt, row0, row_src,
+                                        tile_expert, tile_row0, tile_rows, header);
+  const size_t smem = 9 * E * sizeof(int);
+  if (smem > 48 * 1024) {
+    err = cudaFuncSetAttribute(sched_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+  }
+  sched_scatter_kernel<<<nchunks, 256, smem, st>>>(te, n, E, hist, row0, row_src, slot_row, header);
+  return cudaGetLastError();
+}
+
+// ===========================================================================
+// MXFP8 quantiser ("Mixture-of-Kittens: a deterministic MoE megakernel for
+// NVL72 racks", "Tuning the five hyperparameters before production": MXFP8
+// weights are prequantised by a separate mxfp8_quantize).  One thread per
+// 1x32 block: 64 bytes in, 32 code bytes and one scale byte out.
+// ===========================================================================
+__global__ void __launch_bounds__(256) mx_quantize_kernel(const uint16_t* __restrict__ x, long long nblocks,
+                                                          uint8_t* __restrict__ codes,
+                                                          uint8_t* __restrict__ scales) {
+  for (long long b = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; b < nblocks;
+       b += static_cast<long long>(gridDim.x) * blockDim.x) {
+    float v[32];
+    load_bf16x32(x + b * 32, v);
+    scales[b] = static_cast<uint8_t>(mx_quantize32(v, codes + b * 32));
+  }
+}
+
+// Exact expansion of MXFP8 (codes, scales) to bf16: an E4M3 value times a
+// power of two keeps at most 4 significant bits.
+__global__ void __launch_bounds__(256) mx_dequant_kernel(const uint8_t* __restrict__ codes,
+                                                         const uint8_t* __restrict__ scales,
+                                                         long long nblocks, uint16_t* __restrict__ out) {
+  for (long long b = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; b < nblocks;
+       b += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int s = static_cast<int>(scales[b]) - 127;
+    float v[32];
+    const uint4* src = reinterpret_cast<const uint4*>(codes + b * 32);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const uint4 w = src[q];
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const __nv_fp8_storage_t c = static_cast<__nv_fp8_storage_t>((ws[i] >> (8 * j)) & 0xFF);
+          const __half_raw hr = __nv_cvt_fp8_to_halfraw(c, __NV_E4M3);
+          v[16 * q + 4 * i + j] = ldexpf(__half2float(__half(hr)), s);
+        }
+      }
+    }
+    store_bf16x32(out + b * 32, v);
+  }
+}
+
+static int grid_for(long long work, int per_block, int num_sms) {
+  long long g = (work + per_block - 1) / per_block;
+  const long long cap = static_cast<long long>(num_sms) * 16;
+  if (g > cap) g = cap;
+  if (g < 1) g = 1;
+  return static_cast<int>(g);
+}
+
+cudaError_t launch_mx_quantize(const uint16_t* x, long long nblocks, uint8_t* codes, uint8_t* scales,
+                               int num_sms, cudaStream_t st) {
+  if (nblocks == 0) return cudaSuccess;
+  mx_quantize_kernel<<<grid_for(nblocks, 256, num_sms), 256, 0, st>>>(x, nblocks, codes, scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_dequant(const uint8_t* codes, const uint8_t* scales, long long nblocks,
+                              uint16_t* out, int num_sms, cudaStream_t st) {
+  if (nblocks == 0) return cudaSuccess;
+  mx_dequant_kernel<<<grid_for(nblocks, 256, num_sms), 256, 0, st>>>(codes, scales, nblocks, out);
+  return cudaGetLastError();
+}
+
+// ===========================================================================
+// Fixed-order combine: out[t] = bf16(base[t] + sum_{j<k} slots[t*k + j]),
+// summed in fp32, base first, then j ascending (no floating-point atomics).
+// One thread per 8 columns of one token.
+// ===========================================================================
+__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ slots,
+                                                      const uint16_t* __restrict__ base, int T, int k,
+                                                      int H, uint16_t* __restrict__ out) {
+  const int per_row = H / 8;
+  const long long total = static_cast<long long>(T) * per_row;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long t = i / per_row;
+    const int c = static_cast<int>(i - t * per_row) * 8;
+    float acc[8];
+    if (base) {
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(base + t * H + c));
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[2 * q] = __uint_as_float(ws[q] << 16);
+        acc[2 * q + 1] = __uint_as_float(ws[q] & 0xFFFF0000u);
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+    }
+    for (int j = 0; j < k; ++j) {
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(slots + (t * k + j) * H + c));
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[2 * q] += __uint_as_float(ws[q] << 16);
+        acc[2 * q + 1] += __uint_as_float(ws[q] & 0xFFFF0000u);
+      }
+    }
+    *reinterpret_cast<uint4*>(out + t * H + c) =
+        make_uint4(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]), pack_bf16(acc[4], acc[5]),
+                   pack_bf16(acc[6], acc[7]));
+  }
+}
+
+cudaError_t launch_combine(const uint16_t* slots, const uint16_t* base, int T, int k, int H,
+                           uint16_t* out, int num_sms, cudaStream_t st) {
+  const long long total = static_cast<long long>(T) * (H / 8);
+  combine_kernel<<<grid_for(total, 256, num_sms), 256, 0, st>>>(slots, base, T, k, H, out);
+  return cudaGetLastError();
+}
+
+// d_w[f] = sum over column tiles n (ascending) of part[f][n].
+__global__ void dw_reduce_kernel(const float* __restrict__ part, int nf, int ntiles,
+                                 float* __restrict__ dw) {
+  const int f = blockIdx.x * blockDim.x + threadIdx.x;
+  if (f >= nf) return;
+  float s = 0.f;
+  for (int n = 0; n < ntiles; ++n) s += part[static_cast<long long>(f) * ntiles + n];
+  dw[f] = s;
+}
+
+cudaError_t launch_dw_reduce(const float* part, int nf, int ntiles, float* dw, cudaStream_t st) {
+  if (nf == 0) return cudaSuccess;
+  dw_reduce_kernel<<<(nf + 255) / 256, 256, 0, st>>>(part, nf, ntiles, dw);
+  return cudaGetLastError();
+}
+
+}  // namespace mok

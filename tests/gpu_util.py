@@ -1,0 +1,90 @@
+"""Helpers shared by the GPU parity tests: run the layer through the C ABI and
+compare with the oracle on the same seeded inputs."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from mixture_experts_layer_mok_gb300 import inputs as gen
+
+BF16_TOL = 5e-3     # relative L2, BF16 path and MXFP8 vs its same-quantisation oracle
+MX_UNQ_TOL = 3e-2   # relative L2, MXFP8 forward vs the unquantised oracle
+
+
+_built = False
+
+
+def mok():
+    global _built
+    if not _built:
+        import __graft_entry__ as g
+
+        g.build()
+        _built = True
+    import mixture_experts_layer_mok_gb300 as m
+
+    return m
+
+
+def rel_l2(a, b) -> float:
+    a = a.detach().double().cpu().numpy() if hasattr(a, "detach") else np.asarray(a, np.float64)
+    b = b.detach().double().cpu().numpy() if hasattr(b, "detach") else np.asarray(b, np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def weights_of(g, mode="bf16"):
+    m = mok()
+    w = m.Weights(g.w_gate, g.w_up, g.w_down, g.ws_gate, g.ws_up, g.ws_down)
+    if mode == "mxfp8":
+        w = m.quantize_weights(w)
+    return w
+
+
+def run_layer(inp, mode="bf16", capacity=0.5, minibatch=0, device="cuda"):
+    """Forward + backward through the C ABI; returns (y, grads, sched, ctx)."""
+    m = mok()
+    g = inp.to(device)
+    sched = m.schedule(g.top_experts, inp.meta["E"], capacity)
+    w = weights_of(g, mode)
+    y, ctx = m.forward(g.x, g.router_w, sched, w, mode=mode, minibatch=minibatch)
+    grads = m.backward(g.dy, g.x, g.router_w, sched, ctx, w, minibatch=minibatch)
+    torch.cuda.synchronize()
+    return y, grads, sched, ctx
+
+
+def oracle_args(inp):
+    return (inp.x, inp.router_w, inp.top_experts, inp.w_gate, inp.w_up, inp.w_down,
+            inp.ws_gate, inp.ws_up, inp.ws_down)
+
+
+def oracle_fwd_bwd(inp, mode="bf16"):
+    a = oracle_args(inp)
+    if mode == "mxfp8":
+        y = oracle.layer_forward_mxfp8(*a)
+        g = oracle.layer_backward_mxfp8(*a[:6], inp.dy, *a[6:])
+    else:
+        y = oracle.layer_forward(*a)
+        g = oracle.layer_backward(*a[:6], inp.dy, *a[6:])
+    return y, g
+
+
+GRAD_KEYS = ("dx", "d_router_w", "d_w_gate", "d_w_up", "d_w_down", "d_ws_gate", "d_ws_up", "d_ws_down")
+
+
+def compare_all(y, grads, y_ref, g_ref, tol=BF16_TOL):
+    errs = {"y": rel_l2(y, y_ref)}
+    for key in GRAD_KEYS:
+        if key in g_ref:
+            errs[key] = rel_l2(grads[key], g_ref[key])
+    bad = {k: v for k, v in errs.items() if not v <= tol}
+    return errs, bad
+
+
+def subset_inputs(inp, tokens):
+    """The same layer restricted to a subset of tokens (the layer is per-token
+    in y, dx and d_router_w)."""
+    idx = torch.as_tensor(tokens, dtype=torch.int64)
+    return gen.LayerInputs(inp.x[idx], inp.router_w[idx], inp.top_experts[idx], inp.w_gate, inp.w_up,
+                           inp.w_down, inp.ws_gate, inp.ws_up, inp.ws_down,
+                           None if inp.dy is None else inp.dy[idx], dict(inp.meta))

@@ -1,0 +1,162 @@
+"""GPU parity of the layer forward and backward against the CPU oracle, plus
+determinism, invariance and device-error checks."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mixture_experts_layer_mok_gb300 import inputs as gen
+from tests.gpu_util import (BF16_TOL, MX_UNQ_TOL, compare_all, mok, oracle_args, oracle_fwd_bwd, rel_l2,
+                            run_layer, subset_inputs, weights_of)
+
+pytestmark = pytest.mark.gpu
+
+# (T, H, I, E, k, I_s, skew): the tiny layer, a ragged-T layer with a shared
+# expert whose I is not a multiple of 256, a skewed layer with empty and hot
+# experts (several tiles), and a 2-tile-wide H with a 1-expert layer.
+SHAPES = {
+    "tiny": (128, 128, 256, 8, 2, 0, None),
+    "ragged_shared": (200, 256, 384, 5, 3, 256, None),
+    "skewed": (333, 128, 128, 16, 4, 0, 1.2),
+    "one_expert": (300, 384, 128, 1, 1, 128, None),
+    "wide": (520, 512, 256, 12, 6, 384, 1.2),
+}
+
+
+def _inputs(name, seed=0):
+    T, H, I, E, k, I_s, skew = SHAPES[name]
+    inp = gen.make_layer_inputs(T, H, I, E, k, I_s, skew=skew, seed=seed)
+    inp.meta.update(name=name)
+    return inp
+
+
+@pytest.mark.parametrize("name", list(SHAPES))
+def test_bf16_forward_backward_matches_oracle(name):
+    inp = _inputs(name)
+    y, grads, sched, ctx = run_layer(inp, "bf16")
+    assert ctx.status() == 0
+    y_ref, g_ref = oracle_fwd_bwd(inp, "bf16")
+    errs, bad = compare_all(y, grads, y_ref, g_ref, BF16_TOL)
+    assert not bad, errs
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged_shared", "wide"])
+def test_mxfp8_forward_matches_same_quantisation_oracle(name):
+    inp = _inputs(name, seed=1)
+    y, grads, sched, ctx = run_layer(inp, "mxfp8")
+    assert ctx.status() == 0
+    y_ref, g_ref = oracle_fwd_bwd(inp, "mxfp8")
+    errs, bad = compare_all(y, grads, y_ref, g_ref, BF16_TOL)
+    assert not bad, errs
+    y_unq = oracle.layer_forward(*oracle_args(inp))
+    assert rel_l2(y, y_unq) <= MX_UNQ_TOL
+
+
+def test_repeated_runs_bitwise_identical():
+    inp = _inputs("wide", seed=2)
+    a = run_layer(inp, "bf16")
+    b = run_layer(inp, "bf16")
+    assert torch.equal(a[0], b[0])
+    for key in a[1]:
+        assert torch.equal(a[1][key], b[1][key]), key
+
+
+def test_capacity_and_minibatch_change_no_bit():
+    inp = _inputs("skewed", seed=3)
+    base = run_layer(inp, "bf16", capacity=1.0, minibatch=0)
+    for c, mb in ((0.0, 0), (0.05, 64), (0.5, 128), (3.0, 1)):
+        other = run_layer(inp, "bf16", capacity=c, minibatch=mb)
+        assert torch.equal(base[0], other[0]), (c, mb)
+        for key in base[1]:
+            assert torch.equal(base[1][key], other[1][key]), (c, mb, key)
+
+
+def test_zero_router_weights_give_shared_expert_only():
+    inp = _inputs("ragged_shared", seed=4)
+    inp.router_w.zero_()
+    y, grads, _, _ = run_layer(inp, "bf16")
+    y_ref, g_ref = oracle_fwd_bwd(inp, "bf16")
+    assert rel_l2(y, y_ref) <= BF16_TOL
+    assert grads["d_w_down"].abs().max().item() == 0.0
+    assert rel_l2(grads["d_router_w"], g_ref["d_router_w"]) <= BF16_TOL
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    m = mok()
+    inp = _inputs("tiny", seed=5)
+    g = inp.to("cuda")
+    sched = m.schedule(g.top_experts, inp.meta["E"], 0.5)
+    w = weights_of(g)
+    y, ctx = m.forward(g.x, g.router_w, sched, w, debug=1)   # withholds one accumulator signal
+    assert ctx.status() == 5                                  # MOK_ERR_TIMEOUT
+    # the context is still usable: a normal call afterwards is correct
+    y2, ctx2 = m.forward(g.x, g.router_w, sched, w)
+    assert ctx2.status() == 0
+    y_ref = oracle.layer_forward(*oracle_args(inp))
+    assert rel_l2(y2, y_ref) <= BF16_TOL
+
+
+def test_bad_expert_id_blocks_the_layer_and_reports():
+    m = mok()
+    inp = _inputs("tiny", seed=6)
+    inp.top_experts[7, 1] = 99
+    g = inp.to("cuda")
+    sched = m.schedule(g.top_experts, inp.meta["E"], 0.5)
+    w = weights_of(g)
+    y, ctx = m.forward(g.x, g.router_w, sched, w)
+    assert ctx.status() == 2                                  # MOK_ERR_INDEX
+
+
+def test_host_argument_errors():
+    m = mok()
+    inp = _inputs("tiny")
+    g = inp.to("cuda")
+    sched = m.schedule(g.top_experts, inp.meta["E"], 0.5)
+    w = weights_of(g)
+    with pytest.raises(ValueError):
+        m.forward(g.x.float(), g.router_w, sched, w)            # wrong dtype
+    bad = m.Weights(g.w_gate[:, :, :96].contiguous(), g.w_up[:, :, :96].contiguous(),
+                    g.w_down[:, :96].contiguous())
+    with pytest.raises(ValueError):
+        m.forward(g.x[:, :96].contiguous(), g.router_w, sched, bad)   # H outside the contract
+    with pytest.raises(m.MokError) as ei:
+        m.forward(g.x, g.router_w, sched, w, mode="mxfp8")     # no prequantised weights
+    assert ei.value.code == 1
+
+
+@pytest.mark.parametrize("mode", ["bf16", "mxfp8"])
+def test_full_size_T4096_sampled(mode):
+    """The bf16 / mxfp8 T=4096 layers (H=2048, I=1024, E=64, k=8, I_s=2048) at full
+    size, in the launch configuration the benchmark times: y, dx and d_router_w
+    on 48 sampled tokens, and the full weight gradients of the hottest and the
+    coldest expert, against the oracle."""
+    inp = gen.make_workload("bf16_T4096" if mode == "bf16" else "mxfp8_T4096", seed=0)
+    y, grads, sched, ctx = run_layer(inp, mode, capacity=0.5, minibatch=2048)
+    assert ctx.status() == 0
+    rng = np.random.default_rng(0)
+    tok = np.sort(rng.choice(inp.meta["T"], 48, replace=False))
+    sub = subset_inputs(inp, tok)
+    y_ref, g_ref = oracle_fwd_bwd(sub, mode)
+    assert rel_l2(y[tok], y_ref) <= BF16_TOL
+    assert rel_l2(grads["dx"][tok], g_ref["dx"]) <= BF16_TOL
+    assert rel_l2(grads["d_router_w"][tok], g_ref["d_router_w"]) <= BF16_TOL
+    # full weight gradients of the hottest and the coldest expert: only the rows
+    # routed to expert e reach dW[e], so a k = 1 layer over those rows gives it
+    te = inp.top_experts.numpy()
+    cnt = np.bincount(te.reshape(-1), minlength=inp.meta["E"])
+    for e in (int(cnt.argmax()), int(cnt.argmin())):
+        t_e, j_e = np.nonzero(te == e)
+        idx = torch.as_tensor(t_e)
+        sub_e = gen.LayerInputs(inp.x[idx], inp.router_w[idx, j_e].reshape(-1, 1).contiguous(),
+                                torch.full((len(t_e), 1), e, dtype=torch.int64), inp.w_gate, inp.w_up,
+                                inp.w_down, None, None, None, inp.dy[idx], dict(inp.meta))
+        _, ge = oracle_fwd_bwd(sub_e, mode)
+        for key in ("d_w_gate", "d_w_up", "d_w_down"):
+            assert rel_l2(grads[key][e], ge[key][e]) <= BF16_TOL, (e, key)
+    # shared expert gradients: a layer with no routed experts gives them alone
+    if inp.ws_gate is not None:
+        sub_s = gen.LayerInputs(inp.x, inp.router_w, inp.top_experts, inp.w_gate[:0], inp.w_up[:0],
+                                inp.w_down[:0], inp.ws_gate, inp.ws_up, inp.ws_down, inp.dy, dict(inp.meta))
+        _, gs = oracle_fwd_bwd(sub_s, mode)
+        for key in ("d_ws_gate", "d_ws_up", "d_ws_down"):
+            assert rel_l2(grads[key], gs[key]) <= BF16_TOL, key

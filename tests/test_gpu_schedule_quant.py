@@ -1,0 +1,98 @@
+"""GPU parity of the integer / byte steps: the schedule and the MXFP8 quantiser
+must match the oracle bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mixture_experts_layer_mok_gb300 import inputs as gen
+from tests.gpu_util import mok
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_schedule(te, E, c):
+    m = mok()
+    s = m.schedule(te.cuda(), E, c)
+    st, nt, P = s.status()
+    ref = oracle.build_schedule(te.numpy(), E, c)
+    assert st == ref["status"] == 0
+    assert nt == ref["num_tiles"] and P == ref["P"]
+    arr = {k: v.cpu().numpy() for k, v in s.arrays().items()}
+    for key in ("cnt", "row0", "row_src", "slot_row", "tile_expert", "tile_row0", "tile_rows"):
+        assert np.array_equal(arr[key], ref[key]), key
+    assert arr["header"][3] == ref["num_primary"]
+
+
+@pytest.mark.parametrize("T,k,E,skew,c", [
+    (128, 2, 8, None, 0.5),            # tiny layer
+    (4096, 8, 64, None, 0.5),          # bf16 / mxfp8 T=4096 layers
+    (16384, 8, 128, 1.2, 0.5),         # skewed routing, capacity 0.5
+    (16384, 8, 128, 1.2, 1.0),         # skewed routing, capacity 1.0
+    (65536, 8, 256, None, 0.5),        # large layer
+    (1, 1, 1, None, 0.5), (5, 3, 7, None, 0.0), (4097, 5, 1000, None, 0.5), (3000, 16, 64, 1.2, 0.01),
+])
+def test_schedule_bit_exact(T, k, E, skew, c):
+    te = gen.make_routing(T, k, E, seed=T + E, skew=skew)
+    _check_schedule(te, E, c)
+
+
+def test_schedule_repeated_calls_identical():
+    m = mok()
+    te = gen.make_routing(8192, 8, 64, seed=3).cuda()
+    a = m.schedule(te, 64, 0.5)
+    b = m.schedule(te, 64, 0.5)
+    torch.cuda.synchronize()
+    for (name, x), y in zip(a.arrays().items(), b.arrays().values()):
+        assert torch.equal(x, y), name
+
+
+def test_schedule_bad_expert_id_reports_index_error():
+    m = mok()
+    te = gen.make_routing(300, 4, 16, seed=1)
+    te[123, 2] = 16
+    s = m.schedule(te.cuda(), 16, 0.5)
+    st, nt, P = s.status()
+    assert st == 2 and nt == 0
+    te[123, 2] = -5
+    assert m.schedule(te.cuda(), 16, 0.5).status()[0] == 2
+
+
+def _check_quant(x):
+    m = mok()
+    codes, scales = m.mxfp8_quantize(x.cuda())
+    rc, rs = oracle.mxfp8_quantize(x.double().reshape(-1, x.shape[-1]).numpy())
+    assert np.array_equal(codes.cpu().numpy().reshape(rc.shape), rc)
+    assert np.array_equal(scales.cpu().numpy().reshape(rs.shape), rs)
+
+
+@pytest.mark.parametrize("R,K,std", [(1, 32, 1.0), (257, 96, 1.0), (1024, 2048, 0.02), (64, 7168, 3.0),
+                                     (2048, 4096, 1e-3)])
+def test_quantize_bit_exact(R, K, std):
+    _check_quant(gen.make_matrix(R, K, std=std, seed=R + K))
+
+
+def test_quantize_edge_values():
+    table = oracle.e4m3_decode(np.arange(256, dtype=np.uint8))
+    fin = table[np.isfinite(table)]
+    # exact grid values and midpoints scaled by assorted powers of two, zeros,
+    # negative zeros, tiny and huge magnitudes, bf16 subnormals
+    mids = (np.sort(np.unique(np.abs(fin)))[1:] + np.sort(np.unique(np.abs(fin)))[:-1]) / 2
+    v = np.concatenate([fin, mids, -mids, [0.0, -0.0] * 16, [3e38, -3e38, 1e-38, -1e-39, 9e-41, -9e-41]])
+    v = np.concatenate([v * 2.0 ** s for s in (-100, -9, 0, 3, 100)])
+    x = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16)
+    x = x[torch.isfinite(x)]           # the quantiser's inputs are finite
+    x = x[: x.numel() // 32 * 32].reshape(-1, 32)
+    _check_quant(x)
+    # all-zero and single-nonzero blocks
+    z = torch.zeros(4, 64, dtype=torch.bfloat16)
+    z[1, 5] = -1.0
+    z[2, 40] = 448.0
+    z[3, :] = -0.0
+    _check_quant(z)
+
+
+def test_quantize_empty():
+    m = mok()
+    c, s = m.mxfp8_quantize(torch.empty(0, 64, dtype=torch.bfloat16, device="cuda"))
+    assert c.numel() == 0 and s.numel() == 0

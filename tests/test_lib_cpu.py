@@ -1,0 +1,92 @@
+"""CPU-side checks of the C ABI: the library builds, loads without a GPU,
+exports every symbol include/mok.h declares, sizes its buffers consistently
+and rejects bad arguments before touching the device."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__ as g
+
+    g.build()
+    from mixture_experts_layer_mok_gb300 import _lib
+
+    return _lib.load()
+
+
+def _header_symbols():
+    text = open(os.path.join(ROOT, "include", "mok.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mok_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    syms = _header_symbols()
+    assert len(syms) >= 11
+    for s in syms:
+        assert hasattr(lib, s), s
+    from mixture_experts_layer_mok_gb300 import _lib
+
+    assert sorted(_lib.SIGNATURES) == syms
+
+
+def test_version_and_error(lib):
+    assert lib.mok_version() >= 1
+    assert isinstance(lib.mok_last_error(), bytes)
+
+
+def test_buffer_sizes(lib):
+    T, k, E = 4096, 8, 64
+    mt = (T * k + 127 * E) // 128
+    sb = lib.mok_schedule_bytes(T, k, E)
+    assert sb >= 4 * (E + E + 1 + mt * 128 + T * k + 3 * mt + 8)
+    H, I, Is = 2048, 1024, 2048
+    cb = lib.mok_ctx_bytes(T, k, E, H, I, Is, 0)
+    # gate|up + h per padded row, slots per routed row, shared gate|up/h/out
+    assert cb >= 2 * (mt * 128 * 3 * I + T * k * H + T * 3 * Is + T * H)
+    assert lib.mok_ctx_bytes(T, k, E, H, I, Is, 1) > cb   # MXFP8 adds codes / scales
+    wb = lib.mok_bwd_workspace_bytes(T, k, E, H, I, Is)
+    assert wb >= 2 * (mt * 128 * 3 * I + T * k * H)
+    # shapes outside the contract report 0
+    assert lib.mok_ctx_bytes(T, k, E, 100, I, Is, 0) == 0
+    assert lib.mok_ctx_bytes(T, k, E, H, 96, Is, 0) == 0
+    assert lib.mok_schedule_bytes(0, k, E) == 0
+
+
+def test_argument_errors_need_no_device(lib):
+    from mixture_experts_layer_mok_gb300 import _lib
+
+    s = _lib.MokSchedule()
+    assert lib.mok_schedule(None, 4, 2, 8, 0.5, None, 0, C.byref(s), None) == _lib.MOK_ERR_INVALID_ARG
+    buf = C.create_string_buffer(1 << 16)
+    fake = C.c_void_p(16)  # never dereferenced: validation fails first
+    assert lib.mok_schedule(fake, 4, 0, 8, 0.5, fake, 1 << 16, C.byref(s), None) == _lib.MOK_ERR_INVALID_ARG
+    assert lib.mok_schedule(fake, 4, 2, 2000, 0.5, fake, 1 << 16, C.byref(s), None) == _lib.MOK_ERR_INVALID_ARG
+    assert lib.mok_schedule(fake, 4, 2, 8, float("nan"), fake, 1 << 16, C.byref(s), None) == \
+        _lib.MOK_ERR_INVALID_ARG
+    assert lib.mok_schedule(fake, 4, 2, 8, -1.0, fake, 1 << 16, C.byref(s), None) == _lib.MOK_ERR_INVALID_ARG
+    assert lib.mok_schedule(fake, 4, 2, 8, 0.5, fake, 16, C.byref(s), None) == _lib.MOK_ERR_INVALID_ARG
+    assert b"too small" in lib.mok_last_error()
+    assert lib.mok_mxfp8_quantize(fake, 4, 33, fake, fake, None) == _lib.MOK_ERR_INVALID_ARG
+    assert lib.mok_mxfp8_quantize(C.c_void_p(17), 4, 64, fake, fake, None) == _lib.MOK_ERR_INVALID_ARG
+    assert lib.mok_mxfp8_quantize(None, 0, 64, None, None, None) == _lib.MOK_OK   # empty input
+    cfg = _lib.MokConfig(mode=7)
+    assert lib.mok_forward(C.byref(cfg), fake, fake, C.byref(s), None, fake, fake, 0, None, None) == \
+        _lib.MOK_ERR_INVALID_ARG
+    del buf
+
+
+def test_package_import_does_not_load_library():
+    import subprocess
+    import sys
+
+    code = ("import sys; sys.path.insert(0, %r); import mixture_experts_layer_mok_gb300 as m; "
+            "from mixture_experts_layer_mok_gb300 import _lib; print(_lib._lib is None)") % ROOT
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, check=True)
+    assert out.stdout.strip() == "True"
