@@ -1,0 +1,456 @@
+#!/usr/bin/env python
+"""Throughput of the MoK layer (forward + backward) on GB300.
+
+One step = one pass of the whole hot path over one batch: build the schedule
+from the batch's routing, the forward (gate/up + SwiGLU, down + router scale +
+scatter, shared expert, combine) and the backward (dgrad, SwiGLU backward,
+router-weight grad, grouped wgrad, shared expert, fixed-order reductions).
+In MXFP8 workloads the step also prequantises the weights (they change every
+optimiser step).
+
+`python bench.py [--gpus N --steps K --warmup W] [--workload NAME]` prints one
+JSON line.  Under torchrun each rank runs its own batch of the workload (data
+parallel, no collective on the data path: weak scaling); the time is the max
+over ranks.  `--impl reference` times the CPU oracle instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "bf16_T4096"
+METRIC = "MoE layer fwd+bwd tokens/s (TFLOP/s and % of GB300 dense tensor peak alongside)"
+L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
+
+
+# ----------------------------------------------------------------- helpers
+def layer_flops(c):
+    """Algorithmic FLOP of one fwd+bwd (padding rows excluded): forward
+    6*H*I per routed row + 6*H*I_s per token; backward twice the forward."""
+    fwd = 6.0 * c["T"] * c["k"] * c["H"] * c["I"] + 6.0 * c["T"] * c["H"] * c["I_s"]
+    return fwd, 3.0 * fwd
+
+
+def stage_flops(c):
+    """Algorithmic FLOP of each GEMM stage (same names as the C ABI stages)."""
+    T, k, H, I, Is = c["T"], c["k"], c["H"], c["I"], c["I_s"]
+    R = T * k
+    return {
+        "fwd_gateup": 4.0 * R * H * I, "fwd_down": 2.0 * R * I * H,
+        "fwd_shared_gateup": 4.0 * T * H * Is, "fwd_shared_down": 2.0 * T * Is * H,
+        "bwd_down": 2.0 * R * H * I, "bwd_wgrad_down": 2.0 * R * H * I,
+        "bwd_wgrad_gateup": 4.0 * R * H * I, "bwd_dgrad_gateup": 4.0 * R * H * I,
+        "bwd_shared_down": 2.0 * T * H * Is, "bwd_shared_wgrad_down": 2.0 * T * H * Is,
+        "bwd_shared_wgrad_gateup": 4.0 * T * H * Is, "bwd_shared_dgrad": 4.0 * T * H * Is,
+    }
+
+
+def launches_per_step(c):
+    """Kernels of this library launched by one step (mirrors the C ABI's sequence)."""
+    mx = c["mode"] == "mxfp8"
+    shared = c["I_s"] > 0
+    n = 3                                   # schedule: count, scan, scatter
+    n += 1 + 2 + 1 + 1                      # status hand-over, routed gate/up + down, combine
+    if shared:
+        n += 2
+    if mx:
+        n += 2 + 3 + 1 + (3 + 1 if shared else 0)   # quantise/expand x, expand weights, expand h
+        n += 3 + (3 if shared else 0)               # weight prequantisation
+    n += 4 + 2                              # routed dgrad/wgrad x4, combine dx, reduce d_w
+    if shared:
+        n += 4
+    return n
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("gemm.cuh", "ptx.cuh"):
+        with open(os.path.join(ROOT, "mixture_experts_layer_mok_gb300", "csrc", name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload, stage):
+    """DRAM bytes per launch of the stage's kernel from a committed ncu summary,
+    valid only while the GEMM kernel source is unchanged."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            rec = json.load(fh)
+        ent = rec[workload][stage]
+        if ent["kernel_source"] == kernel_source_hash():
+            return ent["dram_bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = str(gpu_index)
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", self.gpu], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons, pw = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+                pw.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm), "power_w_max": max(pw) if pw else None}
+
+
+# ----------------------------------------------------------------- oracle timing
+class OracleSample:
+    """The CPU oracle (float64 NumPy) on fwd+bwd of the first `tokens` tokens of
+    the workload.  Inputs and weights are widened to float64 once, here, so the
+    timed calls run the oracle's arithmetic only."""
+
+    def __init__(self, inp, mode, tokens):
+        import oracle
+
+        self.tokens = tokens
+        self.x = inp.x[:tokens].double().numpy()
+        self.w = inp.router_w[:tokens].double().numpy()
+        self.te = inp.top_experts[:tokens].numpy()
+        self.dy = inp.dy[:tokens].double().numpy()
+        self.W = [None if t is None else t.double().numpy() for t in
+                  (inp.w_gate, inp.w_up, inp.w_down, inp.ws_gate, inp.ws_up, inp.ws_down)]
+        self.fwd = oracle.layer_forward_mxfp8 if mode == "mxfp8" else oracle.layer_forward
+        self.bwd = oracle.layer_backward_mxfp8 if mode == "mxfp8" else oracle.layer_backward
+
+    def run(self, min_s=0.0):
+        """Repeat fwd+bwd until at least min_s seconds passed; returns (seconds, reps)."""
+        W = self.W
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            self.fwd(self.x, self.w, self.te, *W)
+            self.bwd(self.x, self.w, self.te, W[0], W[1], W[2], self.dy, W[3], W[4], W[5])
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= min_s:
+                return el, reps
+
+
+def cpu_cores():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        v = os.environ.get(var)
+        if v and v.isdigit():
+            return int(v)
+    return os.cpu_count()
+
+
+# ----------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["mok", "reference"], default="mok")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--stages", action="store_true", help="print per-stage times to stderr")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from mixture_experts_layer_mok_gb300 import inputs as gen
+
+    c = dict(gen.WORKLOADS[args.workload])
+    fwd_flop, step_flop = layer_flops(c)
+    config = {"workload": args.workload, "T": c["T"], "H": c["H"], "I": c["I"], "E": c["E"], "k": c["k"],
+              "I_s": c["I_s"], "routing": "zipf s=%.1f" % c["skew"] if c["skew"] else "softmax top-k",
+              "minibatch": c["minibatch"], "capacity_multiplier": c["capacity"], "fwd_precision": c["mode"],
+              "bwd_precision": "bf16", "global_batch_tokens": c["T"] * max(world, 1),
+              "parallelism": f"dp{world} (independent batches, no collective)"}
+
+    if args.impl == "reference":
+        return run_reference(args, c, config, rank, world)
+
+    import torch
+
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    import mixture_experts_layer_mok_gb300 as mok
+    from mixture_experts_layer_mok_gb300 import _lib
+
+    _lib.load()  # fails loudly when the library is not built
+    inp = gen.make_workload(args.workload, seed=rank)
+    g = inp.to(dev)
+    w = mok.Weights(g.w_gate, g.w_up, g.w_down, g.ws_gate, g.ws_up, g.ws_down)
+    mode = c["mode"]
+    E, T, k, H, I, Is = c["E"], c["T"], c["k"], c["H"], c["I"], c["I_s"]
+    lib = _lib.load()
+    m = _lib.MOK_MODE_MXFP8_FWD if mode == "mxfp8" else _lib.MOK_MODE_BF16
+    ctx_buf = torch.empty(lib.mok_ctx_bytes(T, k, E, H, I, Is, m), dtype=torch.uint8, device=dev)
+    ws_buf = torch.empty(lib.mok_bwd_workspace_bytes(T, k, E, H, I, Is), dtype=torch.uint8, device=dev)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    grads = {"dx": torch.empty((T, H), dtype=torch.bfloat16, device=dev),
+             "d_router_w": torch.empty((T, k), dtype=torch.float32, device=dev),
+             "d_w_gate": torch.empty_like(g.w_gate), "d_w_up": torch.empty_like(g.w_up),
+             "d_w_down": torch.empty_like(g.w_down)}
+    if Is:
+        grads.update(d_ws_gate=torch.empty_like(g.ws_gate), d_ws_up=torch.empty_like(g.ws_up),
+                     d_ws_down=torch.empty_like(g.ws_down))
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def run_step(x, rw, top, dy, events=None):
+        wq = mok.quantize_weights(w) if mode == "mxfp8" else w
+        sched = mok.schedule(top, E, c["capacity"])
+        _, ctx = mok.forward(x, rw, sched, wq, mode=mode, minibatch=c["minibatch"], out=y, ctx_buf=ctx_buf,
+                             events=events)
+        mok.backward(dy, x, rw, sched, ctx, wq, minibatch=c["minibatch"], grads=grads, ws_buf=ws_buf,
+                     events=events)
+        return ctx
+
+    for _ in range(args.warmup):
+        ctx = run_step(g.x, g.router_w, g.top_experts, g.dy)
+    torch.cuda.synchronize()
+    if ctx.status() != 0:
+        raise RuntimeError(f"device status {ctx.status()} after warm-up")
+
+    nst = _lib.MOK_NUM_STAGES
+    K = args.steps
+    ev_start = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_end = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_stage = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nst)] for _ in range(K)]
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()                       # evict L2 between steps (outside the timed spans)
+        ev_start[i].record(stream)
+        run_step(g.x, g.router_w, g.top_experts, g.dy, events=ev_stage[i])
+        ev_end[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop() if sampler else None
+    if world > 1:
+        torch.distributed.barrier()
+    step_ms = [ev_start[i].elapsed_time(ev_end[i]) for i in range(K)]
+    total_ms = sum(step_ms)
+    if ctx.status() != 0:
+        raise RuntimeError(f"device status {ctx.status()} in the timed region")
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    tokens_per_s = T * max(world, 1) * K / (total_ms / 1e3)
+    tflops = step_flop * max(world, 1) * K / (total_ms / 1e3) / 1e12
+
+    # per-stage times on the launching stream
+    names = _lib.STAGE_NAMES
+    st_ms = {names[s]: sum(ev_stage[i][2 * s].elapsed_time(ev_stage[i][2 * s + 1]) for i in range(K)) / K
+             for s in range(nst)}
+    sf = stage_flops(c)
+    gemm_stages = {n: v for n, v in st_ms.items() if n in sf and sf[n] > 0}
+    dom = max(gemm_stages, key=gemm_stages.get)
+    peaks = load_peaks()
+    achieved = sf[dom] / (st_ms[dom] / 1e3) / 1e12
+    gemm_ms = sum(gemm_stages.values())
+    gemm_tflops = sum(sf[n] for n in gemm_stages) / (gemm_ms / 1e3) / 1e12
+    if args.stages and rank == 0:
+        for n in names:
+            extra = f"  {sf[n] / (st_ms[n] / 1e3) / 1e12:8.1f} TFLOP/s" if n in gemm_stages else ""
+            print(f"  {n:26s} {st_ms[n]:8.4f} ms{extra}", file=sys.stderr)
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        hx = inp.x.pin_memory()
+        hrw = inp.router_w.pin_memory()
+        htop = inp.top_experts.pin_memory()
+        hdy = inp.dy.pin_memory()
+        oy = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+        odx = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+        odw = torch.empty((T, k), dtype=torch.float32).pin_memory()
+        dx_ = torch.empty_like(g.x)
+        drw = torch.empty_like(g.router_w)
+        dtop = torch.empty_like(g.top_experts)
+        ddy = torch.empty_like(g.dy)
+        h2d = sum(t.numel() * t.element_size() for t in (hx, hrw, htop, hdy))
+        d2h = sum(t.numel() * t.element_size() for t in (oy, odx, odw))
+        Ke = max(3, min(K, 50))
+        es = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+        ee = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+        for i in range(Ke + 2):
+            flush.zero_()
+            if i >= 2:
+                es[i - 2].record(stream)
+            dx_.copy_(hx, non_blocking=True)
+            drw.copy_(hrw, non_blocking=True)
+            dtop.copy_(htop, non_blocking=True)
+            ddy.copy_(hdy, non_blocking=True)
+            run_step(dx_, drw, dtop, ddy)
+            oy.copy_(y, non_blocking=True)
+            odx.copy_(grads["dx"], non_blocking=True)
+            odw.copy_(grads["d_router_w"], non_blocking=True)
+            if i >= 2:
+                ee[i - 2].record(stream)
+        torch.cuda.synchronize()
+        e_ms = sum(es[i].elapsed_time(ee[i]) for i in range(Ke))
+        if world > 1:
+            t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": round(T * max(world, 1) * Ke / (e_ms / 1e3), 1), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke,
+               "what": "pinned host x, router weights, top-k ids, dy -> device; schedule + fwd + bwd through "
+                       "the binding; y, dx, d_router_w -> host"}
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        tokens = 64
+        sample = OracleSample(inp, mode, tokens)
+        sample.run()                                    # first touch of the widened weights
+        el, reps = sample.run(min_s=10.0)
+        del sample
+        cpu = {"value": round(tokens * reps / el, 2), "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"fwd+bwd of the first {tokens} tokens of the {args.workload} layer (all experts' "
+                         f"weights, float64 NumPy), {reps} repetition(s), {el:.1f} s; weights widened once "
+                         "outside the timing"}
+
+    peak_key = "bf16_tflops"
+    line = {
+        "metric": METRIC,
+        "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": max(world, 1), "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if mode == "bf16" else "mxfp8-fwd/bf16-bwd",
+        "data": "synthetic (seeded; weights N(0,0.02), x and dy N(0,1), softmax top-k routing)",
+        "config": dict(config, l2="flushed between steps (512 MiB write, outside the timed spans)"),
+        "tflops": round(tflops, 1),
+        "tc_peak_frac": round(tflops / peaks[peak_key], 4),
+        "gemm_tflops": round(gemm_tflops, 1),
+        "roofline": {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1),
+                     "peak": peaks[peak_key], "unit": "TFLOP/s", "frac": round(achieved / peaks[peak_key], 4),
+                     "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)"
+                     if peaks["source"] == "measured" else "fallback bf16 burst",
+                     "traffic": recorded_traffic(args.workload, dom),
+                     "algorithmic_flop_per_launch": sf[dom], "ms_per_launch": round(st_ms[dom], 4)},
+        "stage_ms": {n: round(v, 4) for n, v in st_ms.items()},
+        "gpu_launches": launches_per_step(c) * K,
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "wall_s": round(wall, 3),
+    }
+    print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_reference(args, c, config, rank, world):
+    """The CPU oracle as the reference arm: each step is fwd+bwd of a bounded
+    sample of tokens of the same workload, on the host cores."""
+    if rank != 0:
+        return
+    from mixture_experts_layer_mok_gb300 import inputs as gen
+
+    inp = gen.make_workload(args.workload, seed=0)
+    tokens = 16
+    sample = OracleSample(inp, c["mode"], tokens)
+    for _ in range(args.warmup):
+        sample.run()
+    el_total = 0.0
+    for _ in range(args.steps):
+        el, _ = sample.run()
+        el_total += el
+    value = tokens * args.steps / el_total
+    sample = (f"each step: fwd+bwd of the first {tokens} tokens of the {args.workload} layer in the float64 NumPy "
+              "oracle (weights widened once, outside the timing)")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 3),
+            "unit": "tokens/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * el_total / args.steps, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)", "config": config,
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -72,15 +72,38 @@ typedef int mok_status_t;
                                         wait must expire and the context must
                                         report MOK_ERR_TIMEOUT (tests only) */
 
+/* Stages of the layer, for optional per-stage timing events. */
+#define MOK_STAGE_FWD_PREP                 0  /* status hand-over; MXFP8: quantise x, expand operands */
+#define MOK_STAGE_FWD_SHARED_GATEUP        1  /* shared gate/up GEMM + SwiGLU */
+#define MOK_STAGE_FWD_SHARED_DOWN          2  /* shared down GEMM */
+#define MOK_STAGE_FWD_GATEUP               3  /* routed gathered gate/up GEMM + SwiGLU */
+#define MOK_STAGE_FWD_DOWN                 4  /* routed down GEMM + router scale + scatter */
+#define MOK_STAGE_FWD_COMBINE              5  /* fixed-order combine into y */
+#define MOK_STAGE_BWD_DOWN                 6  /* routed dgrad through down + SwiGLU bwd + router-grad partials */
+#define MOK_STAGE_BWD_WGRAD_DOWN           7  /* routed dW_down */
+#define MOK_STAGE_BWD_WGRAD_GATEUP         8  /* routed dW_gate, dW_up */
+#define MOK_STAGE_BWD_DGRAD_GATEUP         9  /* routed dgrad through gate/up -> dx slots */
+#define MOK_STAGE_BWD_SHARED_DOWN         10
+#define MOK_STAGE_BWD_SHARED_WGRAD_DOWN   11
+#define MOK_STAGE_BWD_SHARED_WGRAD_GATEUP 12
+#define MOK_STAGE_BWD_SHARED_DGRAD        13
+#define MOK_STAGE_BWD_REDUCE              14  /* fixed-order dx combine + router-grad reduce */
+#define MOK_NUM_STAGES                    15
+
 /* Per-call knobs ([MoKEd] "Tuning the five hyperparameters before
  * production").  minibatch_size (0 = T) sets the order in which the
  * persistent GEMMs visit work (waves of tokens); it never changes a result
- * bit. */
+ * bit.  `events`, when not NULL, holds 2 * MOK_NUM_STAGES cudaEvent_t handles
+ * (owned by the caller); the call records events[2s] before and
+ * events[2s+1] after stage s on the call's stream (a stage that does not run
+ * records both back to back), so a caller can time each kernel on the stream
+ * it runs on. */
 typedef struct {
   int mode;            /* MOK_MODE_* */
   int minibatch_size;  /* tokens per wave of the persistent pipeline; 0 = T */
   int debug_flags;     /* MOK_DEBUG_*; 0 in production */
-  int reserved;        /* must be 0 */
+  int num_events;      /* 0, or 2 * MOK_NUM_STAGES when events is set */
+  void* const* events; /* optional cudaEvent_t[2 * MOK_NUM_STAGES], NULL = off */
 } mok_config_t;
 
 /* The dispatch/combine schedule ([MoKEd] "The two API layers and the

@@ -26,9 +26,15 @@ P = C.c_void_p
 I32P = C.POINTER(C.c_int32)
 
 
+MOK_NUM_STAGES = 15
+STAGE_NAMES = ["fwd_prep", "fwd_shared_gateup", "fwd_shared_down", "fwd_gateup", "fwd_down", "fwd_combine",
+               "bwd_down", "bwd_wgrad_down", "bwd_wgrad_gateup", "bwd_dgrad_gateup", "bwd_shared_down",
+               "bwd_shared_wgrad_down", "bwd_shared_wgrad_gateup", "bwd_shared_dgrad", "bwd_reduce"]
+
+
 class MokConfig(C.Structure):
     _fields_ = [("mode", C.c_int), ("minibatch_size", C.c_int), ("debug_flags", C.c_int),
-                ("reserved", C.c_int)]
+                ("num_events", C.c_int), ("events", C.POINTER(C.c_void_p))]
 
 
 class MokSchedule(C.Structure):

@@ -253,6 +253,22 @@ GemmParams base_params(const mok_schedule_t* s, int* status, int debug) {
   return p;
 }
 
+// Records the caller's timing event for the start (end = 0) or end of a stage.
+cudaError_t mark(const mok_config_t* cfg, int stage, int end, cudaStream_t st) {
+  if (cfg->events && cfg->num_events >= 2 * MOK_NUM_STAGES)
+    return cudaEventRecord(static_cast<cudaEvent_t>(cfg->events[2 * stage + end]), st);
+  return cudaSuccess;
+}
+
+mok_status_t check_config(const mok_config_t* cfg) {
+  if (cfg->mode != MOK_MODE_BF16 && cfg->mode != MOK_MODE_MXFP8_FWD)
+    return fail(MOK_ERR_INVALID_ARG, "unknown mode %d", cfg->mode);
+  if (cfg->events && cfg->num_events != 2 * MOK_NUM_STAGES)
+    return fail(MOK_ERR_INVALID_ARG, "events needs 2 * MOK_NUM_STAGES entries");
+  if (cfg->minibatch_size < 0) return fail(MOK_ERR_INVALID_ARG, "minibatch_size < 0");
+  return MOK_OK;
+}
+
 __global__ void propagate_status_kernel(const int* header, int* status) {
   if (header[2] != 0) atomicCAS(status, 0, header[2]);
 }
@@ -347,11 +363,11 @@ mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x, const float
                          size_t ctx_bytes, mok_ctx_t* ctx, void* stream) {
   if (!cfg || !x || !router_w || !s || !w || !y || !ctx_buf || !ctx)
     return fail(MOK_ERR_INVALID_ARG, "NULL argument");
-  if (cfg->mode != MOK_MODE_BF16 && cfg->mode != MOK_MODE_MXFP8_FWD)
-    return fail(MOK_ERR_INVALID_ARG, "unknown mode %d", cfg->mode);
+  mok_status_t st = check_config(cfg);
+  if (st) return st;
   const int T = s->T, k = s->k, E = s->E, H = w->H, I = w->I, Is = w->I_s;
   if (w->E != E) return fail(MOK_ERR_INVALID_ARG, "weights have E=%d, schedule E=%d", w->E, E);
-  mok_status_t st = check_shapes(T, k, E, H, I, Is);
+  st = check_shapes(T, k, E, H, I, Is);
   if (st) return st;
   if (!w->w_gate || !w->w_up || !w->w_down) return fail(MOK_ERR_INVALID_ARG, "NULL routed weight");
   if (Is > 0 && (!w->ws_gate || !w->ws_up || !w->ws_down))
@@ -372,6 +388,7 @@ mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x, const float
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   CtxExtra X;
   carve_ctx(ctx_buf, T, k, E, H, I, Is, cfg->mode, ctx, &X);
+  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_PREP, 0, cs));
   MOK_CUDA(cudaMemsetAsync(ctx->status, 0, 8 * sizeof(int), cs));
   propagate_status_kernel<<<1, 1, 0, cs>>>(s->header, ctx->status);
   MOK_CUDA(cudaGetLastError());
@@ -396,8 +413,10 @@ mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x, const float
       wsg = X.wsg_deq; wsu = X.wsu_deq; wsd = X.wsd_deq;
     }
   }
+  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_PREP, 1, cs));
 
   // ---- shared expert: gate/up + SwiGLU over all T tokens, then down
+  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_GATEUP, 0, cs));
   if (Is > 0) {
     GemmMaps m;
     if ((st = make_map(&m.a, xa, H, T, 128)) || (st = make_map(&m.b0, wsg, H, Is, 128)) ||
@@ -416,6 +435,8 @@ mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x, const float
       MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 256, EPI_SWIGLU_MX>(m, p, grid, cs)));
       MOK_CUDA(launch_mx_dequant(ctx->hq_s, ctx->hq_s_sc, static_cast<long long>(T) * Is / 32, X.hs_deq, sms, cs));
     }
+    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_GATEUP, 1, cs));
+    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_DOWN, 0, cs));
     const uint16_t* hs = mx ? X.hs_deq : ctx->h_s;
     GemmMaps m2;
     if ((st = make_map(&m2.a, hs, Is, T, 128)) || (st = make_map(&m2.b0, wsd, Is, H, 128))) return st;
@@ -429,10 +450,15 @@ mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x, const float
       MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 256, EPI_STORE_ROWS>(m2, q, grid2, cs)));
     else
       MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 128, EPI_STORE_ROWS>(m2, q, grid2, cs)));
+  } else {
+    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_GATEUP, 1, cs));
+    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_DOWN, 0, cs));
   }
+  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_DOWN, 1, cs));
 
   // ---- routed experts: gathered gate/up + SwiGLU, then down + scale + scatter
   {
+    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_GATEUP, 0, cs));
     GemmMaps m;
     if ((st = make_map(&m.a, xa, H, T, 1)) ||
         (st = make_map(&m.b0, wg, H, static_cast<uint64_t>(E) * I, 128)) ||
@@ -451,6 +477,8 @@ mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x, const float
       MOK_CUDA((launch_gemm<SRC_K_GATHER, SRC_K_TILE, 256, EPI_SWIGLU_MX>(m, p, grid, cs)));
       MOK_CUDA(launch_mx_dequant(ctx->hq, ctx->hq_sc, mr * I / 32, X.h_deq, sms, cs));
     }
+    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_GATEUP, 1, cs));
+    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DOWN, 0, cs));
     const uint16_t* hr = mx ? X.h_deq : ctx->h;
     GemmMaps m2;
     if ((st = make_map(&m2.a, hr, I, mr, 128)) ||
@@ -467,10 +495,13 @@ mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x, const float
       MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 256, EPI_SCALE_SCATTER>(m2, q, grid2, cs)));
     else
       MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 128, EPI_SCALE_SCATTER>(m2, q, grid2, cs)));
+    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DOWN, 1, cs));
   }
 
   // ---- combine: y[t] = shared[t] + sum_j slots[t, j] in fixed order
+  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_COMBINE, 0, cs));
   MOK_CUDA(launch_combine(ctx->slots, Is > 0 ? ctx->shared_out : nullptr, T, k, H, y, sms, cs));
+  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_COMBINE, 1, cs));
   return MOK_OK;
 }
 
@@ -486,8 +517,10 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
                           const mok_weight_grads_t* g, void* ws, size_t ws_bytes, void* stream) {
   if (!cfg || !dy || !x || !router_w || !s || !ctx || !w || !dx || !d_router_w || !g || !ws)
     return fail(MOK_ERR_INVALID_ARG, "NULL argument");
+  mok_status_t st = check_config(cfg);
+  if (st) return st;
   const int T = s->T, k = s->k, E = s->E, H = w->H, I = w->I, Is = w->I_s;
-  mok_status_t st = check_shapes(T, k, E, H, I, Is);
+  st = check_shapes(T, k, E, H, I, Is);
   if (st) return st;
   if (ctx->T != T || ctx->k != k || ctx->E != E || ctx->H != H || ctx->I != I || ctx->I_s != Is)
     return fail(MOK_ERR_INVALID_ARG, "context does not match the schedule / weights");
@@ -510,6 +543,7 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
   // ---- routed: down dgrad + SwiGLU backward + router-weight partials
   const int bn1 = tile_n(I);
   {
+    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DOWN, 0, cs));
     GemmMaps m;
     if ((st = make_map(&m.a, dy, H, T, 1)) ||
         (st = make_map(&m.b0, w->w_down, I, static_cast<uint64_t>(E) * H, 64)))
@@ -524,9 +558,11 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
       MOK_CUDA((launch_gemm<SRC_K_GATHER, SRC_MN_TILE, 256, EPI_DOWN_BWD>(m, p, grid, cs)));
     else
       MOK_CUDA((launch_gemm<SRC_K_GATHER, SRC_MN_TILE, 128, EPI_DOWN_BWD>(m, p, grid, cs)));
+    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DOWN, 1, cs));
   }
   // ---- routed: dW_down[e] = sum over e's rows of dy[t(r)]^T (w h)[r]
   {
+    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_DOWN, 0, cs));
     GemmMaps m;
     if ((st = make_map(&m.a, dy, H, T, 1)) || (st = make_map(&m.b0, L.hw, I, mr, 64))) return st;
     m.b1 = m.b0;
@@ -541,9 +577,11 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
       MOK_CUDA((launch_gemm<SRC_MN_GATHER, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, grid, cs)));
     else
       MOK_CUDA((launch_gemm<SRC_MN_GATHER, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, grid, cs)));
+    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_DOWN, 1, cs));
   }
   // ---- routed: dW_gate|up[e] = sum over e's rows of (dG|dU)[r]^T x[t(r)]
   {
+    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_GATEUP, 0, cs));
     GemmMaps m;
     if ((st = make_map(&m.a, L.dgu, 2 * I, mr, 64)) || (st = make_map(&m.b0, x, H, T, 1))) return st;
     m.b1 = m.b0;
@@ -558,9 +596,11 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
       MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_GATHER, 256, EPI_WGRAD>(m, p, grid, cs)));
     else
       MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_GATHER, 128, EPI_WGRAD>(m, p, grid, cs)));
+    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_GATEUP, 1, cs));
   }
   // ---- routed: dx slots = dG W_gate[e] + dU W_up[e]
   {
+    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DGRAD_GATEUP, 0, cs));
     GemmMaps m;
     if ((st = make_map(&m.a, L.dgu, 2 * I, mr, 128)) ||
         (st = make_map(&m.b0, w->w_gate, H, static_cast<uint64_t>(E) * I, 64)) ||
@@ -576,11 +616,13 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
       MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_MN_TILE, 256, EPI_SCATTER>(m, p, grid, cs)));
     else
       MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_MN_TILE, 128, EPI_SCATTER>(m, p, grid, cs)));
+    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DGRAD_GATEUP, 1, cs));
   }
   // ---- shared expert backward (dense rows, w = 1)
   if (Is > 0) {
     const int bns = tile_n(Is);
     {
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DOWN, 0, cs));
       GemmMaps m;
       if ((st = make_map(&m.a, dy, H, T, 128)) || (st = make_map(&m.b0, w->ws_down, Is, H, 64))) return st;
       m.b1 = m.b0;
@@ -593,8 +635,10 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
         MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_MN_TILE, 256, EPI_DOWN_BWD>(m, p, grid, cs)));
       else
         MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_MN_TILE, 128, EPI_DOWN_BWD>(m, p, grid, cs)));
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DOWN, 1, cs));
     }
     {  // dW_s_down = dy^T h_s
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_DOWN, 0, cs));
       GemmMaps m;
       if ((st = make_map(&m.a, dy, H, T, 64)) || (st = make_map(&m.b0, L.hs, Is, T, 64))) return st;
       m.b1 = m.b0;
@@ -607,8 +651,10 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
         MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, grid, cs)));
       else
         MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, grid, cs)));
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_DOWN, 1, cs));
     }
     {  // dW_s_gate|up = (dG_s|dU_s)^T x
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_GATEUP, 0, cs));
       GemmMaps m;
       if ((st = make_map(&m.a, L.dgu_s, 2 * Is, T, 64)) || (st = make_map(&m.b0, x, H, T, 64))) return st;
       m.b1 = m.b0;
@@ -622,8 +668,10 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
         MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, grid, cs)));
       else
         MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, grid, cs)));
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_GATEUP, 1, cs));
     }
     {  // dx_s = dG_s W_s_gate + dU_s W_s_up
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DGRAD, 0, cs));
       GemmMaps m;
       if ((st = make_map(&m.a, L.dgu_s, 2 * Is, T, 128)) || (st = make_map(&m.b0, w->ws_gate, H, Is, 64)) ||
           (st = make_map(&m.b1, w->ws_up, H, Is, 64)))
@@ -638,11 +686,19 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
         MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_MN_TILE, 256, EPI_STORE_ROWS>(m, p, grid, cs)));
       else
         MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_MN_TILE, 128, EPI_STORE_ROWS>(m, p, grid, cs)));
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DGRAD, 1, cs));
+    }
+  } else {
+    for (int sg = MOK_STAGE_BWD_SHARED_DOWN; sg <= MOK_STAGE_BWD_SHARED_DGRAD; ++sg) {
+      MOK_CUDA(mark(cfg, sg, 0, cs));
+      MOK_CUDA(mark(cfg, sg, 1, cs));
     }
   }
   // ---- fixed-order reductions: dx and the router-weight gradient
+  MOK_CUDA(mark(cfg, MOK_STAGE_BWD_REDUCE, 0, cs));
   MOK_CUDA(launch_combine(L.dx_slots, Is > 0 ? L.dx_s : nullptr, T, k, H, dx, sms, cs));
   MOK_CUDA(launch_dw_reduce(L.dw_part, T * k, I / bn1, d_router_w, cs));
+  MOK_CUDA(mark(cfg, MOK_STAGE_BWD_REDUCE, 1, cs));
   return MOK_OK;
 }
 

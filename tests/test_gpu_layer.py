@@ -48,8 +48,13 @@ def test_mxfp8_forward_matches_same_quantisation_oracle(name):
     y_ref, g_ref = oracle_fwd_bwd(inp, "mxfp8")
     errs, bad = compare_all(y, grads, y_ref, g_ref, BF16_TOL)
     assert not bad, errs
+    # Against the unquantised layer: quantising x, W_gate, W_up, h and W_down to
+    # E4M3 (3 mantissa bits) puts the oracle's own MXFP8 forward about 6.5e-2
+    # (rel-L2) away from the unquantised one, above a 3e-2 bound.  The GPU may add
+    # no more than the same-quantisation tolerance to that intrinsic gap.
     y_unq = oracle.layer_forward(*oracle_args(inp))
-    assert rel_l2(y, y_unq) <= MX_UNQ_TOL
+    intrinsic = rel_l2(y_ref, y_unq)
+    assert rel_l2(y, y_unq) <= max(MX_UNQ_TOL, intrinsic + BF16_TOL), (rel_l2(y, y_unq), intrinsic)
 
 
 def test_repeated_runs_bitwise_identical():
@@ -160,3 +165,23 @@ def test_full_size_T4096_sampled(mode):
         _, gs = oracle_fwd_bwd(sub_s, mode)
         for key in ("d_ws_gate", "d_ws_up", "d_ws_down"):
             assert rel_l2(grads[key], gs[key]) <= BF16_TOL, key
+
+
+def test_stage_events_time_each_stage():
+    m = mok()
+    from mixture_experts_layer_mok_gb300 import _lib
+
+    inp = _inputs("ragged_shared", seed=7)
+    g = inp.to("cuda")
+    sched = m.schedule(g.top_experts, inp.meta["E"], 0.5)
+    w = weights_of(g)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * _lib.MOK_NUM_STAGES)]
+    y, ctx = m.forward(g.x, g.router_w, sched, w, events=ev)
+    m.backward(g.dy, g.x, g.router_w, sched, ctx, w, events=ev)
+    torch.cuda.synchronize()
+    ms = [ev[2 * s].elapsed_time(ev[2 * s + 1]) for s in range(_lib.MOK_NUM_STAGES)]
+    assert all(v >= 0 for v in ms)
+    for name in ("fwd_gateup", "fwd_down", "bwd_down", "bwd_wgrad_gateup", "bwd_shared_dgrad"):
+        assert ms[_lib.STAGE_NAMES.index(name)] > 0, name
+    with pytest.raises(ValueError):
+        m.forward(g.x, g.router_w, sched, w, events=ev[:3])
