@@ -71,6 +71,10 @@ typedef int mok_status_t;
                                         accumulator-ready signal, so a bounded
                                         wait must expire and the context must
                                         report MOK_ERR_TIMEOUT (tests only) */
+#define MOK_DEBUG_TMA_GATHER4     2  /* fetch gathered token rows with TMA
+                                        tile::gather4 loads instead of the
+                                        gather warps' cp.async copies (same
+                                        results, slower; kept for comparison) */
 
 /* Stages of the layer, for optional per-stage timing events. */
 #define MOK_STAGE_FWD_PREP                 0  /* status hand-over; MXFP8: quantise x, expand operands */

@@ -18,6 +18,7 @@ MOK_ERR_CUDA = 6
 MOK_MODE_BF16 = 0
 MOK_MODE_MXFP8_FWD = 1
 MOK_DEBUG_DROP_ACC_SIGNAL = 1
+MOK_DEBUG_TMA_GATHER4 = 2
 
 STATUS_NAMES = {0: "MOK_OK", 1: "MOK_ERR_INVALID_ARG", 2: "MOK_ERR_INDEX", 3: "MOK_ERR_CAPACITY",
                 4: "MOK_ERR_UNSUPPORTED", 5: "MOK_ERR_TIMEOUT", 6: "MOK_ERR_CUDA"}

@@ -386,6 +386,7 @@ mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x, const float
   st = device_info(&sms);
   if (st) return st;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const bool g4 = (cfg->debug_flags & MOK_DEBUG_TMA_GATHER4) != 0;
   CtxExtra X;
   carve_ctx(ctx_buf, T, k, E, H, I, Is, cfg->mode, ctx, &X);
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_PREP, 0, cs));
@@ -466,15 +467,21 @@ mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x, const float
       return st;
     GemmParams p = base_params(s, ctx->status, cfg->debug_flags);
     p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / 128; p.b_rows_per_expert = I;
-    p.out0 = ctx->gu;
+    p.out0 = ctx->gu; p.ga = xa; p.ga_ld = H;
     const long long items = static_cast<long long>(s->max_tiles) * p.n_tiles;
     const int grid = items < sms ? static_cast<int>(items) : sms;
     if (!mx) {
       p.out1 = ctx->h;
-      MOK_CUDA((launch_gemm<SRC_K_GATHER, SRC_K_TILE, 256, EPI_SWIGLU>(m, p, grid, cs)));
+      if (g4)
+        MOK_CUDA((launch_gemm<SRC_K_GATHER, SRC_K_TILE, 256, EPI_SWIGLU>(m, p, grid, cs)));
+      else
+        MOK_CUDA((launch_gemm<SRC_K_GATHER_LSU, SRC_K_TILE, 256, EPI_SWIGLU>(m, p, grid, cs)));
     } else {
       p.out1 = ctx->hq; p.out2 = ctx->hq_sc;
-      MOK_CUDA((launch_gemm<SRC_K_GATHER, SRC_K_TILE, 256, EPI_SWIGLU_MX>(m, p, grid, cs)));
+      if (g4)
+        MOK_CUDA((launch_gemm<SRC_K_GATHER, SRC_K_TILE, 256, EPI_SWIGLU_MX>(m, p, grid, cs)));
+      else
+        MOK_CUDA((launch_gemm<SRC_K_GATHER_LSU, SRC_K_TILE, 256, EPI_SWIGLU_MX>(m, p, grid, cs)));
       MOK_CUDA(launch_mx_dequant(ctx->hq, ctx->hq_sc, mr * I / 32, X.h_deq, sms, cs));
     }
     MOK_CUDA(mark(cfg, MOK_STAGE_FWD_GATEUP, 1, cs));
@@ -536,6 +543,7 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
   st = device_info(&sms);
   if (st) return st;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const bool g4 = (cfg->debug_flags & MOK_DEBUG_TMA_GATHER4) != 0;
   BwdLayout L;
   carve_bwd(ws, T, k, E, H, I, Is, &L);
   const long long mr = static_cast<long long>(s->max_tiles) * kTileRows;
@@ -552,12 +560,17 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
     GemmParams p = base_params(s, ctx->status, 0);
     p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / bn1; p.b_rows_per_expert = H;
     p.aux0 = ctx->gu; p.out0 = L.dgu; p.out1 = L.hw; p.rw = router_w; p.dw_part = L.dw_part;
+    p.ga = dy; p.ga_ld = H;
     const long long items = static_cast<long long>(s->max_tiles) * p.n_tiles;
     const int grid = items < sms ? static_cast<int>(items) : sms;
-    if (bn1 == 256)
+    if (g4 && bn1 == 256)
       MOK_CUDA((launch_gemm<SRC_K_GATHER, SRC_MN_TILE, 256, EPI_DOWN_BWD>(m, p, grid, cs)));
-    else
+    else if (g4)
       MOK_CUDA((launch_gemm<SRC_K_GATHER, SRC_MN_TILE, 128, EPI_DOWN_BWD>(m, p, grid, cs)));
+    else if (bn1 == 256)
+      MOK_CUDA((launch_gemm<SRC_K_GATHER_LSU, SRC_MN_TILE, 256, EPI_DOWN_BWD>(m, p, grid, cs)));
+    else
+      MOK_CUDA((launch_gemm<SRC_K_GATHER_LSU, SRC_MN_TILE, 128, EPI_DOWN_BWD>(m, p, grid, cs)));
     MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DOWN, 1, cs));
   }
   // ---- routed: dW_down[e] = sum over e's rows of dy[t(r)]^T (w h)[r]
@@ -571,12 +584,17 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
     p.wgrad = 1; p.grouped = 1; p.E = E; p.m_tiles = H / 128; p.n_tiles = I / bn;
     p.out0 = g->d_w_down; p.out1 = g->d_w_down; p.ld = I; p.split = H;
     p.estride = static_cast<long long>(H) * I;
+    p.ga = dy; p.ga_ld = H;
     const long long items = static_cast<long long>(E) * p.m_tiles * p.n_tiles;
     const int grid = items < sms ? static_cast<int>(items) : sms;
-    if (bn == 256)
+    if (g4 && bn == 256)
       MOK_CUDA((launch_gemm<SRC_MN_GATHER, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, grid, cs)));
-    else
+    else if (g4)
       MOK_CUDA((launch_gemm<SRC_MN_GATHER, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, grid, cs)));
+    else if (bn == 256)
+      MOK_CUDA((launch_gemm<SRC_MN_GATHER_LSU, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, grid, cs)));
+    else
+      MOK_CUDA((launch_gemm<SRC_MN_GATHER_LSU, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, grid, cs)));
     MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_DOWN, 1, cs));
   }
   // ---- routed: dW_gate|up[e] = sum over e's rows of (dG|dU)[r]^T x[t(r)]
@@ -590,12 +608,17 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
     p.wgrad = 1; p.grouped = 1; p.E = E; p.m_tiles = 2 * I / 128; p.n_tiles = H / bn;
     p.out0 = g->d_w_gate; p.out1 = g->d_w_up; p.ld = H; p.split = I;
     p.estride = static_cast<long long>(I) * H;
+    p.gb = x; p.gb_ld = H;
     const long long items = static_cast<long long>(E) * p.m_tiles * p.n_tiles;
     const int grid = items < sms ? static_cast<int>(items) : sms;
-    if (bn == 256)
+    if (g4 && bn == 256)
       MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_GATHER, 256, EPI_WGRAD>(m, p, grid, cs)));
-    else
+    else if (g4)
       MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_GATHER, 128, EPI_WGRAD>(m, p, grid, cs)));
+    else if (bn == 256)
+      MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_GATHER_LSU, 256, EPI_WGRAD>(m, p, grid, cs)));
+    else
+      MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_GATHER_LSU, 128, EPI_WGRAD>(m, p, grid, cs)));
     MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_GATEUP, 1, cs));
   }
   // ---- routed: dx slots = dG W_gate[e] + dU W_up[e]

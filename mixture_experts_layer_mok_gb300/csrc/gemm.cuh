@@ -1,18 +1,22 @@
 // Persistent grouped GEMM engine on tcgen05 / TMEM / TMA for sm_103a.
 //
-// One CTA per SM, 192 threads:
-//   warp 0      TMA producer: tile loads, and tile::gather4 loads that fetch
-//               the token rows of a schedule tile straight into shared memory
-//               (the on-chip form of MoK's dispatch exchange);
+// One CTA per SM, 192 threads (320 when an operand is gathered):
+//   warp 0      TMA producer: tile loads of the operands that are not gathered
+//               (and, on request, tile::gather4 loads of the gathered ones);
 //   warp 1      MMA issuer (one thread) and TMEM owner;
 //   warps 2..5  epilogue: TMEM -> registers -> fused elementwise -> HBM
 //               (SwiGLU, MXFP8 requantisation, router scaling, scatter to
-//               per-(token, k) slots, SwiGLU backward, router-weight grad).
-// Warp 0/1 (data movement) overlap with warps 2-5 (output) on a
-// double-buffered TMEM accumulator: the single-GPU analogue of MoK's split of
-// SMs into communication and compute roles ("Mixture-of-Kittens: a
-// deterministic MoE megakernel for NVL72 racks", "Tuning the five
-// hyperparameters before production": fwd/bwd_num_comm_sms).
+//               per-(token, k) slots, SwiGLU backward, router-weight grad);
+//   warps 6..9  gather producers: 16-byte cp.async copies of the token rows a
+//               schedule tile needs, written straight into the 128-byte-
+//               swizzled stage layout the tensor core reads (the on-chip form
+//               of MoK's dispatch exchange).
+// The data-movement warps (0, 6..9) and the output warps (2..5) overlap the
+// MMA warp through a ring of shared-memory stages and a double-buffered TMEM
+// accumulator: the single-GPU analogue of MoK's split of SMs into
+// communication and compute roles ("Mixture-of-Kittens: a deterministic MoE
+// megakernel for NVL72 racks", "Tuning the five hyperparameters before
+// production": fwd/bwd_num_comm_sms).
 //
 // Work items are output tiles of 128 rows x BN columns; each is produced by
 // exactly one CTA with a fixed K order, so results do not depend on which CTA
@@ -30,14 +34,15 @@ namespace mok {
 
 constexpr int kBM = 128;        // rows of an output tile (TMEM lanes)
 constexpr int kBK = 64;         // bf16 elements per 128-byte swizzled row
-constexpr int kThreads = 192;
 constexpr int kChunkBytes = 64 * 128;  // one MN-major chunk: 64 K-rows x 64 elements
 
 enum Src : int {
-  SRC_K_TILE = 0,     // K-major rows [p0, p0+128) of a 2-D tensor (box 64 x 128)
-  SRC_K_GATHER = 1,   // K-major: the 128 token rows of a schedule tile (box 64 x 1)
-  SRC_MN_TILE = 2,    // MN-major: K-rows [k, k+64) of a 2-D tensor (box 64 x 64)
-  SRC_MN_GATHER = 3,  // MN-major: 64 token rows of a schedule range (box 64 x 1)
+  SRC_K_TILE = 0,         // K-major rows [p0, p0+128) of a 2-D tensor (TMA box 64 x 128)
+  SRC_K_GATHER = 1,       // K-major: the 128 token rows of a schedule tile (TMA gather4, box 64 x 1)
+  SRC_MN_TILE = 2,        // MN-major: K-rows [k, k+64) of a 2-D tensor (TMA box 64 x 64)
+  SRC_MN_GATHER = 3,      // MN-major: 64 token rows of a schedule range (TMA gather4, box 64 x 1)
+  SRC_K_GATHER_LSU = 4,   // as SRC_K_GATHER, copied by the gather warps (cp.async)
+  SRC_MN_GATHER_LSU = 5,  // as SRC_MN_GATHER, copied by the gather warps (cp.async)
 };
 
 enum Epi : int {
@@ -90,6 +95,11 @@ struct GemmParams {
   long long estride; // EPI_WGRAD: elements per expert in out0 / out1
   int* status;       // device status word
   int debug;         // MOK_DEBUG_* flags
+  // ---- gathered operands (gather warps): token-row tensors [T][ld]
+  const uint16_t* ga;
+  long long ga_ld;
+  const uint16_t* gb;
+  long long gb_ld;
 };
 
 struct Item {
@@ -148,6 +158,12 @@ __device__ __forceinline__ Item get_item(const GemmParams& p, int idx) {
 __device__ __forceinline__ int token_of(const GemmParams& p, int q) {
   const int f = __ldg(p.row_src + q);
   return f >= 0 ? f / p.topk : 0;
+}
+
+// Token row of schedule row q, or -1 for a padding row (copied as zeros).
+__device__ __forceinline__ int token_or_pad(const GemmParams& p, int q) {
+  const int f = __ldg(p.row_src + q);
+  return f >= 0 ? f / p.topk : -1;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -221,10 +237,17 @@ __device__ __forceinline__ uint32_t mx_quantize32(const float* v, uint8_t* codes
 
 template <int A_SRC, int B_SRC, int BN, int EPI>
 struct GemmCfg {
-  static constexpr bool kAMN = (A_SRC == SRC_MN_TILE || A_SRC == SRC_MN_GATHER);
-  static constexpr bool kBMN = (B_SRC == SRC_MN_TILE || B_SRC == SRC_MN_GATHER);
+  static constexpr bool kAMN = (A_SRC == SRC_MN_TILE || A_SRC == SRC_MN_GATHER || A_SRC == SRC_MN_GATHER_LSU);
+  static constexpr bool kBMN = (B_SRC == SRC_MN_TILE || B_SRC == SRC_MN_GATHER || B_SRC == SRC_MN_GATHER_LSU);
+  static constexpr bool kALsu = (A_SRC == SRC_K_GATHER_LSU || A_SRC == SRC_MN_GATHER_LSU);
+  static constexpr bool kBLsu = (B_SRC == SRC_MN_GATHER_LSU);
+  static constexpr bool kHasLsu = kALsu || kBLsu;
+  static constexpr int kThreads = kHasLsu ? 320 : 192;
+  static constexpr int kGatherLag = 2;   // cp.async groups a gather thread keeps in flight
   static constexpr int kABytes = kBM * kBK * 2;
   static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kTmaBytes = (kALsu ? 0 : kABytes) + (kBLsu ? 0 : kBBytes);
+  static constexpr uint32_t kFullArrivals = kHasLsu ? 5 : 1;  // TMA warp + 4 gather warps
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = (BN == 256) ? 4 : 6;
   static constexpr int kTmemCols = 2 * BN;  // two accumulator buffers
@@ -232,6 +255,8 @@ struct GemmCfg {
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
   static constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, kAMN, kBMN);
   static_assert(BN == 128 || BN == 256, "tile N");
+  static_assert(kGatherLag < kStages - 1, "gather lag must leave a stage free");
+  static_assert(!(kALsu && kBLsu), "one gathered operand per GEMM");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
@@ -243,8 +268,49 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// Token of the K-row that lane `lane` of gather warp `gw` fetches for the
+// shuffles of an MN-major gather (rows k0 .. k0+63 of the item's K range).
+template <int B_SRC, int BN>
+__device__ __forceinline__ int mn_gather_token(const GemmParams& p, const Item& it, int kb, int gw, int lane) {
+  if (lane >= 16) return -1;
+  int r;
+  if (B_SRC == SRC_MN_GATHER_LSU && BN == 256)
+    r = lane * 4 + gw;                              // rows i*4 + gw, i = 0..15
+  else
+    r = (lane >> 1) * 8 + gw * 2 + (lane & 1);      // rows i*8 + gw*2 + h, i = 0..7, h = 0..1
+  return token_or_pad(p, it.kbeg + kb * kBK + r);
+}
+
+// One MN-major gathered chunk set: 64 K-rows x (64 * nchunk) elements; each
+// K-row is a contiguous run of the token's row at column col0.
+template <int NCHUNK>
+__device__ __forceinline__ void gather_mn(uint8_t* dst, const uint16_t* src, long long ld, int col0, int tok_reg,
+                                          int gw, int lane) {
+  if (NCHUNK == 4) {  // 32 pieces of 16 B per K-row: one K-row per warp per step
+    const int cc = lane >> 3, q = lane & 7;
+    const uint16_t* base = src + col0 + cc * 64 + q * 8;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int r = i * 4 + gw;
+      const int tok = __shfl_sync(0xffffffffu, tok_reg, i);
+      cp_async16(dst + cc * kChunkBytes + r * 128 + ((q ^ (r & 7)) << 4),
+                 base + static_cast<long long>(tok < 0 ? 0 : tok) * ld, tok >= 0 ? 16u : 0u);
+    }
+  } else {            // 16 pieces per K-row: two K-rows per warp per step
+    const int piece = lane & 15, cc = piece >> 3, q = piece & 7;
+    const uint16_t* base = src + col0 + cc * 64 + q * 8;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = i * 8 + gw * 2 + (lane >> 4);
+      const int tok = __shfl_sync(0xffffffffu, tok_reg, i * 2 + (lane >> 4));
+      cp_async16(dst + cc * kChunkBytes + r * 128 + ((q ^ (r & 7)) << 4),
+                 base + static_cast<long long>(tok < 0 ? 0 : tok) * ld, tok >= 0 ? 16u : 0u);
+    }
+  }
+}
+
 template <int A_SRC, int B_SRC, int BN, int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
     gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
   using C = GemmCfg<A_SRC, B_SRC, BN, EPI>;
   extern __shared__ uint8_t smem_raw[];
@@ -264,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], C::kFullArrivals);
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -322,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        if (lane == 0) mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+        if (lane == 0) mbar_arrive_expect_tx(&full[stage], C::kTmaBytes);
         __syncwarp();
         uint8_t* sA = smem + stage * C::kStageBytes;
         uint8_t* sB = sA + C::kABytes;
@@ -336,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane < 2)
             tma_load_2d(sA + lane * kChunkBytes, &maps.a, &full[stage], it.m0 + 64 * lane,
                         it.kbeg + k0);
-        } else {  // SRC_MN_GATHER
+        } else if (A_SRC == SRC_MN_GATHER) {
           const int c = lane >> 4, g = lane & 15;
           tma_gather4(sA + c * kChunkBytes + g * 512, &maps.a, &full[stage], it.m0 + 64 * c, cur[0],
                       cur[1], cur[2], cur[3]);
@@ -450,6 +516,75 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every MMA issued by this thread must finish before TMEM is released
       umma_commit(done);
       mbar_drain(done, 0);
+    }
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------ gather warps
+    if constexpr (C::kHasLsu) {
+      const int gw = warp - 6;
+      int stage = 0;
+      uint32_t phase = 0;
+      int npend = 0;  // filled stages whose arrival this warp still owes (the latest ones)
+      for (int idx = blockIdx.x; idx < nitems; idx += gridDim.x) {
+        const Item it = get_item(p, idx);
+        const int bn_out = (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_MX) ? BN / 2 : BN;
+        const int n0 = it.nt * bn_out;
+        // K-major gather: this lane holds the token of tile row (lane>>2)*16 + gw*4 + (lane&3)
+        int rtok = -1;
+        if (A_SRC == SRC_K_GATHER_LSU) {
+          const int r = (lane >> 2) * 16 + gw * 4 + (lane & 3);
+          rtok = (r < it.rows) ? token_or_pad(p, it.p0 + r) : -1;
+        }
+        constexpr bool kMN = (A_SRC == SRC_MN_GATHER_LSU || B_SRC == SRC_MN_GATHER_LSU);
+        int ktok = (kMN && it.nk > 0) ? mn_gather_token<B_SRC, BN>(p, it, 0, gw, lane) : -1;
+        bool ok = true;
+        for (int kb = 0; kb < it.nk; ++kb) {
+          const int cur = ktok;
+          int w = (lane == 0) ? (mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status) ? 1 : 0) : 0;
+          w = __shfl_sync(0xffffffffu, w, 0);
+          if (!w) {
+            ok = false;
+            break;
+          }
+          uint8_t* sA = smem + stage * C::kStageBytes;
+          uint8_t* sB = sA + C::kABytes;
+          const int k0 = kb * kBK;
+          if (A_SRC == SRC_K_GATHER_LSU) {
+            const int c = lane & 7;
+            const uint16_t* base = p.ga + k0 + c * 8;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int row = i * 16 + gw * 4 + (lane >> 3);
+              const int tok = __shfl_sync(0xffffffffu, rtok, i * 4 + (lane >> 3));
+              cp_async16(sA + row * 128 + ((c ^ (row & 7)) << 4),
+                         base + static_cast<long long>(tok < 0 ? 0 : tok) * p.ga_ld, tok >= 0 ? 16u : 0u);
+            }
+          } else if (A_SRC == SRC_MN_GATHER_LSU) {
+            gather_mn<2>(sA, p.ga, p.ga_ld, it.m0, cur, gw, lane);
+          }
+          if (B_SRC == SRC_MN_GATHER_LSU) gather_mn<BN / 64>(sB, p.gb, p.gb_ld, n0, cur, gw, lane);
+          cp_async_commit();
+          ++npend;
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+          if (npend > C::kGatherLag) {
+            cp_async_wait<C::kGatherLag>();
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full[(stage - npend + C::kStages) % C::kStages]);
+            --npend;
+          }
+          if (kMN && kb + 1 < it.nk) ktok = mn_gather_token<B_SRC, BN>(p, it, kb + 1, gw, lane);
+        }
+        if (!ok) break;
+      }
+      // every copy issued has landed; signal the stages still owed
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      __syncwarp();
+      for (; npend > 0; --npend)
+        if (lane == 0) mbar_arrive(&full[(stage - npend + C::kStages) % C::kStages]);
     }
   } else {
     // ------------------------------------------------------------ epilogue

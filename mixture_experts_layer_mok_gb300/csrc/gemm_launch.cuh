@@ -14,7 +14,7 @@ cudaError_t launch_gemm(const GemmMaps& maps, const GemmParams& p, int grid, cud
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (err != cudaSuccess) return err;
-  kern<<<grid, kThreads, C::kSmemBytes, st>>>(maps, p);
+  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(maps, p);
   return cudaGetLastError();
 }
 

@@ -185,3 +185,47 @@ def test_stage_events_time_each_stage():
         assert ms[_lib.STAGE_NAMES.index(name)] > 0, name
     with pytest.raises(ValueError):
         m.forward(g.x, g.router_w, sched, w, events=ev[:3])
+
+
+@pytest.mark.parametrize("name", ["skewed", "wide"])
+def test_gather_warps_and_tma_gather4_agree_bitwise(name):
+    """The dispatch gather by the gather warps (cp.async) and by TMA
+    tile::gather4 move the same bytes, so every output must be identical."""
+    m = mok()
+    inp = _inputs(name, seed=8)
+    g = inp.to("cuda")
+    sched = m.schedule(g.top_experts, inp.meta["E"], 0.5)
+    w = weights_of(g)
+    outs = []
+    for flags in (0, 2):
+        y, ctx = m.forward(g.x, g.router_w, sched, w, debug=flags)
+        cfg_grads = m.backward(g.dy, g.x, g.router_w, sched, ctx, w)
+        if flags:
+            # backward with the TMA gather4 path as well
+            from mixture_experts_layer_mok_gb300 import _lib
+            import ctypes as C
+            lib = _lib.load()
+            cfg = _lib.MokConfig(mode=0, minibatch_size=0, debug_flags=flags, num_events=0, events=None)
+            E, H, I, I_s = w.dims
+            T, k = sched.T, sched.k
+            gr = {kk: torch.empty_like(v) for kk, v in cfg_grads.items()}
+            gs = _lib.MokWeightGrads()
+            for kk in ("d_w_gate", "d_w_up", "d_w_down", "d_ws_gate", "d_ws_up", "d_ws_down"):
+                if kk in gr:
+                    setattr(gs, kk, gr[kk].data_ptr())
+            nb = lib.mok_bwd_workspace_bytes(T, k, E, H, I, I_s)
+            ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+            wsd = w.struct()
+            P = C.c_void_p
+            _lib.check(lib.mok_backward(C.byref(cfg), P(g.dy.data_ptr()), P(g.x.data_ptr()),
+                                        P(g.router_w.data_ptr()), C.byref(sched.c), C.byref(ctx.c), C.byref(wsd),
+                                        P(gr["dx"].data_ptr()), P(gr["d_router_w"].data_ptr()), C.byref(gs),
+                                        P(ws.data_ptr()), nb, P(torch.cuda.current_stream().cuda_stream)),
+                       "mok_backward")
+            cfg_grads = gr
+        torch.cuda.synchronize()
+        assert ctx.status() == 0
+        outs.append((y.clone(), {kk: v.clone() for kk, v in cfg_grads.items()}))
+    assert torch.equal(outs[0][0], outs[1][0])
+    for key in outs[0][1]:
+        assert torch.equal(outs[0][1][key], outs[1][1][key]), key
