@@ -243,11 +243,12 @@ struct GemmCfg {
   static constexpr bool kBLsu = (B_SRC == SRC_MN_GATHER_LSU);
   static constexpr bool kHasLsu = kALsu || kBLsu;
   static constexpr int kThreads = kHasLsu ? 320 : 192;
-  static constexpr int kGatherLag = 2;   // cp.async groups a gather thread keeps in flight
   static constexpr int kABytes = kBM * kBK * 2;
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kTmaBytes = (kALsu ? 0 : kABytes) + (kBLsu ? 0 : kBBytes);
-  static constexpr uint32_t kFullArrivals = kHasLsu ? 5 : 1;  // TMA warp + 4 gather warps
+  // stage-full arrivals: the TMA warp's expect_tx, plus one hardware arrival per
+  // gather thread when its copies for the stage have landed
+  static constexpr uint32_t kFullArrivals = kHasLsu ? 1 + 128 : 1;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = (BN == 256) ? 4 : 6;
   static constexpr int kTmemCols = 2 * BN;  // two accumulator buffers
@@ -255,7 +256,6 @@ struct GemmCfg {
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
   static constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, kAMN, kBMN);
   static_assert(BN == 128 || BN == 256, "tile N");
-  static_assert(kGatherLag < kStages - 1, "gather lag must leave a stage free");
   static_assert(!(kALsu && kBLsu), "one gathered operand per GEMM");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
@@ -487,6 +487,9 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
             ok = false;
             break;
           }
+          // gathered rows were written through the generic proxy (cp.async):
+          // order them before the tensor core's async-proxy reads
+          if (C::kHasLsu) fence_proxy_async_smem();
           tc_fence_after();
           const uint32_t a0 = smem_u32(smem + stage * C::kStageBytes);
           const uint32_t b0 = a0 + C::kABytes;
@@ -523,7 +526,6 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
       const int gw = warp - 6;
       int stage = 0;
       uint32_t phase = 0;
-      int npend = 0;  // filled stages whose arrival this warp still owes (the latest ones)
       for (int idx = blockIdx.x; idx < nitems; idx += gridDim.x) {
         const Item it = get_item(p, idx);
         const int bn_out = (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_MX) ? BN / 2 : BN;
@@ -562,29 +564,18 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
             gather_mn<2>(sA, p.ga, p.ga_ld, it.m0, cur, gw, lane);
           }
           if (B_SRC == SRC_MN_GATHER_LSU) gather_mn<BN / 64>(sB, p.gb, p.gb_ld, n0, cur, gw, lane);
-          cp_async_commit();
-          ++npend;
+          // the stage's full barrier completes when every thread's copies have landed
+          cp_async_mbar_arrive_noinc(&full[stage]);
           if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1;
-          }
-          if (npend > C::kGatherLag) {
-            cp_async_wait<C::kGatherLag>();
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&full[(stage - npend + C::kStages) % C::kStages]);
-            --npend;
           }
           if (kMN && kb + 1 < it.nk) ktok = mn_gather_token<B_SRC, BN>(p, it, kb + 1, gw, lane);
         }
         if (!ok) break;
       }
-      // every copy issued has landed; signal the stages still owed
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      __syncwarp();
-      for (; npend > 0; --npend)
-        if (lane == 0) mbar_arrive(&full[(stage - npend + C::kStages) % C::kStages]);
+      // no copy may still be in flight when the CTA exits
+      cp_async_wait_all();
     }
   } else {
     // ------------------------------------------------------------ epilogue

@@ -107,6 +107,12 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
+// Arrive (without raising the expected count) on `bar` once every cp.async
+// this thread has issued so far has landed in shared memory.
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy (tensor core) reads of the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {
