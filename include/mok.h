@@ -208,6 +208,30 @@ mok_status_t mok_schedule(const int64_t* top_experts, int T, int k, int E,
 mok_status_t mok_schedule_status(const mok_schedule_t* sched, int* status,
                                  int* num_tiles, int* P);
 
+/* Schedule build for callers that cannot allocate device memory.  Some
+ * callers own no device allocator of their own: code that runs inside
+ * another framework's fixed memory pool, or a latency-bound loop that must
+ * not call cudaMalloc because it can synchronise the device.  This call
+ * builds the same schedule as mok_schedule(), bit for bit, but takes its
+ * per-chunk histogram scratch from an array of fixed size that the library
+ * itself holds in device memory, so `buf` holds only the output arrays
+ * (mok_schedule_bytes(T, k, E) always suffices; the exact need is checked).
+ * The pages have no counterpart to this call.
+ *   - Limit: ceil(T*k / 4096) * E must not exceed 262144 (a 1 MiB array);
+ *     larger problems return MOK_ERR_INVALID_ARG with a message.  The array
+ *     is held by every GPU that loads the library, until the process exits.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls share the one array, which keeps the last call's contents.
+ *     Every entry a build reads is first written by it, so nothing needs
+ *     clearing, but calls that overlap on the GPU (other streams, other host
+ *     threads) race on it: serialise them.
+ *   - No allocation of any kind happens in this call.
+ * Arguments, outputs and errors are those of mok_schedule(). */
+mok_status_t mok_schedule_noalloc(const int64_t* top_experts, int T, int k, int E,
+                                  float capacity_multiplier, void* buf, size_t bytes,
+                                  mok_schedule_t* out, void* stream);
+
 /* ---- MXFP8 quantiser ([MoKEd] "Tuning the five hyperparameters before
  * production": weights are prequantised by a separate mxfp8_quantize) ----
  * x bf16 [rows][K] -> codes E4M3 [rows][K], scales E8M0 [rows][K/32].  Per

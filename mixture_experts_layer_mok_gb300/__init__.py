@@ -17,7 +17,7 @@ import torch
 from . import _lib
 from ._lib import MokError  # noqa: F401
 
-__all__ = ["schedule", "mxfp8_quantize", "forward", "backward", "Schedule", "Weights", "Context",
+__all__ = ["schedule", "schedule_noalloc", "mxfp8_quantize", "forward", "backward", "Schedule", "Weights", "Context",
            "MokError", "quantize_weights"]
 
 
@@ -125,6 +125,24 @@ def schedule(top_experts: torch.Tensor, E: int, capacity_multiplier: float = 0.5
     c = _lib.MokSchedule()
     _lib.check(lib.mok_schedule(_ptr(top_experts), T, k, E, float(capacity_multiplier), _ptr(buf), nbytes,
                                 C.byref(c), _stream(stream)), "mok_schedule")
+    return Schedule(T, k, E, buf, c)
+
+
+def schedule_noalloc(top_experts: torch.Tensor, E: int, capacity_multiplier: float = 0.5, out_buf=None,
+                     stream=None) -> Schedule:
+    """Same schedule as ``schedule``; the library takes the build's scratch from
+    its own fixed device array (for callers that cannot allocate).  Pass
+    ``out_buf`` (uint8, at least mok_schedule_bytes) to allocate nothing here."""
+    lib = _lib.load()
+    T, k = top_experts.shape
+    _need(top_experts, torch.int64, (T, k), "top_experts")
+    nbytes = lib.mok_schedule_bytes(T, k, E)
+    if nbytes == 0:
+        raise ValueError("invalid schedule shape")
+    buf = out_buf if out_buf is not None else torch.empty(nbytes, dtype=torch.uint8, device=top_experts.device)
+    c = _lib.MokSchedule()
+    _lib.check(lib.mok_schedule_noalloc(_ptr(top_experts), T, k, E, float(capacity_multiplier), _ptr(buf),
+                                        buf.numel(), C.byref(c), _stream(stream)), "mok_schedule_noalloc")
     return Schedule(T, k, E, buf, c)
 
 

@@ -72,6 +72,8 @@ SIGNATURES = {
     "mok_schedule": (C.c_int, [P, C.c_int, C.c_int, C.c_int, C.c_float, P, C.c_size_t,
                                C.POINTER(MokSchedule), P]),
     "mok_schedule_status": (C.c_int, [C.POINTER(MokSchedule), I32P, I32P, I32P]),
+    "mok_schedule_noalloc": (C.c_int, [P, C.c_int, C.c_int, C.c_int, C.c_float, P, C.c_size_t,
+                                       C.POINTER(MokSchedule), P]),
     "mok_mxfp8_quantize": (C.c_int, [P, C.c_int64, C.c_int, P, P, P]),
     "mok_ctx_bytes": (C.c_size_t, [C.c_int] * 7),
     "mok_forward": (C.c_int, [C.POINTER(MokConfig), P, P, C.POINTER(MokSchedule),

@@ -275,6 +275,36 @@ __global__ void propagate_status_kernel(const int* header, int* status) {
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// Scratch for mok_schedule_noalloc: per-chunk expert histograms live in this
+// file-scope device array instead of the caller's buffer.  Every GPU that
+// loads the library holds it until the process exits.
+constexpr long long kStaticSchedScratchInts = 1ll << 18;  // 1 MiB
+static __device__ __align__(256) int32_t g_sched_scratch[kStaticSchedScratchInts];
+
+namespace {
+int32_t* g_sched_scratch_dev[64] = {};
+std::mutex g_sched_scratch_mu;
+
+// Device address of g_sched_scratch on the current device, looked up once per
+// device (host code may not use the symbol itself as a device pointer).
+mok_status_t static_sched_scratch(int32_t** out) {
+  int dev = 0;
+  MOK_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return fail(MOK_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lk(g_sched_scratch_mu);
+  if (!g_sched_scratch_dev[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_sched_scratch);
+    if (e != cudaSuccess || !p)
+      return fail(MOK_ERR_CUDA, "cudaGetSymbolAddress(schedule scratch) failed: %s", cudaGetErrorString(e));
+    g_sched_scratch_dev[dev] = static_cast<int32_t*>(p);
+  }
+  *out = g_sched_scratch_dev[dev];
+  return MOK_OK;
+}
+}  // namespace
+
 // ===========================================================================
 extern "C" {
 
@@ -722,6 +752,48 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
   MOK_CUDA(launch_combine(L.dx_slots, Is > 0 ? L.dx_s : nullptr, T, k, H, dx, sms, cs));
   MOK_CUDA(launch_dw_reduce(L.dw_part, T * k, I / bn1, d_router_w, cs));
   MOK_CUDA(mark(cfg, MOK_STAGE_BWD_REDUCE, 1, cs));
+  return MOK_OK;
+}
+
+mok_status_t mok_schedule_noalloc(const int64_t* top_experts, int T, int k, int E,
+                                  float capacity_multiplier, void* buf, size_t bytes,
+                                  mok_schedule_t* out, void* stream) {
+  if (!top_experts || !buf || !out) return fail(MOK_ERR_INVALID_ARG, "NULL argument");
+  if (T < 1 || k < 1 || k > 64 || E < 1 || E > 1024)
+    return fail(MOK_ERR_INVALID_ARG, "need T >= 1, 1 <= k <= 64, 1 <= E <= 1024");
+  if (static_cast<long long>(T) * k >= (1ll << 31) - 128ll * E)
+    return fail(MOK_ERR_INVALID_ARG, "T*k too large");
+  const long long nchunks = (static_cast<long long>(T) * k + kSchedChunk - 1) / kSchedChunk;
+  if (nchunks * E > kStaticSchedScratchInts)
+    return fail(MOK_ERR_INVALID_ARG,
+                "mok_schedule_noalloc: ceil(T*k/%d) * E = %lld exceeds its fixed scratch of %lld ints",
+                kSchedChunk, nchunks * E, kStaticSchedScratchInts);
+  if (!std::isfinite(capacity_multiplier) || capacity_multiplier < 0.f)
+    return fail(MOK_ERR_INVALID_ARG, "capacity_multiplier must be finite and >= 0");
+  if (!aligned16(top_experts) || !aligned16(buf)) return fail(MOK_ERR_INVALID_ARG, "misaligned pointer");
+  SchedLayout L;
+  carve_schedule(buf, T, k, E, &L);
+  // only the output arrays (everything before the histogram region) live in buf
+  const size_t need = static_cast<size_t>(reinterpret_cast<uint8_t*>(L.hist) - static_cast<uint8_t*>(buf));
+  if (bytes < need) return fail(MOK_ERR_INVALID_ARG, "schedule buffer too small (%zu < %zu)", bytes, need);
+  int sms = 0;
+  mok_status_t st = device_info(&sms);
+  if (st) return st;
+  int32_t* scratch = nullptr;
+  if ((st = static_sched_scratch(&scratch))) return st;
+  const long long mt = max_tiles_of(T, k, E);
+  const double rows = std::ceil(static_cast<double>(capacity_multiplier) * static_cast<double>(T));
+  double capd = std::ceil(rows / kTileRows);
+  if (capd > static_cast<double>(mt)) capd = static_cast<double>(mt);
+  // every histogram entry the build reads is first written by it, so the
+  // array needs no clearing between calls
+  MOK_CUDA(launch_schedule(top_experts, T, k, E, static_cast<int>(capd), static_cast<int>(mt), scratch, L.cnt,
+                           L.row0, L.row_src, L.slot_row, L.tile_expert, L.tile_row0, L.tile_rows, L.header,
+                           static_cast<cudaStream_t>(stream)));
+  out->T = T; out->k = k; out->E = E; out->max_tiles = static_cast<int>(mt);
+  out->cnt = L.cnt; out->row0 = L.row0; out->row_src = L.row_src; out->slot_row = L.slot_row;
+  out->tile_expert = L.tile_expert; out->tile_row0 = L.tile_row0; out->tile_rows = L.tile_rows;
+  out->header = L.header; out->scratch = scratch;
   return MOK_OK;
 }
 
