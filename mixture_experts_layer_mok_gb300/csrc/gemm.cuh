@@ -179,6 +179,47 @@ __device__ __forceinline__ void store_bf16x32(void* dst, const float* v) {
                       pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
 }
 
+__device__ __forceinline__ void pack_bf16x32(const float* v, uint32_t* w) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) w[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
+}
+
+// Warp-cooperative row store: each lane hands in 32 bf16 values (16 packed
+// words) of its own row and the address they go to (NULL = store nothing).
+// The warp stages its 32 row segments in 2 KB of shared memory (XOR-swizzled,
+// conflict-free) and writes them back as 64-byte row segments, 8 rows per
+// instruction, so every global store covers whole 32-byte sectors instead of
+// 32 scattered 16-byte pieces.
+__device__ __forceinline__ void warp_store_row64(const uint32_t* w, void* dst, uint8_t* stage, int lane) {
+  uint4* s = reinterpret_cast<uint4*>(stage);
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    s[lane * 4 + (j ^ sw)] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+  __syncwarp();
+  const unsigned long long mine = reinterpret_cast<unsigned long long>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int row = q * 8 + (lane >> 2), piece = lane & 3;
+    const unsigned long long d = __shfl_sync(0xffffffffu, mine, row);
+    const uint4 v = s[row * 4 + (piece ^ ((row >> 1) & 3))];
+    if (d) reinterpret_cast<uint4*>(d)[piece] = v;
+  }
+  __syncwarp();
+}
+
+// Element i of 32 bf16 values held as 4 raw 16-byte words.
+__device__ __forceinline__ float bf16_at(const uint4* raw, int i) {
+  const uint32_t w = reinterpret_cast<const uint32_t*>(raw)[i >> 1];
+  return __uint_as_float((i & 1) ? (w & 0xFFFF0000u) : (w << 16));
+}
+
+__device__ __forceinline__ void load_raw64(const uint16_t* src, uint4* raw) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) raw[q] = __ldg(s + q);
+}
+
 __device__ __forceinline__ void zero_bytes64(void* dst) {
   uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll
@@ -253,7 +294,8 @@ struct GemmCfg {
   static constexpr int kStages = (BN == 256) ? 4 : 6;
   static constexpr int kTmemCols = 2 * BN;  // two accumulator buffers
   static constexpr int kBarBytes = 256;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+  static constexpr int kEpiStageBytes = 2048;  // per epilogue warp: 32 rows x 64 bytes
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes + 4 * kEpiStageBytes;
   static constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, kAMN, kBMN);
   static_assert(BN == 128 || BN == 256, "tile N");
   static_assert(!(kALsu && kBLsu), "one gathered operand per GEMM");
@@ -581,6 +623,7 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;         // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;    // tile row of this thread
+    uint8_t* wstage = smem + C::kStages * C::kStageBytes + C::kBarBytes + (warp - 2) * C::kEpiStageBytes;
     int abuf = 0;
     uint32_t aphase = 0;
     for (int idx = blockIdx.x; idx < nitems; idx += gridDim.x) {
@@ -592,11 +635,38 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
         if (EPI == EPI_WGRAD) {
           const int m = it.m0 + r;
           uint16_t* dst = (m < p.split)
-                              ? static_cast<uint16_t*>(p.out0) + it.e * p.estride + m * p.ld
-                              : static_cast<uint16_t*>(p.out1) + it.e * p.estride + (m - p.split) * p.ld;
-          for (int c = 0; c < BN / 32; ++c) zero_bytes64(dst + n0 + c * 32);
+                              ? static_cast<uint16_t*>(p.out0) + it.e * p.estride + static_cast<long long>(m) * p.ld
+                              : static_cast<uint16_t*>(p.out1) + it.e * p.estride +
+                                    static_cast<long long>(m - p.split) * p.ld;
+          uint32_t zw[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) zw[i] = 0u;
+          for (int c = 0; c < BN / 32; ++c) warp_store_row64(zw, dst + n0 + c * 32, wstage, lane);
         }
         continue;
+      }
+      // SwiGLU backward: row state and the first chunk of the saved gate|up,
+      // fetched before the accumulator is ready
+      int f_bwd = -1;
+      bool v_bwd = false, inb_bwd = false;
+      float wt_bwd = 1.f;
+      uint4 ng[4], nu[4];
+      if constexpr (EPI == EPI_DOWN_BWD) {
+        const int prow = it.p0 + r;
+        if (p.grouped) {
+          f_bwd = (r < it.rows) ? __ldg(p.row_src + prow) : -1;
+          v_bwd = f_bwd >= 0;
+          inb_bwd = true;
+          if (v_bwd) wt_bwd = __ldg(p.rw + f_bwd);
+        } else {
+          v_bwd = r < it.rows;
+          inb_bwd = v_bwd;
+        }
+        if (v_bwd) {
+          const uint16_t* gu = static_cast<const uint16_t*>(p.aux0) + static_cast<long long>(prow) * 2 * p.N + n0;
+          load_raw64(gu, ng);
+          load_raw64(gu + p.N, nu);
+        }
       }
       int w = (lane == 0) ? (mbar_wait(&tfull[abuf], aphase, abort_flag, p.status) ? 1 : 0) : 0;
       w = __shfl_sync(0xffffffffu, w, 0);
@@ -604,120 +674,115 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
       tc_fence_after();
       const uint32_t tb = tmem_base + static_cast<uint32_t>(abuf * BN) +
                           (static_cast<uint32_t>(q * 32) << 16);
+      uint32_t wv[16];
 
       if constexpr (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_MX) {
         // out0 = gu [rows][2N], out1 = h [rows][N] (bf16) or codes, out2 = scales
         const int prow = it.p0 + r;
         const bool valid = r < it.rows;
         const bool inb = p.grouped ? true : valid;
-        uint16_t* gu = static_cast<uint16_t*>(p.out0) + static_cast<long long>(prow) * 2 * p.N;
+        uint16_t* gu = inb ? static_cast<uint16_t*>(p.out0) + static_cast<long long>(prow) * 2 * p.N + n0 : nullptr;
+        uint16_t* hb = (EPI == EPI_SWIGLU && inb)
+                           ? static_cast<uint16_t*>(p.out1) + static_cast<long long>(prow) * p.N + n0
+                           : nullptr;
 #pragma unroll 1
         for (int c = 0; c < BN / 64; ++c) {
           float g[32], u[32];
           tmem_ld32(tb + c * 32, g);
           tmem_ld32(tb + BN / 2 + c * 32, u);
-          if (inb) {
+          if (!valid) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) g[i] = u[i] = 0.f;
+          }
+          float hv[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float sg = __fdividef(1.f, 1.f + __expf(-g[i]));
+            hv[i] = g[i] * sg * u[i];
+          }
+          pack_bf16x32(g, wv);
+          warp_store_row64(wv, gu ? gu + c * 32 : nullptr, wstage, lane);
+          pack_bf16x32(u, wv);
+          warp_store_row64(wv, gu ? gu + p.N + c * 32 : nullptr, wstage, lane);
+          if constexpr (EPI == EPI_SWIGLU) {
+            pack_bf16x32(hv, wv);
+            warp_store_row64(wv, hb ? hb + c * 32 : nullptr, wstage, lane);
+          } else if (inb) {
             const int col = n0 + c * 32;
-            if (!valid) {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) g[i] = u[i] = 0.f;
-            }
-            float hv[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float sg = 1.f / (1.f + __expf(-g[i]));
-              hv[i] = g[i] * sg * u[i];
-            }
-            store_bf16x32(gu + col, g);
-            store_bf16x32(gu + p.N + col, u);
-            if constexpr (EPI == EPI_SWIGLU) {
-              store_bf16x32(static_cast<uint16_t*>(p.out1) + static_cast<long long>(prow) * p.N + col, hv);
-            } else {
-              uint8_t* codes = static_cast<uint8_t*>(p.out1) + static_cast<long long>(prow) * p.N + col;
-              const uint32_t sc = mx_quantize32(hv, codes);
-              static_cast<uint8_t*>(p.out2)[static_cast<long long>(prow) * (p.N / 32) + col / 32] =
-                  static_cast<uint8_t>(sc);
-            }
+            uint8_t* codes = static_cast<uint8_t*>(p.out1) + static_cast<long long>(prow) * p.N + col;
+            const uint32_t sc = mx_quantize32(hv, codes);
+            static_cast<uint8_t*>(p.out2)[static_cast<long long>(prow) * (p.N / 32) + col / 32] =
+                static_cast<uint8_t>(sc);
           }
         }
       } else if constexpr (EPI == EPI_SCALE_SCATTER || EPI == EPI_SCATTER) {
         const int f = (r < it.rows) ? __ldg(p.row_src + it.p0 + r) : -1;
         const float wt = (EPI == EPI_SCALE_SCATTER && f >= 0) ? __ldg(p.rw + f) : 1.f;
-        uint16_t* dst = static_cast<uint16_t*>(p.out0) + static_cast<long long>(f) * p.ld + n0;
+        uint16_t* dst = f >= 0 ? static_cast<uint16_t*>(p.out0) + static_cast<long long>(f) * p.ld + n0 : nullptr;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           float v[32];
           tmem_ld32(tb + c * 32, v);
-          if (f >= 0) {
-            if (EPI == EPI_SCALE_SCATTER) {
+          if (EPI == EPI_SCALE_SCATTER) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] *= wt;
-            }
-            store_bf16x32(dst + c * 32, v);
+            for (int i = 0; i < 32; ++i) v[i] *= wt;
           }
+          pack_bf16x32(v, wv);
+          warp_store_row64(wv, dst ? dst + c * 32 : nullptr, wstage, lane);
         }
       } else if constexpr (EPI == EPI_STORE_ROWS) {
         const int prow = it.p0 + r;
-        const bool valid = r < it.rows;
-        uint16_t* dst = static_cast<uint16_t*>(p.out0) + static_cast<long long>(prow) * p.ld + n0;
+        uint16_t* dst = (r < it.rows) ? static_cast<uint16_t*>(p.out0) + static_cast<long long>(prow) * p.ld + n0
+                                      : nullptr;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           float v[32];
           tmem_ld32(tb + c * 32, v);
-          if (valid) store_bf16x32(dst + c * 32, v);
+          pack_bf16x32(v, wv);
+          warp_store_row64(wv, dst ? dst + c * 32 : nullptr, wstage, lane);
         }
       } else if constexpr (EPI == EPI_DOWN_BWD) {
         // out0 = dgu [rows][2N], out1 = hw [rows][N]; aux0 = gu [rows][2N]
         const int prow = it.p0 + r;
-        int f = -1;
-        bool valid, inb;
-        float wt = 1.f;
-        if (p.grouped) {
-          f = (r < it.rows) ? __ldg(p.row_src + prow) : -1;
-          valid = f >= 0;
-          inb = true;
-          if (valid) wt = __ldg(p.rw + f);
-        } else {
-          valid = r < it.rows;
-          inb = valid;
-        }
-        const uint16_t* gu = static_cast<const uint16_t*>(p.aux0) + static_cast<long long>(prow) * 2 * p.N;
-        uint16_t* dgu = static_cast<uint16_t*>(p.out0) + static_cast<long long>(prow) * 2 * p.N;
-        uint16_t* hw = static_cast<uint16_t*>(p.out1) + static_cast<long long>(prow) * p.N;
+        const uint16_t* gu = static_cast<const uint16_t*>(p.aux0) + static_cast<long long>(prow) * 2 * p.N + n0;
+        uint16_t* dgu = inb_bwd ? static_cast<uint16_t*>(p.out0) + static_cast<long long>(prow) * 2 * p.N + n0 : nullptr;
+        uint16_t* hw = inb_bwd ? static_cast<uint16_t*>(p.out1) + static_cast<long long>(prow) * p.N + n0 : nullptr;
         float dpart = 0.f;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           float z[32];
           tmem_ld32(tb + c * 32, z);
-          if (inb) {
-            const int col = n0 + c * 32;
-            if (valid) {
-              float g[32], u[32];
-              load_bf16x32(gu + col, g);
-              load_bf16x32(gu + p.N + col, u);
-              float dg[32], du[32], hv[32];
+          uint32_t wdg[16], wdu[16], whv[16];
 #pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                const float sg = 1.f / (1.f + __expf(-g[i]));
-                const float sl = g[i] * sg;
-                const float h = sl * u[i];
-                dpart = fmaf(z[i], h, dpart);
-                const float dh = wt * z[i];
-                dg[i] = dh * u[i] * sg * (1.f + g[i] * (1.f - sg));
-                du[i] = dh * sl;
-                hv[i] = wt * h;
+          for (int i = 0; i < 32; i += 2) {
+            float a[2] = {0.f, 0.f}, b[2] = {0.f, 0.f}, hh[2] = {0.f, 0.f};
+            if (v_bwd) {
+#pragma unroll
+              for (int t = 0; t < 2; ++t) {
+                const float g = bf16_at(ng, i + t), u = bf16_at(nu, i + t);
+                const float sg = __fdividef(1.f, 1.f + __expf(-g));
+                const float sl = g * sg;
+                const float h = sl * u;
+                dpart = fmaf(z[i + t], h, dpart);
+                const float dh = wt_bwd * z[i + t];
+                a[t] = dh * u * sg * (1.f + g * (1.f - sg));
+                b[t] = dh * sl;
+                hh[t] = wt_bwd * h;
               }
-              store_bf16x32(dgu + col, dg);
-              store_bf16x32(dgu + p.N + col, du);
-              store_bf16x32(hw + col, hv);
-            } else {
-              zero_bytes64(dgu + col);
-              zero_bytes64(dgu + p.N + col);
-              zero_bytes64(hw + col);
             }
+            wdg[i >> 1] = pack_bf16(a[0], a[1]);
+            wdu[i >> 1] = pack_bf16(b[0], b[1]);
+            whv[i >> 1] = pack_bf16(hh[0], hh[1]);
           }
+          if (v_bwd && c + 1 < BN / 32) {   // next chunk's gate|up, in flight during the stores
+            load_raw64(gu + (c + 1) * 32, ng);
+            load_raw64(gu + p.N + (c + 1) * 32, nu);
+          }
+          warp_store_row64(wdg, dgu ? dgu + c * 32 : nullptr, wstage, lane);
+          warp_store_row64(wdu, dgu ? dgu + p.N + c * 32 : nullptr, wstage, lane);
+          warp_store_row64(whv, hw ? hw + c * 32 : nullptr, wstage, lane);
         }
-        if (p.grouped && valid) p.dw_part[static_cast<long long>(f) * p.n_tiles + it.nt] = dpart;
+        if (p.grouped && v_bwd) p.dw_part[static_cast<long long>(f_bwd) * p.n_tiles + it.nt] = dpart;
       } else if constexpr (EPI == EPI_WGRAD) {
         const int m = it.m0 + r;
         uint16_t* dst = (m < p.split)
@@ -728,7 +793,8 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
         for (int c = 0; c < BN / 32; ++c) {
           float v[32];
           tmem_ld32(tb + c * 32, v);
-          store_bf16x32(dst + n0 + c * 32, v);
+          pack_bf16x32(v, wv);
+          warp_store_row64(wv, dst + n0 + c * 32, wstage, lane);
         }
       }
       tc_fence_before();
