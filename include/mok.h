@@ -102,10 +102,23 @@ typedef int mok_status_t;
  * events[2s+1] after stage s on the call's stream (a stage that does not run
  * records both back to back), so a caller can time each kernel on the stream
  * it runs on. */
+/* How the routed GEMMs receive the token rows of each expert tile (the
+ * on-chip form of MoK's dispatch exchange).  Every choice moves the same bytes
+ * into the same shared-memory layout, so results are bitwise identical. */
+#define MOK_DISPATCH_AUTO     0  /* the library's choice: MOK_DISPATCH_PERMUTE */
+#define MOK_DISPATCH_PERMUTE  1  /* a bandwidth-bound kernel writes the token rows in
+                                    schedule order once (x in the forward, dy and,
+                                    when needed, x in the backward); the GEMMs then
+                                    read dense TMA tiles */
+#define MOK_DISPATCH_FUSED    2  /* the GEMMs gather the token rows themselves
+                                    (gather warps; TMA tile::gather4 with
+                                    MOK_DEBUG_TMA_GATHER4) */
+
 typedef struct {
   int mode;            /* MOK_MODE_* */
   int minibatch_size;  /* tokens per wave of the persistent pipeline; 0 = T */
   int debug_flags;     /* MOK_DEBUG_*; 0 in production */
+  int dispatch;        /* MOK_DISPATCH_* */
   int num_events;      /* 0, or 2 * MOK_NUM_STAGES when events is set */
   void* const* events; /* optional cudaEvent_t[2 * MOK_NUM_STAGES], NULL = off */
 } mok_config_t;
@@ -169,6 +182,8 @@ typedef struct {
   uint8_t*  xq;       /* [T][H] x codes, MXFP8 mode (scratch) */
   uint8_t*  xq_sc;    /* [T][H/32] */
   int32_t*  status;   /* device status word: MOK_OK or the first device error */
+  uint16_t* x_perm;   /* [max_tiles*128][H] token rows of x in schedule order (MOK_DISPATCH_PERMUTE) */
+  int dispatch;       /* the dispatch the forward used */
 } mok_ctx_t;
 
 /* Weight gradients (bf16, same layouts as the weights; shared ones NULL when

@@ -170,8 +170,9 @@ def quantize_weights(w: Weights, stream=None) -> Weights:
     return Weights(w.w_gate, w.w_up, w.w_down, w.ws_gate, w.ws_up, w.ws_down, mx)
 
 
-def _config(mode, minibatch, debug, events=None):
-    cfg = _lib.MokConfig(mode=mode, minibatch_size=minibatch, debug_flags=debug, num_events=0, events=None)
+def _config(mode, minibatch, debug, events=None, dispatch="auto"):
+    cfg = _lib.MokConfig(mode=mode, minibatch_size=minibatch, debug_flags=debug, dispatch=_lib.DISPATCH[dispatch],
+                         num_events=0, events=None)
     if events is not None:
         if len(events) != 2 * _lib.MOK_NUM_STAGES:
             raise ValueError("events must hold 2 * MOK_NUM_STAGES torch.cuda.Event objects")
@@ -186,8 +187,9 @@ def _config(mode, minibatch, debug, events=None):
 
 
 def forward(x, router_w, sched: Schedule, weights: Weights, mode: str = "bf16", minibatch: int = 0,
-            debug: int = 0, out=None, ctx_buf=None, stream=None, events=None):
-    """y = layer(x); returns (y, Context).  ``mode`` is "bf16" or "mxfp8".
+            debug: int = 0, out=None, ctx_buf=None, stream=None, events=None, dispatch="auto"):
+    """y = layer(x); returns (y, Context).  ``mode`` is "bf16" or "mxfp8";
+    ``dispatch`` is "auto", "permute" or "fused" (same results, different kernels).
     ``events``: optional list of 2 * MOK_NUM_STAGES torch.cuda.Event (timing)."""
     lib = _lib.load()
     m = _lib.MOK_MODE_MXFP8_FWD if mode == "mxfp8" else _lib.MOK_MODE_BF16
@@ -203,14 +205,14 @@ def forward(x, router_w, sched: Schedule, weights: Weights, mode: str = "bf16", 
         ctx_buf = torch.empty(nbytes, dtype=torch.uint8, device=x.device)
     y = out if out is not None else torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
     c = _lib.MokCtx()
-    cfg = _config(m, minibatch, debug, events)
+    cfg = _config(m, minibatch, debug, events, dispatch)
     _lib.check(lib.mok_forward(C.byref(cfg), _ptr(x), _ptr(router_w), C.byref(sched.c), C.byref(ws), _ptr(y),
                                _ptr(ctx_buf), ctx_buf.numel(), C.byref(c), _stream(stream)), "mok_forward")
     return y, Context(ctx_buf, c, m)
 
 
 def backward(dy, x, router_w, sched: Schedule, ctx: Context, weights: Weights, minibatch: int = 0,
-             grads: dict | None = None, ws_buf=None, stream=None, events=None):
+             grads: dict | None = None, ws_buf=None, stream=None, events=None, dispatch="auto", debug: int = 0):
     """Returns dict dx, d_router_w, d_w_gate, d_w_up, d_w_down (+ d_ws_* with a shared expert)."""
     lib = _lib.load()
     E, H, I, I_s = weights.dims
@@ -234,7 +236,7 @@ def backward(dy, x, router_w, sched: Schedule, ctx: Context, weights: Weights, m
     nbytes = lib.mok_bwd_workspace_bytes(T, k, E, H, I, I_s)
     if ws_buf is None or ws_buf.numel() < nbytes:
         ws_buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-    cfg = _config(ctx.mode, minibatch, 0, events)
+    cfg = _config(ctx.mode, minibatch, debug, events, dispatch)
     wsd = weights.struct()
     _lib.check(lib.mok_backward(C.byref(cfg), _ptr(dy), _ptr(x), _ptr(router_w), C.byref(sched.c),
                                 C.byref(ctx.c), C.byref(wsd), _ptr(grads["dx"]), _ptr(grads["d_router_w"]),

@@ -19,6 +19,10 @@ MOK_MODE_BF16 = 0
 MOK_MODE_MXFP8_FWD = 1
 MOK_DEBUG_DROP_ACC_SIGNAL = 1
 MOK_DEBUG_TMA_GATHER4 = 2
+MOK_DISPATCH_AUTO = 0
+MOK_DISPATCH_PERMUTE = 1
+MOK_DISPATCH_FUSED = 2
+DISPATCH = {"auto": 0, "permute": 1, "fused": 2}
 
 STATUS_NAMES = {0: "MOK_OK", 1: "MOK_ERR_INVALID_ARG", 2: "MOK_ERR_INDEX", 3: "MOK_ERR_CAPACITY",
                 4: "MOK_ERR_UNSUPPORTED", 5: "MOK_ERR_TIMEOUT", 6: "MOK_ERR_CUDA"}
@@ -35,7 +39,7 @@ STAGE_NAMES = ["fwd_prep", "fwd_shared_gateup", "fwd_shared_down", "fwd_gateup",
 
 class MokConfig(C.Structure):
     _fields_ = [("mode", C.c_int), ("minibatch_size", C.c_int), ("debug_flags", C.c_int),
-                ("num_events", C.c_int), ("events", C.POINTER(C.c_void_p))]
+                ("dispatch", C.c_int), ("num_events", C.c_int), ("events", C.POINTER(C.c_void_p))]
 
 
 class MokSchedule(C.Structure):
@@ -56,7 +60,8 @@ class MokCtx(C.Structure):
     _fields_ = [("T", C.c_int), ("k", C.c_int), ("E", C.c_int), ("H", C.c_int), ("I", C.c_int),
                 ("I_s", C.c_int), ("mode", C.c_int), ("max_tiles", C.c_int),
                 ("gu", P), ("h", P), ("hq", P), ("hq_sc", P), ("slots", P), ("gu_s", P), ("h_s", P),
-                ("hq_s", P), ("hq_s_sc", P), ("shared_out", P), ("xq", P), ("xq_sc", P), ("status", P)]
+                ("hq_s", P), ("hq_s_sc", P), ("shared_out", P), ("xq", P), ("xq_sc", P), ("status", P),
+                ("x_perm", P), ("dispatch", C.c_int)]
 
 
 class MokWeightGrads(C.Structure):

@@ -169,6 +169,7 @@ size_t carve_ctx(void* buf, int T, int k, int E, int H, int I, int Is, int mode,
   ctx->max_tiles = static_cast<int>(max_tiles_of(T, k, E));
   ctx->status = c.take<int32_t>(8);
   ctx->gu = c.take<uint16_t>(mr * 2 * I);
+  ctx->x_perm = c.take<uint16_t>(mr * H);
   ctx->slots = c.take<uint16_t>(n * H);
   if (!mx) {
     ctx->h = c.take<uint16_t>(mr * I);
@@ -201,7 +202,7 @@ size_t carve_ctx(void* buf, int T, int k, int E, int H, int I, int Is, int mode,
 }
 
 struct BwdLayout {
-  uint16_t *dgu, *hw, *dx_slots, *dgu_s, *hs, *dx_s;
+  uint16_t *dgu, *hw, *dx_slots, *dgu_s, *hs, *dx_s, *dy_perm, *xb_perm;
   float* dw_part;
 };
 
@@ -216,6 +217,8 @@ size_t carve_bwd(void* buf, int T, int k, int E, int H, int I, int Is, BwdLayout
   L->hw = c.take<uint16_t>(mr * I);
   L->dw_part = c.take<float>(n * (I / tile_n(I)));
   L->dx_slots = c.take<uint16_t>(n * H);
+  L->dy_perm = c.take<uint16_t>(mr * H);
+  L->xb_perm = c.take<uint16_t>(mr * H);
   if (Is > 0) {
     L->dgu_s = c.take<uint16_t>(static_cast<long long>(T) * 2 * Is);
     L->hs = c.take<uint16_t>(static_cast<long long>(T) * Is);
@@ -266,7 +269,13 @@ mok_status_t check_config(const mok_config_t* cfg) {
   if (cfg->events && cfg->num_events != 2 * MOK_NUM_STAGES)
     return fail(MOK_ERR_INVALID_ARG, "events needs 2 * MOK_NUM_STAGES entries");
   if (cfg->minibatch_size < 0) return fail(MOK_ERR_INVALID_ARG, "minibatch_size < 0");
+  if (cfg->dispatch < MOK_DISPATCH_AUTO || cfg->dispatch > MOK_DISPATCH_FUSED)
+    return fail(MOK_ERR_INVALID_ARG, "unknown dispatch %d", cfg->dispatch);
   return MOK_OK;
+}
+
+int resolve_dispatch(const mok_config_t* cfg) {
+  return cfg->dispatch == MOK_DISPATCH_FUSED ? MOK_DISPATCH_FUSED : MOK_DISPATCH_PERMUTE;
 }
 
 __global__ void propagate_status_kernel(const int* header, int* status) {
@@ -490,8 +499,13 @@ mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x, const float
   // ---- routed experts: gathered gate/up + SwiGLU, then down + scale + scatter
   {
     MOK_CUDA(mark(cfg, MOK_STAGE_FWD_GATEUP, 0, cs));
+    const int disp = resolve_dispatch(cfg);
+    ctx->dispatch = disp;
+    const bool perm = disp == MOK_DISPATCH_PERMUTE;
+    if (perm)  // token rows of x in schedule order, read below as dense tiles
+      MOK_CUDA(launch_permute_rows(xa, H, k, s->row_src, s->header, mr, ctx->x_perm, sms, cs));
     GemmMaps m;
-    if ((st = make_map(&m.a, xa, H, T, 1)) ||
+    if ((st = perm ? make_map(&m.a, ctx->x_perm, H, mr, 128) : make_map(&m.a, xa, H, T, 1)) ||
         (st = make_map(&m.b0, wg, H, static_cast<uint64_t>(E) * I, 128)) ||
         (st = make_map(&m.b1, wu, H, static_cast<uint64_t>(E) * I, 128)))
       return st;
@@ -502,13 +516,17 @@ mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x, const float
     const int grid = items < sms ? static_cast<int>(items) : sms;
     if (!mx) {
       p.out1 = ctx->h;
-      if (g4)
+      if (perm)
+        MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 256, EPI_SWIGLU>(m, p, grid, cs)));
+      else if (g4)
         MOK_CUDA((launch_gemm<SRC_K_GATHER, SRC_K_TILE, 256, EPI_SWIGLU>(m, p, grid, cs)));
       else
         MOK_CUDA((launch_gemm<SRC_K_GATHER_LSU, SRC_K_TILE, 256, EPI_SWIGLU>(m, p, grid, cs)));
     } else {
       p.out1 = ctx->hq; p.out2 = ctx->hq_sc;
-      if (g4)
+      if (perm)
+        MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 256, EPI_SWIGLU_MX>(m, p, grid, cs)));
+      else if (g4)
         MOK_CUDA((launch_gemm<SRC_K_GATHER, SRC_K_TILE, 256, EPI_SWIGLU_MX>(m, p, grid, cs)));
       else
         MOK_CUDA((launch_gemm<SRC_K_GATHER_LSU, SRC_K_TILE, 256, EPI_SWIGLU_MX>(m, p, grid, cs)));
@@ -580,10 +598,23 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
 
   // ---- routed: down dgrad + SwiGLU backward + router-weight partials
   const int bn1 = tile_n(I);
+  const bool perm = resolve_dispatch(cfg) == MOK_DISPATCH_PERMUTE;
+  // permuted dispatch: token rows of x (unquantised, for the weight gradient)
+  // in schedule order; the forward's copy serves when it holds exactly that
+  const uint16_t* x_rows = nullptr;
+  if (perm) {
+    if (ctx->dispatch == MOK_DISPATCH_PERMUTE && ctx->mode == MOK_MODE_BF16 && ctx->x_perm) {
+      x_rows = ctx->x_perm;
+    } else {
+      MOK_CUDA(launch_permute_rows(x, H, k, s->row_src, s->header, mr, L.xb_perm, sms, cs));
+      x_rows = L.xb_perm;
+    }
+  }
   {
     MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DOWN, 0, cs));
+    if (perm) MOK_CUDA(launch_permute_rows(dy, H, k, s->row_src, s->header, mr, L.dy_perm, sms, cs));
     GemmMaps m;
-    if ((st = make_map(&m.a, dy, H, T, 1)) ||
+    if ((st = perm ? make_map(&m.a, L.dy_perm, H, mr, 128) : make_map(&m.a, dy, H, T, 1)) ||
         (st = make_map(&m.b0, w->w_down, I, static_cast<uint64_t>(E) * H, 64)))
       return st;
     m.b1 = m.b0;
@@ -593,7 +624,11 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
     p.ga = dy; p.ga_ld = H;
     const long long items = static_cast<long long>(s->max_tiles) * p.n_tiles;
     const int grid = items < sms ? static_cast<int>(items) : sms;
-    if (g4 && bn1 == 256)
+    if (perm && bn1 == 256)
+      MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_MN_TILE, 256, EPI_DOWN_BWD>(m, p, grid, cs)));
+    else if (perm)
+      MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_MN_TILE, 128, EPI_DOWN_BWD>(m, p, grid, cs)));
+    else if (g4 && bn1 == 256)
       MOK_CUDA((launch_gemm<SRC_K_GATHER, SRC_MN_TILE, 256, EPI_DOWN_BWD>(m, p, grid, cs)));
     else if (g4)
       MOK_CUDA((launch_gemm<SRC_K_GATHER, SRC_MN_TILE, 128, EPI_DOWN_BWD>(m, p, grid, cs)));
@@ -607,7 +642,9 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
   {
     MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_DOWN, 0, cs));
     GemmMaps m;
-    if ((st = make_map(&m.a, dy, H, T, 1)) || (st = make_map(&m.b0, L.hw, I, mr, 64))) return st;
+    if ((st = perm ? make_map(&m.a, L.dy_perm, H, mr, 64) : make_map(&m.a, dy, H, T, 1)) ||
+        (st = make_map(&m.b0, L.hw, I, mr, 64)))
+      return st;
     m.b1 = m.b0;
     GemmParams p = base_params(s, ctx->status, 0);
     const int bn = tile_n(I);
@@ -617,7 +654,11 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
     p.ga = dy; p.ga_ld = H;
     const long long items = static_cast<long long>(E) * p.m_tiles * p.n_tiles;
     const int grid = items < sms ? static_cast<int>(items) : sms;
-    if (g4 && bn == 256)
+    if (perm && bn == 256)
+      MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, grid, cs)));
+    else if (perm)
+      MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, grid, cs)));
+    else if (g4 && bn == 256)
       MOK_CUDA((launch_gemm<SRC_MN_GATHER, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, grid, cs)));
     else if (g4)
       MOK_CUDA((launch_gemm<SRC_MN_GATHER, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, grid, cs)));
@@ -631,7 +672,9 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
   {
     MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_GATEUP, 0, cs));
     GemmMaps m;
-    if ((st = make_map(&m.a, L.dgu, 2 * I, mr, 64)) || (st = make_map(&m.b0, x, H, T, 1))) return st;
+    if ((st = make_map(&m.a, L.dgu, 2 * I, mr, 64)) ||
+        (st = perm ? make_map(&m.b0, x_rows, H, mr, 64) : make_map(&m.b0, x, H, T, 1)))
+      return st;
     m.b1 = m.b0;
     GemmParams p = base_params(s, ctx->status, 0);
     const int bn = tile_n(H);
@@ -641,7 +684,11 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
     p.gb = x; p.gb_ld = H;
     const long long items = static_cast<long long>(E) * p.m_tiles * p.n_tiles;
     const int grid = items < sms ? static_cast<int>(items) : sms;
-    if (g4 && bn == 256)
+    if (perm && bn == 256)
+      MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, grid, cs)));
+    else if (perm)
+      MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, grid, cs)));
+    else if (g4 && bn == 256)
       MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_GATHER, 256, EPI_WGRAD>(m, p, grid, cs)));
     else if (g4)
       MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_GATHER, 128, EPI_WGRAD>(m, p, grid, cs)));

@@ -566,23 +566,54 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
     // ------------------------------------------------------------ gather warps
     if constexpr (C::kHasLsu) {
       const int gw = warp - 6;
+      constexpr bool kMN = (A_SRC == SRC_MN_GATHER_LSU || B_SRC == SRC_MN_GATHER_LSU);
+      const int bn_out = (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_MX) ? BN / 2 : BN;
+      // token of tile row (lane>>2)*16 + gw*4 + (lane&3) for a K-major gather
+      auto row_token = [&](const Item& t) {
+        const int r = (lane >> 2) * 16 + gw * 4 + (lane & 3);
+        return (r < t.rows) ? token_or_pad(p, t.p0 + r) : -1;
+      };
+      auto k_token = [&](const Item& t, int kb) {
+        return (kb < t.nk) ? mn_gather_token<B_SRC, BN>(p, t, kb, gw, lane) : -1;
+      };
       int stage = 0;
       uint32_t phase = 0;
-      for (int idx = blockIdx.x; idx < nitems; idx += gridDim.x) {
-        const Item it = get_item(p, idx);
-        const int bn_out = (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_MX) ? BN / 2 : BN;
-        const int n0 = it.nt * bn_out;
-        // K-major gather: this lane holds the token of tile row (lane>>2)*16 + gw*4 + (lane&3)
-        int rtok = -1;
-        if (A_SRC == SRC_K_GATHER_LSU) {
-          const int r = (lane >> 2) * 16 + gw * 4 + (lane & 3);
-          rtok = (r < it.rows) ? token_or_pad(p, it.p0 + r) : -1;
+      int idx = blockIdx.x;
+      Item it{};
+      int rtok = -1, kt0 = -1, kt1 = -1, kt2 = -1;  // current item's tokens (K-blocks kb..kb+2)
+      if (idx < nitems) {
+        it = get_item(p, idx);
+        if (A_SRC == SRC_K_GATHER_LSU) rtok = row_token(it);
+        if (kMN) {
+          kt0 = k_token(it, 0);
+          kt1 = k_token(it, 1);
+          kt2 = k_token(it, 2);
         }
-        constexpr bool kMN = (A_SRC == SRC_MN_GATHER_LSU || B_SRC == SRC_MN_GATHER_LSU);
-        int ktok = (kMN && it.nk > 0) ? mn_gather_token<B_SRC, BN>(p, it, 0, gw, lane) : -1;
-        bool ok = true;
+      }
+      bool ok = true;
+      while (idx < nitems && ok) {
+        // the next item's descriptor and first tokens load while this one runs
+        const int nidx = idx + gridDim.x;
+        const bool has_next = nidx < nitems;
+        Item nit{};
+        if (has_next) nit = get_item(p, nidx);
+        int nrtok = -1, nkt0 = -1, nkt1 = -1, nkt2 = -1;
+        auto fetch_next = [&]() {
+          if (!has_next) return;
+          if (A_SRC == SRC_K_GATHER_LSU) nrtok = row_token(nit);
+          if (kMN) {
+            nkt0 = k_token(nit, 0);
+            nkt1 = k_token(nit, 1);
+            nkt2 = k_token(nit, 2);
+          }
+        };
+        const int n0 = it.nt * bn_out;
         for (int kb = 0; kb < it.nk; ++kb) {
-          const int cur = ktok;
+          const int cur = kt0;
+          kt0 = kt1;
+          kt1 = kt2;
+          if (kMN) kt2 = k_token(it, kb + 3);   // three K-blocks ahead
+          if (kb == it.nk - 1) fetch_next();
           int w = (lane == 0) ? (mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status) ? 1 : 0) : 0;
           w = __shfl_sync(0xffffffffu, w, 0);
           if (!w) {
@@ -612,9 +643,14 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
             stage = 0;
             phase ^= 1;
           }
-          if (kMN && kb + 1 < it.nk) ktok = mn_gather_token<B_SRC, BN>(p, it, kb + 1, gw, lane);
         }
-        if (!ok) break;
+        if (it.nk == 0) fetch_next();
+        idx = nidx;
+        it = nit;
+        rtok = nrtok;
+        kt0 = nkt0;
+        kt1 = nkt1;
+        kt2 = nkt2;
       }
       // no copy may still be in flight when the CTA exits
       cp_async_wait_all();
@@ -750,29 +786,33 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
         float dpart = 0.f;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
-          float z[32];
-          tmem_ld32(tb + c * 32, z);
           uint32_t wdg[16], wdu[16], whv[16];
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float a[2] = {0.f, 0.f}, b[2] = {0.f, 0.f}, hh[2] = {0.f, 0.f};
-            if (v_bwd) {
+          for (int half = 0; half < 2; ++half) {   // 16 accumulator columns at a time
+            float z[16];
+            tmem_ld16(tb + c * 32 + half * 16, z);
 #pragma unroll
-              for (int t = 0; t < 2; ++t) {
-                const float g = bf16_at(ng, i + t), u = bf16_at(nu, i + t);
-                const float sg = __fdividef(1.f, 1.f + __expf(-g));
-                const float sl = g * sg;
-                const float h = sl * u;
-                dpart = fmaf(z[i + t], h, dpart);
-                const float dh = wt_bwd * z[i + t];
-                a[t] = dh * u * sg * (1.f + g * (1.f - sg));
-                b[t] = dh * sl;
-                hh[t] = wt_bwd * h;
+            for (int i = 0; i < 16; i += 2) {
+              float a[2] = {0.f, 0.f}, b[2] = {0.f, 0.f}, hh[2] = {0.f, 0.f};
+              if (v_bwd) {
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                  const int e = half * 16 + i + t;
+                  const float g = bf16_at(ng, e), u = bf16_at(nu, e);
+                  const float sg = __fdividef(1.f, 1.f + __expf(-g));
+                  const float sl = g * sg;
+                  const float h = sl * u;
+                  dpart = fmaf(z[i + t], h, dpart);
+                  const float dh = wt_bwd * z[i + t];
+                  a[t] = dh * u * sg * (1.f + g * (1.f - sg));
+                  b[t] = dh * sl;
+                  hh[t] = wt_bwd * h;
+                }
               }
+              wdg[(half * 16 + i) >> 1] = pack_bf16(a[0], a[1]);
+              wdu[(half * 16 + i) >> 1] = pack_bf16(b[0], b[1]);
+              whv[(half * 16 + i) >> 1] = pack_bf16(hh[0], hh[1]);
             }
-            wdg[i >> 1] = pack_bf16(a[0], a[1]);
-            wdu[i >> 1] = pack_bf16(b[0], b[1]);
-            whv[i >> 1] = pack_bf16(hh[0], hh[1]);
           }
           if (v_bwd && c + 1 < BN / 32) {   // next chunk's gate|up, in flight during the stores
             load_raw64(gu + (c + 1) * 32, ng);

@@ -23,6 +23,8 @@ cudaError_t launch_mx_dequant(const uint8_t* codes, const uint8_t* scales, long 
                               uint16_t* out, int num_sms, cudaStream_t st);
 cudaError_t launch_combine(const uint16_t* slots, const uint16_t* base, int T, int k, int H,
                            uint16_t* out, int num_sms, cudaStream_t st);
+cudaError_t launch_permute_rows(const uint16_t* src, int H, int topk, const int* row_src, const int* header,
+                                long long max_rows, uint16_t* out, int num_sms, cudaStream_t st);
 cudaError_t launch_dw_reduce(const float* part, int nf, int ntiles, float* dw, cudaStream_t st);
 
 // Grouped GEMM launch: instantiated for the operand sources / tile widths /

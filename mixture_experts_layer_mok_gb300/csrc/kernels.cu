@@ -311,6 +311,41 @@ cudaError_t launch_combine(const uint16_t* slots, const uint16_t* base, int T, i
   return cudaGetLastError();
 }
 
+// ===========================================================================
+// Dispatch permutation: out[p] = src[row_src[p] / k] for every schedule row
+// p < P (zeros for padding rows), so the routed GEMMs read their gathered
+// operand as dense TMA tiles.  One warp per row, 16-byte accesses; bandwidth
+// bound (reads x or dy from L2, writes P rows).
+// ===========================================================================
+__global__ void __launch_bounds__(256) permute_rows_kernel(const uint16_t* __restrict__ src, int H, int topk,
+                                                           const int* __restrict__ row_src,
+                                                           const int* __restrict__ header, long long max_rows,
+                                                           uint16_t* __restrict__ out) {
+  if (header[2] != 0) return;
+  const long long P = header[1];
+  const int lane = threadIdx.x & 31;
+  const int per_row = H / 8;  // 16-byte words per row
+  for (long long q = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5; q < P && q < max_rows;
+       q += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
+    const int f = __ldg(row_src + q);
+    uint4* d = reinterpret_cast<uint4*>(out + q * H);
+    if (f < 0) {
+      for (int i = lane; i < per_row; i += 32) d[i] = make_uint4(0, 0, 0, 0);
+    } else {
+      const uint4* s = reinterpret_cast<const uint4*>(src + static_cast<long long>(f / topk) * H);
+      for (int i = lane; i < per_row; i += 32) d[i] = __ldg(s + i);
+    }
+  }
+}
+
+cudaError_t launch_permute_rows(const uint16_t* src, int H, int topk, const int* row_src, const int* header,
+                                long long max_rows, uint16_t* out, int num_sms, cudaStream_t st) {
+  if (max_rows == 0) return cudaSuccess;
+  permute_rows_kernel<<<grid_for(max_rows * 32, 256, num_sms), 256, 0, st>>>(src, H, topk, row_src, header,
+                                                                           max_rows, out);
+  return cudaGetLastError();
+}
+
 // d_w[f] = sum over column tiles n (ascending) of part[f][n].
 __global__ void dw_reduce_kernel(const float* __restrict__ part, int nf, int ntiles,
                                  float* __restrict__ dw) {

@@ -187,45 +187,41 @@ def test_stage_events_time_each_stage():
         m.forward(g.x, g.router_w, sched, w, events=ev[:3])
 
 
-@pytest.mark.parametrize("name", ["skewed", "wide"])
-def test_gather_warps_and_tma_gather4_agree_bitwise(name):
-    """The dispatch gather by the gather warps (cp.async) and by TMA
-    tile::gather4 move the same bytes, so every output must be identical."""
+@pytest.mark.parametrize("name", ["skewed", "wide", "ragged_shared"])
+@pytest.mark.parametrize("mode", ["bf16", "mxfp8"])
+def test_dispatch_paths_agree_bitwise(name, mode):
+    """Permuted copies, the gather warps (cp.async) and TMA tile::gather4 move
+    the same token rows into the same shared-memory layout, so every output of
+    forward and backward must be bit-identical across the three."""
     m = mok()
     inp = _inputs(name, seed=8)
     g = inp.to("cuda")
     sched = m.schedule(g.top_experts, inp.meta["E"], 0.5)
-    w = weights_of(g)
+    w = weights_of(g, mode)
     outs = []
-    for flags in (0, 2):
-        y, ctx = m.forward(g.x, g.router_w, sched, w, debug=flags)
-        cfg_grads = m.backward(g.dy, g.x, g.router_w, sched, ctx, w)
-        if flags:
-            # backward with the TMA gather4 path as well
-            from mixture_experts_layer_mok_gb300 import _lib
-            import ctypes as C
-            lib = _lib.load()
-            cfg = _lib.MokConfig(mode=0, minibatch_size=0, debug_flags=flags, num_events=0, events=None)
-            E, H, I, I_s = w.dims
-            T, k = sched.T, sched.k
-            gr = {kk: torch.empty_like(v) for kk, v in cfg_grads.items()}
-            gs = _lib.MokWeightGrads()
-            for kk in ("d_w_gate", "d_w_up", "d_w_down", "d_ws_gate", "d_ws_up", "d_ws_down"):
-                if kk in gr:
-                    setattr(gs, kk, gr[kk].data_ptr())
-            nb = lib.mok_bwd_workspace_bytes(T, k, E, H, I, I_s)
-            ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
-            wsd = w.struct()
-            P = C.c_void_p
-            _lib.check(lib.mok_backward(C.byref(cfg), P(g.dy.data_ptr()), P(g.x.data_ptr()),
-                                        P(g.router_w.data_ptr()), C.byref(sched.c), C.byref(ctx.c), C.byref(wsd),
-                                        P(gr["dx"].data_ptr()), P(gr["d_router_w"].data_ptr()), C.byref(gs),
-                                        P(ws.data_ptr()), nb, P(torch.cuda.current_stream().cuda_stream)),
-                       "mok_backward")
-            cfg_grads = gr
+    for dispatch, flags in (("permute", 0), ("fused", 0), ("fused", 2)):
+        y, ctx = m.forward(g.x, g.router_w, sched, w, mode=mode, debug=flags, dispatch=dispatch)
+        grads = m.backward(g.dy, g.x, g.router_w, sched, ctx, w, debug=flags, dispatch=dispatch)
         torch.cuda.synchronize()
         assert ctx.status() == 0
-        outs.append((y.clone(), {kk: v.clone() for kk, v in cfg_grads.items()}))
-    assert torch.equal(outs[0][0], outs[1][0])
-    for key in outs[0][1]:
-        assert torch.equal(outs[0][1][key], outs[1][1][key]), key
+        outs.append((y.clone(), {kk: v.clone() for kk, v in grads.items()}))
+    for other in outs[1:]:
+        assert torch.equal(outs[0][0], other[0])
+        for key in outs[0][1]:
+            assert torch.equal(outs[0][1][key], other[1][key]), key
+
+
+def test_fused_forward_permuted_backward_mix():
+    """A backward may use another dispatch than its forward (it then makes its
+    own copy of x's rows)."""
+    m = mok()
+    inp = _inputs("wide", seed=9)
+    g = inp.to("cuda")
+    sched = m.schedule(g.top_experts, inp.meta["E"], 0.5)
+    w = weights_of(g)
+    y, ctx = m.forward(g.x, g.router_w, sched, w, dispatch="fused")
+    grads = m.backward(g.dy, g.x, g.router_w, sched, ctx, w, dispatch="permute")
+    torch.cuda.synchronize()
+    y_ref, g_ref = oracle_fwd_bwd(inp, "bf16")
+    errs, bad = compare_all(y, grads, y_ref, g_ref, BF16_TOL)
+    assert not bad, errs
