@@ -88,3 +88,40 @@ def subset_inputs(inp, tokens):
     return gen.LayerInputs(inp.x[idx], inp.router_w[idx], inp.top_experts[idx], inp.w_gate, inp.w_up,
                            inp.w_down, inp.ws_gate, inp.ws_up, inp.ws_down,
                            None if inp.dy is None else inp.dy[idx], dict(inp.meta))
+
+
+def token_inputs(inp, t):
+    """Token t alone, with its k experts remapped to a compact weight set (the
+    layer is per-token, so the oracle on this gives y[t], dx[t], d_w[t])."""
+    ex = inp.top_experts[t].cpu()
+    k = ex.numel()
+    sl = lambda a: None if a is None else a.cpu()  # noqa: E731
+    return gen.LayerInputs(sl(inp.x[t:t + 1]), sl(inp.router_w[t:t + 1]),
+                           torch.arange(k, dtype=torch.int64).reshape(1, k),
+                           sl(inp.w_gate[ex.to(inp.w_gate.device)]), sl(inp.w_up[ex.to(inp.w_up.device)]),
+                           sl(inp.w_down[ex.to(inp.w_down.device)]), sl(inp.ws_gate), sl(inp.ws_up), sl(inp.ws_down),
+                           sl(inp.dy[t:t + 1]), dict(inp.meta))
+
+
+def expert_slice_inputs(inp, e, i0, i1):
+    """Only the rows routed to expert e (a k = 1 layer) and only intermediate
+    columns [i0, i1): the oracle on this gives dW_gate[e][i0:i1],
+    dW_up[e][i0:i1] and dW_down[e][:, i0:i1] exactly (those slices depend only
+    on the same columns of h)."""
+    te = inp.top_experts
+    t_e, j_e = torch.nonzero(te == e, as_tuple=True)
+    dev = inp.x.device
+    return gen.LayerInputs(inp.x[t_e].cpu(), inp.router_w[t_e, j_e].reshape(-1, 1).cpu(),
+                           torch.zeros((t_e.numel(), 1), dtype=torch.int64),
+                           inp.w_gate[e:e + 1, i0:i1].cpu(), inp.w_up[e:e + 1, i0:i1].cpu(),
+                           inp.w_down[e:e + 1, :, i0:i1].contiguous().cpu(), None, None, None,
+                           inp.dy[t_e].cpu(), dict(inp.meta)), t_e.to(dev)
+
+
+def shared_slice_inputs(inp, i0, i1):
+    """All tokens through the shared expert only, intermediate columns
+    [i0, i1): gives the matching slices of the shared weight gradients."""
+    e0 = inp.w_gate[:0].cpu()
+    return gen.LayerInputs(inp.x.cpu(), inp.router_w.cpu(), inp.top_experts.cpu(), e0, inp.w_up[:0].cpu(),
+                           inp.w_down[:0].cpu(), inp.ws_gate[i0:i1].cpu(), inp.ws_up[i0:i1].cpu(),
+                           inp.ws_down[:, i0:i1].contiguous().cpu(), inp.dy.cpu(), dict(inp.meta))
