@@ -104,6 +104,25 @@ mok_status_t make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t
   return MOK_OK;
 }
 
+// MN-major operand tile as one 3-D box: dims {64 elements, rows, width/64
+// chunks}, so a single load brings `nchunks` 64-column chunks of 64 rows,
+// chunk-major in shared memory (the layout the MMA descriptors expect).
+mok_status_t make_map_mn(CUtensorMap* m, const void* base, uint64_t width, uint64_t rows, uint32_t nchunks) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(MOK_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t dims[3] = {64, rows, width / 64};
+  const cuuint64_t strides[2] = {width * 2, 128};
+  const cuuint32_t box[3] = {64, 64, nchunks};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MOK_ERR_CUDA, "cuTensorMapEncodeTiled (MN tile) failed (%d) for [%llu x %llu] x %u chunks", (int)r,
+                (unsigned long long)rows, (unsigned long long)width, nchunks);
+  return MOK_OK;
+}
+
 // ---------------------------------------------------------------- carving
 struct Carver {
   uint8_t* base;
@@ -479,7 +498,7 @@ mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x, const float
     MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_DOWN, 0, cs));
     const uint16_t* hs = mx ? X.hs_deq : ctx->h_s;
     GemmMaps m2;
-    if ((st = make_map(&m2.a, hs, Is, T, 128)) || (st = make_map(&m2.b0, wsd, Is, H, 128))) return st;
+    if ((st = make_map(&m2.a, hs, Is, T, 128)) || (st = make_map(&m2.b0, wsd, Is, H, tile_n(H)))) return st;
     m2.b1 = m2.b0;
     GemmParams q = base_params(nullptr, ctx->status, 0);
     const int bn = tile_n(H);
@@ -537,7 +556,7 @@ mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x, const float
     const uint16_t* hr = mx ? X.h_deq : ctx->h;
     GemmMaps m2;
     if ((st = make_map(&m2.a, hr, I, mr, 128)) ||
-        (st = make_map(&m2.b0, wd, I, static_cast<uint64_t>(E) * H, 128)))
+        (st = make_map(&m2.b0, wd, I, static_cast<uint64_t>(E) * H, tile_n(H))))
       return st;
     m2.b1 = m2.b0;
     GemmParams q = base_params(s, ctx->status, 0);
@@ -615,7 +634,7 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
     if (perm) MOK_CUDA(launch_permute_rows(dy, H, k, s->row_src, s->header, mr, L.dy_perm, sms, cs));
     GemmMaps m;
     if ((st = perm ? make_map(&m.a, L.dy_perm, H, mr, 128) : make_map(&m.a, dy, H, T, 1)) ||
-        (st = make_map(&m.b0, w->w_down, I, static_cast<uint64_t>(E) * H, 64)))
+        (st = make_map_mn(&m.b0, w->w_down, I, static_cast<uint64_t>(E) * H, bn1 / 64)))
       return st;
     m.b1 = m.b0;
     GemmParams p = base_params(s, ctx->status, 0);
@@ -642,8 +661,8 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
   {
     MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_DOWN, 0, cs));
     GemmMaps m;
-    if ((st = perm ? make_map(&m.a, L.dy_perm, H, mr, 64) : make_map(&m.a, dy, H, T, 1)) ||
-        (st = make_map(&m.b0, L.hw, I, mr, 64)))
+    if ((st = perm ? make_map_mn(&m.a, L.dy_perm, H, mr, 2) : make_map(&m.a, dy, H, T, 1)) ||
+        (st = make_map_mn(&m.b0, L.hw, I, mr, tile_n(I) / 64)))
       return st;
     m.b1 = m.b0;
     GemmParams p = base_params(s, ctx->status, 0);
@@ -672,8 +691,8 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
   {
     MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_GATEUP, 0, cs));
     GemmMaps m;
-    if ((st = make_map(&m.a, L.dgu, 2 * I, mr, 64)) ||
-        (st = perm ? make_map(&m.b0, x_rows, H, mr, 64) : make_map(&m.b0, x, H, T, 1)))
+    if ((st = make_map_mn(&m.a, L.dgu, 2 * I, mr, 2)) ||
+        (st = perm ? make_map_mn(&m.b0, x_rows, H, mr, tile_n(H) / 64) : make_map(&m.b0, x, H, T, 1)))
       return st;
     m.b1 = m.b0;
     GemmParams p = base_params(s, ctx->status, 0);
@@ -703,8 +722,8 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
     MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DGRAD_GATEUP, 0, cs));
     GemmMaps m;
     if ((st = make_map(&m.a, L.dgu, 2 * I, mr, 128)) ||
-        (st = make_map(&m.b0, w->w_gate, H, static_cast<uint64_t>(E) * I, 64)) ||
-        (st = make_map(&m.b1, w->w_up, H, static_cast<uint64_t>(E) * I, 64)))
+        (st = make_map_mn(&m.b0, w->w_gate, H, static_cast<uint64_t>(E) * I, tile_n(H) / 64)) ||
+        (st = make_map_mn(&m.b1, w->w_up, H, static_cast<uint64_t>(E) * I, tile_n(H) / 64)))
       return st;
     GemmParams p = base_params(s, ctx->status, 0);
     const int bn = tile_n(H);
@@ -724,7 +743,7 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
     {
       MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DOWN, 0, cs));
       GemmMaps m;
-      if ((st = make_map(&m.a, dy, H, T, 128)) || (st = make_map(&m.b0, w->ws_down, Is, H, 64))) return st;
+      if ((st = make_map(&m.a, dy, H, T, 128)) || (st = make_map_mn(&m.b0, w->ws_down, Is, H, bns / 64))) return st;
       m.b1 = m.b0;
       GemmParams p = base_params(nullptr, ctx->status, 0);
       p.rows = T; p.K = H; p.N = Is; p.n_tiles = Is / bns; p.b_rows_per_expert = 0;
@@ -740,7 +759,7 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
     {  // dW_s_down = dy^T h_s
       MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_DOWN, 0, cs));
       GemmMaps m;
-      if ((st = make_map(&m.a, dy, H, T, 64)) || (st = make_map(&m.b0, L.hs, Is, T, 64))) return st;
+      if ((st = make_map_mn(&m.a, dy, H, T, 2)) || (st = make_map_mn(&m.b0, L.hs, Is, T, bns / 64))) return st;
       m.b1 = m.b0;
       GemmParams p = base_params(nullptr, ctx->status, 0);
       p.wgrad = 1; p.rows = T; p.E = 1; p.m_tiles = H / 128; p.n_tiles = Is / bns;
@@ -756,7 +775,7 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
     {  // dW_s_gate|up = (dG_s|dU_s)^T x
       MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_GATEUP, 0, cs));
       GemmMaps m;
-      if ((st = make_map(&m.a, L.dgu_s, 2 * Is, T, 64)) || (st = make_map(&m.b0, x, H, T, 64))) return st;
+      if ((st = make_map_mn(&m.a, L.dgu_s, 2 * Is, T, 2)) || (st = make_map_mn(&m.b0, x, H, T, tile_n(H) / 64))) return st;
       m.b1 = m.b0;
       GemmParams p = base_params(nullptr, ctx->status, 0);
       const int bn = tile_n(H);
@@ -773,8 +792,8 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
     {  // dx_s = dG_s W_s_gate + dU_s W_s_up
       MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DGRAD, 0, cs));
       GemmMaps m;
-      if ((st = make_map(&m.a, L.dgu_s, 2 * Is, T, 128)) || (st = make_map(&m.b0, w->ws_gate, H, Is, 64)) ||
-          (st = make_map(&m.b1, w->ws_up, H, Is, 64)))
+      if ((st = make_map(&m.a, L.dgu_s, 2 * Is, T, 128)) || (st = make_map_mn(&m.b0, w->ws_gate, H, Is, tile_n(H) / 64)) ||
+          (st = make_map_mn(&m.b1, w->ws_up, H, Is, tile_n(H) / 64)))
         return st;
       GemmParams p = base_params(nullptr, ctx->status, 0);
       const int bn = tile_n(H);

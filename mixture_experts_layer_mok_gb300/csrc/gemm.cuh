@@ -441,9 +441,8 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
         } else if (A_SRC == SRC_K_GATHER) {
           tma_gather4(sA + lane * 512, &maps.a, &full[stage], k0, tok[0], tok[1], tok[2], tok[3]);
         } else if (A_SRC == SRC_MN_TILE) {
-          if (lane < 2)
-            tma_load_2d(sA + lane * kChunkBytes, &maps.a, &full[stage], it.m0 + 64 * lane,
-                        it.kbeg + k0);
+          // one 3-D box {64 elements, 64 K-rows, 2 chunks}: chunk-major in smem
+          if (lane == 0) tma_load_3d(sA, &maps.a, &full[stage], 0, it.kbeg + k0, it.m0 / 64);
         } else if (A_SRC == SRC_MN_GATHER) {
           const int c = lane >> 4, g = lane & 15;
           tma_gather4(sA + c * kChunkBytes + g * 512, &maps.a, &full[stage], it.m0 + 64 * c, cur[0],
@@ -457,14 +456,11 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
               tma_load_2d(sB, &maps.b0, &full[stage], k0, r);
               tma_load_2d(sB + (BN / 2) * 128, &maps.b1, &full[stage], k0, r);
             } else {
-#pragma unroll
-              for (int h = 0; h < BN / 128; ++h)
-                tma_load_2d(sB + h * 128 * 128, &maps.b0, &full[stage], k0,
-                            it.e * p.b_rows_per_expert + n0 + 128 * h);
+              tma_load_2d(sB, &maps.b0, &full[stage], k0, it.e * p.b_rows_per_expert + n0);  // BN rows
             }
           }
         } else if (B_SRC == SRC_MN_TILE) {
-          if (lane < BN / 64) {
+          if (lane == 0) {  // one 3-D box {64 elements, 64 K-rows, BN/64 chunks}
             int krow = k0;
             const CUtensorMap* m = &maps.b0;
             if (p.b_split > 0 && krow >= p.b_split) {
@@ -472,7 +468,7 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
               krow -= p.b_split;
             }
             const int kr = p.wgrad ? (it.kbeg + k0) : (it.e * p.b_rows_per_expert + krow);
-            tma_load_2d(sB + lane * kChunkBytes, m, &full[stage], n0 + 64 * lane, kr);
+            tma_load_3d(sB, m, &full[stage], 0, kr, n0 / 64);
           }
         } else if (B_SRC == SRC_MN_GATHER) {
           const int g = lane & 15;
