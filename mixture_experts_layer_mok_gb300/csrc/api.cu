@@ -85,18 +85,20 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor [outer][inner] with a box of box_outer rows x 64 elements and
-// 128-byte swizzle; out-of-range elements read as zero.
+// 2-D bf16 tensor [outer][inner] with a box of box_outer rows x bk elements
+// (bk = the kernel's K-block: 64 -> 128-byte swizzle, 32 -> 64-byte swizzle);
+// out-of-range elements read as zero.
 mok_status_t make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
-                      uint32_t box_outer) {
+                      uint32_t box_outer, int bk) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(MOK_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {inner * 2};
-  const cuuint32_t box[2] = {64, box_outer};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(bk), box_outer};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  bk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(MOK_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for [%llu x %llu] box %u", (int)r,
@@ -104,24 +106,31 @@ mok_status_t make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t
   return MOK_OK;
 }
 
-// MN-major operand tile as one 3-D box: dims {64 elements, rows, width/64
-// chunks}, so a single load brings `nchunks` 64-column chunks of 64 rows,
-// chunk-major in shared memory (the layout the MMA descriptors expect).
-mok_status_t make_map_mn(CUtensorMap* m, const void* base, uint64_t width, uint64_t rows, uint32_t nchunks) {
+// MN-major operand tile of `tile_width` columns as one 3-D box: dims
+// {bk elements, rows, width/bk chunks}, box {bk, bk K-rows, tile_width/bk},
+// landing chunk-major in shared memory (the layout the MMA descriptors expect).
+mok_status_t make_map_mn(CUtensorMap* m, const void* base, uint64_t width, uint64_t rows, int tile_width,
+                         int bk) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(MOK_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
-  const cuuint64_t dims[3] = {64, rows, width / 64};
-  const cuuint64_t strides[2] = {width * 2, 128};
-  const cuuint32_t box[3] = {64, 64, nchunks};
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(bk), rows, width / bk};
+  const cuuint64_t strides[2] = {width * 2, static_cast<cuuint64_t>(bk) * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(bk), static_cast<cuuint32_t>(bk),
+                             static_cast<cuuint32_t>(tile_width / bk)};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, bk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
-    return fail(MOK_ERR_CUDA, "cuTensorMapEncodeTiled (MN tile) failed (%d) for [%llu x %llu] x %u chunks", (int)r,
-                (unsigned long long)rows, (unsigned long long)width, nchunks);
+    return fail(MOK_ERR_CUDA, "cuTensorMapEncodeTiled (MN tile) failed (%d) for [%llu x %llu], tile %d", (int)r,
+                (unsigned long long)rows, (unsigned long long)width, tile_width);
   return MOK_OK;
 }
+
+// K-block of the GEMM kernels (elements per stage); the map builders also
+// support 32 (64-byte swizzle).
+constexpr int kTileBK = 64;
+constexpr int kGatherBK = 64;
 
 // ---------------------------------------------------------------- carving
 struct Carver {
@@ -234,7 +243,7 @@ size_t carve_bwd(void* buf, int T, int k, int E, int H, int I, int Is, BwdLayout
   memset(L, 0, sizeof(*L));
   L->dgu = c.take<uint16_t>(mr * 2 * I);
   L->hw = c.take<uint16_t>(mr * I);
-  L->dw_part = c.take<float>(n * (I / tile_n(I)));
+  L->dw_part = c.take<float>(n * 2 * (I / tile_n(I)));  // two column halves per N tile
   L->dx_slots = c.take<uint16_t>(n * H);
   L->dy_perm = c.take<uint16_t>(mr * H);
   L->xb_perm = c.take<uint16_t>(mr * H);
@@ -478,8 +487,8 @@ mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x, const float
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_GATEUP, 0, cs));
   if (Is > 0) {
     GemmMaps m;
-    if ((st = make_map(&m.a, xa, H, T, 128)) || (st = make_map(&m.b0, wsg, H, Is, 128)) ||
-        (st = make_map(&m.b1, wsu, H, Is, 128)))
+    if ((st = make_map(&m.a, xa, H, T, 128, kTileBK)) || (st = make_map(&m.b0, wsg, H, Is, 128, kTileBK)) ||
+        (st = make_map(&m.b1, wsu, H, Is, 128, kTileBK)))
       return st;
     GemmParams p = base_params(nullptr, ctx->status, 0);
     p.rows = T; p.K = H; p.N = Is; p.n_tiles = Is / 128; p.b_rows_per_expert = 0;
@@ -498,7 +507,7 @@ mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x, const float
     MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_DOWN, 0, cs));
     const uint16_t* hs = mx ? X.hs_deq : ctx->h_s;
     GemmMaps m2;
-    if ((st = make_map(&m2.a, hs, Is, T, 128)) || (st = make_map(&m2.b0, wsd, Is, H, tile_n(H)))) return st;
+    if ((st = make_map(&m2.a, hs, Is, T, 128, kTileBK)) || (st = make_map(&m2.b0, wsd, Is, H, tile_n(H), kTileBK))) return st;
     m2.b1 = m2.b0;
     GemmParams q = base_params(nullptr, ctx->status, 0);
     const int bn = tile_n(H);
@@ -524,9 +533,10 @@ mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x, const float
     if (perm)  // token rows of x in schedule order, read below as dense tiles
       MOK_CUDA(launch_permute_rows(xa, H, k, s->row_src, s->header, mr, ctx->x_perm, sms, cs));
     GemmMaps m;
-    if ((st = perm ? make_map(&m.a, ctx->x_perm, H, mr, 128) : make_map(&m.a, xa, H, T, 1)) ||
-        (st = make_map(&m.b0, wg, H, static_cast<uint64_t>(E) * I, 128)) ||
-        (st = make_map(&m.b1, wu, H, static_cast<uint64_t>(E) * I, 128)))
+    const int bk = perm ? kTileBK : kGatherBK;
+    if ((st = perm ? make_map(&m.a, ctx->x_perm, H, mr, 128, bk) : make_map(&m.a, xa, H, T, 1, bk)) ||
+        (st = make_map(&m.b0, wg, H, static_cast<uint64_t>(E) * I, 128, bk)) ||
+        (st = make_map(&m.b1, wu, H, static_cast<uint64_t>(E) * I, 128, bk)))
       return st;
     GemmParams p = base_params(s, ctx->status, cfg->debug_flags);
     p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / 128; p.b_rows_per_expert = I;
@@ -555,8 +565,8 @@ mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x, const float
     MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DOWN, 0, cs));
     const uint16_t* hr = mx ? X.h_deq : ctx->h;
     GemmMaps m2;
-    if ((st = make_map(&m2.a, hr, I, mr, 128)) ||
-        (st = make_map(&m2.b0, wd, I, static_cast<uint64_t>(E) * H, tile_n(H))))
+    if ((st = make_map(&m2.a, hr, I, mr, 128, kTileBK)) ||
+        (st = make_map(&m2.b0, wd, I, static_cast<uint64_t>(E) * H, tile_n(H), kTileBK)))
       return st;
     m2.b1 = m2.b0;
     GemmParams q = base_params(s, ctx->status, 0);
@@ -633,8 +643,9 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
     MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DOWN, 0, cs));
     if (perm) MOK_CUDA(launch_permute_rows(dy, H, k, s->row_src, s->header, mr, L.dy_perm, sms, cs));
     GemmMaps m;
-    if ((st = perm ? make_map(&m.a, L.dy_perm, H, mr, 128) : make_map(&m.a, dy, H, T, 1)) ||
-        (st = make_map_mn(&m.b0, w->w_down, I, static_cast<uint64_t>(E) * H, bn1 / 64)))
+    const int bk = perm ? kTileBK : kGatherBK;
+    if ((st = perm ? make_map(&m.a, L.dy_perm, H, mr, 128, bk) : make_map(&m.a, dy, H, T, 1, bk)) ||
+        (st = make_map_mn(&m.b0, w->w_down, I, static_cast<uint64_t>(E) * H, bn1, bk)))
       return st;
     m.b1 = m.b0;
     GemmParams p = base_params(s, ctx->status, 0);
@@ -661,8 +672,9 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
   {
     MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_DOWN, 0, cs));
     GemmMaps m;
-    if ((st = perm ? make_map_mn(&m.a, L.dy_perm, H, mr, 2) : make_map(&m.a, dy, H, T, 1)) ||
-        (st = make_map_mn(&m.b0, L.hw, I, mr, tile_n(I) / 64)))
+    const int bk = perm ? kTileBK : kGatherBK;
+    if ((st = perm ? make_map_mn(&m.a, L.dy_perm, H, mr, 128, bk) : make_map(&m.a, dy, H, T, 1, bk)) ||
+        (st = make_map_mn(&m.b0, L.hw, I, mr, tile_n(I), bk)))
       return st;
     m.b1 = m.b0;
     GemmParams p = base_params(s, ctx->status, 0);
@@ -691,8 +703,9 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
   {
     MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_GATEUP, 0, cs));
     GemmMaps m;
-    if ((st = make_map_mn(&m.a, L.dgu, 2 * I, mr, 2)) ||
-        (st = perm ? make_map_mn(&m.b0, x_rows, H, mr, tile_n(H) / 64) : make_map(&m.b0, x, H, T, 1)))
+    const int bk = perm ? kTileBK : kGatherBK;
+    if ((st = make_map_mn(&m.a, L.dgu, 2 * I, mr, 128, bk)) ||
+        (st = perm ? make_map_mn(&m.b0, x_rows, H, mr, tile_n(H), bk) : make_map(&m.b0, x, H, T, 1, bk)))
       return st;
     m.b1 = m.b0;
     GemmParams p = base_params(s, ctx->status, 0);
@@ -721,9 +734,9 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
   {
     MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DGRAD_GATEUP, 0, cs));
     GemmMaps m;
-    if ((st = make_map(&m.a, L.dgu, 2 * I, mr, 128)) ||
-        (st = make_map_mn(&m.b0, w->w_gate, H, static_cast<uint64_t>(E) * I, tile_n(H) / 64)) ||
-        (st = make_map_mn(&m.b1, w->w_up, H, static_cast<uint64_t>(E) * I, tile_n(H) / 64)))
+    if ((st = make_map(&m.a, L.dgu, 2 * I, mr, 128, kTileBK)) ||
+        (st = make_map_mn(&m.b0, w->w_gate, H, static_cast<uint64_t>(E) * I, tile_n(H), kTileBK)) ||
+        (st = make_map_mn(&m.b1, w->w_up, H, static_cast<uint64_t>(E) * I, tile_n(H), kTileBK)))
       return st;
     GemmParams p = base_params(s, ctx->status, 0);
     const int bn = tile_n(H);
@@ -743,7 +756,7 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
     {
       MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DOWN, 0, cs));
       GemmMaps m;
-      if ((st = make_map(&m.a, dy, H, T, 128)) || (st = make_map_mn(&m.b0, w->ws_down, Is, H, bns / 64))) return st;
+      if ((st = make_map(&m.a, dy, H, T, 128, kTileBK)) || (st = make_map_mn(&m.b0, w->ws_down, Is, H, bns, kTileBK))) return st;
       m.b1 = m.b0;
       GemmParams p = base_params(nullptr, ctx->status, 0);
       p.rows = T; p.K = H; p.N = Is; p.n_tiles = Is / bns; p.b_rows_per_expert = 0;
@@ -759,7 +772,7 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
     {  // dW_s_down = dy^T h_s
       MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_DOWN, 0, cs));
       GemmMaps m;
-      if ((st = make_map_mn(&m.a, dy, H, T, 2)) || (st = make_map_mn(&m.b0, L.hs, Is, T, bns / 64))) return st;
+      if ((st = make_map_mn(&m.a, dy, H, T, 128, kTileBK)) || (st = make_map_mn(&m.b0, L.hs, Is, T, bns, kTileBK))) return st;
       m.b1 = m.b0;
       GemmParams p = base_params(nullptr, ctx->status, 0);
       p.wgrad = 1; p.rows = T; p.E = 1; p.m_tiles = H / 128; p.n_tiles = Is / bns;
@@ -775,7 +788,7 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
     {  // dW_s_gate|up = (dG_s|dU_s)^T x
       MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_GATEUP, 0, cs));
       GemmMaps m;
-      if ((st = make_map_mn(&m.a, L.dgu_s, 2 * Is, T, 2)) || (st = make_map_mn(&m.b0, x, H, T, tile_n(H) / 64))) return st;
+      if ((st = make_map_mn(&m.a, L.dgu_s, 2 * Is, T, 128, kTileBK)) || (st = make_map_mn(&m.b0, x, H, T, tile_n(H), kTileBK))) return st;
       m.b1 = m.b0;
       GemmParams p = base_params(nullptr, ctx->status, 0);
       const int bn = tile_n(H);
@@ -792,8 +805,8 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
     {  // dx_s = dG_s W_s_gate + dU_s W_s_up
       MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DGRAD, 0, cs));
       GemmMaps m;
-      if ((st = make_map(&m.a, L.dgu_s, 2 * Is, T, 128)) || (st = make_map_mn(&m.b0, w->ws_gate, H, Is, tile_n(H) / 64)) ||
-          (st = make_map_mn(&m.b1, w->ws_up, H, Is, tile_n(H) / 64)))
+      if ((st = make_map(&m.a, L.dgu_s, 2 * Is, T, 128, kTileBK)) || (st = make_map_mn(&m.b0, w->ws_gate, H, Is, tile_n(H), kTileBK)) ||
+          (st = make_map_mn(&m.b1, w->ws_up, H, Is, tile_n(H), kTileBK)))
         return st;
       GemmParams p = base_params(nullptr, ctx->status, 0);
       const int bn = tile_n(H);
@@ -816,7 +829,7 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
   // ---- fixed-order reductions: dx and the router-weight gradient
   MOK_CUDA(mark(cfg, MOK_STAGE_BWD_REDUCE, 0, cs));
   MOK_CUDA(launch_combine(L.dx_slots, Is > 0 ? L.dx_s : nullptr, T, k, H, dx, sms, cs));
-  MOK_CUDA(launch_dw_reduce(L.dw_part, T * k, I / bn1, d_router_w, cs));
+  MOK_CUDA(launch_dw_reduce(L.dw_part, T * k, 2 * (I / bn1), d_router_w, cs));
   MOK_CUDA(mark(cfg, MOK_STAGE_BWD_REDUCE, 1, cs));
   return MOK_OK;
 }

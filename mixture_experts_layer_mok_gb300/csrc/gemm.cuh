@@ -33,7 +33,9 @@
 namespace mok {
 
 constexpr int kBM = 128;        // rows of an output tile (TMEM lanes)
-constexpr int kBK = 64;         // bf16 elements per 128-byte swizzled row
+// Kernels that gather token rows use 64-element K-blocks (128-byte swizzle);
+// the gather code below is written for that layout.
+constexpr int kBK = 64;
 constexpr int kChunkBytes = 64 * 128;  // one MN-major chunk: 64 K-rows x 64 elements
 
 enum Src : int {
@@ -115,7 +117,7 @@ __device__ __forceinline__ int num_items(const GemmParams& p) {
   return p.E * p.m_tiles * p.n_tiles;
 }
 
-__device__ __forceinline__ Item get_item(const GemmParams& p, int idx) {
+__device__ __forceinline__ Item get_item(const GemmParams& p, int idx, int bk) {
   Item it;
   if (!p.wgrad) {
     const int mt = idx / p.n_tiles;
@@ -131,7 +133,7 @@ __device__ __forceinline__ Item get_item(const GemmParams& p, int idx) {
     }
     it.m0 = it.p0;
     it.kbeg = 0;
-    it.nk = p.K / kBK;
+    it.nk = p.K / bk;
   } else {
     const int per_e = p.m_tiles * p.n_tiles;
     it.e = idx / per_e;
@@ -144,10 +146,10 @@ __device__ __forceinline__ Item get_item(const GemmParams& p, int idx) {
     if (p.grouped) {
       it.kbeg = __ldg(p.row0 + it.e);
       const int c = __ldg(p.cnt + it.e);
-      it.nk = (c + kBM - 1) / kBM * (kBM / kBK);
+      it.nk = (c + kBM - 1) / kBM * (kBM / bk);
     } else {
       it.kbeg = 0;
-      it.nk = (p.rows + kBK - 1) / kBK;
+      it.nk = (p.rows + bk - 1) / bk;
     }
   }
   return it;
@@ -283,7 +285,18 @@ struct GemmCfg {
   static constexpr bool kALsu = (A_SRC == SRC_K_GATHER_LSU || A_SRC == SRC_MN_GATHER_LSU);
   static constexpr bool kBLsu = (B_SRC == SRC_MN_GATHER_LSU);
   static constexpr bool kHasLsu = kALsu || kBLsu;
-  static constexpr int kThreads = kHasLsu ? 320 : 192;
+  // epilogue warps: the SwiGLU backward's epilogue is the heaviest; with no
+  // gather warps it gets two warps per TMEM lane quarter (each half the columns)
+  static constexpr int kEpiWarps = (EPI == EPI_DOWN_BWD && !kHasLsu) ? 8 : 4;
+  static constexpr int kGatherWarp0 = 2 + kEpiWarps;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps + (kHasLsu ? 128 : 0);
+  // K-block per stage (elements): 64 bf16 = one 128-byte swizzled row.  The
+  // layout code below also supports 32 (64-byte swizzle); measured slower,
+  // since it doubles the TMA instructions per FLOP.
+  static constexpr int kBK = 64;
+  static constexpr int kRowBytes = kBK * 2;                 // one swizzled shared-memory row
+  static constexpr int kMnChunkBytes = kRowBytes * kBK;     // MN-major chunk: kBK K-rows x kBK elements
+  static constexpr uint32_t kSwz = (kBK == 64) ? 2u : 4u;   // descriptor swizzle: 128-byte / 64-byte
   static constexpr int kABytes = kBM * kBK * 2;
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kTmaBytes = (kALsu ? 0 : kABytes) + (kBLsu ? 0 : kBBytes);
@@ -291,11 +304,12 @@ struct GemmCfg {
   // gather thread when its copies for the stage have landed
   static constexpr uint32_t kFullArrivals = kHasLsu ? 1 + 128 : 1;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = (BN == 256) ? 4 : 6;
-  static constexpr int kTmemCols = 2 * BN;  // two accumulator buffers
-  static constexpr int kBarBytes = 256;
+  static constexpr int kBarBytes = 512;
   static constexpr int kEpiStageBytes = 2048;  // per epilogue warp: 32 rows x 64 bytes
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes + 4 * kEpiStageBytes;
+  static constexpr int kStagesFit = (227 * 1024 - 1024 - kBarBytes - kEpiWarps * kEpiStageBytes) / kStageBytes;
+  static constexpr int kStages = kStagesFit > 16 ? 16 : kStagesFit;
+  static constexpr int kTmemCols = 2 * BN;  // two accumulator buffers
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes + kEpiWarps * kEpiStageBytes;
   static constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, kAMN, kBMN);
   static_assert(BN == 128 || BN == 256, "tile N");
   static_assert(!(kALsu && kBLsu), "one gathered operand per GEMM");
@@ -377,7 +391,7 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4);
+      mbar_init(&tempty[b], C::kEpiWarps);
     }
     mbar_init(done, 1);
     *abort_flag = 0;
@@ -403,7 +417,7 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
     long long fills = 0;
     bool ok = true;
     for (int idx = blockIdx.x; idx < nitems && ok; idx += gridDim.x) {
-      const Item it = get_item(p, idx);
+      const Item it = get_item(p, idx, C::kBK);
       const int bn_out = (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_MX) ? BN / 2 : BN;
       const int n0 = it.nt * bn_out;
       // token rows of a row tile (K-major gather): rows 4*lane .. 4*lane+3
@@ -434,7 +448,7 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
         __syncwarp();
         uint8_t* sA = smem + stage * C::kStageBytes;
         uint8_t* sB = sA + C::kABytes;
-        const int k0 = kb * kBK;
+        const int k0 = kb * C::kBK;
         // ---- A operand
         if (A_SRC == SRC_K_TILE) {
           if (lane == 0) tma_load_2d(sA, &maps.a, &full[stage], k0, it.p0);
@@ -442,7 +456,7 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
           tma_gather4(sA + lane * 512, &maps.a, &full[stage], k0, tok[0], tok[1], tok[2], tok[3]);
         } else if (A_SRC == SRC_MN_TILE) {
           // one 3-D box {64 elements, 64 K-rows, 2 chunks}: chunk-major in smem
-          if (lane == 0) tma_load_3d(sA, &maps.a, &full[stage], 0, it.kbeg + k0, it.m0 / 64);
+          if (lane == 0) tma_load_3d(sA, &maps.a, &full[stage], 0, it.kbeg + k0, it.m0 / C::kBK);
         } else if (A_SRC == SRC_MN_GATHER) {
           const int c = lane >> 4, g = lane & 15;
           tma_gather4(sA + c * kChunkBytes + g * 512, &maps.a, &full[stage], it.m0 + 64 * c, cur[0],
@@ -454,7 +468,7 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
             if (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_MX) {
               const int r = it.e * p.b_rows_per_expert + n0;
               tma_load_2d(sB, &maps.b0, &full[stage], k0, r);
-              tma_load_2d(sB + (BN / 2) * 128, &maps.b1, &full[stage], k0, r);
+              tma_load_2d(sB + (BN / 2) * C::kRowBytes, &maps.b1, &full[stage], k0, r);
             } else {
               tma_load_2d(sB, &maps.b0, &full[stage], k0, it.e * p.b_rows_per_expert + n0);  // BN rows
             }
@@ -468,7 +482,7 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
               krow -= p.b_split;
             }
             const int kr = p.wgrad ? (it.kbeg + k0) : (it.e * p.b_rows_per_expert + krow);
-            tma_load_3d(sB, m, &full[stage], 0, kr, n0 / 64);
+            tma_load_3d(sB, m, &full[stage], 0, kr, n0 / C::kBK);
           }
         } else if (B_SRC == SRC_MN_GATHER) {
           const int g = lane & 15;
@@ -514,7 +528,7 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
       uint32_t aphase = 0;
       bool first = true;
       for (int idx = blockIdx.x; idx < nitems; idx += gridDim.x) {
-        const Item it = get_item(p, idx);
+        const Item it = get_item(p, idx, C::kBK);
         if (it.nk == 0) continue;
         if (!mbar_wait(&tempty[abuf], aphase ^ 1, abort_flag, p.status)) break;
         tc_fence_after();
@@ -532,11 +546,13 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
           const uint32_t a0 = smem_u32(smem + stage * C::kStageBytes);
           const uint32_t b0 = a0 + C::kABytes;
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t ad = C::kAMN ? smem_desc_sw128(a0 + kk * 2048, kChunkBytes, 1024)
-                                        : smem_desc_sw128(a0 + kk * 32, 16, 1024);
-            const uint64_t bd = C::kBMN ? smem_desc_sw128(b0 + kk * 2048, kChunkBytes, 1024)
-                                        : smem_desc_sw128(b0 + kk * 32, 16, 1024);
+          for (int kk = 0; kk < C::kBK / 16; ++kk) {
+            // K-major: 16 elements = 32 bytes along the swizzled row; MN-major: 16
+            // K-rows; SBO = 8 rows, LBO (MN-major) = one chunk of kBK elements
+            const uint64_t ad = C::kAMN ? smem_desc(a0 + kk * 16 * C::kRowBytes, C::kMnChunkBytes, 8 * C::kRowBytes, C::kSwz)
+                                        : smem_desc(a0 + kk * 32, 16, 8 * C::kRowBytes, C::kSwz);
+            const uint64_t bd = C::kBMN ? smem_desc(b0 + kk * 16 * C::kRowBytes, C::kMnChunkBytes, 8 * C::kRowBytes, C::kSwz)
+                                        : smem_desc(b0 + kk * 32, 16, 8 * C::kRowBytes, C::kSwz);
             umma_bf16(acc, ad, bd, C::kIdesc, (kb | kk) ? 1u : 0u);
           }
           umma_commit(&empty[stage]);
@@ -558,10 +574,10 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
       umma_commit(done);
       mbar_drain(done, 0);
     }
-  } else if (warp >= 6) {
+  } else if (warp >= C::kGatherWarp0) {
     // ------------------------------------------------------------ gather warps
     if constexpr (C::kHasLsu) {
-      const int gw = warp - 6;
+      const int gw = warp - C::kGatherWarp0;
       constexpr bool kMN = (A_SRC == SRC_MN_GATHER_LSU || B_SRC == SRC_MN_GATHER_LSU);
       const int bn_out = (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_MX) ? BN / 2 : BN;
       // token of tile row (lane>>2)*16 + gw*4 + (lane&3) for a K-major gather
@@ -578,7 +594,7 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
       Item it{};
       int rtok = -1, kt0 = -1, kt1 = -1, kt2 = -1;  // current item's tokens (K-blocks kb..kb+2)
       if (idx < nitems) {
-        it = get_item(p, idx);
+        it = get_item(p, idx, C::kBK);
         if (A_SRC == SRC_K_GATHER_LSU) rtok = row_token(it);
         if (kMN) {
           kt0 = k_token(it, 0);
@@ -592,7 +608,7 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
         const int nidx = idx + gridDim.x;
         const bool has_next = nidx < nitems;
         Item nit{};
-        if (has_next) nit = get_item(p, nidx);
+        if (has_next) nit = get_item(p, nidx, C::kBK);
         int nrtok = -1, nkt0 = -1, nkt1 = -1, nkt2 = -1;
         auto fetch_next = [&]() {
           if (!has_next) return;
@@ -618,7 +634,7 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
           }
           uint8_t* sA = smem + stage * C::kStageBytes;
           uint8_t* sB = sA + C::kABytes;
-          const int k0 = kb * kBK;
+          const int k0 = kb * C::kBK;
           if (A_SRC == SRC_K_GATHER_LSU) {
             const int c = lane & 7;
             const uint16_t* base = p.ga + k0 + c * 8;
@@ -659,7 +675,7 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
     int abuf = 0;
     uint32_t aphase = 0;
     for (int idx = blockIdx.x; idx < nitems; idx += gridDim.x) {
-      const Item it = get_item(p, idx);
+      const Item it = get_item(p, idx, C::kBK);
       const int bn_out = (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_MX) ? BN / 2 : BN;
       const int n0 = it.nt * bn_out;
       if (it.nk == 0) {
@@ -679,6 +695,12 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
       }
       // SwiGLU backward: row state and the first chunk of the saved gate|up,
       // fetched before the accumulator is ready
+      // this warp's 32-column chunks: all of them, or one half when two warps
+      // share a lane quarter
+      constexpr int kChunks = BN / 32;
+      const int epi_half = (warp - 2) >> 2;
+      const int epi_c0 = (C::kEpiWarps == 8) ? epi_half * (kChunks / 2) : 0;
+      const int epi_c1 = (C::kEpiWarps == 8) ? epi_c0 + kChunks / 2 : kChunks;
       int f_bwd = -1;
       bool v_bwd = false, inb_bwd = false;
       float wt_bwd = 1.f;
@@ -695,7 +717,8 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
           inb_bwd = v_bwd;
         }
         if (v_bwd) {
-          const uint16_t* gu = static_cast<const uint16_t*>(p.aux0) + static_cast<long long>(prow) * 2 * p.N + n0;
+          const uint16_t* gu = static_cast<const uint16_t*>(p.aux0) + static_cast<long long>(prow) * 2 * p.N + n0 +
+                               epi_c0 * 32;
           load_raw64(gu, ng);
           load_raw64(gu + p.N, nu);
         }
@@ -779,9 +802,17 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
         const uint16_t* gu = static_cast<const uint16_t*>(p.aux0) + static_cast<long long>(prow) * 2 * p.N + n0;
         uint16_t* dgu = inb_bwd ? static_cast<uint16_t*>(p.out0) + static_cast<long long>(prow) * 2 * p.N + n0 : nullptr;
         uint16_t* hw = inb_bwd ? static_cast<uint16_t*>(p.out1) + static_cast<long long>(prow) * p.N + n0 : nullptr;
+        // router-weight partial sums, one per half of the tile's columns (the
+        // same split whether one warp or two cover the row)
         float dpart = 0.f;
+        float* dwp = (p.grouped && v_bwd) ? p.dw_part + (static_cast<long long>(f_bwd) * p.n_tiles + it.nt) * 2
+                                          : nullptr;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = epi_c0; c < epi_c1; ++c) {
+          if (C::kEpiWarps == 4 && c == kChunks / 2) {
+            if (dwp) dwp[0] = dpart;
+            dpart = 0.f;
+          }
           uint32_t wdg[16], wdu[16], whv[16];
 #pragma unroll
           for (int half = 0; half < 2; ++half) {   // 16 accumulator columns at a time
@@ -810,7 +841,7 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
               whv[(half * 16 + i) >> 1] = pack_bf16(hh[0], hh[1]);
             }
           }
-          if (v_bwd && c + 1 < BN / 32) {   // next chunk's gate|up, in flight during the stores
+          if (v_bwd && c + 1 < epi_c1) {   // next chunk's gate|up, in flight during the stores
             load_raw64(gu + (c + 1) * 32, ng);
             load_raw64(gu + p.N + (c + 1) * 32, nu);
           }
@@ -818,7 +849,7 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
           warp_store_row64(wdu, dgu ? dgu + p.N + c * 32 : nullptr, wstage, lane);
           warp_store_row64(whv, hw ? hw + c * 32 : nullptr, wstage, lane);
         }
-        if (p.grouped && v_bwd) p.dw_part[static_cast<long long>(f_bwd) * p.n_tiles + it.nt] = dpart;
+        if (dwp) dwp[C::kEpiWarps == 8 ? epi_half : 1] = dpart;
       } else if constexpr (EPI == EPI_WGRAD) {
         const int m = it.m0 + r;
         uint16_t* dst = (m < p.split)

@@ -205,16 +205,17 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Shared-memory matrix descriptor (tcgen05 format): 128-byte swizzle, start
-// address, leading- and stride-dimension byte offsets, descriptor version 1.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes,
-                                                    uint32_t sbo_bytes) {
+// Shared-memory matrix descriptor (tcgen05 format): start address, leading-
+// and stride-dimension byte offsets, descriptor version 1, and the swizzle
+// mode (2 = 128-byte, 4 = 64-byte).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                              uint32_t layout) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
   d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
   d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
   d |= static_cast<uint64_t>(1) << 46;   // descriptor version for tcgen05
-  d |= static_cast<uint64_t>(2) << 61;   // SWIZZLE_128B
+  d |= static_cast<uint64_t>(layout & 7u) << 61;
   return d;
 }
 
