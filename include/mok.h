@@ -77,10 +77,10 @@ typedef int mok_status_t;
                                         results, slower; kept for comparison) */
 
 /* Stages of the layer, for optional per-stage timing events. */
-#define MOK_STAGE_FWD_PREP                 0  /* status hand-over; MXFP8: quantise x, expand operands */
+#define MOK_STAGE_FWD_PREP                 0  /* status hand-over; MXFP8: weight scales into the tensor-core layout */
 #define MOK_STAGE_FWD_SHARED_GATEUP        1  /* shared gate/up GEMM + SwiGLU */
 #define MOK_STAGE_FWD_SHARED_DOWN          2  /* shared down GEMM */
-#define MOK_STAGE_FWD_GATEUP               3  /* routed gathered gate/up GEMM + SwiGLU */
+#define MOK_STAGE_FWD_GATEUP               3  /* routed gate/up GEMM + SwiGLU */
 #define MOK_STAGE_FWD_DOWN                 4  /* routed down GEMM + router scale + scatter */
 #define MOK_STAGE_FWD_COMBINE              5  /* fixed-order combine into y */
 #define MOK_STAGE_BWD_DOWN                 6  /* routed dgrad through down + SwiGLU bwd + router-grad partials */
@@ -92,7 +92,9 @@ typedef int mok_status_t;
 #define MOK_STAGE_BWD_SHARED_WGRAD_GATEUP 12
 #define MOK_STAGE_BWD_SHARED_DGRAD        13
 #define MOK_STAGE_BWD_REDUCE              14  /* fixed-order dx combine + router-grad reduce */
-#define MOK_NUM_STAGES                    15
+#define MOK_STAGE_FWD_DISPATCH            15  /* token rows of x into schedule order (MXFP8: quantised on the way) */
+#define MOK_STAGE_BWD_DISPATCH            16  /* token rows of dy (and x) into schedule order */
+#define MOK_NUM_STAGES                    17
 
 /* Per-call knobs ([MoKEd] "Tuning the five hyperparameters before
  * production").  minibatch_size (0 = T) sets the order in which the
@@ -172,19 +174,26 @@ typedef struct {
   uint16_t* gu;       /* [max_tiles*128][2I] gate | up pre-activations per schedule row (saved) */
   uint16_t* h;        /* [max_tiles*128][I]  SwiGLU output, bf16 mode (scratch) */
   uint8_t*  hq;       /* [max_tiles*128][I]  SwiGLU output E4M3 codes, MXFP8 mode (scratch) */
-  uint8_t*  hq_sc;    /* [max_tiles*128][I/32] its E8M0 scales */
+  uint8_t*  hq_sc;    /* its E8M0 scales, tensor-core scale layout (below) */
   uint16_t* slots;    /* [T*k][H] router-weighted expert outputs (scratch) */
   uint16_t* gu_s;     /* [T][2 I_s] shared gate | up (saved) */
   uint16_t* h_s;      /* [T][I_s] shared SwiGLU output, bf16 mode (scratch) */
   uint8_t*  hq_s;     /* [T][I_s] shared SwiGLU output codes, MXFP8 mode */
-  uint8_t*  hq_s_sc;  /* [T][I_s/32] */
+  uint8_t*  hq_s_sc;  /* its scales, tensor-core scale layout (rows padded to 128) */
   uint16_t* shared_out; /* [T][H] shared expert output (scratch) */
-  uint8_t*  xq;       /* [T][H] x codes, MXFP8 mode (scratch) */
-  uint8_t*  xq_sc;    /* [T][H/32] */
+  uint8_t*  xq;       /* [T][H] x codes in token order, MXFP8 mode (scratch) */
+  uint8_t*  xq_sc;    /* their scales, tensor-core scale layout (rows padded to 128) */
   int32_t*  status;   /* device status word: MOK_OK or the first device error */
   uint16_t* x_perm;   /* [max_tiles*128][H] token rows of x in schedule order (MOK_DISPATCH_PERMUTE) */
   int dispatch;       /* the dispatch the forward used */
+  uint8_t*  xq_perm;  /* [max_tiles*128][H] x codes in schedule order, MXFP8 mode (scratch) */
+  uint8_t*  xq_perm_sc; /* their scales, tensor-core scale layout */
 } mok_ctx_t;
+/* Tensor-core scale layout (MXFP8 context scratch): the E8M0 scales of a
+ * [R][K] code tensor as 512-byte atoms, one per (128-row block rb, 128-column
+ * group g), atom index rb * (K/128) + g; inside an atom, row r's scales of
+ * the group's four 32-column blocks are the bytes of one 32-bit word at byte
+ * (r % 32) * 16 + (r / 32) * 4, block b at byte b % 4 of it. */
 
 /* Weight gradients (bf16, same layouts as the weights; shared ones NULL when
  * the layer has no shared expert). */

@@ -31,10 +31,11 @@ P = C.c_void_p
 I32P = C.POINTER(C.c_int32)
 
 
-MOK_NUM_STAGES = 15
+MOK_NUM_STAGES = 17
 STAGE_NAMES = ["fwd_prep", "fwd_shared_gateup", "fwd_shared_down", "fwd_gateup", "fwd_down", "fwd_combine",
                "bwd_down", "bwd_wgrad_down", "bwd_wgrad_gateup", "bwd_dgrad_gateup", "bwd_shared_down",
-               "bwd_shared_wgrad_down", "bwd_shared_wgrad_gateup", "bwd_shared_dgrad", "bwd_reduce"]
+               "bwd_shared_wgrad_down", "bwd_shared_wgrad_gateup", "bwd_shared_dgrad", "bwd_reduce",
+               "fwd_dispatch", "bwd_dispatch"]
 
 
 class MokConfig(C.Structure):
@@ -61,7 +62,7 @@ class MokCtx(C.Structure):
                 ("I_s", C.c_int), ("mode", C.c_int), ("max_tiles", C.c_int),
                 ("gu", P), ("h", P), ("hq", P), ("hq_sc", P), ("slots", P), ("gu_s", P), ("h_s", P),
                 ("hq_s", P), ("hq_s_sc", P), ("shared_out", P), ("xq", P), ("xq_sc", P), ("status", P),
-                ("x_perm", P), ("dispatch", C.c_int)]
+                ("x_perm", P), ("dispatch", C.c_int), ("xq_perm", P), ("xq_perm_sc", P)]
 
 
 class MokWeightGrads(C.Structure):

@@ -127,6 +127,24 @@ mok_status_t make_map_mn(CUtensorMap* m, const void* base, uint64_t width, uint6
   return MOK_OK;
 }
 
+// 2-D tensor of E4M3 codes [outer][inner] (bytes) with a box of box_outer rows
+// x 128 bytes, 128-byte swizzle; out-of-range elements read as zero.
+mok_status_t make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(MOK_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner};
+  const cuuint32_t box[2] = {128, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MOK_ERR_CUDA, "cuTensorMapEncodeTiled (E4M3) failed (%d) for [%llu x %llu] box %u", (int)r,
+                (unsigned long long)outer, (unsigned long long)inner, box_outer);
+  return MOK_OK;
+}
+
 // K-block of the GEMM kernels (elements per stage); the map builders also
 // support 32 (64-byte swizzle).
 constexpr int kTileBK = 64;
@@ -174,16 +192,13 @@ size_t carve_schedule(void* buf, int T, int k, int E, SchedLayout* L) {
 }
 
 struct CtxExtra {  // forward scratch beyond the public context fields
-  uint16_t* h_deq;      // MXFP8 mode: bf16 expansion of h [max_rows][I]
-  uint16_t* hs_deq;     // [T][I_s]
-  uint16_t* x_deq;      // [T][H]
-  uint16_t* wg_deq;     // [E][I][H]
-  uint16_t* wu_deq;
-  uint16_t* wd_deq;     // [E][H][I]
-  uint16_t* wsg_deq;    // [I_s][H]
-  uint16_t* wsu_deq;
-  uint16_t* wsd_deq;    // [H][I_s]
+  // MXFP8 mode: weight scales in the tensor-core scale layout
+  uint8_t *wg_sc, *wu_sc, *wd_sc, *wsg_sc, *wsu_sc, *wsd_sc;
 };
+
+// Bytes of E8M0 scales of a [rows][K] tensor in the tensor-core scale layout
+// (rows padded to whole 128-row blocks).
+long long tiled_scale_bytes(long long rows, long long K) { return (rows + 127) / 128 * 128 * (K / 32); }
 
 size_t carve_ctx(void* buf, int T, int k, int E, int H, int I, int Is, int mode, mok_ctx_t* ctx,
                  CtxExtra* X) {
@@ -197,20 +212,20 @@ size_t carve_ctx(void* buf, int T, int k, int E, int H, int I, int Is, int mode,
   ctx->max_tiles = static_cast<int>(max_tiles_of(T, k, E));
   ctx->status = c.take<int32_t>(8);
   ctx->gu = c.take<uint16_t>(mr * 2 * I);
-  ctx->x_perm = c.take<uint16_t>(mr * H);
   ctx->slots = c.take<uint16_t>(n * H);
   if (!mx) {
+    ctx->x_perm = c.take<uint16_t>(mr * H);
     ctx->h = c.take<uint16_t>(mr * I);
   } else {
-    ctx->hq = c.take<uint8_t>(mr * I);
-    ctx->hq_sc = c.take<uint8_t>(mr * I / 32);
     ctx->xq = c.take<uint8_t>(static_cast<long long>(T) * H);
-    ctx->xq_sc = c.take<uint8_t>(static_cast<long long>(T) * H / 32);
-    X->h_deq = c.take<uint16_t>(mr * I);
-    X->x_deq = c.take<uint16_t>(static_cast<long long>(T) * H);
-    X->wg_deq = c.take<uint16_t>(static_cast<long long>(E) * I * H);
-    X->wu_deq = c.take<uint16_t>(static_cast<long long>(E) * I * H);
-    X->wd_deq = c.take<uint16_t>(static_cast<long long>(E) * H * I);
+    ctx->xq_sc = c.take<uint8_t>(tiled_scale_bytes(T, H));
+    ctx->xq_perm = c.take<uint8_t>(mr * H);
+    ctx->xq_perm_sc = c.take<uint8_t>(tiled_scale_bytes(mr, H));
+    ctx->hq = c.take<uint8_t>(mr * I);
+    ctx->hq_sc = c.take<uint8_t>(tiled_scale_bytes(mr, I));
+    X->wg_sc = c.take<uint8_t>(tiled_scale_bytes(static_cast<long long>(E) * I, H));
+    X->wu_sc = c.take<uint8_t>(tiled_scale_bytes(static_cast<long long>(E) * I, H));
+    X->wd_sc = c.take<uint8_t>(tiled_scale_bytes(static_cast<long long>(E) * H, I));
   }
   if (Is > 0) {
     ctx->gu_s = c.take<uint16_t>(static_cast<long long>(T) * 2 * Is);
@@ -219,11 +234,10 @@ size_t carve_ctx(void* buf, int T, int k, int E, int H, int I, int Is, int mode,
       ctx->h_s = c.take<uint16_t>(static_cast<long long>(T) * Is);
     } else {
       ctx->hq_s = c.take<uint8_t>(static_cast<long long>(T) * Is);
-      ctx->hq_s_sc = c.take<uint8_t>(static_cast<long long>(T) * Is / 32);
-      X->hs_deq = c.take<uint16_t>(static_cast<long long>(T) * Is);
-      X->wsg_deq = c.take<uint16_t>(static_cast<long long>(Is) * H);
-      X->wsu_deq = c.take<uint16_t>(static_cast<long long>(Is) * H);
-      X->wsd_deq = c.take<uint16_t>(static_cast<long long>(H) * Is);
+      ctx->hq_s_sc = c.take<uint8_t>(tiled_scale_bytes(T, Is));
+      X->wsg_sc = c.take<uint8_t>(tiled_scale_bytes(Is, H));
+      X->wsu_sc = c.take<uint8_t>(tiled_scale_bytes(Is, H));
+      X->wsd_sc = c.take<uint8_t>(tiled_scale_bytes(H, Is));
     }
   }
   return c.off + 256;
@@ -342,6 +356,193 @@ mok_status_t static_sched_scratch(int32_t** out) {
 }
 }  // namespace
 
+namespace {
+
+// BF16 forward: shared expert, then the routed experts (token rows of x
+// permuted into schedule order, or gathered inside the GEMM).
+mok_status_t forward_bf16(const mok_config_t* cfg, const uint16_t* x, const float* router_w, const mok_schedule_t* s,
+                          const mok_weights_t* w, mok_ctx_t* ctx, long long mr, int sms, bool g4, cudaStream_t cs) {
+  const int T = s->T, k = s->k, E = s->E, H = w->H, I = w->I, Is = w->I_s;
+  mok_status_t st;
+  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_PREP, 1, cs));
+
+  // ---- shared expert: gate/up + SwiGLU over all T tokens, then down
+  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_GATEUP, 0, cs));
+  if (Is > 0) {
+    GemmMaps m;
+    if ((st = make_map(&m.a, x, H, T, 128, kTileBK)) || (st = make_map(&m.b0, w->ws_gate, H, Is, 128, kTileBK)) ||
+        (st = make_map(&m.b1, w->ws_up, H, Is, 128, kTileBK)))
+      return st;
+    GemmParams p = base_params(nullptr, ctx->status, 0);
+    p.rows = T; p.K = H; p.N = Is; p.n_tiles = Is / 128; p.b_rows_per_expert = 0;
+    p.out0 = ctx->gu_s; p.out1 = ctx->h_s;
+    const int items = ((T + 127) / 128) * p.n_tiles;
+    MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 256, EPI_SWIGLU>(m, p, items < sms ? items : sms, cs)));
+    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_GATEUP, 1, cs));
+    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_DOWN, 0, cs));
+    GemmMaps m2;
+    const int bn = tile_n(H);
+    if ((st = make_map(&m2.a, ctx->h_s, Is, T, 128, kTileBK)) || (st = make_map(&m2.b0, w->ws_down, Is, H, bn, kTileBK)))
+      return st;
+    m2.b1 = m2.b0;
+    GemmParams q = base_params(nullptr, ctx->status, 0);
+    q.rows = T; q.K = Is; q.N = H; q.n_tiles = H / bn; q.out0 = ctx->shared_out; q.ld = H;
+    const int items2 = ((T + 127) / 128) * q.n_tiles;
+    const int grid2 = items2 < sms ? items2 : sms;
+    if (bn == 256)
+      MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 256, EPI_STORE_ROWS>(m2, q, grid2, cs)));
+    else
+      MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 128, EPI_STORE_ROWS>(m2, q, grid2, cs)));
+  } else {
+    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_GATEUP, 1, cs));
+    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_DOWN, 0, cs));
+  }
+  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_DOWN, 1, cs));
+
+  // ---- routed experts: gate/up + SwiGLU, then down + scale + scatter
+  const int disp = resolve_dispatch(cfg);
+  ctx->dispatch = disp;
+  const bool perm = disp == MOK_DISPATCH_PERMUTE;
+  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 0, cs));
+  if (perm)  // token rows of x in schedule order, read below as dense tiles
+    MOK_CUDA(launch_permute_rows(x, H, k, s->row_src, s->header, mr, ctx->x_perm, sms, cs));
+  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 1, cs));
+  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_GATEUP, 0, cs));
+  GemmMaps m;
+  const int bk = perm ? kTileBK : kGatherBK;
+  if ((st = perm ? make_map(&m.a, ctx->x_perm, H, mr, 128, bk) : make_map(&m.a, x, H, T, 1, bk)) ||
+      (st = make_map(&m.b0, w->w_gate, H, static_cast<uint64_t>(E) * I, 128, bk)) ||
+      (st = make_map(&m.b1, w->w_up, H, static_cast<uint64_t>(E) * I, 128, bk)))
+    return st;
+  GemmParams p = base_params(s, ctx->status, cfg->debug_flags);
+  p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / 128; p.b_rows_per_expert = I;
+  p.out0 = ctx->gu; p.out1 = ctx->h; p.ga = x; p.ga_ld = H;
+  const long long items = static_cast<long long>(s->max_tiles) * p.n_tiles;
+  const int grid = items < sms ? static_cast<int>(items) : sms;
+  if (perm)
+    MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 256, EPI_SWIGLU>(m, p, grid, cs)));
+  else if (g4)
+    MOK_CUDA((launch_gemm<SRC_K_GATHER, SRC_K_TILE, 256, EPI_SWIGLU>(m, p, grid, cs)));
+  else
+    MOK_CUDA((launch_gemm<SRC_K_GATHER_LSU, SRC_K_TILE, 256, EPI_SWIGLU>(m, p, grid, cs)));
+  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_GATEUP, 1, cs));
+  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DOWN, 0, cs));
+  GemmMaps m2;
+  const int bn = tile_n(H);
+  if ((st = make_map(&m2.a, ctx->h, I, mr, 128, kTileBK)) ||
+      (st = make_map(&m2.b0, w->w_down, I, static_cast<uint64_t>(E) * H, bn, kTileBK)))
+    return st;
+  m2.b1 = m2.b0;
+  GemmParams q = base_params(s, ctx->status, 0);
+  q.grouped = 1; q.K = I; q.N = H; q.n_tiles = H / bn; q.b_rows_per_expert = H;
+  q.out0 = ctx->slots; q.ld = H; q.rw = router_w;
+  const long long items2 = static_cast<long long>(s->max_tiles) * q.n_tiles;
+  const int grid2 = items2 < sms ? static_cast<int>(items2) : sms;
+  if (bn == 256)
+    MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 256, EPI_SCALE_SCATTER>(m2, q, grid2, cs)));
+  else
+    MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 128, EPI_SCALE_SCATTER>(m2, q, grid2, cs)));
+  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DOWN, 1, cs));
+  return MOK_OK;
+}
+
+// MXFP8 forward: x quantised straight into token order (shared expert) and
+// schedule order (routed experts), weight scales rearranged for the tensor
+// core, then the same four GEMMs on the block-scaled MMA; h is requantised in
+// the SwiGLU epilogue.
+mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const float* router_w,
+                           const mok_schedule_t* s, const mok_weights_t* w, mok_ctx_t* ctx, const CtxExtra& X,
+                           int sms, cudaStream_t cs) {
+  const int T = s->T, k = s->k, E = s->E, H = w->H, I = w->I, Is = w->I_s;
+  const long long mr = static_cast<long long>(s->max_tiles) * kTileRows;
+  mok_status_t st;
+  MOK_CUDA(launch_mx_tile_scales(w->mx_gate_sc, static_cast<long long>(E) * I, H, X.wg_sc, cs));
+  MOK_CUDA(launch_mx_tile_scales(w->mx_up_sc, static_cast<long long>(E) * I, H, X.wu_sc, cs));
+  MOK_CUDA(launch_mx_tile_scales(w->mx_down_sc, static_cast<long long>(E) * H, I, X.wd_sc, cs));
+  if (Is > 0) {
+    MOK_CUDA(launch_mx_tile_scales(w->mxs_gate_sc, Is, H, X.wsg_sc, cs));
+    MOK_CUDA(launch_mx_tile_scales(w->mxs_up_sc, Is, H, X.wsu_sc, cs));
+    MOK_CUDA(launch_mx_tile_scales(w->mxs_down_sc, H, Is, X.wsd_sc, cs));
+  }
+  ctx->dispatch = MOK_DISPATCH_PERMUTE;
+  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_PREP, 1, cs));
+  // x quantised once per token, into token order and schedule order
+  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 0, cs));
+  MOK_CUDA(launch_mx_dispatch(x, T, H, k, s->slot_row, s->row_src, s->header, mr, ctx->xq, ctx->xq_sc, ctx->xq_perm,
+                              ctx->xq_perm_sc, sms, cs));
+  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 1, cs));
+
+  const int bn = tile_n(H);
+  // ---- shared expert
+  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_GATEUP, 0, cs));
+  if (Is > 0) {
+    GemmMaps m;
+    if ((st = make_map_u8(&m.a, ctx->xq, H, T, 128)) || (st = make_map_u8(&m.b0, w->mxs_gate, H, Is, 128)) ||
+        (st = make_map_u8(&m.b1, w->mxs_up, H, Is, 128)))
+      return st;
+    GemmParams p = base_params(nullptr, ctx->status, 0);
+    p.rows = T; p.K = H; p.N = Is; p.n_tiles = Is / 128; p.b_rows_per_expert = 0;
+    p.out0 = ctx->gu_s; p.out1 = ctx->hq_s; p.sf_out = ctx->hq_s_sc;
+    p.sfa = ctx->xq_sc; p.sfb0 = X.wsg_sc; p.sfb1 = X.wsu_sc;
+    const int items = ((T + 127) / 128) * p.n_tiles;
+    MOK_CUDA((launch_gemm_mx<256, EPI_SWIGLU_MX>(m, p, items < sms ? items : sms, cs)));
+    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_GATEUP, 1, cs));
+    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_DOWN, 0, cs));
+    GemmMaps m2;
+    if ((st = make_map_u8(&m2.a, ctx->hq_s, Is, T, 128)) || (st = make_map_u8(&m2.b0, w->mxs_down, Is, H, bn)))
+      return st;
+    m2.b1 = m2.b0;
+    GemmParams q = base_params(nullptr, ctx->status, 0);
+    q.rows = T; q.K = Is; q.N = H; q.n_tiles = H / bn; q.out0 = ctx->shared_out; q.ld = H;
+    q.sfa = ctx->hq_s_sc; q.sfb0 = X.wsd_sc;
+    const int items2 = ((T + 127) / 128) * q.n_tiles;
+    const int grid2 = items2 < sms ? items2 : sms;
+    if (bn == 256)
+      MOK_CUDA((launch_gemm_mx<256, EPI_STORE_ROWS>(m2, q, grid2, cs)));
+    else
+      MOK_CUDA((launch_gemm_mx<128, EPI_STORE_ROWS>(m2, q, grid2, cs)));
+  } else {
+    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_GATEUP, 1, cs));
+    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_DOWN, 0, cs));
+  }
+  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_DOWN, 1, cs));
+
+  // ---- routed experts
+  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_GATEUP, 0, cs));
+  GemmMaps m;
+  if ((st = make_map_u8(&m.a, ctx->xq_perm, H, mr, 128)) ||
+      (st = make_map_u8(&m.b0, w->mx_gate, H, static_cast<uint64_t>(E) * I, 128)) ||
+      (st = make_map_u8(&m.b1, w->mx_up, H, static_cast<uint64_t>(E) * I, 128)))
+    return st;
+  GemmParams p = base_params(s, ctx->status, cfg->debug_flags);
+  p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / 128; p.b_rows_per_expert = I;
+  p.out0 = ctx->gu; p.out1 = ctx->hq; p.sf_out = ctx->hq_sc;
+  p.sfa = ctx->xq_perm_sc; p.sfb0 = X.wg_sc; p.sfb1 = X.wu_sc;
+  const long long items = static_cast<long long>(s->max_tiles) * p.n_tiles;
+  MOK_CUDA((launch_gemm_mx<256, EPI_SWIGLU_MX>(m, p, items < sms ? static_cast<int>(items) : sms, cs)));
+  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_GATEUP, 1, cs));
+  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DOWN, 0, cs));
+  GemmMaps m2;
+  if ((st = make_map_u8(&m2.a, ctx->hq, I, mr, 128)) ||
+      (st = make_map_u8(&m2.b0, w->mx_down, I, static_cast<uint64_t>(E) * H, bn)))
+    return st;
+  m2.b1 = m2.b0;
+  GemmParams q = base_params(s, ctx->status, 0);
+  q.grouped = 1; q.K = I; q.N = H; q.n_tiles = H / bn; q.b_rows_per_expert = H;
+  q.out0 = ctx->slots; q.ld = H; q.rw = router_w;
+  q.sfa = ctx->hq_sc; q.sfb0 = X.wd_sc;
+  const long long items2 = static_cast<long long>(s->max_tiles) * q.n_tiles;
+  const int grid2 = items2 < sms ? static_cast<int>(items2) : sms;
+  if (bn == 256)
+    MOK_CUDA((launch_gemm_mx<256, EPI_SCALE_SCATTER>(m2, q, grid2, cs)));
+  else
+    MOK_CUDA((launch_gemm_mx<128, EPI_SCALE_SCATTER>(m2, q, grid2, cs)));
+  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DOWN, 1, cs));
+  return MOK_OK;
+}
+
+}  // namespace
+
 // ===========================================================================
 extern "C" {
 
@@ -444,6 +645,12 @@ mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x, const float
              (Is > 0 && (!w->mxs_gate || !w->mxs_gate_sc || !w->mxs_up || !w->mxs_up_sc || !w->mxs_down ||
                          !w->mxs_down_sc))))
     return fail(MOK_ERR_INVALID_ARG, "MXFP8 mode needs the prequantised weights");
+  if (mx) {
+    const void* mp[] = {w->mx_gate, w->mx_gate_sc, w->mx_up, w->mx_up_sc, w->mx_down, w->mx_down_sc,
+                        w->mxs_gate, w->mxs_gate_sc, w->mxs_up, w->mxs_up_sc, w->mxs_down, w->mxs_down_sc};
+    for (const void* q : mp)
+      if (!aligned16(q)) return fail(MOK_ERR_INVALID_ARG, "misaligned MXFP8 weight pointer");
+  }
   const void* ptrs[] = {x, router_w, y, ctx_buf, w->w_gate, w->w_up, w->w_down};
   for (const void* q : ptrs)
     if (!aligned16(q)) return fail(MOK_ERR_INVALID_ARG, "misaligned pointer");
@@ -462,124 +669,12 @@ mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x, const float
   MOK_CUDA(cudaGetLastError());
 
   const long long mr = static_cast<long long>(s->max_tiles) * kTileRows;
-  const uint16_t *xa = x, *wg = w->w_gate, *wu = w->w_up, *wd = w->w_down;
-  const uint16_t *wsg = w->ws_gate, *wsu = w->ws_up, *wsd = w->ws_down;
   if (mx) {
-    // MXFP8 operands, expanded exactly to bf16 for the tensor-core GEMMs
-    MOK_CUDA(launch_mx_quantize(x, static_cast<long long>(T) * H / 32, ctx->xq, ctx->xq_sc, sms, cs));
-    MOK_CUDA(launch_mx_dequant(ctx->xq, ctx->xq_sc, static_cast<long long>(T) * H / 32, X.x_deq, sms, cs));
-    const long long nw = static_cast<long long>(E) * I * H / 32;
-    MOK_CUDA(launch_mx_dequant(w->mx_gate, w->mx_gate_sc, nw, X.wg_deq, sms, cs));
-    MOK_CUDA(launch_mx_dequant(w->mx_up, w->mx_up_sc, nw, X.wu_deq, sms, cs));
-    MOK_CUDA(launch_mx_dequant(w->mx_down, w->mx_down_sc, nw, X.wd_deq, sms, cs));
-    xa = X.x_deq; wg = X.wg_deq; wu = X.wu_deq; wd = X.wd_deq;
-    if (Is > 0) {
-      const long long ns = static_cast<long long>(Is) * H / 32;
-      MOK_CUDA(launch_mx_dequant(w->mxs_gate, w->mxs_gate_sc, ns, X.wsg_deq, sms, cs));
-      MOK_CUDA(launch_mx_dequant(w->mxs_up, w->mxs_up_sc, ns, X.wsu_deq, sms, cs));
-      MOK_CUDA(launch_mx_dequant(w->mxs_down, w->mxs_down_sc, ns, X.wsd_deq, sms, cs));
-      wsg = X.wsg_deq; wsu = X.wsu_deq; wsd = X.wsd_deq;
-    }
-  }
-  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_PREP, 1, cs));
-
-  // ---- shared expert: gate/up + SwiGLU over all T tokens, then down
-  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_GATEUP, 0, cs));
-  if (Is > 0) {
-    GemmMaps m;
-    if ((st = make_map(&m.a, xa, H, T, 128, kTileBK)) || (st = make_map(&m.b0, wsg, H, Is, 128, kTileBK)) ||
-        (st = make_map(&m.b1, wsu, H, Is, 128, kTileBK)))
-      return st;
-    GemmParams p = base_params(nullptr, ctx->status, 0);
-    p.rows = T; p.K = H; p.N = Is; p.n_tiles = Is / 128; p.b_rows_per_expert = 0;
-    p.out0 = ctx->gu_s;
-    const int items = ((T + 127) / 128) * p.n_tiles;
-    const int grid = items < sms ? items : sms;
-    if (!mx) {
-      p.out1 = ctx->h_s;
-      MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 256, EPI_SWIGLU>(m, p, grid, cs)));
-    } else {
-      p.out1 = ctx->hq_s; p.out2 = ctx->hq_s_sc;
-      MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 256, EPI_SWIGLU_MX>(m, p, grid, cs)));
-      MOK_CUDA(launch_mx_dequant(ctx->hq_s, ctx->hq_s_sc, static_cast<long long>(T) * Is / 32, X.hs_deq, sms, cs));
-    }
-    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_GATEUP, 1, cs));
-    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_DOWN, 0, cs));
-    const uint16_t* hs = mx ? X.hs_deq : ctx->h_s;
-    GemmMaps m2;
-    if ((st = make_map(&m2.a, hs, Is, T, 128, kTileBK)) || (st = make_map(&m2.b0, wsd, Is, H, tile_n(H), kTileBK))) return st;
-    m2.b1 = m2.b0;
-    GemmParams q = base_params(nullptr, ctx->status, 0);
-    const int bn = tile_n(H);
-    q.rows = T; q.K = Is; q.N = H; q.n_tiles = H / bn; q.out0 = ctx->shared_out; q.ld = H;
-    const int items2 = ((T + 127) / 128) * q.n_tiles;
-    const int grid2 = items2 < sms ? items2 : sms;
-    if (bn == 256)
-      MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 256, EPI_STORE_ROWS>(m2, q, grid2, cs)));
-    else
-      MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 128, EPI_STORE_ROWS>(m2, q, grid2, cs)));
+    st = forward_mxfp8(cfg, x, router_w, s, w, ctx, X, sms, cs);
+    if (st) return st;
   } else {
-    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_GATEUP, 1, cs));
-    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_DOWN, 0, cs));
-  }
-  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_DOWN, 1, cs));
-
-  // ---- routed experts: gathered gate/up + SwiGLU, then down + scale + scatter
-  {
-    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_GATEUP, 0, cs));
-    const int disp = resolve_dispatch(cfg);
-    ctx->dispatch = disp;
-    const bool perm = disp == MOK_DISPATCH_PERMUTE;
-    if (perm)  // token rows of x in schedule order, read below as dense tiles
-      MOK_CUDA(launch_permute_rows(xa, H, k, s->row_src, s->header, mr, ctx->x_perm, sms, cs));
-    GemmMaps m;
-    const int bk = perm ? kTileBK : kGatherBK;
-    if ((st = perm ? make_map(&m.a, ctx->x_perm, H, mr, 128, bk) : make_map(&m.a, xa, H, T, 1, bk)) ||
-        (st = make_map(&m.b0, wg, H, static_cast<uint64_t>(E) * I, 128, bk)) ||
-        (st = make_map(&m.b1, wu, H, static_cast<uint64_t>(E) * I, 128, bk)))
-      return st;
-    GemmParams p = base_params(s, ctx->status, cfg->debug_flags);
-    p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / 128; p.b_rows_per_expert = I;
-    p.out0 = ctx->gu; p.ga = xa; p.ga_ld = H;
-    const long long items = static_cast<long long>(s->max_tiles) * p.n_tiles;
-    const int grid = items < sms ? static_cast<int>(items) : sms;
-    if (!mx) {
-      p.out1 = ctx->h;
-      if (perm)
-        MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 256, EPI_SWIGLU>(m, p, grid, cs)));
-      else if (g4)
-        MOK_CUDA((launch_gemm<SRC_K_GATHER, SRC_K_TILE, 256, EPI_SWIGLU>(m, p, grid, cs)));
-      else
-        MOK_CUDA((launch_gemm<SRC_K_GATHER_LSU, SRC_K_TILE, 256, EPI_SWIGLU>(m, p, grid, cs)));
-    } else {
-      p.out1 = ctx->hq; p.out2 = ctx->hq_sc;
-      if (perm)
-        MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 256, EPI_SWIGLU_MX>(m, p, grid, cs)));
-      else if (g4)
-        MOK_CUDA((launch_gemm<SRC_K_GATHER, SRC_K_TILE, 256, EPI_SWIGLU_MX>(m, p, grid, cs)));
-      else
-        MOK_CUDA((launch_gemm<SRC_K_GATHER_LSU, SRC_K_TILE, 256, EPI_SWIGLU_MX>(m, p, grid, cs)));
-      MOK_CUDA(launch_mx_dequant(ctx->hq, ctx->hq_sc, mr * I / 32, X.h_deq, sms, cs));
-    }
-    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_GATEUP, 1, cs));
-    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DOWN, 0, cs));
-    const uint16_t* hr = mx ? X.h_deq : ctx->h;
-    GemmMaps m2;
-    if ((st = make_map(&m2.a, hr, I, mr, 128, kTileBK)) ||
-        (st = make_map(&m2.b0, wd, I, static_cast<uint64_t>(E) * H, tile_n(H), kTileBK)))
-      return st;
-    m2.b1 = m2.b0;
-    GemmParams q = base_params(s, ctx->status, 0);
-    const int bn = tile_n(H);
-    q.grouped = 1; q.K = I; q.N = H; q.n_tiles = H / bn; q.b_rows_per_expert = H;
-    q.out0 = ctx->slots; q.ld = H; q.rw = router_w;
-    const long long items2 = static_cast<long long>(s->max_tiles) * q.n_tiles;
-    const int grid2 = items2 < sms ? static_cast<int>(items2) : sms;
-    if (bn == 256)
-      MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 256, EPI_SCALE_SCATTER>(m2, q, grid2, cs)));
-    else
-      MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 128, EPI_SCALE_SCATTER>(m2, q, grid2, cs)));
-    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DOWN, 1, cs));
+    st = forward_bf16(cfg, x, router_w, s, w, ctx, mr, sms, g4, cs);
+    if (st) return st;
   }
 
   // ---- combine: y[t] = shared[t] + sum_j slots[t, j] in fixed order
@@ -631,6 +726,7 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
   // permuted dispatch: token rows of x (unquantised, for the weight gradient)
   // in schedule order; the forward's copy serves when it holds exactly that
   const uint16_t* x_rows = nullptr;
+  MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 0, cs));
   if (perm) {
     if (ctx->dispatch == MOK_DISPATCH_PERMUTE && ctx->mode == MOK_MODE_BF16 && ctx->x_perm) {
       x_rows = ctx->x_perm;
@@ -638,10 +734,11 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
       MOK_CUDA(launch_permute_rows(x, H, k, s->row_src, s->header, mr, L.xb_perm, sms, cs));
       x_rows = L.xb_perm;
     }
+    MOK_CUDA(launch_permute_rows(dy, H, k, s->row_src, s->header, mr, L.dy_perm, sms, cs));
   }
+  MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 1, cs));
   {
     MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DOWN, 0, cs));
-    if (perm) MOK_CUDA(launch_permute_rows(dy, H, k, s->row_src, s->header, mr, L.dy_perm, sms, cs));
     GemmMaps m;
     const int bk = perm ? kTileBK : kGatherBK;
     if ((st = perm ? make_map(&m.a, L.dy_perm, H, mr, 128, bk) : make_map(&m.a, dy, H, T, 1, bk)) ||

@@ -49,7 +49,7 @@ enum Src : int {
 
 enum Epi : int {
   EPI_SWIGLU = 0,        // gate|up accumulators -> G, U (bf16), h = silu(G) U (bf16)
-  EPI_SWIGLU_MX = 1,     // same, h written as MXFP8 codes + E8M0 scales
+  EPI_SWIGLU_MX = 1,     // same, h written as MXFP8 codes + E8M0 scales (gemm_mx_kernel)
   EPI_SCALE_SCATTER = 2, // slot[f] = bf16(w[f] * acc) for the tile's routed rows
   EPI_STORE_ROWS = 3,    // out[row] = bf16(acc) for dense rows
   EPI_DOWN_BWD = 4,      // dH = w Z; SwiGLU backward; d_w partial = sum Z h; hw = w h
@@ -102,6 +102,11 @@ struct GemmParams {
   long long ga_ld;
   const uint16_t* gb;
   long long gb_ld;
+  // ---- MXFP8 operands: E8M0 scales in the tensor-core layout (mx_tiled_scale_offset)
+  const uint8_t* sfa;
+  const uint8_t* sfb0;
+  const uint8_t* sfb1;
+  uint8_t* sf_out;   // EPI_SWIGLU_MX: scales of h, same layout
 };
 
 struct Item {
@@ -278,6 +283,19 @@ __device__ __forceinline__ uint32_t mx_quantize32(const float* v, uint8_t* codes
   return static_cast<uint32_t>(s + 127);
 }
 
+// Byte offset of the E8M0 scale of element block (row, cblk) (cblk = column /
+// 32) in the tensor-core scale layout of a tensor with `cgroups` = K/128
+// column groups: one 512-byte atom per (128-row block, 128-column group),
+// holding row r's four block scales of the group as one 32-bit word at byte
+// (r % 32) * 16 + (r / 32) * 4 - the form a 32x128b.warpx4 copy puts into
+// four TMEM columns, where the block-scaled MMA reads row r's scale at column
+// r / 32, byte cblk % 4.
+__host__ __device__ __forceinline__ long long mx_tiled_scale_offset(long long row, int cblk, int cgroups) {
+  const long long atom = (row >> 7) * cgroups + (cblk >> 2);
+  const int r = static_cast<int>(row & 127);
+  return atom * 512 + (r & 31) * 16 + (r >> 5) * 4 + (cblk & 3);
+}
+
 template <int A_SRC, int B_SRC, int BN, int EPI>
 struct GemmCfg {
   static constexpr bool kAMN = (A_SRC == SRC_MN_TILE || A_SRC == SRC_MN_GATHER || A_SRC == SRC_MN_GATHER_LSU);
@@ -313,6 +331,7 @@ struct GemmCfg {
   static constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, kAMN, kBMN);
   static_assert(BN == 128 || BN == 256, "tile N");
   static_assert(!(kALsu && kBLsu), "one gathered operand per GEMM");
+  static_assert(EPI != EPI_SWIGLU_MX, "the MXFP8 SwiGLU epilogue runs in gemm_mx_kernel");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
@@ -731,15 +750,13 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
                           (static_cast<uint32_t>(q * 32) << 16);
       uint32_t wv[16];
 
-      if constexpr (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_MX) {
-        // out0 = gu [rows][2N], out1 = h [rows][N] (bf16) or codes, out2 = scales
+      if constexpr (EPI == EPI_SWIGLU) {
+        // out0 = gu [rows][2N], out1 = h [rows][N] (bf16)
         const int prow = it.p0 + r;
         const bool valid = r < it.rows;
         const bool inb = p.grouped ? true : valid;
         uint16_t* gu = inb ? static_cast<uint16_t*>(p.out0) + static_cast<long long>(prow) * 2 * p.N + n0 : nullptr;
-        uint16_t* hb = (EPI == EPI_SWIGLU && inb)
-                           ? static_cast<uint16_t*>(p.out1) + static_cast<long long>(prow) * p.N + n0
-                           : nullptr;
+        uint16_t* hb = inb ? static_cast<uint16_t*>(p.out1) + static_cast<long long>(prow) * p.N + n0 : nullptr;
 #pragma unroll 1
         for (int c = 0; c < BN / 64; ++c) {
           float g[32], u[32];
@@ -759,16 +776,8 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
           warp_store_row64(wv, gu ? gu + c * 32 : nullptr, wstage, lane);
           pack_bf16x32(u, wv);
           warp_store_row64(wv, gu ? gu + p.N + c * 32 : nullptr, wstage, lane);
-          if constexpr (EPI == EPI_SWIGLU) {
-            pack_bf16x32(hv, wv);
-            warp_store_row64(wv, hb ? hb + c * 32 : nullptr, wstage, lane);
-          } else if (inb) {
-            const int col = n0 + c * 32;
-            uint8_t* codes = static_cast<uint8_t*>(p.out1) + static_cast<long long>(prow) * p.N + col;
-            const uint32_t sc = mx_quantize32(hv, codes);
-            static_cast<uint8_t*>(p.out2)[static_cast<long long>(prow) * (p.N / 32) + col / 32] =
-                static_cast<uint8_t>(sc);
-          }
+          pack_bf16x32(hv, wv);
+          warp_store_row64(wv, hb ? hb + c * 32 : nullptr, wstage, lane);
         }
       } else if constexpr (EPI == EPI_SCALE_SCATTER || EPI == EPI_SCATTER) {
         const int f = (r < it.rows) ? __ldg(p.row_src + it.p0 + r) : -1;

@@ -1,0 +1,334 @@
+// Persistent grouped GEMM on the block-scaled tensor-core path
+// (tcgen05.mma kind::mxf8f6f4, E4M3 operands with E8M0 scales per 32 K-elements)
+// for the MXFP8 forward.
+//
+// One CTA per SM, 320 threads:
+//   warp 0      TMA producer: operand tiles (128-byte rows of E4M3 codes) and
+//               the matching 512-byte scale atoms (1-D bulk copies);
+//   warp 1      MMA issuer (one thread) and TMEM owner: per stage it copies the
+//               scale atoms into TMEM (tcgen05.cp) and issues four K=32 MMAs;
+//   warps 2..9  epilogue, two warps per TMEM lane quarter, each half the
+//               columns.
+// The accumulator (BN fp32 columns) is single-buffered: the scale ring takes
+// the rest of TMEM.  The epilogue reads its whole share of the accumulator
+// into registers first and releases TMEM at once, so the next tile's MMAs
+// overlap the epilogue's arithmetic and stores.
+//
+// Follows "Mixture-of-Kittens: a deterministic MoE megakernel for NVL72 racks"
+// (MXFP8 forward; experts as fused SwiGLU grouped GEMMs) with MXFP8 as the OCP
+// Microscaling v1.0 format: E4M3 elements, one E8M0 power-of-two scale per
+// block of 32 along K.
+#pragma once
+
+#include "gemm.cuh"
+
+namespace mok {
+
+template <int BN, int EPI>
+struct MxCfg {
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr int kBK = 128;                      // E4M3 elements (= bytes) per stage: one swizzled row
+  static constexpr int kABytes = kBM * kBK;
+  static constexpr int kBBytes = BN * kBK;
+  static constexpr int kSfaBytes = 512;                // one scale atom: 128 rows x 4 blocks
+  static constexpr int kSfbBytes = (BN / 128) * 512;
+  static constexpr int kSfStride = 2048;               // per stage: A atom at 0, B atoms at 512, 1024
+  static constexpr int kTmaBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kBarBytes = 512;
+  static constexpr int kEpiStageBytes = 2048;
+  static constexpr int kStagesFit =
+      (227 * 1024 - 1024 - kBarBytes - kEpiWarps * kEpiStageBytes) / (kStageBytes + kSfStride);
+  static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+  // TMEM: accumulator columns [0, BN), then one 16-column scale slot per stage
+  // (A: 4 columns at +0, B: 4 columns per 128 rows at +8)
+  static constexpr int kSfCol0 = BN;
+  static constexpr int kTmemCols = 512;
+  static constexpr int kSmemBytes =
+      1024 + kStages * (kStageBytes + kSfStride) + kBarBytes + kEpiWarps * kEpiStageBytes;
+  static_assert(BN == 128 || BN == 256, "tile N");
+  // SwiGLU tiles pair 128 gate rows with 128 up rows: whole scale atoms
+  static_assert(EPI != EPI_SWIGLU_MX || BN == 256, "SwiGLU tile");
+  static_assert(kSfCol0 + 16 * kStages <= kTmemCols, "TMEM scale ring");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+};
+
+// Shared-memory descriptor of a 512-byte scale atom as the tcgen05.cp source:
+// 32 rows of 16 bytes, no swizzle, 8-row groups 128 bytes apart.
+__device__ __forceinline__ uint64_t sf_atom_desc(uint32_t saddr) { return smem_desc(saddr, 128, 128, 0); }
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(MxCfg<BN, EPI>::kThreads, 1)
+    gemm_mx_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
+  using C = MxCfg<BN, EPI>;
+  static_assert(EPI == EPI_SWIGLU_MX || EPI == EPI_SCALE_SCATTER || EPI == EPI_STORE_ROWS, "epilogue");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sf_smem = smem + C::kStages * C::kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sf_smem + C::kStages * C::kSfStride);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::kStages;
+  uint64_t* tfull = bars + 2 * C::kStages;
+  uint64_t* tempty = tfull + 1;
+  uint64_t* done = tempty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int kgroups = p.K / C::kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, C::kEpiWarps);
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&maps.a);
+    tma_prefetch_desc(&maps.b0);
+    tma_prefetch_desc(&maps.b1);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int nitems = num_items(p);
+  constexpr bool kSwiGLU = (EPI == EPI_SWIGLU_MX);
+  constexpr int kBnOut = kSwiGLU ? BN / 2 : BN;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long long fills = 0;
+      bool ok = true;
+      for (int idx = blockIdx.x; idx < nitems && ok; idx += gridDim.x) {
+        const Item it = get_item(p, idx, C::kBK);
+        const int n0 = it.nt * kBnOut;
+        const long long brow = static_cast<long long>(it.e) * p.b_rows_per_expert + n0;
+        const uint8_t* sfa = p.sfa + ((it.p0 >> 7) * static_cast<long long>(kgroups)) * 512;
+        const uint8_t* sfb0 = p.sfb0 + ((brow >> 7) * static_cast<long long>(kgroups)) * 512;
+        const uint8_t* sfb1 = kSwiGLU ? p.sfb1 + ((brow >> 7) * static_cast<long long>(kgroups)) * 512
+                                      : sfb0 + static_cast<long long>(kgroups) * 512;  // next 128 rows
+        for (int kb = 0; kb < it.nk; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], C::kTmaBytes);
+          uint8_t* sA = smem + stage * C::kStageBytes;
+          uint8_t* sB = sA + C::kABytes;
+          uint8_t* sS = sf_smem + stage * C::kSfStride;
+          const int k0 = kb * C::kBK;
+          tma_load_2d(sA, &maps.a, &full[stage], k0, it.p0);
+          if (kSwiGLU) {
+            tma_load_2d(sB, &maps.b0, &full[stage], k0, static_cast<int>(brow));
+            tma_load_2d(sB + (BN / 2) * C::kBK, &maps.b1, &full[stage], k0, static_cast<int>(brow));
+          } else {
+            tma_load_2d(sB, &maps.b0, &full[stage], k0, static_cast<int>(brow));
+          }
+          bulk_load(sS, sfa + kb * 512, 512, &full[stage]);
+          bulk_load(sS + 512, sfb0 + kb * 512, 512, &full[stage]);
+          if (BN == 256) bulk_load(sS + 1024, sfb1 + kb * 512, 512, &full[stage]);
+          ++fills;
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        // drain: wait until every load issued into a stage has landed
+        const long long n = fills < C::kStages ? fills : C::kStages;
+        int s = stage;
+        uint32_t ph = phase;
+        for (long long i = 0; i < n; ++i) {
+          if (--s < 0) {
+            s = C::kStages - 1;
+            ph ^= 1;
+          }
+          mbar_drain(&full[s], ph);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t aphase = 0;
+      bool first = true;
+      for (int idx = blockIdx.x; idx < nitems; idx += gridDim.x) {
+        const Item it = get_item(p, idx, C::kBK);
+        if (it.nk == 0) continue;
+        if (!mbar_wait(tempty, aphase ^ 1, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t acc = tmem_base;
+        bool ok = true;
+        for (int kb = 0; kb < it.nk; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + stage * C::kStageBytes);
+          const uint32_t b0 = a0 + C::kABytes;
+          const uint32_t s0 = smem_u32(sf_smem + stage * C::kSfStride);
+          const uint32_t sfa_t = tmem_base + C::kSfCol0 + stage * 16;
+          const uint32_t sfb_t = sfa_t + 8;
+          // scale atoms -> TMEM (executed in order with the MMAs below)
+          tmem_cp_32x128b_warpx4(sfa_t, sf_atom_desc(s0));
+          tmem_cp_32x128b_warpx4(sfb_t, sf_atom_desc(s0 + 512));
+          if (BN == 256) tmem_cp_32x128b_warpx4(sfb_t + 4, sf_atom_desc(s0 + 1024));
+#pragma unroll
+          for (int kk = 0; kk < C::kBK / 32; ++kk) {
+            // K-major 128-byte swizzled rows: 32 E4M3 elements = 32 bytes per step
+            const uint64_t ad = smem_desc(a0 + kk * 32, 16, 8 * C::kBK, 2);
+            const uint64_t bd = smem_desc(b0 + kk * 32, 16, 8 * C::kBK, 2);
+            umma_mxf8(acc, ad, bd, idesc_mxf8(kBM, BN, kk, kk), sfa_t, sfb_t, (kb | kk) ? 1u : 0u);
+          }
+          umma_commit(&empty[stage]);
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        const bool drop = (p.debug & 1) && first && blockIdx.x == 0;
+        if (!drop) umma_commit(tfull);
+        first = false;
+        aphase ^= 1;
+      }
+      // every MMA issued by this thread must finish before TMEM is released
+      umma_commit(done);
+      mbar_drain(done, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;      // which half of the columns
+    const int r = q * 32 + lane;           // tile row of this thread
+    uint8_t* wstage = sf_smem + C::kStages * C::kSfStride + C::kBarBytes + (warp - 2) * C::kEpiStageBytes;
+    uint32_t aphase = 0;
+    constexpr int kCols = BN / 2;          // accumulator columns per thread
+    for (int idx = blockIdx.x; idx < nitems; idx += gridDim.x) {
+      const Item it = get_item(p, idx, C::kBK);
+      if (it.nk == 0) continue;
+      const int n0 = it.nt * kBnOut;
+      const int prow = it.p0 + r;
+      const bool valid = r < it.rows;
+      int f = -1;
+      float wt = 1.f;
+      if (EPI == EPI_SCALE_SCATTER && valid) {
+        f = __ldg(p.row_src + prow);
+        if (f >= 0) wt = __ldg(p.rw + f);
+      }
+      int w = (lane == 0) ? (mbar_wait(tfull, aphase, abort_flag, p.status) ? 1 : 0) : 0;
+      w = __shfl_sync(0xffffffffu, w, 0);
+      if (!w) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+      // this thread's share of the accumulator, then TMEM goes back to the MMA
+      float v[kCols];
+      if (kSwiGLU) {   // gate columns [half*BN/4, +BN/4), up columns BN/2 later
+#pragma unroll
+        for (int c = 0; c < kCols / 64; ++c) {
+          tmem_ld32(tb + half * (BN / 4) + c * 32, v + c * 32);
+          tmem_ld32(tb + BN / 2 + half * (BN / 4) + c * 32, v + kCols / 2 + c * 32);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < kCols / 32; ++c) tmem_ld32(tb + half * kCols + c * 32, v + c * 32);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty);
+      aphase ^= 1;
+
+      uint32_t wv[16];
+      if constexpr (EPI == EPI_SWIGLU_MX) {
+        // out0 = gu [rows][2N] (bf16), out1 = h codes [rows][N], sf_out = h scales
+        constexpr int kH = kCols / 2;        // h columns of this thread
+        const bool inb = p.grouped ? true : valid;
+        const int col0 = n0 + half * kH;
+        float* g = v;
+        float* u = v + kH;
+        if (!valid) {
+#pragma unroll
+          for (int i = 0; i < kCols; ++i) v[i] = 0.f;
+        }
+        uint16_t* gu = inb ? static_cast<uint16_t*>(p.out0) + static_cast<long long>(prow) * 2 * p.N + col0 : nullptr;
+#pragma unroll
+        for (int c = 0; c < kH / 32; ++c) {
+          pack_bf16x32(g + c * 32, wv);
+          warp_store_row64(wv, gu ? gu + c * 32 : nullptr, wstage, lane);
+          pack_bf16x32(u + c * 32, wv);
+          warp_store_row64(wv, gu ? gu + p.N + c * 32 : nullptr, wstage, lane);
+        }
+        uint32_t sc = 0;
+#pragma unroll
+        for (int c = 0; c < kH / 32; ++c) {
+          float* hv = g + c * 32;        // h overwrites the gate values (already stored)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float x = hv[i];
+            const float sg = __fdividef(1.f, 1.f + __expf(-x));
+            hv[i] = x * sg * u[c * 32 + i];
+          }
+          uint8_t codes[32];
+          const uint32_t s8 = mx_quantize32(hv, codes);
+          sc |= s8 << (8 * c);
+          if (inb) {
+            uint4* d = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out1) + static_cast<long long>(prow) * p.N +
+                                                col0 + c * 32);
+            d[0] = reinterpret_cast<const uint4*>(codes)[0];
+            d[1] = reinterpret_cast<const uint4*>(codes)[1];
+          }
+        }
+        // the scales of this thread's blocks are adjacent bytes of its row's word
+        uint8_t* sdst = p.sf_out + mx_tiled_scale_offset(prow, col0 / 32, p.N / 128);
+        if (kH == 64) {
+          *reinterpret_cast<uint16_t*>(sdst) = static_cast<uint16_t>(sc);
+        } else {
+          *sdst = static_cast<uint8_t>(sc);
+        }
+      } else {
+        uint16_t* dst = nullptr;
+        if (EPI == EPI_SCALE_SCATTER) {
+          if (f >= 0) dst = static_cast<uint16_t*>(p.out0) + static_cast<long long>(f) * p.ld + n0 + half * kCols;
+        } else if (valid) {
+          dst = static_cast<uint16_t*>(p.out0) + static_cast<long long>(prow) * p.ld + n0 + half * kCols;
+        }
+#pragma unroll
+        for (int c = 0; c < kCols / 32; ++c) {
+          if (EPI == EPI_SCALE_SCATTER) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[c * 32 + i] *= wt;
+          }
+          pack_bf16x32(v + c * 32, wv);
+          warp_store_row64(wv, dst ? dst + c * 32 : nullptr, wstage, lane);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+}  // namespace mok

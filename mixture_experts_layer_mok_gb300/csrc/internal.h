@@ -19,8 +19,10 @@ cudaError_t launch_schedule(const int64_t* te, int T, int k, int E, int cap_tile
                             cudaStream_t st);
 cudaError_t launch_mx_quantize(const uint16_t* x, long long nblocks, uint8_t* codes, uint8_t* scales,
                                int num_sms, cudaStream_t st);
-cudaError_t launch_mx_dequant(const uint8_t* codes, const uint8_t* scales, long long nblocks,
-                              uint16_t* out, int num_sms, cudaStream_t st);
+cudaError_t launch_mx_dispatch(const uint16_t* x, int T, int H, int topk, const int* slot_row, const int* row_src,
+                               const int* header, long long max_rows, uint8_t* xq, uint8_t* xq_sc, uint8_t* xp,
+                               uint8_t* xp_sc, int num_sms, cudaStream_t st);
+cudaError_t launch_mx_tile_scales(const uint8_t* src, long long rows, int K, uint8_t* dst, cudaStream_t st);
 cudaError_t launch_combine(const uint16_t* slots, const uint16_t* base, int T, int k, int H,
                            uint16_t* out, int num_sms, cudaStream_t st);
 cudaError_t launch_permute_rows(const uint16_t* src, int H, int topk, const int* row_src, const int* header,
@@ -31,5 +33,9 @@ cudaError_t launch_dw_reduce(const float* part, int nf, int ntiles, float* dw, c
 // epilogues the layer uses (gemm_fwd.cu, gemm_bwd.cu).
 template <int A_SRC, int B_SRC, int BN, int EPI>
 cudaError_t launch_gemm(const GemmMaps& maps, const GemmParams& p, int grid, cudaStream_t st);
+
+// Block-scaled (MXFP8) grouped GEMM launch (gemm_mx.cu).
+template <int BN, int EPI>
+cudaError_t launch_gemm_mx(const GemmMaps& maps, const GemmParams& p, int grid, cudaStream_t st);
 
 }  // namespace mok

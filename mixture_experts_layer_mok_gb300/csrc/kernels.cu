@@ -212,34 +212,6 @@ __global__ void __launch_bounds__(256) mx_quantize_kernel(const uint16_t* __rest
   }
 }
 
-// Exact expansion of MXFP8 (codes, scales) to bf16: an E4M3 value times a
-// power of two keeps at most 4 significant bits.
-__global__ void __launch_bounds__(256) mx_dequant_kernel(const uint8_t* __restrict__ codes,
-                                                         const uint8_t* __restrict__ scales,
-                                                         long long nblocks, uint16_t* __restrict__ out) {
-  for (long long b = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; b < nblocks;
-       b += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int s = static_cast<int>(scales[b]) - 127;
-    float v[32];
-    const uint4* src = reinterpret_cast<const uint4*>(codes + b * 32);
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const uint4 w = src[q];
-      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const __nv_fp8_storage_t c = static_cast<__nv_fp8_storage_t>((ws[i] >> (8 * j)) & 0xFF);
-          const __half_raw hr = __nv_cvt_fp8_to_halfraw(c, __NV_E4M3);
-          v[16 * q + 4 * i + j] = ldexpf(__half2float(__half(hr)), s);
-        }
-      }
-    }
-    store_bf16x32(out + b * 32, v);
-  }
-}
-
 static int grid_for(long long work, int per_block, int num_sms) {
   long long g = (work + per_block - 1) / per_block;
   const long long cap = static_cast<long long>(num_sms) * 16;
@@ -255,10 +227,119 @@ cudaError_t launch_mx_quantize(const uint16_t* x, long long nblocks, uint8_t* co
   return cudaGetLastError();
 }
 
-cudaError_t launch_mx_dequant(const uint8_t* codes, const uint8_t* scales, long long nblocks,
-                              uint16_t* out, int num_sms, cudaStream_t st) {
-  if (nblocks == 0) return cudaSuccess;
-  mx_dequant_kernel<<<grid_for(nblocks, 256, num_sms), 256, 0, st>>>(codes, scales, nblocks, out);
+// ===========================================================================
+// MXFP8 dispatch: every token row of x is quantised once (E4M3 codes + E8M0
+// scales, OCP MX v1.0 blocks of 32) and written to its own row of the
+// token-order copy (the shared expert's operand) and to the k schedule rows
+// that route it (the routed experts' operand: MoK's dispatch exchange, done on
+// one GPU as a write into schedule order).  Scales go straight into the
+// tensor-core scale layout.  Padding rows of the schedule get zero codes and
+// unit scales; so do the scales of the token-order copy's last partial
+// 128-row block.  One warp per job: tokens, then schedule rows, then the tail.
+// ===========================================================================
+__global__ void __launch_bounds__(256) mx_dispatch_kernel(
+    const uint16_t* __restrict__ x, int T, int H, int topk, const int* __restrict__ slot_row,
+    const int* __restrict__ row_src, const int* __restrict__ header, long long max_rows, uint8_t* __restrict__ xq,
+    uint8_t* __restrict__ xq_sc, uint8_t* __restrict__ xp, uint8_t* __restrict__ xp_sc) {
+  if (header[2] != 0) return;
+  const long long P = header[1];
+  const int lane = threadIdx.x & 31;
+  const int nb = H / 32;             // blocks per row (a multiple of 4)
+  const int cg = H / 128;            // column groups of the scale layout
+  const long long t_pad = (static_cast<long long>(T) + 127) / 128 * 128;
+  const long long jobs = T + max_rows + (t_pad - T);
+  for (long long j = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5; j < jobs;
+       j += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
+    if (j < T) {
+      const long long t = j;
+      // schedule rows of this token's k copies, spread over the lanes
+      const int p_lo = lane < topk ? __ldg(slot_row + t * topk + lane) : -1;
+      const int p_hi = lane + 32 < topk ? __ldg(slot_row + t * topk + lane + 32) : -1;
+      for (int b0 = 0; b0 < nb; b0 += 32) {
+        const int b = b0 + lane;
+        const bool act = b < nb;       // whole aligned groups of 4 lanes share this
+        float v[32];
+        uint8_t codes[32];
+        uint32_t sc = 127;
+        if (act) {
+          load_bf16x32(x + t * H + static_cast<long long>(b) * 32, v);
+          sc = mx_quantize32(v, codes);
+        }
+        // the 4 scales of an aligned group of blocks form one 32-bit word
+        const uint32_t s1 = __shfl_down_sync(0xffffffffu, sc, 1);
+        const uint32_t s2 = __shfl_down_sync(0xffffffffu, sc, 2);
+        const uint32_t s3 = __shfl_down_sync(0xffffffffu, sc, 3);
+        const uint32_t word = sc | (s1 << 8) | (s2 << 16) | (s3 << 24);
+        uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0;
+        if (act) {
+          c0 = reinterpret_cast<const uint4*>(codes)[0];
+          c1 = reinterpret_cast<const uint4*>(codes)[1];
+          uint4* d = reinterpret_cast<uint4*>(xq + t * H + static_cast<long long>(b) * 32);
+          d[0] = c0;
+          d[1] = c1;
+          if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(xq_sc + mx_tiled_scale_offset(t, b, cg)) = word;
+        }
+        for (int jj = 0; jj < topk; ++jj) {   // all lanes take part in the shuffle
+          const int pr = __shfl_sync(0xffffffffu, jj < 32 ? p_lo : p_hi, jj & 31);
+          if (!act) continue;
+          uint4* dp = reinterpret_cast<uint4*>(xp + static_cast<long long>(pr) * H + static_cast<long long>(b) * 32);
+          dp[0] = c0;
+          dp[1] = c1;
+          if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(xp_sc + mx_tiled_scale_offset(pr, b, cg)) = word;
+        }
+      }
+    } else if (j < T + max_rows) {
+      const long long pr = j - T;
+      if (pr >= P || __ldg(row_src + pr) >= 0) continue;
+      uint4* d = reinterpret_cast<uint4*>(xp + pr * H);
+      for (int i = lane; i < H / 16; i += 32) d[i] = make_uint4(0, 0, 0, 0);
+      for (int g = lane; g < cg; g += 32)
+        *reinterpret_cast<uint32_t*>(xp_sc + mx_tiled_scale_offset(pr, 4 * g, cg)) = 0x7F7F7F7Fu;
+    } else {
+      const long long tr = T + (j - T - max_rows);
+      for (int g = lane; g < cg; g += 32)
+        *reinterpret_cast<uint32_t*>(xq_sc + mx_tiled_scale_offset(tr, 4 * g, cg)) = 0x7F7F7F7Fu;
+    }
+  }
+}
+
+cudaError_t launch_mx_dispatch(const uint16_t* x, int T, int H, int topk, const int* slot_row, const int* row_src,
+                               const int* header, long long max_rows, uint8_t* xq, uint8_t* xq_sc, uint8_t* xp,
+                               uint8_t* xp_sc, int num_sms, cudaStream_t st) {
+  const long long jobs = T + max_rows + ((static_cast<long long>(T) + 127) / 128 * 128 - T);
+  mx_dispatch_kernel<<<grid_for(jobs * 32, 256, num_sms), 256, 0, st>>>(x, T, H, topk, slot_row, row_src, header,
+                                                                        max_rows, xq, xq_sc, xp, xp_sc);
+  return cudaGetLastError();
+}
+
+// Row-major E8M0 scales [rows][K/32] -> the tensor-core scale layout.  One
+// block per (128-row block, 16 column groups): coalesced row reads into shared
+// memory, coalesced atom writes out of it.
+__global__ void __launch_bounds__(256) mx_tile_scales_kernel(const uint8_t* __restrict__ src, int K,
+                                                             uint8_t* __restrict__ dst) {
+  __shared__ uint32_t tile[128][17];
+  const int cg = K / 128;
+  const long long rb = blockIdx.x;
+  const int g0 = blockIdx.y * 16;
+  const int ng = min(16, cg - g0);
+  const uint32_t* s = reinterpret_cast<const uint32_t*>(src);  // one word = one column group of a row
+  for (int i = threadIdx.x; i < 128 * 16; i += 256) {
+    const int row = i >> 4, g = i & 15;
+    if (g < ng) tile[row][g] = __ldg(s + (rb * 128 + row) * cg + g0 + g);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < 128 * 16; i += 256) {
+    const int g = i >> 7, w = i & 127;       // atom g, word w = (row % 32) * 4 + row / 32
+    if (g >= ng) continue;
+    const int row = (w >> 2) + 32 * (w & 3);
+    reinterpret_cast<uint32_t*>(dst + ((rb * cg) + g0 + g) * 512)[w] = tile[row][g];
+  }
+}
+
+cudaError_t launch_mx_tile_scales(const uint8_t* src, long long rows, int K, uint8_t* dst, cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>(rows / 128), static_cast<unsigned>((K / 128 + 15) / 16));
+  mx_tile_scales_kernel<<<grid, 256, 0, st>>>(src, K, dst);
   return cudaGetLastError();
 }
 

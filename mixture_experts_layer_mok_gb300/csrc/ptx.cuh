@@ -104,6 +104,16 @@ __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// 1-D bulk copy global -> shared (both addresses and the size 16-byte aligned),
+// completing `bytes` of the barrier's transaction count.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // ---------------------------------------------------------------- cp.async
 // 16-byte global -> shared copy through L2 (generic proxy); src_bytes = 0
 // writes zeros.
@@ -159,6 +169,27 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// D[tmem] (+)= (A * 2^sA)[smem] * ((B * 2^sB)[smem])^T, E4M3 inputs with one
+// E8M0 scale per 32 K-elements and row (scale_vec::1X), fp32 accumulate.  The
+// scales are read from TMEM columns sfa / sfb; the instruction descriptor
+// selects which byte of each 32-bit scale word applies.
+__device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Shared -> TMEM copy of 32 rows x 16 bytes, replicated into all four 32-lane
+// quarters (columns taddr .. taddr+3 of every lane).
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // Arrive once on `bar` when every tcgen05 op issued so far by this thread is done.
@@ -228,6 +259,17 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
          | ((b_mn_major ? 1u : 0u) << 16)            // B major-ness
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
+// Instruction descriptor for kind::mxf8f6f4 with E4M3 A/B (K-major), E8M0
+// scales, fp32 D; sf_a / sf_b pick the byte of the scale word (0..3).
+__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, int sf_a, int sf_b) {
+  return (static_cast<uint32_t>(sf_b & 3) << 4)    // B scale byte
+         | (0u << 7) | (0u << 10)                  // A, B format: E4M3
+         | (static_cast<uint32_t>(N >> 3) << 17)   // N / 8
+         | (1u << 23)                              // scale format: E8M0
+         | (static_cast<uint32_t>(M >> 4) << 24)   // M / 16
+         | (static_cast<uint32_t>(sf_a & 3) << 29);  // A scale byte
 }
 
 }  // namespace mok

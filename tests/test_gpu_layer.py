@@ -40,7 +40,7 @@ def test_bf16_forward_backward_matches_oracle(name):
     assert not bad, errs
 
 
-@pytest.mark.parametrize("name", ["tiny", "ragged_shared", "wide"])
+@pytest.mark.parametrize("name", list(SHAPES))
 def test_mxfp8_forward_matches_same_quantisation_oracle(name):
     inp = _inputs(name, seed=1)
     y, grads, sched, ctx = run_layer(inp, "mxfp8")
@@ -225,3 +225,57 @@ def test_fused_forward_permuted_backward_mix():
     y_ref, g_ref = oracle_fwd_bwd(inp, "bf16")
     errs, bad = compare_all(y, grads, y_ref, g_ref, BF16_TOL)
     assert not bad, errs
+
+
+def _ctx_bytes(ctx, field, nbytes):
+    """nbytes of the context buffer at the device pointer ctx.c.<field>."""
+    off = getattr(ctx.c, field) - ctx.buf.data_ptr()
+    assert 0 <= off and off + nbytes <= ctx.buf.numel()
+    return ctx.buf[off:off + nbytes].cpu().numpy()
+
+
+def _untile_scales(tiled, rows, K):
+    """Row-major [rows][K/32] scales from the tensor-core scale layout (512-byte
+    atoms per 128-row block and 128-column group; row r's four block scales of
+    a group are one 32-bit word at byte (r % 32) * 16 + (r / 32) * 4)."""
+    cg = K // 128
+    out = np.empty((rows, K // 32), np.uint8)
+    for row in range(rows):
+        r = row % 128
+        for b in range(K // 32):
+            atom = (row // 128) * cg + b // 4
+            out[row, b] = tiled[atom * 512 + (r % 32) * 16 + (r // 32) * 4 + b % 4]
+    return out
+
+
+@pytest.mark.parametrize("name", ["ragged_shared", "skewed"])
+def test_mxfp8_dispatch_codes_and_scales_bit_exact(name):
+    """The MXFP8 forward's quantise-and-dispatch step: x's E4M3 codes and E8M0
+    scales in token order and in schedule order equal the oracle's quantiser,
+    row for row; padding rows hold zero codes and unit scales."""
+    m = mok()
+    inp = _inputs(name, seed=3)
+    T, H, k = inp.meta["T"], inp.meta["H"], inp.meta["k"]
+    g = inp.to("cuda")
+    sched = m.schedule(g.top_experts, inp.meta["E"], 0.5)
+    w = weights_of(g, "mxfp8")
+    _, ctx = m.forward(g.x, g.router_w, sched, w, mode="mxfp8")
+    torch.cuda.synchronize()
+    assert ctx.status() == 0
+    codes, scales = oracle.mxfp8_quantize(inp.x.float().numpy())
+    t_pad = (T + 127) // 128 * 128
+    xq = _ctx_bytes(ctx, "xq", T * H).reshape(T, H)
+    assert np.array_equal(xq, codes)
+    xs = _untile_scales(_ctx_bytes(ctx, "xq_sc", t_pad * H // 32), t_pad, H)
+    assert np.array_equal(xs[:T], scales)
+    assert np.all(xs[T:] == 127)
+    st, _, P = sched.status()
+    assert st == 0
+    row_src = sched.arrays()["row_src"][:P].cpu().numpy()
+    xp = _ctx_bytes(ctx, "xq_perm", P * H).reshape(P, H)
+    xps = _untile_scales(_ctx_bytes(ctx, "xq_perm_sc", (P + 127) // 128 * 128 * H // 32), P, H)
+    tok = np.where(row_src >= 0, row_src // k, 0)
+    valid = row_src >= 0
+    assert np.array_equal(xp[valid], codes[tok[valid]])
+    assert np.array_equal(xps[valid], scales[tok[valid]])
+    assert np.all(xp[~valid] == 0) and np.all(xps[~valid] == 127)
