@@ -94,7 +94,7 @@ def load_peaks():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for name in ("gemm.cuh", "ptx.cuh"):
+    for name in ("gemm.cuh", "gemm_mx.cuh", "ptx.cuh"):
         with open(os.path.join(ROOT, "mixture_experts_layer_mok_gb300", "csrc", name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
