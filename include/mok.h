@@ -75,6 +75,9 @@ typedef int mok_status_t;
                                         tile::gather4 loads instead of the
                                         gather warps' cp.async copies (same
                                         results, slower; kept for comparison) */
+#define MOK_DEBUG_NO_CTA_PAIR     4  /* run every GEMM on single CTAs instead of
+                                        CTA pairs (M = 256 over two SMs sharing
+                                        B; same results; for comparison) */
 
 /* Stages of the layer, for optional per-stage timing events. */
 #define MOK_STAGE_FWD_PREP                 0  /* status hand-over; MXFP8: weight scales into the tensor-core layout */
@@ -140,8 +143,11 @@ typedef struct {
   int32_t* tile_expert;   /* [max_tiles] expert of each 128-row tile, or -1 */
   int32_t* tile_row0;     /* [max_tiles] first schedule row of the tile, or -1 */
   int32_t* tile_rows;     /* [max_tiles] valid rows in the tile (1..128), or -1 */
-  int32_t* header;        /* [8] num_tiles, P, status, num_primary, 0... */
+  int32_t* header;        /* [8] num_tiles, P, status, num_primary, num_pairs, 0... */
   int32_t* scratch;       /* internal: per-chunk histograms */
+  int32_t* pair_tile;     /* [max_tiles][2] tile pairs for CTA-pair GEMMs: two consecutive
+                             tiles of one expert (within the primary list, then within the
+                             overflow list), second -1 for an odd tile; unused pairs -1 */
 } mok_schedule_t;
 
 /* Layer weights, [MoKDoc] _MoKRuntime.forward layouts.  The shared expert is
@@ -241,7 +247,7 @@ mok_status_t mok_schedule_status(const mok_schedule_t* sched, int* status,
  * itself holds in device memory, so `buf` holds only the output arrays
  * (mok_schedule_bytes(T, k, E) always suffices; the exact need is checked).
  * The pages have no counterpart to this call.
- *   - Limit: ceil(T*k / 4096) * E must not exceed 262144 (a 1 MiB array);
+ *   - Limit: ceil(T*k / 1024) * E must not exceed 1048576 (a 4 MiB array);
  *     larger problems return MOK_ERR_INVALID_ARG with a message.  The array
  *     is held by every GPU that loads the library, until the process exits.
  *   - The first call on a device looks up the array's device address (with

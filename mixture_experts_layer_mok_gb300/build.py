@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 ROOT = os.path.dirname(PKG)
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmok.so")
-SOURCES = ["api.cu", "kernels.cu", "gemm_fwd.cu", "gemm_mx.cu", "gemm_bwd_a.cu", "gemm_bwd_b.cu"]
+SOURCES = ["api.cu", "kernels.cu", "gemm_fwd.cu", "gemm_mx.cu", "gemm_pair.cu", "gemm_bwd_a.cu", "gemm_bwd_b.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
 

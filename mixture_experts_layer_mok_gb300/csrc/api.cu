@@ -171,7 +171,7 @@ long long max_tiles_of(int T, int k, int E) {
 }
 
 struct SchedLayout {
-  int32_t *cnt, *row0, *row_src, *slot_row, *tile_expert, *tile_row0, *tile_rows, *header, *hist;
+  int32_t *cnt, *row0, *row_src, *slot_row, *tile_expert, *tile_row0, *tile_rows, *header, *hist, *pair_tile;
 };
 
 size_t carve_schedule(void* buf, int T, int k, int E, SchedLayout* L) {
@@ -187,6 +187,7 @@ size_t carve_schedule(void* buf, int T, int k, int E, SchedLayout* L) {
   L->tile_row0 = c.take<int32_t>(mt);
   L->tile_rows = c.take<int32_t>(mt);
   L->header = c.take<int32_t>(8);
+  L->pair_tile = c.take<int32_t>(2 * mt);
   L->hist = c.take<int32_t>(nchunks * E);
   return c.off + 256;
 }
@@ -250,6 +251,24 @@ struct BwdLayout {
 
 int tile_n(int N) { return (N % 256 == 0) ? 256 : 128; }
 
+// CTA pairs (M = 256 over two SMs sharing each B tile) for the 256-wide
+// TMA-fed GEMMs, unless the caller turns them off.
+bool pair_on(const mok_config_t* cfg, int bn) { return bn == 256 && !(cfg->debug_flags & MOK_DEBUG_NO_CTA_PAIR); }
+
+// One TMA-fed GEMM as CTA pairs or as single CTAs; items / pair_items bound
+// the work items of each form.
+template <int A, int B, int BN, int EPI>
+cudaError_t launch_tiles(const GemmMaps& m, const GemmParams& p, long long items, long long pair_items, bool pair,
+                         int sms, cudaStream_t st) {
+  if constexpr (BN == 256) {
+    if (pair) return launch_gemm_pair<A, B, BN, EPI>(m, p, pair_items, st);
+  }
+  return launch_gemm<A, B, BN, EPI>(m, p, items < sms ? static_cast<int>(items) : sms, st);
+}
+
+// Pair work items: row tiles taken two at a time.
+long long row_pairs(long long rows) { return ((rows + 127) / 128 + 1) / 2; }
+
 size_t carve_bwd(void* buf, int T, int k, int E, int H, int I, int Is, BwdLayout* L) {
   const long long mr = max_tiles_of(T, k, E) * kTileRows;
   const long long n = static_cast<long long>(T) * k;
@@ -291,6 +310,7 @@ GemmParams base_params(const mok_schedule_t* s, int* status, int debug) {
     p.row_src = s->row_src;
     p.row0 = s->row0;
     p.cnt = s->cnt;
+    p.pair_tile = s->pair_tile;
   }
   p.status = status;
   p.debug = debug;
@@ -326,11 +346,42 @@ __global__ void propagate_status_kernel(const int* header, int* status) {
 
 }  // namespace
 
+namespace {
+
+// ---------------------------------------------------------------------------
+// Side stream for work that overlaps the caller's stream inside one call (the
+// dispatch permutes): one per host thread and device, created on first use.
+// Every call forks it from the caller's stream with an event and joins it back
+// before the work that reads its results, so all of the call's work stays
+// ordered after what precedes it on the caller's stream.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr;
+  cudaEvent_t join = nullptr;
+};
+thread_local SideStream g_side[64];
+
+mok_status_t side_stream(SideStream** out) {
+  int dev = 0;
+  MOK_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return fail(MOK_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  SideStream& sd = g_side[dev];
+  if (!sd.s) {
+    MOK_CUDA(cudaStreamCreateWithFlags(&sd.s, cudaStreamNonBlocking));
+    MOK_CUDA(cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming));
+    MOK_CUDA(cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming));
+  }
+  *out = &sd;
+  return MOK_OK;
+}
+
+}  // namespace
+
 // ---------------------------------------------------------------------------
 // Scratch for mok_schedule_noalloc: per-chunk expert histograms live in this
 // file-scope device array instead of the caller's buffer.  Every GPU that
 // loads the library holds it until the process exits.
-constexpr long long kStaticSchedScratchInts = 1ll << 18;  // 1 MiB
+constexpr long long kStaticSchedScratchInts = 1ll << 20;  // 4 MiB
 static __device__ __align__(256) int32_t g_sched_scratch[kStaticSchedScratchInts];
 
 namespace {
@@ -365,6 +416,24 @@ mok_status_t forward_bf16(const mok_config_t* cfg, const uint16_t* x, const floa
   const int T = s->T, k = s->k, E = s->E, H = w->H, I = w->I, Is = w->I_s;
   mok_status_t st;
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_PREP, 1, cs));
+  const int disp = resolve_dispatch(cfg);
+  ctx->dispatch = disp;
+  const bool perm = disp == MOK_DISPATCH_PERMUTE;
+  // token rows of x in schedule order (read by the routed gate/up GEMM as
+  // dense tiles), written on a side stream while the shared expert runs
+  SideStream* side = nullptr;
+  if (perm) {
+    if ((st = side_stream(&side))) return st;
+    MOK_CUDA(cudaEventRecord(side->fork, cs));
+    MOK_CUDA(cudaStreamWaitEvent(side->s, side->fork, 0));
+    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 0, side->s));
+    MOK_CUDA(launch_permute_rows(x, H, k, s->row_src, s->header, mr, ctx->x_perm, sms, side->s));
+    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 1, side->s));
+    MOK_CUDA(cudaEventRecord(side->join, side->s));
+  } else {
+    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 0, cs));
+    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 1, cs));
+  }
 
   // ---- shared expert: gate/up + SwiGLU over all T tokens, then down
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_GATEUP, 0, cs));
@@ -376,23 +445,26 @@ mok_status_t forward_bf16(const mok_config_t* cfg, const uint16_t* x, const floa
     GemmParams p = base_params(nullptr, ctx->status, 0);
     p.rows = T; p.K = H; p.N = Is; p.n_tiles = Is / 128; p.b_rows_per_expert = 0;
     p.out0 = ctx->gu_s; p.out1 = ctx->h_s;
-    const int items = ((T + 127) / 128) * p.n_tiles;
-    MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 256, EPI_SWIGLU>(m, p, items < sms ? items : sms, cs)));
+    const long long items = ((T + 127) / 128) * static_cast<long long>(p.n_tiles);
+    MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_K_TILE, 256, EPI_SWIGLU>(m, p, items, row_pairs(T) * p.n_tiles,
+                                                                     pair_on(cfg, 256), sms, cs)));
     MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_GATEUP, 1, cs));
     MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_DOWN, 0, cs));
     GemmMaps m2;
     const int bn = tile_n(H);
-    if ((st = make_map(&m2.a, ctx->h_s, Is, T, 128, kTileBK)) || (st = make_map(&m2.b0, w->ws_down, Is, H, bn, kTileBK)))
+    const bool pr = pair_on(cfg, bn);
+    if ((st = make_map(&m2.a, ctx->h_s, Is, T, 128, kTileBK)) ||
+        (st = make_map(&m2.b0, w->ws_down, Is, H, pr ? bn / 2 : bn, kTileBK)))
       return st;
     m2.b1 = m2.b0;
     GemmParams q = base_params(nullptr, ctx->status, 0);
     q.rows = T; q.K = Is; q.N = H; q.n_tiles = H / bn; q.out0 = ctx->shared_out; q.ld = H;
-    const int items2 = ((T + 127) / 128) * q.n_tiles;
-    const int grid2 = items2 < sms ? items2 : sms;
+    const long long items2 = ((T + 127) / 128) * static_cast<long long>(q.n_tiles);
     if (bn == 256)
-      MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 256, EPI_STORE_ROWS>(m2, q, grid2, cs)));
+      MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_K_TILE, 256, EPI_STORE_ROWS>(m2, q, items2, row_pairs(T) * q.n_tiles, pr,
+                                                                          sms, cs)));
     else
-      MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 128, EPI_STORE_ROWS>(m2, q, grid2, cs)));
+      MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_K_TILE, 128, EPI_STORE_ROWS>(m2, q, items2, 0, false, sms, cs)));
   } else {
     MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_GATEUP, 1, cs));
     MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_DOWN, 0, cs));
@@ -400,13 +472,7 @@ mok_status_t forward_bf16(const mok_config_t* cfg, const uint16_t* x, const floa
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_DOWN, 1, cs));
 
   // ---- routed experts: gate/up + SwiGLU, then down + scale + scatter
-  const int disp = resolve_dispatch(cfg);
-  ctx->dispatch = disp;
-  const bool perm = disp == MOK_DISPATCH_PERMUTE;
-  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 0, cs));
-  if (perm)  // token rows of x in schedule order, read below as dense tiles
-    MOK_CUDA(launch_permute_rows(x, H, k, s->row_src, s->header, mr, ctx->x_perm, sms, cs));
-  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 1, cs));
+  if (side) MOK_CUDA(cudaStreamWaitEvent(cs, side->join, 0));
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_GATEUP, 0, cs));
   GemmMaps m;
   const int bk = perm ? kTileBK : kGatherBK;
@@ -420,7 +486,7 @@ mok_status_t forward_bf16(const mok_config_t* cfg, const uint16_t* x, const floa
   const long long items = static_cast<long long>(s->max_tiles) * p.n_tiles;
   const int grid = items < sms ? static_cast<int>(items) : sms;
   if (perm)
-    MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 256, EPI_SWIGLU>(m, p, grid, cs)));
+    MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_K_TILE, 256, EPI_SWIGLU>(m, p, items, items, pair_on(cfg, 256), sms, cs)));
   else if (g4)
     MOK_CUDA((launch_gemm<SRC_K_GATHER, SRC_K_TILE, 256, EPI_SWIGLU>(m, p, grid, cs)));
   else
@@ -429,19 +495,19 @@ mok_status_t forward_bf16(const mok_config_t* cfg, const uint16_t* x, const floa
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DOWN, 0, cs));
   GemmMaps m2;
   const int bn = tile_n(H);
+  const bool pr = pair_on(cfg, bn);
   if ((st = make_map(&m2.a, ctx->h, I, mr, 128, kTileBK)) ||
-      (st = make_map(&m2.b0, w->w_down, I, static_cast<uint64_t>(E) * H, bn, kTileBK)))
+      (st = make_map(&m2.b0, w->w_down, I, static_cast<uint64_t>(E) * H, pr ? bn / 2 : bn, kTileBK)))
     return st;
   m2.b1 = m2.b0;
   GemmParams q = base_params(s, ctx->status, 0);
   q.grouped = 1; q.K = I; q.N = H; q.n_tiles = H / bn; q.b_rows_per_expert = H;
   q.out0 = ctx->slots; q.ld = H; q.rw = router_w;
   const long long items2 = static_cast<long long>(s->max_tiles) * q.n_tiles;
-  const int grid2 = items2 < sms ? static_cast<int>(items2) : sms;
   if (bn == 256)
-    MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 256, EPI_SCALE_SCATTER>(m2, q, grid2, cs)));
+    MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_K_TILE, 256, EPI_SCALE_SCATTER>(m2, q, items2, items2, pr, sms, cs)));
   else
-    MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_K_TILE, 128, EPI_SCALE_SCATTER>(m2, q, grid2, cs)));
+    MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_K_TILE, 128, EPI_SCALE_SCATTER>(m2, q, items2, 0, false, sms, cs)));
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DOWN, 1, cs));
   return MOK_OK;
 }
@@ -456,21 +522,28 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
   const int T = s->T, k = s->k, E = s->E, H = w->H, I = w->I, Is = w->I_s;
   const long long mr = static_cast<long long>(s->max_tiles) * kTileRows;
   mok_status_t st;
-  MOK_CUDA(launch_mx_tile_scales(w->mx_gate_sc, static_cast<long long>(E) * I, H, X.wg_sc, cs));
-  MOK_CUDA(launch_mx_tile_scales(w->mx_up_sc, static_cast<long long>(E) * I, H, X.wu_sc, cs));
-  MOK_CUDA(launch_mx_tile_scales(w->mx_down_sc, static_cast<long long>(E) * H, I, X.wd_sc, cs));
+  // weight scales into the tensor-core layout on a side stream, while x is
+  // quantised once per token into token order and schedule order
+  SideStream* side = nullptr;
+  if ((st = side_stream(&side))) return st;
+  MOK_CUDA(cudaEventRecord(side->fork, cs));
+  MOK_CUDA(cudaStreamWaitEvent(side->s, side->fork, 0));
+  MOK_CUDA(launch_mx_tile_scales(w->mx_gate_sc, static_cast<long long>(E) * I, H, X.wg_sc, side->s));
+  MOK_CUDA(launch_mx_tile_scales(w->mx_up_sc, static_cast<long long>(E) * I, H, X.wu_sc, side->s));
+  MOK_CUDA(launch_mx_tile_scales(w->mx_down_sc, static_cast<long long>(E) * H, I, X.wd_sc, side->s));
   if (Is > 0) {
-    MOK_CUDA(launch_mx_tile_scales(w->mxs_gate_sc, Is, H, X.wsg_sc, cs));
-    MOK_CUDA(launch_mx_tile_scales(w->mxs_up_sc, Is, H, X.wsu_sc, cs));
-    MOK_CUDA(launch_mx_tile_scales(w->mxs_down_sc, H, Is, X.wsd_sc, cs));
+    MOK_CUDA(launch_mx_tile_scales(w->mxs_gate_sc, Is, H, X.wsg_sc, side->s));
+    MOK_CUDA(launch_mx_tile_scales(w->mxs_up_sc, Is, H, X.wsu_sc, side->s));
+    MOK_CUDA(launch_mx_tile_scales(w->mxs_down_sc, H, Is, X.wsd_sc, side->s));
   }
+  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_PREP, 1, side->s));
+  MOK_CUDA(cudaEventRecord(side->join, side->s));
   ctx->dispatch = MOK_DISPATCH_PERMUTE;
-  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_PREP, 1, cs));
-  // x quantised once per token, into token order and schedule order
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 0, cs));
   MOK_CUDA(launch_mx_dispatch(x, T, H, k, s->slot_row, s->row_src, s->header, mr, ctx->xq, ctx->xq_sc, ctx->xq_perm,
                               ctx->xq_perm_sc, sms, cs));
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 1, cs));
+  MOK_CUDA(cudaStreamWaitEvent(cs, side->join, 0));
 
   const int bn = tile_n(H);
   // ---- shared expert
@@ -579,12 +652,12 @@ mok_status_t mok_schedule(const int64_t* top_experts, int T, int k, int E, float
   if (capd > static_cast<double>(mt)) capd = static_cast<double>(mt);
   const int cap = static_cast<int>(capd);
   MOK_CUDA(launch_schedule(top_experts, T, k, E, cap, static_cast<int>(mt), L.hist, L.cnt, L.row0,
-                           L.row_src, L.slot_row, L.tile_expert, L.tile_row0, L.tile_rows, L.header,
-                           static_cast<cudaStream_t>(stream)));
+                           L.row_src, L.slot_row, L.tile_expert, L.tile_row0, L.tile_rows, L.pair_tile,
+                           L.header, static_cast<cudaStream_t>(stream)));
   out->T = T; out->k = k; out->E = E; out->max_tiles = static_cast<int>(mt);
   out->cnt = L.cnt; out->row0 = L.row0; out->row_src = L.row_src; out->slot_row = L.slot_row;
   out->tile_expert = L.tile_expert; out->tile_row0 = L.tile_row0; out->tile_rows = L.tile_rows;
-  out->header = L.header; out->scratch = L.hist;
+  out->header = L.header; out->scratch = L.hist; out->pair_tile = L.pair_tile;
   return MOK_OK;
 }
 
@@ -720,29 +793,128 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
   carve_bwd(ws, T, k, E, H, I, Is, &L);
   const long long mr = static_cast<long long>(s->max_tiles) * kTileRows;
 
-  // ---- routed: down dgrad + SwiGLU backward + router-weight partials
   const int bn1 = tile_n(I);
   const bool perm = resolve_dispatch(cfg) == MOK_DISPATCH_PERMUTE;
-  // permuted dispatch: token rows of x (unquantised, for the weight gradient)
-  // in schedule order; the forward's copy serves when it holds exactly that
+  // ---- permuted dispatch: token rows of dy, and of x (unquantised, for the
+  // weight gradient), in schedule order; the forward's copy of x serves when it
+  // holds exactly that.  The permutes run on a side stream, overlapping the
+  // shared expert's backward, which reads token-order rows only.
   const uint16_t* x_rows = nullptr;
-  MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 0, cs));
+  SideStream* side = nullptr;
   if (perm) {
+    if ((st = side_stream(&side))) return st;
+    MOK_CUDA(cudaEventRecord(side->fork, cs));
+    MOK_CUDA(cudaStreamWaitEvent(side->s, side->fork, 0));
+    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 0, side->s));
     if (ctx->dispatch == MOK_DISPATCH_PERMUTE && ctx->mode == MOK_MODE_BF16 && ctx->x_perm) {
       x_rows = ctx->x_perm;
     } else {
-      MOK_CUDA(launch_permute_rows(x, H, k, s->row_src, s->header, mr, L.xb_perm, sms, cs));
+      MOK_CUDA(launch_permute_rows(x, H, k, s->row_src, s->header, mr, L.xb_perm, sms, side->s));
       x_rows = L.xb_perm;
     }
-    MOK_CUDA(launch_permute_rows(dy, H, k, s->row_src, s->header, mr, L.dy_perm, sms, cs));
+    MOK_CUDA(launch_permute_rows(dy, H, k, s->row_src, s->header, mr, L.dy_perm, sms, side->s));
+    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 1, side->s));
+    MOK_CUDA(cudaEventRecord(side->join, side->s));
+  } else {
+    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 0, cs));
+    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 1, cs));
   }
-  MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 1, cs));
+  // ---- shared expert backward (dense rows, w = 1)
+  if (Is > 0) {
+    const int bns = tile_n(Is);
+    {
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DOWN, 0, cs));
+      GemmMaps m;
+      const bool pr = pair_on(cfg, bns);
+      if ((st = make_map(&m.a, dy, H, T, 128, kTileBK)) ||
+          (st = make_map_mn(&m.b0, w->ws_down, Is, H, pr ? bns / 2 : bns, kTileBK)))
+        return st;
+      m.b1 = m.b0;
+      GemmParams p = base_params(nullptr, ctx->status, 0);
+      p.rows = T; p.K = H; p.N = Is; p.n_tiles = Is / bns; p.b_rows_per_expert = 0;
+      p.aux0 = ctx->gu_s; p.out0 = L.dgu_s; p.out1 = L.hs;
+      const long long items = ((T + 127) / 128) * static_cast<long long>(p.n_tiles);
+      if (bns == 256)
+        MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_MN_TILE, 256, EPI_DOWN_BWD>(m, p, items, row_pairs(T) * p.n_tiles, pr,
+                                                                           sms, cs)));
+      else
+        MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_MN_TILE, 128, EPI_DOWN_BWD>(m, p, items, 0, false, sms, cs)));
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DOWN, 1, cs));
+    }
+    {  // dW_s_down = dy^T h_s
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_DOWN, 0, cs));
+      GemmMaps m;
+      const bool pr = pair_on(cfg, bns);
+      if ((st = make_map_mn(&m.a, dy, H, T, 128, kTileBK)) ||
+          (st = make_map_mn(&m.b0, L.hs, Is, T, pr ? bns / 2 : bns, kTileBK)))
+        return st;
+      m.b1 = m.b0;
+      GemmParams p = base_params(nullptr, ctx->status, 0);
+      p.wgrad = 1; p.rows = T; p.E = 1; p.m_tiles = H / 128; p.n_tiles = Is / bns;
+      p.out0 = g->d_ws_down; p.out1 = g->d_ws_down; p.ld = Is; p.split = H; p.estride = 0;
+      const long long items = static_cast<long long>(p.m_tiles) * p.n_tiles;
+      const long long pitems = static_cast<long long>((p.m_tiles + 1) / 2) * p.n_tiles;
+      if (bns == 256)
+        MOK_CUDA((launch_tiles<SRC_MN_TILE, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, items, pitems, pr, sms, cs)));
+      else
+        MOK_CUDA((launch_tiles<SRC_MN_TILE, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, items, 0, false, sms, cs)));
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_DOWN, 1, cs));
+    }
+    {  // dW_s_gate|up = (dG_s|dU_s)^T x
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_GATEUP, 0, cs));
+      GemmMaps m;
+      const int bn = tile_n(H);
+      const bool pr = pair_on(cfg, bn);
+      if ((st = make_map_mn(&m.a, L.dgu_s, 2 * Is, T, 128, kTileBK)) ||
+          (st = make_map_mn(&m.b0, x, H, T, pr ? bn / 2 : bn, kTileBK)))
+        return st;
+      m.b1 = m.b0;
+      GemmParams p = base_params(nullptr, ctx->status, 0);
+      p.wgrad = 1; p.rows = T; p.E = 1; p.m_tiles = 2 * Is / 128; p.n_tiles = H / bn;
+      p.out0 = g->d_ws_gate; p.out1 = g->d_ws_up; p.ld = H; p.split = Is; p.estride = 0;
+      const long long items = static_cast<long long>(p.m_tiles) * p.n_tiles;
+      const long long pitems = static_cast<long long>((p.m_tiles + 1) / 2) * p.n_tiles;
+      if (bn == 256)
+        MOK_CUDA((launch_tiles<SRC_MN_TILE, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, items, pitems, pr, sms, cs)));
+      else
+        MOK_CUDA((launch_tiles<SRC_MN_TILE, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, items, 0, false, sms, cs)));
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_GATEUP, 1, cs));
+    }
+    {  // dx_s = dG_s W_s_gate + dU_s W_s_up
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DGRAD, 0, cs));
+      GemmMaps m;
+      const int bn = tile_n(H);
+      const bool pr = pair_on(cfg, bn);
+      if ((st = make_map(&m.a, L.dgu_s, 2 * Is, T, 128, kTileBK)) ||
+          (st = make_map_mn(&m.b0, w->ws_gate, H, Is, pr ? bn / 2 : bn, kTileBK)) ||
+          (st = make_map_mn(&m.b1, w->ws_up, H, Is, pr ? bn / 2 : bn, kTileBK)))
+        return st;
+      GemmParams p = base_params(nullptr, ctx->status, 0);
+      p.rows = T; p.K = 2 * Is; p.N = H; p.n_tiles = H / bn; p.b_rows_per_expert = 0; p.b_split = Is;
+      p.out0 = L.dx_s; p.ld = H;
+      const long long items = ((T + 127) / 128) * static_cast<long long>(p.n_tiles);
+      if (bn == 256)
+        MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_MN_TILE, 256, EPI_STORE_ROWS>(m, p, items, row_pairs(T) * p.n_tiles, pr,
+                                                                             sms, cs)));
+      else
+        MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_MN_TILE, 128, EPI_STORE_ROWS>(m, p, items, 0, false, sms, cs)));
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DGRAD, 1, cs));
+    }
+  } else {
+    for (int sg = MOK_STAGE_BWD_SHARED_DOWN; sg <= MOK_STAGE_BWD_SHARED_DGRAD; ++sg) {
+      MOK_CUDA(mark(cfg, sg, 0, cs));
+      MOK_CUDA(mark(cfg, sg, 1, cs));
+    }
+  }
+  // ---- routed: down dgrad + SwiGLU backward + router-weight partials
+  if (side) MOK_CUDA(cudaStreamWaitEvent(cs, side->join, 0));
   {
     MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DOWN, 0, cs));
     GemmMaps m;
     const int bk = perm ? kTileBK : kGatherBK;
+    const bool pr = perm && pair_on(cfg, bn1);
     if ((st = perm ? make_map(&m.a, L.dy_perm, H, mr, 128, bk) : make_map(&m.a, dy, H, T, 1, bk)) ||
-        (st = make_map_mn(&m.b0, w->w_down, I, static_cast<uint64_t>(E) * H, bn1, bk)))
+        (st = make_map_mn(&m.b0, w->w_down, I, static_cast<uint64_t>(E) * H, pr ? bn1 / 2 : bn1, bk)))
       return st;
     m.b1 = m.b0;
     GemmParams p = base_params(s, ctx->status, 0);
@@ -752,7 +924,7 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
     const long long items = static_cast<long long>(s->max_tiles) * p.n_tiles;
     const int grid = items < sms ? static_cast<int>(items) : sms;
     if (perm && bn1 == 256)
-      MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_MN_TILE, 256, EPI_DOWN_BWD>(m, p, grid, cs)));
+      MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_MN_TILE, 256, EPI_DOWN_BWD>(m, p, items, items, pr, sms, cs)));
     else if (perm)
       MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_MN_TILE, 128, EPI_DOWN_BWD>(m, p, grid, cs)));
     else if (g4 && bn1 == 256)
@@ -770,20 +942,22 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
     MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_DOWN, 0, cs));
     GemmMaps m;
     const int bk = perm ? kTileBK : kGatherBK;
+    const int bn = tile_n(I);
+    const bool pr = perm && pair_on(cfg, bn);
     if ((st = perm ? make_map_mn(&m.a, L.dy_perm, H, mr, 128, bk) : make_map(&m.a, dy, H, T, 1, bk)) ||
-        (st = make_map_mn(&m.b0, L.hw, I, mr, tile_n(I), bk)))
+        (st = make_map_mn(&m.b0, L.hw, I, mr, pr ? bn / 2 : bn, bk)))
       return st;
     m.b1 = m.b0;
     GemmParams p = base_params(s, ctx->status, 0);
-    const int bn = tile_n(I);
     p.wgrad = 1; p.grouped = 1; p.E = E; p.m_tiles = H / 128; p.n_tiles = I / bn;
     p.out0 = g->d_w_down; p.out1 = g->d_w_down; p.ld = I; p.split = H;
     p.estride = static_cast<long long>(H) * I;
     p.ga = dy; p.ga_ld = H;
     const long long items = static_cast<long long>(E) * p.m_tiles * p.n_tiles;
+    const long long pitems = static_cast<long long>(E) * ((p.m_tiles + 1) / 2) * p.n_tiles;
     const int grid = items < sms ? static_cast<int>(items) : sms;
     if (perm && bn == 256)
-      MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, grid, cs)));
+      MOK_CUDA((launch_tiles<SRC_MN_TILE, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, items, pitems, pr, sms, cs)));
     else if (perm)
       MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, grid, cs)));
     else if (g4 && bn == 256)
@@ -801,20 +975,22 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
     MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_GATEUP, 0, cs));
     GemmMaps m;
     const int bk = perm ? kTileBK : kGatherBK;
+    const int bn = tile_n(H);
+    const bool pr = perm && pair_on(cfg, bn);
     if ((st = make_map_mn(&m.a, L.dgu, 2 * I, mr, 128, bk)) ||
-        (st = perm ? make_map_mn(&m.b0, x_rows, H, mr, tile_n(H), bk) : make_map(&m.b0, x, H, T, 1, bk)))
+        (st = perm ? make_map_mn(&m.b0, x_rows, H, mr, pr ? bn / 2 : bn, bk) : make_map(&m.b0, x, H, T, 1, bk)))
       return st;
     m.b1 = m.b0;
     GemmParams p = base_params(s, ctx->status, 0);
-    const int bn = tile_n(H);
     p.wgrad = 1; p.grouped = 1; p.E = E; p.m_tiles = 2 * I / 128; p.n_tiles = H / bn;
     p.out0 = g->d_w_gate; p.out1 = g->d_w_up; p.ld = H; p.split = I;
     p.estride = static_cast<long long>(I) * H;
     p.gb = x; p.gb_ld = H;
     const long long items = static_cast<long long>(E) * p.m_tiles * p.n_tiles;
+    const long long pitems = static_cast<long long>(E) * ((p.m_tiles + 1) / 2) * p.n_tiles;
     const int grid = items < sms ? static_cast<int>(items) : sms;
     if (perm && bn == 256)
-      MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, grid, cs)));
+      MOK_CUDA((launch_tiles<SRC_MN_TILE, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, items, pitems, pr, sms, cs)));
     else if (perm)
       MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, grid, cs)));
     else if (g4 && bn == 256)
@@ -831,97 +1007,22 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
   {
     MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DGRAD_GATEUP, 0, cs));
     GemmMaps m;
+    const int bn = tile_n(H);
+    const bool pr = pair_on(cfg, bn);
+    const int bw = pr ? bn / 2 : bn;
     if ((st = make_map(&m.a, L.dgu, 2 * I, mr, 128, kTileBK)) ||
-        (st = make_map_mn(&m.b0, w->w_gate, H, static_cast<uint64_t>(E) * I, tile_n(H), kTileBK)) ||
-        (st = make_map_mn(&m.b1, w->w_up, H, static_cast<uint64_t>(E) * I, tile_n(H), kTileBK)))
+        (st = make_map_mn(&m.b0, w->w_gate, H, static_cast<uint64_t>(E) * I, bw, kTileBK)) ||
+        (st = make_map_mn(&m.b1, w->w_up, H, static_cast<uint64_t>(E) * I, bw, kTileBK)))
       return st;
     GemmParams p = base_params(s, ctx->status, 0);
-    const int bn = tile_n(H);
     p.grouped = 1; p.K = 2 * I; p.N = H; p.n_tiles = H / bn; p.b_rows_per_expert = I; p.b_split = I;
     p.out0 = L.dx_slots; p.ld = H;
     const long long items = static_cast<long long>(s->max_tiles) * p.n_tiles;
-    const int grid = items < sms ? static_cast<int>(items) : sms;
     if (bn == 256)
-      MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_MN_TILE, 256, EPI_SCATTER>(m, p, grid, cs)));
+      MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_MN_TILE, 256, EPI_SCATTER>(m, p, items, items, pr, sms, cs)));
     else
-      MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_MN_TILE, 128, EPI_SCATTER>(m, p, grid, cs)));
+      MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_MN_TILE, 128, EPI_SCATTER>(m, p, items, 0, false, sms, cs)));
     MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DGRAD_GATEUP, 1, cs));
-  }
-  // ---- shared expert backward (dense rows, w = 1)
-  if (Is > 0) {
-    const int bns = tile_n(Is);
-    {
-      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DOWN, 0, cs));
-      GemmMaps m;
-      if ((st = make_map(&m.a, dy, H, T, 128, kTileBK)) || (st = make_map_mn(&m.b0, w->ws_down, Is, H, bns, kTileBK))) return st;
-      m.b1 = m.b0;
-      GemmParams p = base_params(nullptr, ctx->status, 0);
-      p.rows = T; p.K = H; p.N = Is; p.n_tiles = Is / bns; p.b_rows_per_expert = 0;
-      p.aux0 = ctx->gu_s; p.out0 = L.dgu_s; p.out1 = L.hs;
-      const int items = ((T + 127) / 128) * p.n_tiles;
-      const int grid = items < sms ? items : sms;
-      if (bns == 256)
-        MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_MN_TILE, 256, EPI_DOWN_BWD>(m, p, grid, cs)));
-      else
-        MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_MN_TILE, 128, EPI_DOWN_BWD>(m, p, grid, cs)));
-      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DOWN, 1, cs));
-    }
-    {  // dW_s_down = dy^T h_s
-      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_DOWN, 0, cs));
-      GemmMaps m;
-      if ((st = make_map_mn(&m.a, dy, H, T, 128, kTileBK)) || (st = make_map_mn(&m.b0, L.hs, Is, T, bns, kTileBK))) return st;
-      m.b1 = m.b0;
-      GemmParams p = base_params(nullptr, ctx->status, 0);
-      p.wgrad = 1; p.rows = T; p.E = 1; p.m_tiles = H / 128; p.n_tiles = Is / bns;
-      p.out0 = g->d_ws_down; p.out1 = g->d_ws_down; p.ld = Is; p.split = H; p.estride = 0;
-      const int items = p.m_tiles * p.n_tiles;
-      const int grid = items < sms ? items : sms;
-      if (bns == 256)
-        MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, grid, cs)));
-      else
-        MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, grid, cs)));
-      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_DOWN, 1, cs));
-    }
-    {  // dW_s_gate|up = (dG_s|dU_s)^T x
-      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_GATEUP, 0, cs));
-      GemmMaps m;
-      if ((st = make_map_mn(&m.a, L.dgu_s, 2 * Is, T, 128, kTileBK)) || (st = make_map_mn(&m.b0, x, H, T, tile_n(H), kTileBK))) return st;
-      m.b1 = m.b0;
-      GemmParams p = base_params(nullptr, ctx->status, 0);
-      const int bn = tile_n(H);
-      p.wgrad = 1; p.rows = T; p.E = 1; p.m_tiles = 2 * Is / 128; p.n_tiles = H / bn;
-      p.out0 = g->d_ws_gate; p.out1 = g->d_ws_up; p.ld = H; p.split = Is; p.estride = 0;
-      const int items = p.m_tiles * p.n_tiles;
-      const int grid = items < sms ? items : sms;
-      if (bn == 256)
-        MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, grid, cs)));
-      else
-        MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, grid, cs)));
-      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_GATEUP, 1, cs));
-    }
-    {  // dx_s = dG_s W_s_gate + dU_s W_s_up
-      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DGRAD, 0, cs));
-      GemmMaps m;
-      if ((st = make_map(&m.a, L.dgu_s, 2 * Is, T, 128, kTileBK)) || (st = make_map_mn(&m.b0, w->ws_gate, H, Is, tile_n(H), kTileBK)) ||
-          (st = make_map_mn(&m.b1, w->ws_up, H, Is, tile_n(H), kTileBK)))
-        return st;
-      GemmParams p = base_params(nullptr, ctx->status, 0);
-      const int bn = tile_n(H);
-      p.rows = T; p.K = 2 * Is; p.N = H; p.n_tiles = H / bn; p.b_rows_per_expert = 0; p.b_split = Is;
-      p.out0 = L.dx_s; p.ld = H;
-      const int items = ((T + 127) / 128) * p.n_tiles;
-      const int grid = items < sms ? items : sms;
-      if (bn == 256)
-        MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_MN_TILE, 256, EPI_STORE_ROWS>(m, p, grid, cs)));
-      else
-        MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_MN_TILE, 128, EPI_STORE_ROWS>(m, p, grid, cs)));
-      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DGRAD, 1, cs));
-    }
-  } else {
-    for (int sg = MOK_STAGE_BWD_SHARED_DOWN; sg <= MOK_STAGE_BWD_SHARED_DGRAD; ++sg) {
-      MOK_CUDA(mark(cfg, sg, 0, cs));
-      MOK_CUDA(mark(cfg, sg, 1, cs));
-    }
   }
   // ---- fixed-order reductions: dx and the router-weight gradient
   MOK_CUDA(mark(cfg, MOK_STAGE_BWD_REDUCE, 0, cs));
@@ -964,12 +1065,12 @@ mok_status_t mok_schedule_noalloc(const int64_t* top_experts, int T, int k, int 
   // every histogram entry the build reads is first written by it, so the
   // array needs no clearing between calls
   MOK_CUDA(launch_schedule(top_experts, T, k, E, static_cast<int>(capd), static_cast<int>(mt), scratch, L.cnt,
-                           L.row0, L.row_src, L.slot_row, L.tile_expert, L.tile_row0, L.tile_rows, L.header,
-                           static_cast<cudaStream_t>(stream)));
+                           L.row0, L.row_src, L.slot_row, L.tile_expert, L.tile_row0, L.tile_rows, L.pair_tile,
+                           L.header, static_cast<cudaStream_t>(stream)));
   out->T = T; out->k = k; out->E = E; out->max_tiles = static_cast<int>(mt);
   out->cnt = L.cnt; out->row0 = L.row0; out->row_src = L.row_src; out->slot_row = L.slot_row;
   out->tile_expert = L.tile_expert; out->tile_row0 = L.tile_row0; out->tile_rows = L.tile_rows;
-  out->header = L.header; out->scratch = scratch;
+  out->header = L.header; out->scratch = scratch; out->pair_tile = L.pair_tile;
   return MOK_OK;
 }
 

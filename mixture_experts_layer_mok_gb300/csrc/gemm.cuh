@@ -80,6 +80,7 @@ struct GemmParams {
   const int* row_src;
   const int* row0;
   const int* cnt;
+  const int* pair_tile;  // CTA-pair GEMMs: [pairs][2] tile indices (second -1 = none)
   // ---- operand coordinates
   int b_rows_per_expert;  // weight rows (K-major B) or K-rows (MN-major B) per expert
   int b_split;            // MN-major B: K index where map b1 takes over (0 = never)
@@ -111,6 +112,7 @@ struct GemmParams {
 
 struct Item {
   int e, p0, rows, m0, nt, kbeg, nk;
+  bool empty;  // CTA-pair GEMMs: this CTA's half of the pair has no tile
 };
 
 __device__ __forceinline__ int num_items(const GemmParams& p) {
@@ -124,6 +126,7 @@ __device__ __forceinline__ int num_items(const GemmParams& p) {
 
 __device__ __forceinline__ Item get_item(const GemmParams& p, int idx, int bk) {
   Item it;
+  it.empty = false;
   if (!p.wgrad) {
     const int mt = idx / p.n_tiles;
     it.nt = idx - mt * p.n_tiles;
@@ -146,6 +149,65 @@ __device__ __forceinline__ Item get_item(const GemmParams& p, int idx, int bk) {
     const int mt = r / p.n_tiles;
     it.nt = r - mt * p.n_tiles;
     it.m0 = mt * kBM;
+    it.p0 = 0;
+    it.rows = 0;
+    if (p.grouped) {
+      it.kbeg = __ldg(p.row0 + it.e);
+      const int c = __ldg(p.cnt + it.e);
+      it.nk = (c + kBM - 1) / kBM * (kBM / bk);
+    } else {
+      it.kbeg = 0;
+      it.nk = (p.rows + bk - 1) / bk;
+    }
+  }
+  return it;
+}
+
+// CTA-pair GEMMs: work items are pairs of 128-row tiles (rank 0 takes the
+// first, rank 1 the second) sharing one B tile; weight gradients pair
+// adjacent output row tiles of one expert.
+__device__ __forceinline__ int num_items_pair(const GemmParams& p) {
+  if (p.grouped && p.header[2] != 0) return 0;
+  if (!p.wgrad) {
+    const int pairs = p.grouped ? p.header[4] : ((p.rows + kBM - 1) / kBM + 1) / 2;
+    return pairs * p.n_tiles;
+  }
+  return p.E * ((p.m_tiles + 1) / 2) * p.n_tiles;
+}
+
+__device__ __forceinline__ Item get_item_pair(const GemmParams& p, int idx, int bk, int rank) {
+  Item it;
+  it.empty = false;
+  if (!p.wgrad) {
+    const int pr = idx / p.n_tiles;
+    it.nt = idx - pr * p.n_tiles;
+    if (p.grouped) {
+      const int t0 = __ldg(p.pair_tile + 2 * pr);
+      const int t1 = __ldg(p.pair_tile + 2 * pr + 1);
+      const int t = (rank && t1 >= 0) ? t1 : t0;   // an empty half loads its partner's rows
+      it.e = __ldg(p.tile_expert + t);
+      it.p0 = __ldg(p.tile_row0 + t);
+      it.rows = __ldg(p.tile_rows + t);
+      it.empty = rank && t1 < 0;
+    } else {
+      it.e = 0;
+      it.p0 = (2 * pr + rank) * kBM;               // past the last row: loads read zeros
+      it.rows = min(kBM, p.rows - it.p0);
+      it.empty = it.rows <= 0;
+    }
+    it.m0 = it.p0;
+    it.kbeg = 0;
+    it.nk = p.K / bk;
+  } else {
+    const int mp_n = (p.m_tiles + 1) / 2;
+    const int per_e = mp_n * p.n_tiles;
+    it.e = idx / per_e;
+    const int r = idx - it.e * per_e;
+    const int mp = r / p.n_tiles;
+    it.nt = r - mp * p.n_tiles;
+    const int mt = 2 * mp + rank;
+    it.empty = mt >= p.m_tiles;
+    it.m0 = (it.empty ? 2 * mp : mt) * kBM;
     it.p0 = 0;
     it.rows = 0;
     if (p.grouped) {
@@ -296,7 +358,7 @@ __host__ __device__ __forceinline__ long long mx_tiled_scale_offset(long long ro
   return atom * 512 + (r & 31) * 16 + (r >> 5) * 4 + (cblk & 3);
 }
 
-template <int A_SRC, int B_SRC, int BN, int EPI>
+template <int A_SRC, int B_SRC, int BN, int EPI, bool PAIR = false>
 struct GemmCfg {
   static constexpr bool kAMN = (A_SRC == SRC_MN_TILE || A_SRC == SRC_MN_GATHER || A_SRC == SRC_MN_GATHER_LSU);
   static constexpr bool kBMN = (B_SRC == SRC_MN_TILE || B_SRC == SRC_MN_GATHER || B_SRC == SRC_MN_GATHER_LSU);
@@ -316,7 +378,9 @@ struct GemmCfg {
   static constexpr int kMnChunkBytes = kRowBytes * kBK;     // MN-major chunk: kBK K-rows x kBK elements
   static constexpr uint32_t kSwz = (kBK == 64) ? 2u : 4u;   // descriptor swizzle: 128-byte / 64-byte
   static constexpr int kABytes = kBM * kBK * 2;
-  static constexpr int kBBytes = BN * kBK * 2;
+  // CTA pair: each CTA holds half of B's BN rows (the pair's MMA reads both)
+  static constexpr int kBRows = PAIR ? BN / 2 : BN;
+  static constexpr int kBBytes = kBRows * kBK * 2;
   static constexpr int kTmaBytes = (kALsu ? 0 : kABytes) + (kBLsu ? 0 : kBBytes);
   // stage-full arrivals: the TMA warp's expect_tx, plus one hardware arrival per
   // gather thread when its copies for the stage have landed
@@ -328,8 +392,11 @@ struct GemmCfg {
   static constexpr int kStages = kStagesFit > 16 ? 16 : kStagesFit;
   static constexpr int kTmemCols = 2 * BN;  // two accumulator buffers
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes + kEpiWarps * kEpiStageBytes;
-  static constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, kAMN, kBMN);
+  static constexpr uint32_t kIdesc = idesc_bf16(PAIR ? 2 * kBM : kBM, BN, kAMN, kBMN);
   static_assert(BN == 128 || BN == 256, "tile N");
+  static_assert(!PAIR || (!kHasLsu && A_SRC != SRC_K_GATHER && A_SRC != SRC_MN_GATHER && B_SRC != SRC_MN_GATHER),
+                "CTA pairs take TMA tiles only");
+  static_assert(!PAIR || BN == 256, "CTA pairs split a 256-wide B tile");
   static_assert(!(kALsu && kBLsu), "one gathered operand per GEMM");
   static_assert(EPI != EPI_SWIGLU_MX, "the MXFP8 SwiGLU epilogue runs in gemm_mx_kernel");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
@@ -384,10 +451,10 @@ __device__ __forceinline__ void gather_mn(uint8_t* dst, const uint16_t* src, lon
   }
 }
 
-template <int A_SRC, int B_SRC, int BN, int EPI>
-__global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
+template <int A_SRC, int B_SRC, int BN, int EPI, bool PAIR = false>
+__global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI, PAIR>::kThreads, 1)
     gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
-  using C = GemmCfg<A_SRC, B_SRC, BN, EPI>;
+  using C = GemmCfg<A_SRC, B_SRC, BN, EPI, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -402,6 +469,11 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // CTA pair: rank in the pair, persistent loop over the pair's items
+  const int rank = PAIR ? static_cast<int>(cluster_rank()) : 0;
+  const int item0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int istep = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  auto item_at = [&](int idx, int bk) { return PAIR ? get_item_pair(p, idx, bk, rank) : get_item(p, idx, bk); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -410,7 +482,7 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], C::kEpiWarps);
+      mbar_init(&tempty[b], (PAIR ? 2 : 1) * C::kEpiWarps);   // the leader's counts both CTAs' warps
     }
     mbar_init(done, 1);
     *abort_flag = 0;
@@ -420,14 +492,22 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
     tma_prefetch_desc(&maps.b1);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, C::kTmemCols);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(tmem_slot, C::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, C::kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if (PAIR)
+    cluster_sync();   // both CTAs' barriers initialised before any cross-CTA signal
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int nitems = num_items(p);
+  const int nitems = PAIR ? num_items_pair(p) : num_items(p);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -435,8 +515,8 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
     uint32_t phase = 0;
     long long fills = 0;
     bool ok = true;
-    for (int idx = blockIdx.x; idx < nitems && ok; idx += gridDim.x) {
-      const Item it = get_item(p, idx, C::kBK);
+    for (int idx = item0; idx < nitems && ok; idx += istep) {
+      const Item it = item_at(idx, C::kBK);
       const int bn_out = (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_MX) ? BN / 2 : BN;
       const int n0 = it.nt * bn_out;
       // token rows of a row tile (K-major gather): rows 4*lane .. 4*lane+3
@@ -463,19 +543,33 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
           ok = false;
           break;
         }
-        if (lane == 0) mbar_arrive_expect_tx(&full[stage], C::kTmaBytes);
+        // CTA pair: both CTAs' loads complete on the leader's barrier
+        if (lane == 0 && (!PAIR || rank == 0)) mbar_arrive_expect_tx(&full[stage], (PAIR ? 2 : 1) * C::kTmaBytes);
         __syncwarp();
         uint8_t* sA = smem + stage * C::kStageBytes;
         uint8_t* sB = sA + C::kABytes;
         const int k0 = kb * C::kBK;
+        const uint32_t lead_full = PAIR ? cluster_addr(&full[stage], 0) : 0u;
+        auto ld2 = [&](void* dst, const CUtensorMap* m, int c0, int c1) {
+          if (PAIR)
+            tma_load_2d_pair(dst, m, lead_full, c0, c1);
+          else
+            tma_load_2d(dst, m, &full[stage], c0, c1);
+        };
+        auto ld3 = [&](void* dst, const CUtensorMap* m, int c0, int c1, int c2) {
+          if (PAIR)
+            tma_load_3d_pair(dst, m, lead_full, c0, c1, c2);
+          else
+            tma_load_3d(dst, m, &full[stage], c0, c1, c2);
+        };
         // ---- A operand
         if (A_SRC == SRC_K_TILE) {
-          if (lane == 0) tma_load_2d(sA, &maps.a, &full[stage], k0, it.p0);
+          if (lane == 0) ld2(sA, &maps.a, k0, it.p0);
         } else if (A_SRC == SRC_K_GATHER) {
           tma_gather4(sA + lane * 512, &maps.a, &full[stage], k0, tok[0], tok[1], tok[2], tok[3]);
         } else if (A_SRC == SRC_MN_TILE) {
           // one 3-D box {64 elements, 64 K-rows, 2 chunks}: chunk-major in smem
-          if (lane == 0) tma_load_3d(sA, &maps.a, &full[stage], 0, it.kbeg + k0, it.m0 / C::kBK);
+          if (lane == 0) ld3(sA, &maps.a, 0, it.kbeg + k0, it.m0 / C::kBK);
         } else if (A_SRC == SRC_MN_GATHER) {
           const int c = lane >> 4, g = lane & 15;
           tma_gather4(sA + c * kChunkBytes + g * 512, &maps.a, &full[stage], it.m0 + 64 * c, cur[0],
@@ -485,15 +579,16 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
         if (B_SRC == SRC_K_TILE) {
           if (lane == 0) {
             if (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_MX) {
+              // gate rows then up rows; a CTA pair splits them between its CTAs
               const int r = it.e * p.b_rows_per_expert + n0;
-              tma_load_2d(sB, &maps.b0, &full[stage], k0, r);
-              tma_load_2d(sB + (BN / 2) * C::kRowBytes, &maps.b1, &full[stage], k0, r);
-            } else {
-              tma_load_2d(sB, &maps.b0, &full[stage], k0, it.e * p.b_rows_per_expert + n0);  // BN rows
+              if (!PAIR || rank == 0) ld2(sB, &maps.b0, k0, r);
+              if (!PAIR || rank == 1) ld2(PAIR ? sB : sB + (BN / 2) * C::kRowBytes, &maps.b1, k0, r);
+            } else {   // BN rows (one half per CTA of a pair)
+              ld2(sB, &maps.b0, k0, it.e * p.b_rows_per_expert + n0 + rank * C::kBRows);
             }
           }
         } else if (B_SRC == SRC_MN_TILE) {
-          if (lane == 0) {  // one 3-D box {64 elements, 64 K-rows, BN/64 chunks}
+          if (lane == 0) {  // one 3-D box {64 elements, 64 K-rows, kBRows/64 chunks}
             int krow = k0;
             const CUtensorMap* m = &maps.b0;
             if (p.b_split > 0 && krow >= p.b_split) {
@@ -501,7 +596,7 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
               krow -= p.b_split;
             }
             const int kr = p.wgrad ? (it.kbeg + k0) : (it.e * p.b_rows_per_expert + krow);
-            tma_load_3d(sB, m, &full[stage], 0, kr, n0 / C::kBK);
+            ld3(sB, m, 0, kr, (n0 + rank * C::kBRows) / C::kBK);
           }
         } else if (B_SRC == SRC_MN_GATHER) {
           const int g = lane & 15;
@@ -525,8 +620,9 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
         }
       }
     }
-    if (!ok && lane == 0) {
-      // drain: wait until every load issued into a stage has landed
+    if (!ok && lane == 0 && (!PAIR || rank == 0)) {
+      // drain: wait until every load issued into a stage has landed (a CTA
+      // pair's loads all complete on the leader's barriers)
       const long long n = fills < C::kStages ? fills : C::kStages;
       int s = stage;
       uint32_t ph = phase;
@@ -540,14 +636,14 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && (!PAIR || rank == 0)) {   // a CTA pair's leader issues for both
       int stage = 0;
       uint32_t phase = 0;
       int abuf = 0;
       uint32_t aphase = 0;
       bool first = true;
-      for (int idx = blockIdx.x; idx < nitems; idx += gridDim.x) {
-        const Item it = get_item(p, idx, C::kBK);
+      for (int idx = item0; idx < nitems; idx += istep) {
+        const Item it = item_at(idx, C::kBK);
         if (it.nk == 0) continue;
         if (!mbar_wait(&tempty[abuf], aphase ^ 1, abort_flag, p.status)) break;
         tc_fence_after();
@@ -572,9 +668,15 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
                                         : smem_desc(a0 + kk * 32, 16, 8 * C::kRowBytes, C::kSwz);
             const uint64_t bd = C::kBMN ? smem_desc(b0 + kk * 16 * C::kRowBytes, C::kMnChunkBytes, 8 * C::kRowBytes, C::kSwz)
                                         : smem_desc(b0 + kk * 32, 16, 8 * C::kRowBytes, C::kSwz);
-            umma_bf16(acc, ad, bd, C::kIdesc, (kb | kk) ? 1u : 0u);
+            if (PAIR)
+              umma_bf16_pair(acc, ad, bd, C::kIdesc, (kb | kk) ? 1u : 0u);
+            else
+              umma_bf16(acc, ad, bd, C::kIdesc, (kb | kk) ? 1u : 0u);
           }
-          umma_commit(&empty[stage]);
+          if (PAIR)
+            umma_commit_pair(&empty[stage], 0x3);
+          else
+            umma_commit(&empty[stage]);
           if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1;
@@ -582,7 +684,12 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
         }
         if (!ok) break;
         const bool drop = (p.debug & 1) && first && blockIdx.x == 0;
-        if (!drop) umma_commit(&tfull[abuf]);
+        if (!drop) {
+          if (PAIR)
+            umma_commit_pair(&tfull[abuf], 0x3);
+          else
+            umma_commit(&tfull[abuf]);
+        }
         first = false;
         if (++abuf == 2) {
           abuf = 0;
@@ -590,7 +697,10 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
         }
       }
       // every MMA issued by this thread must finish before TMEM is released
-      umma_commit(done);
+      if (PAIR)
+        umma_commit_pair(done, 0x1);
+      else
+        umma_commit(done);
       mbar_drain(done, 0);
     }
   } else if (warp >= C::kGatherWarp0) {
@@ -693,13 +803,14 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
     uint8_t* wstage = smem + C::kStages * C::kStageBytes + C::kBarBytes + (warp - 2) * C::kEpiStageBytes;
     int abuf = 0;
     uint32_t aphase = 0;
-    for (int idx = blockIdx.x; idx < nitems; idx += gridDim.x) {
-      const Item it = get_item(p, idx, C::kBK);
+    for (int idx = item0; idx < nitems; idx += istep) {
+      const Item it = item_at(idx, C::kBK);
       const int bn_out = (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_MX) ? BN / 2 : BN;
       const int n0 = it.nt * bn_out;
+      const bool live = !it.empty;   // an empty half of a CTA pair stores nothing
       if (it.nk == 0) {
         // weight gradient of an expert with no rows: zeros
-        if (EPI == EPI_WGRAD) {
+        if (EPI == EPI_WGRAD && live) {
           const int m = it.m0 + r;
           uint16_t* dst = (m < p.split)
                               ? static_cast<uint16_t*>(p.out0) + it.e * p.estride + static_cast<long long>(m) * p.ld
@@ -727,12 +838,12 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
       if constexpr (EPI == EPI_DOWN_BWD) {
         const int prow = it.p0 + r;
         if (p.grouped) {
-          f_bwd = (r < it.rows) ? __ldg(p.row_src + prow) : -1;
+          f_bwd = (live && r < it.rows) ? __ldg(p.row_src + prow) : -1;
           v_bwd = f_bwd >= 0;
-          inb_bwd = true;
+          inb_bwd = live;
           if (v_bwd) wt_bwd = __ldg(p.rw + f_bwd);
         } else {
-          v_bwd = r < it.rows;
+          v_bwd = live && r < it.rows;
           inb_bwd = v_bwd;
         }
         if (v_bwd) {
@@ -754,7 +865,7 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
         // out0 = gu [rows][2N], out1 = h [rows][N] (bf16)
         const int prow = it.p0 + r;
         const bool valid = r < it.rows;
-        const bool inb = p.grouped ? true : valid;
+        const bool inb = (p.grouped ? true : valid) && live;
         uint16_t* gu = inb ? static_cast<uint16_t*>(p.out0) + static_cast<long long>(prow) * 2 * p.N + n0 : nullptr;
         uint16_t* hb = inb ? static_cast<uint16_t*>(p.out1) + static_cast<long long>(prow) * p.N + n0 : nullptr;
 #pragma unroll 1
@@ -780,7 +891,7 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
           warp_store_row64(wv, hb ? hb + c * 32 : nullptr, wstage, lane);
         }
       } else if constexpr (EPI == EPI_SCALE_SCATTER || EPI == EPI_SCATTER) {
-        const int f = (r < it.rows) ? __ldg(p.row_src + it.p0 + r) : -1;
+        const int f = (live && r < it.rows) ? __ldg(p.row_src + it.p0 + r) : -1;
         const float wt = (EPI == EPI_SCALE_SCATTER && f >= 0) ? __ldg(p.rw + f) : 1.f;
         uint16_t* dst = f >= 0 ? static_cast<uint16_t*>(p.out0) + static_cast<long long>(f) * p.ld + n0 : nullptr;
 #pragma unroll 1
@@ -796,8 +907,9 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
         }
       } else if constexpr (EPI == EPI_STORE_ROWS) {
         const int prow = it.p0 + r;
-        uint16_t* dst = (r < it.rows) ? static_cast<uint16_t*>(p.out0) + static_cast<long long>(prow) * p.ld + n0
-                                      : nullptr;
+        uint16_t* dst = (live && r < it.rows)
+                            ? static_cast<uint16_t*>(p.out0) + static_cast<long long>(prow) * p.ld + n0
+                            : nullptr;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           float v[32];
@@ -861,7 +973,8 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
         if (dwp) dwp[C::kEpiWarps == 8 ? epi_half : 1] = dpart;
       } else if constexpr (EPI == EPI_WGRAD) {
         const int m = it.m0 + r;
-        uint16_t* dst = (m < p.split)
+        uint16_t* dst = !live ? nullptr
+                        : (m < p.split)
                             ? static_cast<uint16_t*>(p.out0) + it.e * p.estride + static_cast<long long>(m) * p.ld
                             : static_cast<uint16_t*>(p.out1) + it.e * p.estride +
                                   static_cast<long long>(m - p.split) * p.ld;
@@ -870,12 +983,17 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
           float v[32];
           tmem_ld32(tb + c * 32, v);
           pack_bf16x32(v, wv);
-          warp_store_row64(wv, dst + n0 + c * 32, wstage, lane);
+          warp_store_row64(wv, dst ? dst + n0 + c * 32 : nullptr, wstage, lane);
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[abuf]);
+      if (lane == 0) {   // the accumulator buffer is free again (a pair: on the leader's barrier)
+        if (PAIR && rank != 0)
+          mbar_arrive_cluster(cluster_addr(&tempty[abuf], 0));
+        else
+          mbar_arrive(&tempty[abuf]);
+      }
       if (++abuf == 2) {
         abuf = 0;
         aphase ^= 1;
@@ -884,10 +1002,16 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI>::kThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  if (PAIR)
+    cluster_sync();   // the leader's MMAs into this CTA's TMEM are done before either frees it
+  else
+    __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::kTmemCols);
+    if (PAIR)
+      tmem_dealloc_pair(tmem_base, C::kTmemCols);
+    else
+      tmem_dealloc(tmem_base, C::kTmemCols);
   }
 }
 

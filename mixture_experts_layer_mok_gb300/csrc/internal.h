@@ -8,14 +8,14 @@
 namespace mok {
 
 constexpr int kTileRows = 128;     // rows per expert tile
-constexpr int kSchedChunk = 4096;  // routed rows per schedule block
+constexpr int kSchedChunk = 1024;  // routed rows per schedule block
 
 struct GemmMaps;
 struct GemmParams;
 
 cudaError_t launch_schedule(const int64_t* te, int T, int k, int E, int cap_tiles, int max_tiles,
                             int* hist, int* cnt, int* row0, int* row_src, int* slot_row,
-                            int* tile_expert, int* tile_row0, int* tile_rows, int* header,
+                            int* tile_expert, int* tile_row0, int* tile_rows, int* pair_tile, int* header,
                             cudaStream_t st);
 cudaError_t launch_mx_quantize(const uint16_t* x, long long nblocks, uint8_t* codes, uint8_t* scales,
                                int num_sms, cudaStream_t st);
@@ -33,6 +33,11 @@ cudaError_t launch_dw_reduce(const float* part, int nf, int ntiles, float* dw, c
 // epilogues the layer uses (gemm_fwd.cu, gemm_bwd.cu).
 template <int A_SRC, int B_SRC, int BN, int EPI>
 cudaError_t launch_gemm(const GemmMaps& maps, const GemmParams& p, int grid, cudaStream_t st);
+
+// CTA-pair launch of the same engine (M = 256 per pair, B split between the
+// two CTAs); max_items bounds the pair work items (gemm_pair.cu).
+template <int A_SRC, int B_SRC, int BN, int EPI>
+cudaError_t launch_gemm_pair(const GemmMaps& maps, const GemmParams& p, long long max_items, cudaStream_t st);
 
 // Block-scaled (MXFP8) grouped GEMM launch (gemm_mx.cu).
 template <int BN, int EPI>

@@ -72,6 +72,7 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int n, int E, int nchu
                                                           int* __restrict__ tile_expert,
                                                           int* __restrict__ tile_row0,
                                                           int* __restrict__ tile_rows,
+                                                          int* __restrict__ pair_tile,
                                                           int* __restrict__ header) {
   __shared__ int tmp[32];
   const int e = threadIdx.x;  // E <= 1024: one thread per expert
@@ -81,6 +82,7 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int n, int E, int nchu
       header[0] = 0;
       header[1] = 0;
       header[3] = 0;
+      header[4] = 0;
     }
     return;
   }
@@ -115,6 +117,28 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int n, int E, int nchu
     for (int q = r0 + c; q < r0 + padded; ++q) row_src[q] = -1;
   }
   const int num_tiles = total_prim + total_ovf;
+  // tile pairs for CTA-pair GEMMs: consecutive tiles of one expert within the
+  // primary list, then within the overflow list; an odd tile pairs with none
+  const int pp = (prim + 1) / 2, po = (ntile - prim + 1) / 2;
+  int total_pp, total_po;
+  const int pp_off = block_exclusive_scan(pp, tmp, &total_pp);
+  const int po_off = block_exclusive_scan(po, tmp, &total_po);
+  if (e < E) {
+    for (int j = 0; j < pp; ++j) {
+      pair_tile[2 * (pp_off + j)] = prim_off + 2 * j;
+      pair_tile[2 * (pp_off + j) + 1] = (2 * j + 1 < prim) ? prim_off + 2 * j + 1 : -1;
+    }
+    const int no = ntile - prim;
+    for (int j = 0; j < po; ++j) {
+      pair_tile[2 * (total_pp + po_off + j)] = total_prim + ovf_off + 2 * j;
+      pair_tile[2 * (total_pp + po_off + j) + 1] = (2 * j + 1 < no) ? total_prim + ovf_off + 2 * j + 1 : -1;
+    }
+  }
+  const int num_pairs = total_pp + total_po;
+  for (int i = num_pairs + threadIdx.x; i < max_tiles; i += blockDim.x) {
+    pair_tile[2 * i] = -1;
+    pair_tile[2 * i + 1] = -1;
+  }
   for (int i = num_tiles + threadIdx.x; i < max_tiles; i += blockDim.x) {
     tile_expert[i] = -1;
     tile_row0[i] = -1;
@@ -125,6 +149,7 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int n, int E, int nchu
     header[0] = num_tiles;
     header[1] = total_rows;
     header[3] = total_prim;
+    header[4] = num_pairs;
   }
 }
 
@@ -176,7 +201,7 @@ __global__ void __launch_bounds__(256) sched_scatter_kernel(const int64_t* __res
 
 cudaError_t launch_schedule(const int64_t* te, int T, int k, int E, int cap_tiles, int max_tiles,
                             int* hist, int* cnt, int* row0, int* row_src, int* slot_row,
-                            int* tile_expert, int* tile_row0, int* tile_rows, int* header,
+                            int* tile_expert, int* tile_row0, int* tile_rows, int* pair_tile, int* header,
                             cudaStream_t st) {
   const int n = T * k;
   const int nchunks = (n + kSchedChunk - 1) / kSchedChunk;
@@ -184,7 +209,7 @@ cudaError_t launch_schedule(const int64_t* te, int T, int k, int E, int cap_tile
   if (err != cudaSuccess) return err;
   sched_count_kernel<<<nchunks, 256, E * sizeof(int), st>>>(te, n, E, hist, header);
   sched_scan_kernel<<<1, 1024, 0, st>>>(n, E, nchunks, cap_tiles, max_tiles, hist, cnt, row0, row_src,
-                                        tile_expert, tile_row0, tile_rows, header);
+                                        tile_expert, tile_row0, tile_rows, pair_tile, header);
   const size_t smem = 9 * E * sizeof(int);
   if (smem > 48 * 1024) {
     err = cudaFuncSetAttribute(sched_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

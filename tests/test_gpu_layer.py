@@ -211,6 +211,28 @@ def test_dispatch_paths_agree_bitwise(name, mode):
             assert torch.equal(outs[0][1][key], other[1][key]), key
 
 
+@pytest.mark.parametrize("name", list(SHAPES))
+def test_cta_pairs_match_single_ctas_bitwise(name):
+    """CTA pairs (M = 256 over two SMs, each holding half of B) and single CTAs
+    run every output element's K loop in the same order, so forward and
+    backward must be bit-identical between the two."""
+    m = mok()
+    inp = _inputs(name, seed=9)
+    g = inp.to("cuda")
+    sched = m.schedule(g.top_experts, inp.meta["E"], 0.5)
+    w = weights_of(g, "bf16")
+    outs = []
+    for flags in (0, 4):   # 4 = MOK_DEBUG_NO_CTA_PAIR
+        y, ctx = m.forward(g.x, g.router_w, sched, w, debug=flags)
+        grads = m.backward(g.dy, g.x, g.router_w, sched, ctx, w, debug=flags)
+        torch.cuda.synchronize()
+        assert ctx.status() == 0
+        outs.append((y.clone(), {kk: v.clone() for kk, v in grads.items()}))
+    assert torch.equal(outs[0][0], outs[1][0])
+    for key in outs[0][1]:
+        assert torch.equal(outs[0][1][key], outs[1][1][key]), key
+
+
 def test_fused_forward_permuted_backward_mix():
     """A backward may use another dispatch than its forward (it then makes its
     own copy of x's rows)."""

@@ -22,6 +22,26 @@ def _check_schedule(te, E, c):
     for key in ("cnt", "row0", "row_src", "slot_row", "tile_expert", "tile_row0", "tile_rows"):
         assert np.array_equal(arr[key], ref[key]), key
     assert arr["header"][3] == ref["num_primary"]
+    _check_pairs(arr, ref)
+
+
+def _check_pairs(arr, ref):
+    """The tile pairs of the CTA-pair GEMMs: consecutive tiles of one expert,
+    paired from the start of its run within the primary list, then within the
+    overflow list; each tile in exactly one pair."""
+    nt, npr = ref["num_tiles"], ref["num_primary"]
+    te = ref["tile_expert"]
+    want = []
+    for lo, hi in ((0, npr), (npr, nt)):
+        i = lo
+        while i < hi:
+            j = i + 1 if i + 1 < hi and te[i + 1] == te[i] else -1
+            want.append((i, j))
+            i += 2 if j >= 0 else 1
+    pairs = arr["pair_tile"].reshape(-1, 2)
+    assert arr["header"][4] == len(want)
+    assert [tuple(int(v) for v in p) for p in pairs[:len(want)]] == want
+    assert np.all(pairs[len(want):] == -1)
 
 
 @pytest.mark.parametrize("T,k,E,skew,c", [

@@ -68,7 +68,7 @@ def test_noalloc_schedule_rejects_sizes_beyond_its_scratch():
     from mixture_experts_layer_mok_gb300 import _lib
 
     lib = _lib.load()
-    T, k, E = 300000, 8, 1024            # ceil(T*k/4096) * E = 586 * 1024 > 262144
+    T, k, E = 300000, 8, 1024            # ceil(T*k/1024) * E = 2344 * 1024 > 1048576
     sc = _lib.MokSchedule()
     fake = C.c_void_p(256)               # never touched: the size check comes first
     st = lib.mok_schedule_noalloc(fake, T, k, E, 0.5, fake, 1 << 30, C.byref(sc), None)
