@@ -100,13 +100,16 @@ typedef int mok_status_t;
 #define MOK_NUM_STAGES                    17
 
 /* Per-call knobs ([MoKEd] "Tuning the five hyperparameters before
- * production").  minibatch_size (0 = T) sets the order in which the
- * persistent GEMMs visit work (waves of tokens); it never changes a result
- * bit.  `events`, when not NULL, holds 2 * MOK_NUM_STAGES cudaEvent_t handles
- * (owned by the caller); the call records events[2s] before and
- * events[2s+1] after stage s on the call's stream (a stage that does not run
- * records both back to back), so a caller can time each kernel on the stream
- * it runs on. */
+ * production").  minibatch_size (0 = T) is accepted and checked; on one GPU
+ * the GEMMs visit work expert by expert for every size (there is no exchange
+ * to overlap, and wave order would re-read every expert's weights once per
+ * wave), so it never changes a result bit.  `events`, when not NULL, holds
+ * 2 * MOK_NUM_STAGES cudaEvent_t handles (owned by the caller); the call
+ * records events[2s] before and events[2s+1] after stage s on the stream the
+ * stage runs on (the caller's, or for the dispatch stages the library's side
+ * stream; a stage that does not run records both back to back), so a caller
+ * can time each kernel.  A NULL entry records nothing: each record costs the
+ * device a few microseconds, so a timing run can watch one stage alone. */
 /* How the routed GEMMs receive the token rows of each expert tile (the
  * on-chip form of MoK's dispatch exchange).  Every choice moves the same bytes
  * into the same shared-memory layout, so results are bitwise identical. */

@@ -175,11 +175,11 @@ def _config(mode, minibatch, debug, events=None, dispatch="auto"):
                          num_events=0, events=None)
     if events is not None:
         if len(events) != 2 * _lib.MOK_NUM_STAGES:
-            raise ValueError("events must hold 2 * MOK_NUM_STAGES torch.cuda.Event objects")
+            raise ValueError("events must hold 2 * MOK_NUM_STAGES torch.cuda.Event objects (or None)")
         for e in events:                 # torch creates the CUDA event on first record
-            if not e.cuda_event:
+            if e is not None and not e.cuda_event:
                 e.record()
-        arr = (C.c_void_p * len(events))(*[e.cuda_event for e in events])
+        arr = (C.c_void_p * len(events))(*[None if e is None else e.cuda_event for e in events])
         cfg.num_events = len(events)
         cfg.events = C.cast(arr, C.POINTER(C.c_void_p))
         cfg._keep = arr
@@ -190,7 +190,9 @@ def forward(x, router_w, sched: Schedule, weights: Weights, mode: str = "bf16", 
             debug: int = 0, out=None, ctx_buf=None, stream=None, events=None, dispatch="auto"):
     """y = layer(x); returns (y, Context).  ``mode`` is "bf16" or "mxfp8";
     ``dispatch`` is "auto", "permute" or "fused" (same results, different kernels).
-    ``events``: optional list of 2 * MOK_NUM_STAGES torch.cuda.Event (timing)."""
+    ``events``: optional list of 2 * MOK_NUM_STAGES torch.cuda.Event (timing); a
+    None entry records nothing (each record costs a few microseconds on the
+    device, so a timing run can watch one stage alone)."""
     lib = _lib.load()
     m = _lib.MOK_MODE_MXFP8_FWD if mode == "mxfp8" else _lib.MOK_MODE_BF16
     E, H, I, I_s = weights.dims

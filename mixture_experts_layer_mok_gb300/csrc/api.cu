@@ -318,9 +318,10 @@ GemmParams base_params(const mok_schedule_t* s, int* status, int debug) {
   return p;
 }
 
-// Records the caller's timing event for the start (end = 0) or end of a stage.
+// Records the caller's timing event for the start (end = 0) or end of a stage
+// (a NULL entry: nothing).
 cudaError_t mark(const mok_config_t* cfg, int stage, int end, cudaStream_t st) {
-  if (cfg->events && cfg->num_events >= 2 * MOK_NUM_STAGES)
+  if (cfg->events && cfg->num_events >= 2 * MOK_NUM_STAGES && cfg->events[2 * stage + end])
     return cudaEventRecord(static_cast<cudaEvent_t>(cfg->events[2 * stage + end]), st);
   return cudaSuccess;
 }

@@ -367,7 +367,7 @@ struct GemmCfg {
   static constexpr bool kHasLsu = kALsu || kBLsu;
   // epilogue warps: the SwiGLU backward's epilogue is the heaviest; with no
   // gather warps it gets two warps per TMEM lane quarter (each half the columns)
-  static constexpr int kEpiWarps = (EPI == EPI_DOWN_BWD && !kHasLsu) ? 8 : 4;
+  static constexpr int kEpiWarps = ((EPI == EPI_DOWN_BWD || EPI == EPI_WGRAD) && !kHasLsu) ? 8 : 4;
   static constexpr int kGatherWarp0 = 2 + kEpiWarps;
   static constexpr int kThreads = 64 + 32 * kEpiWarps + (kHasLsu ? 128 : 0);
   // K-block per stage (elements): 64 bf16 = one 128-byte swizzled row.  The
@@ -506,6 +506,10 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI, PAIR>::kThreads
   else
     __syncthreads();
   tc_fence_after();
+  // everything above touches only on-chip state; the inputs below may come
+  // from the kernel launched just before this one
+  griddep_wait();
+  griddep_launch_dependents();
   const uint32_t tmem_base = *tmem_slot;
   const int nitems = PAIR ? num_items_pair(p) : num_items(p);
 
@@ -808,6 +812,12 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI, PAIR>::kThreads
       const int bn_out = (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_MX) ? BN / 2 : BN;
       const int n0 = it.nt * bn_out;
       const bool live = !it.empty;   // an empty half of a CTA pair stores nothing
+      // this warp's 32-column chunks: all of them, or one half when two warps
+      // share a lane quarter
+      constexpr int kChunks = BN / 32;
+      const int epi_half = (warp - 2) >> 2;
+      const int epi_c0 = (C::kEpiWarps == 8) ? epi_half * (kChunks / 2) : 0;
+      const int epi_c1 = (C::kEpiWarps == 8) ? epi_c0 + kChunks / 2 : kChunks;
       if (it.nk == 0) {
         // weight gradient of an expert with no rows: zeros
         if (EPI == EPI_WGRAD && live) {
@@ -819,18 +829,12 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI, PAIR>::kThreads
           uint32_t zw[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) zw[i] = 0u;
-          for (int c = 0; c < BN / 32; ++c) warp_store_row64(zw, dst + n0 + c * 32, wstage, lane);
+          for (int c = epi_c0; c < epi_c1; ++c) warp_store_row64(zw, dst + n0 + c * 32, wstage, lane);
         }
         continue;
       }
       // SwiGLU backward: row state and the first chunk of the saved gate|up,
       // fetched before the accumulator is ready
-      // this warp's 32-column chunks: all of them, or one half when two warps
-      // share a lane quarter
-      constexpr int kChunks = BN / 32;
-      const int epi_half = (warp - 2) >> 2;
-      const int epi_c0 = (C::kEpiWarps == 8) ? epi_half * (kChunks / 2) : 0;
-      const int epi_c1 = (C::kEpiWarps == 8) ? epi_c0 + kChunks / 2 : kChunks;
       int f_bwd = -1;
       bool v_bwd = false, inb_bwd = false;
       float wt_bwd = 1.f;
@@ -979,7 +983,7 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI, PAIR>::kThreads
                             : static_cast<uint16_t*>(p.out1) + it.e * p.estride +
                                   static_cast<long long>(m - p.split) * p.ld;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = epi_c0; c < epi_c1; ++c) {
           float v[32];
           tmem_ld32(tb + c * 32, v);
           pack_bf16x32(v, wv);

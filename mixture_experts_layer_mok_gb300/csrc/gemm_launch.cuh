@@ -7,6 +7,14 @@
 
 namespace mok {
 
+// Every GEMM launch allows programmatic stream serialization: its CTAs may
+// start while the previous kernel on the stream finishes, and wait for it in
+// griddep_wait() before reading any global memory.
+inline void set_dependent_launch(cudaLaunchAttribute* a) {
+  a->id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a->val.programmaticStreamSerializationAllowed = 1;
+}
+
 template <int A_SRC, int B_SRC, int BN, int EPI>
 cudaError_t launch_gemm(const GemmMaps& maps, const GemmParams& p, int grid, cudaStream_t st) {
   using C = GemmCfg<A_SRC, B_SRC, BN, EPI>;
@@ -15,7 +23,17 @@ cudaError_t launch_gemm(const GemmMaps& maps, const GemmParams& p, int grid, cud
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (err != cudaSuccess) return err;
-  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(maps, p);
+  cudaLaunchAttribute attr[1];
+  set_dependent_launch(&attr[0]);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  err = cudaLaunchKernelEx(&cfg, kern, maps, p);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
@@ -32,17 +50,18 @@ cudaError_t launch_gemm_pair(const GemmMaps& maps, const GemmParams& p, long lon
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  set_dependent_launch(&attr[1]);
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 1;   // the occupancy query takes the cluster shape only
   if (resident[dev] == 0) {
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (err != cudaSuccess) return err;
@@ -58,6 +77,7 @@ cudaError_t launch_gemm_pair(const GemmMaps& maps, const GemmParams& p, long lon
   }
   const long long clusters = max_items < resident[dev] ? max_items : resident[dev];
   cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+  cfg.numAttrs = 2;
   err = cudaLaunchKernelEx(&cfg, kern, maps, p);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();

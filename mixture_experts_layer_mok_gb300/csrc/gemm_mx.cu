@@ -1,6 +1,7 @@
 // Block-scaled (MXFP8) grouped-GEMM instantiations for the MXFP8 forward:
 // gate/up + SwiGLU + h requantisation, down + router scale + scatter, dense
 // store (shared expert).
+#include "gemm_launch.cuh"
 #include "gemm_mx.cuh"
 #include "internal.h"
 
@@ -13,7 +14,17 @@ cudaError_t launch_gemm_mx(const GemmMaps& maps, const GemmParams& p, int grid, 
   auto kern = gemm_mx_kernel<BN, EPI>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (err != cudaSuccess) return err;
-  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(maps, p);
+  cudaLaunchAttribute attr[1];
+  set_dependent_launch(&attr[0]);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  err = cudaLaunchKernelEx(&cfg, kern, maps, p);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 

@@ -101,6 +101,10 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI>::kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // everything above touches only on-chip state; the inputs below may come
+  // from the kernel launched just before this one
+  griddep_wait();
+  griddep_launch_dependents();
   const uint32_t tmem_base = *tmem_slot;
   const int nitems = num_items(p);
   constexpr bool kSwiGLU = (EPI == EPI_SWIGLU_MX);

@@ -88,10 +88,23 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int n, int E, int nchu
   }
   int c = 0;
   if (e < E) {
+    // each chunk's count becomes its exclusive offset within expert e; eight
+    // chunks per round so the loads overlap
     int run = 0;
-    for (int k = 0; k < nchunks; ++k) {
+    int k = 0;
+    for (; k + 8 <= nchunks; k += 8) {
+      int v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v[q] = hist[(k + q) * E + e];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        hist[(k + q) * E + e] = run;
+        run += v[q];
+      }
+    }
+    for (; k < nchunks; ++k) {
       const int v = hist[k * E + e];
-      hist[k * E + e] = run;  // becomes the chunk's exclusive offset within expert e
+      hist[k * E + e] = run;
       run += v;
     }
     c = run;
