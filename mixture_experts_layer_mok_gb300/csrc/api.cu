@@ -342,6 +342,8 @@ int resolve_dispatch(const mok_config_t* cfg) {
 }
 
 __global__ void propagate_status_kernel(const int* header, int* status) {
+  griddep_wait();
+  griddep_launch_dependents();
   if (header[2] != 0) atomicCAS(status, 0, header[2]);
 }
 
@@ -739,8 +741,8 @@ mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x, const float
   carve_ctx(ctx_buf, T, k, E, H, I, Is, cfg->mode, ctx, &X);
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_PREP, 0, cs));
   MOK_CUDA(cudaMemsetAsync(ctx->status, 0, 8 * sizeof(int), cs));
-  propagate_status_kernel<<<1, 1, 0, cs>>>(s->header, ctx->status);
-  MOK_CUDA(cudaGetLastError());
+  MOK_CUDA(launch_dependent(propagate_status_kernel, dim3(1), dim3(1), 0, cs, static_cast<const int*>(s->header),
+                            ctx->status));
 
   const long long mr = static_cast<long long>(s->max_tiles) * kTileRows;
   if (mx) {

@@ -13,6 +13,24 @@ constexpr int kSchedChunk = 1024;  // routed rows per schedule block
 struct GemmMaps;
 struct GemmParams;
 
+// Launches `kern` allowing programmatic stream serialization: it may start
+// while the previous kernel on the stream finishes, so it must call
+// griddep_wait() before touching global memory.
+template <typename... P, typename... A>
+cudaError_t launch_dependent(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, A... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 cudaError_t launch_schedule(const int64_t* te, int T, int k, int E, int cap_tiles, int max_tiles,
                             int* hist, int* cnt, int* row0, int* row_src, int* slot_row,
                             int* tile_expert, int* tile_row0, int* tile_rows, int* pair_tile, int* header,

@@ -20,6 +20,8 @@ namespace mok {
 
 __global__ void sched_count_kernel(const int64_t* __restrict__ te, int n, int E,
                                    int* __restrict__ hist, int* __restrict__ header) {
+  griddep_wait();
+  griddep_launch_dependents();
   extern __shared__ int sh_cnt[];
   for (int i = threadIdx.x; i < E; i += blockDim.x) sh_cnt[i] = 0;
   __syncthreads();
@@ -74,6 +76,8 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int n, int E, int nchu
                                                           int* __restrict__ tile_rows,
                                                           int* __restrict__ pair_tile,
                                                           int* __restrict__ header) {
+  griddep_wait();
+  griddep_launch_dependents();
   __shared__ int tmp[32];
   const int e = threadIdx.x;  // E <= 1024: one thread per expert
   const long long max_rows = static_cast<long long>(max_tiles) * kTileRows;
@@ -176,6 +180,8 @@ __global__ void __launch_bounds__(256) sched_scatter_kernel(const int64_t* __res
                                                             int* __restrict__ row_src,
                                                             int* __restrict__ slot_row,
                                                             const int* __restrict__ header) {
+  griddep_wait();
+  griddep_launch_dependents();
   extern __shared__ int sh[];
   int* run = sh;               // [E]
   int* wcnt = sh + E;          // [8][E]
@@ -220,16 +226,21 @@ cudaError_t launch_schedule(const int64_t* te, int T, int k, int E, int cap_tile
   const int nchunks = (n + kSchedChunk - 1) / kSchedChunk;
   cudaError_t err = cudaMemsetAsync(header, 0, 8 * sizeof(int), st);
   if (err != cudaSuccess) return err;
-  sched_count_kernel<<<nchunks, 256, E * sizeof(int), st>>>(te, n, E, hist, header);
-  sched_scan_kernel<<<1, 1024, 0, st>>>(n, E, nchunks, cap_tiles, max_tiles, hist, cnt, row0, row_src,
-                                        tile_expert, tile_row0, tile_rows, pair_tile, header);
+  err = launch_dependent(sched_count_kernel, dim3(nchunks), dim3(256), E * sizeof(int), st, te, n, E, hist, header);
+  if (err != cudaSuccess) return err;
+  err = launch_dependent(sched_scan_kernel, dim3(1), dim3(1024), 0, st, n, E, nchunks, cap_tiles, max_tiles, hist, cnt,
+                         row0, row_src, tile_expert, tile_row0, tile_rows, pair_tile, header);
+  if (err != cudaSuccess) return err;
   const size_t smem = 9 * E * sizeof(int);
   if (smem > 48 * 1024) {
     err = cudaFuncSetAttribute(sched_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(smem));
     if (err != cudaSuccess) return err;
   }
-  sched_scatter_kernel<<<nchunks, 256, smem, st>>>(te, n, E, hist, row0, row_src, slot_row, header);
+  err = launch_dependent(sched_scatter_kernel, dim3(nchunks), dim3(256), smem, st, te, n, E,
+                         static_cast<const int*>(hist), static_cast<const int*>(row0), row_src, slot_row,
+                         static_cast<const int*>(header));
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
@@ -242,6 +253,8 @@ cudaError_t launch_schedule(const int64_t* te, int T, int k, int E, int cap_tile
 __global__ void __launch_bounds__(256) mx_quantize_kernel(const uint16_t* __restrict__ x, long long nblocks,
                                                           uint8_t* __restrict__ codes,
                                                           uint8_t* __restrict__ scales) {
+  griddep_wait();
+  griddep_launch_dependents();
   for (long long b = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; b < nblocks;
        b += static_cast<long long>(gridDim.x) * blockDim.x) {
     float v[32];
@@ -261,7 +274,9 @@ static int grid_for(long long work, int per_block, int num_sms) {
 cudaError_t launch_mx_quantize(const uint16_t* x, long long nblocks, uint8_t* codes, uint8_t* scales,
                                int num_sms, cudaStream_t st) {
   if (nblocks == 0) return cudaSuccess;
-  mx_quantize_kernel<<<grid_for(nblocks, 256, num_sms), 256, 0, st>>>(x, nblocks, codes, scales);
+  cudaError_t err = launch_dependent(mx_quantize_kernel, dim3(grid_for(nblocks, 256, num_sms)), dim3(256), 0, st, x,
+                                     nblocks, codes, scales);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
@@ -279,6 +294,8 @@ __global__ void __launch_bounds__(256) mx_dispatch_kernel(
     const uint16_t* __restrict__ x, int T, int H, int topk, const int* __restrict__ slot_row,
     const int* __restrict__ row_src, const int* __restrict__ header, long long max_rows, uint8_t* __restrict__ xq,
     uint8_t* __restrict__ xq_sc, uint8_t* __restrict__ xp, uint8_t* __restrict__ xp_sc) {
+  griddep_wait();
+  griddep_launch_dependents();
   if (header[2] != 0) return;
   const long long P = header[1];
   const int lane = threadIdx.x & 31;
@@ -345,8 +362,9 @@ cudaError_t launch_mx_dispatch(const uint16_t* x, int T, int H, int topk, const 
                                const int* header, long long max_rows, uint8_t* xq, uint8_t* xq_sc, uint8_t* xp,
                                uint8_t* xp_sc, int num_sms, cudaStream_t st) {
   const long long jobs = T + max_rows + ((static_cast<long long>(T) + 127) / 128 * 128 - T);
-  mx_dispatch_kernel<<<grid_for(jobs * 32, 256, num_sms), 256, 0, st>>>(x, T, H, topk, slot_row, row_src, header,
-                                                                        max_rows, xq, xq_sc, xp, xp_sc);
+  cudaError_t err = launch_dependent(mx_dispatch_kernel, dim3(grid_for(jobs * 32, 256, num_sms)), dim3(256), 0, st, x,
+                                     T, H, topk, slot_row, row_src, header, max_rows, xq, xq_sc, xp, xp_sc);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
@@ -355,6 +373,8 @@ cudaError_t launch_mx_dispatch(const uint16_t* x, int T, int H, int topk, const 
 // memory, coalesced atom writes out of it.
 __global__ void __launch_bounds__(256) mx_tile_scales_kernel(const uint8_t* __restrict__ src, int K,
                                                              uint8_t* __restrict__ dst) {
+  griddep_wait();
+  griddep_launch_dependents();
   __shared__ uint32_t tile[128][17];
   const int cg = K / 128;
   const long long rb = blockIdx.x;
@@ -377,7 +397,8 @@ __global__ void __launch_bounds__(256) mx_tile_scales_kernel(const uint8_t* __re
 cudaError_t launch_mx_tile_scales(const uint8_t* src, long long rows, int K, uint8_t* dst, cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
   const dim3 grid(static_cast<unsigned>(rows / 128), static_cast<unsigned>((K / 128 + 15) / 16));
-  mx_tile_scales_kernel<<<grid, 256, 0, st>>>(src, K, dst);
+  cudaError_t err = launch_dependent(mx_tile_scales_kernel, grid, dim3(256), 0, st, src, K, dst);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
@@ -389,6 +410,8 @@ cudaError_t launch_mx_tile_scales(const uint8_t* src, long long rows, int K, uin
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ slots,
                                                       const uint16_t* __restrict__ base, int T, int k,
                                                       int H, uint16_t* __restrict__ out) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int per_row = H / 8;
   const long long total = static_cast<long long>(T) * per_row;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
@@ -426,7 +449,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
 cudaError_t launch_combine(const uint16_t* slots, const uint16_t* base, int T, int k, int H,
                            uint16_t* out, int num_sms, cudaStream_t st) {
   const long long total = static_cast<long long>(T) * (H / 8);
-  combine_kernel<<<grid_for(total, 256, num_sms), 256, 0, st>>>(slots, base, T, k, H, out);
+  cudaError_t err = launch_dependent(combine_kernel, dim3(grid_for(total, 256, num_sms)), dim3(256), 0, st, slots, base, T,
+                                     k, H, out);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
@@ -440,6 +465,8 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(const uint16_t* __res
                                                            const int* __restrict__ row_src,
                                                            const int* __restrict__ header, long long max_rows,
                                                            uint16_t* __restrict__ out) {
+  griddep_wait();
+  griddep_launch_dependents();
   if (header[2] != 0) return;
   const long long P = header[1];
   const int lane = threadIdx.x & 31;
@@ -460,14 +487,17 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(const uint16_t* __res
 cudaError_t launch_permute_rows(const uint16_t* src, int H, int topk, const int* row_src, const int* header,
                                 long long max_rows, uint16_t* out, int num_sms, cudaStream_t st) {
   if (max_rows == 0) return cudaSuccess;
-  permute_rows_kernel<<<grid_for(max_rows * 32, 256, num_sms), 256, 0, st>>>(src, H, topk, row_src, header,
-                                                                           max_rows, out);
+  cudaError_t err = launch_dependent(permute_rows_kernel, dim3(grid_for(max_rows * 32, 256, num_sms)), dim3(256), 0, st,
+                                     src, H, topk, row_src, header, max_rows, out);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
 // d_w[f] = sum over column tiles n (ascending) of part[f][n].
 __global__ void dw_reduce_kernel(const float* __restrict__ part, int nf, int ntiles,
                                  float* __restrict__ dw) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int f = blockIdx.x * blockDim.x + threadIdx.x;
   if (f >= nf) return;
   float s = 0.f;
@@ -477,7 +507,8 @@ __global__ void dw_reduce_kernel(const float* __restrict__ part, int nf, int nti
 
 cudaError_t launch_dw_reduce(const float* part, int nf, int ntiles, float* dw, cudaStream_t st) {
   if (nf == 0) return cudaSuccess;
-  dw_reduce_kernel<<<(nf + 255) / 256, 256, 0, st>>>(part, nf, ntiles, dw);
+  cudaError_t err = launch_dependent(dw_reduce_kernel, dim3((nf + 255) / 256), dim3(256), 0, st, part, nf, ntiles, dw);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
