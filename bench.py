@@ -60,6 +60,29 @@ FWD_GEMM_STAGES = ("fwd_gateup", "fwd_down", "fwd_shared_gateup", "fwd_shared_do
 LONG_STEP_MS = 20.0   # steps longer than this run the tensor cores under the power cap
 
 
+def dist_env():
+    """(rank, world size, local rank) of this process as torchrun sets them."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(value, world, device):
+    """The largest of every rank's value (the job's time is its slowest rank's)."""
+    if world <= 1:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(T, world, steps, total_ms):
+    """Whole-job throughput: every rank processes its own T tokens per step
+    (weak scaling); total_ms is the slowest rank's time for all steps."""
+    return T * max(world, 1) * steps / (total_ms / 1e3)
+
+
 def launches_per_step(c):
     """Kernels of this library launched by one step (mirrors the C ABI's sequence
     with the default permuted dispatch)."""
@@ -224,9 +247,7 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
 
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    rank, world, local = dist_env()
 
     from mixture_experts_layer_mok_gb300 import inputs as gen
 
@@ -341,12 +362,9 @@ def main():
     total_ms = sum(step_ms)
     if ctx.status() != 0:
         raise RuntimeError(f"device status {ctx.status()} in the timed region")
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / K
-    tokens_per_s = T * max(world, 1) * K / (total_ms / 1e3)
+    tokens_per_s = job_tokens_per_s(T, world, K, total_ms)
     tflops = step_flop * max(world, 1) * K / (total_ms / 1e3) / 1e12
 
     # the dominant GEMM's launches inside the timed region, on their stream
@@ -395,11 +413,8 @@ def main():
                 ee[i - 2].record(stream)
         torch.cuda.synchronize()
         e_ms = sum(es[i].elapsed_time(ee[i]) for i in range(Ke))
-        if world > 1:
-            t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": round(T * max(world, 1) * Ke / (e_ms / 1e3), 1), "unit": "tokens/s",
+        e_ms = max_over_ranks(e_ms, world, dev)
+        e2e = {"value": round(job_tokens_per_s(T, world, Ke, e_ms), 1), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke,
                "what": "pinned host x, router weights, top-k ids, dy -> device; schedule + fwd + bwd through "
                        "the binding; y, dx, d_router_w -> host"}
