@@ -12,6 +12,7 @@
 
 #include "../../include/mok.h"
 #include "gemm.cuh"
+#include "gemm_mx.cuh"
 #include "internal.h"
 
 using namespace mok;
@@ -142,6 +143,22 @@ mok_status_t make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint6
   if (r != CUDA_SUCCESS)
     return fail(MOK_ERR_CUDA, "cuTensorMapEncodeTiled (E4M3) failed (%d) for [%llu x %llu] box %u", (int)r,
                 (unsigned long long)outer, (unsigned long long)inner, box_outer);
+  return MOK_OK;
+}
+
+// E8M0 scales in the tensor-core scale layout as rows of 128 bytes, four per
+// 512-byte atom (box: one atom), for the TMA loads of CTA-pair GEMMs.
+mok_status_t make_map_sf(CUtensorMap* m, const void* base, long long atoms) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(MOK_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(atoms) * 4};
+  const cuuint64_t strides[1] = {128};
+  const cuuint32_t box[2] = {128, 4};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MOK_ERR_CUDA, "cuTensorMapEncodeTiled (scales) failed (%d), %lld atoms", (int)r, atoms);
   return MOK_OK;
 }
 
@@ -549,31 +566,47 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
   MOK_CUDA(cudaStreamWaitEvent(cs, side->join, 0));
 
   const int bn = tile_n(H);
+  // CTA pairs only on request here (MOK_DEBUG_MX_CTA_PAIR): with the
+  // single-buffered accumulator they measured slower than single CTAs
+  const bool mx_pair = (cfg->debug_flags & MOK_DEBUG_MX_CTA_PAIR) != 0;
+  const bool pr = mx_pair && bn == 256;    // the down GEMMs; gate/up tiles are always 256 wide
+  const bool pr_gu = mx_pair;
+  const long long t_atoms = (T + 127) / 128, r_atoms = mr / 128;   // 128-row blocks
   // ---- shared expert
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_GATEUP, 0, cs));
   if (Is > 0) {
-    GemmMaps m;
+    MxMaps m;
     if ((st = make_map_u8(&m.a, ctx->xq, H, T, 128)) || (st = make_map_u8(&m.b0, w->mxs_gate, H, Is, 128)) ||
-        (st = make_map_u8(&m.b1, w->mxs_up, H, Is, 128)))
+        (st = make_map_u8(&m.b1, w->mxs_up, H, Is, 128)) || (st = make_map_sf(&m.sfa, ctx->xq_sc, t_atoms * (H / 128))) ||
+        (st = make_map_sf(&m.sfb0, X.wsg_sc, (Is / 128) * (H / 128))) ||
+        (st = make_map_sf(&m.sfb1, X.wsu_sc, (Is / 128) * (H / 128))))
       return st;
     GemmParams p = base_params(nullptr, ctx->status, 0);
     p.rows = T; p.K = H; p.N = Is; p.n_tiles = Is / 128; p.b_rows_per_expert = 0;
     p.out0 = ctx->gu_s; p.out1 = ctx->hq_s; p.sf_out = ctx->hq_s_sc;
     p.sfa = ctx->xq_sc; p.sfb0 = X.wsg_sc; p.sfb1 = X.wsu_sc;
     const int items = ((T + 127) / 128) * p.n_tiles;
-    MOK_CUDA((launch_gemm_mx<256, EPI_SWIGLU_MX>(m, p, items < sms ? items : sms, cs)));
+    if (pr_gu)
+      MOK_CUDA((launch_gemm_mx_pair<256, EPI_SWIGLU_MX>(m, p, row_pairs(T) * p.n_tiles, cs)));
+    else
+      MOK_CUDA((launch_gemm_mx<256, EPI_SWIGLU_MX>(m, p, items < sms ? items : sms, cs)));
     MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_GATEUP, 1, cs));
     MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_DOWN, 0, cs));
-    GemmMaps m2;
-    if ((st = make_map_u8(&m2.a, ctx->hq_s, Is, T, 128)) || (st = make_map_u8(&m2.b0, w->mxs_down, Is, H, bn)))
+    MxMaps m2;
+    if ((st = make_map_u8(&m2.a, ctx->hq_s, Is, T, 128)) || (st = make_map_u8(&m2.b0, w->mxs_down, Is, H, pr ? 128 : bn)) ||
+        (st = make_map_sf(&m2.sfa, ctx->hq_s_sc, t_atoms * (Is / 128))) ||
+        (st = make_map_sf(&m2.sfb0, X.wsd_sc, (H / 128) * (Is / 128))))
       return st;
     m2.b1 = m2.b0;
+    m2.sfb1 = m2.sfb0;
     GemmParams q = base_params(nullptr, ctx->status, 0);
     q.rows = T; q.K = Is; q.N = H; q.n_tiles = H / bn; q.out0 = ctx->shared_out; q.ld = H;
     q.sfa = ctx->hq_s_sc; q.sfb0 = X.wsd_sc;
     const int items2 = ((T + 127) / 128) * q.n_tiles;
     const int grid2 = items2 < sms ? items2 : sms;
-    if (bn == 256)
+    if (pr)
+      MOK_CUDA((launch_gemm_mx_pair<256, EPI_STORE_ROWS>(m2, q, row_pairs(T) * q.n_tiles, cs)));
+    else if (bn == 256)
       MOK_CUDA((launch_gemm_mx<256, EPI_STORE_ROWS>(m2, q, grid2, cs)));
     else
       MOK_CUDA((launch_gemm_mx<128, EPI_STORE_ROWS>(m2, q, grid2, cs)));
@@ -585,31 +618,42 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
 
   // ---- routed experts
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_GATEUP, 0, cs));
-  GemmMaps m;
+  MxMaps m;
   if ((st = make_map_u8(&m.a, ctx->xq_perm, H, mr, 128)) ||
       (st = make_map_u8(&m.b0, w->mx_gate, H, static_cast<uint64_t>(E) * I, 128)) ||
-      (st = make_map_u8(&m.b1, w->mx_up, H, static_cast<uint64_t>(E) * I, 128)))
+      (st = make_map_u8(&m.b1, w->mx_up, H, static_cast<uint64_t>(E) * I, 128)) ||
+      (st = make_map_sf(&m.sfa, ctx->xq_perm_sc, r_atoms * (H / 128))) ||
+      (st = make_map_sf(&m.sfb0, X.wg_sc, (static_cast<long long>(E) * I / 128) * (H / 128))) ||
+      (st = make_map_sf(&m.sfb1, X.wu_sc, (static_cast<long long>(E) * I / 128) * (H / 128))))
     return st;
   GemmParams p = base_params(s, ctx->status, cfg->debug_flags);
   p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / 128; p.b_rows_per_expert = I;
   p.out0 = ctx->gu; p.out1 = ctx->hq; p.sf_out = ctx->hq_sc;
   p.sfa = ctx->xq_perm_sc; p.sfb0 = X.wg_sc; p.sfb1 = X.wu_sc;
   const long long items = static_cast<long long>(s->max_tiles) * p.n_tiles;
-  MOK_CUDA((launch_gemm_mx<256, EPI_SWIGLU_MX>(m, p, items < sms ? static_cast<int>(items) : sms, cs)));
+  if (pr_gu)
+    MOK_CUDA((launch_gemm_mx_pair<256, EPI_SWIGLU_MX>(m, p, items, cs)));
+  else
+    MOK_CUDA((launch_gemm_mx<256, EPI_SWIGLU_MX>(m, p, items < sms ? static_cast<int>(items) : sms, cs)));
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_GATEUP, 1, cs));
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DOWN, 0, cs));
-  GemmMaps m2;
+  MxMaps m2;
   if ((st = make_map_u8(&m2.a, ctx->hq, I, mr, 128)) ||
-      (st = make_map_u8(&m2.b0, w->mx_down, I, static_cast<uint64_t>(E) * H, bn)))
+      (st = make_map_u8(&m2.b0, w->mx_down, I, static_cast<uint64_t>(E) * H, pr ? 128 : bn)) ||
+      (st = make_map_sf(&m2.sfa, ctx->hq_sc, r_atoms * (I / 128))) ||
+      (st = make_map_sf(&m2.sfb0, X.wd_sc, (static_cast<long long>(E) * H / 128) * (I / 128))))
     return st;
   m2.b1 = m2.b0;
+  m2.sfb1 = m2.sfb0;
   GemmParams q = base_params(s, ctx->status, 0);
   q.grouped = 1; q.K = I; q.N = H; q.n_tiles = H / bn; q.b_rows_per_expert = H;
   q.out0 = ctx->slots; q.ld = H; q.rw = router_w;
   q.sfa = ctx->hq_sc; q.sfb0 = X.wd_sc;
   const long long items2 = static_cast<long long>(s->max_tiles) * q.n_tiles;
   const int grid2 = items2 < sms ? static_cast<int>(items2) : sms;
-  if (bn == 256)
+  if (pr)
+    MOK_CUDA((launch_gemm_mx_pair<256, EPI_SCALE_SCATTER>(m2, q, items2, cs)));
+  else if (bn == 256)
     MOK_CUDA((launch_gemm_mx<256, EPI_SCALE_SCATTER>(m2, q, grid2, cs)));
   else
     MOK_CUDA((launch_gemm_mx<128, EPI_SCALE_SCATTER>(m2, q, grid2, cs)));

@@ -24,13 +24,23 @@
 
 namespace mok {
 
-template <int BN, int EPI>
+// Tensor maps of a block-scaled GEMM: the E4M3 operand tiles and, for CTA
+// pairs, the scale atoms viewed as rows of 128 bytes (4 rows per atom), so
+// that the peer CTA's atoms also complete on the leader's barrier.
+struct MxMaps {
+  CUtensorMap a, b0, b1;
+  CUtensorMap sfa, sfb0, sfb1;
+};
+
+template <int BN, int EPI, bool PAIR = false>
 struct MxCfg {
   static constexpr int kEpiWarps = 8;
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr int kBK = 128;                      // E4M3 elements (= bytes) per stage: one swizzled row
   static constexpr int kABytes = kBM * kBK;
-  static constexpr int kBBytes = BN * kBK;
+  // CTA pair: each CTA holds half of B's rows, and the scales of all of them
+  static constexpr int kBRows = PAIR ? BN / 2 : BN;
+  static constexpr int kBBytes = kBRows * kBK;
   static constexpr int kSfaBytes = 512;                // one scale atom: 128 rows x 4 blocks
   static constexpr int kSfbBytes = (BN / 128) * 512;
   static constexpr int kSfStride = 2048;               // per stage: A atom at 0, B atoms at 512, 1024
@@ -52,16 +62,17 @@ struct MxCfg {
   static_assert(EPI != EPI_SWIGLU_MX || BN == 256, "SwiGLU tile");
   static_assert(kSfCol0 + 16 * kStages <= kTmemCols, "TMEM scale ring");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert(!PAIR || BN == 256, "CTA pairs split a 256-wide B tile");
 };
 
 // Shared-memory descriptor of a 512-byte scale atom as the tcgen05.cp source:
 // 32 rows of 16 bytes, no swizzle, 8-row groups 128 bytes apart.
 __device__ __forceinline__ uint64_t sf_atom_desc(uint32_t saddr) { return smem_desc(saddr, 128, 128, 0); }
 
-template <int BN, int EPI>
-__global__ void __launch_bounds__(MxCfg<BN, EPI>::kThreads, 1)
-    gemm_mx_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
-  using C = MxCfg<BN, EPI>;
+template <int BN, int EPI, bool PAIR = false>
+__global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
+    gemm_mx_kernel(const __grid_constant__ MxMaps maps, const GemmParams p) {
+  using C = MxCfg<BN, EPI, PAIR>;
   static_assert(EPI == EPI_SWIGLU_MX || EPI == EPI_SCALE_SCATTER || EPI == EPI_STORE_ROWS, "epilogue");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -79,6 +90,11 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI>::kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int kgroups = p.K / C::kBK;
+  // CTA pair: rank in the pair, persistent loop over the pair's items
+  const int rank = PAIR ? static_cast<int>(cluster_rank()) : 0;
+  const int item0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int istep = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  auto item_at = [&](int idx) { return PAIR ? get_item_pair(p, idx, C::kBK, rank) : get_item(p, idx, C::kBK); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -86,7 +102,7 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI>::kThreads, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(tfull, 1);
-    mbar_init(tempty, C::kEpiWarps);
+    mbar_init(tempty, (PAIR ? 2 : 1) * C::kEpiWarps);   // the leader's counts both CTAs' warps
     mbar_init(done, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -95,18 +111,26 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI>::kThreads, 1)
     tma_prefetch_desc(&maps.b1);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, C::kTmemCols);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(tmem_slot, C::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, C::kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if (PAIR)
+    cluster_sync();   // both CTAs' barriers initialised before any cross-CTA signal
+  else
+    __syncthreads();
   tc_fence_after();
   // everything above touches only on-chip state; the inputs below may come
   // from the kernel launched just before this one
   griddep_wait();
   griddep_launch_dependents();
   const uint32_t tmem_base = *tmem_slot;
-  const int nitems = num_items(p);
+  const int nitems = PAIR ? num_items_pair(p) : num_items(p);
   constexpr bool kSwiGLU = (EPI == EPI_SWIGLU_MX);
   constexpr int kBnOut = kSwiGLU ? BN / 2 : BN;
 
@@ -117,34 +141,50 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI>::kThreads, 1)
       uint32_t phase = 0;
       long long fills = 0;
       bool ok = true;
-      for (int idx = blockIdx.x; idx < nitems && ok; idx += gridDim.x) {
-        const Item it = get_item(p, idx, C::kBK);
+      for (int idx = item0; idx < nitems && ok; idx += istep) {
+        const Item it = item_at(idx);
         const int n0 = it.nt * kBnOut;
         const long long brow = static_cast<long long>(it.e) * p.b_rows_per_expert + n0;
-        const uint8_t* sfa = p.sfa + ((it.p0 >> 7) * static_cast<long long>(kgroups)) * 512;
-        const uint8_t* sfb0 = p.sfb0 + ((brow >> 7) * static_cast<long long>(kgroups)) * 512;
-        const uint8_t* sfb1 = kSwiGLU ? p.sfb1 + ((brow >> 7) * static_cast<long long>(kgroups)) * 512
-                                      : sfb0 + static_cast<long long>(kgroups) * 512;  // next 128 rows
+        // scale atoms of the item's A rows and B rows (B: gate then up, or two
+        // consecutive 128-row blocks), as atom indices
+        const long long atom_a = (it.p0 >> 7) * static_cast<long long>(kgroups);
+        const long long atom_b0 = (brow >> 7) * static_cast<long long>(kgroups);
+        const long long atom_b1 = kSwiGLU ? atom_b0 : atom_b0 + kgroups;
         for (int kb = 0; kb < it.nk; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], C::kTmaBytes);
+          // CTA pair: both CTAs' loads complete on the leader's barrier
+          if (!PAIR || rank == 0) mbar_arrive_expect_tx(&full[stage], (PAIR ? 2 : 1) * C::kTmaBytes);
           uint8_t* sA = smem + stage * C::kStageBytes;
           uint8_t* sB = sA + C::kABytes;
           uint8_t* sS = sf_smem + stage * C::kSfStride;
           const int k0 = kb * C::kBK;
-          tma_load_2d(sA, &maps.a, &full[stage], k0, it.p0);
-          if (kSwiGLU) {
-            tma_load_2d(sB, &maps.b0, &full[stage], k0, static_cast<int>(brow));
-            tma_load_2d(sB + (BN / 2) * C::kBK, &maps.b1, &full[stage], k0, static_cast<int>(brow));
+          if constexpr (PAIR) {
+            const uint32_t lf = cluster_addr(&full[stage], 0);
+            tma_load_2d_pair(sA, &maps.a, lf, k0, it.p0);
+            if (kSwiGLU)   // the leader holds the gate rows, the peer the up rows
+              tma_load_2d_pair(sB, rank == 0 ? &maps.b0 : &maps.b1, lf, k0, static_cast<int>(brow));
+            else
+              tma_load_2d_pair(sB, &maps.b0, lf, k0, static_cast<int>(brow) + rank * C::kBRows);
+            tma_load_2d_pair(sS, &maps.sfa, lf, 0, static_cast<int>((atom_a + kb) * 4));
+            tma_load_2d_pair(sS + 512, &maps.sfb0, lf, 0, static_cast<int>((atom_b0 + kb) * 4));
+            tma_load_2d_pair(sS + 1024, kSwiGLU ? &maps.sfb1 : &maps.sfb0, lf, 0,
+                             static_cast<int>((atom_b1 + kb) * 4));
           } else {
-            tma_load_2d(sB, &maps.b0, &full[stage], k0, static_cast<int>(brow));
+            tma_load_2d(sA, &maps.a, &full[stage], k0, it.p0);
+            if (kSwiGLU) {
+              tma_load_2d(sB, &maps.b0, &full[stage], k0, static_cast<int>(brow));
+              tma_load_2d(sB + (BN / 2) * C::kBK, &maps.b1, &full[stage], k0, static_cast<int>(brow));
+            } else {
+              tma_load_2d(sB, &maps.b0, &full[stage], k0, static_cast<int>(brow));
+            }
+            bulk_load(sS, p.sfa + (atom_a + kb) * 512, 512, &full[stage]);
+            bulk_load(sS + 512, p.sfb0 + (atom_b0 + kb) * 512, 512, &full[stage]);
+            if (BN == 256)
+              bulk_load(sS + 1024, (kSwiGLU ? p.sfb1 : p.sfb0) + (atom_b1 + kb) * 512, 512, &full[stage]);
           }
-          bulk_load(sS, sfa + kb * 512, 512, &full[stage]);
-          bulk_load(sS + 512, sfb0 + kb * 512, 512, &full[stage]);
-          if (BN == 256) bulk_load(sS + 1024, sfb1 + kb * 512, 512, &full[stage]);
           ++fills;
           if (++stage == C::kStages) {
             stage = 0;
@@ -152,8 +192,9 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI>::kThreads, 1)
           }
         }
       }
-      if (!ok) {
-        // drain: wait until every load issued into a stage has landed
+      if (!ok && (!PAIR || rank == 0)) {
+        // drain: wait until every load issued into a stage has landed (a CTA
+        // pair's loads all complete on the leader's barriers)
         const long long n = fills < C::kStages ? fills : C::kStages;
         int s = stage;
         uint32_t ph = phase;
@@ -168,13 +209,13 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI>::kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && (!PAIR || rank == 0)) {   // a CTA pair's leader issues for both
       int stage = 0;
       uint32_t phase = 0;
       uint32_t aphase = 0;
       bool first = true;
-      for (int idx = blockIdx.x; idx < nitems; idx += gridDim.x) {
-        const Item it = get_item(p, idx, C::kBK);
+      for (int idx = item0; idx < nitems; idx += istep) {
+        const Item it = item_at(idx);
         if (it.nk == 0) continue;
         if (!mbar_wait(tempty, aphase ^ 1, abort_flag, p.status)) break;
         tc_fence_after();
@@ -191,18 +232,31 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI>::kThreads, 1)
           const uint32_t s0 = smem_u32(sf_smem + stage * C::kSfStride);
           const uint32_t sfa_t = tmem_base + C::kSfCol0 + stage * 16;
           const uint32_t sfb_t = sfa_t + 8;
-          // scale atoms -> TMEM (executed in order with the MMAs below)
-          tmem_cp_32x128b_warpx4(sfa_t, sf_atom_desc(s0));
-          tmem_cp_32x128b_warpx4(sfb_t, sf_atom_desc(s0 + 512));
-          if (BN == 256) tmem_cp_32x128b_warpx4(sfb_t + 4, sf_atom_desc(s0 + 1024));
+          // scale atoms -> TMEM (executed in order with the MMAs below; a pair's
+          // copy moves each CTA's atoms into its own TMEM)
+          if (PAIR) {
+            tmem_cp_32x128b_warpx4_pair(sfa_t, sf_atom_desc(s0));
+            tmem_cp_32x128b_warpx4_pair(sfb_t, sf_atom_desc(s0 + 512));
+            tmem_cp_32x128b_warpx4_pair(sfb_t + 4, sf_atom_desc(s0 + 1024));
+          } else {
+            tmem_cp_32x128b_warpx4(sfa_t, sf_atom_desc(s0));
+            tmem_cp_32x128b_warpx4(sfb_t, sf_atom_desc(s0 + 512));
+            if (BN == 256) tmem_cp_32x128b_warpx4(sfb_t + 4, sf_atom_desc(s0 + 1024));
+          }
 #pragma unroll
           for (int kk = 0; kk < C::kBK / 32; ++kk) {
             // K-major 128-byte swizzled rows: 32 E4M3 elements = 32 bytes per step
             const uint64_t ad = smem_desc(a0 + kk * 32, 16, 8 * C::kBK, 2);
             const uint64_t bd = smem_desc(b0 + kk * 32, 16, 8 * C::kBK, 2);
-            umma_mxf8(acc, ad, bd, idesc_mxf8(kBM, BN, kk, kk), sfa_t, sfb_t, (kb | kk) ? 1u : 0u);
+            if (PAIR)
+              umma_mxf8_pair(acc, ad, bd, idesc_mxf8(2 * kBM, BN, kk, kk), sfa_t, sfb_t, (kb | kk) ? 1u : 0u);
+            else
+              umma_mxf8(acc, ad, bd, idesc_mxf8(kBM, BN, kk, kk), sfa_t, sfb_t, (kb | kk) ? 1u : 0u);
           }
-          umma_commit(&empty[stage]);
+          if (PAIR)
+            umma_commit_pair(&empty[stage], 0x3);
+          else
+            umma_commit(&empty[stage]);
           if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1;
@@ -210,12 +264,20 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI>::kThreads, 1)
         }
         if (!ok) break;
         const bool drop = (p.debug & 1) && first && blockIdx.x == 0;
-        if (!drop) umma_commit(tfull);
+        if (!drop) {
+          if (PAIR)
+            umma_commit_pair(tfull, 0x3);
+          else
+            umma_commit(tfull);
+        }
         first = false;
         aphase ^= 1;
       }
       // every MMA issued by this thread must finish before TMEM is released
-      umma_commit(done);
+      if (PAIR)
+        umma_commit_pair(done, 0x1);
+      else
+        umma_commit(done);
       mbar_drain(done, 0);
     }
   } else {
@@ -226,12 +288,13 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI>::kThreads, 1)
     uint8_t* wstage = sf_smem + C::kStages * C::kSfStride + C::kBarBytes + (warp - 2) * C::kEpiStageBytes;
     uint32_t aphase = 0;
     constexpr int kCols = BN / 2;          // accumulator columns per thread
-    for (int idx = blockIdx.x; idx < nitems; idx += gridDim.x) {
-      const Item it = get_item(p, idx, C::kBK);
+    for (int idx = item0; idx < nitems; idx += istep) {
+      const Item it = item_at(idx);
       if (it.nk == 0) continue;
       const int n0 = it.nt * kBnOut;
       const int prow = it.p0 + r;
-      const bool valid = r < it.rows;
+      const bool live = !it.empty;     // an empty half of a CTA pair stores nothing
+      const bool valid = live && r < it.rows;
       int f = -1;
       float wt = 1.f;
       if (EPI == EPI_SCALE_SCATTER && valid) {
@@ -257,14 +320,19 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI>::kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty);
+      if (lane == 0) {   // TMEM is free again (a pair: on the leader's barrier)
+        if (PAIR && rank != 0)
+          mbar_arrive_cluster(cluster_addr(tempty, 0));
+        else
+          mbar_arrive(tempty);
+      }
       aphase ^= 1;
 
       uint32_t wv[16];
       if constexpr (EPI == EPI_SWIGLU_MX) {
         // out0 = gu [rows][2N] (bf16), out1 = h codes [rows][N], sf_out = h scales
         constexpr int kH = kCols / 2;        // h columns of this thread
-        const bool inb = p.grouped ? true : valid;
+        const bool inb = (p.grouped ? true : valid) && live;
         const int col0 = n0 + half * kH;
         float* g = v;
         float* u = v + kH;
@@ -301,11 +369,14 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI>::kThreads, 1)
           }
         }
         // the scales of this thread's blocks are adjacent bytes of its row's word
-        uint8_t* sdst = p.sf_out + mx_tiled_scale_offset(prow, col0 / 32, p.N / 128);
-        if (kH == 64) {
-          *reinterpret_cast<uint16_t*>(sdst) = static_cast<uint16_t>(sc);
-        } else {
-          *sdst = static_cast<uint8_t>(sc);
+        // (rows past the end of a dense layer get the unit scales of zeros)
+        if (live) {
+          uint8_t* sdst = p.sf_out + mx_tiled_scale_offset(prow, col0 / 32, p.N / 128);
+          if (kH == 64) {
+            *reinterpret_cast<uint16_t*>(sdst) = static_cast<uint16_t>(sc);
+          } else {
+            *sdst = static_cast<uint8_t>(sc);
+          }
         }
       } else {
         uint16_t* dst = nullptr;
@@ -328,10 +399,16 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI>::kThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  if (PAIR)
+    cluster_sync();   // the leader's MMAs into this CTA's TMEM are done before either frees it
+  else
+    __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::kTmemCols);
+    if (PAIR)
+      tmem_dealloc_pair(tmem_base, C::kTmemCols);
+    else
+      tmem_dealloc(tmem_base, C::kTmemCols);
   }
 }
 

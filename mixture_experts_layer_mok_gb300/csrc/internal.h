@@ -57,8 +57,12 @@ cudaError_t launch_gemm(const GemmMaps& maps, const GemmParams& p, int grid, cud
 template <int A_SRC, int B_SRC, int BN, int EPI>
 cudaError_t launch_gemm_pair(const GemmMaps& maps, const GemmParams& p, long long max_items, cudaStream_t st);
 
-// Block-scaled (MXFP8) grouped GEMM launch (gemm_mx.cu).
+// Block-scaled (MXFP8) grouped GEMM launches (gemm_mx.cu): single CTAs and
+// CTA pairs.
+struct MxMaps;
 template <int BN, int EPI>
-cudaError_t launch_gemm_mx(const GemmMaps& maps, const GemmParams& p, int grid, cudaStream_t st);
+cudaError_t launch_gemm_mx(const MxMaps& maps, const GemmParams& p, int grid, cudaStream_t st);
+template <int BN, int EPI>
+cudaError_t launch_gemm_mx_pair(const MxMaps& maps, const GemmParams& p, long long max_items, cudaStream_t st);
 
 }  // namespace mok

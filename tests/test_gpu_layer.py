@@ -211,19 +211,21 @@ def test_dispatch_paths_agree_bitwise(name, mode):
             assert torch.equal(outs[0][1][key], other[1][key]), key
 
 
-@pytest.mark.parametrize("name", list(SHAPES))
-def test_cta_pairs_match_single_ctas_bitwise(name):
+@pytest.mark.parametrize("name,mode", [(n, "bf16") for n in SHAPES] + [(n, "mxfp8") for n in SHAPES])
+def test_cta_pairs_match_single_ctas_bitwise(name, mode):
     """CTA pairs (M = 256 over two SMs, each holding half of B) and single CTAs
     run every output element's K loop in the same order, so forward and
-    backward must be bit-identical between the two."""
+    backward must be bit-identical between the two (bf16 GEMMs: pairs by
+    default, 4 = MOK_DEBUG_NO_CTA_PAIR; block-scaled GEMMs: single CTAs by
+    default, 8 = MOK_DEBUG_MX_CTA_PAIR)."""
     m = mok()
     inp = _inputs(name, seed=9)
     g = inp.to("cuda")
     sched = m.schedule(g.top_experts, inp.meta["E"], 0.5)
-    w = weights_of(g, "bf16")
+    w = weights_of(g, mode)
     outs = []
-    for flags in (0, 4):   # 4 = MOK_DEBUG_NO_CTA_PAIR
-        y, ctx = m.forward(g.x, g.router_w, sched, w, debug=flags)
+    for flags in ((0, 4) if mode == "bf16" else (0, 8)):
+        y, ctx = m.forward(g.x, g.router_w, sched, w, mode=mode, debug=flags)
         grads = m.backward(g.dy, g.x, g.router_w, sched, ctx, w, debug=flags)
         torch.cuda.synchronize()
         assert ctx.status() == 0
