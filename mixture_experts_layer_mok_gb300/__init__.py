@@ -89,6 +89,7 @@ class Weights:
         _need(self.w_up, torch.bfloat16, (E, I, H), "w_up")
         _need(self.w_down, torch.bfloat16, (E, H, I), "w_down")
         if I_s:
+            _need(self.ws_gate, torch.bfloat16, (I_s, H), "ws_gate")
             _need(self.ws_up, torch.bfloat16, (I_s, H), "ws_up")
             _need(self.ws_down, torch.bfloat16, (H, I_s), "ws_down")
         w = _lib.MokWeights(E=E, H=H, I=I, I_s=I_s)

@@ -94,3 +94,18 @@ def test_package_import_does_not_load_library():
             "from mixture_experts_layer_mok_gb300 import _lib; print(_lib._lib is None)") % ROOT
     out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, check=True)
     assert out.stdout.strip() == "True"
+
+
+def test_autograd_layer_needs_cuda_tensors():
+    """The autograd module is argument marshalling only: on CPU tensors it
+    refuses (there is no CPU path) before touching the library."""
+    import torch
+
+    from mixture_experts_layer_mok_gb300.autograd import MoKLayer
+
+    layer = MoKLayer(4, 128, 128, 0)
+    assert tuple(layer.w_gate.shape) == (4, 128, 128) and tuple(layer.w_down.shape) == (4, 128, 128)
+    assert layer.ws_gate is None
+    x = torch.zeros(8, 128, dtype=torch.bfloat16)
+    with pytest.raises((ValueError, RuntimeError)):
+        layer(x, torch.full((8, 2), 0.5), torch.zeros(8, 2, dtype=torch.int64))
