@@ -255,23 +255,37 @@ def _f64(a):
     return np.asarray(a, dtype=np.float64)
 
 
-def _expert(v, wg, wu, wd):
-    """F(v) = W_down (silu(W_gate v) * (W_up v)) for a batch of rows v [n, H].
-    Returns (output [n, H], g [n, I], u [n, I], h [n, I])."""
+def clamp_gate_up(g, u, limit):
+    """The ``swiglu_limit`` of [MoKDoc] _MoKRuntime (named there, not
+    defined), read as the usual clamped SwiGLU: with limit > 0 the gate
+    pre-activation is clamped from above at limit and the up pre-activation
+    to [-limit, limit] before the SwiGLU; limit <= 0 (the default) leaves
+    both as they are."""
+    if not limit or limit <= 0:
+        return g, u
+    return np.minimum(g, limit), np.clip(u, -limit, limit)
+
+
+def _expert(v, wg, wu, wd, limit=0.0):
+    """F(v) = W_down (silu(W_gate v) * (W_up v)) for a batch of rows v [n, H]
+    (gate/up clamped by ``clamp_gate_up``).  Returns (output [n, H], g [n, I],
+    u [n, I], h [n, I])."""
     g = v @ wg.T
     u = v @ wu.T
-    h = silu(g) * u
+    gc, uc = clamp_gate_up(g, u, limit)
+    h = silu(gc) * uc
     return h @ wd.T, g, u, h
 
 
 def layer_forward(x, router_w, top_experts, w_gate, w_up, w_down,
-                  ws_gate=None, ws_up=None, ws_down=None):
+                  ws_gate=None, ws_up=None, ws_down=None, swiglu_limit=0.0):
     """y[t] = S(x[t]) + sum_j w[t,j] * F_{e[t,j]}(x[t])   (float64).
 
     Shapes ([MoKDoc] _MoKAutogradFunction.forward): x [T, H]; router_w [T, k]
     float32; top_experts [T, k] int64; routed gate/up [E, I, H], down
     [E, H, I]; shared gate/up [I_s, H], down [H, I_s] (absent -> no shared
-    expert).  No expert bias ([MoKDoc] down_proj_bias).
+    expert).  No expert bias ([MoKDoc] down_proj_bias).  ``swiglu_limit``:
+    see ``clamp_gate_up`` (routed and shared experts alike).
     """
     x, w = _f64(x), _f64(router_w)
     wg, wu, wd = _f64(w_gate), _f64(w_up), _f64(w_down)
@@ -281,18 +295,18 @@ def layer_forward(x, router_w, top_experts, w_gate, w_up, w_down,
     E = wg.shape[0]
     y = np.zeros((T, H))
     if ws_gate is not None:
-        y += _expert(x, _f64(ws_gate), _f64(ws_up), _f64(ws_down))[0]
+        y += _expert(x, _f64(ws_gate), _f64(ws_up), _f64(ws_down), swiglu_limit)[0]
     for e in range(E):
         t_idx, j_idx = np.nonzero(te == e)
         if t_idx.size == 0:
             continue
-        o = _expert(x[t_idx], wg[e], wu[e], wd[e])[0]
+        o = _expert(x[t_idx], wg[e], wu[e], wd[e], swiglu_limit)[0]
         np.add.at(y, t_idx, w[t_idx, j_idx][:, None] * o)
     return y
 
 
 def layer_backward(x, router_w, top_experts, w_gate, w_up, w_down, dy,
-                   ws_gate=None, ws_up=None, ws_down=None, gu_override=None):
+                   ws_gate=None, ws_up=None, ws_down=None, gu_override=None, swiglu_limit=0.0):
     """Exact gradients of ``layer_forward`` given dL/dy = dy (float64).
 
     Returns dict: dx [T,H], d_router_w [T,k], d_w_gate/d_w_up [E,I,H],
@@ -303,6 +317,9 @@ def layer_backward(x, router_w, top_experts, w_gate, w_up, w_down, dy,
     ``gu_override`` (used by the MXFP8 straight-through backward) supplies the
     gate/up pre-activations to evaluate the derivative at: a callable
     (expert or None, v) -> (g, u).
+    With ``swiglu_limit`` > 0 the clamp of ``clamp_gate_up`` is
+    differentiated as the clamp itself: the gate gradient passes where
+    g <= limit, the up gradient where |u| <= limit (the bounds included).
     """
     x, w, dy = _f64(x), _f64(router_w), _f64(dy)
     wg, wu, wd = _f64(w_gate), _f64(w_up), _f64(w_down)
@@ -320,14 +337,18 @@ def layer_backward(x, router_w, top_experts, w_gate, w_up, w_down, dy,
             g, u = v @ Wg.T, v @ Wu.T
         else:
             g, u = gu_override(e, v)
-        sg = sigmoid(g)
-        h = g * sg * u
+        gc, uc = clamp_gate_up(g, u, swiglu_limit)
+        sg = sigmoid(gc)
+        h = gc * sg * uc
         o = h @ Wd.T
         d_scale = np.sum(dyv * o, axis=1)            # <dy, F(x)>
         dh = scale[:, None] * (dyv @ Wd)              # w * W_down^T dy
         dWd = (scale[:, None] * dyv).T @ h            # dy (w h)^T
-        dg = dh * u * sg * (1.0 + g * (1.0 - sg))     # silu'(g) = s (1 + g (1 - s))
-        du = dh * g * sg
+        dg = dh * uc * sg * (1.0 + gc * (1.0 - sg))   # silu'(g) = s (1 + g (1 - s))
+        du = dh * gc * sg
+        if swiglu_limit and swiglu_limit > 0:         # the clamp's own derivative
+            dg = dg * (g <= swiglu_limit)
+            du = du * (np.abs(u) <= swiglu_limit)
         dWg = dg.T @ v
         dWu = du.T @ v
         dv = dg @ Wg + du @ Wu
@@ -355,7 +376,7 @@ def layer_backward(x, router_w, top_experts, w_gate, w_up, w_down, dy,
 
 
 def layer_forward_mxfp8(x, router_w, top_experts, w_gate, w_up, w_down,
-                        ws_gate=None, ws_up=None, ws_down=None):
+                        ws_gate=None, ws_up=None, ws_down=None, swiglu_limit=0.0):
     """MXFP8 forward with the quantisation the MXFP8 configurations define:
     x (along H), every weight (along its K axis: H for gate/up, I for down)
     and the intermediate activation h (along I) are quantised to E4M3 with one
@@ -373,6 +394,7 @@ def layer_forward_mxfp8(x, router_w, top_experts, w_gate, w_up, w_down,
     def expert_q(v, Wg, Wu, Wd):
         g = v @ mxfp8_roundtrip(Wg).T
         u = v @ mxfp8_roundtrip(Wu).T
+        g, u = clamp_gate_up(g, u, swiglu_limit)
         h = mxfp8_roundtrip(silu(g) * u)
         return h @ mxfp8_roundtrip(Wd).T
 
@@ -389,7 +411,7 @@ def layer_forward_mxfp8(x, router_w, top_experts, w_gate, w_up, w_down,
 
 
 def layer_backward_mxfp8(x, router_w, top_experts, w_gate, w_up, w_down, dy,
-                         ws_gate=None, ws_up=None, ws_down=None):
+                         ws_gate=None, ws_up=None, ws_down=None, swiglu_limit=0.0):
     """Backward of the MXFP8 forward in BF16 weights, straight-through: the
     derivative treats every quantiser as the identity and is evaluated at the
     gate/up pre-activations g, u that the quantised forward produced.
@@ -414,4 +436,4 @@ def layer_backward_mxfp8(x, router_w, top_experts, w_gate, w_up, w_down, dy,
 
     del xq
     return layer_backward(x, router_w, top_experts, w_gate, w_up, w_down, dy,
-                          ws_gate, ws_up, ws_down, gu_override=gu)
+                          ws_gate, ws_up, ws_down, gu_override=gu, swiglu_limit=swiglu_limit)

@@ -403,3 +403,120 @@ def test_mxfp8_forward_close_to_unquantised():
     b = O.layer_forward(*_args(inp))
     rel = np.linalg.norm(a - b) / np.linalg.norm(b)
     assert 1e-3 < rel < 0.1
+
+
+# ------------------------------------------------------------------ swiglu_limit
+
+def _gate_up_values(inp):
+    """Every gate and |up| pre-activation value the layer forms (test helper
+    for choosing a clamp limit away from all of them)."""
+    x = inp.x.double().numpy()
+    vals = []
+    te = inp.top_experts.numpy()
+    for t in range(x.shape[0]):
+        for e in te[t]:
+            vals += list(inp.w_gate[e].double().numpy() @ x[t])
+            vals += list(np.abs(inp.w_up[e].double().numpy() @ x[t]))
+    if inp.ws_gate is not None:
+        vals += list((x @ inp.ws_gate.double().numpy().T).ravel())
+        vals += list(np.abs(x @ inp.ws_up.double().numpy().T).ravel())
+    return np.sort(np.asarray(vals))
+
+
+def _limit_between(vals, lo_q=0.6, hi_q=0.9):
+    """A limit in the widest gap between consecutive values of the given
+    quantile range, and the distance to the nearest value."""
+    a = vals[int(lo_q * len(vals)):int(hi_q * len(vals))]
+    i = int(np.argmax(np.diff(a)))
+    return 0.5 * (a[i] + a[i + 1]), 0.5 * (a[i + 1] - a[i])
+
+
+def test_swiglu_limit_off_and_huge_equal_the_plain_layer():
+    inp = _tiny(T=12, H=32, I=32, E=4, k=2, I_s=16, seed=21)
+    a = _args(inp)
+    y0 = O.layer_forward(*a)
+    assert np.array_equal(O.layer_forward(*a, swiglu_limit=0.0), y0)
+    assert np.array_equal(O.layer_forward(*a, swiglu_limit=1e30), y0)
+    g0 = O.layer_backward(*a[:6], inp.dy, *a[6:])
+    g1 = O.layer_backward(*a[:6], inp.dy, *a[6:], swiglu_limit=1e30)
+    for key in g0:
+        assert np.array_equal(g0[key], g1[key]), key
+
+
+def test_swiglu_limit_matches_per_token_scalar_loop():
+    """With a limit that clamps a good share of the pre-activations, the layer
+    equals a per-token loop in plain Python floats, the clamp written as
+    comparisons."""
+    inp = _tiny(T=6, H=16, I=12, E=3, k=2, I_s=8, seed=22)
+    vals = _gate_up_values(inp)
+    L = float(np.quantile(vals, 0.7))
+    y = O.layer_forward(*_args(inp), swiglu_limit=L)
+    x = inp.x.double().tolist()
+    rw = inp.router_w.double().tolist()
+    te = inp.top_experts.tolist()
+    clamped = 0
+
+    def expert(v, wg, wu, wd, scale, acc):
+        nonlocal clamped
+        for i in range(len(wg)):
+            g = sum(a * b for a, b in zip(v, wg[i]))
+            u = sum(a * b for a, b in zip(v, wu[i]))
+            if g > L:
+                g, clamped = L, clamped + 1
+            if u > L:
+                u, clamped = L, clamped + 1
+            elif u < -L:
+                u, clamped = -L, clamped + 1
+            h = g / (1.0 + math.exp(-g)) * u
+            for r in range(len(acc)):
+                acc[r] += scale * wd[r][i] * h
+
+    sg, su, sd = (a.double().tolist() for a in (inp.ws_gate, inp.ws_up, inp.ws_down))
+    for t in range(6):
+        acc = [0.0] * 16
+        expert(x[t], sg, su, sd, 1.0, acc)
+        for j in range(2):
+            e = te[t][j]
+            expert(x[t], inp.w_gate[e].double().tolist(), inp.w_up[e].double().tolist(),
+                   inp.w_down[e].double().tolist(), rw[t][j], acc)
+        np.testing.assert_allclose(y[t], acc, rtol=1e-12, atol=1e-14)
+    assert clamped > 20
+
+
+@pytest.mark.parametrize("shared", [False, True])
+def test_swiglu_limit_backward_matches_finite_differences(shared):
+    """Central differences of the clamped layer, with the limit placed between
+    pre-activation values (so no perturbation crosses a clamp kink): the
+    analytic gradients, masked where the clamp holds, must match."""
+    inp = _tiny(T=6, H=32, I=32, E=4, k=2, I_s=16 if shared else 0, seed=23)
+    vals = _gate_up_values(inp)
+    L, margin = _limit_between(vals)
+    assert margin > 1e-4 and np.mean(vals > L) > 0.05     # the clamp is active somewhere
+    dy = inp.dy.double().numpy()
+    a = _args(inp)
+    g = O.layer_backward(*a[:6], inp.dy, *a[6:], swiglu_limit=L)
+    arrays = [v.double().numpy() if v is not None and v.dtype != torch.int64 else
+              (v.numpy() if v is not None else None) for v in a]
+    rng = np.random.default_rng(1)
+    names = {0: "dx", 1: "d_router_w", 3: "d_w_gate", 4: "d_w_up", 5: "d_w_down",
+             6: "d_ws_gate", 7: "d_ws_up", 8: "d_ws_down"}
+    eps = 1e-6
+
+    def loss(arrs):
+        return float(np.sum(O.layer_forward(*arrs, swiglu_limit=L) * dy))
+
+    for idx, key in names.items():
+        if arrays[idx] is None:
+            continue
+        for _ in range(8):
+            pos = tuple(rng.integers(0, s) for s in arrays[idx].shape)
+            plus = [v.copy() if isinstance(v, np.ndarray) else v for v in arrays]
+            minus = [v.copy() if isinstance(v, np.ndarray) else v for v in arrays]
+            plus[idx][pos] += eps
+            minus[idx][pos] -= eps
+            fd = (loss(plus) - loss(minus)) / (2 * eps)
+            an = g[key][pos]
+            assert abs(fd - an) <= 1e-6 * max(1.0, abs(fd)), (key, pos, fd, an)
+    # the mask matters: the unclamped gradients differ
+    g_plain = O.layer_backward(*a[:6], inp.dy, *a[6:])
+    assert not np.allclose(g_plain["dx"], g["dx"])
