@@ -134,6 +134,15 @@ typedef struct {
   int dispatch;        /* MOK_DISPATCH_* */
   int num_events;      /* 0, or 2 * MOK_NUM_STAGES when events is set */
   void* const* events; /* optional cudaEvent_t[2 * MOK_NUM_STAGES], NULL = off */
+  float swiglu_limit;  /* forward: 0 = plain SwiGLU; L > 0 clamps the gate
+                          pre-activation to <= L and the up pre-activation to
+                          [-L, L] before the SwiGLU ([MoKDoc] _MoKRuntime names
+                          swiglu_limit without defining it; this is the usual
+                          clamped SwiGLU).  The backward takes the value the
+                          forward recorded in the context and differentiates
+                          the clamp (gate gradient where G <= L, up gradient
+                          where |U| <= L).  Negative or non-finite:
+                          MOK_ERR_INVALID_ARG. */
 } mok_config_t;
 
 /* The dispatch/combine schedule ([MoKEd] "The two API layers and the
@@ -202,6 +211,7 @@ typedef struct {
   int dispatch;       /* the dispatch the forward used */
   uint8_t*  xq_perm;  /* [max_tiles*128][H] x codes in schedule order, MXFP8 mode (scratch) */
   uint8_t*  xq_perm_sc; /* their scales, tensor-core scale layout */
+  float swiglu_limit; /* the forward's mok_config_t.swiglu_limit */
 } mok_ctx_t;
 /* Tensor-core scale layout (MXFP8 context scratch): the E8M0 scales of a
  * [R][K] code tensor as 512-byte atoms, one per (128-row block rb, 128-column

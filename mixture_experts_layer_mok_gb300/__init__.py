@@ -171,9 +171,9 @@ def quantize_weights(w: Weights, stream=None) -> Weights:
     return Weights(w.w_gate, w.w_up, w.w_down, w.ws_gate, w.ws_up, w.ws_down, mx)
 
 
-def _config(mode, minibatch, debug, events=None, dispatch="auto"):
+def _config(mode, minibatch, debug, events=None, dispatch="auto", swiglu_limit=0.0):
     cfg = _lib.MokConfig(mode=mode, minibatch_size=minibatch, debug_flags=debug, dispatch=_lib.DISPATCH[dispatch],
-                         num_events=0, events=None)
+                         num_events=0, events=None, swiglu_limit=float(swiglu_limit))
     if events is not None:
         if len(events) != 2 * _lib.MOK_NUM_STAGES:
             raise ValueError("events must hold 2 * MOK_NUM_STAGES torch.cuda.Event objects (or None)")
@@ -188,9 +188,12 @@ def _config(mode, minibatch, debug, events=None, dispatch="auto"):
 
 
 def forward(x, router_w, sched: Schedule, weights: Weights, mode: str = "bf16", minibatch: int = 0,
-            debug: int = 0, out=None, ctx_buf=None, stream=None, events=None, dispatch="auto"):
+            debug: int = 0, out=None, ctx_buf=None, stream=None, events=None, dispatch="auto",
+            swiglu_limit: float = 0.0):
     """y = layer(x); returns (y, Context).  ``mode`` is "bf16" or "mxfp8";
     ``dispatch`` is "auto", "permute" or "fused" (same results, different kernels).
+    ``swiglu_limit`` > 0 clamps the SwiGLU pre-activations (gate to <= L, up
+    to [-L, L]); the backward follows the forward's value.
     ``events``: optional list of 2 * MOK_NUM_STAGES torch.cuda.Event (timing); a
     None entry records nothing (each record costs a few microseconds on the
     device, so a timing run can watch one stage alone)."""
@@ -208,7 +211,7 @@ def forward(x, router_w, sched: Schedule, weights: Weights, mode: str = "bf16", 
         ctx_buf = torch.empty(nbytes, dtype=torch.uint8, device=x.device)
     y = out if out is not None else torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
     c = _lib.MokCtx()
-    cfg = _config(m, minibatch, debug, events, dispatch)
+    cfg = _config(m, minibatch, debug, events, dispatch, swiglu_limit)
     _lib.check(lib.mok_forward(C.byref(cfg), _ptr(x), _ptr(router_w), C.byref(sched.c), C.byref(ws), _ptr(y),
                                _ptr(ctx_buf), ctx_buf.numel(), C.byref(c), _stream(stream)), "mok_forward")
     return y, Context(ctx_buf, c, m)

@@ -40,7 +40,8 @@ STAGE_NAMES = ["fwd_prep", "fwd_shared_gateup", "fwd_shared_down", "fwd_gateup",
 
 class MokConfig(C.Structure):
     _fields_ = [("mode", C.c_int), ("minibatch_size", C.c_int), ("debug_flags", C.c_int),
-                ("dispatch", C.c_int), ("num_events", C.c_int), ("events", C.POINTER(C.c_void_p))]
+                ("dispatch", C.c_int), ("num_events", C.c_int), ("events", C.POINTER(C.c_void_p)),
+                ("swiglu_limit", C.c_float)]
 
 
 class MokSchedule(C.Structure):
@@ -62,7 +63,8 @@ class MokCtx(C.Structure):
                 ("I_s", C.c_int), ("mode", C.c_int), ("max_tiles", C.c_int),
                 ("gu", P), ("h", P), ("hq", P), ("hq_sc", P), ("slots", P), ("gu_s", P), ("h_s", P),
                 ("hq_s", P), ("hq_s_sc", P), ("shared_out", P), ("xq", P), ("xq_sc", P), ("status", P),
-                ("x_perm", P), ("dispatch", C.c_int), ("xq_perm", P), ("xq_perm_sc", P)]
+                ("x_perm", P), ("dispatch", C.c_int), ("xq_perm", P), ("xq_perm_sc", P),
+                ("swiglu_limit", C.c_float)]
 
 
 class MokWeightGrads(C.Structure):

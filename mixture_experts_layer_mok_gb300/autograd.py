@@ -22,13 +22,13 @@ class MoKFunction(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, x, router_w, top_experts, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, mode, capacity,
-                minibatch):
+                minibatch, swiglu_limit=0.0):
         E = w_gate.shape[0]
         sched = schedule(top_experts, E, capacity)
         weights = Weights(w_gate, w_up, w_down, ws_gate, ws_up, ws_down)
         if mode == "mxfp8":
             weights = quantize_weights(weights)
-        y, mctx = forward(x, router_w, sched, weights, mode=mode, minibatch=minibatch)
+        y, mctx = forward(x, router_w, sched, weights, mode=mode, minibatch=minibatch, swiglu_limit=swiglu_limit)
         ctx.save_for_backward(x, router_w)
         ctx.mok = (sched, mctx, weights, minibatch, ws_gate is not None)
         return y
@@ -41,16 +41,16 @@ class MoKFunction(torch.autograd.Function):
         ctx.mok = None
         return (g["dx"], g["d_router_w"], None, g["d_w_gate"], g["d_w_up"], g["d_w_down"],
                 g["d_ws_gate"] if shared else None, g["d_ws_up"] if shared else None,
-                g["d_ws_down"] if shared else None, None, None, None)
+                g["d_ws_down"] if shared else None, None, None, None, None)
 
 
 def mok_layer(x, router_w, top_experts, w_gate, w_up, w_down, ws_gate=None, ws_up=None, ws_down=None,
-              mode: str = "bf16", capacity: float = 0.5, minibatch: int = 0):
+              mode: str = "bf16", capacity: float = 0.5, minibatch: int = 0, swiglu_limit: float = 0.0):
     """Functional form: x bf16 [T, H], router_w fp32 [T, k], top_experts int64
     [T, k]; routed weights [E, I, H], [E, I, H], [E, H, I]; shared weights
     [I_s, H], [I_s, H], [H, I_s] or None."""
     return MoKFunction.apply(x, router_w, top_experts, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, mode, capacity,
-                             minibatch)
+                             minibatch, swiglu_limit)
 
 
 class MoKLayer(torch.nn.Module):
@@ -60,7 +60,8 @@ class MoKLayer(torch.nn.Module):
     chosen experts and their weights), as on the pages."""
 
     def __init__(self, E: int, H: int, I: int, I_s: int = 0, mode: str = "bf16", capacity: float = 0.5,
-                 minibatch: int = 0, device=None, init_std: float = 0.02, generator=None):
+                 minibatch: int = 0, swiglu_limit: float = 0.0, device=None, init_std: float = 0.02,
+                 generator=None):
         super().__init__()
         kw = dict(dtype=torch.bfloat16, device=device)
 
@@ -74,8 +75,8 @@ class MoKLayer(torch.nn.Module):
             self.ws_gate, self.ws_up, self.ws_down = param(I_s, H), param(I_s, H), param(H, I_s)
         else:
             self.ws_gate = self.ws_up = self.ws_down = None
-        self.mode, self.capacity, self.minibatch = mode, capacity, minibatch
+        self.mode, self.capacity, self.minibatch, self.swiglu_limit = mode, capacity, minibatch, swiglu_limit
 
     def forward(self, x, router_w, top_experts):
         return mok_layer(x, router_w, top_experts, self.w_gate, self.w_up, self.w_down, self.ws_gate, self.ws_up,
-                         self.ws_down, self.mode, self.capacity, self.minibatch)
+                         self.ws_down, self.mode, self.capacity, self.minibatch, self.swiglu_limit)

@@ -146,6 +146,25 @@ mok_status_t make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint6
   return MOK_OK;
 }
 
+// Row-major bf16 output [rows][cols] for TMA stores: box 32 rows x 32 columns
+// with 64-byte swizzle (the epilogue's staging layout); rows and columns past
+// the tensor's end are not written.
+mok_status_t make_map_out(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(MOK_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MOK_ERR_CUDA, "cuTensorMapEncodeTiled (output) failed (%d) for [%llu x %llu]", (int)r,
+                (unsigned long long)rows, (unsigned long long)cols);
+  return MOK_OK;
+}
+
 // E8M0 scales in the tensor-core scale layout as rows of 128 bytes, four per
 // 512-byte atom (box: one atom), for the TMA loads of CTA-pair GEMMs.
 mok_status_t make_map_sf(CUtensorMap* m, const void* base, long long atoms) {
@@ -351,6 +370,8 @@ mok_status_t check_config(const mok_config_t* cfg) {
   if (cfg->minibatch_size < 0) return fail(MOK_ERR_INVALID_ARG, "minibatch_size < 0");
   if (cfg->dispatch < MOK_DISPATCH_AUTO || cfg->dispatch > MOK_DISPATCH_FUSED)
     return fail(MOK_ERR_INVALID_ARG, "unknown dispatch %d", cfg->dispatch);
+  if (!std::isfinite(cfg->swiglu_limit) || cfg->swiglu_limit < 0.f)
+    return fail(MOK_ERR_INVALID_ARG, "swiglu_limit must be finite and >= 0");
   return MOK_OK;
 }
 
@@ -462,9 +483,11 @@ mok_status_t forward_bf16(const mok_config_t* cfg, const uint16_t* x, const floa
     if ((st = make_map(&m.a, x, H, T, 128, kTileBK)) || (st = make_map(&m.b0, w->ws_gate, H, Is, 128, kTileBK)) ||
         (st = make_map(&m.b1, w->ws_up, H, Is, 128, kTileBK)))
       return st;
+    if ((st = make_map_out(&m.o0, ctx->gu_s, 2ull * Is, T)) || (st = make_map_out(&m.o1, ctx->h_s, Is, T))) return st;
     GemmParams p = base_params(nullptr, ctx->status, 0);
     p.rows = T; p.K = H; p.N = Is; p.n_tiles = Is / 128; p.b_rows_per_expert = 0;
     p.out0 = ctx->gu_s; p.out1 = ctx->h_s;
+    p.swiglu_limit = cfg->swiglu_limit;
     const long long items = ((T + 127) / 128) * static_cast<long long>(p.n_tiles);
     MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_K_TILE, 256, EPI_SWIGLU>(m, p, items, row_pairs(T) * p.n_tiles,
                                                                      pair_on(cfg, 256), sms, cs)));
@@ -474,7 +497,8 @@ mok_status_t forward_bf16(const mok_config_t* cfg, const uint16_t* x, const floa
     const int bn = tile_n(H);
     const bool pr = pair_on(cfg, bn);
     if ((st = make_map(&m2.a, ctx->h_s, Is, T, 128, kTileBK)) ||
-        (st = make_map(&m2.b0, w->ws_down, Is, H, pr ? bn / 2 : bn, kTileBK)))
+        (st = make_map(&m2.b0, w->ws_down, Is, H, pr ? bn / 2 : bn, kTileBK)) ||
+        (st = make_map_out(&m2.o0, ctx->shared_out, H, T)))
       return st;
     m2.b1 = m2.b0;
     GemmParams q = base_params(nullptr, ctx->status, 0);
@@ -498,11 +522,13 @@ mok_status_t forward_bf16(const mok_config_t* cfg, const uint16_t* x, const floa
   const int bk = perm ? kTileBK : kGatherBK;
   if ((st = perm ? make_map(&m.a, ctx->x_perm, H, mr, 128, bk) : make_map(&m.a, x, H, T, 1, bk)) ||
       (st = make_map(&m.b0, w->w_gate, H, static_cast<uint64_t>(E) * I, 128, bk)) ||
-      (st = make_map(&m.b1, w->w_up, H, static_cast<uint64_t>(E) * I, 128, bk)))
+      (st = make_map(&m.b1, w->w_up, H, static_cast<uint64_t>(E) * I, 128, bk)) ||
+      (st = make_map_out(&m.o0, ctx->gu, 2ull * I, mr)) || (st = make_map_out(&m.o1, ctx->h, I, mr)))
     return st;
   GemmParams p = base_params(s, ctx->status, cfg->debug_flags);
   p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / 128; p.b_rows_per_expert = I;
   p.out0 = ctx->gu; p.out1 = ctx->h; p.ga = x; p.ga_ld = H;
+  p.swiglu_limit = cfg->swiglu_limit;
   const long long items = static_cast<long long>(s->max_tiles) * p.n_tiles;
   const int grid = items < sms ? static_cast<int>(items) : sms;
   if (perm)
@@ -584,6 +610,7 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
     GemmParams p = base_params(nullptr, ctx->status, 0);
     p.rows = T; p.K = H; p.N = Is; p.n_tiles = Is / 128; p.b_rows_per_expert = 0;
     p.out0 = ctx->gu_s; p.out1 = ctx->hq_s; p.sf_out = ctx->hq_s_sc;
+    p.swiglu_limit = cfg->swiglu_limit;
     p.sfa = ctx->xq_sc; p.sfb0 = X.wsg_sc; p.sfb1 = X.wsu_sc;
     const int items = ((T + 127) / 128) * p.n_tiles;
     if (pr_gu)
@@ -629,6 +656,7 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
   GemmParams p = base_params(s, ctx->status, cfg->debug_flags);
   p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / 128; p.b_rows_per_expert = I;
   p.out0 = ctx->gu; p.out1 = ctx->hq; p.sf_out = ctx->hq_sc;
+  p.swiglu_limit = cfg->swiglu_limit;
   p.sfa = ctx->xq_perm_sc; p.sfb0 = X.wg_sc; p.sfb1 = X.wu_sc;
   const long long items = static_cast<long long>(s->max_tiles) * p.n_tiles;
   if (pr_gu)
@@ -783,6 +811,7 @@ mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x, const float
   const bool g4 = (cfg->debug_flags & MOK_DEBUG_TMA_GATHER4) != 0;
   CtxExtra X;
   carve_ctx(ctx_buf, T, k, E, H, I, Is, cfg->mode, ctx, &X);
+  ctx->swiglu_limit = cfg->swiglu_limit;
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_PREP, 0, cs));
   MOK_CUDA(cudaMemsetAsync(ctx->status, 0, 8 * sizeof(int), cs));
   MOK_CUDA(launch_dependent(propagate_status_kernel, dim3(1), dim3(1), 0, cs, static_cast<const int*>(s->header),
@@ -874,12 +903,14 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
       GemmMaps m;
       const bool pr = pair_on(cfg, bns);
       if ((st = make_map(&m.a, dy, H, T, 128, kTileBK)) ||
-          (st = make_map_mn(&m.b0, w->ws_down, Is, H, pr ? bns / 2 : bns, kTileBK)))
+          (st = make_map_mn(&m.b0, w->ws_down, Is, H, pr ? bns / 2 : bns, kTileBK)) ||
+          (st = make_map_out(&m.o0, L.dgu_s, 2ull * Is, T)) || (st = make_map_out(&m.o1, L.hs, Is, T)))
         return st;
       m.b1 = m.b0;
       GemmParams p = base_params(nullptr, ctx->status, 0);
       p.rows = T; p.K = H; p.N = Is; p.n_tiles = Is / bns; p.b_rows_per_expert = 0;
       p.aux0 = ctx->gu_s; p.out0 = L.dgu_s; p.out1 = L.hs;
+      p.swiglu_limit = ctx->swiglu_limit;
       const long long items = ((T + 127) / 128) * static_cast<long long>(p.n_tiles);
       if (bns == 256)
         MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_MN_TILE, 256, EPI_DOWN_BWD>(m, p, items, row_pairs(T) * p.n_tiles, pr,
@@ -893,8 +924,10 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
       GemmMaps m;
       const bool pr = pair_on(cfg, bns);
       if ((st = make_map_mn(&m.a, dy, H, T, 128, kTileBK)) ||
-          (st = make_map_mn(&m.b0, L.hs, Is, T, pr ? bns / 2 : bns, kTileBK)))
+          (st = make_map_mn(&m.b0, L.hs, Is, T, pr ? bns / 2 : bns, kTileBK)) ||
+          (st = make_map_out(&m.o0, g->d_ws_down, Is, H)))
         return st;
+      m.o1 = m.o0;
       m.b1 = m.b0;
       GemmParams p = base_params(nullptr, ctx->status, 0);
       p.wgrad = 1; p.rows = T; p.E = 1; p.m_tiles = H / 128; p.n_tiles = Is / bns;
@@ -913,7 +946,8 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
       const int bn = tile_n(H);
       const bool pr = pair_on(cfg, bn);
       if ((st = make_map_mn(&m.a, L.dgu_s, 2 * Is, T, 128, kTileBK)) ||
-          (st = make_map_mn(&m.b0, x, H, T, pr ? bn / 2 : bn, kTileBK)))
+          (st = make_map_mn(&m.b0, x, H, T, pr ? bn / 2 : bn, kTileBK)) ||
+          (st = make_map_out(&m.o0, g->d_ws_gate, H, Is)) || (st = make_map_out(&m.o1, g->d_ws_up, H, Is)))
         return st;
       m.b1 = m.b0;
       GemmParams p = base_params(nullptr, ctx->status, 0);
@@ -934,7 +968,8 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
       const bool pr = pair_on(cfg, bn);
       if ((st = make_map(&m.a, L.dgu_s, 2 * Is, T, 128, kTileBK)) ||
           (st = make_map_mn(&m.b0, w->ws_gate, H, Is, pr ? bn / 2 : bn, kTileBK)) ||
-          (st = make_map_mn(&m.b1, w->ws_up, H, Is, pr ? bn / 2 : bn, kTileBK)))
+          (st = make_map_mn(&m.b1, w->ws_up, H, Is, pr ? bn / 2 : bn, kTileBK)) ||
+          (st = make_map_out(&m.o0, L.dx_s, H, T)))
         return st;
       GemmParams p = base_params(nullptr, ctx->status, 0);
       p.rows = T; p.K = 2 * Is; p.N = H; p.n_tiles = H / bn; p.b_rows_per_expert = 0; p.b_split = Is;
@@ -961,12 +996,14 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
     const int bk = perm ? kTileBK : kGatherBK;
     const bool pr = perm && pair_on(cfg, bn1);
     if ((st = perm ? make_map(&m.a, L.dy_perm, H, mr, 128, bk) : make_map(&m.a, dy, H, T, 1, bk)) ||
-        (st = make_map_mn(&m.b0, w->w_down, I, static_cast<uint64_t>(E) * H, pr ? bn1 / 2 : bn1, bk)))
+        (st = make_map_mn(&m.b0, w->w_down, I, static_cast<uint64_t>(E) * H, pr ? bn1 / 2 : bn1, bk)) ||
+        (st = make_map_out(&m.o0, L.dgu, 2ull * I, mr)) || (st = make_map_out(&m.o1, L.hw, I, mr)))
       return st;
     m.b1 = m.b0;
     GemmParams p = base_params(s, ctx->status, 0);
     p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / bn1; p.b_rows_per_expert = H;
     p.aux0 = ctx->gu; p.out0 = L.dgu; p.out1 = L.hw; p.rw = router_w; p.dw_part = L.dw_part;
+    p.swiglu_limit = ctx->swiglu_limit;
     p.ga = dy; p.ga_ld = H;
     const long long items = static_cast<long long>(s->max_tiles) * p.n_tiles;
     const int grid = items < sms ? static_cast<int>(items) : sms;
@@ -992,8 +1029,10 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
     const int bn = tile_n(I);
     const bool pr = perm && pair_on(cfg, bn);
     if ((st = perm ? make_map_mn(&m.a, L.dy_perm, H, mr, 128, bk) : make_map(&m.a, dy, H, T, 1, bk)) ||
-        (st = make_map_mn(&m.b0, L.hw, I, mr, pr ? bn / 2 : bn, bk)))
+        (st = make_map_mn(&m.b0, L.hw, I, mr, pr ? bn / 2 : bn, bk)) ||
+        (st = make_map_out(&m.o0, g->d_w_down, I, static_cast<uint64_t>(E) * H)))
       return st;
+    m.o1 = m.o0;
     m.b1 = m.b0;
     GemmParams p = base_params(s, ctx->status, 0);
     p.wgrad = 1; p.grouped = 1; p.E = E; p.m_tiles = H / 128; p.n_tiles = I / bn;
@@ -1025,7 +1064,9 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
     const int bn = tile_n(H);
     const bool pr = perm && pair_on(cfg, bn);
     if ((st = make_map_mn(&m.a, L.dgu, 2 * I, mr, 128, bk)) ||
-        (st = perm ? make_map_mn(&m.b0, x_rows, H, mr, pr ? bn / 2 : bn, bk) : make_map(&m.b0, x, H, T, 1, bk)))
+        (st = perm ? make_map_mn(&m.b0, x_rows, H, mr, pr ? bn / 2 : bn, bk) : make_map(&m.b0, x, H, T, 1, bk)) ||
+        (st = make_map_out(&m.o0, g->d_w_gate, H, static_cast<uint64_t>(E) * I)) ||
+        (st = make_map_out(&m.o1, g->d_w_up, H, static_cast<uint64_t>(E) * I)))
       return st;
     m.b1 = m.b0;
     GemmParams p = base_params(s, ctx->status, 0);

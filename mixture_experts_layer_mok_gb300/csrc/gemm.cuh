@@ -61,6 +61,11 @@ struct GemmMaps {
   CUtensorMap a;
   CUtensorMap b0;
   CUtensorMap b1;
+  // outputs written by TMA stores (row-major bf16, box 32 rows x 32 columns,
+  // 64-byte swizzle): SwiGLU G|U and h, SwiGLU backward dG|dU and w h, the
+  // weight gradients' two tensors, dense rows
+  CUtensorMap o0;
+  CUtensorMap o1;
 };
 
 struct GemmParams {
@@ -98,6 +103,7 @@ struct GemmParams {
   long long estride; // EPI_WGRAD: elements per expert in out0 / out1
   int* status;       // device status word
   int debug;         // MOK_DEBUG_* flags
+  float swiglu_limit;  // SwiGLU epilogues: 0 = plain; L > 0 clamps gate to <= L, up to [-L, L]
   // ---- gathered operands (gather warps): token-row tensors [T][ld]
   const uint16_t* ga;
   long long ga_ld;
@@ -277,6 +283,31 @@ __device__ __forceinline__ void warp_store_row64(const uint32_t* w, void* dst, u
   __syncwarp();
 }
 
+// Warp-cooperative TMA store of a 32-row x 32-column bf16 block at {col, row}
+// of the output tensor: each lane hands in 16 packed words of its row; the
+// warp stages them in the 64-byte-swizzled layout of the output's tensor map
+// (the layout warp_store_row64 uses) and lane 0 stores the block with one
+// bulk tensor copy.  Two 2 KB halves alternate, so staging the next block
+// overlaps the copy of this one; `slot` tracks the half in use.
+__device__ __forceinline__ void warp_store_tma(const uint32_t* w, const CUtensorMap* map, int col, int row,
+                                               uint8_t* stage2, int& slot, int lane) {
+  uint8_t* stage = stage2 + slot * 2048;
+  if (lane == 0) bulk_wait_read<1>();   // the copy that last read this half is done reading
+  __syncwarp();
+  uint4* s = reinterpret_cast<uint4*>(stage);
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    s[lane * 4 + (j ^ sw)] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+  fence_proxy_async_smem();             // generic-proxy writes, then the async-proxy read
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(map, stage, col, row);
+    bulk_commit();
+  }
+  slot ^= 1;
+}
+
 // Element i of 32 bf16 values held as 4 raw 16-byte words.
 __device__ __forceinline__ float bf16_at(const uint4* raw, int i) {
   const uint32_t w = reinterpret_cast<const uint32_t*>(raw)[i >> 1];
@@ -387,7 +418,7 @@ struct GemmCfg {
   static constexpr uint32_t kFullArrivals = kHasLsu ? 1 + 128 : 1;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kBarBytes = 512;
-  static constexpr int kEpiStageBytes = 2048;  // per epilogue warp: 32 rows x 64 bytes
+  static constexpr int kEpiStageBytes = 4096;  // per epilogue warp: two 32-row x 64-byte blocks
   static constexpr int kStagesFit = (227 * 1024 - 1024 - kBarBytes - kEpiWarps * kEpiStageBytes) / kStageBytes;
   static constexpr int kStages = kStagesFit > 16 ? 16 : kStagesFit;
   static constexpr int kTmemCols = 2 * BN;  // two accumulator buffers
@@ -805,8 +836,20 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI, PAIR>::kThreads
     const int q = warp & 3;         // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;    // tile row of this thread
     uint8_t* wstage = smem + C::kStages * C::kStageBytes + C::kBarBytes + (warp - 2) * C::kEpiStageBytes;
+    int tslot = 0;   // half of wstage the next TMA store stages into
     int abuf = 0;
     uint32_t aphase = 0;
+    // weight gradients: the tensor map and row coordinate of a 32-row block
+    // (row m of expert e: rows below `split` go to out0, the rest to out1)
+    auto wgrad_dst = [&](const Item& t, int mblock, const CUtensorMap*& map, int& row) {
+      if (mblock < p.split) {
+        map = &maps.o0;
+        row = t.e * p.split + mblock;
+      } else {
+        map = &maps.o1;
+        row = t.e * (p.m_tiles * kBM - p.split) + (mblock - p.split);
+      }
+    };
     for (int idx = item0; idx < nitems; idx += istep) {
       const Item it = item_at(idx, C::kBK);
       const int bn_out = (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_MX) ? BN / 2 : BN;
@@ -821,22 +864,20 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI, PAIR>::kThreads
       if (it.nk == 0) {
         // weight gradient of an expert with no rows: zeros
         if (EPI == EPI_WGRAD && live) {
-          const int m = it.m0 + r;
-          uint16_t* dst = (m < p.split)
-                              ? static_cast<uint16_t*>(p.out0) + it.e * p.estride + static_cast<long long>(m) * p.ld
-                              : static_cast<uint16_t*>(p.out1) + it.e * p.estride +
-                                    static_cast<long long>(m - p.split) * p.ld;
+          const CUtensorMap* omap;
+          int orow;
+          wgrad_dst(it, it.m0 + q * 32, omap, orow);
           uint32_t zw[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) zw[i] = 0u;
-          for (int c = epi_c0; c < epi_c1; ++c) warp_store_row64(zw, dst + n0 + c * 32, wstage, lane);
+          for (int c = epi_c0; c < epi_c1; ++c) warp_store_tma(zw, omap, n0 + c * 32, orow, wstage, tslot, lane);
         }
         continue;
       }
       // SwiGLU backward: row state and the first chunk of the saved gate|up,
       // fetched before the accumulator is ready
       int f_bwd = -1;
-      bool v_bwd = false, inb_bwd = false;
+      bool v_bwd = false;
       float wt_bwd = 1.f;
       uint4 ng[4], nu[4];
       if constexpr (EPI == EPI_DOWN_BWD) {
@@ -844,11 +885,9 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI, PAIR>::kThreads
         if (p.grouped) {
           f_bwd = (live && r < it.rows) ? __ldg(p.row_src + prow) : -1;
           v_bwd = f_bwd >= 0;
-          inb_bwd = live;
           if (v_bwd) wt_bwd = __ldg(p.rw + f_bwd);
         } else {
           v_bwd = live && r < it.rows;
-          inb_bwd = v_bwd;
         }
         if (v_bwd) {
           const uint16_t* gu = static_cast<const uint16_t*>(p.aux0) + static_cast<long long>(prow) * 2 * p.N + n0 +
@@ -866,12 +905,8 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI, PAIR>::kThreads
       uint32_t wv[16];
 
       if constexpr (EPI == EPI_SWIGLU) {
-        // out0 = gu [rows][2N], out1 = h [rows][N] (bf16)
-        const int prow = it.p0 + r;
+        // G|U [rows][2N] and h [rows][N] (bf16), through the maps o0 and o1
         const bool valid = r < it.rows;
-        const bool inb = (p.grouped ? true : valid) && live;
-        uint16_t* gu = inb ? static_cast<uint16_t*>(p.out0) + static_cast<long long>(prow) * 2 * p.N + n0 : nullptr;
-        uint16_t* hb = inb ? static_cast<uint16_t*>(p.out1) + static_cast<long long>(prow) * p.N + n0 : nullptr;
 #pragma unroll 1
         for (int c = 0; c < BN / 64; ++c) {
           float g[32], u[32];
@@ -882,17 +917,25 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI, PAIR>::kThreads
             for (int i = 0; i < 32; ++i) g[i] = u[i] = 0.f;
           }
           float hv[32];
+          const float lim = p.swiglu_limit;
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const float sg = __fdividef(1.f, 1.f + __expf(-g[i]));
-            hv[i] = g[i] * sg * u[i];
+            float gc = g[i], uc = u[i];
+            if (lim > 0.f) {   // clamped SwiGLU (G|U are saved unclamped for the backward)
+              gc = fminf(gc, lim);
+              uc = fminf(fmaxf(uc, -lim), lim);
+            }
+            const float sg = __fdividef(1.f, 1.f + __expf(-gc));
+            hv[i] = gc * sg * uc;
           }
+          // G|U and h by TMA (rows past a dense layer's end are clipped)
+          const int orow = it.p0 + q * 32;
           pack_bf16x32(g, wv);
-          warp_store_row64(wv, gu ? gu + c * 32 : nullptr, wstage, lane);
+          if (live) warp_store_tma(wv, &maps.o0, n0 + c * 32, orow, wstage, tslot, lane);
           pack_bf16x32(u, wv);
-          warp_store_row64(wv, gu ? gu + p.N + c * 32 : nullptr, wstage, lane);
+          if (live) warp_store_tma(wv, &maps.o0, p.N + n0 + c * 32, orow, wstage, tslot, lane);
           pack_bf16x32(hv, wv);
-          warp_store_row64(wv, hb ? hb + c * 32 : nullptr, wstage, lane);
+          if (live) warp_store_tma(wv, &maps.o1, n0 + c * 32, orow, wstage, tslot, lane);
         }
       } else if constexpr (EPI == EPI_SCALE_SCATTER || EPI == EPI_SCATTER) {
         const int f = (live && r < it.rows) ? __ldg(p.row_src + it.p0 + r) : -1;
@@ -910,26 +953,22 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI, PAIR>::kThreads
           warp_store_row64(wv, dst ? dst + c * 32 : nullptr, wstage, lane);
         }
       } else if constexpr (EPI == EPI_STORE_ROWS) {
-        const int prow = it.p0 + r;
-        uint16_t* dst = (live && r < it.rows)
-                            ? static_cast<uint16_t*>(p.out0) + static_cast<long long>(prow) * p.ld + n0
-                            : nullptr;
+        // dense rows by TMA (rows past the layer's end are clipped)
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           float v[32];
           tmem_ld32(tb + c * 32, v);
           pack_bf16x32(v, wv);
-          warp_store_row64(wv, dst ? dst + c * 32 : nullptr, wstage, lane);
+          if (live) warp_store_tma(wv, &maps.o0, n0 + c * 32, it.p0 + q * 32, wstage, tslot, lane);
         }
       } else if constexpr (EPI == EPI_DOWN_BWD) {
         // out0 = dgu [rows][2N], out1 = hw [rows][N]; aux0 = gu [rows][2N]
         const int prow = it.p0 + r;
         const uint16_t* gu = static_cast<const uint16_t*>(p.aux0) + static_cast<long long>(prow) * 2 * p.N + n0;
-        uint16_t* dgu = inb_bwd ? static_cast<uint16_t*>(p.out0) + static_cast<long long>(prow) * 2 * p.N + n0 : nullptr;
-        uint16_t* hw = inb_bwd ? static_cast<uint16_t*>(p.out1) + static_cast<long long>(prow) * p.N + n0 : nullptr;
         // router-weight partial sums, one per half of the tile's columns (the
         // same split whether one warp or two cover the row)
         float dpart = 0.f;
+        const float lim = p.swiglu_limit;
         float* dwp = (p.grouped && v_bwd) ? p.dw_part + (static_cast<long long>(f_bwd) * p.n_tiles + it.nt) * 2
                                           : nullptr;
 #pragma unroll 1
@@ -950,14 +989,21 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI, PAIR>::kThreads
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
                   const int e = half * 16 + i + t;
-                  const float g = bf16_at(ng, e), u = bf16_at(nu, e);
+                  float g = bf16_at(ng, e), u = bf16_at(nu, e);
+                  float mg = 1.f, mu = 1.f;   // the clamp's derivative (SwiGLU limit)
+                  if (lim > 0.f) {
+                    mg = (g <= lim) ? 1.f : 0.f;
+                    mu = (fabsf(u) <= lim) ? 1.f : 0.f;
+                    g = fminf(g, lim);
+                    u = fminf(fmaxf(u, -lim), lim);
+                  }
                   const float sg = __fdividef(1.f, 1.f + __expf(-g));
                   const float sl = g * sg;
                   const float h = sl * u;
                   dpart = fmaf(z[i + t], h, dpart);
                   const float dh = wt_bwd * z[i + t];
-                  a[t] = dh * u * sg * (1.f + g * (1.f - sg));
-                  b[t] = dh * sl;
+                  a[t] = dh * u * sg * (1.f + g * (1.f - sg)) * mg;
+                  b[t] = dh * sl * mu;
                   hh[t] = wt_bwd * h;
                 }
               }
@@ -970,24 +1016,24 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI, PAIR>::kThreads
             load_raw64(gu + (c + 1) * 32, ng);
             load_raw64(gu + p.N + (c + 1) * 32, nu);
           }
-          warp_store_row64(wdg, dgu ? dgu + c * 32 : nullptr, wstage, lane);
-          warp_store_row64(wdu, dgu ? dgu + p.N + c * 32 : nullptr, wstage, lane);
-          warp_store_row64(whv, hw ? hw + c * 32 : nullptr, wstage, lane);
+          if (live) {   // dG|dU and w h by TMA (dense rows past the end are clipped)
+            const int orow = it.p0 + q * 32;
+            warp_store_tma(wdg, &maps.o0, n0 + c * 32, orow, wstage, tslot, lane);
+            warp_store_tma(wdu, &maps.o0, p.N + n0 + c * 32, orow, wstage, tslot, lane);
+            warp_store_tma(whv, &maps.o1, n0 + c * 32, orow, wstage, tslot, lane);
+          }
         }
         if (dwp) dwp[C::kEpiWarps == 8 ? epi_half : 1] = dpart;
       } else if constexpr (EPI == EPI_WGRAD) {
-        const int m = it.m0 + r;
-        uint16_t* dst = !live ? nullptr
-                        : (m < p.split)
-                            ? static_cast<uint16_t*>(p.out0) + it.e * p.estride + static_cast<long long>(m) * p.ld
-                            : static_cast<uint16_t*>(p.out1) + it.e * p.estride +
-                                  static_cast<long long>(m - p.split) * p.ld;
+        const CUtensorMap* omap;
+        int orow;
+        wgrad_dst(it, it.m0 + q * 32, omap, orow);
 #pragma unroll 1
         for (int c = epi_c0; c < epi_c1; ++c) {
           float v[32];
           tmem_ld32(tb + c * 32, v);
           pack_bf16x32(v, wv);
-          warp_store_row64(wv, dst ? dst + n0 + c * 32 : nullptr, wstage, lane);
+          if (live) warp_store_tma(wv, omap, n0 + c * 32, orow, wstage, tslot, lane);
         }
       }
       tc_fence_before();
@@ -1003,6 +1049,7 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI, PAIR>::kThreads
         aphase ^= 1;
       }
     }
+    if (lane == 0) bulk_wait<0>();   // this warp's TMA stores are complete before the CTA ends
   }
 
   tc_fence_before();

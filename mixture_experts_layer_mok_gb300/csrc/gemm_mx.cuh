@@ -352,11 +352,16 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
 #pragma unroll
         for (int c = 0; c < kH / 32; ++c) {
           float* hv = g + c * 32;        // h overwrites the gate values (already stored)
+          const float lim = p.swiglu_limit;
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const float x = hv[i];
+            float x = hv[i], uc = u[c * 32 + i];
+            if (lim > 0.f) {   // clamped SwiGLU (G|U are saved unclamped for the backward)
+              x = fminf(x, lim);
+              uc = fminf(fmaxf(uc, -lim), lim);
+            }
             const float sg = __fdividef(1.f, 1.f + __expf(-x));
-            hv[i] = x * sg * u[c * 32 + i];
+            hv[i] = x * sg * uc;
           }
           uint8_t codes[32];
           const uint32_t s8 = mx_quantize32(hv, codes);

@@ -41,13 +41,13 @@ def weights_of(g, mode="bf16"):
     return w
 
 
-def run_layer(inp, mode="bf16", capacity=0.5, minibatch=0, device="cuda"):
+def run_layer(inp, mode="bf16", capacity=0.5, minibatch=0, device="cuda", swiglu_limit=0.0):
     """Forward + backward through the C ABI; returns (y, grads, sched, ctx)."""
     m = mok()
     g = inp.to(device)
     sched = m.schedule(g.top_experts, inp.meta["E"], capacity)
     w = weights_of(g, mode)
-    y, ctx = m.forward(g.x, g.router_w, sched, w, mode=mode, minibatch=minibatch)
+    y, ctx = m.forward(g.x, g.router_w, sched, w, mode=mode, minibatch=minibatch, swiglu_limit=swiglu_limit)
     grads = m.backward(g.dy, g.x, g.router_w, sched, ctx, w, minibatch=minibatch)
     torch.cuda.synchronize()
     return y, grads, sched, ctx
@@ -58,14 +58,14 @@ def oracle_args(inp):
             inp.ws_gate, inp.ws_up, inp.ws_down)
 
 
-def oracle_fwd_bwd(inp, mode="bf16"):
+def oracle_fwd_bwd(inp, mode="bf16", swiglu_limit=0.0):
     a = oracle_args(inp)
     if mode == "mxfp8":
-        y = oracle.layer_forward_mxfp8(*a)
-        g = oracle.layer_backward_mxfp8(*a[:6], inp.dy, *a[6:])
+        y = oracle.layer_forward_mxfp8(*a, swiglu_limit=swiglu_limit)
+        g = oracle.layer_backward_mxfp8(*a[:6], inp.dy, *a[6:], swiglu_limit=swiglu_limit)
     else:
-        y = oracle.layer_forward(*a)
-        g = oracle.layer_backward(*a[:6], inp.dy, *a[6:])
+        y = oracle.layer_forward(*a, swiglu_limit=swiglu_limit)
+        g = oracle.layer_backward(*a[:6], inp.dy, *a[6:], swiglu_limit=swiglu_limit)
     return y, g
 
 

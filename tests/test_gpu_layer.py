@@ -303,3 +303,32 @@ def test_mxfp8_dispatch_codes_and_scales_bit_exact(name):
     assert np.array_equal(xp[valid], codes[tok[valid]])
     assert np.array_equal(xps[valid], scales[tok[valid]])
     assert np.all(xp[~valid] == 0) and np.all(xps[~valid] == 127)
+
+
+@pytest.mark.parametrize("name,mode", [("ragged_shared", "bf16"), ("wide", "bf16"), ("skewed", "bf16"),
+                                       ("ragged_shared", "mxfp8"), ("wide", "mxfp8")])
+def test_swiglu_limit_matches_oracle(name, mode):
+    """The clamped SwiGLU (swiglu_limit L: gate <= L, up in [-L, L]) against the
+    oracle's clamped layer, forward and backward, with L low enough that a
+    large share of the pre-activations is clamped; and L = 0 is the plain layer."""
+    inp = _inputs(name, seed=12)
+    L = 0.25
+    y, grads, sched, ctx = run_layer(inp, mode, swiglu_limit=L)
+    assert ctx.status() == 0
+    y_ref, g_ref = oracle_fwd_bwd(inp, mode, swiglu_limit=L)
+    errs, bad = compare_all(y, grads, y_ref, g_ref, BF16_TOL)
+    assert not bad, errs
+    # the clamp changed the result: the plain layer is far from it
+    y_plain, _ = oracle_fwd_bwd(inp, mode)
+    assert rel_l2(y_ref, y_plain) > 10 * BF16_TOL
+
+
+def test_swiglu_limit_rejects_bad_values():
+    m = mok()
+    inp = _inputs("tiny", seed=1)
+    g = inp.to("cuda")
+    sched = m.schedule(g.top_experts, inp.meta["E"], 0.5)
+    w = weights_of(g)
+    for bad in (-1.0, float("nan"), float("inf")):
+        with pytest.raises(m.MokError):
+            m.forward(g.x, g.router_w, sched, w, swiglu_limit=bad)

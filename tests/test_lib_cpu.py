@@ -83,6 +83,13 @@ def test_argument_errors_need_no_device(lib):
     cfg = _lib.MokConfig(mode=7)
     assert lib.mok_forward(C.byref(cfg), fake, fake, C.byref(s), None, fake, fake, 0, None, None) == \
         _lib.MOK_ERR_INVALID_ARG
+    w = _lib.MokWeights(E=8, H=128, I=128, I_s=0)
+    ctx = _lib.MokCtx()
+    for bad in (-0.5, float("nan"), float("inf")):   # swiglu_limit must be finite and >= 0
+        cfg = _lib.MokConfig(mode=0, swiglu_limit=bad)
+        assert lib.mok_forward(C.byref(cfg), fake, fake, C.byref(s), C.byref(w), fake, fake, 1 << 16,
+                               C.byref(ctx), None) == _lib.MOK_ERR_INVALID_ARG
+        assert b"swiglu_limit" in lib.mok_last_error()
     del buf
 
 
