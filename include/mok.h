@@ -94,7 +94,7 @@ typedef int mok_status_t;
 #define MOK_STAGE_BWD_DOWN                 6  /* routed dgrad through down + SwiGLU bwd + router-grad partials */
 #define MOK_STAGE_BWD_WGRAD_DOWN           7  /* routed dW_down */
 #define MOK_STAGE_BWD_WGRAD_GATEUP         8  /* routed dW_gate, dW_up */
-#define MOK_STAGE_BWD_DGRAD_GATEUP         9  /* routed dgrad through gate/up -> dx slots */
+#define MOK_STAGE_BWD_DGRAD_GATEUP         9  /* routed dgrad through gate/up -> dx rows in schedule order */
 #define MOK_STAGE_BWD_SHARED_DOWN         10
 #define MOK_STAGE_BWD_SHARED_WGRAD_DOWN   11
 #define MOK_STAGE_BWD_SHARED_WGRAD_GATEUP 12
@@ -198,7 +198,8 @@ typedef struct {
   uint16_t* h;        /* [max_tiles*128][I]  SwiGLU output, bf16 mode (scratch) */
   uint8_t*  hq;       /* [max_tiles*128][I]  SwiGLU output E4M3 codes, MXFP8 mode (scratch) */
   uint8_t*  hq_sc;    /* its E8M0 scales, tensor-core scale layout (below) */
-  uint16_t* slots;    /* [T*k][H] router-weighted expert outputs (scratch) */
+  uint16_t* slots;    /* [max_tiles*128][H] router-weighted expert outputs in schedule order
+                         (scratch; the combine reads row slot_row[t*k + j] for (t, j)) */
   uint16_t* gu_s;     /* [T][2 I_s] shared gate | up (saved) */
   uint16_t* h_s;      /* [T][I_s] shared SwiGLU output, bf16 mode (scratch) */
   uint8_t*  hq_s;     /* [T][I_s] shared SwiGLU output codes, MXFP8 mode */

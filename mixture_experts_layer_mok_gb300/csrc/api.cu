@@ -249,7 +249,7 @@ size_t carve_ctx(void* buf, int T, int k, int E, int H, int I, int Is, int mode,
   ctx->max_tiles = static_cast<int>(max_tiles_of(T, k, E));
   ctx->status = c.take<int32_t>(8);
   ctx->gu = c.take<uint16_t>(mr * 2 * I);
-  ctx->slots = c.take<uint16_t>(n * H);
+  ctx->slots = c.take<uint16_t>(mr * H);
   if (!mx) {
     ctx->x_perm = c.take<uint16_t>(mr * H);
     ctx->h = c.take<uint16_t>(mr * I);
@@ -313,7 +313,7 @@ size_t carve_bwd(void* buf, int T, int k, int E, int H, int I, int Is, BwdLayout
   L->dgu = c.take<uint16_t>(mr * 2 * I);
   L->hw = c.take<uint16_t>(mr * I);
   L->dw_part = c.take<float>(n * 2 * (I / tile_n(I)));  // two column halves per N tile
-  L->dx_slots = c.take<uint16_t>(n * H);
+  L->dx_slots = c.take<uint16_t>(mr * H);
   L->dy_perm = c.take<uint16_t>(mr * H);
   L->xb_perm = c.take<uint16_t>(mr * H);
   if (Is > 0) {
@@ -543,7 +543,8 @@ mok_status_t forward_bf16(const mok_config_t* cfg, const uint16_t* x, const floa
   const int bn = tile_n(H);
   const bool pr = pair_on(cfg, bn);
   if ((st = make_map(&m2.a, ctx->h, I, mr, 128, kTileBK)) ||
-      (st = make_map(&m2.b0, w->w_down, I, static_cast<uint64_t>(E) * H, pr ? bn / 2 : bn, kTileBK)))
+      (st = make_map(&m2.b0, w->w_down, I, static_cast<uint64_t>(E) * H, pr ? bn / 2 : bn, kTileBK)) ||
+      (st = make_map_out(&m2.o0, ctx->slots, H, mr)))
     return st;
   m2.b1 = m2.b0;
   GemmParams q = base_params(s, ctx->status, 0);
@@ -551,9 +552,9 @@ mok_status_t forward_bf16(const mok_config_t* cfg, const uint16_t* x, const floa
   q.out0 = ctx->slots; q.ld = H; q.rw = router_w;
   const long long items2 = static_cast<long long>(s->max_tiles) * q.n_tiles;
   if (bn == 256)
-    MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_K_TILE, 256, EPI_SCALE_SCATTER>(m2, q, items2, items2, pr, sms, cs)));
+    MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_K_TILE, 256, EPI_SCALE_ROWS>(m2, q, items2, items2, pr, sms, cs)));
   else
-    MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_K_TILE, 128, EPI_SCALE_SCATTER>(m2, q, items2, 0, false, sms, cs)));
+    MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_K_TILE, 128, EPI_SCALE_ROWS>(m2, q, items2, 0, false, sms, cs)));
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DOWN, 1, cs));
   return MOK_OK;
 }
@@ -680,11 +681,11 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
   const long long items2 = static_cast<long long>(s->max_tiles) * q.n_tiles;
   const int grid2 = items2 < sms ? static_cast<int>(items2) : sms;
   if (pr)
-    MOK_CUDA((launch_gemm_mx_pair<256, EPI_SCALE_SCATTER>(m2, q, items2, cs)));
+    MOK_CUDA((launch_gemm_mx_pair<256, EPI_SCALE_ROWS>(m2, q, items2, cs)));
   else if (bn == 256)
-    MOK_CUDA((launch_gemm_mx<256, EPI_SCALE_SCATTER>(m2, q, grid2, cs)));
+    MOK_CUDA((launch_gemm_mx<256, EPI_SCALE_ROWS>(m2, q, grid2, cs)));
   else
-    MOK_CUDA((launch_gemm_mx<128, EPI_SCALE_SCATTER>(m2, q, grid2, cs)));
+    MOK_CUDA((launch_gemm_mx<128, EPI_SCALE_ROWS>(m2, q, grid2, cs)));
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DOWN, 1, cs));
   return MOK_OK;
 }
@@ -828,7 +829,8 @@ mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x, const float
 
   // ---- combine: y[t] = shared[t] + sum_j slots[t, j] in fixed order
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_COMBINE, 0, cs));
-  MOK_CUDA(launch_combine(ctx->slots, Is > 0 ? ctx->shared_out : nullptr, T, k, H, y, sms, cs));
+  MOK_CUDA(launch_combine(ctx->slots, s->slot_row, s->header, mr, Is > 0 ? ctx->shared_out : nullptr, T, k, H, y,
+                          sms, cs));
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_COMBINE, 1, cs));
   return MOK_OK;
 }
@@ -1100,21 +1102,23 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
     const int bw = pr ? bn / 2 : bn;
     if ((st = make_map(&m.a, L.dgu, 2 * I, mr, 128, kTileBK)) ||
         (st = make_map_mn(&m.b0, w->w_gate, H, static_cast<uint64_t>(E) * I, bw, kTileBK)) ||
-        (st = make_map_mn(&m.b1, w->w_up, H, static_cast<uint64_t>(E) * I, bw, kTileBK)))
+        (st = make_map_mn(&m.b1, w->w_up, H, static_cast<uint64_t>(E) * I, bw, kTileBK)) ||
+        (st = make_map_out(&m.o0, L.dx_slots, H, mr)))
       return st;
     GemmParams p = base_params(s, ctx->status, 0);
     p.grouped = 1; p.K = 2 * I; p.N = H; p.n_tiles = H / bn; p.b_rows_per_expert = I; p.b_split = I;
     p.out0 = L.dx_slots; p.ld = H;
     const long long items = static_cast<long long>(s->max_tiles) * p.n_tiles;
     if (bn == 256)
-      MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_MN_TILE, 256, EPI_SCATTER>(m, p, items, items, pr, sms, cs)));
+      MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_MN_TILE, 256, EPI_STORE_ROWS>(m, p, items, items, pr, sms, cs)));
     else
-      MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_MN_TILE, 128, EPI_SCATTER>(m, p, items, 0, false, sms, cs)));
+      MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_MN_TILE, 128, EPI_STORE_ROWS>(m, p, items, 0, false, sms, cs)));
     MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DGRAD_GATEUP, 1, cs));
   }
   // ---- fixed-order reductions: dx and the router-weight gradient
   MOK_CUDA(mark(cfg, MOK_STAGE_BWD_REDUCE, 0, cs));
-  MOK_CUDA(launch_combine(L.dx_slots, Is > 0 ? L.dx_s : nullptr, T, k, H, dx, sms, cs));
+  MOK_CUDA(launch_combine(L.dx_slots, s->slot_row, s->header, mr, Is > 0 ? L.dx_s : nullptr, T, k, H, dx, sms,
+                          cs));
   MOK_CUDA(launch_dw_reduce(L.dw_part, T * k, 2 * (I / bn1), d_router_w, cs));
   MOK_CUDA(mark(cfg, MOK_STAGE_BWD_REDUCE, 1, cs));
   return MOK_OK;

@@ -1,26 +1,28 @@
 // Persistent grouped GEMM engine on tcgen05 / TMEM / TMA for sm_103a.
 //
-// One CTA per SM, 192 threads (320 when an operand is gathered):
+// One CTA per SM, or one cluster of two CTAs per SM pair (CTA pairs:
+// tcgen05.mma.cta_group::2, M = 256, each CTA holding half of B):
 //   warp 0      TMA producer: tile loads of the operands that are not gathered
 //               (and, on request, tile::gather4 loads of the gathered ones);
-//   warp 1      MMA issuer (one thread) and TMEM owner;
-//   warps 2..5  epilogue: TMEM -> registers -> fused elementwise -> HBM
-//               (SwiGLU, MXFP8 requantisation, router scaling, scatter to
-//               per-(token, k) slots, SwiGLU backward, router-weight grad);
-//   warps 6..9  gather producers: 16-byte cp.async copies of the token rows a
-//               schedule tile needs, written straight into the 128-byte-
-//               swizzled stage layout the tensor core reads (the on-chip form
-//               of MoK's dispatch exchange).
-// The data-movement warps (0, 6..9) and the output warps (2..5) overlap the
-// MMA warp through a ring of shared-memory stages and a double-buffered TMEM
-// accumulator: the single-GPU analogue of MoK's split of SMs into
-// communication and compute roles ("Mixture-of-Kittens: a deterministic MoE
-// megakernel for NVL72 racks", "Tuning the five hyperparameters before
-// production": fwd/bwd_num_comm_sms).
+//   warp 1      MMA issuer (one thread; a pair's leader issues for both) and
+//               TMEM owner;
+//   warps 2..   epilogue (4 warps, or 8 for the SwiGLU backward and the weight
+//               gradients): TMEM -> registers -> fused elementwise -> TMA
+//               stores of 32x32 blocks (SwiGLU, router scaling, SwiGLU
+//               backward with the router-weight grad, weight gradients);
+//   last 4      gather producers (fused-dispatch variants only): 16-byte
+//               cp.async copies of the token rows a schedule tile needs,
+//               written straight into the 128-byte-swizzled stage layout the
+//               tensor core reads (the on-chip form of MoK's dispatch exchange).
+// The data-movement warps and the output warps overlap the MMA warp through a
+// ring of shared-memory stages and a double-buffered TMEM accumulator: the
+// single-GPU analogue of MoK's split of SMs into communication and compute
+// roles ("Mixture-of-Kittens: a deterministic MoE megakernel for NVL72 racks",
+// "Tuning the five hyperparameters before production": fwd/bwd_num_comm_sms).
 //
-// Work items are output tiles of 128 rows x BN columns; each is produced by
-// exactly one CTA with a fixed K order, so results do not depend on which CTA
-// takes which item or on the item order.
+// Work items are output tiles of 128 rows x BN columns (pairs: two such tiles
+// sharing B); each is produced by exactly one CTA with a fixed K order, so
+// results do not depend on which CTA takes which item or on the item order.
 #pragma once
 
 #include <cuda.h>
@@ -50,10 +52,9 @@ enum Src : int {
 enum Epi : int {
   EPI_SWIGLU = 0,        // gate|up accumulators -> G, U (bf16), h = silu(G) U (bf16)
   EPI_SWIGLU_MX = 1,     // same, h written as MXFP8 codes + E8M0 scales (gemm_mx_kernel)
-  EPI_SCALE_SCATTER = 2, // slot[f] = bf16(w[f] * acc) for the tile's routed rows
+  EPI_SCALE_ROWS = 2,    // out[p] = bf16(w[row_src[p]] * acc), rows in schedule order (0 for padding)
   EPI_STORE_ROWS = 3,    // out[row] = bf16(acc) for dense rows
   EPI_DOWN_BWD = 4,      // dH = w Z; SwiGLU backward; d_w partial = sum Z h; hw = w h
-  EPI_SCATTER = 5,       // out[f] = bf16(acc) for the tile's routed rows
   EPI_WGRAD = 6,         // out[e][m][n] = bf16(acc), rows split over two tensors
 };
 
@@ -937,20 +938,19 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI, PAIR>::kThreads
           pack_bf16x32(hv, wv);
           if (live) warp_store_tma(wv, &maps.o1, n0 + c * 32, orow, wstage, tslot, lane);
         }
-      } else if constexpr (EPI == EPI_SCALE_SCATTER || EPI == EPI_SCATTER) {
+      } else if constexpr (EPI == EPI_SCALE_ROWS) {
+        // router-weighted rows in schedule order by TMA; the combine reads
+        // them back per (token, k) through slot_row
         const int f = (live && r < it.rows) ? __ldg(p.row_src + it.p0 + r) : -1;
-        const float wt = (EPI == EPI_SCALE_SCATTER && f >= 0) ? __ldg(p.rw + f) : 1.f;
-        uint16_t* dst = f >= 0 ? static_cast<uint16_t*>(p.out0) + static_cast<long long>(f) * p.ld + n0 : nullptr;
+        const float wt = f >= 0 ? __ldg(p.rw + f) : 0.f;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           float v[32];
           tmem_ld32(tb + c * 32, v);
-          if (EPI == EPI_SCALE_SCATTER) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] *= wt;
-          }
+          for (int i = 0; i < 32; ++i) v[i] *= wt;
           pack_bf16x32(v, wv);
-          warp_store_row64(wv, dst ? dst + c * 32 : nullptr, wstage, lane);
+          if (live) warp_store_tma(wv, &maps.o0, n0 + c * 32, it.p0 + q * 32, wstage, tslot, lane);
         }
       } else if constexpr (EPI == EPI_STORE_ROWS) {
         // dense rows by TMA (rows past the layer's end are clipped)

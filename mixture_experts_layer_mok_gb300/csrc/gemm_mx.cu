@@ -1,5 +1,5 @@
 // Block-scaled (MXFP8) grouped-GEMM instantiations for the MXFP8 forward:
-// gate/up + SwiGLU + h requantisation, down + router scale + scatter, dense
+// gate/up + SwiGLU + h requantisation, down + router scale (rows in schedule order), dense
 // store (shared expert); single CTAs and CTA pairs.
 #include "gemm_launch.cuh"
 #include "gemm_mx.cuh"
@@ -79,12 +79,12 @@ cudaError_t launch_gemm_mx_pair(const MxMaps& maps, const GemmParams& p, long lo
   template cudaError_t launch_gemm_mx_pair<BN, EPI>(const MxMaps&, const GemmParams&, long long, cudaStream_t);
 
 MOK_INSTANTIATE_MX(256, EPI_SWIGLU_MX)
-MOK_INSTANTIATE_MX(256, EPI_SCALE_SCATTER)
-MOK_INSTANTIATE_MX(128, EPI_SCALE_SCATTER)
+MOK_INSTANTIATE_MX(256, EPI_SCALE_ROWS)
+MOK_INSTANTIATE_MX(128, EPI_SCALE_ROWS)
 MOK_INSTANTIATE_MX(256, EPI_STORE_ROWS)
 MOK_INSTANTIATE_MX(128, EPI_STORE_ROWS)
 MOK_INSTANTIATE_MX_PAIR(256, EPI_SWIGLU_MX)
-MOK_INSTANTIATE_MX_PAIR(256, EPI_SCALE_SCATTER)
+MOK_INSTANTIATE_MX_PAIR(256, EPI_SCALE_ROWS)
 MOK_INSTANTIATE_MX_PAIR(256, EPI_STORE_ROWS)
 
 }  // namespace mok

@@ -73,7 +73,7 @@ template <int BN, int EPI, bool PAIR = false>
 __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
     gemm_mx_kernel(const __grid_constant__ MxMaps maps, const GemmParams p) {
   using C = MxCfg<BN, EPI, PAIR>;
-  static_assert(EPI == EPI_SWIGLU_MX || EPI == EPI_SCALE_SCATTER || EPI == EPI_STORE_ROWS, "epilogue");
+  static_assert(EPI == EPI_SWIGLU_MX || EPI == EPI_SCALE_ROWS || EPI == EPI_STORE_ROWS, "epilogue");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
       const bool valid = live && r < it.rows;
       int f = -1;
       float wt = 1.f;
-      if (EPI == EPI_SCALE_SCATTER && valid) {
+      if (EPI == EPI_SCALE_ROWS && valid) {
         f = __ldg(p.row_src + prow);
         if (f >= 0) wt = __ldg(p.rw + f);
       }
@@ -384,15 +384,13 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
           }
         }
       } else {
+        // rows in schedule order (router-weighted: the combine reads them
+        // back per (token, k) through slot_row), or dense rows
         uint16_t* dst = nullptr;
-        if (EPI == EPI_SCALE_SCATTER) {
-          if (f >= 0) dst = static_cast<uint16_t*>(p.out0) + static_cast<long long>(f) * p.ld + n0 + half * kCols;
-        } else if (valid) {
-          dst = static_cast<uint16_t*>(p.out0) + static_cast<long long>(prow) * p.ld + n0 + half * kCols;
-        }
+        if (valid) dst = static_cast<uint16_t*>(p.out0) + static_cast<long long>(prow) * p.ld + n0 + half * kCols;
 #pragma unroll
         for (int c = 0; c < kCols / 32; ++c) {
-          if (EPI == EPI_SCALE_SCATTER) {
+          if (EPI == EPI_SCALE_ROWS) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[c * 32 + i] *= wt;
           }

@@ -5,10 +5,9 @@
 
 namespace mok {
 MOK_INSTANTIATE_GEMM_PAIR(SRC_K_TILE, SRC_K_TILE, 256, EPI_SWIGLU)
-MOK_INSTANTIATE_GEMM_PAIR(SRC_K_TILE, SRC_K_TILE, 256, EPI_SCALE_SCATTER)
+MOK_INSTANTIATE_GEMM_PAIR(SRC_K_TILE, SRC_K_TILE, 256, EPI_SCALE_ROWS)
 MOK_INSTANTIATE_GEMM_PAIR(SRC_K_TILE, SRC_K_TILE, 256, EPI_STORE_ROWS)
 MOK_INSTANTIATE_GEMM_PAIR(SRC_K_TILE, SRC_MN_TILE, 256, EPI_DOWN_BWD)
-MOK_INSTANTIATE_GEMM_PAIR(SRC_K_TILE, SRC_MN_TILE, 256, EPI_SCATTER)
 MOK_INSTANTIATE_GEMM_PAIR(SRC_K_TILE, SRC_MN_TILE, 256, EPI_STORE_ROWS)
 MOK_INSTANTIATE_GEMM_PAIR(SRC_MN_TILE, SRC_MN_TILE, 256, EPI_WGRAD)
 }  // namespace mok

@@ -41,8 +41,8 @@ cudaError_t launch_mx_dispatch(const uint16_t* x, int T, int H, int topk, const 
                                const int* header, long long max_rows, uint8_t* xq, uint8_t* xq_sc, uint8_t* xp,
                                uint8_t* xp_sc, int num_sms, cudaStream_t st);
 cudaError_t launch_mx_tile_scales(const uint8_t* src, long long rows, int K, uint8_t* dst, cudaStream_t st);
-cudaError_t launch_combine(const uint16_t* slots, const uint16_t* base, int T, int k, int H,
-                           uint16_t* out, int num_sms, cudaStream_t st);
+cudaError_t launch_combine(const uint16_t* rows, const int* slot_row, const int* header, long long max_rows,
+                           const uint16_t* base, int T, int k, int H, uint16_t* out, int num_sms, cudaStream_t st);
 cudaError_t launch_permute_rows(const uint16_t* src, int H, int topk, const int* row_src, const int* header,
                                 long long max_rows, uint16_t* out, int num_sms, cudaStream_t st);
 cudaError_t launch_dw_reduce(const float* part, int nf, int ntiles, float* dw, cudaStream_t st);

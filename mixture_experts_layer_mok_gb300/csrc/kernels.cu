@@ -403,15 +403,19 @@ cudaError_t launch_mx_tile_scales(const uint8_t* src, long long rows, int K, uin
 }
 
 // ===========================================================================
-// Fixed-order combine: out[t] = bf16(base[t] + sum_{j<k} slots[t*k + j]),
-// summed in fp32, base first, then j ascending (no floating-point atomics).
-// One thread per 8 columns of one token.
+// Fixed-order combine: out[t] = bf16(base[t] + sum_{j<k} rows[slot_row[t*k + j]]),
+// summed in fp32, base first, then j ascending (no floating-point atomics):
+// the expert outputs sit in schedule order and are gathered back per
+// (token, k) here.  One thread per 8 columns of one token.
 // ===========================================================================
-__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ slots,
+__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ rows,
+                                                      const int* __restrict__ slot_row,
+                                                      const int* __restrict__ header, long long max_rows,
                                                       const uint16_t* __restrict__ base, int T, int k,
                                                       int H, uint16_t* __restrict__ out) {
   griddep_wait();
   griddep_launch_dependents();
+  if (header[2] != 0) return;   // no schedule (bad expert id): slot_row was never written
   const int per_row = H / 8;
   const long long total = static_cast<long long>(T) * per_row;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
@@ -432,7 +436,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
       for (int q = 0; q < 8; ++q) acc[q] = 0.f;
     }
     for (int j = 0; j < k; ++j) {
-      const uint4 w = __ldg(reinterpret_cast<const uint4*>(slots + (t * k + j) * H + c));
+      long long row = __ldg(slot_row + t * k + j);
+      row = row < 0 ? 0 : (row >= max_rows ? max_rows - 1 : row);   // in bounds whatever the array holds
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(rows + row * H + c));
       const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -446,11 +452,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
   }
 }
 
-cudaError_t launch_combine(const uint16_t* slots, const uint16_t* base, int T, int k, int H,
-                           uint16_t* out, int num_sms, cudaStream_t st) {
+cudaError_t launch_combine(const uint16_t* rows, const int* slot_row, const int* header, long long max_rows,
+                           const uint16_t* base, int T, int k, int H, uint16_t* out, int num_sms, cudaStream_t st) {
   const long long total = static_cast<long long>(T) * (H / 8);
-  cudaError_t err = launch_dependent(combine_kernel, dim3(grid_for(total, 256, num_sms)), dim3(256), 0, st, slots, base, T,
-                                     k, H, out);
+  cudaError_t err = launch_dependent(combine_kernel, dim3(grid_for(total, 256, num_sms)), dim3(256), 0, st, rows,
+                                     slot_row, header, max_rows, base, T, k, H, out);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }

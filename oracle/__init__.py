@@ -18,6 +18,8 @@ from .mok_oracle import (  # noqa: F401
     mxfp8_quantize,
     mxfp8_dequantize,
     silu,
+    round_bf16,
+    clamp_gate_up,
     layer_forward,
     layer_backward,
     layer_forward_mxfp8,

@@ -255,6 +255,14 @@ def _f64(a):
     return np.asarray(a, dtype=np.float64)
 
 
+def round_bf16(x) -> np.ndarray:
+    """Round to the nearest bf16 value (ties to even), via float32: the top
+    16 bits of the float32 pattern after round-to-nearest-even."""
+    b = np.asarray(x, dtype=np.float64).astype(np.float32).view(np.uint32).astype(np.uint64)
+    r = (b + 0x7FFF + ((b >> 16) & 1)) & 0xFFFF0000
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
 def clamp_gate_up(g, u, limit):
     """The ``swiglu_limit`` of [MoKDoc] _MoKRuntime (named there, not
     defined), read as the usual clamped SwiGLU: with limit > 0 the gate
@@ -320,6 +328,9 @@ def layer_backward(x, router_w, top_experts, w_gate, w_up, w_down, dy,
     With ``swiglu_limit`` > 0 the clamp of ``clamp_gate_up`` is
     differentiated as the clamp itself: the gate gradient passes where
     g <= limit, the up gradient where |u| <= limit (the bounds included).
+    Those pass/stop decisions are taken on g and u rounded to bf16, the form
+    in which the forward keeps them for the backward (a decision is taken in
+    the kernel's precision; the values themselves stay float64 here).
     """
     x, w, dy = _f64(x), _f64(router_w), _f64(dy)
     wg, wu, wd = _f64(w_gate), _f64(w_up), _f64(w_down)
@@ -347,8 +358,9 @@ def layer_backward(x, router_w, top_experts, w_gate, w_up, w_down, dy,
         dg = dh * uc * sg * (1.0 + gc * (1.0 - sg))   # silu'(g) = s (1 + g (1 - s))
         du = dh * gc * sg
         if swiglu_limit and swiglu_limit > 0:         # the clamp's own derivative
-            dg = dg * (g <= swiglu_limit)
-            du = du * (np.abs(u) <= swiglu_limit)
+            lim = float(np.float32(swiglu_limit))
+            dg = dg * (round_bf16(g) <= lim)
+            du = du * (np.abs(round_bf16(u)) <= lim)
         dWg = dg.T @ v
         dWu = du.T @ v
         dv = dg @ Wg + du @ Wu

@@ -424,11 +424,28 @@ def _gate_up_values(inp):
 
 
 def _limit_between(vals, lo_q=0.6, hi_q=0.9):
-    """A limit in the widest gap between consecutive values of the given
-    quantile range, and the distance to the nearest value."""
+    """A limit in a gap between consecutive values of the given quantile
+    range, the widest one where every value and its bf16 rounding fall on
+    the same side of the limit (the backward's clamp decisions are taken on
+    bf16 values); returns the limit and the distance to the nearest value."""
     a = vals[int(lo_q * len(vals)):int(hi_q * len(vals))]
-    i = int(np.argmax(np.diff(a)))
-    return 0.5 * (a[i] + a[i + 1]), 0.5 * (a[i + 1] - a[i])
+    for i in np.argsort(-np.diff(a)):
+        L = float(np.float32(0.5 * (a[i] + a[i + 1])))
+        if np.array_equal(vals <= L, O.round_bf16(vals) <= L):
+            return L, 0.5 * (a[i + 1] - a[i])
+    raise AssertionError("no limit with consistent bf16 decisions")
+
+
+def test_round_bf16_matches_torch_cast():
+    """The oracle's bf16 rounding (float32 bits, ties to even) against
+    torch's float32 -> bfloat16 conversion, over wide magnitudes and exact
+    ties."""
+    rng = np.random.default_rng(5)
+    x = rng.normal(size=50000) * np.exp(rng.normal(size=50000) * 4)
+    ties = (np.arange(1, 2001, dtype=np.uint32) << 16 | 0x8000).view(np.float32).astype(np.float64)
+    for v in (x, ties, -ties):
+        ref = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16).double().numpy()
+        assert np.array_equal(O.round_bf16(v), ref)
 
 
 def test_swiglu_limit_off_and_huge_equal_the_plain_layer():
