@@ -11,6 +11,7 @@ from .mok_oracle import (  # noqa: F401
     STATUS_OK,
     STATUS_INDEX,
     mxfp8_roundtrip,
+    mxfp8_roundtrip_cols,
     build_schedule,
     e4m3_decode,
     e4m3_encode,
@@ -24,4 +25,5 @@ from .mok_oracle import (  # noqa: F401
     layer_backward,
     layer_forward_mxfp8,
     layer_backward_mxfp8,
+    layer_backward_mxfp8_full,
 )

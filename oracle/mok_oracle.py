@@ -449,3 +449,102 @@ def layer_backward_mxfp8(x, router_w, top_experts, w_gate, w_up, w_down, dy,
     del xq
     return layer_backward(x, router_w, top_experts, w_gate, w_up, w_down, dy,
                           ws_gate, ws_up, ws_down, gu_override=gu, swiglu_limit=swiglu_limit)
+
+
+# ---------------------------------------------------------------------------
+# MXFP8 backward  ([MoKEd] "Where MoK is the wrong tool": the MXFP8 backward
+#                  is one of the two measured layer passes; [OCP-MX])
+# ---------------------------------------------------------------------------
+
+def mxfp8_roundtrip_cols(m) -> np.ndarray:
+    """Quantise then dequantise along axis 0: every column is cut into blocks
+    of 32 consecutive rows (rows past the end count as zeros, which leave the
+    block amax unchanged), each block with its own E8M0 scale."""
+    m = np.asarray(m, dtype=np.float64)
+    R, C = m.shape
+    pad = (-R) % MX_BLOCK
+    mp = np.vstack([m, np.zeros((pad, C))]) if pad else m
+    return mxfp8_roundtrip(mp.T).T[:R]
+
+
+def layer_backward_mxfp8_full(x, router_w, top_experts, w_gate, w_up, w_down, dy,
+                              ws_gate=None, ws_up=None, ws_down=None, swiglu_limit=0.0):
+    """Backward of the MXFP8 forward with every backward GEMM on MXFP8
+    operands too (E4M3 values, one E8M0 scale per 32 elements along that
+    GEMM's contraction axis, exact products, float64 sums here):
+
+      dgrad through down     Z = dy . W_down[e]      dy rows along H;
+                                                     W_down[e] [H, I] along H
+      dgrad through gate/up  dx = dG W_gate + dU W_up  dG|dU rows along I;
+                                                     W_gate[e], W_up[e] [I, H] along I
+      weight gradients       dW_down = dy^T (w h), dW_gate = dG^T x, dW_up = dU^T x:
+                             both operands along the expert's rows, in
+                             schedule order (ascending f = t*k + j), 32
+                             consecutive rows per block; the shared expert
+                             takes 32 consecutive tokens per block.
+
+    The quantisers see the values the backward holds in bf16: the inputs dy
+    and x and the bf16 weights; the gate/up pre-activations of the quantised
+    forward as the forward saves them (rounded to bf16); dG, dU and w h
+    rounded to bf16.  The derivative is straight-through (quantisers count as
+    the identity); the router-weight gradient is <Z, h>; the clamp of
+    ``clamp_gate_up`` is differentiated as in ``layer_backward``.
+    Returns the dict of ``layer_backward``.
+    """
+    x, w, dy = _f64(x), _f64(router_w), _f64(dy)
+    wg, wu, wd = _f64(w_gate), _f64(w_up), _f64(w_down)
+    te = np.asarray(top_experts if not hasattr(top_experts, "numpy")
+                    else top_experts.cpu().numpy(), np.int64)
+    T, H = x.shape
+    k = te.shape[1]
+    E = wg.shape[0]
+    xq = mxfp8_roundtrip(x)
+    rows_q = mxfp8_roundtrip
+    cols_q = mxfp8_roundtrip_cols
+    lim = float(np.float32(swiglu_limit)) if swiglu_limit and swiglu_limit > 0 else 0.0
+
+    def one(v, vq, scale, dyv, Wg, Wu, Wd):
+        # the forward's pre-activations (quantised operands), kept as bf16
+        g = round_bf16(vq @ rows_q(Wg).T)
+        u = round_bf16(vq @ rows_q(Wu).T)
+        gc, uc = clamp_gate_up(g, u, lim)
+        sg = sigmoid(gc)
+        h = gc * sg * uc
+        z = rows_q(dyv) @ cols_q(Wd)                   # [n, I]
+        d_scale = np.sum(z * h, axis=1)
+        dh = scale[:, None] * z
+        dg = dh * uc * sg * (1.0 + gc * (1.0 - sg))
+        du = dh * gc * sg
+        if lim > 0:
+            dg = dg * (g <= lim)
+            du = du * (np.abs(u) <= lim)
+        dg, du = round_bf16(dg), round_bf16(du)
+        hw = round_bf16(scale[:, None] * h)
+        dWd = cols_q(dyv).T @ cols_q(hw)
+        vc = cols_q(v)
+        dWg = cols_q(dg).T @ vc
+        dWu = cols_q(du).T @ vc
+        dv = rows_q(dg) @ cols_q(Wg) + rows_q(du) @ cols_q(Wu)
+        return d_scale, dv, dWg, dWu, dWd
+
+    dx = np.zeros_like(x)
+    dw = np.zeros((T, k))
+    dwg, dwu, dwd = np.zeros_like(wg), np.zeros_like(wu), np.zeros_like(wd)
+    out = {}
+    if ws_gate is not None:
+        _, dv, dWg, dWu, dWd = one(x, xq, np.ones(T), dy, _f64(ws_gate), _f64(ws_up), _f64(ws_down))
+        dx += dv
+        out["d_ws_gate"], out["d_ws_up"], out["d_ws_down"] = dWg, dWu, dWd
+    for e in range(E):
+        t_idx, j_idx = np.nonzero(te == e)            # row-major: ascending f
+        if t_idx.size == 0:
+            continue
+        d_scale, dv, dWg, dWu, dWd = one(x[t_idx], xq[t_idx], w[t_idx, j_idx], dy[t_idx],
+                                         wg[e], wu[e], wd[e])
+        dw[t_idx, j_idx] = d_scale
+        np.add.at(dx, t_idx, dv)
+        dwg[e] += dWg
+        dwu[e] += dWu
+        dwd[e] += dWd
+    out.update(dx=dx, d_router_w=dw, d_w_gate=dwg, d_w_up=dwu, d_w_down=dwd)
+    return out

@@ -537,3 +537,109 @@ def test_swiglu_limit_backward_matches_finite_differences(shared):
     # the mask matters: the unclamped gradients differ
     g_plain = O.layer_backward(*a[:6], inp.dy, *a[6:])
     assert not np.allclose(g_plain["dx"], g["dx"])
+
+
+# ------------------------------------------------------------------ MXFP8 backward
+
+def _bf16_torch(a):
+    """bf16 rounding through torch casts (float64 -> float32 -> bfloat16)."""
+    return torch.from_numpy(np.asarray(a, np.float64)).float().bfloat16().double().numpy()
+
+
+def test_mxfp8_full_backward_matches_brute_force():
+    """Every backward GEMM operand quantised by the brute-force codec, vector
+    by vector along the axis the reading names (rows of dy and dG|dU; columns
+    of W_down along H and of W_gate, W_up along I; columns of the weight
+    gradients' operands over 32-row groups of each expert's rows, taken in
+    ascending f), then contracted by explicit scalar sums."""
+    T, H, I, E, k, Is = 24, 64, 32, 2, 2, 32
+    inp = _tiny(T=T, H=H, I=I, E=E, k=k, I_s=Is, seed=13)
+    got = O.layer_backward_mxfp8_full(*_args(inp)[:6], inp.dy, *_args(inp)[6:])
+    x, dy = inp.x.double().numpy(), inp.dy.double().numpy()
+    te, rw = inp.top_experts.numpy(), inp.router_w.double().numpy()
+
+    def q_vec_rows(m):           # quantise each row of m (blocks along the row)
+        return np.stack([_brute_q(r) for r in m])
+
+    def q_vec_cols(m):           # quantise each column of m (blocks down the column)
+        n = m.shape[0]
+        pad = (-n) % 32
+        out = np.empty_like(m)
+        for c in range(m.shape[1]):
+            col = np.concatenate([m[:, c], np.zeros(pad)])
+            out[:, c] = _brute_q(col)[:n]
+        return out
+
+    def dot(a, b):
+        return sum(a[i] * b[i] for i in range(len(a)))
+
+    def expert_bwd(rows, wts, Wg, Wu, Wd):
+        n, Iw = len(rows), Wg.shape[0]
+        v, d = x[rows], dy[rows]
+        vq, dq = q_vec_rows(v), q_vec_rows(d)
+        Wgq, Wuq = q_vec_rows(Wg), q_vec_rows(Wu)          # forward: along H
+        Wdc = q_vec_cols(Wd)                               # dgrad through down: along H
+        Wgc, Wuc = q_vec_cols(Wg), q_vec_cols(Wu)          # dgrad through gate/up: along I
+        dsc = np.zeros(n)
+        dg, du, hw = np.zeros((n, Iw)), np.zeros((n, Iw)), np.zeros((n, Iw))
+        for r in range(n):
+            for i in range(Iw):
+                g = _bf16_torch(dot(vq[r], Wgq[i]))
+                u = _bf16_torch(dot(vq[r], Wuq[i]))
+                s = 1.0 / (1.0 + math.exp(-g))
+                z = dot(dq[r], Wdc[:, i])
+                h = g * s * u
+                dsc[r] += z * h
+                dg[r, i] = wts[r] * z * u * s * (1.0 + g * (1.0 - s))
+                du[r, i] = wts[r] * z * g * s
+                hw[r, i] = wts[r] * h
+        dg, du, hw = _bf16_torch(dg), _bf16_torch(du), _bf16_torch(hw)
+        dgq, duq = q_vec_rows(dg), q_vec_rows(du)
+        dv = np.array([[dot(dgq[r], Wgc[:, c]) + dot(duq[r], Wuc[:, c]) for c in range(H)] for r in range(n)])
+        dc, hc, gc_, uc_, vc = (q_vec_cols(a) for a in (d, hw, dg, du, v))
+        dWd = np.array([[dot(dc[:, a], hc[:, b]) for b in range(Iw)] for a in range(H)])
+        dWg = np.array([[dot(gc_[:, a], vc[:, b]) for b in range(H)] for a in range(Iw)])
+        dWu = np.array([[dot(uc_[:, a], vc[:, b]) for b in range(H)] for a in range(Iw)])
+        return dsc, dv, dWg, dWu, dWd
+
+    dx = np.zeros((T, H))
+    dsc, dv, dWg, dWu, dWd = expert_bwd(list(range(T)), np.ones(T), inp.ws_gate.double().numpy(),
+                                        inp.ws_up.double().numpy(), inp.ws_down.double().numpy())
+    dx += dv
+    for key, want in (("d_ws_gate", dWg), ("d_ws_up", dWu), ("d_ws_down", dWd)):
+        np.testing.assert_allclose(got[key], want, rtol=1e-9, atol=1e-12)
+    for e in range(E):
+        fl = sorted(t * k + j for t in range(T) for j in range(k) if te[t, j] == e)
+        rows = [f // k for f in fl]
+        wts = np.array([rw[f // k, f % k] for f in fl])
+        dsc, dv, dWg, dWu, dWd = expert_bwd(rows, wts, inp.w_gate[e].double().numpy(),
+                                            inp.w_up[e].double().numpy(), inp.w_down[e].double().numpy())
+        for n, f in enumerate(fl):
+            dx[f // k] += dv[n]
+            np.testing.assert_allclose(got["d_router_w"][f // k, f % k], dsc[n], rtol=1e-9, atol=1e-12)
+        np.testing.assert_allclose(got["d_w_gate"][e], dWg, rtol=1e-9, atol=1e-12)
+        np.testing.assert_allclose(got["d_w_up"][e], dWu, rtol=1e-9, atol=1e-12)
+        np.testing.assert_allclose(got["d_w_down"][e], dWd, rtol=1e-9, atol=1e-12)
+    np.testing.assert_allclose(got["dx"], dx, rtol=1e-9, atol=1e-12)
+
+
+def test_mxfp8_full_backward_scales_with_dy_by_powers_of_two():
+    """Scaling dy by 2^5 scales every gradient by exactly 2^5: every
+    quantiser commutes with power-of-two scaling (the block scale absorbs
+    it) and the bf16 roundings do too."""
+    inp = _tiny(T=20, H=64, I=64, E=3, k=2, I_s=32, seed=14)
+    a = O.layer_backward_mxfp8_full(*_args(inp)[:6], inp.dy, *_args(inp)[6:])
+    b = O.layer_backward_mxfp8_full(*_args(inp)[:6], inp.dy.double() * 32.0, *_args(inp)[6:])
+    for key in a:
+        np.testing.assert_array_equal(b[key], 32.0 * a[key])
+
+
+def test_mxfp8_full_backward_close_to_straight_through_bf16_backward():
+    """The quantised backward stays within the MXFP8 error of the bf16
+    backward of the same quantised forward, output by output."""
+    inp = _tiny(T=64, H=128, I=64, E=4, k=2, I_s=64, seed=15)
+    a = O.layer_backward_mxfp8_full(*_args(inp)[:6], inp.dy, *_args(inp)[6:])
+    b = O.layer_backward_mxfp8(*_args(inp)[:6], inp.dy, *_args(inp)[6:])
+    for key in b:
+        rel = np.linalg.norm(a[key] - b[key]) / np.linalg.norm(b[key])
+        assert 3e-3 < rel < 0.12, (key, rel)
