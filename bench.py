@@ -86,18 +86,28 @@ def job_tokens_per_s(T, world, steps, total_ms):
 def launches_per_step(c):
     """Kernels of this library launched by one step (mirrors the C ABI's sequence
     with the default permuted dispatch)."""
-    mx = c["mode"] == "mxfp8"
+    mode = c["mode"]
+    mx = mode in ("mxfp8", "mxfp8_full")
+    full = mode == "mxfp8_full"
     shared = c["I_s"] > 0
+    s3 = 3 if shared else 0
     n = 3                                   # schedule: count, scan, scatter
     n += 1 + 2 + 1                          # status hand-over, routed gate/up + down, combine
     if shared:
         n += 2
     if mx:
-        n += 3 + (3 if shared else 0)       # weight prequantisation (every step)
-        n += 3 + (3 if shared else 0)       # weight scales into the tensor-core layout
+        n += 3 + s3                         # weight prequantisation (every step)
+        n += 3 + s3                         # weight scales into the tensor-core layout
         n += 1                              # x quantised into token and schedule order
     else:
         n += 1                              # x rows into schedule order
+    if full:
+        n += 3 + s3                         # transposed weight prequantisation (every step)
+        n += 3 + s3                         # their scales into the tensor-core layout
+        n += 3 + (2 if shared else 0)       # x transposed, dy rows, dy transposed (+ token order)
+        n += 7 + (7 if shared else 0)       # per expert set: 4 GEMMs + 3 quantisations of dG|dU, w h
+        n += 2                              # combine dx, reduce d_w
+        return n
     n += 1 + (1 if mx else 0)               # dy rows (and bf16 x rows) into schedule order
     n += 4 + 2                              # routed dgrad/wgrad x4, combine dx, reduce d_w
     if shared:
@@ -208,8 +218,9 @@ class OracleSample:
         self.dy = inp.dy[:tokens].double().numpy()
         self.W = [None if t is None else t.double().numpy() for t in
                   (inp.w_gate, inp.w_up, inp.w_down, inp.ws_gate, inp.ws_up, inp.ws_down)]
-        self.fwd = oracle.layer_forward_mxfp8 if mode == "mxfp8" else oracle.layer_forward
-        self.bwd = oracle.layer_backward_mxfp8 if mode == "mxfp8" else oracle.layer_backward
+        self.fwd = oracle.layer_forward_mxfp8 if mode in ("mxfp8", "mxfp8_full") else oracle.layer_forward
+        self.bwd = {"mxfp8": oracle.layer_backward_mxfp8,
+                    "mxfp8_full": oracle.layer_backward_mxfp8_full}.get(mode, oracle.layer_backward)
 
     def run(self, min_s=0.0):
         """Repeat fwd+bwd until at least min_s seconds passed; returns (seconds, reps)."""
@@ -255,8 +266,9 @@ def main():
     fwd_flop, step_flop = layer_flops(c)
     config = {"workload": args.workload, "T": c["T"], "H": c["H"], "I": c["I"], "E": c["E"], "k": c["k"],
               "I_s": c["I_s"], "routing": "zipf s=%.1f" % c["skew"] if c["skew"] else "softmax top-k",
-              "minibatch": c["minibatch"], "capacity_multiplier": c["capacity"], "fwd_precision": c["mode"],
-              "bwd_precision": "bf16", "global_batch_tokens": c["T"] * max(world, 1),
+              "minibatch": c["minibatch"], "capacity_multiplier": c["capacity"],
+              "fwd_precision": "bf16" if c["mode"] == "bf16" else "mxfp8",
+              "bwd_precision": "mxfp8" if c["mode"] == "mxfp8_full" else "bf16", "global_batch_tokens": c["T"] * max(world, 1),
               "parallelism": f"dp{world} (independent batches, no collective)"}
 
     if args.impl == "reference":
@@ -284,9 +296,9 @@ def main():
     mode = c["mode"]
     E, T, k, H, I, Is = c["E"], c["T"], c["k"], c["H"], c["I"], c["I_s"]
     lib = _lib.load()
-    m = _lib.MOK_MODE_MXFP8_FWD if mode == "mxfp8" else _lib.MOK_MODE_BF16
+    m = mok.MODES[mode]
     ctx_buf = torch.empty(lib.mok_ctx_bytes(T, k, E, H, I, Is, m), dtype=torch.uint8, device=dev)
-    ws_buf = torch.empty(lib.mok_bwd_workspace_bytes(T, k, E, H, I, Is), dtype=torch.uint8, device=dev)
+    ws_buf = torch.empty(lib.mok_bwd_workspace_bytes(T, k, E, H, I, Is, m), dtype=torch.uint8, device=dev)
     y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     grads = {"dx": torch.empty((T, H), dtype=torch.bfloat16, device=dev),
              "d_router_w": torch.empty((T, k), dtype=torch.float32, device=dev),
@@ -299,7 +311,7 @@ def main():
     stream = torch.cuda.current_stream()
 
     def run_step(x, rw, top, dy, events=None):
-        wq = mok.quantize_weights(w) if mode == "mxfp8" else w
+        wq = mok.quantize_weights(w, backward=(mode == "mxfp8_full")) if mode != "bf16" else w
         sched = mok.schedule(top, E, c["capacity"])
         _, ctx = mok.forward(x, rw, sched, wq, mode=mode, minibatch=c["minibatch"], out=y, ctx_buf=ctx_buf,
                              events=events)
@@ -446,7 +458,7 @@ def main():
     kind = "sustained" if long_step else "burst"
     base_src = (f"{peaks['source']} bf16 {kind} (MEASURED_PEAKS.json)" if peaks["source"] == "measured"
                 else f"fallback bf16 {kind}")
-    if mode == "mxfp8" and dom in FWD_GEMM_STAGES:
+    if (mode == "mxfp8" and dom in FWD_GEMM_STAGES) or mode == "mxfp8_full":
         # block-scaled E4M3 GEMM: the bf16 figure times the nominal dense fp8:bf16 ratio (4.5 / 2.25)
         dom_peak, dom_src = 2.0 * peaks[peak_key], base_src + " x 2 (nominal dense fp8:bf16 ratio)"
     else:
@@ -455,7 +467,8 @@ def main():
         "metric": METRIC,
         "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": max(world, 1), "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if mode == "bf16" else "mxfp8-fwd/bf16-bwd",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": {"bf16": "bf16", "mxfp8": "mxfp8-fwd/bf16-bwd"}.get(mode, "mxfp8-fwd/mxfp8-bwd"),
         "data": "synthetic (seeded; weights N(0,0.02), x and dy N(0,1), softmax top-k routing)",
         "config": dict(config, l2="flushed between steps (512 MiB write, outside the timed spans)"),
         "tflops": round(tflops, 1),

@@ -65,6 +65,13 @@ typedef int mok_status_t;
 
 #define MOK_MODE_BF16       0   /* forward and backward in bf16, fp32 accumulate */
 #define MOK_MODE_MXFP8_FWD  1   /* forward GEMMs on MXFP8 operands, backward in bf16 */
+#define MOK_MODE_MXFP8      2   /* forward and backward GEMMs on MXFP8 operands: each
+                                   backward GEMM quantises both operands along its own
+                                   contraction axis (dgrad: dy and dG|dU by rows, the
+                                   weights along H or I; weight gradients: both
+                                   operands over 32 consecutive rows of an expert in
+                                   schedule order, or 32 consecutive tokens for the
+                                   shared expert); fp32 accumulate, bf16 outputs */
 
 /* Debug flags (mok_config_t.debug_flags). */
 #define MOK_DEBUG_DROP_ACC_SIGNAL 1  /* the first forward GEMM withholds one
@@ -187,6 +194,15 @@ typedef struct {
   const uint8_t* mxs_gate; const uint8_t* mxs_gate_sc;  /* [I_s][H], [I_s][H/32] */
   const uint8_t* mxs_up;   const uint8_t* mxs_up_sc;    /* [I_s][H], [I_s][H/32] */
   const uint8_t* mxs_down; const uint8_t* mxs_down_sc;  /* [H][I_s], [H][I_s/32] */
+  /* MOK_MODE_MXFP8 only: each weight quantised along its leading axis (the
+   * axis the backward's dgrad GEMMs contract over), as made by
+   * mok_mxfp8_quantize_t: codes of the transpose, scales [..][leading/32]. */
+  const uint8_t* mxt_gate;  const uint8_t* mxt_gate_sc;   /* [E][H][I], [E][H][I/32] */
+  const uint8_t* mxt_up;    const uint8_t* mxt_up_sc;     /* [E][H][I], [E][H][I/32] */
+  const uint8_t* mxt_down;  const uint8_t* mxt_down_sc;   /* [E][I][H], [E][I][H/32] */
+  const uint8_t* mxts_gate; const uint8_t* mxts_gate_sc;  /* [H][I_s], [H][I_s/32] */
+  const uint8_t* mxts_up;   const uint8_t* mxts_up_sc;    /* [H][I_s], [H][I_s/32] */
+  const uint8_t* mxts_down; const uint8_t* mxts_down_sc;  /* [I_s][H], [I_s][H/32] */
 } mok_weights_t;
 
 /* Forward context: activations saved for the backward plus forward scratch,
@@ -291,6 +307,17 @@ mok_status_t mok_schedule_noalloc(const int64_t* top_experts, int T, int k, int 
 mok_status_t mok_mxfp8_quantize(const uint16_t* x, int64_t rows, int K,
                                 uint8_t* codes, uint8_t* scales, void* stream);
 
+/* Transposing MXFP8 quantiser for the MOK_MODE_MXFP8 backward (the weights'
+ * copies quantised along their leading axis, [MoKEd] "Tuning the five
+ * hyperparameters before production": weights are prequantised by the
+ * caller).  x bf16 [batch][rows][cols] -> codes E4M3 [batch][cols][rows] (the
+ * transpose) and scales E8M0 [batch][cols][rows/32]: one scale per 32
+ * consecutive rows of each column, with the block rule of
+ * mok_mxfp8_quantize.  Needs rows % 32 == 0 and cols % 64 == 0; inputs
+ * finite; x and codes 16-byte aligned. */
+mok_status_t mok_mxfp8_quantize_t(const uint16_t* x, int64_t batch, int rows, int cols,
+                                  uint8_t* codes, uint8_t* scales, void* stream);
+
 /* ---- forward ([MoKDoc] _MoKRuntime.forward) -----------------------------
  * y[t] = S(x[t]) + sum_j w[t,j] * F_{e[t,j]}(x[t]),
  * F_e(v) = W_down[e] (silu(W_gate[e] v) * (W_up[e] v)), S the same with the
@@ -309,13 +336,16 @@ mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x,
 mok_status_t mok_ctx_status(const mok_ctx_t* ctx, int* status);
 
 /* ---- backward ([MoKDoc] _MoKRuntime.backward) ---------------------------
- * Exact gradients of the forward given dy = dL/dy (bf16 [T][H]); in MXFP8
- * mode the derivative treats the quantisers as the identity and is taken at
- * the saved gate/up pre-activations.  x and router_w are the forward's
- * inputs.  Outputs: dx bf16 [T][H], d_router_w fp32 [T][k] (= <dy[t],
- * F_e(x[t])>), the six weight gradients.  Scratch comes from `ws`
- * (mok_bwd_workspace_bytes).  Device errors land in ctx->status. */
-size_t mok_bwd_workspace_bytes(int T, int k, int E, int H, int I, int I_s);
+ * Exact gradients of the forward given dy = dL/dy (bf16 [T][H]); in the
+ * MXFP8 modes the derivative treats the quantisers as the identity and is
+ * taken at the saved gate/up pre-activations.  The backward runs in the mode
+ * the forward recorded in the context: bf16 GEMMs after MOK_MODE_BF16 and
+ * MOK_MODE_MXFP8_FWD, MXFP8 GEMMs after MOK_MODE_MXFP8 (which needs the
+ * weights' mxt* copies).  x and router_w are the forward's inputs.  Outputs:
+ * dx bf16 [T][H], d_router_w fp32 [T][k] (= <dy[t], F_e(x[t])>), the six
+ * weight gradients.  Scratch comes from `ws` (mok_bwd_workspace_bytes with
+ * the context's mode).  Device errors land in ctx->status. */
+size_t mok_bwd_workspace_bytes(int T, int k, int E, int H, int I, int I_s, int mode);
 mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy,
                           const uint16_t* x, const float* router_w,
                           const mok_schedule_t* sched, const mok_ctx_t* ctx,

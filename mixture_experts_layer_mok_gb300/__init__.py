@@ -17,8 +17,12 @@ import torch
 from . import _lib
 from ._lib import MokError  # noqa: F401
 
-__all__ = ["schedule", "schedule_noalloc", "mxfp8_quantize", "forward", "backward", "Schedule", "Weights", "Context",
-           "MokError", "quantize_weights"]
+__all__ = ["schedule", "schedule_noalloc", "mxfp8_quantize", "mxfp8_quantize_t", "forward", "backward", "Schedule",
+           "Weights", "Context", "MokError", "quantize_weights", "MODES"]
+
+# forward/backward precision: "bf16"; "mxfp8" (MXFP8 forward GEMMs, bf16
+# backward); "mxfp8_full" (MXFP8 forward and backward GEMMs)
+MODES = {"bf16": _lib.MOK_MODE_BF16, "mxfp8": _lib.MOK_MODE_MXFP8_FWD, "mxfp8_full": _lib.MOK_MODE_MXFP8}
 
 
 def _ptr(t):
@@ -75,7 +79,7 @@ class Weights:
     ws_gate: torch.Tensor | None = None
     ws_up: torch.Tensor | None = None
     ws_down: torch.Tensor | None = None
-    mx: dict | None = None  # name -> (codes, scales) for MXFP8 mode
+    mx: dict | None = None  # name -> (codes, scales) for the MXFP8 modes
 
     @property
     def dims(self):
@@ -161,13 +165,39 @@ def mxfp8_quantize(x: torch.Tensor, stream=None):
     return codes, scales
 
 
-def quantize_weights(w: Weights, stream=None) -> Weights:
-    """Prequantise every weight along its K axis for MXFP8 mode."""
+def mxfp8_quantize_t(x: torch.Tensor, stream=None):
+    """bf16 [batch, rows, cols] (or [rows, cols]) -> (E4M3 codes of the
+    transpose uint8 [batch, cols, rows], E8M0 scales uint8 [batch, cols,
+    rows/32]): one scale per 32 consecutive rows of each column."""
+    lib = _lib.load()
+    if x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous() or x.dim() not in (2, 3):
+        raise ValueError("x must be a contiguous CUDA bf16 matrix or batch of matrices")
+    x3 = x if x.dim() == 3 else x.unsqueeze(0)
+    B, R, Cc = x3.shape
+    codes = torch.empty((B, Cc, R), dtype=torch.uint8, device=x.device)
+    scales = torch.empty((B, Cc, R // 32), dtype=torch.uint8, device=x.device)
+    _lib.check(lib.mok_mxfp8_quantize_t(_ptr(x3), B, R, Cc, _ptr(codes), _ptr(scales), _stream(stream)),
+               "mok_mxfp8_quantize_t")
+    if x.dim() == 2:
+        codes, scales = codes[0], scales[0]
+    return codes, scales
+
+
+def quantize_weights(w: Weights, stream=None, backward: bool = False) -> Weights:
+    """Prequantise every weight along its K axis for the MXFP8 modes; with
+    ``backward`` also along its leading axis (the transposed copies the
+    "mxfp8_full" backward's dgrad GEMMs read)."""
     mx = {"_gate": mxfp8_quantize(w.w_gate, stream), "_up": mxfp8_quantize(w.w_up, stream),
           "_down": mxfp8_quantize(w.w_down, stream)}
     if w.ws_gate is not None:
         mx.update({"s_gate": mxfp8_quantize(w.ws_gate, stream), "s_up": mxfp8_quantize(w.ws_up, stream),
                    "s_down": mxfp8_quantize(w.ws_down, stream)})
+    if backward:
+        mx.update({"t_gate": mxfp8_quantize_t(w.w_gate, stream), "t_up": mxfp8_quantize_t(w.w_up, stream),
+                   "t_down": mxfp8_quantize_t(w.w_down, stream)})
+        if w.ws_gate is not None:
+            mx.update({"ts_gate": mxfp8_quantize_t(w.ws_gate, stream), "ts_up": mxfp8_quantize_t(w.ws_up, stream),
+                       "ts_down": mxfp8_quantize_t(w.ws_down, stream)})
     return Weights(w.w_gate, w.w_up, w.w_down, w.ws_gate, w.ws_up, w.ws_down, mx)
 
 
@@ -190,7 +220,8 @@ def _config(mode, minibatch, debug, events=None, dispatch="auto", swiglu_limit=0
 def forward(x, router_w, sched: Schedule, weights: Weights, mode: str = "bf16", minibatch: int = 0,
             debug: int = 0, out=None, ctx_buf=None, stream=None, events=None, dispatch="auto",
             swiglu_limit: float = 0.0):
-    """y = layer(x); returns (y, Context).  ``mode`` is "bf16" or "mxfp8";
+    """y = layer(x); returns (y, Context).  ``mode`` is "bf16", "mxfp8" or
+    "mxfp8_full" (see ``MODES``; the backward follows the forward's mode);
     ``dispatch`` is "auto", "permute" or "fused" (same results, different kernels).
     ``swiglu_limit`` > 0 clamps the SwiGLU pre-activations (gate to <= L, up
     to [-L, L]); the backward follows the forward's value.
@@ -198,7 +229,9 @@ def forward(x, router_w, sched: Schedule, weights: Weights, mode: str = "bf16", 
     None entry records nothing (each record costs a few microseconds on the
     device, so a timing run can watch one stage alone)."""
     lib = _lib.load()
-    m = _lib.MOK_MODE_MXFP8_FWD if mode == "mxfp8" else _lib.MOK_MODE_BF16
+    if mode not in MODES:
+        raise ValueError(f"mode must be one of {sorted(MODES)}")
+    m = MODES[mode]
     E, H, I, I_s = weights.dims
     T, k = sched.T, sched.k
     _need(x, torch.bfloat16, (T, H), "x")
@@ -239,7 +272,7 @@ def backward(dy, x, router_w, sched: Schedule, ctx: Context, weights: Weights, m
     for name in ("d_w_gate", "d_w_up", "d_w_down", "d_ws_gate", "d_ws_up", "d_ws_down"):
         if name in grads:
             setattr(g, name, grads[name].data_ptr())
-    nbytes = lib.mok_bwd_workspace_bytes(T, k, E, H, I, I_s)
+    nbytes = lib.mok_bwd_workspace_bytes(T, k, E, H, I, I_s, ctx.mode)
     if ws_buf is None or ws_buf.numel() < nbytes:
         ws_buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     cfg = _config(ctx.mode, minibatch, debug, events, dispatch)

@@ -17,6 +17,7 @@ MOK_ERR_TIMEOUT = 5
 MOK_ERR_CUDA = 6
 MOK_MODE_BF16 = 0
 MOK_MODE_MXFP8_FWD = 1
+MOK_MODE_MXFP8 = 2
 MOK_DEBUG_DROP_ACC_SIGNAL = 1
 MOK_DEBUG_TMA_GATHER4 = 2
 MOK_DISPATCH_AUTO = 0
@@ -55,7 +56,10 @@ class MokWeights(C.Structure):
                 ("w_gate", P), ("w_up", P), ("w_down", P), ("ws_gate", P), ("ws_up", P), ("ws_down", P),
                 ("mx_gate", P), ("mx_gate_sc", P), ("mx_up", P), ("mx_up_sc", P),
                 ("mx_down", P), ("mx_down_sc", P), ("mxs_gate", P), ("mxs_gate_sc", P),
-                ("mxs_up", P), ("mxs_up_sc", P), ("mxs_down", P), ("mxs_down_sc", P)]
+                ("mxs_up", P), ("mxs_up_sc", P), ("mxs_down", P), ("mxs_down_sc", P),
+                ("mxt_gate", P), ("mxt_gate_sc", P), ("mxt_up", P), ("mxt_up_sc", P),
+                ("mxt_down", P), ("mxt_down_sc", P), ("mxts_gate", P), ("mxts_gate_sc", P),
+                ("mxts_up", P), ("mxts_up_sc", P), ("mxts_down", P), ("mxts_down_sc", P)]
 
 
 class MokCtx(C.Structure):
@@ -83,11 +87,12 @@ SIGNATURES = {
     "mok_schedule_noalloc": (C.c_int, [P, C.c_int, C.c_int, C.c_int, C.c_float, P, C.c_size_t,
                                        C.POINTER(MokSchedule), P]),
     "mok_mxfp8_quantize": (C.c_int, [P, C.c_int64, C.c_int, P, P, P]),
+    "mok_mxfp8_quantize_t": (C.c_int, [P, C.c_int64, C.c_int, C.c_int, P, P, P]),
     "mok_ctx_bytes": (C.c_size_t, [C.c_int] * 7),
     "mok_forward": (C.c_int, [C.POINTER(MokConfig), P, P, C.POINTER(MokSchedule),
                               C.POINTER(MokWeights), P, P, C.c_size_t, C.POINTER(MokCtx), P]),
     "mok_ctx_status": (C.c_int, [C.POINTER(MokCtx), I32P]),
-    "mok_bwd_workspace_bytes": (C.c_size_t, [C.c_int] * 6),
+    "mok_bwd_workspace_bytes": (C.c_size_t, [C.c_int] * 7),
     "mok_backward": (C.c_int, [C.POINTER(MokConfig), P, P, P, C.POINTER(MokSchedule), C.POINTER(MokCtx),
                                C.POINTER(MokWeights), P, P, C.POINTER(MokWeightGrads), P, C.c_size_t, P]),
 }

@@ -26,8 +26,8 @@ class MoKFunction(torch.autograd.Function):
         E = w_gate.shape[0]
         sched = schedule(top_experts, E, capacity)
         weights = Weights(w_gate, w_up, w_down, ws_gate, ws_up, ws_down)
-        if mode == "mxfp8":
-            weights = quantize_weights(weights)
+        if mode in ("mxfp8", "mxfp8_full"):
+            weights = quantize_weights(weights, backward=(mode == "mxfp8_full"))
         y, mctx = forward(x, router_w, sched, weights, mode=mode, minibatch=minibatch, swiglu_limit=swiglu_limit)
         ctx.save_for_backward(x, router_w)
         ctx.mok = (sched, mctx, weights, minibatch, ws_gate is not None)

@@ -241,7 +241,7 @@ size_t carve_ctx(void* buf, int T, int k, int E, int H, int I, int Is, int mode,
                  CtxExtra* X) {
   const long long mr = max_tiles_of(T, k, E) * kTileRows;
   const long long n = static_cast<long long>(T) * k;
-  const bool mx = (mode == MOK_MODE_MXFP8_FWD);
+  const bool mx = (mode == MOK_MODE_MXFP8_FWD || mode == MOK_MODE_MXFP8);
   Carver c(buf);
   memset(ctx, 0, sizeof(*ctx));
   memset(X, 0, sizeof(*X));
@@ -283,6 +283,14 @@ size_t carve_ctx(void* buf, int T, int k, int E, int H, int I, int Is, int mode,
 struct BwdLayout {
   uint16_t *dgu, *hw, *dx_slots, *dgu_s, *hs, *dx_s, *dy_perm, *xb_perm;
   float* dw_part;
+  // MOK_MODE_MXFP8: E4M3 operands of the backward GEMMs and their E8M0 scales
+  // (tensor-core scale layout).  Row-quantised: dy (schedule and token order),
+  // dG|dU.  Transposed (blocks along the rows): dy, x, dG|dU, w h, and the
+  // shared expert's.  Weight scales of the caller's transposed copies.
+  uint8_t *dyq, *dyq_sc, *dyq_tok, *dyq_tok_sc, *dyT, *dyT_sc, *dyT_tok, *dyT_tok_sc;
+  uint8_t *xT, *xT_sc, *xT_tok, *xT_tok_sc, *dguq, *dguq_sc, *dguT, *dguT_sc, *hwT, *hwT_sc;
+  uint8_t *dgusq, *dgusq_sc, *dgusT, *dgusT_sc, *hsT, *hsT_sc;
+  uint8_t *wtg_sc, *wtu_sc, *wtd_sc, *wtsg_sc, *wtsu_sc, *wtsd_sc;
 };
 
 int tile_n(int N) { return (N % 256 == 0) ? 256 : 128; }
@@ -305,21 +313,60 @@ cudaError_t launch_tiles(const GemmMaps& m, const GemmParams& p, long long items
 // Pair work items: row tiles taken two at a time.
 long long row_pairs(long long rows) { return ((rows + 127) / 128 + 1) / 2; }
 
-size_t carve_bwd(void* buf, int T, int k, int E, int H, int I, int Is, BwdLayout* L) {
+size_t carve_bwd(void* buf, int T, int k, int E, int H, int I, int Is, int mode, BwdLayout* L) {
   const long long mr = max_tiles_of(T, k, E) * kTileRows;
   const long long n = static_cast<long long>(T) * k;
+  const long long Tl = T, Tp = (Tl + 127) / 128 * 128;
+  const bool mx = (mode == MOK_MODE_MXFP8);
   Carver c(buf);
   memset(L, 0, sizeof(*L));
   L->dgu = c.take<uint16_t>(mr * 2 * I);
   L->hw = c.take<uint16_t>(mr * I);
-  L->dw_part = c.take<float>(n * 2 * (I / tile_n(I)));  // two column halves per N tile
+  // two column halves per N tile (128-wide tiles in the MXFP8 backward)
+  L->dw_part = c.take<float>(n * 2 * (I / (mx ? 128 : tile_n(I))));
   L->dx_slots = c.take<uint16_t>(mr * H);
-  L->dy_perm = c.take<uint16_t>(mr * H);
-  L->xb_perm = c.take<uint16_t>(mr * H);
+  if (!mx) {
+    L->dy_perm = c.take<uint16_t>(mr * H);
+    L->xb_perm = c.take<uint16_t>(mr * H);
+  }
   if (Is > 0) {
-    L->dgu_s = c.take<uint16_t>(static_cast<long long>(T) * 2 * Is);
-    L->hs = c.take<uint16_t>(static_cast<long long>(T) * Is);
-    L->dx_s = c.take<uint16_t>(static_cast<long long>(T) * H);
+    L->dgu_s = c.take<uint16_t>(Tl * 2 * Is);
+    L->hs = c.take<uint16_t>(Tl * Is);
+    L->dx_s = c.take<uint16_t>(Tl * H);
+  }
+  if (mx) {
+    L->dyq = c.take<uint8_t>(mr * H);
+    L->dyq_sc = c.take<uint8_t>(tiled_scale_bytes(mr, H));
+    L->dyq_tok = c.take<uint8_t>(Tl * H);
+    L->dyq_tok_sc = c.take<uint8_t>(tiled_scale_bytes(Tl, H));
+    L->dyT = c.take<uint8_t>(mr * H);
+    L->dyT_sc = c.take<uint8_t>(tiled_scale_bytes(H, mr));
+    L->xT = c.take<uint8_t>(mr * H);
+    L->xT_sc = c.take<uint8_t>(tiled_scale_bytes(H, mr));
+    L->dguq = c.take<uint8_t>(mr * 2 * I);
+    L->dguq_sc = c.take<uint8_t>(tiled_scale_bytes(mr, 2 * I));
+    L->dguT = c.take<uint8_t>(mr * 2 * I);
+    L->dguT_sc = c.take<uint8_t>(tiled_scale_bytes(2 * I, mr));
+    L->hwT = c.take<uint8_t>(mr * I);
+    L->hwT_sc = c.take<uint8_t>(tiled_scale_bytes(I, mr));
+    L->wtg_sc = c.take<uint8_t>(tiled_scale_bytes(static_cast<long long>(E) * H, I));
+    L->wtu_sc = c.take<uint8_t>(tiled_scale_bytes(static_cast<long long>(E) * H, I));
+    L->wtd_sc = c.take<uint8_t>(tiled_scale_bytes(static_cast<long long>(E) * I, H));
+    if (Is > 0) {
+      L->dyT_tok = c.take<uint8_t>(Tp * H);
+      L->dyT_tok_sc = c.take<uint8_t>(tiled_scale_bytes(H, Tp));
+      L->xT_tok = c.take<uint8_t>(Tp * H);
+      L->xT_tok_sc = c.take<uint8_t>(tiled_scale_bytes(H, Tp));
+      L->dgusq = c.take<uint8_t>(Tl * 2 * Is);
+      L->dgusq_sc = c.take<uint8_t>(tiled_scale_bytes(Tl, 2 * Is));
+      L->dgusT = c.take<uint8_t>(Tp * 2 * Is);
+      L->dgusT_sc = c.take<uint8_t>(tiled_scale_bytes(2 * Is, Tp));
+      L->hsT = c.take<uint8_t>(Tp * Is);
+      L->hsT_sc = c.take<uint8_t>(tiled_scale_bytes(Is, Tp));
+      L->wtsg_sc = c.take<uint8_t>(tiled_scale_bytes(H, Is));
+      L->wtsu_sc = c.take<uint8_t>(tiled_scale_bytes(H, Is));
+      L->wtsd_sc = c.take<uint8_t>(tiled_scale_bytes(Is, H));
+    }
   }
   return c.off + 256;
 }
@@ -363,7 +410,7 @@ cudaError_t mark(const mok_config_t* cfg, int stage, int end, cudaStream_t st) {
 }
 
 mok_status_t check_config(const mok_config_t* cfg) {
-  if (cfg->mode != MOK_MODE_BF16 && cfg->mode != MOK_MODE_MXFP8_FWD)
+  if (cfg->mode != MOK_MODE_BF16 && cfg->mode != MOK_MODE_MXFP8_FWD && cfg->mode != MOK_MODE_MXFP8)
     return fail(MOK_ERR_INVALID_ARG, "unknown mode %d", cfg->mode);
   if (cfg->events && cfg->num_events != 2 * MOK_NUM_STAGES)
     return fail(MOK_ERR_INVALID_ARG, "events needs 2 * MOK_NUM_STAGES entries");
@@ -690,6 +737,196 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
   return MOK_OK;
 }
 
+// One block-scaled GEMM on single CTAs: BN = 256 when the output width allows.
+template <int EPI>
+cudaError_t launch_mx_tiles(const MxMaps& m, const GemmParams& p, int bn, long long items, int sms,
+                            cudaStream_t st) {
+  const int grid = items < sms ? static_cast<int>(items) : sms;
+  if (bn == 256) return launch_gemm_mx<256, EPI>(m, p, grid, st);
+  return launch_gemm_mx<128, EPI>(m, p, grid, st);
+}
+
+// MXFP8 backward (MOK_MODE_MXFP8): the eight backward GEMMs on the
+// block-scaled MMA, each operand quantised along that GEMM's contraction axis.
+//   dgrad through down    A = dy rows (along H)            B = W_down^T (along H)
+//   weight gradients      A, B = transposes of the row operands (along rows)
+//   dgrad through gate/up A = dG|dU rows (along I)          B = W_gate^T | W_up^T (along I)
+// dy and x are quantised here (rows, and transposed through the schedule);
+// dG|dU and w h are quantised after the SwiGLU backward writes them in bf16.
+mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const uint16_t* x, const float* router_w,
+                            const mok_schedule_t* s, const mok_ctx_t* ctx, const mok_weights_t* w,
+                            uint16_t* dx, float* d_router_w, const mok_weight_grads_t* g, const BwdLayout& L,
+                            int sms, cudaStream_t cs) {
+  const int T = s->T, k = s->k, E = s->E, H = w->H, I = w->I, Is = w->I_s;
+  const long long mr = static_cast<long long>(s->max_tiles) * kTileRows;
+  const int Tp = (T + 127) / 128 * 128;
+  const int mri = static_cast<int>(mr);
+  mok_status_t st;
+  // ---- weight scales into the tensor-core layout and the transposed x, on the side stream
+  SideStream* side = nullptr;
+  if ((st = side_stream(&side))) return st;
+  MOK_CUDA(cudaEventRecord(side->fork, cs));
+  MOK_CUDA(cudaStreamWaitEvent(side->s, side->fork, 0));
+  MOK_CUDA(launch_mx_tile_scales(w->mxt_gate_sc, static_cast<long long>(E) * H, I, L.wtg_sc, side->s));
+  MOK_CUDA(launch_mx_tile_scales(w->mxt_up_sc, static_cast<long long>(E) * H, I, L.wtu_sc, side->s));
+  MOK_CUDA(launch_mx_tile_scales(w->mxt_down_sc, static_cast<long long>(E) * I, H, L.wtd_sc, side->s));
+  MOK_CUDA(launch_mx_quantize_t(x, H, 1, mri, H, mri, s->row_src, k, s->header, L.xT, L.xT_sc, 1, sms, side->s));
+  if (Is > 0) {
+    MOK_CUDA(launch_mx_tile_scales(w->mxts_gate_sc, H, Is, L.wtsg_sc, side->s));
+    MOK_CUDA(launch_mx_tile_scales(w->mxts_up_sc, H, Is, L.wtsu_sc, side->s));
+    MOK_CUDA(launch_mx_tile_scales(w->mxts_down_sc, Is, H, L.wtsd_sc, side->s));
+    MOK_CUDA(launch_mx_quantize_t(x, H, 1, Tp, H, T, nullptr, 1, nullptr, L.xT_tok, L.xT_tok_sc, 1, sms, side->s));
+  }
+  MOK_CUDA(cudaEventRecord(side->join, side->s));
+  // ---- dy: rows (token and schedule order) and transposed
+  MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 0, cs));
+  MOK_CUDA(launch_mx_dispatch(dy, T, H, k, s->slot_row, s->row_src, s->header, mr, L.dyq_tok, L.dyq_tok_sc, L.dyq,
+                              L.dyq_sc, sms, cs));
+  MOK_CUDA(launch_mx_quantize_t(dy, H, 1, mri, H, mri, s->row_src, k, s->header, L.dyT, L.dyT_sc, 1, sms, cs));
+  if (Is > 0)
+    MOK_CUDA(launch_mx_quantize_t(dy, H, 1, Tp, H, T, nullptr, 1, nullptr, L.dyT_tok, L.dyT_tok_sc, 1, sms, cs));
+  MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 1, cs));
+  MOK_CUDA(cudaStreamWaitEvent(cs, side->join, 0));
+  const int bnH = tile_n(H);
+
+  // ---- shared expert (dense rows, w = 1)
+  if (Is > 0) {
+    const int bnS = tile_n(Is);
+    {  // dgrad through down + SwiGLU backward
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DOWN, 0, cs));
+      MxMaps m;
+      if ((st = make_map_u8(&m.a, L.dyq_tok, H, T, 128)) || (st = make_map_u8(&m.b0, w->mxts_down, H, Is, 128)))
+        return st;
+      m.b1 = m.b0;
+      GemmParams p = base_params(nullptr, ctx->status, 0);
+      p.rows = T; p.K = H; p.N = Is; p.n_tiles = Is / 128; p.b_rows_per_expert = 0;
+      p.aux0 = ctx->gu_s; p.out0 = L.dgu_s; p.out1 = L.hs;
+      p.swiglu_limit = ctx->swiglu_limit;
+      p.sfa = L.dyq_tok_sc; p.sfb0 = L.wtsd_sc;
+      const long long items = static_cast<long long>(Tp / 128) * p.n_tiles;
+      MOK_CUDA((launch_gemm_mx<128, EPI_DOWN_BWD>(m, p, items < sms ? static_cast<int>(items) : sms, cs)));
+      // dG|dU by rows (for the dgrad) and transposed (weight gradient); h transposed
+      MOK_CUDA(launch_mx_quantize_rows(L.dgu_s, T, 2 * Is, T, nullptr, L.dgusq, L.dgusq_sc, sms, cs));
+      MOK_CUDA(launch_mx_quantize_t(L.dgu_s, 2 * Is, 1, Tp, 2 * Is, T, nullptr, 1, nullptr, L.dgusT, L.dgusT_sc, 1,
+                                    sms, cs));
+      MOK_CUDA(launch_mx_quantize_t(L.hs, Is, 1, Tp, Is, T, nullptr, 1, nullptr, L.hsT, L.hsT_sc, 1, sms, cs));
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DOWN, 1, cs));
+    }
+    {  // dW_s_down = dy^T h_s
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_DOWN, 0, cs));
+      MxMaps m;
+      if ((st = make_map_u8(&m.a, L.dyT_tok, Tp, H, 128)) || (st = make_map_u8(&m.b0, L.hsT, Tp, Is, bnS)))
+        return st;
+      m.b1 = m.b0;
+      GemmParams p = base_params(nullptr, ctx->status, 0);
+      p.wgrad = 1; p.rows = T; p.K = Tp; p.E = 1; p.m_tiles = H / 128; p.n_tiles = Is / bnS;
+      p.out0 = g->d_ws_down; p.out1 = g->d_ws_down; p.ld = Is; p.split = H;
+      p.sfa = L.dyT_tok_sc; p.sfb0 = L.hsT_sc;
+      MOK_CUDA(launch_mx_tiles<EPI_WGRAD>(m, p, bnS, static_cast<long long>(p.m_tiles) * p.n_tiles, sms, cs));
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_DOWN, 1, cs));
+    }
+    {  // dW_s_gate|up = (dG_s|dU_s)^T x
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_GATEUP, 0, cs));
+      MxMaps m;
+      if ((st = make_map_u8(&m.a, L.dgusT, Tp, 2ull * Is, 128)) || (st = make_map_u8(&m.b0, L.xT_tok, Tp, H, bnH)))
+        return st;
+      m.b1 = m.b0;
+      GemmParams p = base_params(nullptr, ctx->status, 0);
+      p.wgrad = 1; p.rows = T; p.K = Tp; p.E = 1; p.m_tiles = 2 * Is / 128; p.n_tiles = H / bnH;
+      p.out0 = g->d_ws_gate; p.out1 = g->d_ws_up; p.ld = H; p.split = Is;
+      p.sfa = L.dgusT_sc; p.sfb0 = L.xT_tok_sc;
+      MOK_CUDA(launch_mx_tiles<EPI_WGRAD>(m, p, bnH, static_cast<long long>(p.m_tiles) * p.n_tiles, sms, cs));
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_GATEUP, 1, cs));
+    }
+    {  // dx_s = dG_s W_s_gate + dU_s W_s_up
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DGRAD, 0, cs));
+      MxMaps m;
+      if ((st = make_map_u8(&m.a, L.dgusq, 2ull * Is, T, 128)) || (st = make_map_u8(&m.b0, w->mxts_gate, Is, H, bnH)) ||
+          (st = make_map_u8(&m.b1, w->mxts_up, Is, H, bnH)))
+        return st;
+      GemmParams p = base_params(nullptr, ctx->status, 0);
+      p.rows = T; p.K = 2 * Is; p.N = H; p.n_tiles = H / bnH; p.b_rows_per_expert = 0; p.b_split = Is;
+      p.out0 = L.dx_s; p.ld = H;
+      p.sfa = L.dgusq_sc; p.sfb0 = L.wtsg_sc; p.sfb1 = L.wtsu_sc; p.sf_kgb = Is / 128;
+      MOK_CUDA(launch_mx_tiles<EPI_STORE_ROWS>(m, p, bnH, static_cast<long long>(Tp / 128) * p.n_tiles, sms, cs));
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DGRAD, 1, cs));
+    }
+  } else {
+    for (int sg = MOK_STAGE_BWD_SHARED_DOWN; sg <= MOK_STAGE_BWD_SHARED_DGRAD; ++sg) {
+      MOK_CUDA(mark(cfg, sg, 0, cs));
+      MOK_CUDA(mark(cfg, sg, 1, cs));
+    }
+  }
+
+  // ---- routed: dgrad through down + SwiGLU backward + router-weight partials
+  {
+    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DOWN, 0, cs));
+    MxMaps m;
+    if ((st = make_map_u8(&m.a, L.dyq, H, mr, 128)) ||
+        (st = make_map_u8(&m.b0, w->mxt_down, H, static_cast<uint64_t>(E) * I, 128)))
+      return st;
+    m.b1 = m.b0;
+    GemmParams p = base_params(s, ctx->status, 0);
+    p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / 128; p.b_rows_per_expert = I;
+    p.aux0 = ctx->gu; p.out0 = L.dgu; p.out1 = L.hw; p.rw = router_w; p.dw_part = L.dw_part;
+    p.swiglu_limit = ctx->swiglu_limit;
+    p.sfa = L.dyq_sc; p.sfb0 = L.wtd_sc;
+    const long long items = static_cast<long long>(s->max_tiles) * p.n_tiles;
+    MOK_CUDA((launch_gemm_mx<128, EPI_DOWN_BWD>(m, p, items < sms ? static_cast<int>(items) : sms, cs)));
+    MOK_CUDA(launch_mx_quantize_rows(L.dgu, mr, 2 * I, mr, s->header, L.dguq, L.dguq_sc, sms, cs));
+    MOK_CUDA(launch_mx_quantize_t(L.dgu, 2 * I, 1, mri, 2 * I, mri, nullptr, 1, s->header, L.dguT, L.dguT_sc, 1, sms,
+                                  cs));
+    MOK_CUDA(launch_mx_quantize_t(L.hw, I, 1, mri, I, mri, nullptr, 1, s->header, L.hwT, L.hwT_sc, 1, sms, cs));
+    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DOWN, 1, cs));
+  }
+  {  // dW_down[e] = sum over e's rows of dy[t(r)]^T (w h)[r]
+    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_DOWN, 0, cs));
+    const int bn = tile_n(I);
+    MxMaps m;
+    if ((st = make_map_u8(&m.a, L.dyT, mr, H, 128)) || (st = make_map_u8(&m.b0, L.hwT, mr, I, bn))) return st;
+    m.b1 = m.b0;
+    GemmParams p = base_params(s, ctx->status, 0);
+    p.wgrad = 1; p.grouped = 1; p.K = mri; p.E = E; p.m_tiles = H / 128; p.n_tiles = I / bn;
+    p.out0 = g->d_w_down; p.out1 = g->d_w_down; p.ld = I; p.split = H;
+    p.sfa = L.dyT_sc; p.sfb0 = L.hwT_sc;
+    MOK_CUDA(launch_mx_tiles<EPI_WGRAD>(m, p, bn, static_cast<long long>(E) * p.m_tiles * p.n_tiles, sms, cs));
+    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_DOWN, 1, cs));
+  }
+  {  // dW_gate|up[e] = sum over e's rows of (dG|dU)[r]^T x[t(r)]
+    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_GATEUP, 0, cs));
+    MxMaps m;
+    if ((st = make_map_u8(&m.a, L.dguT, mr, 2ull * I, 128)) || (st = make_map_u8(&m.b0, L.xT, mr, H, bnH)))
+      return st;
+    m.b1 = m.b0;
+    GemmParams p = base_params(s, ctx->status, 0);
+    p.wgrad = 1; p.grouped = 1; p.K = mri; p.E = E; p.m_tiles = 2 * I / 128; p.n_tiles = H / bnH;
+    p.out0 = g->d_w_gate; p.out1 = g->d_w_up; p.ld = H; p.split = I;
+    p.sfa = L.dguT_sc; p.sfb0 = L.xT_sc;
+    MOK_CUDA(launch_mx_tiles<EPI_WGRAD>(m, p, bnH, static_cast<long long>(E) * p.m_tiles * p.n_tiles, sms, cs));
+    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_GATEUP, 1, cs));
+  }
+  {  // dx rows = dG W_gate[e] + dU W_up[e], in schedule order
+    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DGRAD_GATEUP, 0, cs));
+    MxMaps m;
+    if ((st = make_map_u8(&m.a, L.dguq, 2ull * I, mr, 128)) ||
+        (st = make_map_u8(&m.b0, w->mxt_gate, I, static_cast<uint64_t>(E) * H, bnH)) ||
+        (st = make_map_u8(&m.b1, w->mxt_up, I, static_cast<uint64_t>(E) * H, bnH)))
+      return st;
+    GemmParams p = base_params(s, ctx->status, 0);
+    p.grouped = 1; p.K = 2 * I; p.N = H; p.n_tiles = H / bnH; p.b_rows_per_expert = H; p.b_split = I;
+    p.out0 = L.dx_slots; p.ld = H;
+    p.sfa = L.dguq_sc; p.sfb0 = L.wtg_sc; p.sfb1 = L.wtu_sc; p.sf_kgb = I / 128;
+    MOK_CUDA(launch_mx_tiles<EPI_STORE_ROWS>(m, p, bnH, static_cast<long long>(s->max_tiles) * p.n_tiles, sms, cs));
+    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DGRAD_GATEUP, 1, cs));
+  }
+  // ---- fixed-order reductions: dx and the router-weight gradient
+  MOK_CUDA(mark(cfg, MOK_STAGE_BWD_REDUCE, 0, cs));
+  MOK_CUDA(launch_combine(L.dx_slots, s->slot_row, s->header, mr, Is > 0 ? L.dx_s : nullptr, T, k, H, dx, sms, cs));
+  MOK_CUDA(launch_dw_reduce(L.dw_part, T * k, 2 * (I / 128), d_router_w, cs));
+  MOK_CUDA(mark(cfg, MOK_STAGE_BWD_REDUCE, 1, cs));
+  return MOK_OK;
+}
+
 }  // namespace
 
 // ===========================================================================
@@ -761,6 +998,22 @@ mok_status_t mok_mxfp8_quantize(const uint16_t* x, int64_t rows, int K, uint8_t*
   return MOK_OK;
 }
 
+mok_status_t mok_mxfp8_quantize_t(const uint16_t* x, int64_t batch, int rows, int cols, uint8_t* codes,
+                                  uint8_t* scales, void* stream) {
+  if (batch < 0 || rows < 0 || cols < 0 || rows % 32 || cols % 64)
+    return fail(MOK_ERR_INVALID_ARG, "need batch, rows, cols >= 0, rows %% 32 == 0 and cols %% 64 == 0");
+  if (batch == 0 || rows == 0 || cols == 0) return MOK_OK;
+  if (batch > (1ll << 30) / 64) return fail(MOK_ERR_INVALID_ARG, "batch too large");
+  if (!x || !codes || !scales) return fail(MOK_ERR_INVALID_ARG, "NULL argument");
+  if (!aligned16(x) || !aligned16(codes)) return fail(MOK_ERR_INVALID_ARG, "misaligned pointer");
+  int sms = 0;
+  mok_status_t st = device_info(&sms);
+  if (st) return st;
+  MOK_CUDA(launch_mx_quantize_t(x, cols, static_cast<int>(batch), rows, cols, rows, nullptr, 1, nullptr, codes, scales,
+                                0, sms, static_cast<cudaStream_t>(stream)));
+  return MOK_OK;
+}
+
 size_t mok_ctx_bytes(int T, int k, int E, int H, int I, int I_s, int mode) {
   if (check_shapes(T, k, E, H, I, I_s) != MOK_OK) return 0;
   mok_ctx_t c;
@@ -789,7 +1042,7 @@ mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x, const float
   if (!w->w_gate || !w->w_up || !w->w_down) return fail(MOK_ERR_INVALID_ARG, "NULL routed weight");
   if (Is > 0 && (!w->ws_gate || !w->ws_up || !w->ws_down))
     return fail(MOK_ERR_INVALID_ARG, "NULL shared weight");
-  const bool mx = cfg->mode == MOK_MODE_MXFP8_FWD;
+  const bool mx = cfg->mode == MOK_MODE_MXFP8_FWD || cfg->mode == MOK_MODE_MXFP8;
   if (mx && (!w->mx_gate || !w->mx_gate_sc || !w->mx_up || !w->mx_up_sc || !w->mx_down || !w->mx_down_sc ||
              (Is > 0 && (!w->mxs_gate || !w->mxs_gate_sc || !w->mxs_up || !w->mxs_up_sc || !w->mxs_down ||
                          !w->mxs_down_sc))))
@@ -835,10 +1088,11 @@ mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x, const float
   return MOK_OK;
 }
 
-size_t mok_bwd_workspace_bytes(int T, int k, int E, int H, int I, int I_s) {
+size_t mok_bwd_workspace_bytes(int T, int k, int E, int H, int I, int I_s, int mode) {
   if (check_shapes(T, k, E, H, I, I_s) != MOK_OK) return 0;
+  if (mode != MOK_MODE_BF16 && mode != MOK_MODE_MXFP8_FWD && mode != MOK_MODE_MXFP8) return 0;
   BwdLayout L;
-  return carve_bwd(nullptr, T, k, E, H, I, I_s, &L);
+  return carve_bwd(nullptr, T, k, E, H, I, I_s, mode, &L);
 }
 
 mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uint16_t* x,
@@ -860,7 +1114,17 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
   const void* ptrs[] = {dy, x, router_w, dx, d_router_w, ws, g->d_w_gate, g->d_w_up, g->d_w_down};
   for (const void* q : ptrs)
     if (!aligned16(q)) return fail(MOK_ERR_INVALID_ARG, "misaligned pointer");
-  if (ws_bytes < mok_bwd_workspace_bytes(T, k, E, H, I, Is))
+  const bool mxb = ctx->mode == MOK_MODE_MXFP8;
+  if (mxb) {
+    const void* mp[] = {w->mxt_gate, w->mxt_gate_sc, w->mxt_up, w->mxt_up_sc, w->mxt_down, w->mxt_down_sc};
+    const void* ms[] = {w->mxts_gate, w->mxts_gate_sc, w->mxts_up, w->mxts_up_sc, w->mxts_down, w->mxts_down_sc};
+    for (const void* q : mp)
+      if (!q || !aligned16(q)) return fail(MOK_ERR_INVALID_ARG, "MXFP8 backward needs the transposed weight copies");
+    for (const void* q : ms)
+      if (Is > 0 && (!q || !aligned16(q)))
+        return fail(MOK_ERR_INVALID_ARG, "MXFP8 backward needs the transposed shared weight copies");
+  }
+  if (ws_bytes < mok_bwd_workspace_bytes(T, k, E, H, I, Is, ctx->mode))
     return fail(MOK_ERR_INVALID_ARG, "backward workspace too small");
   int sms = 0;
   st = device_info(&sms);
@@ -868,7 +1132,8 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const bool g4 = (cfg->debug_flags & MOK_DEBUG_TMA_GATHER4) != 0;
   BwdLayout L;
-  carve_bwd(ws, T, k, E, H, I, Is, &L);
+  carve_bwd(ws, T, k, E, H, I, Is, ctx->mode, &L);
+  if (mxb) return backward_mxfp8(cfg, dy, x, router_w, s, ctx, w, dx, d_router_w, g, L, sms, cs);
   const long long mr = static_cast<long long>(s->max_tiles) * kTileRows;
 
   const int bn1 = tile_n(I);

@@ -115,6 +115,8 @@ struct GemmParams {
   const uint8_t* sfb0;
   const uint8_t* sfb1;
   uint8_t* sf_out;   // EPI_SWIGLU_MX: scales of h, same layout
+  int sf_kga;        // 128-column groups of A's / B's scale layout (0 = K / 128); a weight
+  int sf_kgb;        // gradient's operands span the whole row range, not one item's K
 };
 
 struct Item {

@@ -1,6 +1,7 @@
-// Block-scaled (MXFP8) grouped-GEMM instantiations for the MXFP8 forward:
-// gate/up + SwiGLU + h requantisation, down + router scale (rows in schedule order), dense
-// store (shared expert); single CTAs and CTA pairs.
+// Block-scaled (MXFP8) grouped-GEMM instantiations.  Forward: gate/up + SwiGLU
+// + h requantisation, down + router scale (rows in schedule order), dense store
+// (shared expert); single CTAs and CTA pairs.  Backward (MXFP8 mode): SwiGLU
+// backward, weight gradients and the dgrad rows; single CTAs.
 #include "gemm_launch.cuh"
 #include "gemm_mx.cuh"
 #include "internal.h"
@@ -83,6 +84,11 @@ MOK_INSTANTIATE_MX(256, EPI_SCALE_ROWS)
 MOK_INSTANTIATE_MX(128, EPI_SCALE_ROWS)
 MOK_INSTANTIATE_MX(256, EPI_STORE_ROWS)
 MOK_INSTANTIATE_MX(128, EPI_STORE_ROWS)
+// MXFP8 backward: SwiGLU backward through down (128-wide tiles keep its
+// per-thread accumulator share in registers), weight gradients, dgrad rows
+MOK_INSTANTIATE_MX(128, EPI_DOWN_BWD)
+MOK_INSTANTIATE_MX(256, EPI_WGRAD)
+MOK_INSTANTIATE_MX(128, EPI_WGRAD)
 MOK_INSTANTIATE_MX_PAIR(256, EPI_SWIGLU_MX)
 MOK_INSTANTIATE_MX_PAIR(256, EPI_SCALE_ROWS)
 MOK_INSTANTIATE_MX_PAIR(256, EPI_STORE_ROWS)

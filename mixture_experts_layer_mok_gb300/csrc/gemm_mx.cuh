@@ -73,7 +73,10 @@ template <int BN, int EPI, bool PAIR = false>
 __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
     gemm_mx_kernel(const __grid_constant__ MxMaps maps, const GemmParams p) {
   using C = MxCfg<BN, EPI, PAIR>;
-  static_assert(EPI == EPI_SWIGLU_MX || EPI == EPI_SCALE_ROWS || EPI == EPI_STORE_ROWS, "epilogue");
+  static_assert(EPI == EPI_SWIGLU_MX || EPI == EPI_SCALE_ROWS || EPI == EPI_STORE_ROWS || EPI == EPI_WGRAD ||
+                    EPI == EPI_DOWN_BWD,
+                "epilogue");
+  static_assert(!PAIR || (EPI != EPI_WGRAD && EPI != EPI_DOWN_BWD), "backward epilogues run on single CTAs");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -89,7 +92,9 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int kgroups = p.K / C::kBK;
+  // 128-column groups of the A and B scale layouts
+  const int kga = p.sf_kga > 0 ? p.sf_kga : p.K / C::kBK;
+  const int kgb = p.sf_kgb > 0 ? p.sf_kgb : p.K / C::kBK;
   // CTA pair: rank in the pair, persistent loop over the pair's items
   const int rank = PAIR ? static_cast<int>(cluster_rank()) : 0;
   const int item0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
@@ -144,12 +149,17 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
       for (int idx = item0; idx < nitems && ok; idx += istep) {
         const Item it = item_at(idx);
         const int n0 = it.nt * kBnOut;
-        const long long brow = static_cast<long long>(it.e) * p.b_rows_per_expert + n0;
+        // row GEMMs: A rows are layer rows p0.., B rows the expert's weight
+        // rows; weight gradients: A rows m0.., B rows n0.. of tensors whose
+        // columns are the layer rows, the expert's K range starting at kbeg
+        const bool wg = p.wgrad != 0;
+        const long long arow = wg ? it.m0 : it.p0;
+        const long long brow = wg ? n0 : static_cast<long long>(it.e) * p.b_rows_per_expert + n0;
         // scale atoms of the item's A rows and B rows (B: gate then up, or two
-        // consecutive 128-row blocks), as atom indices
-        const long long atom_a = (it.p0 >> 7) * static_cast<long long>(kgroups);
-        const long long atom_b0 = (brow >> 7) * static_cast<long long>(kgroups);
-        const long long atom_b1 = kSwiGLU ? atom_b0 : atom_b0 + kgroups;
+        // consecutive 128-row blocks), as atom indices at K-block 0
+        const long long atom_a = (arow >> 7) * static_cast<long long>(kga);
+        const long long atom_b0 = (brow >> 7) * static_cast<long long>(kgb);
+        const long long atom_b1 = kSwiGLU ? atom_b0 : atom_b0 + kgb;
         for (int kb = 0; kb < it.nk; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) {
             ok = false;
@@ -173,17 +183,27 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
             tma_load_2d_pair(sS + 1024, kSwiGLU ? &maps.sfb1 : &maps.sfb0, lf, 0,
                              static_cast<int>((atom_b1 + kb) * 4));
           } else {
-            tma_load_2d(sA, &maps.a, &full[stage], k0, it.p0);
+            // K coordinate of this K-block in the operand tensors, and which B
+            // tensor holds it (a K range split over two weights: b_split)
+            const int ka = (wg ? it.kbeg : 0) + k0;
+            int kbb = ka;
+            bool second = false;
+            if (!wg && p.b_split > 0 && k0 >= p.b_split) {
+              kbb = k0 - p.b_split;
+              second = true;
+            }
+            const long long kba = ka / C::kBK, kbq = kbb / C::kBK;   // K-block index within each scale layout
+            tma_load_2d(sA, &maps.a, &full[stage], ka, static_cast<int>(arow));
             if (kSwiGLU) {
               tma_load_2d(sB, &maps.b0, &full[stage], k0, static_cast<int>(brow));
               tma_load_2d(sB + (BN / 2) * C::kBK, &maps.b1, &full[stage], k0, static_cast<int>(brow));
             } else {
-              tma_load_2d(sB, &maps.b0, &full[stage], k0, static_cast<int>(brow));
+              tma_load_2d(sB, second ? &maps.b1 : &maps.b0, &full[stage], kbb, static_cast<int>(brow));
             }
-            bulk_load(sS, p.sfa + (atom_a + kb) * 512, 512, &full[stage]);
-            bulk_load(sS + 512, p.sfb0 + (atom_b0 + kb) * 512, 512, &full[stage]);
-            if (BN == 256)
-              bulk_load(sS + 1024, (kSwiGLU ? p.sfb1 : p.sfb0) + (atom_b1 + kb) * 512, 512, &full[stage]);
+            const uint8_t* sfb = (kSwiGLU || second) ? p.sfb1 : p.sfb0;
+            bulk_load(sS, p.sfa + (atom_a + kba) * 512, 512, &full[stage]);
+            bulk_load(sS + 512, (kSwiGLU ? p.sfb0 : sfb) + (atom_b0 + kbq) * 512, 512, &full[stage]);
+            if (BN == 256) bulk_load(sS + 1024, sfb + (atom_b1 + kbq) * 512, 512, &full[stage]);
           }
           ++fills;
           if (++stage == C::kStages) {
@@ -288,9 +308,28 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
     uint8_t* wstage = sf_smem + C::kStages * C::kSfStride + C::kBarBytes + (warp - 2) * C::kEpiStageBytes;
     uint32_t aphase = 0;
     constexpr int kCols = BN / 2;          // accumulator columns per thread
+    // weight gradients: destination of output row m of expert e (rows below
+    // `split` go to out0, the rest to out1), at column col
+    auto wgrad_row = [&](const Item& t, int m, int col) -> uint16_t* {
+      const int mrows = p.m_tiles * kBM;
+      if (m < p.split)
+        return static_cast<uint16_t*>(p.out0) + (static_cast<long long>(t.e) * p.split + m) * p.ld + col;
+      return static_cast<uint16_t*>(p.out1) +
+             (static_cast<long long>(t.e) * (mrows - p.split) + (m - p.split)) * p.ld + col;
+    };
     for (int idx = item0; idx < nitems; idx += istep) {
       const Item it = item_at(idx);
-      if (it.nk == 0) continue;
+      if (it.nk == 0) {
+        if constexpr (EPI == EPI_WGRAD) {   // an expert with no rows: zero gradient
+          uint32_t zw[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) zw[i] = 0u;
+          uint16_t* dst = wgrad_row(it, it.m0 + r, it.nt * kBnOut + half * kCols);
+#pragma unroll
+          for (int c = 0; c < kCols / 32; ++c) warp_store_row64(zw, dst + c * 32, wstage, lane);
+        }
+        continue;
+      }
       const int n0 = it.nt * kBnOut;
       const int prow = it.p0 + r;
       const bool live = !it.empty;     // an empty half of a CTA pair stores nothing
@@ -383,6 +422,79 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
             *sdst = static_cast<uint8_t>(sc);
           }
         }
+      } else if constexpr (EPI == EPI_WGRAD) {
+        // out[e][m][n] = bf16(acc): every row of a weight-gradient tile is real
+        uint16_t* dst = wgrad_row(it, it.m0 + r, n0 + half * kCols);
+#pragma unroll
+        for (int c = 0; c < kCols / 32; ++c) {
+          pack_bf16x32(v + c * 32, wv);
+          warp_store_row64(wv, dst + c * 32, wstage, lane);
+        }
+      } else if constexpr (EPI == EPI_DOWN_BWD) {
+        // Z = dy . W_down (this thread's kCols columns in v); aux0 = the saved
+        // gate|up pre-activations [rows][2N]; out0 = dG|dU [rows][2N], out1 =
+        // w h [rows][N], dw_part[f][n_tiles][2] = sum over the columns of Z h.
+        // Grouped rows: padding rows of an expert's range get zeros (the weight
+        // gradients contract over them); dense rows past the end store nothing.
+        int f = -1;
+        bool v_ok;
+        float wt = 1.f;
+        if (p.grouped) {
+          f = valid ? __ldg(p.row_src + prow) : -1;
+          v_ok = f >= 0;
+          if (v_ok) wt = __ldg(p.rw + f);
+        } else {
+          v_ok = valid;
+        }
+        const bool st_ok = live && (p.grouped ? true : valid);
+        const int col0 = n0 + half * kCols;
+        const uint16_t* gu = static_cast<const uint16_t*>(p.aux0) + static_cast<long long>(prow) * 2 * p.N + col0;
+        uint16_t* dgu = static_cast<uint16_t*>(p.out0) + static_cast<long long>(prow) * 2 * p.N + col0;
+        uint16_t* hwo = static_cast<uint16_t*>(p.out1) + static_cast<long long>(prow) * p.N + col0;
+        const float lim = p.swiglu_limit;
+        float dpart = 0.f;
+#pragma unroll
+        for (int c = 0; c < kCols / 32; ++c) {   // unrolled: v stays in registers
+          uint4 ng[4], nu[4];
+          if (v_ok) {
+            load_raw64(gu + c * 32, ng);
+            load_raw64(gu + p.N + c * 32, nu);
+          }
+          uint32_t wdg[16], wdu[16], whv[16];
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float a[2] = {0.f, 0.f}, b[2] = {0.f, 0.f}, hh[2] = {0.f, 0.f};
+            if (v_ok) {
+#pragma unroll
+              for (int t = 0; t < 2; ++t) {
+                float g = bf16_at(ng, i + t), u = bf16_at(nu, i + t);
+                float mg = 1.f, mu = 1.f;   // the clamp's derivative (SwiGLU limit)
+                if (lim > 0.f) {
+                  mg = (g <= lim) ? 1.f : 0.f;
+                  mu = (fabsf(u) <= lim) ? 1.f : 0.f;
+                  g = fminf(g, lim);
+                  u = fminf(fmaxf(u, -lim), lim);
+                }
+                const float z = v[c * 32 + i + t];
+                const float sg = __fdividef(1.f, 1.f + __expf(-g));
+                const float sl = g * sg;
+                const float h = sl * u;
+                dpart = fmaf(z, h, dpart);
+                const float dh = wt * z;
+                a[t] = dh * u * sg * (1.f + g * (1.f - sg)) * mg;
+                b[t] = dh * sl * mu;
+                hh[t] = wt * h;
+              }
+            }
+            wdg[i >> 1] = pack_bf16(a[0], a[1]);
+            wdu[i >> 1] = pack_bf16(b[0], b[1]);
+            whv[i >> 1] = pack_bf16(hh[0], hh[1]);
+          }
+          warp_store_row64(wdg, st_ok ? dgu + c * 32 : nullptr, wstage, lane);
+          warp_store_row64(wdu, st_ok ? dgu + p.N + c * 32 : nullptr, wstage, lane);
+          warp_store_row64(whv, st_ok ? hwo + c * 32 : nullptr, wstage, lane);
+        }
+        if (p.grouped && v_ok) p.dw_part[(static_cast<long long>(f) * p.n_tiles + it.nt) * 2 + half] = dpart;
       } else {
         // rows in schedule order (router-weighted: the combine reads them
         // back per (token, k) through slot_row), or dense rows

@@ -368,6 +368,150 @@ cudaError_t launch_mx_dispatch(const uint16_t* x, int T, int H, int topk, const 
   return cudaGetLastError();
 }
 
+// ===========================================================================
+// Transposing MXFP8 quantiser: bf16 rows -> E4M3 codes of the transpose, one
+// E8M0 scale per 32 consecutive input rows of each column.  This is the
+// operand form of a GEMM whose contraction runs along the rows: the weight
+// gradients (contraction over an expert's rows) and the dgrad GEMMs (over a
+// weight's leading axis).  Input row r of batch b is src[b][r] (dense; zero
+// from valid_rows on), or, with row_src, the token row of schedule row r
+// (src[row_src[r] / topk]; zero for padding rows).  With a schedule header,
+// rows from P on read as zero and a failed schedule skips the work.  Output
+// codes [batch][C][R]; scales row-major [batch*C][R/32], or (tiled) in the
+// tensor-core scale layout with rows batch*C and K = R.  One block per
+// 128-row x 64-column tile: coalesced row loads into shared memory, then one
+// thread per (column, 32-row block).
+// ===========================================================================
+__global__ void __launch_bounds__(256) mx_quantize_t_kernel(const uint16_t* __restrict__ src, long long ld, int batch,
+                                                            int R, int C, int valid_rows,
+                                                            const int* __restrict__ row_src, int topk,
+                                                            const int* __restrict__ header,
+                                                            uint8_t* __restrict__ codes,
+                                                            uint8_t* __restrict__ scales, int tiled) {
+  griddep_wait();
+  griddep_launch_dependents();
+  int vrows = valid_rows;
+  if (header) {
+    if (header[2] != 0) return;
+    vrows = min(vrows, header[1]);
+  }
+  __shared__ __align__(16) uint16_t tile[128][64];
+  const int rtiles = (R + 127) / 128, ctiles = C / 64;
+  const long long ntiles = static_cast<long long>(batch) * rtiles * ctiles;
+  const int c = threadIdx.x & 63, rb = threadIdx.x >> 6;
+  for (long long t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const int ct = static_cast<int>(t % ctiles);
+    const long long rest = t / ctiles;
+    const int rt = static_cast<int>(rest % rtiles);
+    const int b = static_cast<int>(rest / rtiles);
+    const int r0 = rt * 128, c0 = ct * 64;
+    __syncthreads();   // the previous tile's readers are done with the buffer
+    for (int i = threadIdx.x; i < 128 * 8; i += 256) {   // 8 pieces of 16 bytes per row
+      const int row = i >> 3, piece = i & 7;
+      const int r = r0 + row;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (r < R && r < vrows) {
+        long long srow = r;
+        if (row_src) {
+          const int f = __ldg(row_src + r);
+          srow = f >= 0 ? f / topk : -1;
+        }
+        if (srow >= 0)
+          v = __ldg(reinterpret_cast<const uint4*>(src + (static_cast<long long>(b) * R + srow) * ld + c0) + piece);
+      }
+      reinterpret_cast<uint4*>(&tile[row][0])[piece] = v;
+    }
+    __syncthreads();
+    const int rr = r0 + rb * 32;
+    if (rr < R) {
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(static_cast<uint32_t>(tile[rb * 32 + i][c]) << 16);
+      uint8_t q[32];
+      const uint32_t s = mx_quantize32(v, q);
+      const long long orow = static_cast<long long>(b) * C + c0 + c;
+      uint4* d = reinterpret_cast<uint4*>(codes + orow * R + rr);
+      d[0] = reinterpret_cast<const uint4*>(q)[0];
+      d[1] = reinterpret_cast<const uint4*>(q)[1];
+      if (tiled)
+        scales[mx_tiled_scale_offset(orow, rr / 32, R / 128)] = static_cast<uint8_t>(s);
+      else
+        scales[orow * (R / 32) + rr / 32] = static_cast<uint8_t>(s);
+    }
+  }
+}
+
+cudaError_t launch_mx_quantize_t(const uint16_t* src, long long ld, int batch, int R, int C, int valid_rows,
+                                 const int* row_src, int topk, const int* header, uint8_t* codes, uint8_t* scales,
+                                 int tiled, int num_sms, cudaStream_t st) {
+  const long long tiles = static_cast<long long>(batch) * ((R + 127) / 128) * (C / 64);
+  if (tiles == 0) return cudaSuccess;
+  const long long cap = static_cast<long long>(num_sms) * 8;
+  const int grid = static_cast<int>(tiles < cap ? tiles : cap);
+  cudaError_t err = launch_dependent(mx_quantize_t_kernel, dim3(grid), dim3(256), 0, st, src, ld, batch, R, C,
+                                     valid_rows, row_src, topk, header, codes, scales, tiled);
+  if (err != cudaSuccess) return err;
+  return cudaGetLastError();
+}
+
+// Row-wise MXFP8 quantiser with the scales written straight into the
+// tensor-core scale layout (rows R, K): rows below valid_rows (and below P
+// with a schedule header) are quantised; the rest of the 128-row blocks get
+// unit scales (their codes are never read: tiles stop at P, and TMA reads
+// zeros past a tensor's end).  One warp per row.
+__global__ void __launch_bounds__(256) mx_quantize_rows_kernel(const uint16_t* __restrict__ x, long long R, int K,
+                                                               long long valid_rows, const int* __restrict__ header,
+                                                               uint8_t* __restrict__ codes,
+                                                               uint8_t* __restrict__ sc) {
+  griddep_wait();
+  griddep_launch_dependents();
+  long long vrows = valid_rows;
+  if (header) {
+    if (header[2] != 0) return;
+    vrows = min(vrows, static_cast<long long>(header[1]));
+  }
+  const int lane = threadIdx.x & 31;
+  const int nb = K / 32, cg = K / 128;
+  const long long rpad = (R + 127) / 128 * 128;
+  for (long long j = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5; j < rpad;
+       j += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
+    if (j < vrows) {
+      for (int b0 = 0; b0 < nb; b0 += 32) {
+        const int b = b0 + lane;
+        const bool act = b < nb;       // whole aligned groups of 4 lanes share this
+        float v[32];
+        uint8_t q[32];
+        uint32_t s = 127;
+        if (act) {
+          load_bf16x32(x + j * K + static_cast<long long>(b) * 32, v);
+          s = mx_quantize32(v, q);
+          uint4* d = reinterpret_cast<uint4*>(codes + j * K + static_cast<long long>(b) * 32);
+          d[0] = reinterpret_cast<const uint4*>(q)[0];
+          d[1] = reinterpret_cast<const uint4*>(q)[1];
+        }
+        const uint32_t s1 = __shfl_down_sync(0xffffffffu, s, 1);
+        const uint32_t s2 = __shfl_down_sync(0xffffffffu, s, 2);
+        const uint32_t s3 = __shfl_down_sync(0xffffffffu, s, 3);
+        if (act && (lane & 3) == 0)
+          *reinterpret_cast<uint32_t*>(sc + mx_tiled_scale_offset(j, b, cg)) = s | (s1 << 8) | (s2 << 16) | (s3 << 24);
+      }
+    } else {
+      for (int g = lane; g < cg; g += 32)
+        *reinterpret_cast<uint32_t*>(sc + mx_tiled_scale_offset(j, 4 * g, cg)) = 0x7F7F7F7Fu;
+    }
+  }
+}
+
+cudaError_t launch_mx_quantize_rows(const uint16_t* x, long long R, int K, long long valid_rows, const int* header,
+                                    uint8_t* codes, uint8_t* sc, int num_sms, cudaStream_t st) {
+  if (R == 0) return cudaSuccess;
+  const long long rpad = (R + 127) / 128 * 128;
+  cudaError_t err = launch_dependent(mx_quantize_rows_kernel, dim3(grid_for(rpad * 32, 256, num_sms)), dim3(256), 0,
+                                     st, x, R, K, valid_rows, header, codes, sc);
+  if (err != cudaSuccess) return err;
+  return cudaGetLastError();
+}
+
 // Row-major E8M0 scales [rows][K/32] -> the tensor-core scale layout.  One
 // block per (128-row block, 16 column groups): coalesced row reads into shared
 // memory, coalesced atom writes out of it.

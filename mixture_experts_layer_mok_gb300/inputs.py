@@ -29,6 +29,8 @@ WORKLOADS = {
                        minibatch=2048, capacity=0.5, mode="bf16"),
     "mxfp8_T4096": dict(T=4096, H=2048, I=1024, E=64, k=8, I_s=2048, skew=None,
                         minibatch=2048, capacity=0.5, mode="mxfp8"),
+    "mxfp8full_T4096": dict(T=4096, H=2048, I=1024, E=64, k=8, I_s=2048, skew=None,
+                            minibatch=2048, capacity=0.5, mode="mxfp8_full"),
     "skewed_T16384": dict(T=16384, H=4096, I=1536, E=128, k=8, I_s=0, skew=1.2,
                           minibatch=4096, capacity=0.5, mode="bf16"),
     "large_T65536": dict(T=65536, H=7168, I=2048, E=256, k=8, I_s=2048, skew=None,

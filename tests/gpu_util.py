@@ -36,8 +36,8 @@ def rel_l2(a, b) -> float:
 def weights_of(g, mode="bf16"):
     m = mok()
     w = m.Weights(g.w_gate, g.w_up, g.w_down, g.ws_gate, g.ws_up, g.ws_down)
-    if mode == "mxfp8":
-        w = m.quantize_weights(w)
+    if mode in ("mxfp8", "mxfp8_full"):
+        w = m.quantize_weights(w, backward=(mode == "mxfp8_full"))
     return w
 
 
@@ -63,6 +63,9 @@ def oracle_fwd_bwd(inp, mode="bf16", swiglu_limit=0.0):
     if mode == "mxfp8":
         y = oracle.layer_forward_mxfp8(*a, swiglu_limit=swiglu_limit)
         g = oracle.layer_backward_mxfp8(*a[:6], inp.dy, *a[6:], swiglu_limit=swiglu_limit)
+    elif mode == "mxfp8_full":
+        y = oracle.layer_forward_mxfp8(*a, swiglu_limit=swiglu_limit)
+        g = oracle.layer_backward_mxfp8_full(*a[:6], inp.dy, *a[6:], swiglu_limit=swiglu_limit)
     else:
         y = oracle.layer_forward(*a, swiglu_limit=swiglu_limit)
         g = oracle.layer_backward(*a[:6], inp.dy, *a[6:], swiglu_limit=swiglu_limit)

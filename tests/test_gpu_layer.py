@@ -57,6 +57,28 @@ def test_mxfp8_forward_matches_same_quantisation_oracle(name):
     assert rel_l2(y, y_unq) <= max(MX_UNQ_TOL, intrinsic + BF16_TOL), (rel_l2(y, y_unq), intrinsic)
 
 
+@pytest.mark.parametrize("name", list(SHAPES))
+def test_mxfp8_full_backward_matches_same_quantisation_oracle(name):
+    """MXFP8 forward and backward: every backward GEMM on block-scaled E4M3
+    operands, against the oracle that quantises the same operands along the
+    same axes."""
+    inp = _inputs(name, seed=9)
+    y, grads, sched, ctx = run_layer(inp, "mxfp8_full")
+    assert ctx.status() == 0
+    y_ref, g_ref = oracle_fwd_bwd(inp, "mxfp8_full")
+    errs, bad = compare_all(y, grads, y_ref, g_ref, BF16_TOL)
+    assert not bad, errs
+
+
+def test_mxfp8_full_repeated_runs_bitwise_identical():
+    inp = _inputs("wide", seed=10)
+    a = run_layer(inp, "mxfp8_full")
+    b = run_layer(inp, "mxfp8_full")
+    assert torch.equal(a[0], b[0])
+    for key in a[1]:
+        assert torch.equal(a[1][key], b[1][key]), key
+
+
 def test_repeated_runs_bitwise_identical():
     inp = _inputs("wide", seed=2)
     a = run_layer(inp, "bf16")
@@ -129,13 +151,15 @@ def test_host_argument_errors():
     assert ei.value.code == 1
 
 
-@pytest.mark.parametrize("mode", ["bf16", "mxfp8"])
+@pytest.mark.parametrize("mode", ["bf16", "mxfp8", "mxfp8_full"])
 def test_full_size_T4096_sampled(mode):
-    """The bf16 / mxfp8 T=4096 layers (H=2048, I=1024, E=64, k=8, I_s=2048) at full
+    """The T=4096 layers (H=2048, I=1024, E=64, k=8, I_s=2048; bf16, MXFP8 forward,
+    MXFP8 forward and backward) at full
     size, in the launch configuration the benchmark times: y, dx and d_router_w
     on 48 sampled tokens, and the full weight gradients of the hottest and the
     coldest expert, against the oracle."""
-    inp = gen.make_workload("bf16_T4096" if mode == "bf16" else "mxfp8_T4096", seed=0)
+    wl = {"bf16": "bf16_T4096", "mxfp8": "mxfp8_T4096", "mxfp8_full": "mxfp8full_T4096"}[mode]
+    inp = gen.make_workload(wl, seed=0)
     y, grads, sched, ctx = run_layer(inp, mode, capacity=0.5, minibatch=2048)
     assert ctx.status() == 0
     rng = np.random.default_rng(0)

@@ -116,3 +116,43 @@ def test_quantize_empty():
     m = mok()
     c, s = m.mxfp8_quantize(torch.empty(0, 64, dtype=torch.bfloat16, device="cuda"))
     assert c.numel() == 0 and s.numel() == 0
+
+
+def _check_quant_t(x3):
+    """The transposing quantiser against the oracle's quantiser applied to the
+    transpose of each matrix of the batch, bit for bit."""
+    m = mok()
+    codes, scales = m.mxfp8_quantize_t(x3.cuda())
+    for b in range(x3.shape[0]):
+        rc, rs = oracle.mxfp8_quantize(x3[b].double().numpy().T)
+        assert np.array_equal(codes[b].cpu().numpy(), rc), b
+        assert np.array_equal(scales[b].cpu().numpy(), rs), b
+
+
+@pytest.mark.parametrize("B,R,C,std", [(1, 32, 64, 1.0), (3, 160, 192, 0.02), (2, 1024, 2048, 0.02),
+                                       (1, 2048, 64, 3.0), (4, 128, 128, 1e-3)])
+def test_quantize_t_bit_exact(B, R, C, std):
+    x = gen.make_matrix(B * R, C, std=std, seed=B + R + C).reshape(B, R, C).contiguous()
+    _check_quant_t(x)
+
+
+def test_quantize_t_edge_values():
+    table = oracle.e4m3_decode(np.arange(256, dtype=np.uint8))
+    fin = table[np.isfinite(table)]
+    mids = (np.sort(np.unique(np.abs(fin)))[1:] + np.sort(np.unique(np.abs(fin)))[:-1]) / 2
+    v = np.concatenate([fin, mids, -mids, [0.0, -0.0] * 16, [3e38, -3e38, 1e-38, -1e-39]])
+    v = np.concatenate([v * 2.0 ** s for s in (-100, -9, 0, 3, 100)])
+    x = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16)
+    x = x[torch.isfinite(x)]
+    n = x.numel() // (32 * 64) * (32 * 64)
+    x = x[:n].reshape(-1, 32, 64).permute(1, 0, 2).reshape(32, -1)   # 32-row blocks of mixed values
+    x = x[:, : x.shape[1] // 64 * 64].contiguous()
+    z = torch.zeros(64, 64, dtype=torch.bfloat16)                    # zero and single-value blocks
+    z[5, 1] = -1.0
+    z[40, 2] = 448.0
+    z[:, 3] = -0.0
+    _check_quant_t(x.unsqueeze(0))
+    _check_quant_t(z.unsqueeze(0))
+    m = mok()
+    c2, s2 = m.mxfp8_quantize_t(z.cuda())                            # a single matrix
+    assert c2.shape == (64, 64) and s2.shape == (64, 2)
