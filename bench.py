@@ -101,11 +101,10 @@ def launches_per_step(c):
         n += 1                              # x quantised into token and schedule order
     else:
         n += 1                              # x rows into schedule order
-    if full:
-        n += 3 + s3                         # transposed weight prequantisation (every step)
-        n += 3 + s3                         # their scales into the tensor-core layout
-        n += 3 + (2 if shared else 0)       # x transposed, dy rows, dy transposed (+ token order)
-        n += 7 + (7 if shared else 0)       # per expert set: 4 GEMMs + 3 quantisations of dG|dU, w h
+    if full:                                # (the prequantisation above writes both weight copies)
+        n += 3 + s3                         # transposed weights' scales into the tensor-core layout
+        n += 2 + (2 if shared else 0)       # x transposed; dy rows + transposed (schedule, token order)
+        n += 4 + (4 if shared else 0)       # GEMMs (the SwiGLU backward writes its MXFP8 outputs)
         n += 2                              # combine dx, reduce d_w
         return n
     n += 1 + (1 if mx else 0)               # dy rows (and bf16 x rows) into schedule order
@@ -310,9 +309,13 @@ def main():
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
-    def run_step(x, rw, top, dy, events=None):
+    def run_step(x, rw, top, dy, events=None, prep_events=None):
+        if prep_events:
+            prep_events[0].record()
         wq = mok.quantize_weights(w, backward=(mode == "mxfp8_full")) if mode != "bf16" else w
         sched = mok.schedule(top, E, c["capacity"])
+        if prep_events:
+            prep_events[1].record()
         _, ctx = mok.forward(x, rw, sched, wq, mode=mode, minibatch=c["minibatch"], out=y, ctx_buf=ctx_buf,
                              events=events)
         mok.backward(dy, x, rw, sched, ctx, wq, minibatch=c["minibatch"], grads=grads, ws_buf=ws_buf,
@@ -334,12 +337,15 @@ def main():
     # below record only the dominant stage's pair.
     prof_steps = 5
     ev_prof = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nst)] for _ in range(prof_steps)]
+    ev_prep = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(prof_steps)]
     for i in range(prof_steps):
         flush.zero_()
-        run_step(g.x, g.router_w, g.top_experts, g.dy, events=ev_prof[i])
+        run_step(g.x, g.router_w, g.top_experts, g.dy, events=ev_prof[i], prep_events=ev_prep[i])
     torch.cuda.synchronize()
     st_ms = {names[s]: sum(ev_prof[i][2 * s].elapsed_time(ev_prof[i][2 * s + 1]) for i in range(prof_steps)) /
              prof_steps for s in range(nst)}
+    # the caller's part of a step: weight prequantisation (MXFP8 modes) and the schedule build
+    st_ms["step_prep"] = sum(e[0].elapsed_time(e[1]) for e in ev_prep) / prof_steps
     gemm_stages = {n: v for n, v in st_ms.items() if n in sf and sf[n] > 0}
     dom = max(gemm_stages, key=gemm_stages.get)
     di = names.index(dom)
@@ -386,7 +392,7 @@ def main():
     gemm_ms = sum(gemm_stages.values())
     gemm_tflops = sum(sf[n] for n in gemm_stages) / (gemm_ms / 1e3) / 1e12
     if args.stages and rank == 0:
-        for n in names:
+        for n in names + ["step_prep"]:
             extra = f"  {sf[n] / (st_ms[n] / 1e3) / 1e12:8.1f} TFLOP/s" if n in gemm_stages else ""
             print(f"  {n:26s} {st_ms[n]:8.4f} ms{extra}", file=sys.stderr)
 

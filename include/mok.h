@@ -318,6 +318,17 @@ mok_status_t mok_mxfp8_quantize(const uint16_t* x, int64_t rows, int K,
 mok_status_t mok_mxfp8_quantize_t(const uint16_t* x, int64_t batch, int rows, int cols,
                                   uint8_t* codes, uint8_t* scales, void* stream);
 
+/* Both orientations from one read of x: the output of mok_mxfp8_quantize
+ * (codes [batch][rows][cols], scales [batch][rows][cols/32]) and that of
+ * mok_mxfp8_quantize_t (codes_t [batch][cols][rows], scales_t
+ * [batch][cols][rows/32]), bit for bit.  This is the MOK_MODE_MXFP8 weight
+ * prequantisation: a weight needs its forward copy (blocks along K) and its
+ * backward copy (blocks along the leading axis).  Same conditions as
+ * mok_mxfp8_quantize_t; codes and codes_t 16-byte aligned. */
+mok_status_t mok_mxfp8_quantize_dual(const uint16_t* x, int64_t batch, int rows, int cols,
+                                     uint8_t* codes, uint8_t* scales, uint8_t* codes_t,
+                                     uint8_t* scales_t, void* stream);
+
 /* ---- forward ([MoKDoc] _MoKRuntime.forward) -----------------------------
  * y[t] = S(x[t]) + sum_j w[t,j] * F_{e[t,j]}(x[t]),
  * F_e(v) = W_down[e] (silu(W_gate[e] v) * (W_up[e] v)), S the same with the

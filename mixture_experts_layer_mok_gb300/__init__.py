@@ -17,7 +17,7 @@ import torch
 from . import _lib
 from ._lib import MokError  # noqa: F401
 
-__all__ = ["schedule", "schedule_noalloc", "mxfp8_quantize", "mxfp8_quantize_t", "forward", "backward", "Schedule",
+__all__ = ["schedule", "schedule_noalloc", "mxfp8_quantize", "mxfp8_quantize_t", "mxfp8_quantize_dual", "forward", "backward", "Schedule",
            "Weights", "Context", "MokError", "quantize_weights", "MODES"]
 
 # forward/backward precision: "bf16"; "mxfp8" (MXFP8 forward GEMMs, bf16
@@ -183,21 +183,39 @@ def mxfp8_quantize_t(x: torch.Tensor, stream=None):
     return codes, scales
 
 
+def mxfp8_quantize_dual(x: torch.Tensor, stream=None):
+    """Both orientations from one read: ((codes, scales) as ``mxfp8_quantize``,
+    (codes_t, scales_t) as ``mxfp8_quantize_t``), for a [batch, rows, cols] or
+    [rows, cols] bf16 tensor."""
+    lib = _lib.load()
+    if x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous() or x.dim() not in (2, 3):
+        raise ValueError("x must be a contiguous CUDA bf16 matrix or batch of matrices")
+    x3 = x if x.dim() == 3 else x.unsqueeze(0)
+    B, R, Cc = x3.shape
+    codes = torch.empty((B, R, Cc), dtype=torch.uint8, device=x.device)
+    scales = torch.empty((B, R, Cc // 32), dtype=torch.uint8, device=x.device)
+    codes_t = torch.empty((B, Cc, R), dtype=torch.uint8, device=x.device)
+    scales_t = torch.empty((B, Cc, R // 32), dtype=torch.uint8, device=x.device)
+    _lib.check(lib.mok_mxfp8_quantize_dual(_ptr(x3), B, R, Cc, _ptr(codes), _ptr(scales), _ptr(codes_t),
+                                           _ptr(scales_t), _stream(stream)), "mok_mxfp8_quantize_dual")
+    if x.dim() == 2:
+        codes, scales, codes_t, scales_t = codes[0], scales[0], codes_t[0], scales_t[0]
+    return (codes, scales), (codes_t, scales_t)
+
+
 def quantize_weights(w: Weights, stream=None, backward: bool = False) -> Weights:
     """Prequantise every weight along its K axis for the MXFP8 modes; with
     ``backward`` also along its leading axis (the transposed copies the
     "mxfp8_full" backward's dgrad GEMMs read)."""
-    mx = {"_gate": mxfp8_quantize(w.w_gate, stream), "_up": mxfp8_quantize(w.w_up, stream),
-          "_down": mxfp8_quantize(w.w_down, stream)}
+    names = [("_gate", "t_gate", w.w_gate), ("_up", "t_up", w.w_up), ("_down", "t_down", w.w_down)]
     if w.ws_gate is not None:
-        mx.update({"s_gate": mxfp8_quantize(w.ws_gate, stream), "s_up": mxfp8_quantize(w.ws_up, stream),
-                   "s_down": mxfp8_quantize(w.ws_down, stream)})
-    if backward:
-        mx.update({"t_gate": mxfp8_quantize_t(w.w_gate, stream), "t_up": mxfp8_quantize_t(w.w_up, stream),
-                   "t_down": mxfp8_quantize_t(w.w_down, stream)})
-        if w.ws_gate is not None:
-            mx.update({"ts_gate": mxfp8_quantize_t(w.ws_gate, stream), "ts_up": mxfp8_quantize_t(w.ws_up, stream),
-                       "ts_down": mxfp8_quantize_t(w.ws_down, stream)})
+        names += [("s_gate", "ts_gate", w.ws_gate), ("s_up", "ts_up", w.ws_up), ("s_down", "ts_down", w.ws_down)]
+    mx = {}
+    for fwd_name, bwd_name, t in names:
+        if backward:   # both copies from one read of the weight
+            mx[fwd_name], mx[bwd_name] = mxfp8_quantize_dual(t, stream)
+        else:
+            mx[fwd_name] = mxfp8_quantize(t, stream)
     return Weights(w.w_gate, w.w_up, w.w_down, w.ws_gate, w.ws_up, w.ws_down, mx)
 
 

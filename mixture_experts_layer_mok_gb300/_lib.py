@@ -88,6 +88,7 @@ SIGNATURES = {
                                        C.POINTER(MokSchedule), P]),
     "mok_mxfp8_quantize": (C.c_int, [P, C.c_int64, C.c_int, P, P, P]),
     "mok_mxfp8_quantize_t": (C.c_int, [P, C.c_int64, C.c_int, C.c_int, P, P, P]),
+    "mok_mxfp8_quantize_dual": (C.c_int, [P, C.c_int64, C.c_int, C.c_int, P, P, P, P, P]),
     "mok_ctx_bytes": (C.c_size_t, [C.c_int] * 7),
     "mok_forward": (C.c_int, [C.POINTER(MokConfig), P, P, C.POINTER(MokSchedule),
                               C.POINTER(MokWeights), P, P, C.c_size_t, C.POINTER(MokCtx), P]),

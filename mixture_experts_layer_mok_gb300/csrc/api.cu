@@ -320,8 +320,10 @@ size_t carve_bwd(void* buf, int T, int k, int E, int H, int I, int Is, int mode,
   const bool mx = (mode == MOK_MODE_MXFP8);
   Carver c(buf);
   memset(L, 0, sizeof(*L));
-  L->dgu = c.take<uint16_t>(mr * 2 * I);
-  L->hw = c.take<uint16_t>(mr * I);
+  if (!mx) {   // the MXFP8 backward keeps these only as E4M3 codes
+    L->dgu = c.take<uint16_t>(mr * 2 * I);
+    L->hw = c.take<uint16_t>(mr * I);
+  }
   // two column halves per N tile (128-wide tiles in the MXFP8 backward)
   L->dw_part = c.take<float>(n * 2 * (I / (mx ? 128 : tile_n(I))));
   L->dx_slots = c.take<uint16_t>(mr * H);
@@ -330,14 +332,16 @@ size_t carve_bwd(void* buf, int T, int k, int E, int H, int I, int Is, int mode,
     L->xb_perm = c.take<uint16_t>(mr * H);
   }
   if (Is > 0) {
-    L->dgu_s = c.take<uint16_t>(Tl * 2 * Is);
-    L->hs = c.take<uint16_t>(Tl * Is);
+    if (!mx) {
+      L->dgu_s = c.take<uint16_t>(Tl * 2 * Is);
+      L->hs = c.take<uint16_t>(Tl * Is);
+    }
     L->dx_s = c.take<uint16_t>(Tl * H);
   }
   if (mx) {
     L->dyq = c.take<uint8_t>(mr * H);
     L->dyq_sc = c.take<uint8_t>(tiled_scale_bytes(mr, H));
-    L->dyq_tok = c.take<uint8_t>(Tl * H);
+    L->dyq_tok = c.take<uint8_t>(Tp * H);   // rows up to the 128-row boundary (zeros past T)
     L->dyq_tok_sc = c.take<uint8_t>(tiled_scale_bytes(Tl, H));
     L->dyT = c.take<uint8_t>(mr * H);
     L->dyT_sc = c.take<uint8_t>(tiled_scale_bytes(H, mr));
@@ -752,7 +756,8 @@ cudaError_t launch_mx_tiles(const MxMaps& m, const GemmParams& p, int bn, long l
 //   weight gradients      A, B = transposes of the row operands (along rows)
 //   dgrad through gate/up A = dG|dU rows (along I)          B = W_gate^T | W_up^T (along I)
 // dy and x are quantised here (rows, and transposed through the schedule);
-// dG|dU and w h are quantised after the SwiGLU backward writes them in bf16.
+// the SwiGLU backward's epilogue writes dG|dU (rows and transposed) and w h
+// (transposed) straight as E4M3 codes, quantised from their bf16 values.
 mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const uint16_t* x, const float* router_w,
                             const mok_schedule_t* s, const mok_ctx_t* ctx, const mok_weights_t* w,
                             uint16_t* dx, float* d_router_w, const mok_weight_grads_t* g, const BwdLayout& L,
@@ -778,13 +783,14 @@ mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const u
     MOK_CUDA(launch_mx_quantize_t(x, H, 1, Tp, H, T, nullptr, 1, nullptr, L.xT_tok, L.xT_tok_sc, 1, sms, side->s));
   }
   MOK_CUDA(cudaEventRecord(side->join, side->s));
-  // ---- dy: rows (token and schedule order) and transposed
+  // ---- dy, rows and transposed from one read: in schedule order (routed) and
+  // in token order (shared expert)
   MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 0, cs));
-  MOK_CUDA(launch_mx_dispatch(dy, T, H, k, s->slot_row, s->row_src, s->header, mr, L.dyq_tok, L.dyq_tok_sc, L.dyq,
-                              L.dyq_sc, sms, cs));
-  MOK_CUDA(launch_mx_quantize_t(dy, H, 1, mri, H, mri, s->row_src, k, s->header, L.dyT, L.dyT_sc, 1, sms, cs));
+  MOK_CUDA(launch_mx_quantize_t(dy, H, 1, mri, H, mri, s->row_src, k, s->header, L.dyT, L.dyT_sc, 1, sms, cs, L.dyq,
+                                L.dyq_sc, 1));
   if (Is > 0)
-    MOK_CUDA(launch_mx_quantize_t(dy, H, 1, Tp, H, T, nullptr, 1, nullptr, L.dyT_tok, L.dyT_tok_sc, 1, sms, cs));
+    MOK_CUDA(launch_mx_quantize_t(dy, H, 1, Tp, H, T, nullptr, 1, nullptr, L.dyT_tok, L.dyT_tok_sc, 1, sms, cs,
+                                  L.dyq_tok, L.dyq_tok_sc, 1));
   MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 1, cs));
   MOK_CUDA(cudaStreamWaitEvent(cs, side->join, 0));
   const int bnH = tile_n(H);
@@ -794,22 +800,20 @@ mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const u
     const int bnS = tile_n(Is);
     {  // dgrad through down + SwiGLU backward
       MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DOWN, 0, cs));
+      // its epilogue writes dG|dU by rows (for the dgrad) and transposed (weight
+      // gradient), and h transposed, all as E4M3 codes
       MxMaps m;
       if ((st = make_map_u8(&m.a, L.dyq_tok, H, T, 128)) || (st = make_map_u8(&m.b0, w->mxts_down, H, Is, 128)))
         return st;
       m.b1 = m.b0;
       GemmParams p = base_params(nullptr, ctx->status, 0);
       p.rows = T; p.K = H; p.N = Is; p.n_tiles = Is / 128; p.b_rows_per_expert = 0;
-      p.aux0 = ctx->gu_s; p.out0 = L.dgu_s; p.out1 = L.hs;
-      p.swiglu_limit = ctx->swiglu_limit;
+      p.aux0 = ctx->gu_s; p.swiglu_limit = ctx->swiglu_limit;
+      p.out0 = L.dgusq; p.sf_out = L.dgusq_sc; p.out1 = L.dgusT; p.out2 = L.dgusT_sc; p.out3 = L.hsT;
+      p.sf_out2 = L.hsT_sc; p.ld = Tp;
       p.sfa = L.dyq_tok_sc; p.sfb0 = L.wtsd_sc;
       const long long items = static_cast<long long>(Tp / 128) * p.n_tiles;
-      MOK_CUDA((launch_gemm_mx<128, EPI_DOWN_BWD>(m, p, items < sms ? static_cast<int>(items) : sms, cs)));
-      // dG|dU by rows (for the dgrad) and transposed (weight gradient); h transposed
-      MOK_CUDA(launch_mx_quantize_rows(L.dgu_s, T, 2 * Is, T, nullptr, L.dgusq, L.dgusq_sc, sms, cs));
-      MOK_CUDA(launch_mx_quantize_t(L.dgu_s, 2 * Is, 1, Tp, 2 * Is, T, nullptr, 1, nullptr, L.dgusT, L.dgusT_sc, 1,
-                                    sms, cs));
-      MOK_CUDA(launch_mx_quantize_t(L.hs, Is, 1, Tp, Is, T, nullptr, 1, nullptr, L.hsT, L.hsT_sc, 1, sms, cs));
+      MOK_CUDA((launch_gemm_mx<128, EPI_DOWN_BWD_MX>(m, p, items < sms ? static_cast<int>(items) : sms, cs)));
       MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DOWN, 1, cs));
     }
     {  // dW_s_down = dy^T h_s
@@ -868,15 +872,12 @@ mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const u
     m.b1 = m.b0;
     GemmParams p = base_params(s, ctx->status, 0);
     p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / 128; p.b_rows_per_expert = I;
-    p.aux0 = ctx->gu; p.out0 = L.dgu; p.out1 = L.hw; p.rw = router_w; p.dw_part = L.dw_part;
-    p.swiglu_limit = ctx->swiglu_limit;
+    p.aux0 = ctx->gu; p.rw = router_w; p.dw_part = L.dw_part; p.swiglu_limit = ctx->swiglu_limit;
+    p.out0 = L.dguq; p.sf_out = L.dguq_sc; p.out1 = L.dguT; p.out2 = L.dguT_sc; p.out3 = L.hwT;
+    p.sf_out2 = L.hwT_sc; p.ld = mr;
     p.sfa = L.dyq_sc; p.sfb0 = L.wtd_sc;
     const long long items = static_cast<long long>(s->max_tiles) * p.n_tiles;
-    MOK_CUDA((launch_gemm_mx<128, EPI_DOWN_BWD>(m, p, items < sms ? static_cast<int>(items) : sms, cs)));
-    MOK_CUDA(launch_mx_quantize_rows(L.dgu, mr, 2 * I, mr, s->header, L.dguq, L.dguq_sc, sms, cs));
-    MOK_CUDA(launch_mx_quantize_t(L.dgu, 2 * I, 1, mri, 2 * I, mri, nullptr, 1, s->header, L.dguT, L.dguT_sc, 1, sms,
-                                  cs));
-    MOK_CUDA(launch_mx_quantize_t(L.hw, I, 1, mri, I, mri, nullptr, 1, s->header, L.hwT, L.hwT_sc, 1, sms, cs));
+    MOK_CUDA((launch_gemm_mx<128, EPI_DOWN_BWD_MX>(m, p, items < sms ? static_cast<int>(items) : sms, cs)));
     MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DOWN, 1, cs));
   }
   {  // dW_down[e] = sum over e's rows of dy[t(r)]^T (w h)[r]
@@ -1011,6 +1012,22 @@ mok_status_t mok_mxfp8_quantize_t(const uint16_t* x, int64_t batch, int rows, in
   if (st) return st;
   MOK_CUDA(launch_mx_quantize_t(x, cols, static_cast<int>(batch), rows, cols, rows, nullptr, 1, nullptr, codes, scales,
                                 0, sms, static_cast<cudaStream_t>(stream)));
+  return MOK_OK;
+}
+
+mok_status_t mok_mxfp8_quantize_dual(const uint16_t* x, int64_t batch, int rows, int cols, uint8_t* codes,
+                                     uint8_t* scales, uint8_t* codes_t, uint8_t* scales_t, void* stream) {
+  if (batch < 0 || rows < 0 || cols < 0 || rows % 32 || cols % 64)
+    return fail(MOK_ERR_INVALID_ARG, "need batch, rows, cols >= 0, rows %% 32 == 0 and cols %% 64 == 0");
+  if (batch == 0 || rows == 0 || cols == 0) return MOK_OK;
+  if (batch > (1ll << 30) / 64) return fail(MOK_ERR_INVALID_ARG, "batch too large");
+  if (!x || !codes || !scales || !codes_t || !scales_t) return fail(MOK_ERR_INVALID_ARG, "NULL argument");
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(codes_t)) return fail(MOK_ERR_INVALID_ARG, "misaligned pointer");
+  int sms = 0;
+  mok_status_t st = device_info(&sms);
+  if (st) return st;
+  MOK_CUDA(launch_mx_quantize_t(x, cols, static_cast<int>(batch), rows, cols, rows, nullptr, 1, nullptr, codes_t,
+                                scales_t, 0, sms, static_cast<cudaStream_t>(stream), codes, scales, 0));
   return MOK_OK;
 }
 

@@ -56,6 +56,8 @@ enum Epi : int {
   EPI_STORE_ROWS = 3,    // out[row] = bf16(acc) for dense rows
   EPI_DOWN_BWD = 4,      // dH = w Z; SwiGLU backward; d_w partial = sum Z h; hw = w h
   EPI_WGRAD = 6,         // out[e][m][n] = bf16(acc), rows split over two tensors
+  EPI_DOWN_BWD_MX = 7,   // EPI_DOWN_BWD with MXFP8 outputs (gemm_mx_kernel): dG|dU by rows,
+                         // and dG|dU, w h transposed in 32-row blocks
 };
 
 struct GemmMaps {
@@ -114,7 +116,8 @@ struct GemmParams {
   const uint8_t* sfa;
   const uint8_t* sfb0;
   const uint8_t* sfb1;
-  uint8_t* sf_out;   // EPI_SWIGLU_MX: scales of h, same layout
+  uint8_t* sf_out;   // EPI_SWIGLU_MX: scales of h, same layout; EPI_DOWN_BWD_MX: of dG|dU rows
+  uint8_t* sf_out2;  // EPI_DOWN_BWD_MX: scales of the transposed w h
   int sf_kga;        // 128-column groups of A's / B's scale layout (0 = K / 128); a weight
   int sf_kgb;        // gradient's operands span the whole row range, not one item's K
 };

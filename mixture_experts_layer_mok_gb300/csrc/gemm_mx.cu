@@ -86,7 +86,7 @@ MOK_INSTANTIATE_MX(256, EPI_STORE_ROWS)
 MOK_INSTANTIATE_MX(128, EPI_STORE_ROWS)
 // MXFP8 backward: SwiGLU backward through down (128-wide tiles keep its
 // per-thread accumulator share in registers), weight gradients, dgrad rows
-MOK_INSTANTIATE_MX(128, EPI_DOWN_BWD)
+MOK_INSTANTIATE_MX(128, EPI_DOWN_BWD_MX)
 MOK_INSTANTIATE_MX(256, EPI_WGRAD)
 MOK_INSTANTIATE_MX(128, EPI_WGRAD)
 MOK_INSTANTIATE_MX_PAIR(256, EPI_SWIGLU_MX)

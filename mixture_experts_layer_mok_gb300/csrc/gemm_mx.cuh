@@ -47,14 +47,18 @@ struct MxCfg {
   static constexpr int kTmaBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kBarBytes = 512;
-  static constexpr int kEpiStageBytes = 2048;
+  // per epilogue warp: one 32-row staging block (2 KB); the MXFP8 SwiGLU
+  // backward stages its three 32 x 32 output blocks (dG, dU, w h)
+  static constexpr int kEpiStageBytes = EPI == EPI_DOWN_BWD_MX ? 3 * 2048 : 2048;
   static constexpr int kStagesFit =
       (227 * 1024 - 1024 - kBarBytes - kEpiWarps * kEpiStageBytes) / (kStageBytes + kSfStride);
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
-  // TMEM: accumulator columns [0, BN), then one 16-column scale slot per stage
-  // (A: 4 columns at +0, B: 4 columns per 128 rows at +8)
-  static constexpr int kSfCol0 = BN;
+  // TMEM: accumulator columns (two buffers of BN when they fit beside the
+  // scale ring, else one), then one 16-column scale slot per stage (A: 4
+  // columns at +0, B: 4 columns per 128 rows at +8)
   static constexpr int kTmemCols = 512;
+  static constexpr int kAccBufs = (2 * BN + 16 * kStages <= kTmemCols) ? 2 : 1;
+  static constexpr int kSfCol0 = kAccBufs * BN;
   static constexpr int kSmemBytes =
       1024 + kStages * (kStageBytes + kSfStride) + kBarBytes + kEpiWarps * kEpiStageBytes;
   static_assert(BN == 128 || BN == 256, "tile N");
@@ -65,6 +69,51 @@ struct MxCfg {
   static_assert(!PAIR || BN == 256, "CTA pairs split a 256-wide B tile");
 };
 
+// A 32 x 32 bf16 block staged in shared memory: 32 rows of 16 packed words,
+// word w of row l at l*16 + (w ^ (l & 15)), so that both a lane reading its
+// own row and a lane reading one column (across the 32 rows) spread over the
+// banks.
+__device__ __forceinline__ void stage_put(uint32_t* blk, int row, int w, uint32_t val) {
+  blk[row * 16 + (w ^ (row & 15))] = val;
+}
+
+__device__ __forceinline__ uint32_t mx_store_codes(const float* v, uint8_t* dst) {
+  uint8_t q[32];
+  const uint32_t s = mx_quantize32(v, q);
+  if (dst) {
+    uint4* d = reinterpret_cast<uint4*>(dst);
+    d[0] = reinterpret_cast<const uint4*>(q)[0];
+    d[1] = reinterpret_cast<const uint4*>(q)[1];
+  }
+  return s;
+}
+
+// MXFP8 block along this lane's row of a staged block: the 32 E4M3 codes go to
+// dst (NULL = nowhere); returns the E8M0 scale code.
+__device__ __forceinline__ uint32_t mx_row_from_stage(const uint32_t* blk, int lane, uint8_t* dst) {
+  float v[32];
+#pragma unroll
+  for (int w = 0; w < 16; ++w) {
+    const uint32_t x = blk[lane * 16 + (w ^ (lane & 15))];
+    v[2 * w] = __uint_as_float(x << 16);
+    v[2 * w + 1] = __uint_as_float(x & 0xFFFF0000u);
+  }
+  return mx_store_codes(v, dst);
+}
+
+// MXFP8 block down column `lane` of a staged block (its 32 rows): the 32 E4M3
+// codes go to dst (a row of the transposed tensor); returns the scale code.
+__device__ __forceinline__ uint32_t mx_col_from_stage(const uint32_t* blk, int lane, uint8_t* dst) {
+  float v[32];
+  const int wc = lane >> 1;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const uint32_t x = blk[i * 16 + (wc ^ (i & 15))];
+    v[i] = __uint_as_float((lane & 1) ? (x & 0xFFFF0000u) : (x << 16));
+  }
+  return mx_store_codes(v, dst);
+}
+
 // Shared-memory descriptor of a 512-byte scale atom as the tcgen05.cp source:
 // 32 rows of 16 bytes, no swizzle, 8-row groups 128 bytes apart.
 __device__ __forceinline__ uint64_t sf_atom_desc(uint32_t saddr) { return smem_desc(saddr, 128, 128, 0); }
@@ -74,9 +123,11 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
     gemm_mx_kernel(const __grid_constant__ MxMaps maps, const GemmParams p) {
   using C = MxCfg<BN, EPI, PAIR>;
   static_assert(EPI == EPI_SWIGLU_MX || EPI == EPI_SCALE_ROWS || EPI == EPI_STORE_ROWS || EPI == EPI_WGRAD ||
-                    EPI == EPI_DOWN_BWD,
+                    EPI == EPI_DOWN_BWD_MX,
                 "epilogue");
-  static_assert(!PAIR || (EPI != EPI_WGRAD && EPI != EPI_DOWN_BWD), "backward epilogues run on single CTAs");
+  static_assert(!PAIR || (EPI != EPI_WGRAD && EPI != EPI_DOWN_BWD_MX), "backward epilogues run on single CTAs");
+  static_assert(EPI != EPI_DOWN_BWD_MX || (BN == 128 && C::kAccBufs == 2),
+                "MXFP8 SwiGLU backward: 64 columns per thread, double-buffered accumulator");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -84,9 +135,9 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sf_smem + C::kStages * C::kSfStride);
   uint64_t* full = bars;
   uint64_t* empty = bars + C::kStages;
-  uint64_t* tfull = bars + 2 * C::kStages;
-  uint64_t* tempty = tfull + 1;
-  uint64_t* done = tempty + 1;
+  uint64_t* tfull = bars + 2 * C::kStages;   // per accumulator buffer
+  uint64_t* tempty = tfull + 2;
+  uint64_t* done = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -106,8 +157,10 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(tfull, 1);
-    mbar_init(tempty, (PAIR ? 2 : 1) * C::kEpiWarps);   // the leader's counts both CTAs' warps
+    for (int b = 0; b < C::kAccBufs; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], (PAIR ? 2 : 1) * C::kEpiWarps);   // the leader's counts both CTAs' warps
+    }
     mbar_init(done, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -232,14 +285,15 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
     if (lane == 0 && (!PAIR || rank == 0)) {   // a CTA pair's leader issues for both
       int stage = 0;
       uint32_t phase = 0;
+      int abuf = 0;
       uint32_t aphase = 0;
       bool first = true;
       for (int idx = item0; idx < nitems; idx += istep) {
         const Item it = item_at(idx);
         if (it.nk == 0) continue;
-        if (!mbar_wait(tempty, aphase ^ 1, abort_flag, p.status)) break;
+        if (!mbar_wait(&tempty[abuf], aphase ^ 1, abort_flag, p.status)) break;
         tc_fence_after();
-        const uint32_t acc = tmem_base;
+        const uint32_t acc = tmem_base + static_cast<uint32_t>(abuf * BN);
         bool ok = true;
         for (int kb = 0; kb < it.nk; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
@@ -286,12 +340,15 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
         const bool drop = (p.debug & 1) && first && blockIdx.x == 0;
         if (!drop) {
           if (PAIR)
-            umma_commit_pair(tfull, 0x3);
+            umma_commit_pair(&tfull[abuf], 0x3);
           else
-            umma_commit(tfull);
+            umma_commit(&tfull[abuf]);
         }
         first = false;
-        aphase ^= 1;
+        if (++abuf == C::kAccBufs) {
+          abuf = 0;
+          aphase ^= 1;
+        }
       }
       // every MMA issued by this thread must finish before TMEM is released
       if (PAIR)
@@ -306,6 +363,7 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
     const int half = (warp - 2) >> 2;      // which half of the columns
     const int r = q * 32 + lane;           // tile row of this thread
     uint8_t* wstage = sf_smem + C::kStages * C::kSfStride + C::kBarBytes + (warp - 2) * C::kEpiStageBytes;
+    int abuf = 0;
     uint32_t aphase = 0;
     constexpr int kCols = BN / 2;          // accumulator columns per thread
     // weight gradients: destination of output row m of expert e (rows below
@@ -340,32 +398,42 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
         f = __ldg(p.row_src + prow);
         if (f >= 0) wt = __ldg(p.rw + f);
       }
-      int w = (lane == 0) ? (mbar_wait(tfull, aphase, abort_flag, p.status) ? 1 : 0) : 0;
+      int w = (lane == 0) ? (mbar_wait(&tfull[abuf], aphase, abort_flag, p.status) ? 1 : 0) : 0;
       w = __shfl_sync(0xffffffffu, w, 0);
       if (!w) break;
       tc_fence_after();
-      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-      // this thread's share of the accumulator, then TMEM goes back to the MMA
-      float v[kCols];
-      if (kSwiGLU) {   // gate columns [half*BN/4, +BN/4), up columns BN/2 later
-#pragma unroll
-        for (int c = 0; c < kCols / 64; ++c) {
-          tmem_ld32(tb + half * (BN / 4) + c * 32, v + c * 32);
-          tmem_ld32(tb + BN / 2 + half * (BN / 4) + c * 32, v + kCols / 2 + c * 32);
+      const uint32_t tb = tmem_base + static_cast<uint32_t>(abuf * BN) + (static_cast<uint32_t>(q * 32) << 16);
+      // the accumulator buffer goes back to the MMA (a pair: on the leader's barrier)
+      auto release_acc = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (PAIR && rank != 0)
+            mbar_arrive_cluster(cluster_addr(&tempty[abuf], 0));
+          else
+            mbar_arrive(&tempty[abuf]);
         }
-      } else {
+        if (++abuf == C::kAccBufs) {
+          abuf = 0;
+          aphase ^= 1;
+        }
+      };
+      // this thread's share of the accumulator, then TMEM goes back to the MMA
+      // (the SwiGLU backward reads its chunks as it goes, from a second buffer)
+      float v[EPI == EPI_DOWN_BWD_MX ? 1 : kCols];
+      if constexpr (EPI != EPI_DOWN_BWD_MX) {
+        if (kSwiGLU) {   // gate columns [half*BN/4, +BN/4), up columns BN/2 later
 #pragma unroll
-        for (int c = 0; c < kCols / 32; ++c) tmem_ld32(tb + half * kCols + c * 32, v + c * 32);
+          for (int c = 0; c < kCols / 64; ++c) {
+            tmem_ld32(tb + half * (BN / 4) + c * 32, v + c * 32);
+            tmem_ld32(tb + BN / 2 + half * (BN / 4) + c * 32, v + kCols / 2 + c * 32);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < kCols / 32; ++c) tmem_ld32(tb + half * kCols + c * 32, v + c * 32);
+        }
+        release_acc();
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {   // TMEM is free again (a pair: on the leader's barrier)
-        if (PAIR && rank != 0)
-          mbar_arrive_cluster(cluster_addr(tempty, 0));
-        else
-          mbar_arrive(tempty);
-      }
-      aphase ^= 1;
 
       uint32_t wv[16];
       if constexpr (EPI == EPI_SWIGLU_MX) {
@@ -430,12 +498,14 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
           pack_bf16x32(v + c * 32, wv);
           warp_store_row64(wv, dst + c * 32, wstage, lane);
         }
-      } else if constexpr (EPI == EPI_DOWN_BWD) {
-        // Z = dy . W_down (this thread's kCols columns in v); aux0 = the saved
-        // gate|up pre-activations [rows][2N]; out0 = dG|dU [rows][2N], out1 =
-        // w h [rows][N], dw_part[f][n_tiles][2] = sum over the columns of Z h.
-        // Grouped rows: padding rows of an expert's range get zeros (the weight
-        // gradients contract over them); dense rows past the end store nothing.
+      } else if constexpr (EPI == EPI_DOWN_BWD_MX) {
+        // dgrad through down + SwiGLU backward, with the MXFP8 operands of the
+        // next GEMMs as outputs, each quantised from the bf16-rounded value:
+        // out0 = dG|dU codes [rows][2N] by rows (scales sf_out, tensor-core
+        // layout), out1 = dG|dU codes transposed [2N][ld] and out3 = (w h) codes
+        // transposed [N][ld], both in 32-row blocks (scales out2, sf_out2);
+        // ld = rows of the transposed tensors (schedule rows, or tokens padded
+        // to 128).  Padding rows and dense rows past the end count as zeros.
         int f = -1;
         bool v_ok;
         float wt = 1.f;
@@ -446,53 +516,89 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
         } else {
           v_ok = valid;
         }
-        const bool st_ok = live && (p.grouped ? true : valid);
+        const bool st_ok = live && (p.grouped ? true : valid);   // the row exists in out0
         const int col0 = n0 + half * kCols;
         const uint16_t* gu = static_cast<const uint16_t*>(p.aux0) + static_cast<long long>(prow) * 2 * p.N + col0;
-        uint16_t* dgu = static_cast<uint16_t*>(p.out0) + static_cast<long long>(prow) * 2 * p.N + col0;
-        uint16_t* hwo = static_cast<uint16_t*>(p.out1) + static_cast<long long>(prow) * p.N + col0;
+        uint8_t* rowq = static_cast<uint8_t*>(p.out0) + static_cast<long long>(prow) * 2 * p.N;
+        const long long ldt = p.ld;
+        const int cgr = 2 * p.N / 128, cgt = static_cast<int>(ldt / 128);
+        const int rblk = (it.p0 + q * 32) / 32;                // 32-row block of this warp's rows
+        const long long tcol = it.p0 + q * 32;                 // its first row in the transposed tensors
+        uint32_t* blk_g = reinterpret_cast<uint32_t*>(wstage);   // staged dG, dU, w h blocks
+        uint32_t* blk_u = blk_g + 512;
+        uint32_t* blk_h = blk_g + 1024;
         const float lim = p.swiglu_limit;
         float dpart = 0.f;
-#pragma unroll
-        for (int c = 0; c < kCols / 32; ++c) {   // unrolled: v stays in registers
-          uint4 ng[4], nu[4];
-          if (v_ok) {
-            load_raw64(gu + c * 32, ng);
-            load_raw64(gu + p.N + c * 32, nu);
-          }
-          uint32_t wdg[16], wdu[16], whv[16];
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float a[2] = {0.f, 0.f}, b[2] = {0.f, 0.f}, hh[2] = {0.f, 0.f};
+        uint32_t rsc_g = 0, rsc_u = 0;
+#pragma unroll 1
+        for (int c = 0; c < kCols / 32; ++c) {
+#pragma unroll 1
+          for (int hf = 0; hf < 2; ++hf) {   // 16 columns at a time keep the registers low
+            float z[16];
+            tmem_ld16(tb + half * kCols + c * 32 + hf * 16, z);
+            uint4 ng[2], nu[2];
             if (v_ok) {
-#pragma unroll
-              for (int t = 0; t < 2; ++t) {
-                float g = bf16_at(ng, i + t), u = bf16_at(nu, i + t);
-                float mg = 1.f, mu = 1.f;   // the clamp's derivative (SwiGLU limit)
-                if (lim > 0.f) {
-                  mg = (g <= lim) ? 1.f : 0.f;
-                  mu = (fabsf(u) <= lim) ? 1.f : 0.f;
-                  g = fminf(g, lim);
-                  u = fminf(fmaxf(u, -lim), lim);
-                }
-                const float z = v[c * 32 + i + t];
-                const float sg = __fdividef(1.f, 1.f + __expf(-g));
-                const float sl = g * sg;
-                const float h = sl * u;
-                dpart = fmaf(z, h, dpart);
-                const float dh = wt * z;
-                a[t] = dh * u * sg * (1.f + g * (1.f - sg)) * mg;
-                b[t] = dh * sl * mu;
-                hh[t] = wt * h;
-              }
+              const uint4* sg4 = reinterpret_cast<const uint4*>(gu + c * 32 + hf * 16);
+              const uint4* su4 = reinterpret_cast<const uint4*>(gu + p.N + c * 32 + hf * 16);
+              ng[0] = __ldg(sg4); ng[1] = __ldg(sg4 + 1);
+              nu[0] = __ldg(su4); nu[1] = __ldg(su4 + 1);
             }
-            wdg[i >> 1] = pack_bf16(a[0], a[1]);
-            wdu[i >> 1] = pack_bf16(b[0], b[1]);
-            whv[i >> 1] = pack_bf16(hh[0], hh[1]);
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) {
+              float a[2] = {0.f, 0.f}, b[2] = {0.f, 0.f}, hh[2] = {0.f, 0.f};
+              if (v_ok) {
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                  float g = bf16_at(ng, i + t), u = bf16_at(nu, i + t);
+                  float mg = 1.f, mu = 1.f;   // the clamp's derivative (SwiGLU limit)
+                  if (lim > 0.f) {
+                    mg = (g <= lim) ? 1.f : 0.f;
+                    mu = (fabsf(u) <= lim) ? 1.f : 0.f;
+                    g = fminf(g, lim);
+                    u = fminf(fmaxf(u, -lim), lim);
+                  }
+                  const float sg = __fdividef(1.f, 1.f + __expf(-g));
+                  const float sl = g * sg;
+                  const float h = sl * u;
+                  dpart = fmaf(z[i + t], h, dpart);
+                  const float dh = wt * z[i + t];
+                  a[t] = dh * u * sg * (1.f + g * (1.f - sg)) * mg;
+                  b[t] = dh * sl * mu;
+                  hh[t] = wt * h;
+                }
+              }
+              const int wi = hf * 8 + (i >> 1);
+              stage_put(blk_g, lane, wi, pack_bf16(a[0], a[1]));
+              stage_put(blk_u, lane, wi, pack_bf16(b[0], b[1]));
+              stage_put(blk_h, lane, wi, pack_bf16(hh[0], hh[1]));
+            }
           }
-          warp_store_row64(wdg, st_ok ? dgu + c * 32 : nullptr, wstage, lane);
-          warp_store_row64(wdu, st_ok ? dgu + p.N + c * 32 : nullptr, wstage, lane);
-          warp_store_row64(whv, st_ok ? hwo + c * 32 : nullptr, wstage, lane);
+          __syncwarp();
+          // transposed blocks: this lane's column of each, over the warp's 32 rows
+          const int tg = col0 + c * 32 + lane;
+          uint8_t* dguT = static_cast<uint8_t*>(p.out1);
+          uint8_t* dguT_sc = static_cast<uint8_t*>(p.out2);
+          const uint32_t cg_s = mx_col_from_stage(blk_g, lane, dguT + tg * ldt + tcol);
+          const uint32_t cu_s = mx_col_from_stage(blk_u, lane, dguT + (p.N + tg) * ldt + tcol);
+          const uint32_t ch_s = mx_col_from_stage(blk_h, lane, static_cast<uint8_t*>(p.out3) + tg * ldt + tcol);
+          if (live) {
+            dguT_sc[mx_tiled_scale_offset(tg, rblk, cgt)] = static_cast<uint8_t>(cg_s);
+            dguT_sc[mx_tiled_scale_offset(p.N + tg, rblk, cgt)] = static_cast<uint8_t>(cu_s);
+            p.sf_out2[mx_tiled_scale_offset(tg, rblk, cgt)] = static_cast<uint8_t>(ch_s);
+          }
+          // row blocks of dG and dU
+          rsc_g |= mx_row_from_stage(blk_g, lane, st_ok ? rowq + col0 + c * 32 : nullptr) << (8 * c);
+          rsc_u |= mx_row_from_stage(blk_u, lane, st_ok ? rowq + p.N + col0 + c * 32 : nullptr) << (8 * c);
+          __syncwarp();   // the blocks are read before the next chunk overwrites them
+        }
+        release_acc();
+        // this thread's two row blocks of dG and of dU are adjacent bytes of
+        // its row's scale word (rows past a dense layer's end: unit scales)
+        if (live) {
+          *reinterpret_cast<uint16_t*>(p.sf_out + mx_tiled_scale_offset(prow, col0 / 32, cgr)) =
+              static_cast<uint16_t>(rsc_g);
+          *reinterpret_cast<uint16_t*>(p.sf_out + mx_tiled_scale_offset(prow, (p.N + col0) / 32, cgr)) =
+              static_cast<uint16_t>(rsc_u);
         }
         if (p.grouped && v_ok) p.dw_part[(static_cast<long long>(f) * p.n_tiles + it.nt) * 2 + half] = dpart;
       } else {

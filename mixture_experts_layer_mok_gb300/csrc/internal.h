@@ -42,9 +42,8 @@ cudaError_t launch_mx_dispatch(const uint16_t* x, int T, int H, int topk, const 
                                uint8_t* xp_sc, int num_sms, cudaStream_t st);
 cudaError_t launch_mx_quantize_t(const uint16_t* src, long long ld, int batch, int R, int C, int valid_rows,
                                  const int* row_src, int topk, const int* header, uint8_t* codes, uint8_t* scales,
-                                 int tiled, int num_sms, cudaStream_t st);
-cudaError_t launch_mx_quantize_rows(const uint16_t* x, long long R, int K, long long valid_rows, const int* header,
-                                    uint8_t* codes, uint8_t* sc, int num_sms, cudaStream_t st);
+                                 int tiled, int num_sms, cudaStream_t st, uint8_t* rcodes = nullptr,
+                                 uint8_t* rscales = nullptr, int rtiled = 0);
 cudaError_t launch_mx_tile_scales(const uint8_t* src, long long rows, int K, uint8_t* dst, cudaStream_t st);
 cudaError_t launch_combine(const uint16_t* rows, const int* slot_row, const int* header, long long max_rows,
                            const uint16_t* base, int T, int k, int H, uint16_t* out, int num_sms, cudaStream_t st);

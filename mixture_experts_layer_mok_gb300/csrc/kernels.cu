@@ -379,15 +379,21 @@ cudaError_t launch_mx_dispatch(const uint16_t* x, int T, int H, int topk, const 
 // rows from P on read as zero and a failed schedule skips the work.  Output
 // codes [batch][C][R]; scales row-major [batch*C][R/32], or (tiled) in the
 // tensor-core scale layout with rows batch*C and K = R.  One block per
-// 128-row x 64-column tile: coalesced row loads into shared memory, then one
-// thread per (column, 32-row block).
+// 128-row x 64-column tile: coalesced row loads into shared memory, one
+// thread per (column, 32-row block) quantising into a shared-memory output
+// tile, then whole 128-byte code rows and one 4-byte scale word per column
+// out to global memory.  With rcodes, the same read also yields the codes
+// along the rows (blocks of 32 columns, scales rscales, row-major or tiled):
+// both orientations of one tensor from a single pass over it.
 // ===========================================================================
 __global__ void __launch_bounds__(256) mx_quantize_t_kernel(const uint16_t* __restrict__ src, long long ld, int batch,
                                                             int R, int C, int valid_rows,
                                                             const int* __restrict__ row_src, int topk,
                                                             const int* __restrict__ header,
                                                             uint8_t* __restrict__ codes,
-                                                            uint8_t* __restrict__ scales, int tiled) {
+                                                            uint8_t* __restrict__ scales, int tiled,
+                                                            uint8_t* __restrict__ rcodes,
+                                                            uint8_t* __restrict__ rscales, int rtiled) {
   griddep_wait();
   griddep_launch_dependents();
   int vrows = valid_rows;
@@ -395,7 +401,13 @@ __global__ void __launch_bounds__(256) mx_quantize_t_kernel(const uint16_t* __re
     if (header[2] != 0) return;
     vrows = min(vrows, header[1]);
   }
+  constexpr int kOutStride = 144;   // bytes per output row in shared memory (128 + 16: no bank conflicts)
+  // input tile: row r's 16-byte piece p sits at piece p ^ (r & 7), so that both
+  // column reads (one element of 32 rows) and row reads (half a row per
+  // thread) spread over the banks
   __shared__ __align__(16) uint16_t tile[128][64];
+  __shared__ __align__(16) uint8_t out[64 * kOutStride];
+  __shared__ uint32_t osc[64];
   const int rtiles = (R + 127) / 128, ctiles = C / 64;
   const long long ntiles = static_cast<long long>(batch) * rtiles * ctiles;
   const int c = threadIdx.x & 63, rb = threadIdx.x >> 6;
@@ -405,7 +417,7 @@ __global__ void __launch_bounds__(256) mx_quantize_t_kernel(const uint16_t* __re
     const int rt = static_cast<int>(rest % rtiles);
     const int b = static_cast<int>(rest / rtiles);
     const int r0 = rt * 128, c0 = ct * 64;
-    __syncthreads();   // the previous tile's readers are done with the buffer
+    __syncthreads();   // the previous tile's buffers are drained
     for (int i = threadIdx.x; i < 128 * 8; i += 256) {   // 8 pieces of 16 bytes per row
       const int row = i >> 3, piece = i & 7;
       const int r = r0 + row;
@@ -419,95 +431,83 @@ __global__ void __launch_bounds__(256) mx_quantize_t_kernel(const uint16_t* __re
         if (srow >= 0)
           v = __ldg(reinterpret_cast<const uint4*>(src + (static_cast<long long>(b) * R + srow) * ld + c0) + piece);
       }
-      reinterpret_cast<uint4*>(&tile[row][0])[piece] = v;
+      reinterpret_cast<uint4*>(&tile[row][0])[piece ^ (row & 7)] = v;
     }
     __syncthreads();
-    const int rr = r0 + rb * 32;
-    if (rr < R) {
+    {   // column c0 + c, rows r0 + 32 rb ..: codes into the output tile
       float v[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(static_cast<uint32_t>(tile[rb * 32 + i][c]) << 16);
+      for (int i = 0; i < 32; ++i) {
+        const int row = rb * 32 + i;
+        v[i] = __uint_as_float(static_cast<uint32_t>(tile[row][(((c >> 3) ^ (row & 7)) << 3) | (c & 7)]) << 16);
+      }
       uint8_t q[32];
       const uint32_t s = mx_quantize32(v, q);
-      const long long orow = static_cast<long long>(b) * C + c0 + c;
-      uint4* d = reinterpret_cast<uint4*>(codes + orow * R + rr);
-      d[0] = reinterpret_cast<const uint4*>(q)[0];
-      d[1] = reinterpret_cast<const uint4*>(q)[1];
-      if (tiled)
-        scales[mx_tiled_scale_offset(orow, rr / 32, R / 128)] = static_cast<uint8_t>(s);
-      else
-        scales[orow * (R / 32) + rr / 32] = static_cast<uint8_t>(s);
+      uint4* o = reinterpret_cast<uint4*>(out + c * kOutStride + rb * 32);
+      o[0] = reinterpret_cast<const uint4*>(q)[0];
+      o[1] = reinterpret_cast<const uint4*>(q)[1];
+      reinterpret_cast<uint8_t*>(osc)[c * 4 + rb] = static_cast<uint8_t>(s);
+    }
+    if (rcodes) {   // row r0 + (tid >> 1), columns c0 + 32 (tid & 1) ..: a block along the row
+      const int row = threadIdx.x >> 1, hb = threadIdx.x & 1;
+      const long long orr = static_cast<long long>(b) * R + r0 + row;
+      if (r0 + row < R) {
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 w = reinterpret_cast<const uint4*>(&tile[row][0])[(hb * 4 + j) ^ (row & 7)];
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            v[8 * j + 2 * k] = __uint_as_float(ws[k] << 16);
+            v[8 * j + 2 * k + 1] = __uint_as_float(ws[k] & 0xFFFF0000u);
+          }
+        }
+        uint8_t q[32];
+        const uint32_t s = mx_quantize32(v, q);
+        uint4* d = reinterpret_cast<uint4*>(rcodes + orr * C + c0 + hb * 32);
+        d[0] = reinterpret_cast<const uint4*>(q)[0];
+        d[1] = reinterpret_cast<const uint4*>(q)[1];
+        const int cb = (c0 >> 5) + hb;
+        if (rtiled)
+          rscales[mx_tiled_scale_offset(orr, cb, C / 128)] = static_cast<uint8_t>(s);
+        else
+          rscales[orr * (C / 32) + cb] = static_cast<uint8_t>(s);
+      }
+    }
+    __syncthreads();
+    const long long orow0 = static_cast<long long>(b) * C + c0;
+    for (int i = threadIdx.x; i < 64 * 8; i += 256) {   // 8 pieces of 16 code bytes per output row
+      const int row = i >> 3, piece = i & 7;
+      if (r0 + piece * 16 < R)
+        *reinterpret_cast<uint4*>(codes + (orow0 + row) * R + r0 + piece * 16) =
+            *reinterpret_cast<const uint4*>(out + row * kOutStride + piece * 16);
+    }
+    if (threadIdx.x < 64) {   // the column's four block scales
+      const long long orow = orow0 + threadIdx.x;
+      const uint32_t word = osc[threadIdx.x];
+      if (tiled) {
+        *reinterpret_cast<uint32_t*>(scales + mx_tiled_scale_offset(orow, r0 / 32, R / 128)) = word;
+      } else if ((R / 32) % 4 == 0 && (reinterpret_cast<uintptr_t>(scales) & 3u) == 0) {
+        *reinterpret_cast<uint32_t*>(scales + orow * (R / 32) + r0 / 32) = word;
+      } else {
+        for (int k = 0; k < 4 && r0 + 32 * k < R; ++k)
+          scales[orow * (R / 32) + r0 / 32 + k] = static_cast<uint8_t>(word >> (8 * k));
+      }
     }
   }
 }
 
 cudaError_t launch_mx_quantize_t(const uint16_t* src, long long ld, int batch, int R, int C, int valid_rows,
                                  const int* row_src, int topk, const int* header, uint8_t* codes, uint8_t* scales,
-                                 int tiled, int num_sms, cudaStream_t st) {
+                                 int tiled, int num_sms, cudaStream_t st, uint8_t* rcodes, uint8_t* rscales,
+                                 int rtiled) {
   const long long tiles = static_cast<long long>(batch) * ((R + 127) / 128) * (C / 64);
   if (tiles == 0) return cudaSuccess;
   const long long cap = static_cast<long long>(num_sms) * 8;
   const int grid = static_cast<int>(tiles < cap ? tiles : cap);
   cudaError_t err = launch_dependent(mx_quantize_t_kernel, dim3(grid), dim3(256), 0, st, src, ld, batch, R, C,
-                                     valid_rows, row_src, topk, header, codes, scales, tiled);
-  if (err != cudaSuccess) return err;
-  return cudaGetLastError();
-}
-
-// Row-wise MXFP8 quantiser with the scales written straight into the
-// tensor-core scale layout (rows R, K): rows below valid_rows (and below P
-// with a schedule header) are quantised; the rest of the 128-row blocks get
-// unit scales (their codes are never read: tiles stop at P, and TMA reads
-// zeros past a tensor's end).  One warp per row.
-__global__ void __launch_bounds__(256) mx_quantize_rows_kernel(const uint16_t* __restrict__ x, long long R, int K,
-                                                               long long valid_rows, const int* __restrict__ header,
-                                                               uint8_t* __restrict__ codes,
-                                                               uint8_t* __restrict__ sc) {
-  griddep_wait();
-  griddep_launch_dependents();
-  long long vrows = valid_rows;
-  if (header) {
-    if (header[2] != 0) return;
-    vrows = min(vrows, static_cast<long long>(header[1]));
-  }
-  const int lane = threadIdx.x & 31;
-  const int nb = K / 32, cg = K / 128;
-  const long long rpad = (R + 127) / 128 * 128;
-  for (long long j = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5; j < rpad;
-       j += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
-    if (j < vrows) {
-      for (int b0 = 0; b0 < nb; b0 += 32) {
-        const int b = b0 + lane;
-        const bool act = b < nb;       // whole aligned groups of 4 lanes share this
-        float v[32];
-        uint8_t q[32];
-        uint32_t s = 127;
-        if (act) {
-          load_bf16x32(x + j * K + static_cast<long long>(b) * 32, v);
-          s = mx_quantize32(v, q);
-          uint4* d = reinterpret_cast<uint4*>(codes + j * K + static_cast<long long>(b) * 32);
-          d[0] = reinterpret_cast<const uint4*>(q)[0];
-          d[1] = reinterpret_cast<const uint4*>(q)[1];
-        }
-        const uint32_t s1 = __shfl_down_sync(0xffffffffu, s, 1);
-        const uint32_t s2 = __shfl_down_sync(0xffffffffu, s, 2);
-        const uint32_t s3 = __shfl_down_sync(0xffffffffu, s, 3);
-        if (act && (lane & 3) == 0)
-          *reinterpret_cast<uint32_t*>(sc + mx_tiled_scale_offset(j, b, cg)) = s | (s1 << 8) | (s2 << 16) | (s3 << 24);
-      }
-    } else {
-      for (int g = lane; g < cg; g += 32)
-        *reinterpret_cast<uint32_t*>(sc + mx_tiled_scale_offset(j, 4 * g, cg)) = 0x7F7F7F7Fu;
-    }
-  }
-}
-
-cudaError_t launch_mx_quantize_rows(const uint16_t* x, long long R, int K, long long valid_rows, const int* header,
-                                    uint8_t* codes, uint8_t* sc, int num_sms, cudaStream_t st) {
-  if (R == 0) return cudaSuccess;
-  const long long rpad = (R + 127) / 128 * 128;
-  cudaError_t err = launch_dependent(mx_quantize_rows_kernel, dim3(grid_for(rpad * 32, 256, num_sms)), dim3(256), 0,
-                                     st, x, R, K, valid_rows, header, codes, sc);
+                                     valid_rows, row_src, topk, header, codes, scales, tiled, rcodes, rscales, rtiled);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }

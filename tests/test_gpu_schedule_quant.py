@@ -120,13 +120,20 @@ def test_quantize_empty():
 
 def _check_quant_t(x3):
     """The transposing quantiser against the oracle's quantiser applied to the
-    transpose of each matrix of the batch, bit for bit."""
+    transpose of each matrix of the batch, bit for bit; the dual quantiser
+    gives that and the row-wise quantisation from one read."""
     m = mok()
     codes, scales = m.mxfp8_quantize_t(x3.cuda())
+    (dc, ds), (dtc, dts) = m.mxfp8_quantize_dual(x3.cuda())
     for b in range(x3.shape[0]):
         rc, rs = oracle.mxfp8_quantize(x3[b].double().numpy().T)
         assert np.array_equal(codes[b].cpu().numpy(), rc), b
         assert np.array_equal(scales[b].cpu().numpy(), rs), b
+        assert np.array_equal(dtc[b].cpu().numpy(), rc), b
+        assert np.array_equal(dts[b].cpu().numpy(), rs), b
+        qc, qs = oracle.mxfp8_quantize(x3[b].double().numpy())
+        assert np.array_equal(dc[b].cpu().numpy(), qc), b
+        assert np.array_equal(ds[b].cpu().numpy(), qs), b
 
 
 @pytest.mark.parametrize("B,R,C,std", [(1, 32, 64, 1.0), (3, 160, 192, 0.02), (2, 1024, 2048, 0.02),

@@ -58,10 +58,12 @@ def test_buffer_sizes(lib):
     wb = lib.mok_bwd_workspace_bytes(T, k, E, H, I, Is, 0)
     assert wb >= 2 * (mt * 128 * 3 * I + T * k * H)
     assert lib.mok_bwd_workspace_bytes(T, k, E, H, I, Is, 1) == wb
-    # MXFP8 backward: E4M3 copies of dy, x (rows and transposed), dG|dU (rows
-    # and transposed) and w h (transposed), in place of the bf16 permuted copies
+    # MXFP8 backward: the bf16 dx rows, and E4M3 codes of dy (rows and
+    # transposed), x (transposed), dG|dU (rows and transposed) and w h
+    # (transposed) in place of the bf16 permuted copies and SwiGLU-backward rows
     wm = lib.mok_bwd_workspace_bytes(T, k, E, H, I, Is, 2)
-    assert wm >= 2 * (mt * 128 * 3 * I + T * k * H) + mt * 128 * (3 * H + 5 * I)
+    assert wm >= 2 * mt * 128 * H + mt * 128 * (3 * H + 5 * I)
+    assert wm < wb
     assert lib.mok_bwd_workspace_bytes(T, k, E, H, I, Is, 3) == 0
     # shapes outside the contract report 0
     assert lib.mok_ctx_bytes(T, k, E, 100, I, Is, 0) == 0
@@ -89,6 +91,8 @@ def test_argument_errors_need_no_device(lib):
     assert lib.mok_mxfp8_quantize_t(fake, -1, 64, 64, fake, fake, None) == _lib.MOK_ERR_INVALID_ARG
     assert lib.mok_mxfp8_quantize_t(None, 1, 64, 64, fake, fake, None) == _lib.MOK_ERR_INVALID_ARG
     assert lib.mok_mxfp8_quantize_t(fake, 0, 64, 64, fake, fake, None) == _lib.MOK_OK   # nothing to do
+    assert lib.mok_mxfp8_quantize_dual(fake, 1, 48, 64, fake, fake, fake, fake, None) == _lib.MOK_ERR_INVALID_ARG
+    assert lib.mok_mxfp8_quantize_dual(fake, 1, 64, 64, fake, fake, None, fake, None) == _lib.MOK_ERR_INVALID_ARG
     assert lib.mok_mxfp8_quantize(C.c_void_p(17), 4, 64, fake, fake, None) == _lib.MOK_ERR_INVALID_ARG
     assert lib.mok_mxfp8_quantize(None, 0, 64, None, None, None) == _lib.MOK_OK   # empty input
     cfg = _lib.MokConfig(mode=7)
