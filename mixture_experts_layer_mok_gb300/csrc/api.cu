@@ -165,6 +165,24 @@ mok_status_t make_map_out(CUtensorMap* m, const void* base, uint64_t cols, uint6
   return MOK_OK;
 }
 
+// Byte tensor [outer][inner] (E4M3 codes) for TMA stores of 32 x 32-byte
+// boxes, no swizzle; rows and columns past the tensor's end are not written.
+mok_status_t make_map_codes_out(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(MOK_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MOK_ERR_CUDA, "cuTensorMapEncodeTiled (code output) failed (%d) for [%llu x %llu]", (int)r,
+                (unsigned long long)outer, (unsigned long long)inner);
+  return MOK_OK;
+}
+
 // E8M0 scales in the tensor-core scale layout as rows of 128 bytes, four per
 // 512-byte atom (box: one atom), for the TMA loads of CTA-pair GEMMs.
 mok_status_t make_map_sf(CUtensorMap* m, const void* base, long long atoms) {
@@ -450,6 +468,7 @@ struct SideStream {
   cudaStream_t s = nullptr;
   cudaEvent_t fork = nullptr;
   cudaEvent_t join = nullptr;
+  cudaEvent_t join2 = nullptr;   // a second hand-back point within one call
 };
 thread_local SideStream g_side[64];
 
@@ -462,6 +481,7 @@ mok_status_t side_stream(SideStream** out) {
     MOK_CUDA(cudaStreamCreateWithFlags(&sd.s, cudaStreamNonBlocking));
     MOK_CUDA(cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming));
     MOK_CUDA(cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming));
+    MOK_CUDA(cudaEventCreateWithFlags(&sd.join2, cudaEventDisableTiming));
   }
   *out = &sd;
   return MOK_OK;
@@ -767,22 +787,26 @@ mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const u
   const int Tp = (T + 127) / 128 * 128;
   const int mri = static_cast<int>(mr);
   mok_status_t st;
-  // ---- weight scales into the tensor-core layout and the transposed x, on the side stream
+  // ---- on the side stream: weight scales into the tensor-core layout (the
+  // shared expert's first, handed back at `join`), then the transposed x,
+  // which only the gate/up weight gradients read (handed back at `join2`)
   SideStream* side = nullptr;
   if ((st = side_stream(&side))) return st;
   MOK_CUDA(cudaEventRecord(side->fork, cs));
   MOK_CUDA(cudaStreamWaitEvent(side->s, side->fork, 0));
-  MOK_CUDA(launch_mx_tile_scales(w->mxt_gate_sc, static_cast<long long>(E) * H, I, L.wtg_sc, side->s));
-  MOK_CUDA(launch_mx_tile_scales(w->mxt_up_sc, static_cast<long long>(E) * H, I, L.wtu_sc, side->s));
-  MOK_CUDA(launch_mx_tile_scales(w->mxt_down_sc, static_cast<long long>(E) * I, H, L.wtd_sc, side->s));
-  MOK_CUDA(launch_mx_quantize_t(x, H, 1, mri, H, mri, s->row_src, k, s->header, L.xT, L.xT_sc, 1, sms, side->s));
   if (Is > 0) {
     MOK_CUDA(launch_mx_tile_scales(w->mxts_gate_sc, H, Is, L.wtsg_sc, side->s));
     MOK_CUDA(launch_mx_tile_scales(w->mxts_up_sc, H, Is, L.wtsu_sc, side->s));
     MOK_CUDA(launch_mx_tile_scales(w->mxts_down_sc, Is, H, L.wtsd_sc, side->s));
-    MOK_CUDA(launch_mx_quantize_t(x, H, 1, Tp, H, T, nullptr, 1, nullptr, L.xT_tok, L.xT_tok_sc, 1, sms, side->s));
   }
+  MOK_CUDA(launch_mx_tile_scales(w->mxt_gate_sc, static_cast<long long>(E) * H, I, L.wtg_sc, side->s));
+  MOK_CUDA(launch_mx_tile_scales(w->mxt_up_sc, static_cast<long long>(E) * H, I, L.wtu_sc, side->s));
+  MOK_CUDA(launch_mx_tile_scales(w->mxt_down_sc, static_cast<long long>(E) * I, H, L.wtd_sc, side->s));
   MOK_CUDA(cudaEventRecord(side->join, side->s));
+  if (Is > 0)
+    MOK_CUDA(launch_mx_quantize_t(x, H, 1, Tp, H, T, nullptr, 1, nullptr, L.xT_tok, L.xT_tok_sc, 1, sms, side->s));
+  MOK_CUDA(launch_mx_quantize_t(x, H, 1, mri, H, mri, s->row_src, k, s->header, L.xT, L.xT_sc, 1, sms, side->s));
+  MOK_CUDA(cudaEventRecord(side->join2, side->s));
   // ---- dy, rows and transposed from one read: in schedule order (routed) and
   // in token order (shared expert)
   MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 0, cs));
@@ -803,14 +827,15 @@ mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const u
       // its epilogue writes dG|dU by rows (for the dgrad) and transposed (weight
       // gradient), and h transposed, all as E4M3 codes
       MxMaps m;
-      if ((st = make_map_u8(&m.a, L.dyq_tok, H, T, 128)) || (st = make_map_u8(&m.b0, w->mxts_down, H, Is, 128)))
+      if ((st = make_map_u8(&m.a, L.dyq_tok, H, T, 128)) || (st = make_map_u8(&m.b0, w->mxts_down, H, Is, 128)) ||
+          (st = make_map_codes_out(&m.o0, L.dgusq, 2ull * Is, T)) ||
+          (st = make_map_codes_out(&m.o1, L.dgusT, Tp, 2ull * Is)) || (st = make_map_codes_out(&m.o2, L.hsT, Tp, Is)))
         return st;
       m.b1 = m.b0;
       GemmParams p = base_params(nullptr, ctx->status, 0);
       p.rows = T; p.K = H; p.N = Is; p.n_tiles = Is / 128; p.b_rows_per_expert = 0;
       p.aux0 = ctx->gu_s; p.swiglu_limit = ctx->swiglu_limit;
-      p.out0 = L.dgusq; p.sf_out = L.dgusq_sc; p.out1 = L.dgusT; p.out2 = L.dgusT_sc; p.out3 = L.hsT;
-      p.sf_out2 = L.hsT_sc; p.ld = Tp;
+      p.sf_out = L.dgusq_sc; p.out2 = L.dgusT_sc; p.sf_out2 = L.hsT_sc; p.ld = Tp;   // codes: maps o0..o2
       p.sfa = L.dyq_tok_sc; p.sfb0 = L.wtsd_sc;
       const long long items = static_cast<long long>(Tp / 128) * p.n_tiles;
       MOK_CUDA((launch_gemm_mx<128, EPI_DOWN_BWD_MX>(m, p, items < sms ? static_cast<int>(items) : sms, cs)));
@@ -829,6 +854,7 @@ mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const u
       MOK_CUDA(launch_mx_tiles<EPI_WGRAD>(m, p, bnS, static_cast<long long>(p.m_tiles) * p.n_tiles, sms, cs));
       MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_DOWN, 1, cs));
     }
+    MOK_CUDA(cudaStreamWaitEvent(cs, side->join2, 0));   // the transposed x is ready
     {  // dW_s_gate|up = (dG_s|dU_s)^T x
       MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_GATEUP, 0, cs));
       MxMaps m;
@@ -860,6 +886,7 @@ mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const u
       MOK_CUDA(mark(cfg, sg, 0, cs));
       MOK_CUDA(mark(cfg, sg, 1, cs));
     }
+    MOK_CUDA(cudaStreamWaitEvent(cs, side->join2, 0));   // the transposed x is ready
   }
 
   // ---- routed: dgrad through down + SwiGLU backward + router-weight partials
@@ -867,14 +894,15 @@ mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const u
     MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DOWN, 0, cs));
     MxMaps m;
     if ((st = make_map_u8(&m.a, L.dyq, H, mr, 128)) ||
-        (st = make_map_u8(&m.b0, w->mxt_down, H, static_cast<uint64_t>(E) * I, 128)))
+        (st = make_map_u8(&m.b0, w->mxt_down, H, static_cast<uint64_t>(E) * I, 128)) ||
+        (st = make_map_codes_out(&m.o0, L.dguq, 2ull * I, mr)) || (st = make_map_codes_out(&m.o1, L.dguT, mr, 2ull * I)) ||
+        (st = make_map_codes_out(&m.o2, L.hwT, mr, I)))
       return st;
     m.b1 = m.b0;
     GemmParams p = base_params(s, ctx->status, 0);
     p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / 128; p.b_rows_per_expert = I;
     p.aux0 = ctx->gu; p.rw = router_w; p.dw_part = L.dw_part; p.swiglu_limit = ctx->swiglu_limit;
-    p.out0 = L.dguq; p.sf_out = L.dguq_sc; p.out1 = L.dguT; p.out2 = L.dguT_sc; p.out3 = L.hwT;
-    p.sf_out2 = L.hwT_sc; p.ld = mr;
+    p.sf_out = L.dguq_sc; p.out2 = L.dguT_sc; p.sf_out2 = L.hwT_sc; p.ld = mr;   // codes: maps o0..o2
     p.sfa = L.dyq_sc; p.sfb0 = L.wtd_sc;
     const long long items = static_cast<long long>(s->max_tiles) * p.n_tiles;
     MOK_CUDA((launch_gemm_mx<128, EPI_DOWN_BWD_MX>(m, p, items < sms ? static_cast<int>(items) : sms, cs)));

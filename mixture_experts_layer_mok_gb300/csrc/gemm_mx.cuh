@@ -30,6 +30,9 @@ namespace mok {
 struct MxMaps {
   CUtensorMap a, b0, b1;
   CUtensorMap sfa, sfb0, sfb1;
+  // EPI_DOWN_BWD_MX: its E4M3 outputs, stored by TMA in 32 x 32-byte boxes
+  // (dG|dU by rows, dG|dU transposed, w h transposed)
+  CUtensorMap o0, o1, o2;
 };
 
 template <int BN, int EPI, bool PAIR = false>
@@ -500,12 +503,13 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
         }
       } else if constexpr (EPI == EPI_DOWN_BWD_MX) {
         // dgrad through down + SwiGLU backward, with the MXFP8 operands of the
-        // next GEMMs as outputs, each quantised from the bf16-rounded value:
-        // out0 = dG|dU codes [rows][2N] by rows (scales sf_out, tensor-core
-        // layout), out1 = dG|dU codes transposed [2N][ld] and out3 = (w h) codes
-        // transposed [N][ld], both in 32-row blocks (scales out2, sf_out2);
-        // ld = rows of the transposed tensors (schedule rows, or tokens padded
-        // to 128).  Padding rows and dense rows past the end count as zeros.
+        // next GEMMs as outputs, each quantised from the bf16-rounded value and
+        // stored by TMA: map o0 = dG|dU codes [rows][2N] by rows (scales sf_out,
+        // tensor-core layout), o1 = dG|dU codes transposed [2N][ld] and o2 =
+        // (w h) codes transposed [N][ld], both in 32-row blocks (scales in out2
+        // and sf_out2); ld = rows of the transposed tensors (schedule rows, or
+        // tokens padded to 128).  Padding rows and dense rows past the end count
+        // as zeros (o0 clips the latter).
         int f = -1;
         bool v_ok;
         float wt = 1.f;
@@ -516,10 +520,8 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
         } else {
           v_ok = valid;
         }
-        const bool st_ok = live && (p.grouped ? true : valid);   // the row exists in out0
         const int col0 = n0 + half * kCols;
         const uint16_t* gu = static_cast<const uint16_t*>(p.aux0) + static_cast<long long>(prow) * 2 * p.N + col0;
-        uint8_t* rowq = static_cast<uint8_t*>(p.out0) + static_cast<long long>(prow) * 2 * p.N;
         const long long ldt = p.ld;
         const int cgr = 2 * p.N / 128, cgt = static_cast<int>(ldt / 128);
         const int rblk = (it.p0 + q * 32) / 32;                // 32-row block of this warp's rows
@@ -530,19 +532,28 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
         const float lim = p.swiglu_limit;
         float dpart = 0.f;
         uint32_t rsc_g = 0, rsc_u = 0;
+        const int prow0 = it.p0 + q * 32;                      // the warp's first row
+        // saved gate|up of the next 16 columns, loaded one slice ahead
+        uint4 pg[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)}, pu[2] = {pg[0], pg[1]};
+        auto fetch_gu = [&](int col) {
+          if (v_ok) {
+            const uint4* sg4 = reinterpret_cast<const uint4*>(gu + col);
+            const uint4* su4 = reinterpret_cast<const uint4*>(gu + p.N + col);
+            pg[0] = __ldg(sg4); pg[1] = __ldg(sg4 + 1);
+            pu[0] = __ldg(su4); pu[1] = __ldg(su4 + 1);
+          }
+        };
+        fetch_gu(0);
 #pragma unroll 1
         for (int c = 0; c < kCols / 32; ++c) {
+          if (lane == 0) bulk_wait_read<0>();   // the last chunk's code boxes have left the blocks
+          __syncwarp();
 #pragma unroll 1
           for (int hf = 0; hf < 2; ++hf) {   // 16 columns at a time keep the registers low
+            const uint4 ng[2] = {pg[0], pg[1]}, nu[2] = {pu[0], pu[1]};
+            if (c * 32 + hf * 16 + 16 < kCols) fetch_gu(c * 32 + hf * 16 + 16);
             float z[16];
             tmem_ld16(tb + half * kCols + c * 32 + hf * 16, z);
-            uint4 ng[2], nu[2];
-            if (v_ok) {
-              const uint4* sg4 = reinterpret_cast<const uint4*>(gu + c * 32 + hf * 16);
-              const uint4* su4 = reinterpret_cast<const uint4*>(gu + p.N + c * 32 + hf * 16);
-              ng[0] = __ldg(sg4); ng[1] = __ldg(sg4 + 1);
-              nu[0] = __ldg(su4); nu[1] = __ldg(su4 + 1);
-            }
 #pragma unroll
             for (int i = 0; i < 16; i += 2) {
               float a[2] = {0.f, 0.f}, b[2] = {0.f, 0.f}, hh[2] = {0.f, 0.f};
@@ -574,22 +585,44 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
             }
           }
           __syncwarp();
-          // transposed blocks: this lane's column of each, over the warp's 32 rows
-          const int tg = col0 + c * 32 + lane;
-          uint8_t* dguT = static_cast<uint8_t*>(p.out1);
+          // each staged block -> its codes: lane j takes column j (transposed
+          // output) and row j (row output); the codes then replace the block in
+          // shared memory (transposed box at +0, row box at +1 KB) for the TMA stores
+          const int tg0 = col0 + c * 32;
+          const int tg = tg0 + lane;
           uint8_t* dguT_sc = static_cast<uint8_t*>(p.out2);
-          const uint32_t cg_s = mx_col_from_stage(blk_g, lane, dguT + tg * ldt + tcol);
-          const uint32_t cu_s = mx_col_from_stage(blk_u, lane, dguT + (p.N + tg) * ldt + tcol);
-          const uint32_t ch_s = mx_col_from_stage(blk_h, lane, static_cast<uint8_t*>(p.out3) + tg * ldt + tcol);
-          if (live) {
-            dguT_sc[mx_tiled_scale_offset(tg, rblk, cgt)] = static_cast<uint8_t>(cg_s);
-            dguT_sc[mx_tiled_scale_offset(p.N + tg, rblk, cgt)] = static_cast<uint8_t>(cu_s);
-            p.sf_out2[mx_tiled_scale_offset(tg, rblk, cgt)] = static_cast<uint8_t>(ch_s);
+#pragma unroll 1
+          for (int o = 0; o < 3; ++o) {
+            uint32_t* blk = o == 0 ? blk_g : (o == 1 ? blk_u : blk_h);
+            uint32_t cq[8], rq[8];
+            const uint32_t cs = mx_col_from_stage(blk, lane, reinterpret_cast<uint8_t*>(cq));
+            uint32_t rs = 0;
+            if (o < 2) rs = mx_row_from_stage(blk, lane, reinterpret_cast<uint8_t*>(rq));
+            __syncwarp();
+            uint4* box = reinterpret_cast<uint4*>(blk);
+            box[lane * 2] = make_uint4(cq[0], cq[1], cq[2], cq[3]);
+            box[lane * 2 + 1] = make_uint4(cq[4], cq[5], cq[6], cq[7]);
+            if (o < 2) {
+              box[64 + lane * 2] = make_uint4(rq[0], rq[1], rq[2], rq[3]);
+              box[64 + lane * 2 + 1] = make_uint4(rq[4], rq[5], rq[6], rq[7]);
+            }
+            if (live) {
+              const int trow = (o == 1 ? p.N : 0) + tg;
+              (o == 2 ? p.sf_out2 : dguT_sc)[mx_tiled_scale_offset(trow, rblk, cgt)] = static_cast<uint8_t>(cs);
+            }
+            if (o == 0) rsc_g |= rs << (8 * c);
+            if (o == 1) rsc_u |= rs << (8 * c);
           }
-          // row blocks of dG and dU
-          rsc_g |= mx_row_from_stage(blk_g, lane, st_ok ? rowq + col0 + c * 32 : nullptr) << (8 * c);
-          rsc_u |= mx_row_from_stage(blk_u, lane, st_ok ? rowq + p.N + col0 + c * 32 : nullptr) << (8 * c);
-          __syncwarp();   // the blocks are read before the next chunk overwrites them
+          fence_proxy_async_smem();   // generic-proxy writes, then the TMA stores read them
+          __syncwarp();
+          if (lane == 0 && live) {
+            tma_store_2d(&maps.o1, blk_g, static_cast<int>(tcol), tg0);          // dG transposed
+            tma_store_2d(&maps.o1, blk_u, static_cast<int>(tcol), p.N + tg0);    // dU transposed
+            tma_store_2d(&maps.o2, blk_h, static_cast<int>(tcol), tg0);          // w h transposed
+            tma_store_2d(&maps.o0, blk_g + 256, tg0, prow0);                    // dG rows (clipped past the end)
+            tma_store_2d(&maps.o0, blk_u + 256, p.N + tg0, prow0);              // dU rows
+            bulk_commit();
+          }
         }
         release_acc();
         // this thread's two row blocks of dG and of dU are adjacent bytes of
@@ -616,6 +649,9 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
           warp_store_row64(wv, dst ? dst + c * 32 : nullptr, wstage, lane);
         }
       }
+    }
+    if constexpr (EPI == EPI_DOWN_BWD_MX) {
+      if (lane == 0) bulk_wait<0>();   // this warp's TMA stores are complete before the CTA ends
     }
   }
 

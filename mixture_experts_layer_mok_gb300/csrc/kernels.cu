@@ -379,10 +379,11 @@ cudaError_t launch_mx_dispatch(const uint16_t* x, int T, int H, int topk, const 
 // rows from P on read as zero and a failed schedule skips the work.  Output
 // codes [batch][C][R]; scales row-major [batch*C][R/32], or (tiled) in the
 // tensor-core scale layout with rows batch*C and K = R.  One block per
-// 128-row x 64-column tile: coalesced row loads into shared memory, one
-// thread per (column, 32-row block) quantising into a shared-memory output
-// tile, then whole 128-byte code rows and one 4-byte scale word per column
-// out to global memory.  With rcodes, the same read also yields the codes
+// 128-row x 64-column tile: coalesced row loads into shared memory (cp.async,
+// the next tile's while this one is quantised), one thread per (column,
+// 32-row block) quantising into a shared-memory output tile, then whole
+// 128-byte code rows and one 4-byte scale word per column out to global
+// memory.  With rcodes, the same read also yields the codes
 // along the rows (blocks of 32 columns, scales rscales, row-major or tiled):
 // both orientations of one tensor from a single pass over it.
 // ===========================================================================
@@ -402,44 +403,57 @@ __global__ void __launch_bounds__(256) mx_quantize_t_kernel(const uint16_t* __re
     vrows = min(vrows, header[1]);
   }
   constexpr int kOutStride = 144;   // bytes per output row in shared memory (128 + 16: no bank conflicts)
-  // input tile: row r's 16-byte piece p sits at piece p ^ (r & 7), so that both
-  // column reads (one element of 32 rows) and row reads (half a row per
+  // two input tiles (the next one loads by cp.async while this one is
+  // quantised); row r's 16-byte piece p sits at piece p ^ (r & 7), so that
+  // both column reads (one element of 32 rows) and row reads (half a row per
   // thread) spread over the banks
-  __shared__ __align__(16) uint16_t tile[128][64];
+  __shared__ __align__(16) uint16_t tile[2][128][64];
   __shared__ __align__(16) uint8_t out[64 * kOutStride];
   __shared__ uint32_t osc[64];
   const int rtiles = (R + 127) / 128, ctiles = C / 64;
   const long long ntiles = static_cast<long long>(batch) * rtiles * ctiles;
   const int c = threadIdx.x & 63, rb = threadIdx.x >> 6;
-  for (long long t = blockIdx.x; t < ntiles; t += gridDim.x) {
+  auto coords = [&](long long t, int& b, int& r0, int& c0) {
     const int ct = static_cast<int>(t % ctiles);
     const long long rest = t / ctiles;
-    const int rt = static_cast<int>(rest % rtiles);
-    const int b = static_cast<int>(rest / rtiles);
-    const int r0 = rt * 128, c0 = ct * 64;
-    __syncthreads();   // the previous tile's buffers are drained
-    for (int i = threadIdx.x; i < 128 * 8; i += 256) {   // 8 pieces of 16 bytes per row
+    r0 = static_cast<int>(rest % rtiles) * 128;
+    b = static_cast<int>(rest / rtiles);
+    c0 = ct * 64;
+  };
+  auto issue = [&](long long t, int buf) {   // cp.async of tile t's rows (zeros past the valid rows)
+    int b, r0, c0;
+    coords(t, b, r0, c0);
+    for (int i = threadIdx.x; i < 128 * 8; i += 256) {
       const int row = i >> 3, piece = i & 7;
       const int r = r0 + row;
-      uint4 v = make_uint4(0, 0, 0, 0);
+      long long srow = -1;
       if (r < R && r < vrows) {
-        long long srow = r;
+        srow = r;
         if (row_src) {
           const int f = __ldg(row_src + r);
           srow = f >= 0 ? f / topk : -1;
         }
-        if (srow >= 0)
-          v = __ldg(reinterpret_cast<const uint4*>(src + (static_cast<long long>(b) * R + srow) * ld + c0) + piece);
       }
-      reinterpret_cast<uint4*>(&tile[row][0])[piece ^ (row & 7)] = v;
+      const uint16_t* g = src + (static_cast<long long>(b) * R + (srow >= 0 ? srow : 0)) * ld + c0 + piece * 8;
+      cp_async16(&tile[buf][row][(piece ^ (row & 7)) * 8], g, srow >= 0 ? 16u : 0u);
     }
+  };
+  int buf = 0;
+  if (blockIdx.x < ntiles) issue(blockIdx.x, 0);
+  cp_async_commit();
+  for (long long t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    int b, r0, c0;
+    coords(t, b, r0, c0);
+    if (t + gridDim.x < ntiles) issue(t + gridDim.x, buf ^ 1);
+    cp_async_commit();
+    cp_async_wait<1>();   // this tile's copies have landed (the next tile's may still fly)
     __syncthreads();
     {   // column c0 + c, rows r0 + 32 rb ..: codes into the output tile
       float v[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const int row = rb * 32 + i;
-        v[i] = __uint_as_float(static_cast<uint32_t>(tile[row][(((c >> 3) ^ (row & 7)) << 3) | (c & 7)]) << 16);
+        v[i] = __uint_as_float(static_cast<uint32_t>(tile[buf][row][(((c >> 3) ^ (row & 7)) << 3) | (c & 7)]) << 16);
       }
       uint8_t q[32];
       const uint32_t s = mx_quantize32(v, q);
@@ -455,7 +469,7 @@ __global__ void __launch_bounds__(256) mx_quantize_t_kernel(const uint16_t* __re
         float v[32];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const uint4 w = reinterpret_cast<const uint4*>(&tile[row][0])[(hb * 4 + j) ^ (row & 7)];
+          const uint4 w = reinterpret_cast<const uint4*>(&tile[buf][row][0])[(hb * 4 + j) ^ (row & 7)];
           const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
@@ -475,7 +489,7 @@ __global__ void __launch_bounds__(256) mx_quantize_t_kernel(const uint16_t* __re
           rscales[orr * (C / 32) + cb] = static_cast<uint8_t>(s);
       }
     }
-    __syncthreads();
+    __syncthreads();   // the output tile is complete; the input buffer may be refilled
     const long long orow0 = static_cast<long long>(b) * C + c0;
     for (int i = threadIdx.x; i < 64 * 8; i += 256) {   // 8 pieces of 16 code bytes per output row
       const int row = i >> 3, piece = i & 7;
@@ -495,7 +509,9 @@ __global__ void __launch_bounds__(256) mx_quantize_t_kernel(const uint16_t* __re
           scales[orow * (R / 32) + r0 / 32 + k] = static_cast<uint8_t>(word >> (8 * k));
       }
     }
+    buf ^= 1;
   }
+  cp_async_wait<0>();   // no copy is left in flight when the block exits
 }
 
 cudaError_t launch_mx_quantize_t(const uint16_t* src, long long ld, int batch, int R, int C, int valid_rows,
