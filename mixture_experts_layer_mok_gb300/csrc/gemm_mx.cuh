@@ -554,29 +554,29 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
             if (c * 32 + hf * 16 + 16 < kCols) fetch_gu(c * 32 + hf * 16 + 16);
             float z[16];
             tmem_ld16(tb + half * kCols + c * 32 + hf * 16, z);
+            // no branch on the row: a padding row (or a dense row past the end)
+            // has zero gate|up and a zero accumulator row, so every output is 0
 #pragma unroll
             for (int i = 0; i < 16; i += 2) {
-              float a[2] = {0.f, 0.f}, b[2] = {0.f, 0.f}, hh[2] = {0.f, 0.f};
-              if (v_ok) {
+              float a[2], b[2], hh[2];
 #pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                  float g = bf16_at(ng, i + t), u = bf16_at(nu, i + t);
-                  float mg = 1.f, mu = 1.f;   // the clamp's derivative (SwiGLU limit)
-                  if (lim > 0.f) {
-                    mg = (g <= lim) ? 1.f : 0.f;
-                    mu = (fabsf(u) <= lim) ? 1.f : 0.f;
-                    g = fminf(g, lim);
-                    u = fminf(fmaxf(u, -lim), lim);
-                  }
-                  const float sg = __fdividef(1.f, 1.f + __expf(-g));
-                  const float sl = g * sg;
-                  const float h = sl * u;
-                  dpart = fmaf(z[i + t], h, dpart);
-                  const float dh = wt * z[i + t];
-                  a[t] = dh * u * sg * (1.f + g * (1.f - sg)) * mg;
-                  b[t] = dh * sl * mu;
-                  hh[t] = wt * h;
+              for (int t = 0; t < 2; ++t) {
+                float g = bf16_at(ng, i + t), u = bf16_at(nu, i + t);
+                float mg = 1.f, mu = 1.f;   // the clamp's derivative (SwiGLU limit)
+                if (lim > 0.f) {
+                  mg = (g <= lim) ? 1.f : 0.f;
+                  mu = (fabsf(u) <= lim) ? 1.f : 0.f;
+                  g = fminf(g, lim);
+                  u = fminf(fmaxf(u, -lim), lim);
                 }
+                const float sg = __fdividef(1.f, 1.f + __expf(-g));
+                const float sl = g * sg;
+                const float h = sl * u;
+                dpart = fmaf(z[i + t], h, dpart);
+                const float dh = wt * z[i + t];
+                a[t] = dh * u * sg * (1.f + g * (1.f - sg)) * mg;
+                b[t] = dh * sl * mu;
+                hh[t] = wt * h;
               }
               const int wi = hf * 8 + (i >> 1);
               stage_put(blk_g, lane, wi, pack_bf16(a[0], a[1]));

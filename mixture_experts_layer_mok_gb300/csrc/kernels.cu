@@ -423,19 +423,25 @@ __global__ void __launch_bounds__(256) mx_quantize_t_kernel(const uint16_t* __re
   auto issue = [&](long long t, int buf) {   // cp.async of tile t's rows (zeros past the valid rows)
     int b, r0, c0;
     coords(t, b, r0, c0);
-    for (int i = threadIdx.x; i < 128 * 8; i += 256) {
-      const int row = i >> 3, piece = i & 7;
-      const int r = r0 + row;
-      long long srow = -1;
-      if (r < R && r < vrows) {
-        srow = r;
-        if (row_src) {
-          const int f = __ldg(row_src + r);
-          srow = f >= 0 ? f / topk : -1;
-        }
+    // this thread copies piece (tid & 7) of rows (tid >> 3) + 32 j, j < 4: their
+    // source rows first (independent index loads), then the four copies
+    const int piece = threadIdx.x & 7;
+    long long srow[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int r = r0 + (threadIdx.x >> 3) + 32 * j;
+      srow[j] = (r < R && r < vrows) ? r : -1;
+      if (row_src && srow[j] >= 0) {
+        const int f = __ldg(row_src + r);
+        srow[j] = f >= 0 ? f / topk : -1;
       }
-      const uint16_t* g = src + (static_cast<long long>(b) * R + (srow >= 0 ? srow : 0)) * ld + c0 + piece * 8;
-      cp_async16(&tile[buf][row][(piece ^ (row & 7)) * 8], g, srow >= 0 ? 16u : 0u);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int row = (threadIdx.x >> 3) + 32 * j;
+      const uint16_t* g =
+          src + (static_cast<long long>(b) * R + (srow[j] >= 0 ? srow[j] : 0)) * ld + c0 + piece * 8;
+      cp_async16(&tile[buf][row][(piece ^ (row & 7)) * 8], g, srow[j] >= 0 ? 16u : 0u);
     }
   };
   int buf = 0;

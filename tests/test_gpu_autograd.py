@@ -1,6 +1,6 @@
 """The torch.autograd face of the layer (MoKFunction / MoKLayer): gradients
 that autograd delivers for a loss <y, dy> equal the oracle's gradients of the
-same layer, in both modes."""
+same layer, in every mode."""
 import pytest
 import torch
 
@@ -10,7 +10,7 @@ from tests.gpu_util import BF16_TOL, mok, oracle_fwd_bwd, rel_l2
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("mode", ["bf16", "mxfp8"])
+@pytest.mark.parametrize("mode", ["bf16", "mxfp8", "mxfp8_full"])
 @pytest.mark.parametrize("shape", [(200, 256, 384, 5, 3, 256), (333, 128, 128, 16, 4, 0)])
 def test_autograd_gradients_match_oracle(mode, shape):
     mok()   # builds / loads the library

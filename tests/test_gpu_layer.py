@@ -149,6 +149,14 @@ def test_host_argument_errors():
     with pytest.raises(m.MokError) as ei:
         m.forward(g.x, g.router_w, sched, w, mode="mxfp8")     # no prequantised weights
     assert ei.value.code == 1
+    # the MXFP8 backward needs the weights' transposed copies as well
+    wq = m.quantize_weights(w)
+    y, ctx = m.forward(g.x, g.router_w, sched, wq, mode="mxfp8_full")
+    with pytest.raises(m.MokError) as ei:
+        m.backward(g.dy, g.x, g.router_w, sched, ctx, wq)
+    assert ei.value.code == 1
+    with pytest.raises(ValueError):
+        m.forward(g.x, g.router_w, sched, wq, mode="fp4")
 
 
 @pytest.mark.parametrize("mode", ["bf16", "mxfp8", "mxfp8_full"])
