@@ -309,17 +309,17 @@ def main():
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
-    def run_step(x, rw, top, dy, events=None, prep_events=None):
+    def run_step(x, rw, top, dy, events=None, prep_events=None, y_out=None, g_out=None):
         if prep_events:
             prep_events[0].record()
         wq = mok.quantize_weights(w, backward=(mode == "mxfp8_full")) if mode != "bf16" else w
         sched = mok.schedule(top, E, c["capacity"])
         if prep_events:
             prep_events[1].record()
-        _, ctx = mok.forward(x, rw, sched, wq, mode=mode, minibatch=c["minibatch"], out=y, ctx_buf=ctx_buf,
-                             events=events)
-        mok.backward(dy, x, rw, sched, ctx, wq, minibatch=c["minibatch"], grads=grads, ws_buf=ws_buf,
-                     events=events)
+        _, ctx = mok.forward(x, rw, sched, wq, mode=mode, minibatch=c["minibatch"],
+                             out=y if y_out is None else y_out, ctx_buf=ctx_buf, events=events)
+        mok.backward(dy, x, rw, sched, ctx, wq, minibatch=c["minibatch"], grads=grads if g_out is None else g_out,
+                     ws_buf=ws_buf, events=events)
         return ctx
 
     for _ in range(args.warmup):
@@ -396,7 +396,13 @@ def main():
             extra = f"  {sf[n] / (st_ms[n] / 1e3) / 1e12:8.1f} TFLOP/s" if n in gemm_stages else ""
             print(f"  {n:26s} {st_ms[n]:8.4f} ms{extra}", file=sys.stderr)
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers.  Like a training
+    # loop with a prefetching loader: each step's inputs come from pinned host
+    # memory and its results go back to it, on a copy stream that overlaps the
+    # neighbouring steps' compute (inputs and outputs double-buffered on the
+    # device).  The timed region runs from the first input copy to the last
+    # result copy.  No L2 flush: every step streams its 0.8 GB or more of
+    # weights through the 129 MB L2.
     e2e = None
     if not args.no_e2e:
         hx = inp.x.cpu().pin_memory()
@@ -406,36 +412,59 @@ def main():
         oy = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
         odx = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
         odw = torch.empty((T, k), dtype=torch.float32).pin_memory()
-        dx_ = torch.empty_like(g.x)
-        drw = torch.empty_like(g.router_w)
-        dtop = torch.empty_like(g.top_experts)
-        ddy = torch.empty_like(g.dy)
-        h2d = sum(t.numel() * t.element_size() for t in (hx, hrw, htop, hdy))
+        hosts_in = (hx, hrw, htop, hdy)
+        ins = [tuple(torch.empty_like(t) for t in (g.x, g.router_w, g.top_experts, g.dy)) for _ in range(2)]
+        outs = [(torch.empty_like(y), {n: torch.empty_like(v) for n, v in grads.items()}) for _ in range(2)]
+        h2d = sum(t.numel() * t.element_size() for t in hosts_in)
         d2h = sum(t.numel() * t.element_size() for t in (oy, odx, odw))
+        copy = torch.cuda.Stream()
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_done = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
+        e_start = torch.cuda.Event(enable_timing=True)
+        e_end = torch.cuda.Event(enable_timing=True)
+
+        def put(slot):                      # host -> device inputs of one step, on the copy stream
+            with torch.cuda.stream(copy):
+                for d, hsrc in zip(ins[slot], hosts_in):
+                    d.copy_(hsrc, non_blocking=True)
+                ev_in[slot].record(copy)
+
+        def pipeline(n, timed):
+            torch.cuda.synchronize()
+            if timed:
+                e_start.record(copy)
+            for slot in range(min(n, 2)):
+                put(slot)
+            for i in range(n):
+                slot = i % 2
+                stream.wait_event(ev_in[slot])
+                if i >= 2:
+                    stream.wait_event(ev_out[slot])   # step i-2's results have left this slot
+                run_step(*ins[slot], y_out=outs[slot][0], g_out=outs[slot][1])
+                ev_done[slot].record(stream)
+                with torch.cuda.stream(copy):
+                    copy.wait_event(ev_done[slot])
+                    oy.copy_(outs[slot][0], non_blocking=True)
+                    odx.copy_(outs[slot][1]["dx"], non_blocking=True)
+                    odw.copy_(outs[slot][1]["d_router_w"], non_blocking=True)
+                    ev_out[slot].record(copy)
+                if i + 2 < n:
+                    put(slot)                       # step i+2's inputs (step i is done with the slot)
+            if timed:
+                e_end.record(copy)
+            torch.cuda.synchronize()
+
         Ke = max(3, min(K, 50))
-        es = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
-        ee = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
-        for i in range(Ke + 2):
-            flush.zero_()
-            if i >= 2:
-                es[i - 2].record(stream)
-            dx_.copy_(hx, non_blocking=True)
-            drw.copy_(hrw, non_blocking=True)
-            dtop.copy_(htop, non_blocking=True)
-            ddy.copy_(hdy, non_blocking=True)
-            run_step(dx_, drw, dtop, ddy)
-            oy.copy_(y, non_blocking=True)
-            odx.copy_(grads["dx"], non_blocking=True)
-            odw.copy_(grads["d_router_w"], non_blocking=True)
-            if i >= 2:
-                ee[i - 2].record(stream)
-        torch.cuda.synchronize()
-        e_ms = sum(es[i].elapsed_time(ee[i]) for i in range(Ke))
+        pipeline(3, False)
+        pipeline(Ke, True)
+        e_ms = e_start.elapsed_time(e_end)
         e_ms = max_over_ranks(e_ms, world, dev)
         e2e = {"value": round(job_tokens_per_s(T, world, Ke, e_ms), 1), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke,
                "what": "pinned host x, router weights, top-k ids, dy -> device; schedule + fwd + bwd through "
-                       "the binding; y, dx, d_router_w -> host"}
+                       "the binding; y, dx, d_router_w -> host; copies on a second stream overlap the "
+                       "neighbouring steps' compute (double-buffered), all inside the timed region"}
 
     if rank != 0:
         if world > 1:
