@@ -125,9 +125,13 @@ def load_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
-def kernel_source_hash():
+def kernel_source_hash(kernel="gemm_kernel"):
+    """Hash of the sources a GEMM kernel is built from: the bf16 engine
+    (gemm_kernel) from gemm.cuh and ptx.cuh, the block-scaled one
+    (gemm_mx_kernel) from those and gemm_mx.cuh."""
+    names = ["gemm.cuh", "ptx.cuh"] + (["gemm_mx.cuh"] if kernel.startswith("gemm_mx_kernel") else [])
     h = hashlib.sha256()
-    for name in ("gemm.cuh", "gemm_mx.cuh", "ptx.cuh"):
+    for name in names:
         with open(os.path.join(ROOT, "mixture_experts_layer_mok_gb300", "csrc", name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -141,7 +145,7 @@ def recorded_traffic(workload, stage):
         with open(path) as fh:
             rec = json.load(fh)
         ent = rec[workload][stage]
-        if ent["kernel_source"] == kernel_source_hash():
+        if ent["kernel_source"] == kernel_source_hash(ent["kernel"]):
             return ent["dram_bytes_per_launch"]
     except Exception:
         pass
