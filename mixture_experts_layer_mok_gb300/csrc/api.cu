@@ -7,6 +7,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <cmath>
 #include <mutex>
 
@@ -423,9 +425,42 @@ GemmParams base_params(const mok_schedule_t* s, int* status, int debug) {
   return p;
 }
 
+// NVTX ranges (host timeline; they cost nothing unless a tool is attached):
+// one per C-ABI call and one per stage inside it, so that a profiler can pick
+// a call's or a stage's kernels (e.g. ncu --nvtx --nvtx-include "mok_backward/").
+const char* const kStageNames[MOK_NUM_STAGES] = {
+    "fwd_prep", "fwd_shared_gateup", "fwd_shared_down", "fwd_gateup", "fwd_down", "fwd_combine",
+    "bwd_down", "bwd_wgrad_down", "bwd_wgrad_gateup", "bwd_dgrad_gateup", "bwd_shared_down",
+    "bwd_shared_wgrad_down", "bwd_shared_wgrad_gateup", "bwd_shared_dgrad", "bwd_reduce",
+    "fwd_dispatch", "bwd_dispatch"};
+thread_local int g_nvtx_depth = 0;
+
+// The call's range; on the way out it also closes stage ranges an early
+// (error) return left open.
+struct NvtxCall {
+  int base;
+  explicit NvtxCall(const char* name) : base(g_nvtx_depth) {
+    nvtxRangePushA(name);
+    ++g_nvtx_depth;
+  }
+  ~NvtxCall() {
+    while (g_nvtx_depth > base) {
+      nvtxRangePop();
+      --g_nvtx_depth;
+    }
+  }
+};
+
 // Records the caller's timing event for the start (end = 0) or end of a stage
-// (a NULL entry: nothing).
+// (a NULL entry: nothing), and opens or closes the stage's NVTX range.
 cudaError_t mark(const mok_config_t* cfg, int stage, int end, cudaStream_t st) {
+  if (!end) {
+    nvtxRangePushA(kStageNames[stage]);
+    ++g_nvtx_depth;
+  } else if (g_nvtx_depth > 0) {
+    nvtxRangePop();
+    --g_nvtx_depth;
+  }
   if (cfg->events && cfg->num_events >= 2 * MOK_NUM_STAGES && cfg->events[2 * stage + end])
     return cudaEventRecord(static_cast<cudaEvent_t>(cfg->events[2 * stage + end]), st);
   return cudaSuccess;
@@ -973,6 +1008,7 @@ size_t mok_schedule_bytes(int T, int k, int E) {
 
 mok_status_t mok_schedule(const int64_t* top_experts, int T, int k, int E, float capacity_multiplier,
                           void* buf, size_t bytes, mok_schedule_t* out, void* stream) {
+  NvtxCall nvtx("mok_schedule");
   if (!top_experts || !buf || !out) return fail(MOK_ERR_INVALID_ARG, "NULL argument");
   if (T < 1 || k < 1 || k > 64 || E < 1 || E > 1024)
     return fail(MOK_ERR_INVALID_ARG, "need T >= 1, 1 <= k <= 64, 1 <= E <= 1024");
@@ -1016,6 +1052,7 @@ mok_status_t mok_schedule_status(const mok_schedule_t* s, int* status, int* num_
 
 mok_status_t mok_mxfp8_quantize(const uint16_t* x, int64_t rows, int K, uint8_t* codes,
                                 uint8_t* scales, void* stream) {
+  NvtxCall nvtx("mok_mxfp8_quantize");
   if (rows < 0 || K <= 0 || K % 32) return fail(MOK_ERR_INVALID_ARG, "need rows >= 0 and K % 32 == 0");
   if (rows == 0) return MOK_OK;
   if (!x || !codes || !scales) return fail(MOK_ERR_INVALID_ARG, "NULL argument");
@@ -1029,6 +1066,7 @@ mok_status_t mok_mxfp8_quantize(const uint16_t* x, int64_t rows, int K, uint8_t*
 
 mok_status_t mok_mxfp8_quantize_t(const uint16_t* x, int64_t batch, int rows, int cols, uint8_t* codes,
                                   uint8_t* scales, void* stream) {
+  NvtxCall nvtx("mok_mxfp8_quantize_t");
   if (batch < 0 || rows < 0 || cols < 0 || rows % 32 || cols % 64)
     return fail(MOK_ERR_INVALID_ARG, "need batch, rows, cols >= 0, rows %% 32 == 0 and cols %% 64 == 0");
   if (batch == 0 || rows == 0 || cols == 0) return MOK_OK;
@@ -1045,6 +1083,7 @@ mok_status_t mok_mxfp8_quantize_t(const uint16_t* x, int64_t batch, int rows, in
 
 mok_status_t mok_mxfp8_quantize_dual(const uint16_t* x, int64_t batch, int rows, int cols, uint8_t* codes,
                                      uint8_t* scales, uint8_t* codes_t, uint8_t* scales_t, void* stream) {
+  NvtxCall nvtx("mok_mxfp8_quantize_dual");
   if (batch < 0 || rows < 0 || cols < 0 || rows % 32 || cols % 64)
     return fail(MOK_ERR_INVALID_ARG, "need batch, rows, cols >= 0, rows %% 32 == 0 and cols %% 64 == 0");
   if (batch == 0 || rows == 0 || cols == 0) return MOK_OK;
@@ -1076,6 +1115,7 @@ mok_status_t mok_ctx_status(const mok_ctx_t* ctx, int* status) {
 mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x, const float* router_w,
                          const mok_schedule_t* s, const mok_weights_t* w, uint16_t* y, void* ctx_buf,
                          size_t ctx_bytes, mok_ctx_t* ctx, void* stream) {
+  NvtxCall nvtx("mok_forward");
   if (!cfg || !x || !router_w || !s || !w || !y || !ctx_buf || !ctx)
     return fail(MOK_ERR_INVALID_ARG, "NULL argument");
   mok_status_t st = check_config(cfg);
@@ -1144,6 +1184,7 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
                           const float* router_w, const mok_schedule_t* s, const mok_ctx_t* ctx,
                           const mok_weights_t* w, uint16_t* dx, float* d_router_w,
                           const mok_weight_grads_t* g, void* ws, size_t ws_bytes, void* stream) {
+  NvtxCall nvtx("mok_backward");
   if (!cfg || !dy || !x || !router_w || !s || !ctx || !w || !dx || !d_router_w || !g || !ws)
     return fail(MOK_ERR_INVALID_ARG, "NULL argument");
   mok_status_t st = check_config(cfg);
@@ -1437,6 +1478,7 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
 mok_status_t mok_schedule_noalloc(const int64_t* top_experts, int T, int k, int E,
                                   float capacity_multiplier, void* buf, size_t bytes,
                                   mok_schedule_t* out, void* stream) {
+  NvtxCall nvtx("mok_schedule_noalloc");
   if (!top_experts || !buf || !out) return fail(MOK_ERR_INVALID_ARG, "NULL argument");
   if (T < 1 || k < 1 || k > 64 || E < 1 || E > 1024)
     return fail(MOK_ERR_INVALID_ARG, "need T >= 1, 1 <= k <= 64, 1 <= E <= 1024");
