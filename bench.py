@@ -418,7 +418,10 @@ def main():
         odw = torch.empty((T, k), dtype=torch.float32).pin_memory()
         hosts_in = (hx, hrw, htop, hdy)
         ins = [tuple(torch.empty_like(t) for t in (g.x, g.router_w, g.top_experts, g.dy)) for _ in range(2)]
-        outs = [(torch.empty_like(y), {n: torch.empty_like(v) for n, v in grads.items()}) for _ in range(2)]
+        # y, dx and d_router_w go back to the host: two copies each; the weight
+        # gradients stay on the device and are shared by the two slots
+        outs = [(torch.empty_like(y), {n: (torch.empty_like(v) if n in ("dx", "d_router_w") else v)
+                                       for n, v in grads.items()}) for _ in range(2)]
         h2d = sum(t.numel() * t.element_size() for t in hosts_in)
         d2h = sum(t.numel() * t.element_size() for t in (oy, odx, odw))
         copy = torch.cuda.Stream()

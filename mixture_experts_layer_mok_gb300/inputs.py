@@ -35,6 +35,8 @@ WORKLOADS = {
                           minibatch=4096, capacity=0.5, mode="bf16"),
     "large_T65536": dict(T=65536, H=7168, I=2048, E=256, k=8, I_s=2048, skew=None,
                          minibatch=4096, capacity=0.5, mode="mxfp8"),
+    "mxfp8full_T65536": dict(T=65536, H=7168, I=2048, E=256, k=8, I_s=2048, skew=None,
+                             minibatch=4096, capacity=0.5, mode="mxfp8_full"),
 }
 
 
