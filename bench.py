@@ -238,6 +238,13 @@ class OracleSample:
                 return el, reps
 
 
+# Tokens per oracle sample.  In the MXFP8 modes each call quantises the weights
+# of every expert the sample touches (several 2 M-element matrices each), so a
+# handful of tokens already costs seconds on the host.
+CPU_SAMPLE_TOKENS = {"bf16": 64, "mxfp8": 2, "mxfp8_full": 1}
+REF_STEP_TOKENS = {"bf16": 16, "mxfp8": 2, "mxfp8_full": 1}
+
+
 def cpu_cores():
     for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
         v = os.environ.get(var)
@@ -483,7 +490,7 @@ def main():
         cpu = {"value": None, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
                "sample": "skipped: the float64 oracle would widen more than 3e8 weight elements per expert set"}
     elif world == 1 and not args.no_cpu_baseline:
-        tokens = 64
+        tokens = CPU_SAMPLE_TOKENS[mode]
         sample = OracleSample(inp, mode, tokens)
         sample.run()                                    # first touch of the widened weights
         el, reps = sample.run(min_s=10.0)
@@ -543,7 +550,7 @@ def run_reference(args, c, config, rank, world):
     from mixture_experts_layer_mok_gb300 import inputs as gen
 
     inp = gen.make_workload(args.workload, seed=0)
-    tokens = 16
+    tokens = REF_STEP_TOKENS[c["mode"]]
     sample = OracleSample(inp, c["mode"], tokens)
     for _ in range(args.warmup):
         sample.run()
