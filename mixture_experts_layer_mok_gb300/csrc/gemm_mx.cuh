@@ -1,6 +1,6 @@
 // Persistent grouped GEMM on the block-scaled tensor-core path
 // (tcgen05.mma kind::mxf8f6f4, E4M3 operands with E8M0 scales per 32 K-elements)
-// for the MXFP8 forward.
+// for the MXFP8 forward and the MXFP8 backward.
 //
 // One CTA per SM, 320 threads:
 //   warp 0      TMA producer: operand tiles (128-byte rows of E4M3 codes) and
@@ -9,15 +9,20 @@
 //               scale atoms into TMEM (tcgen05.cp) and issues four K=32 MMAs;
 //   warps 2..9  epilogue, two warps per TMEM lane quarter, each half the
 //               columns.
-// The accumulator (BN fp32 columns) is single-buffered: the scale ring takes
-// the rest of TMEM.  The epilogue reads its whole share of the accumulator
-// into registers first and releases TMEM at once, so the next tile's MMAs
-// overlap the epilogue's arithmetic and stores.
+// A 256-column accumulator is single-buffered (the scale ring takes the rest
+// of TMEM); a 128-column one is double-buffered.  The epilogue reads its share
+// of the accumulator into registers and releases TMEM at once, so the next
+// tile's MMAs overlap the epilogue's arithmetic and stores; the SwiGLU
+// backward instead reads its 128-column buffer as it goes.
+//
+// Row GEMMs take their rows from the schedule's tile list (or dense rows);
+// weight-gradient GEMMs contract over an expert's row range, with both
+// operands stored transposed (the layer's rows as K).
 //
 // Follows "Mixture-of-Kittens: a deterministic MoE megakernel for NVL72 racks"
-// (MXFP8 forward; experts as fused SwiGLU grouped GEMMs) with MXFP8 as the OCP
-// Microscaling v1.0 format: E4M3 elements, one E8M0 power-of-two scale per
-// block of 32 along K.
+// (MXFP8 forward and backward; experts as fused SwiGLU grouped GEMMs) with
+// MXFP8 as the OCP Microscaling v1.0 format: E4M3 elements, one E8M0
+// power-of-two scale per block of 32 along K.
 #pragma once
 
 #include "gemm.cuh"
