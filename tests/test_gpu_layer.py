@@ -88,11 +88,12 @@ def test_repeated_runs_bitwise_identical():
         assert torch.equal(a[1][key], b[1][key]), key
 
 
-def test_capacity_and_minibatch_change_no_bit():
+@pytest.mark.parametrize("mode", ["bf16", "mxfp8_full"])
+def test_capacity_and_minibatch_change_no_bit(mode):
     inp = _inputs("skewed", seed=3)
-    base = run_layer(inp, "bf16", capacity=1.0, minibatch=0)
+    base = run_layer(inp, mode, capacity=1.0, minibatch=0)
     for c, mb in ((0.0, 0), (0.05, 64), (0.5, 128), (3.0, 1)):
-        other = run_layer(inp, "bf16", capacity=c, minibatch=mb)
+        other = run_layer(inp, mode, capacity=c, minibatch=mb)
         assert torch.equal(base[0], other[0]), (c, mb)
         for key in base[1]:
             assert torch.equal(base[1][key], other[1][key]), (c, mb, key)
@@ -338,7 +339,8 @@ def test_mxfp8_dispatch_codes_and_scales_bit_exact(name):
 
 
 @pytest.mark.parametrize("name,mode", [("ragged_shared", "bf16"), ("wide", "bf16"), ("skewed", "bf16"),
-                                       ("ragged_shared", "mxfp8"), ("wide", "mxfp8")])
+                                       ("ragged_shared", "mxfp8"), ("wide", "mxfp8"),
+                                       ("ragged_shared", "mxfp8_full"), ("wide", "mxfp8_full")])
 def test_swiglu_limit_matches_oracle(name, mode):
     """The clamped SwiGLU (swiglu_limit L: gate <= L, up in [-L, L]) against the
     oracle's clamped layer, forward and backward, with L low enough that a
