@@ -43,6 +43,41 @@ def _need(t, dtype, shape, name):
     return t
 
 
+def _pointer_fields(struct_cls):
+    return tuple(name for name, typ in struct_cls._fields_ if typ is _lib.P)
+
+
+def _flatten_struct(c, buf):
+    """The struct's scalar fields and its pointers: a pointer into buf as
+    ("off", offset), NULL as None, and one that points elsewhere (the
+    library's own fixed scratch array, which never moves) as ("abs", address).
+    Everything needed to rebuild the struct over a copy of buf."""
+    base, size = buf.data_ptr(), buf.numel() * buf.element_size()
+    scalars, ptrs = {}, {}
+    for name, _ in c._fields_:
+        v = getattr(c, name)
+        if name in _pointer_fields(type(c)):
+            ptrs[name] = None if not v else (("off", v - base) if base <= v < base + size else ("abs", v))
+        else:
+            scalars[name] = v
+    return scalars, ptrs
+
+
+def _unflatten_struct(struct_cls, buf, scalars, ptrs):
+    c = struct_cls(**scalars)
+    base, size = buf.data_ptr(), buf.numel() * buf.element_size()
+    for name, p in ptrs.items():
+        if p is None:
+            continue
+        kind, v = p
+        if kind == "off":
+            if not 0 <= v < size:
+                raise ValueError(f"{name}: offset {v} outside the {size}-byte buffer")
+            v = base + v
+        setattr(c, name, v)
+    return c
+
+
 @dataclass
 class Schedule:
     """The dispatch/combine schedule; ``buf`` owns the device memory."""
@@ -51,6 +86,18 @@ class Schedule:
     E: int
     buf: torch.Tensor
     c: _lib.MokSchedule
+
+    def flatten(self):
+        """(buf, meta): the one tensor that holds the schedule, and plain
+        metadata.  Saving ``buf`` through ``save_for_backward`` lets saved-tensor
+        hooks (offload, checkpointing) move it; ``unflatten`` rebuilds the
+        schedule over wherever it lands (the arrays hold no pointers)."""
+        return self.buf, (self.T, self.k, self.E) + _flatten_struct(self.c, self.buf)
+
+    @classmethod
+    def unflatten(cls, buf, meta):
+        T, k, E, scalars, offsets = meta
+        return cls(T, k, E, buf, _unflatten_struct(_lib.MokSchedule, buf, scalars, offsets))
 
     def status(self):
         st, nt, P = C.c_int32(), C.c_int32(), C.c_int32()
@@ -112,6 +159,16 @@ class Context:
     buf: torch.Tensor
     c: _lib.MokCtx
     mode: int
+
+    def flatten(self):
+        """(buf, meta), as ``Schedule.flatten``: the forward's saved
+        activations live in ``buf`` and hold no pointers."""
+        return self.buf, (self.mode,) + _flatten_struct(self.c, self.buf)
+
+    @classmethod
+    def unflatten(cls, buf, meta):
+        mode, scalars, offsets = meta
+        return cls(buf, _unflatten_struct(_lib.MokCtx, buf, scalars, offsets), mode)
 
     def status(self) -> int:
         st = C.c_int32()

@@ -12,7 +12,7 @@ from __future__ import annotations
 
 import torch
 
-from . import Weights, backward, forward, quantize_weights, schedule
+from . import Context, Schedule, Weights, backward, forward, quantize_weights, schedule
 
 
 class MoKFunction(torch.autograd.Function):
@@ -29,14 +29,20 @@ class MoKFunction(torch.autograd.Function):
         if mode in ("mxfp8", "mxfp8_full"):
             weights = quantize_weights(weights, backward=(mode == "mxfp8_full"))
         y, mctx = forward(x, router_w, sched, weights, mode=mode, minibatch=minibatch, swiglu_limit=swiglu_limit)
-        ctx.save_for_backward(x, router_w)
-        ctx.mok = (sched, mctx, weights, minibatch, ws_gate is not None)
+        # the schedule and the context go through save_for_backward as their
+        # buffers, so saved-tensor hooks (offload, checkpointing) see them
+        sbuf, smeta = sched.flatten()
+        cbuf, cmeta = mctx.flatten()
+        ctx.save_for_backward(x, router_w, sbuf, cbuf)
+        ctx.mok = (smeta, cmeta, weights, minibatch, ws_gate is not None)
         return y
 
     @staticmethod
     def backward(ctx, dy):
-        x, router_w = ctx.saved_tensors
-        sched, mctx, weights, minibatch, shared = ctx.mok
+        x, router_w, sbuf, cbuf = ctx.saved_tensors
+        smeta, cmeta, weights, minibatch, shared = ctx.mok
+        sched = Schedule.unflatten(sbuf, smeta)     # over wherever the hooks put the buffers
+        mctx = Context.unflatten(cbuf, cmeta)
         g = backward(dy.to(torch.bfloat16).contiguous(), x, router_w, sched, mctx, weights, minibatch=minibatch)
         ctx.mok = None
         return (g["dx"], g["d_router_w"], None, g["d_w_gate"], g["d_w_up"], g["d_w_down"],

@@ -37,3 +37,36 @@ def test_autograd_gradients_match_oracle(mode, shape):
     for key, val in got.items():
         assert val is not None, key
         assert rel_l2(val, g_ref[key]) <= BF16_TOL, key
+
+
+@pytest.mark.parametrize("mode", ["bf16", "mxfp8_full"])
+def test_saved_schedule_and_context_survive_offload(mode):
+    """The schedule and the forward context reach backward through
+    save_for_backward, so saved-tensor hooks see them: under save_on_cpu they
+    leave the device after the forward and come back at new addresses for the
+    backward.  The gradients equal those of a run without offload, bit for bit."""
+    mok()
+    from mixture_experts_layer_mok_gb300.autograd import MoKLayer
+
+    T, H, I, E, k, I_s = 200, 256, 384, 5, 3, 256
+    inp = gen.make_layer_inputs(T, H, I, E, k, I_s, seed=13)
+
+    def run(offload):
+        layer = MoKLayer(E, H, I, I_s, mode=mode, device="cuda")
+        with torch.no_grad():
+            for name in ("w_gate", "w_up", "w_down", "ws_gate", "ws_up", "ws_down"):
+                getattr(layer, name).copy_(getattr(inp, name))
+        x = inp.x.cuda().requires_grad_(True)
+        rw = inp.router_w.cuda().requires_grad_(True)
+        if offload:
+            with torch.autograd.graph.save_on_cpu(pin_memory=True):
+                y = layer(x, rw, inp.top_experts.cuda())
+        else:
+            y = layer(x, rw, inp.top_experts.cuda())
+        (y.float() * inp.dy.cuda().float()).sum().backward()
+        torch.cuda.synchronize()
+        return [y, x.grad, rw.grad] + [getattr(layer, n).grad for n in ("w_gate", "w_up", "w_down", "ws_gate",
+                                                                        "ws_up", "ws_down")]
+
+    for a, b in zip(run(False), run(True)):
+        assert torch.equal(a, b)

@@ -131,3 +131,37 @@ def test_autograd_layer_needs_cuda_tensors():
     x = torch.zeros(8, 128, dtype=torch.bfloat16)
     with pytest.raises((ValueError, RuntimeError)):
         layer(x, torch.full((8, 2), 0.5), torch.zeros(8, 2, dtype=torch.int64))
+
+
+def test_schedule_and_context_flatten_over_a_moved_buffer():
+    """flatten/unflatten carry the schedule and the context as (buffer,
+    metadata): rebuilt over a copy of the buffer, every pointer keeps its
+    offset, NULL stays NULL, and a pointer outside the buffer (the library's
+    fixed scratch) keeps its address."""
+    import torch
+
+    import mixture_experts_layer_mok_gb300 as m
+    from mixture_experts_layer_mok_gb300 import _lib
+
+    buf = torch.zeros(4096, dtype=torch.uint8)
+    base = buf.data_ptr()
+    c = _lib.MokSchedule(T=8, k=2, E=4, max_tiles=3)
+    c.cnt, c.row0, c.row_src, c.header = base + 0, base + 256, base + 512, base + 3840
+    c.scratch = 0x7F0000001000                       # outside the buffer
+    s = m.Schedule(8, 2, 4, buf, c)
+    sbuf, meta = s.flatten()
+    moved = sbuf.clone()
+    s2 = m.Schedule.unflatten(moved, meta)
+    nb = moved.data_ptr()
+    assert (s2.T, s2.k, s2.E, s2.c.max_tiles) == (8, 2, 4, 3)
+    assert (s2.c.cnt, s2.c.row0, s2.c.row_src, s2.c.header) == (nb, nb + 256, nb + 512, nb + 3840)
+    assert s2.c.scratch == 0x7F0000001000 and not s2.c.slot_row
+    cc = _lib.MokCtx(T=8, k=2, E=4, H=128, I=128, I_s=0, mode=2, max_tiles=3, dispatch=1, swiglu_limit=0.5)
+    cc.gu, cc.status = base + 1024, base + 2048
+    ctx = m.Context(buf, cc, 2)
+    cbuf, cmeta = ctx.flatten()
+    ctx2 = m.Context.unflatten(moved, cmeta)
+    assert ctx2.mode == 2 and ctx2.c.mode == 2 and ctx2.c.dispatch == 1 and abs(ctx2.c.swiglu_limit - 0.5) < 1e-7
+    assert (ctx2.c.gu, ctx2.c.status) == (nb + 1024, nb + 2048) and not ctx2.c.h
+    with pytest.raises(ValueError):
+        m.Schedule.unflatten(moved[:100], meta)      # offsets past a too-small buffer
