@@ -138,7 +138,10 @@ typedef struct {
   int mode;            /* MOK_MODE_* */
   int minibatch_size;  /* tokens per wave of the persistent pipeline; 0 = T */
   int debug_flags;     /* MOK_DEBUG_*; 0 in production */
-  int dispatch;        /* MOK_DISPATCH_* */
+  int dispatch;        /* MOK_DISPATCH_*: the bf16 GEMMs' choice (the bf16
+                          forward, and every bf16 backward).  The MXFP8 GEMMs
+                          always read rows that a quantiser wrote in schedule
+                          order. */
   int num_events;      /* 0, or 2 * MOK_NUM_STAGES when events is set */
   void* const* events; /* optional cudaEvent_t[2 * MOK_NUM_STAGES], NULL = off */
   float swiglu_limit;  /* forward: 0 = plain SwiGLU; L > 0 clamps the gate
