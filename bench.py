@@ -264,6 +264,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--stages", action="store_true", help="print per-stage times to stderr")
+    ap.add_argument("--capacity", type=float, default=None, help="override the workload's capacity multiplier")
+    ap.add_argument("--minibatch", type=int, default=None, help="override the workload's minibatch size")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -273,6 +275,10 @@ def main():
     from mixture_experts_layer_mok_gb300 import inputs as gen
 
     c = dict(gen.WORKLOADS[args.workload])
+    if args.capacity is not None:
+        c["capacity"] = args.capacity
+    if args.minibatch is not None:
+        c["minibatch"] = args.minibatch
     fwd_flop, step_flop = layer_flops(c)
     config = {"workload": args.workload, "T": c["T"], "H": c["H"], "I": c["I"], "E": c["E"], "k": c["k"],
               "I_s": c["I_s"], "routing": "zipf s=%.1f" % c["skew"] if c["skew"] else "softmax top-k",
