@@ -51,6 +51,7 @@ def _check_pairs(arr, ref):
     (16384, 8, 128, 1.2, 1.0),         # skewed routing, capacity 1.0
     (65536, 8, 256, None, 0.5),        # large layer
     (1, 1, 1, None, 0.5), (5, 3, 7, None, 0.0), (4097, 5, 1000, None, 0.5), (3000, 16, 64, 1.2, 0.01),
+    (8192, 8, 64, 1.2, 0.5), (65537, 1, 16, 1.2, 0.5),
 ])
 def test_schedule_bit_exact(T, k, E, skew, c):
     te = gen.make_routing(T, k, E, seed=T + E, skew=skew)
