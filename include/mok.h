@@ -355,7 +355,11 @@ mok_status_t mok_ctx_status(const mok_ctx_t* ctx, int* status);
  * taken at the saved gate/up pre-activations.  The backward runs in the mode
  * the forward recorded in the context: bf16 GEMMs after MOK_MODE_BF16 and
  * MOK_MODE_MXFP8_FWD, MXFP8 GEMMs after MOK_MODE_MXFP8 (which needs the
- * weights' mxt* copies).  x and router_w are the forward's inputs.  Outputs:
+ * weights' mxt* copies).  In MOK_MODE_MXFP8 every backward GEMM quantises
+ * both of its operands in blocks of 32 along its own contraction axis; for
+ * the weight gradients that axis is the expert's rows in schedule order.
+ * The quantisers see bf16 values: dy, x, the saved gate/up, and the bf16
+ * roundings of dG, dU and w*h.  x and router_w are the forward's inputs.  Outputs:
  * dx bf16 [T][H], d_router_w fp32 [T][k] (= <dy[t], F_e(x[t])>), the six
  * weight gradients.  Scratch comes from `ws` (mok_bwd_workspace_bytes with
  * the context's mode).  Device errors land in ctx->status. */
