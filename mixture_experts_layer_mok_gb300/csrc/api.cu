@@ -1141,6 +1141,8 @@ mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x, const float
   const void* ptrs[] = {x, router_w, y, ctx_buf, w->w_gate, w->w_up, w->w_down};
   for (const void* q : ptrs)
     if (!aligned16(q)) return fail(MOK_ERR_INVALID_ARG, "misaligned pointer");
+  if (Is > 0 && (!aligned16(w->ws_gate) || !aligned16(w->ws_up) || !aligned16(w->ws_down)))
+    return fail(MOK_ERR_INVALID_ARG, "misaligned shared weight pointer");
   if (ctx_bytes < mok_ctx_bytes(T, k, E, H, I, Is, cfg->mode))
     return fail(MOK_ERR_INVALID_ARG, "context buffer too small");
   int sms = 0;
@@ -1192,14 +1194,22 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
   const int T = s->T, k = s->k, E = s->E, H = w->H, I = w->I, Is = w->I_s;
   st = check_shapes(T, k, E, H, I, Is);
   if (st) return st;
+  if (w->E != E) return fail(MOK_ERR_INVALID_ARG, "weights have E=%d, schedule E=%d", w->E, E);
   if (ctx->T != T || ctx->k != k || ctx->E != E || ctx->H != H || ctx->I != I || ctx->I_s != Is)
     return fail(MOK_ERR_INVALID_ARG, "context does not match the schedule / weights");
+  if (ctx->mode != MOK_MODE_BF16 && ctx->mode != MOK_MODE_MXFP8_FWD && ctx->mode != MOK_MODE_MXFP8)
+    return fail(MOK_ERR_INVALID_ARG, "context mode %d is not one a forward records", ctx->mode);
   if (!g->d_w_gate || !g->d_w_up || !g->d_w_down) return fail(MOK_ERR_INVALID_ARG, "NULL routed grad");
   if (Is > 0 && (!g->d_ws_gate || !g->d_ws_up || !g->d_ws_down || !w->ws_gate || !w->ws_up || !w->ws_down))
     return fail(MOK_ERR_INVALID_ARG, "NULL shared weight or grad");
   const void* ptrs[] = {dy, x, router_w, dx, d_router_w, ws, g->d_w_gate, g->d_w_up, g->d_w_down};
   for (const void* q : ptrs)
     if (!aligned16(q)) return fail(MOK_ERR_INVALID_ARG, "misaligned pointer");
+  if (Is > 0) {
+    const void* sp[] = {w->ws_gate, w->ws_up, w->ws_down, g->d_ws_gate, g->d_ws_up, g->d_ws_down};
+    for (const void* q : sp)
+      if (!aligned16(q)) return fail(MOK_ERR_INVALID_ARG, "misaligned shared weight or grad pointer");
+  }
   const bool mxb = ctx->mode == MOK_MODE_MXFP8;
   if (mxb) {
     const void* mp[] = {w->mxt_gate, w->mxt_gate_sc, w->mxt_up, w->mxt_up_sc, w->mxt_down, w->mxt_down_sc};

@@ -108,6 +108,46 @@ def test_argument_errors_need_no_device(lib):
     del buf
 
 
+def test_layer_argument_checks_need_no_device(lib):
+    """Mismatched or misaligned arguments to the layer calls are refused on
+    the host, before any device work."""
+    from mixture_experts_layer_mok_gb300 import _lib
+
+    fake = C.c_void_p(16)           # never dereferenced: validation fails first
+    odd = C.c_void_p(16 + 8)        # not 16-byte aligned
+    cfg = _lib.MokConfig(mode=0)
+    s = _lib.MokSchedule(T=8, k=2, E=4, max_tiles=6)
+    w = _lib.MokWeights(E=4, H=128, I=128, I_s=128, w_gate=fake, w_up=fake, w_down=fake,
+                        ws_gate=fake, ws_up=odd, ws_down=fake)
+    ctx = _lib.MokCtx()
+    assert lib.mok_forward(C.byref(cfg), fake, fake, C.byref(s), C.byref(w), fake, fake, 1 << 40,
+                           C.byref(ctx), None) == _lib.MOK_ERR_INVALID_ARG
+    assert b"misaligned shared weight" in lib.mok_last_error()
+
+    w.ws_up = fake
+    g = _lib.MokWeightGrads(d_w_gate=fake, d_w_up=fake, d_w_down=fake, d_ws_gate=fake, d_ws_up=odd, d_ws_down=fake)
+    ctx = _lib.MokCtx(T=8, k=2, E=4, H=128, I=128, I_s=128, mode=0)
+
+    def backward():
+        return lib.mok_backward(C.byref(cfg), fake, fake, fake, C.byref(s), C.byref(ctx), C.byref(w), fake, fake,
+                                C.byref(g), fake, 1 << 40, None)
+
+    assert backward() == _lib.MOK_ERR_INVALID_ARG
+    assert b"misaligned shared weight or grad" in lib.mok_last_error()
+    g.d_ws_up = fake
+    ctx.mode = 7                    # no forward records this mode
+    assert backward() == _lib.MOK_ERR_INVALID_ARG
+    assert b"context mode 7" in lib.mok_last_error()
+    ctx.mode = 0
+    w.E = 5                         # weights for another expert count than the schedule's
+    assert backward() == _lib.MOK_ERR_INVALID_ARG
+    assert b"weights have E=5" in lib.mok_last_error()
+    w.E = 4
+    ctx.I = 256                     # a context from another layer
+    assert backward() == _lib.MOK_ERR_INVALID_ARG
+    assert b"context does not match" in lib.mok_last_error()
+
+
 def test_package_import_does_not_load_library():
     import subprocess
     import sys
