@@ -568,7 +568,8 @@ def run_reference(args, c, config, rank, world):
     sample = (f"each step: fwd+bwd of the first {tokens} tokens of the {args.workload} layer in the float64 NumPy "
               "oracle (weights widened once, outside the timing)")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 3),
-            "unit": "tokens/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+            "unit": "tokens/s", "n_gpus": world, "device": "host cores only (rank 0; no GPU work)",
+            "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * el_total / args.steps, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)", "config": config,
             "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",

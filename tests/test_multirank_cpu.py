@@ -82,3 +82,4 @@ def test_reference_arm_prints_on_rank0_only(tmp_path):
     line = json.loads(out0[0])
     assert line["impl"] == "reference" and line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+    assert line["n_gpus"] == 2                       # the job's N, though only host cores work
