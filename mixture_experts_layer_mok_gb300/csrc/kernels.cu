@@ -526,7 +526,11 @@ cudaError_t launch_mx_quantize_t(const uint16_t* src, long long ld, int batch, i
                                  int rtiled) {
   const long long tiles = static_cast<long long>(batch) * ((R + 127) / 128) * (C / 64);
   if (tiles == 0) return cudaSuccess;
-  const long long cap = static_cast<long long>(num_sms) * 8;
+  // up to 32 blocks per SM, far more than are resident at once (5): blocks
+  // that start as others finish keep more tiles' copies in flight than a
+  // single resident wave walking its tiles does (measured on one GB300: 8, 16,
+  // 32, 64 and 128 per SM; 32 was fastest)
+  const long long cap = static_cast<long long>(num_sms) * 32;
   const int grid = static_cast<int>(tiles < cap ? tiles : cap);
   cudaError_t err = launch_dependent(mx_quantize_t_kernel, dim3(grid), dim3(256), 0, st, src, ld, batch, R, C,
                                      valid_rows, row_src, topk, header, codes, scales, tiled, rcodes, rscales, rtiled);
