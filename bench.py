@@ -97,12 +97,12 @@ def launches_per_step(c):
         n += 2
     if mx:
         n += 3 + s3                         # weight prequantisation (every step)
-        n += 3 + s3                         # weight scales into the tensor-core layout
+        n += 1                              # weight scales into the tensor-core layout (one launch)
         n += 1                              # x quantised into token and schedule order
     else:
         n += 1                              # x rows into schedule order
     if full:                                # (the prequantisation above writes both weight copies)
-        n += 3 + s3                         # transposed weights' scales into the tensor-core layout
+        n += 1                              # transposed weights' scales into the tensor-core layout
         n += 2 + (2 if shared else 0)       # x transposed; dy rows + transposed (schedule, token order)
         n += 4 + (4 if shared else 0)       # GEMMs (the SwiGLU backward writes its MXFP8 outputs)
         n += 2                              # combine dx, reduce d_w

@@ -681,13 +681,16 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
   if ((st = side_stream(&side))) return st;
   MOK_CUDA(cudaEventRecord(side->fork, cs));
   MOK_CUDA(cudaStreamWaitEvent(side->s, side->fork, 0));
-  MOK_CUDA(launch_mx_tile_scales(w->mx_gate_sc, static_cast<long long>(E) * I, H, X.wg_sc, side->s));
-  MOK_CUDA(launch_mx_tile_scales(w->mx_up_sc, static_cast<long long>(E) * I, H, X.wu_sc, side->s));
-  MOK_CUDA(launch_mx_tile_scales(w->mx_down_sc, static_cast<long long>(E) * H, I, X.wd_sc, side->s));
-  if (Is > 0) {
-    MOK_CUDA(launch_mx_tile_scales(w->mxs_gate_sc, Is, H, X.wsg_sc, side->s));
-    MOK_CUDA(launch_mx_tile_scales(w->mxs_up_sc, Is, H, X.wsu_sc, side->s));
-    MOK_CUDA(launch_mx_tile_scales(w->mxs_down_sc, H, Is, X.wsd_sc, side->s));
+  {
+    const long long sr = Is > 0 ? 1 : 0;   // the shared expert's jobs are skipped without one
+    const MxTileScaleJob jobs[] = {
+        {w->mx_gate_sc, static_cast<long long>(E) * I, H, X.wg_sc},
+        {w->mx_up_sc, static_cast<long long>(E) * I, H, X.wu_sc},
+        {w->mx_down_sc, static_cast<long long>(E) * H, I, X.wd_sc},
+        {w->mxs_gate_sc, sr * Is, H, X.wsg_sc},
+        {w->mxs_up_sc, sr * Is, H, X.wsu_sc},
+        {w->mxs_down_sc, sr * H, Is, X.wsd_sc}};
+    MOK_CUDA(launch_mx_tile_scales(jobs, 6, side->s));
   }
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_PREP, 1, side->s));
   MOK_CUDA(cudaEventRecord(side->join, side->s));
@@ -822,21 +825,24 @@ mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const u
   const int Tp = (T + 127) / 128 * 128;
   const int mri = static_cast<int>(mr);
   mok_status_t st;
-  // ---- on the side stream: weight scales into the tensor-core layout (the
-  // shared expert's first, handed back at `join`), then the transposed x,
+  // ---- on the side stream: weight scales into the tensor-core layout (one
+  // launch, handed back at `join`), then the transposed x,
   // which only the gate/up weight gradients read (handed back at `join2`)
   SideStream* side = nullptr;
   if ((st = side_stream(&side))) return st;
   MOK_CUDA(cudaEventRecord(side->fork, cs));
   MOK_CUDA(cudaStreamWaitEvent(side->s, side->fork, 0));
-  if (Is > 0) {
-    MOK_CUDA(launch_mx_tile_scales(w->mxts_gate_sc, H, Is, L.wtsg_sc, side->s));
-    MOK_CUDA(launch_mx_tile_scales(w->mxts_up_sc, H, Is, L.wtsu_sc, side->s));
-    MOK_CUDA(launch_mx_tile_scales(w->mxts_down_sc, Is, H, L.wtsd_sc, side->s));
+  {
+    const long long sr = Is > 0 ? 1 : 0;   // the shared expert's jobs are skipped without one
+    const MxTileScaleJob jobs[] = {
+        {w->mxts_gate_sc, sr * H, Is, L.wtsg_sc},
+        {w->mxts_up_sc, sr * H, Is, L.wtsu_sc},
+        {w->mxts_down_sc, sr * Is, H, L.wtsd_sc},
+        {w->mxt_gate_sc, static_cast<long long>(E) * H, I, L.wtg_sc},
+        {w->mxt_up_sc, static_cast<long long>(E) * H, I, L.wtu_sc},
+        {w->mxt_down_sc, static_cast<long long>(E) * I, H, L.wtd_sc}};
+    MOK_CUDA(launch_mx_tile_scales(jobs, 6, side->s));
   }
-  MOK_CUDA(launch_mx_tile_scales(w->mxt_gate_sc, static_cast<long long>(E) * H, I, L.wtg_sc, side->s));
-  MOK_CUDA(launch_mx_tile_scales(w->mxt_up_sc, static_cast<long long>(E) * H, I, L.wtu_sc, side->s));
-  MOK_CUDA(launch_mx_tile_scales(w->mxt_down_sc, static_cast<long long>(E) * I, H, L.wtd_sc, side->s));
   MOK_CUDA(cudaEventRecord(side->join, side->s));
   if (Is > 0)
     MOK_CUDA(launch_mx_quantize_t(x, H, 1, Tp, H, T, nullptr, 1, nullptr, L.xT_tok, L.xT_tok_sc, 1, sms, side->s));

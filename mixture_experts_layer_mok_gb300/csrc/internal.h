@@ -44,7 +44,17 @@ cudaError_t launch_mx_quantize_t(const uint16_t* src, long long ld, int batch, i
                                  const int* row_src, int topk, const int* header, uint8_t* codes, uint8_t* scales,
                                  int tiled, int num_sms, cudaStream_t st, uint8_t* rcodes = nullptr,
                                  uint8_t* rscales = nullptr, int rtiled = 0);
-cudaError_t launch_mx_tile_scales(const uint8_t* src, long long rows, int K, uint8_t* dst, cudaStream_t st);
+// One matrix of row-major E8M0 scales [rows][K/32] to rearrange into the
+// tensor-core scale layout at dst (rows and K multiples of 128; rows 0 = skip).
+struct MxTileScaleJob {
+  const uint8_t* src;
+  long long rows;
+  int K;
+  uint8_t* dst;
+};
+constexpr int kMaxScaleJobs = 6;
+// All jobs (at most kMaxScaleJobs that are not skipped) in one launch.
+cudaError_t launch_mx_tile_scales(const MxTileScaleJob* jobs, int n, cudaStream_t st);
 cudaError_t launch_combine(const uint16_t* rows, const int* slot_row, const int* header, long long max_rows,
                            const uint16_t* base, int T, int k, int H, uint16_t* out, int num_sms, cudaStream_t st);
 cudaError_t launch_permute_rows(const uint16_t* src, int H, int topk, const int* row_src, const int* header,

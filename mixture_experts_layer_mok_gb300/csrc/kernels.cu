@@ -538,19 +538,32 @@ cudaError_t launch_mx_quantize_t(const uint16_t* src, long long ld, int batch, i
   return cudaGetLastError();
 }
 
-// Row-major E8M0 scales [rows][K/32] -> the tensor-core scale layout.  One
-// block per (128-row block, 16 column groups): coalesced row reads into shared
-// memory, coalesced atom writes out of it.
-__global__ void __launch_bounds__(256) mx_tile_scales_kernel(const uint8_t* __restrict__ src, int K,
-                                                             uint8_t* __restrict__ dst) {
+// Row-major E8M0 scales [rows][K/32] -> the tensor-core scale layout, for up
+// to kMaxScaleJobs matrices in one launch (a forward or a backward needs six;
+// separate launches would each wait for the last).  One block per (128-row
+// block of one job, 16 column groups): coalesced row reads into shared memory,
+// coalesced atom writes out of it.
+struct TileScaleJobs {
+  const uint8_t* src[kMaxScaleJobs];
+  uint8_t* dst[kMaxScaleJobs];
+  int K[kMaxScaleJobs];
+  int rb0[kMaxScaleJobs + 1];   // job j owns blocks [rb0[j], rb0[j+1]) of grid.x
+  int n;
+};
+
+__global__ void __launch_bounds__(256) mx_tile_scales_kernel(const __grid_constant__ TileScaleJobs J) {
   griddep_wait();
   griddep_launch_dependents();
   __shared__ uint32_t tile[128][17];
-  const int cg = K / 128;
-  const long long rb = blockIdx.x;
+  int j = 0;
+  while (j + 1 < J.n && static_cast<int>(blockIdx.x) >= J.rb0[j + 1]) ++j;
+  const int cg = J.K[j] / 128;
   const int g0 = blockIdx.y * 16;
+  if (g0 >= cg) return;   // this job has fewer column groups than the grid's y extent
+  const long long rb = static_cast<long long>(blockIdx.x) - J.rb0[j];
   const int ng = min(16, cg - g0);
-  const uint32_t* s = reinterpret_cast<const uint32_t*>(src);  // one word = one column group of a row
+  const uint32_t* s = reinterpret_cast<const uint32_t*>(J.src[j]);  // one word = one column group of a row
+  uint8_t* dst = J.dst[j];
   for (int i = threadIdx.x; i < 128 * 16; i += 256) {
     const int row = i >> 4, g = i & 15;
     if (g < ng) tile[row][g] = __ldg(s + (rb * 128 + row) * cg + g0 + g);
@@ -564,10 +577,27 @@ __global__ void __launch_bounds__(256) mx_tile_scales_kernel(const uint8_t* __re
   }
 }
 
-cudaError_t launch_mx_tile_scales(const uint8_t* src, long long rows, int K, uint8_t* dst, cudaStream_t st) {
-  if (rows == 0) return cudaSuccess;
-  const dim3 grid(static_cast<unsigned>(rows / 128), static_cast<unsigned>((K / 128 + 15) / 16));
-  cudaError_t err = launch_dependent(mx_tile_scales_kernel, grid, dim3(256), 0, st, src, K, dst);
+cudaError_t launch_mx_tile_scales(const MxTileScaleJob* jobs, int n, cudaStream_t st) {
+  TileScaleJobs J = {};
+  long long total = 0;
+  int ymax = 0, m = 0;
+  for (int i = 0; i < n; ++i) {
+    if (jobs[i].rows <= 0) continue;
+    if (m == kMaxScaleJobs || jobs[i].rows % 128 || jobs[i].K <= 0 || jobs[i].K % 128) return cudaErrorInvalidValue;
+    J.src[m] = jobs[i].src;
+    J.dst[m] = jobs[i].dst;
+    J.K[m] = jobs[i].K;
+    J.rb0[m] = static_cast<int>(total);
+    total += jobs[i].rows / 128;
+    if (total > 0x7fffffffll) return cudaErrorInvalidValue;
+    ymax = max(ymax, (jobs[i].K / 128 + 15) / 16);
+    ++m;
+  }
+  if (m == 0) return cudaSuccess;
+  J.rb0[m] = static_cast<int>(total);
+  J.n = m;
+  cudaError_t err = launch_dependent(mx_tile_scales_kernel, dim3(static_cast<unsigned>(total),
+                                     static_cast<unsigned>(ymax)), dim3(256), 0, st, J);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
