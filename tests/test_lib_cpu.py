@@ -205,3 +205,37 @@ def test_schedule_and_context_flatten_over_a_moved_buffer():
     assert (ctx2.c.gu, ctx2.c.status) == (nb + 1024, nb + 2048) and not ctx2.c.h
     with pytest.raises(ValueError):
         m.Schedule.unflatten(moved[:100], meta)      # offsets past a too-small buffer
+
+
+def test_ctypes_structs_match_the_c_header(tmp_path):
+    """The binding's ctypes structs against the C header itself: a C99 program
+    built from include/mok.h prints each struct's size and every field's
+    offset, and the ctypes view must agree field by field."""
+    import shutil
+    import subprocess
+
+    from mixture_experts_layer_mok_gb300 import _lib
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    pairs = [("mok_config_t", _lib.MokConfig), ("mok_schedule_t", _lib.MokSchedule),
+             ("mok_weights_t", _lib.MokWeights), ("mok_ctx_t", _lib.MokCtx),
+             ("mok_weight_grads_t", _lib.MokWeightGrads)]
+    lines = ["#include <stddef.h>", "#include <stdio.h>", '#include "mok.h"', "int main(void) {"]
+    for cname, cls in pairs:
+        lines.append(f'  printf("{cname} sizeof %zu\\n", sizeof({cname}));')
+        for field, _ in cls._fields_:
+            lines.append(f'  printf("{cname} {field} %zu\\n", offsetof({cname}, {field}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-o", str(exe)], check=True, capture_output=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    got = {(a, b): int(c) for a, b, c in (ln.split() for ln in out if ln)}
+    for cname, cls in pairs:
+        assert got[(cname, "sizeof")] == C.sizeof(cls), cname
+        for field, _ in cls._fields_:
+            assert got[(cname, field)] == getattr(cls, field).offset, (cname, field)
