@@ -34,7 +34,12 @@ an out-of-range expert id is an error; the E8M0 scale is the smallest power
 of two that brings the block amax to <= 448 (no clipping); an all-zero block
 gets scale 2^0; a negative value that rounds to zero keeps its sign bit; the
 MXFP8 backward is straight-through (quantisation treated as identity) and is
-evaluated at the gate/up pre-activations of the quantised forward.
+evaluated at the gate/up pre-activations of the quantised forward; in the
+fully MXFP8 backward every backward contraction takes both operands quantised
+in blocks of 32 along its own contraction axis (for the weight gradients, 32
+consecutive rows of an expert in schedule order), from the bf16 values the
+backward holds; ``swiglu_limit`` is the usual clamped SwiGLU (gate <= L, up
+in [-L, L]).
 """
 from __future__ import annotations
 
