@@ -260,7 +260,8 @@ size_t mok_schedule_bytes(int T, int k, int E);
 
 /* Build the schedule for top_experts (device int64 [T][k]) over E experts.
  * capacity_multiplier (>= 0, finite) sets the per-expert tile budget
- * ceil(ceil(c*T)/128) of the static work table ([MoKEd] "Tuning the five
+ * ceil(ceil(c*T)/128) of the static work table, with c*T rounded up in
+ * double precision on exactly the caller's value ([MoKEd] "Tuning the five
  * hyperparameters before production": the worst-case fraction of tokens on
  * one expert); tiles beyond it go to an overflow list that follows the
  * primary list.  It changes the order of the tile list only, never a row or a
@@ -268,7 +269,7 @@ size_t mok_schedule_bytes(int T, int k, int E);
  * [0, E) sets status MOK_ERR_INDEX in header[2] and num_tiles = 0.
  * Limits: 1 <= k <= 64, 1 <= E <= 1024, T*k < 2^31. */
 mok_status_t mok_schedule(const int64_t* top_experts, int T, int k, int E,
-                          float capacity_multiplier, void* buf, size_t bytes,
+                          double capacity_multiplier, void* buf, size_t bytes,
                           mok_schedule_t* out, void* stream);
 
 /* Synchronise `stream`'s work on the schedule and read its header.  Any of the
@@ -297,7 +298,7 @@ mok_status_t mok_schedule_status(const mok_schedule_t* sched, int* status,
  *   - No allocation of any kind happens in this call.
  * Arguments, outputs and errors are those of mok_schedule(). */
 mok_status_t mok_schedule_noalloc(const int64_t* top_experts, int T, int k, int E,
-                                  float capacity_multiplier, void* buf, size_t bytes,
+                                  double capacity_multiplier, void* buf, size_t bytes,
                                   mok_schedule_t* out, void* stream);
 
 /* ---- MXFP8 quantiser ([MoKEd] "Tuning the five hyperparameters before

@@ -81,10 +81,10 @@ SIGNATURES = {
     "mok_version": (C.c_int, []),
     "mok_last_error": (C.c_char_p, []),
     "mok_schedule_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int]),
-    "mok_schedule": (C.c_int, [P, C.c_int, C.c_int, C.c_int, C.c_float, P, C.c_size_t,
+    "mok_schedule": (C.c_int, [P, C.c_int, C.c_int, C.c_int, C.c_double, P, C.c_size_t,
                                C.POINTER(MokSchedule), P]),
     "mok_schedule_status": (C.c_int, [C.POINTER(MokSchedule), I32P, I32P, I32P]),
-    "mok_schedule_noalloc": (C.c_int, [P, C.c_int, C.c_int, C.c_int, C.c_float, P, C.c_size_t,
+    "mok_schedule_noalloc": (C.c_int, [P, C.c_int, C.c_int, C.c_int, C.c_double, P, C.c_size_t,
                                        C.POINTER(MokSchedule), P]),
     "mok_mxfp8_quantize": (C.c_int, [P, C.c_int64, C.c_int, P, P, P]),
     "mok_mxfp8_quantize_t": (C.c_int, [P, C.c_int64, C.c_int, C.c_int, P, P, P]),

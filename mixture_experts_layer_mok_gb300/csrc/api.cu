@@ -1012,7 +1012,7 @@ size_t mok_schedule_bytes(int T, int k, int E) {
   return carve_schedule(nullptr, T, k, E, &L);
 }
 
-mok_status_t mok_schedule(const int64_t* top_experts, int T, int k, int E, float capacity_multiplier,
+mok_status_t mok_schedule(const int64_t* top_experts, int T, int k, int E, double capacity_multiplier,
                           void* buf, size_t bytes, mok_schedule_t* out, void* stream) {
   NvtxCall nvtx("mok_schedule");
   if (!top_experts || !buf || !out) return fail(MOK_ERR_INVALID_ARG, "NULL argument");
@@ -1020,7 +1020,7 @@ mok_status_t mok_schedule(const int64_t* top_experts, int T, int k, int E, float
     return fail(MOK_ERR_INVALID_ARG, "need T >= 1, 1 <= k <= 64, 1 <= E <= 1024");
   if (static_cast<long long>(T) * k >= (1ll << 31) - 128ll * E)
     return fail(MOK_ERR_INVALID_ARG, "T*k too large");
-  if (!std::isfinite(capacity_multiplier) || capacity_multiplier < 0.f)
+  if (!std::isfinite(capacity_multiplier) || capacity_multiplier < 0.0)
     return fail(MOK_ERR_INVALID_ARG, "capacity_multiplier must be finite and >= 0");
   if (!aligned16(top_experts) || !aligned16(buf)) return fail(MOK_ERR_INVALID_ARG, "misaligned pointer");
   if (bytes < mok_schedule_bytes(T, k, E)) return fail(MOK_ERR_INVALID_ARG, "schedule buffer too small");
@@ -1030,8 +1030,8 @@ mok_status_t mok_schedule(const int64_t* top_experts, int T, int k, int E, float
   SchedLayout L;
   carve_schedule(buf, T, k, E, &L);
   const long long mt = max_tiles_of(T, k, E);
-  // per-expert tile budget, decided in double precision
-  const double rows = std::ceil(static_cast<double>(capacity_multiplier) * static_cast<double>(T));
+  // per-expert tile budget, decided in double precision on the caller's value
+  const double rows = std::ceil(capacity_multiplier * static_cast<double>(T));
   double capd = std::ceil(rows / kTileRows);
   if (capd > static_cast<double>(mt)) capd = static_cast<double>(mt);
   const int cap = static_cast<int>(capd);
@@ -1492,7 +1492,7 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
 }
 
 mok_status_t mok_schedule_noalloc(const int64_t* top_experts, int T, int k, int E,
-                                  float capacity_multiplier, void* buf, size_t bytes,
+                                  double capacity_multiplier, void* buf, size_t bytes,
                                   mok_schedule_t* out, void* stream) {
   NvtxCall nvtx("mok_schedule_noalloc");
   if (!top_experts || !buf || !out) return fail(MOK_ERR_INVALID_ARG, "NULL argument");
@@ -1505,7 +1505,7 @@ mok_status_t mok_schedule_noalloc(const int64_t* top_experts, int T, int k, int 
     return fail(MOK_ERR_INVALID_ARG,
                 "mok_schedule_noalloc: ceil(T*k/%d) * E = %lld exceeds its fixed scratch of %lld ints",
                 kSchedChunk, nchunks * E, kStaticSchedScratchInts);
-  if (!std::isfinite(capacity_multiplier) || capacity_multiplier < 0.f)
+  if (!std::isfinite(capacity_multiplier) || capacity_multiplier < 0.0)
     return fail(MOK_ERR_INVALID_ARG, "capacity_multiplier must be finite and >= 0");
   if (!aligned16(top_experts) || !aligned16(buf)) return fail(MOK_ERR_INVALID_ARG, "misaligned pointer");
   SchedLayout L;
@@ -1519,7 +1519,7 @@ mok_status_t mok_schedule_noalloc(const int64_t* top_experts, int T, int k, int 
   int32_t* scratch = nullptr;
   if ((st = static_sched_scratch(&scratch))) return st;
   const long long mt = max_tiles_of(T, k, E);
-  const double rows = std::ceil(static_cast<double>(capacity_multiplier) * static_cast<double>(T));
+  const double rows = std::ceil(capacity_multiplier * static_cast<double>(T));
   double capd = std::ceil(rows / kTileRows);
   if (capd > static_cast<double>(mt)) capd = static_cast<double>(mt);
   // every histogram entry the build reads is first written by it, so the

@@ -332,10 +332,8 @@ def layer_backward(x, router_w, top_experts, w_gate, w_up, w_down, dy,
     (expert or None, v) -> (g, u).
     With ``swiglu_limit`` > 0 the clamp of ``clamp_gate_up`` is
     differentiated as the clamp itself: the gate gradient passes where
-    g <= limit, the up gradient where |u| <= limit (the bounds included).
-    Those pass/stop decisions are taken on g and u rounded to bf16, the form
-    in which the forward keeps them for the backward (a decision is taken in
-    the kernel's precision; the values themselves stay float64 here).
+    g <= limit, the up gradient where |u| <= limit (the bounds included),
+    decided on the float64 g and u.
     """
     x, w, dy = _f64(x), _f64(router_w), _f64(dy)
     wg, wu, wd = _f64(w_gate), _f64(w_up), _f64(w_down)
@@ -364,8 +362,8 @@ def layer_backward(x, router_w, top_experts, w_gate, w_up, w_down, dy,
         du = dh * gc * sg
         if swiglu_limit and swiglu_limit > 0:         # the clamp's own derivative
             lim = float(np.float32(swiglu_limit))
-            dg = dg * (round_bf16(g) <= lim)
-            du = du * (np.abs(round_bf16(u)) <= lim)
+            dg = dg * (g <= lim)
+            du = du * (np.abs(u) <= lim)
         dWg = dg.T @ v
         dWu = du.T @ v
         dv = dg @ Wg + du @ Wu

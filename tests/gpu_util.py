@@ -128,3 +128,48 @@ def shared_slice_inputs(inp, i0, i1):
     return gen.LayerInputs(inp.x.cpu(), inp.router_w.cpu(), inp.top_experts.cpu(), e0, inp.w_up[:0].cpu(),
                            inp.w_down[:0].cpu(), inp.ws_gate[i0:i1].cpu(), inp.ws_up[i0:i1].cpu(),
                            inp.ws_down[:, i0:i1].contiguous().cpu(), inp.dy.cpu(), dict(inp.meta))
+
+
+def gate_up_preactivations(inp, mode="bf16"):
+    """Every gate and |up| pre-activation value the layer's forward forms
+    (float64; those of the quantised forward in the MXFP8 modes), sorted."""
+    x = inp.x.double().numpy()
+    quant = mode in ("mxfp8", "mxfp8_full")
+    q = oracle.mxfp8_roundtrip if quant else (lambda a: a)
+    xq = q(x)
+    te = inp.top_experts.numpy()
+    vals = []
+    for e in range(inp.w_gate.shape[0]):
+        rows = np.nonzero((te == e).any(axis=1))[0]
+        if rows.size == 0:
+            continue
+        vals.append((xq[rows] @ q(inp.w_gate[e].double().numpy()).T).ravel())
+        vals.append(np.abs(xq[rows] @ q(inp.w_up[e].double().numpy()).T).ravel())
+    if inp.ws_gate is not None:
+        vals.append((xq @ q(inp.ws_gate.double().numpy()).T).ravel())
+        vals.append(np.abs(xq @ q(inp.ws_up.double().numpy()).T).ravel())
+    return np.sort(np.concatenate(vals))
+
+
+def clamp_limit(inp, mode="bf16", lo_q=0.5, hi_q=0.8):
+    """A swiglu_limit for parity tests: a midpoint between two consecutive
+    bf16 values (so a value and its bf16 rounding fall on the same side of
+    it), inside the given quantile range of the pre-activations, chosen as
+    far as possible from every pre-activation value.  The kernels decide the
+    clamp's derivative on bf16-rounded fp32 pre-activations and the oracle on
+    float64 ones; at such a limit the two decisions agree unless a value lies
+    within the fp32 accumulation error of the limit.  Returns (limit,
+    distance to the nearest value)."""
+    vals = gate_up_preactivations(inp, mode)
+    lo, hi = np.quantile(vals, lo_q), np.quantile(vals, hi_q)
+    assert lo > 0
+    b0 = int(np.float32(lo).view(np.uint32)) >> 16
+    b1 = int(np.float32(hi).view(np.uint32)) >> 16
+    bf = (np.arange(b0, b1 + 2, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
+    mids = 0.5 * (bf[:-1] + bf[1:])              # exact in float32
+    pos = np.searchsorted(vals, mids)
+    left = np.abs(mids - vals[np.clip(pos - 1, 0, len(vals) - 1)])
+    right = np.abs(vals[np.clip(pos, 0, len(vals) - 1)] - mids)
+    gap = np.minimum(left, right)
+    i = int(np.argmax(gap))
+    return float(np.float32(mids[i])), float(gap[i])

@@ -52,6 +52,9 @@ def _check_pairs(arr, ref):
     (65536, 8, 256, None, 0.5),        # large layer
     (1, 1, 1, None, 0.5), (5, 3, 7, None, 0.0), (4097, 5, 1000, None, 0.5), (3000, 16, 64, 1.2, 0.01),
     (8192, 8, 64, 1.2, 0.5), (65537, 1, 16, 1.2, 0.5),
+    # multipliers that float32 cannot hold, where c*T lands on a whole tile in
+    # double precision but just above it in float32 (the tile order differs)
+    (2560, 8, 16, 1.2, 0.05), (1280, 8, 16, 1.2, 0.1), (1280, 4, 32, 1.2, 0.3), (640, 8, 16, 1.2, 0.6),
 ])
 def test_schedule_bit_exact(T, k, E, skew, c):
     te = gen.make_routing(T, k, E, seed=T + E, skew=skew)

@@ -239,3 +239,30 @@ def test_ctypes_structs_match_the_c_header(tmp_path):
         assert got[(cname, "sizeof")] == C.sizeof(cls), cname
         for field, _ in cls._fields_:
             assert got[(cname, field)] == getattr(cls, field).offset, (cname, field)
+
+
+def test_schedule_calls_take_the_multiplier_as_double(tmp_path):
+    """The two schedule builds take capacity_multiplier as a C double (so c*T
+    is rounded up on exactly the caller's value), and the binding passes one:
+    a C99 translation unit assigns each declaration to a pointer of the
+    expected type, which -Werror turns into an error on any mismatch."""
+    import shutil
+    import subprocess
+
+    from mixture_experts_layer_mok_gb300 import _lib
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "sig.c"
+    src.write_text("\n".join([
+        '#include "mok.h"',
+        "typedef mok_status_t (*sched_fn)(const int64_t*, int, int, int, double, void*, size_t,",
+        "                                 mok_schedule_t*, void*);",
+        "sched_fn a = mok_schedule;",
+        "sched_fn b = mok_schedule_noalloc;",
+        "int main(void) { return a == b; }", ""]))
+    subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), "-c", str(src), "-o",
+                    str(tmp_path / "sig.o")], check=True, capture_output=True)
+    for name in ("mok_schedule", "mok_schedule_noalloc"):
+        assert _lib.SIGNATURES[name][1][4] is C.c_double, name

@@ -397,6 +397,111 @@ def test_mxfp8_backward_equals_bf16_backward_on_grid_inputs():
         np.testing.assert_allclose(a[key], b[key], rtol=1e-12, atol=1e-14)
 
 
+def _brute_mxfp8_backward(inp):
+    """The straight-through backward of the MXFP8 forward, token by token in
+    plain Python floats: the gate/up pre-activations from the brute-force
+    quantised x and gate/up weight rows; everything after them (the SwiGLU
+    derivative, dx, the weight gradients, <dy, F(x)>) with the bf16 weights
+    and the unquantised x."""
+    x = inp.x.double().tolist()
+    dy = inp.dy.double().tolist()
+    rw = inp.router_w.double().tolist()
+    te = inp.top_experts.tolist()
+    T, H, k = len(x), len(x[0]), len(te[0])
+    E, I = inp.w_gate.shape[0], inp.w_gate.shape[1]
+    out = {"dx": [[0.0] * H for _ in range(T)], "d_router_w": [[0.0] * k for _ in range(T)],
+           "d_w_gate": np.zeros((E, I, H)), "d_w_up": np.zeros((E, I, H)), "d_w_down": np.zeros((E, H, I))}
+    if inp.ws_gate is not None:
+        Is = inp.ws_gate.shape[0]
+        out.update(d_ws_gate=np.zeros((Is, H)), d_ws_up=np.zeros((Is, H)), d_ws_down=np.zeros((H, Is)))
+    qcache = {}
+
+    def qrows(key, m):
+        if key not in qcache:
+            qcache[key] = [list(_brute_q(np.asarray(r))) for r in m]
+        return qcache[key]
+
+    def expert(t, key, wg, wu, wd, scale, dWg, dWu, dWd):
+        xq = list(_brute_q(np.asarray(x[t])))
+        qg, qu = qrows((key, "g"), wg), qrows((key, "u"), wu)
+        n_i = len(wg)
+        g = [sum(a * b for a, b in zip(qg[i], xq)) for i in range(n_i)]
+        u = [sum(a * b for a, b in zip(qu[i], xq)) for i in range(n_i)]
+        sg = [1.0 / (1.0 + math.exp(-v)) for v in g]
+        h = [g[i] * sg[i] * u[i] for i in range(n_i)]
+        dot = sum(dy[t][r] * sum(wd[r][i] * h[i] for i in range(n_i)) for r in range(H))
+        for i in range(n_i):
+            z = sum(wd[r][i] * dy[t][r] for r in range(H))
+            dh = scale * z
+            dg = dh * u[i] * sg[i] * (1.0 + g[i] * (1.0 - sg[i]))
+            du = dh * g[i] * sg[i]
+            for c in range(H):
+                out["dx"][t][c] += dg * wg[i][c] + du * wu[i][c]
+                dWg[i, c] += dg * x[t][c]
+                dWu[i, c] += du * x[t][c]
+                dWd[c, i] += scale * dy[t][c] * h[i]
+        return dot
+
+    for t in range(T):
+        if inp.ws_gate is not None:
+            expert(t, "s", inp.ws_gate.double().tolist(), inp.ws_up.double().tolist(),
+                   inp.ws_down.double().tolist(), 1.0, out["d_ws_gate"], out["d_ws_up"], out["d_ws_down"])
+        for j in range(k):
+            e = te[t][j]
+            out["d_router_w"][t][j] = expert(
+                t, e, inp.w_gate[e].double().tolist(), inp.w_up[e].double().tolist(),
+                inp.w_down[e].double().tolist(), rw[t][j], out["d_w_gate"][e], out["d_w_up"][e], out["d_w_down"][e])
+    return {key: np.asarray(v) for key, v in out.items()}
+
+
+def test_mxfp8_backward_matches_per_token_brute_force():
+    """The MXFP8-forward layer's BF16 backward (straight-through, taken at the
+    quantised forward's pre-activations) against its per-token restatement."""
+    inp = _tiny(T=4, H=64, I=32, E=3, k=2, I_s=32, seed=14)
+    got = O.layer_backward_mxfp8(*_args(inp)[:6], inp.dy, *_args(inp)[6:])
+    ref = _brute_mxfp8_backward(inp)
+    assert set(got) == set(ref)
+    for key in ref:
+        np.testing.assert_allclose(got[key], ref[key], rtol=1e-9, atol=1e-13, err_msg=key)
+
+
+def test_mxfp8_backward_pin_rejects_other_evaluation_points():
+    """Planted mistakes, in copies of the oracle's MXFP8 backward: the
+    derivative taken at the unquantised pre-activations, or with only x or
+    only the weights quantised.  Each must miss the per-token restatement."""
+    inp = _tiny(T=4, H=64, I=32, E=3, k=2, I_s=32, seed=14)
+    ref = _brute_mxfp8_backward(inp)
+    a = _args(inp)
+    wg, wu = inp.w_gate.double().numpy(), inp.w_up.double().numpy()
+    sg, su = inp.ws_gate.double().numpy(), inp.ws_up.double().numpy()
+
+    def mutant(qx, qw):
+        def gu(e, v):
+            vv = O.mxfp8_roundtrip(v) if qx else v
+            mg, mu = (sg, su) if e is None else (wg[e], wu[e])
+            if qw:
+                mg, mu = O.mxfp8_roundtrip(mg), O.mxfp8_roundtrip(mu)
+            return vv @ mg.T, vv @ mu.T
+        return O.layer_backward(*a[:6], inp.dy, *a[6:], gu_override=gu)
+
+    for qx, qw in ((False, False), (True, False), (False, True)):
+        bad = mutant(qx, qw)
+        assert not np.allclose(bad["dx"], ref["dx"], rtol=1e-6, atol=1e-9), (qx, qw)
+    # the same construction with both quantised passes (the copies are faithful)
+    good = mutant(True, True)
+    for key in ref:
+        np.testing.assert_allclose(good[key], ref[key], rtol=1e-9, atol=1e-13, err_msg=key)
+
+
+def test_capacity_budget_is_rounded_up_in_double_precision():
+    """c*T rounded up on the float64 value of the multiplier: 0.05 * 2560 is
+    128 rows (one tile), although float32(0.05) * 2560 is just above 128."""
+    assert O.capacity_tiles(2560, 0.05, 1000) == 1
+    assert O.capacity_tiles(1280, 0.3, 1000) == 3
+    assert O.capacity_tiles(2560, 0.0501, 1000) == 2
+    assert O.capacity_tiles(100, 50.0, 7) == 7          # never above the tile bound
+
+
 def test_mxfp8_forward_close_to_unquantised():
     inp = _tiny(T=32, H=64, I=64, E=4, k=2, seed=12)
     a = O.layer_forward_mxfp8(*_args(inp))
@@ -424,10 +529,10 @@ def _gate_up_values(inp):
 
 
 def _limit_between(vals, lo_q=0.6, hi_q=0.9):
-    """A limit in a gap between consecutive values of the given quantile
-    range, the widest one where every value and its bf16 rounding fall on
-    the same side of the limit (the backward's clamp decisions are taken on
-    bf16 values); returns the limit and the distance to the nearest value."""
+    """A limit in the widest gap between consecutive values of the given
+    quantile range (so a central difference never crosses a clamp kink),
+    where moreover every value and its bf16 rounding fall on the same side of
+    the limit; returns the limit and the distance to the nearest value."""
     a = vals[int(lo_q * len(vals)):int(hi_q * len(vals))]
     for i in np.argsort(-np.diff(a)):
         L = float(np.float32(0.5 * (a[i] + a[i + 1])))

@@ -5,8 +5,8 @@ framework's fixed memory pool, or a loop that must not call cudaMalloc
 because it can synchronise the device.  For them the library takes the
 schedule build's scratch from its own fixed device array.  This file checks,
 through the C ABI, that the result matches mok_schedule() bit for bit on two
-calls in a row (the second runs over the first's leftover scratch), and that
-sizes beyond the array's limit are refused.  It sits last in collection order
+calls in a row, over scratch that earlier calls left behind, and that sizes
+beyond the array's limit are refused.  It sits last in collection order
 so a stop-at-first-failure run has already run every other test.
 """
 import ctypes as C
@@ -53,14 +53,21 @@ def _build(fn_name, te, E, c):
 
 
 def test_noalloc_schedule_matches_mok_schedule_on_two_calls_in_a_row():
-    cases = [(4096, 8, 64, None, 0.5, 1), (16384, 8, 128, 1.2, 0.5, 2)]
+    """Each case builds the schedule with mok_schedule(), then twice in a row
+    with mok_schedule_noalloc(); both must match bit for bit.  The first case
+    has the largest histogram footprint (128 chunks x 128 experts), so every
+    later build runs over entries an earlier call left behind, and the last
+    case repeats that footprint with other routing."""
+    cases = [(16384, 8, 128, 1.2, 0.5, 2), (4096, 8, 64, None, 0.5, 1), (2560, 8, 16, 1.2, 0.05, 3),
+             (16384, 8, 128, 1.2, 1.0, 4)]
     for T, k, E, skew, c, seed in cases:
         te = gen.make_routing(T, k, E, seed=seed, skew=skew).cuda()
         ref = _build("mok_schedule", te, E, c)
-        got = _build("mok_schedule_noalloc", te, E, c)
-        for name in ARRAYS:
-            assert np.array_equal(got[name], ref[name]), (T, E, name)
-        assert got["header"][2] == 0
+        for call in range(2):
+            got = _build("mok_schedule_noalloc", te, E, c)
+            for name in ARRAYS:
+                assert np.array_equal(got[name], ref[name]), (T, E, call, name)
+            assert got["header"][2] == 0
 
 
 def test_noalloc_schedule_rejects_sizes_beyond_its_scratch():
