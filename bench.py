@@ -29,7 +29,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-DEFAULT_WORKLOAD = "bf16_T4096"
+DEFAULT_WORKLOAD = "large_T65536"
 METRIC = "MoE layer fwd+bwd tokens/s (TFLOP/s and % of GB300 dense tensor peak alongside)"
 L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
 
@@ -207,42 +207,111 @@ class ClockSampler:
 
 # ----------------------------------------------------------------- oracle timing
 class OracleSample:
-    """The CPU oracle (float64 NumPy) on fwd+bwd of the first `tokens` tokens of
-    the workload.  Inputs and weights are widened to float64 once, here, so the
-    timed calls run the oracle's arithmetic only."""
+    """The CPU oracle (float64 NumPy) timed on units of the workload that
+    together make up a whole layer, each with the amortisation it has in a
+    whole-layer run:
 
-    def __init__(self, inp, mode, tokens):
+    - a routed unit is forward + backward of one expert over the rows routed
+      to it (a k = 1 layer over those rows with their router weights; at most
+      ``max_rows`` of them).  In the MXFP8 modes the oracle quantises the
+      expert's weights inside the call, once per unit, as a whole-layer call
+      does once per expert;
+    - a shared unit is the shared expert alone over as many tokens.
+
+    A token costs k routed rows and one shared row, so tokens/s =
+    1 / (k * s_routed + s_shared), with s_* the measured seconds per row of
+    each kind.  Units run one shared to k routed (experts in turn).  Each
+    unit's inputs are cut out and widened to float64 before its timed call."""
+
+    def __init__(self, inp, mode, max_rows):
         import oracle
 
-        self.tokens = tokens
-        self.x = inp.x[:tokens].double().numpy()
-        self.w = inp.router_w[:tokens].double().numpy()
-        self.te = inp.top_experts[:tokens].numpy()
-        self.dy = inp.dy[:tokens].double().numpy()
-        self.W = [None if t is None else t.double().numpy() for t in
-                  (inp.w_gate, inp.w_up, inp.w_down, inp.ws_gate, inp.ws_up, inp.ws_down)]
+        self.inp = inp
+        self.k = inp.top_experts.shape[1]
+        self.E = inp.w_gate.shape[0]
+        self.shared = inp.ws_gate is not None
+        self.max_rows = max_rows
         self.fwd = oracle.layer_forward_mxfp8 if mode in ("mxfp8", "mxfp8_full") else oracle.layer_forward
         self.bwd = {"mxfp8": oracle.layer_backward_mxfp8,
                     "mxfp8_full": oracle.layer_backward_mxfp8_full}.get(mode, oracle.layer_backward)
+        te = inp.top_experts
+        self.cnt = torch_bincount(te, self.E)
+        self.next_e = 0
+        self.n = 0                       # units run so far (decides the next unit's kind)
+        self.reset()
 
-    def run(self, min_s=0.0):
-        """Repeat fwd+bwd until at least min_s seconds passed; returns (seconds, reps)."""
-        W = self.W
-        reps, t0 = 0, time.perf_counter()
-        while True:
-            self.fwd(self.x, self.w, self.te, *W)
-            self.bwd(self.x, self.w, self.te, W[0], W[1], W[2], self.dy, W[3], W[4], W[5])
-            reps += 1
-            el = time.perf_counter() - t0
-            if el >= min_s:
-                return el, reps
+    def reset(self):
+        """Forget the units timed so far (the unit cycle goes on)."""
+        self.time = {"routed": 0.0, "shared": 0.0}
+        self.rows = {"routed": 0, "shared": 0}
+        self.units = {"routed": 0, "shared": 0}
+
+    @staticmethod
+    def _np(t):
+        return None if t is None else t.detach().to("cpu").double().numpy()
+
+    def _routed_unit(self):
+        while self.cnt[self.next_e] == 0:
+            self.next_e = (self.next_e + 1) % self.E
+        e = self.next_e
+        self.next_e = (e + 1) % self.E
+        inp = self.inp
+        t_e, j_e = (v[:self.max_rows] for v in (inp.top_experts == e).nonzero(as_tuple=True))
+        n = int(t_e.numel())
+        args = (self._np(inp.x[t_e]), self._np(inp.router_w[t_e, j_e].reshape(-1, 1)),
+                __import__("numpy").zeros((n, 1), dtype="int64"), self._np(inp.w_gate[e:e + 1]),
+                self._np(inp.w_up[e:e + 1]), self._np(inp.w_down[e:e + 1]), None, None, None)
+        return "routed", n, args, self._np(inp.dy[t_e])
+
+    def _shared_unit(self):
+        import numpy as np
+
+        inp = self.inp
+        n = min(self.max_rows, inp.x.shape[0])
+        e0 = np.zeros((0,) + tuple(inp.w_gate.shape[1:]))
+        d0 = np.zeros((0,) + tuple(inp.w_down.shape[1:]))
+        args = (self._np(inp.x[:n]), np.zeros((n, 0)), np.zeros((n, 0), dtype=np.int64), e0, e0, d0,
+                self._np(inp.ws_gate), self._np(inp.ws_up), self._np(inp.ws_down))
+        return "shared", n, args, self._np(inp.dy[:n])
+
+    def run_unit(self):
+        """One unit (the next in the 1 shared : k routed cycle, shared first);
+        returns its seconds."""
+        shared = self.shared and self.n % (self.k + 1) == 0
+        kind, n, a, dy = self._shared_unit() if shared else self._routed_unit()
+        t0 = time.perf_counter()
+        self.fwd(*a)
+        self.bwd(*a[:6], dy, *a[6:])
+        el = time.perf_counter() - t0
+        self.n += 1
+        self.time[kind] += el
+        self.rows[kind] += n
+        self.units[kind] += 1
+        return el
+
+    def tokens_per_s(self):
+        s_r = self.time["routed"] / max(self.rows["routed"], 1)
+        s_s = self.time["shared"] / self.rows["shared"] if self.rows["shared"] else 0.0
+        return 1.0 / (self.k * s_r + s_s)
+
+    def describe(self):
+        d = (f"{self.units['routed']} routed units (one expert each over at most {self.max_rows} of the rows "
+             f"routed to it; {self.rows['routed']} rows in {self.time['routed']:.1f} s)")
+        if self.shared:
+            d += (f" and {self.units['shared']} shared units (the shared expert over {self.max_rows} tokens; "
+                  f"{self.rows['shared']} rows in {self.time['shared']:.1f} s)")
+        return d + ", float64 NumPy; tokens/s = 1 / (k * s_routed_row + s_shared_row)"
 
 
-# Tokens per oracle sample.  In the MXFP8 modes each call quantises the weights
-# of every expert the sample touches (several 2 M-element matrices each), so a
-# handful of tokens already costs seconds on the host.
-CPU_SAMPLE_TOKENS = {"bf16": 64, "mxfp8": 2, "mxfp8_full": 1}
-REF_STEP_TOKENS = {"bf16": 16, "mxfp8": 2, "mxfp8_full": 1}
+def torch_bincount(te, E):
+    import torch
+
+    return torch.bincount(te.reshape(-1).to("cpu"), minlength=E).tolist()
+
+
+# Rows per oracle unit: at most this many of an expert's rows (the T=4096
+# layers route about 512 rows to an expert, the large layer about 2048).
+CPU_UNIT_ROWS = 1024
 
 
 def cpu_cores():
@@ -285,7 +354,8 @@ def main():
               "minibatch": c["minibatch"], "capacity_multiplier": c["capacity"],
               "fwd_precision": "bf16" if c["mode"] == "bf16" else "mxfp8",
               "bwd_precision": "mxfp8" if c["mode"] == "mxfp8_full" else "bf16", "global_batch_tokens": c["T"] * max(world, 1),
-              "parallelism": f"dp{world} (independent batches, no collective)"}
+              "parallelism": f"dp{world} (independent batches, no collective)",
+              "l2": "flushed between steps (512 MiB write, outside the timed spans)"}
 
     if args.impl == "reference":
         return run_reference(args, c, config, rank, world)
@@ -492,19 +562,15 @@ def main():
         return
 
     cpu = None
-    if world == 1 and not args.no_cpu_baseline and big:
-        cpu = {"value": None, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
-               "sample": "skipped: the float64 oracle would widen more than 3e8 weight elements per expert set"}
-    elif world == 1 and not args.no_cpu_baseline:
-        tokens = CPU_SAMPLE_TOKENS[mode]
-        sample = OracleSample(inp, mode, tokens)
-        sample.run()                                    # first touch of the widened weights
-        el, reps = sample.run(min_s=10.0)
+    if world == 1 and not args.no_cpu_baseline:
+        sample = OracleSample(inp, mode, CPU_UNIT_ROWS)
+        need = 1 + (1 if sample.shared else 0)        # at least one unit of each kind
+        el = 0.0
+        while el < 10.0 or sample.n < need:
+            el += sample.run_unit()
+        cpu = {"value": round(sample.tokens_per_s(), 3), "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"{args.workload} layer: " + sample.describe()}
         del sample
-        cpu = {"value": round(tokens * reps / el, 2), "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
-               "sample": f"fwd+bwd of the first {tokens} tokens of the {args.workload} layer (all experts' "
-                         f"weights, float64 NumPy), {reps} repetition(s), {el:.1f} s; weights widened once "
-                         "outside the timing"}
 
     # a kernel timed inside a long step runs at the sustained (power-capped)
     # rate; one inside a short step at the burst rate
@@ -525,7 +591,7 @@ def main():
         "scaling": "weak", "vs_baseline": None,
         "dtype": {"bf16": "bf16", "mxfp8": "mxfp8-fwd/bf16-bwd"}.get(mode, "mxfp8-fwd/mxfp8-bwd"),
         "data": "synthetic (seeded; weights N(0,0.02), x and dy N(0,1), softmax top-k routing)",
-        "config": dict(config, l2="flushed between steps (512 MiB write, outside the timed spans)"),
+        "config": config,
         "tflops": round(tflops, 1),
         "tc_peak_frac": round(tflops / peaks[peak_key], 4),
         "gemm_tflops": round(gemm_tflops, 1),
@@ -549,31 +615,42 @@ def main():
 
 
 def run_reference(args, c, config, rank, world):
-    """The CPU oracle as the reference arm: each step is fwd+bwd of a bounded
-    sample of tokens of the same workload, on the host cores."""
+    """The CPU oracle as the reference arm: each step is one oracle unit of the
+    same workload (see OracleSample) on the host cores; tokens/s follows from
+    the per-row times of the units run in the timed steps."""
     if rank != 0:
         return
     from mixture_experts_layer_mok_gb300 import inputs as gen
 
-    inp = gen.make_workload(args.workload, seed=0)
-    tokens = REF_STEP_TOKENS[c["mode"]]
-    sample = OracleSample(inp, c["mode"], tokens)
+    dev = "cpu"
+    if c["E"] * c["I"] * c["H"] > 3e8:   # the same seeded draw as the measured arm (on the GPU), cut up on the host
+        import torch
+
+        if torch.cuda.is_available():
+            dev = torch.device("cuda", 0)
+    inp = gen.make_workload(args.workload, seed=0, device=dev)
+    sample = OracleSample(inp, c["mode"], CPU_UNIT_ROWS)
     for _ in range(args.warmup):
-        sample.run()
+        sample.run_unit()
+    warm = (dict(sample.time), dict(sample.rows), dict(sample.units))
+    sample.reset()
     el_total = 0.0
     for _ in range(args.steps):
-        el, _ = sample.run()
-        el_total += el
-    value = tokens * args.steps / el_total
-    sample = (f"each step: fwd+bwd of the first {tokens} tokens of the {args.workload} layer in the float64 NumPy "
-              "oracle (weights widened once, outside the timing)")
+        el_total += sample.run_unit()
+    if sample.rows["routed"] == 0 or (sample.shared and sample.rows["shared"] == 0):
+        # too few timed steps for both kinds: take the missing kind from the warm-up units
+        for kind in sample.time:
+            if sample.rows[kind] == 0:
+                sample.time[kind], sample.rows[kind], sample.units[kind] = (w[kind] for w in warm)
+    value = sample.tokens_per_s()
+    desc = f"{args.workload} layer, each timed step one oracle unit: " + sample.describe()
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 3),
-            "unit": "tokens/s", "n_gpus": world, "device": "host cores only (rank 0; no GPU work)",
+            "unit": "tokens/s", "n_gpus": world, "device": "host cores only (rank 0; the oracle does no GPU work)",
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * el_total / args.steps, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)", "config": config,
             "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
-                             "sample": sample},
+                             "sample": desc},
             "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 

@@ -121,15 +121,6 @@ def expert_slice_inputs(inp, e, i0, i1):
                            inp.dy[t_e].cpu(), dict(inp.meta)), t_e.to(dev)
 
 
-def shared_slice_inputs(inp, i0, i1):
-    """All tokens through the shared expert only, intermediate columns
-    [i0, i1): gives the matching slices of the shared weight gradients."""
-    e0 = inp.w_gate[:0].cpu()
-    return gen.LayerInputs(inp.x.cpu(), inp.router_w.cpu(), inp.top_experts.cpu(), e0, inp.w_up[:0].cpu(),
-                           inp.w_down[:0].cpu(), inp.ws_gate[i0:i1].cpu(), inp.ws_up[i0:i1].cpu(),
-                           inp.ws_down[:, i0:i1].contiguous().cpu(), inp.dy.cpu(), dict(inp.meta))
-
-
 def gate_up_preactivations(inp, mode="bf16"):
     """Every gate and |up| pre-activation value the layer's forward forms
     (float64; those of the quantised forward in the MXFP8 modes), sorted."""

@@ -70,25 +70,17 @@ def test_mxfp8_full_backward_matches_same_quantisation_oracle(name):
     assert not bad, errs
 
 
-def test_mxfp8_full_repeated_runs_bitwise_identical():
-    inp = _inputs("wide", seed=10)
-    a = run_layer(inp, "mxfp8_full")
-    b = run_layer(inp, "mxfp8_full")
+@pytest.mark.parametrize("mode,seed", [("bf16", 2), ("mxfp8", 11), ("mxfp8_full", 10)])
+def test_repeated_runs_bitwise_identical(mode, seed):
+    inp = _inputs("wide", seed=seed)
+    a = run_layer(inp, mode)
+    b = run_layer(inp, mode)
     assert torch.equal(a[0], b[0])
     for key in a[1]:
         assert torch.equal(a[1][key], b[1][key]), key
 
 
-def test_repeated_runs_bitwise_identical():
-    inp = _inputs("wide", seed=2)
-    a = run_layer(inp, "bf16")
-    b = run_layer(inp, "bf16")
-    assert torch.equal(a[0], b[0])
-    for key in a[1]:
-        assert torch.equal(a[1][key], b[1][key]), key
-
-
-@pytest.mark.parametrize("mode", ["bf16", "mxfp8_full"])
+@pytest.mark.parametrize("mode", ["bf16", "mxfp8", "mxfp8_full"])
 def test_capacity_and_minibatch_change_no_bit(mode):
     inp = _inputs("skewed", seed=3)
     base = run_layer(inp, mode, capacity=1.0, minibatch=0)
