@@ -335,9 +335,15 @@ def main():
     ap.add_argument("--stages", action="store_true", help="print per-stage times to stderr")
     ap.add_argument("--capacity", type=float, default=None, help="override the workload's capacity multiplier")
     ap.add_argument("--minibatch", type=int, default=None, help="override the workload's minibatch size")
+    ap.add_argument("--dispatch", choices=["auto", "permute", "fused"], default="auto",
+                    help="how the bf16 GEMMs receive token rows (same results)")
+    ap.add_argument("--debug-flags", type=int, default=0,
+                    help="MOK_DEBUG_* flags that change kernel choices only (e.g. 4: single CTAs, 8: MXFP8 CTA pairs)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.debug_flags & 1:
+        ap.error("--debug-flags 1 withholds a GEMM signal (a timeout test), not a kernel choice")
 
     rank, world, local = dist_env()
 
@@ -356,6 +362,8 @@ def main():
               "bwd_precision": "mxfp8" if c["mode"] == "mxfp8_full" else "bf16", "global_batch_tokens": c["T"] * max(world, 1),
               "parallelism": f"dp{world} (independent batches, no collective)",
               "l2": "flushed between steps (512 MiB write, outside the timed spans)"}
+    if args.dispatch != "auto" or args.debug_flags:
+        config.update(dispatch=args.dispatch, debug_flags=args.debug_flags)
 
     if args.impl == "reference":
         return run_reference(args, c, config, rank, world)
@@ -404,9 +412,10 @@ def main():
         if prep_events:
             prep_events[1].record()
         _, ctx = mok.forward(x, rw, sched, wq, mode=mode, minibatch=c["minibatch"],
-                             out=y if y_out is None else y_out, ctx_buf=ctx_buf, events=events)
+                             out=y if y_out is None else y_out, ctx_buf=ctx_buf, events=events,
+                             dispatch=args.dispatch, debug=args.debug_flags)
         mok.backward(dy, x, rw, sched, ctx, wq, minibatch=c["minibatch"], grads=grads if g_out is None else g_out,
-                     ws_buf=ws_buf, events=events)
+                     ws_buf=ws_buf, events=events, dispatch=args.dispatch, debug=args.debug_flags)
         return ctx
 
     for _ in range(args.warmup):

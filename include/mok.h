@@ -85,11 +85,14 @@ typedef int mok_status_t;
 #define MOK_DEBUG_NO_CTA_PAIR     4  /* run every bf16 GEMM on single CTAs instead
                                         of CTA pairs (M = 256 over two SMs
                                         sharing B; same results; for comparison) */
-#define MOK_DEBUG_MX_CTA_PAIR     8  /* run the block-scaled MXFP8 GEMMs as CTA
-                                        pairs too (same results; measured slower
-                                        on one GB300: their accumulator is
-                                        single-buffered, so each tile waits for
-                                        both CTAs' epilogues) */
+#define MOK_DEBUG_MX_CTA_PAIR     8  /* run the block-scaled MXFP8 forward GEMMs as
+                                        CTA pairs with 256-wide tiles (same results;
+                                        measured slower on one GB300: their
+                                        accumulator is single-buffered, so each
+                                        tile waits for both CTAs' epilogues) */
+#define MOK_DEBUG_MX_PAIR128     16  /* run the block-scaled MXFP8 forward GEMMs as
+                                        CTA pairs with 128-wide tiles and a
+                                        double-buffered accumulator (same results) */
 
 /* Stages of the layer, for optional per-stage timing events. */
 #define MOK_STAGE_FWD_PREP                 0  /* status hand-over; MXFP8: weight scales into the tensor-core layout */

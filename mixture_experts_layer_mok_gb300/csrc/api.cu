@@ -280,8 +280,10 @@ size_t carve_ctx(void* buf, int T, int k, int E, int H, int I, int Is, int mode,
     ctx->xq_perm_sc = c.take<uint8_t>(tiled_scale_bytes(mr, H));
     ctx->hq = c.take<uint8_t>(mr * I);
     ctx->hq_sc = c.take<uint8_t>(tiled_scale_bytes(mr, I));
-    X->wg_sc = c.take<uint8_t>(tiled_scale_bytes(static_cast<long long>(E) * I, H));
-    X->wu_sc = c.take<uint8_t>(tiled_scale_bytes(static_cast<long long>(E) * I, H));
+    // gate and up scales back to back: the CTA-pair 128-wide SwiGLU GEMM reads
+    // the same bytes as one interleaved gate|up tensor of 2 E I rows
+    X->wg_sc = c.take<uint8_t>(2 * tiled_scale_bytes(static_cast<long long>(E) * I, H));
+    X->wu_sc = X->wg_sc ? X->wg_sc + tiled_scale_bytes(static_cast<long long>(E) * I, H) : nullptr;
     X->wd_sc = c.take<uint8_t>(tiled_scale_bytes(static_cast<long long>(E) * H, I));
   }
   if (Is > 0) {
@@ -292,8 +294,8 @@ size_t carve_ctx(void* buf, int T, int k, int E, int H, int I, int Is, int mode,
     } else {
       ctx->hq_s = c.take<uint8_t>(static_cast<long long>(T) * Is);
       ctx->hq_s_sc = c.take<uint8_t>(tiled_scale_bytes(T, Is));
-      X->wsg_sc = c.take<uint8_t>(tiled_scale_bytes(Is, H));
-      X->wsu_sc = c.take<uint8_t>(tiled_scale_bytes(Is, H));
+      X->wsg_sc = c.take<uint8_t>(2 * tiled_scale_bytes(Is, H));
+      X->wsu_sc = X->wsg_sc ? X->wsg_sc + tiled_scale_bytes(Is, H) : nullptr;
       X->wsd_sc = c.take<uint8_t>(tiled_scale_bytes(H, Is));
     }
   }
@@ -675,6 +677,11 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
   const int T = s->T, k = s->k, E = s->E, H = w->H, I = w->I, Is = w->I_s;
   const long long mr = static_cast<long long>(s->max_tiles) * kTileRows;
   mok_status_t st;
+  // Tiling of the block-scaled GEMMs: single CTAs with 256-wide tiles (the
+  // accumulator single-buffered beside the scale ring), or CTA pairs (M = 256)
+  // with 256-wide tiles (single-buffered) or 128-wide tiles (double-buffered;
+  // the gate/up weights' scales then go into the interleaved gate|up layout).
+  const int tiling = (cfg->debug_flags & MOK_DEBUG_MX_CTA_PAIR) ? 1 : (cfg->debug_flags & MOK_DEBUG_MX_PAIR128) ? 2 : 0;
   // weight scales into the tensor-core layout on a side stream, while x is
   // quantised once per token into token order and schedule order
   SideStream* side = nullptr;
@@ -683,13 +690,14 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
   MOK_CUDA(cudaStreamWaitEvent(side->s, side->fork, 0));
   {
     const long long sr = Is > 0 ? 1 : 0;   // the shared expert's jobs are skipped without one
+    const int gu = tiling == 2 ? 1 : 0;    // interleaved gate|up scales for the 128-wide pairs
     const MxTileScaleJob jobs[] = {
-        {w->mx_gate_sc, static_cast<long long>(E) * I, H, X.wg_sc},
-        {w->mx_up_sc, static_cast<long long>(E) * I, H, X.wu_sc},
-        {w->mx_down_sc, static_cast<long long>(E) * H, I, X.wd_sc},
-        {w->mxs_gate_sc, sr * Is, H, X.wsg_sc},
-        {w->mxs_up_sc, sr * Is, H, X.wsu_sc},
-        {w->mxs_down_sc, sr * H, Is, X.wsd_sc}};
+        {w->mx_gate_sc, static_cast<long long>(E) * I, H, X.wg_sc, gu, I},
+        {w->mx_up_sc, static_cast<long long>(E) * I, H, gu ? X.wg_sc : X.wu_sc, 2 * gu, I},
+        {w->mx_down_sc, static_cast<long long>(E) * H, I, X.wd_sc, 0, 0},
+        {w->mxs_gate_sc, sr * Is, H, X.wsg_sc, gu, Is},
+        {w->mxs_up_sc, sr * Is, H, gu ? X.wsg_sc : X.wsu_sc, 2 * gu, Is},
+        {w->mxs_down_sc, sr * H, Is, X.wsd_sc, 0, 0}};
     MOK_CUDA(launch_mx_tile_scales(jobs, 6, side->s));
   }
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_PREP, 1, side->s));
@@ -702,51 +710,74 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
   MOK_CUDA(cudaStreamWaitEvent(cs, side->join, 0));
 
   const int bn = tile_n(H);
-  // CTA pairs only on request here (MOK_DEBUG_MX_CTA_PAIR): with the
-  // single-buffered accumulator they measured slower than single CTAs
-  const bool mx_pair = (cfg->debug_flags & MOK_DEBUG_MX_CTA_PAIR) != 0;
-  const bool pr = mx_pair && bn == 256;    // the down GEMMs; gate/up tiles are always 256 wide
-  const bool pr_gu = mx_pair;
+  // per-CTA B rows of a gate/up tile (gate rows, then up rows, for single
+  // CTAs; one CTA of a pair holds the gate rows, the other the up rows)
+  const int gu_box = tiling == 2 ? 64 : 128;
+  const int gu_cols = tiling == 2 ? 64 : 128;          // h columns per gate/up tile
+  // down tiles: width and per-CTA B rows
+  const int dn_bn = tiling == 2 ? 128 : bn;
+  const bool dn_pair = tiling == 2 || (tiling == 1 && bn == 256);
+  const int dn_box = dn_pair ? dn_bn / 2 : dn_bn;
   const long long t_atoms = (T + 127) / 128, r_atoms = mr / 128;   // 128-row blocks
+  // gate|up scale maps: two tensors, or one interleaved tensor of 2 * rows
+  auto gu_sf_maps = [&](MxMaps& m, const uint8_t* g_sc, const uint8_t* u_sc, long long rows) -> mok_status_t {
+    mok_status_t r;
+    if (tiling == 2) {
+      if ((r = make_map_sf(&m.sfb0, g_sc, (2 * rows / 128) * (H / 128)))) return r;
+      m.sfb1 = m.sfb0;
+      return MOK_OK;
+    }
+    if ((r = make_map_sf(&m.sfb0, g_sc, (rows / 128) * (H / 128)))) return r;
+    return make_map_sf(&m.sfb1, u_sc, (rows / 128) * (H / 128));
+  };
+  auto launch_gu = [&](const MxMaps& m, const GemmParams& p, long long items, long long pair_items) -> cudaError_t {
+    if (tiling == 2) return launch_gemm_mx_pair<128, EPI_SWIGLU_MX>(m, p, pair_items, cs);
+    if (tiling == 1) return launch_gemm_mx_pair<256, EPI_SWIGLU_MX>(m, p, pair_items, cs);
+    return launch_gemm_mx<256, EPI_SWIGLU_MX>(m, p, items < sms ? static_cast<int>(items) : sms, cs);
+  };
+  auto launch_dn = [&](int EPI_tag, const MxMaps& m, const GemmParams& p, long long items,
+                       long long pair_items) -> cudaError_t {
+    const int grid = items < sms ? static_cast<int>(items) : sms;
+    if (EPI_tag == EPI_SCALE_ROWS) {
+      if (dn_pair) return dn_bn == 128 ? launch_gemm_mx_pair<128, EPI_SCALE_ROWS>(m, p, pair_items, cs)
+                                       : launch_gemm_mx_pair<256, EPI_SCALE_ROWS>(m, p, pair_items, cs);
+      return bn == 256 ? launch_gemm_mx<256, EPI_SCALE_ROWS>(m, p, grid, cs)
+                       : launch_gemm_mx<128, EPI_SCALE_ROWS>(m, p, grid, cs);
+    }
+    if (dn_pair) return dn_bn == 128 ? launch_gemm_mx_pair<128, EPI_STORE_ROWS>(m, p, pair_items, cs)
+                                     : launch_gemm_mx_pair<256, EPI_STORE_ROWS>(m, p, pair_items, cs);
+    return bn == 256 ? launch_gemm_mx<256, EPI_STORE_ROWS>(m, p, grid, cs)
+                     : launch_gemm_mx<128, EPI_STORE_ROWS>(m, p, grid, cs);
+  };
   // ---- shared expert
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_GATEUP, 0, cs));
   if (Is > 0) {
     MxMaps m;
-    if ((st = make_map_u8(&m.a, ctx->xq, H, T, 128)) || (st = make_map_u8(&m.b0, w->mxs_gate, H, Is, 128)) ||
-        (st = make_map_u8(&m.b1, w->mxs_up, H, Is, 128)) || (st = make_map_sf(&m.sfa, ctx->xq_sc, t_atoms * (H / 128))) ||
-        (st = make_map_sf(&m.sfb0, X.wsg_sc, (Is / 128) * (H / 128))) ||
-        (st = make_map_sf(&m.sfb1, X.wsu_sc, (Is / 128) * (H / 128))))
+    if ((st = make_map_u8(&m.a, ctx->xq, H, T, 128)) || (st = make_map_u8(&m.b0, w->mxs_gate, H, Is, gu_box)) ||
+        (st = make_map_u8(&m.b1, w->mxs_up, H, Is, gu_box)) ||
+        (st = make_map_sf(&m.sfa, ctx->xq_sc, t_atoms * (H / 128))) || (st = gu_sf_maps(m, X.wsg_sc, X.wsu_sc, Is)))
       return st;
     GemmParams p = base_params(nullptr, ctx->status, 0);
-    p.rows = T; p.K = H; p.N = Is; p.n_tiles = Is / 128; p.b_rows_per_expert = 0;
+    p.rows = T; p.K = H; p.N = Is; p.n_tiles = Is / gu_cols; p.b_rows_per_expert = 0;
     p.out0 = ctx->gu_s; p.out1 = ctx->hq_s; p.sf_out = ctx->hq_s_sc;
     p.swiglu_limit = cfg->swiglu_limit;
     p.sfa = ctx->xq_sc; p.sfb0 = X.wsg_sc; p.sfb1 = X.wsu_sc;
-    const int items = ((T + 127) / 128) * p.n_tiles;
-    if (pr_gu)
-      MOK_CUDA((launch_gemm_mx_pair<256, EPI_SWIGLU_MX>(m, p, row_pairs(T) * p.n_tiles, cs)));
-    else
-      MOK_CUDA((launch_gemm_mx<256, EPI_SWIGLU_MX>(m, p, items < sms ? items : sms, cs)));
+    const long long items = ((T + 127) / 128) * static_cast<long long>(p.n_tiles);
+    MOK_CUDA(launch_gu(m, p, items, row_pairs(T) * p.n_tiles));
     MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_GATEUP, 1, cs));
     MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_DOWN, 0, cs));
     MxMaps m2;
-    if ((st = make_map_u8(&m2.a, ctx->hq_s, Is, T, 128)) || (st = make_map_u8(&m2.b0, w->mxs_down, Is, H, pr ? 128 : bn)) ||
+    if ((st = make_map_u8(&m2.a, ctx->hq_s, Is, T, 128)) || (st = make_map_u8(&m2.b0, w->mxs_down, Is, H, dn_box)) ||
         (st = make_map_sf(&m2.sfa, ctx->hq_s_sc, t_atoms * (Is / 128))) ||
         (st = make_map_sf(&m2.sfb0, X.wsd_sc, (H / 128) * (Is / 128))))
       return st;
     m2.b1 = m2.b0;
     m2.sfb1 = m2.sfb0;
     GemmParams q = base_params(nullptr, ctx->status, 0);
-    q.rows = T; q.K = Is; q.N = H; q.n_tiles = H / bn; q.out0 = ctx->shared_out; q.ld = H;
+    q.rows = T; q.K = Is; q.N = H; q.n_tiles = H / dn_bn; q.out0 = ctx->shared_out; q.ld = H;
     q.sfa = ctx->hq_s_sc; q.sfb0 = X.wsd_sc;
-    const int items2 = ((T + 127) / 128) * q.n_tiles;
-    const int grid2 = items2 < sms ? items2 : sms;
-    if (pr)
-      MOK_CUDA((launch_gemm_mx_pair<256, EPI_STORE_ROWS>(m2, q, row_pairs(T) * q.n_tiles, cs)));
-    else if (bn == 256)
-      MOK_CUDA((launch_gemm_mx<256, EPI_STORE_ROWS>(m2, q, grid2, cs)));
-    else
-      MOK_CUDA((launch_gemm_mx<128, EPI_STORE_ROWS>(m2, q, grid2, cs)));
+    const long long items2 = ((T + 127) / 128) * static_cast<long long>(q.n_tiles);
+    MOK_CUDA(launch_dn(EPI_STORE_ROWS, m2, q, items2, row_pairs(T) * q.n_tiles));
   } else {
     MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_GATEUP, 1, cs));
     MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_DOWN, 0, cs));
@@ -757,44 +788,34 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_GATEUP, 0, cs));
   MxMaps m;
   if ((st = make_map_u8(&m.a, ctx->xq_perm, H, mr, 128)) ||
-      (st = make_map_u8(&m.b0, w->mx_gate, H, static_cast<uint64_t>(E) * I, 128)) ||
-      (st = make_map_u8(&m.b1, w->mx_up, H, static_cast<uint64_t>(E) * I, 128)) ||
+      (st = make_map_u8(&m.b0, w->mx_gate, H, static_cast<uint64_t>(E) * I, gu_box)) ||
+      (st = make_map_u8(&m.b1, w->mx_up, H, static_cast<uint64_t>(E) * I, gu_box)) ||
       (st = make_map_sf(&m.sfa, ctx->xq_perm_sc, r_atoms * (H / 128))) ||
-      (st = make_map_sf(&m.sfb0, X.wg_sc, (static_cast<long long>(E) * I / 128) * (H / 128))) ||
-      (st = make_map_sf(&m.sfb1, X.wu_sc, (static_cast<long long>(E) * I / 128) * (H / 128))))
+      (st = gu_sf_maps(m, X.wg_sc, X.wu_sc, static_cast<long long>(E) * I)))
     return st;
   GemmParams p = base_params(s, ctx->status, cfg->debug_flags);
-  p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / 128; p.b_rows_per_expert = I;
+  p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / gu_cols; p.b_rows_per_expert = I;
   p.out0 = ctx->gu; p.out1 = ctx->hq; p.sf_out = ctx->hq_sc;
   p.swiglu_limit = cfg->swiglu_limit;
   p.sfa = ctx->xq_perm_sc; p.sfb0 = X.wg_sc; p.sfb1 = X.wu_sc;
   const long long items = static_cast<long long>(s->max_tiles) * p.n_tiles;
-  if (pr_gu)
-    MOK_CUDA((launch_gemm_mx_pair<256, EPI_SWIGLU_MX>(m, p, items, cs)));
-  else
-    MOK_CUDA((launch_gemm_mx<256, EPI_SWIGLU_MX>(m, p, items < sms ? static_cast<int>(items) : sms, cs)));
+  MOK_CUDA(launch_gu(m, p, items, items));
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_GATEUP, 1, cs));
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DOWN, 0, cs));
   MxMaps m2;
   if ((st = make_map_u8(&m2.a, ctx->hq, I, mr, 128)) ||
-      (st = make_map_u8(&m2.b0, w->mx_down, I, static_cast<uint64_t>(E) * H, pr ? 128 : bn)) ||
+      (st = make_map_u8(&m2.b0, w->mx_down, I, static_cast<uint64_t>(E) * H, dn_box)) ||
       (st = make_map_sf(&m2.sfa, ctx->hq_sc, r_atoms * (I / 128))) ||
       (st = make_map_sf(&m2.sfb0, X.wd_sc, (static_cast<long long>(E) * H / 128) * (I / 128))))
     return st;
   m2.b1 = m2.b0;
   m2.sfb1 = m2.sfb0;
   GemmParams q = base_params(s, ctx->status, 0);
-  q.grouped = 1; q.K = I; q.N = H; q.n_tiles = H / bn; q.b_rows_per_expert = H;
+  q.grouped = 1; q.K = I; q.N = H; q.n_tiles = H / dn_bn; q.b_rows_per_expert = H;
   q.out0 = ctx->slots; q.ld = H; q.rw = router_w;
   q.sfa = ctx->hq_sc; q.sfb0 = X.wd_sc;
   const long long items2 = static_cast<long long>(s->max_tiles) * q.n_tiles;
-  const int grid2 = items2 < sms ? static_cast<int>(items2) : sms;
-  if (pr)
-    MOK_CUDA((launch_gemm_mx_pair<256, EPI_SCALE_ROWS>(m2, q, items2, cs)));
-  else if (bn == 256)
-    MOK_CUDA((launch_gemm_mx<256, EPI_SCALE_ROWS>(m2, q, grid2, cs)));
-  else
-    MOK_CUDA((launch_gemm_mx<128, EPI_SCALE_ROWS>(m2, q, grid2, cs)));
+  MOK_CUDA(launch_dn(EPI_SCALE_ROWS, m2, q, items2, items2));
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DOWN, 1, cs));
   return MOK_OK;
 }

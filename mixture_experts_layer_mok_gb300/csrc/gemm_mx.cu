@@ -92,5 +92,10 @@ MOK_INSTANTIATE_MX(128, EPI_WGRAD)
 MOK_INSTANTIATE_MX_PAIR(256, EPI_SWIGLU_MX)
 MOK_INSTANTIATE_MX_PAIR(256, EPI_SCALE_ROWS)
 MOK_INSTANTIATE_MX_PAIR(256, EPI_STORE_ROWS)
+// CTA pairs with 128-wide tiles: M = 256 over the pair, a double-buffered
+// 128-column accumulator beside an 8-stage scale ring in each CTA's TMEM
+MOK_INSTANTIATE_MX_PAIR(128, EPI_SWIGLU_MX)
+MOK_INSTANTIATE_MX_PAIR(128, EPI_SCALE_ROWS)
+MOK_INSTANTIATE_MX_PAIR(128, EPI_STORE_ROWS)
 
 }  // namespace mok

@@ -70,11 +70,12 @@ struct MxCfg {
   static constexpr int kSmemBytes =
       1024 + kStages * (kStageBytes + kSfStride) + kBarBytes + kEpiWarps * kEpiStageBytes;
   static_assert(BN == 128 || BN == 256, "tile N");
-  // SwiGLU tiles pair 128 gate rows with 128 up rows: whole scale atoms
-  static_assert(EPI != EPI_SWIGLU_MX || BN == 256, "SwiGLU tile");
+  // SwiGLU tiles pair 128 gate rows with 128 up rows (whole scale atoms); a
+  // CTA pair's 128-wide tile pairs 64 gate with 64 up rows, whose scales sit
+  // in one atom of the interleaved gate|up layout
+  static_assert(EPI != EPI_SWIGLU_MX || BN == 256 || PAIR, "SwiGLU tile");
   static_assert(kSfCol0 + 16 * kStages <= kTmemCols, "TMEM scale ring");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
-  static_assert(!PAIR || BN == 256, "CTA pairs split a 256-wide B tile");
 };
 
 // A 32 x 32 bf16 block staged in shared memory: 32 rows of 16 packed words,
@@ -217,9 +218,13 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
         const long long arow = wg ? it.m0 : it.p0;
         const long long brow = wg ? n0 : static_cast<long long>(it.e) * p.b_rows_per_expert + n0;
         // scale atoms of the item's A rows and B rows (B: gate then up, or two
-        // consecutive 128-row blocks), as atom indices at K-block 0
+        // consecutive 128-row blocks; a pair's 128-wide SwiGLU tile: one atom of
+        // the interleaved gate|up layout, 2 * b_rows_per_expert rows per expert),
+        // as atom indices at K-block 0
         const long long atom_a = (arow >> 7) * static_cast<long long>(kga);
-        const long long atom_b0 = (brow >> 7) * static_cast<long long>(kgb);
+        const long long brow_sf =
+            (PAIR && BN == 128 && kSwiGLU) ? 2ll * it.e * p.b_rows_per_expert + 2ll * n0 : brow;
+        const long long atom_b0 = (brow_sf >> 7) * static_cast<long long>(kgb);
         const long long atom_b1 = kSwiGLU ? atom_b0 : atom_b0 + kgb;
         for (int kb = 0; kb < it.nk; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) {
@@ -241,8 +246,9 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
               tma_load_2d_pair(sB, &maps.b0, lf, k0, static_cast<int>(brow) + rank * C::kBRows);
             tma_load_2d_pair(sS, &maps.sfa, lf, 0, static_cast<int>((atom_a + kb) * 4));
             tma_load_2d_pair(sS + 512, &maps.sfb0, lf, 0, static_cast<int>((atom_b0 + kb) * 4));
-            tma_load_2d_pair(sS + 1024, kSwiGLU ? &maps.sfb1 : &maps.sfb0, lf, 0,
-                             static_cast<int>((atom_b1 + kb) * 4));
+            if (BN == 256)
+              tma_load_2d_pair(sS + 1024, kSwiGLU ? &maps.sfb1 : &maps.sfb0, lf, 0,
+                               static_cast<int>((atom_b1 + kb) * 4));
           } else {
             // K coordinate of this K-block in the operand tensors, and which B
             // tensor holds it (a K range split over two weights: b_split)
@@ -319,7 +325,7 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
           if (PAIR) {
             tmem_cp_32x128b_warpx4_pair(sfa_t, sf_atom_desc(s0));
             tmem_cp_32x128b_warpx4_pair(sfb_t, sf_atom_desc(s0 + 512));
-            tmem_cp_32x128b_warpx4_pair(sfb_t + 4, sf_atom_desc(s0 + 1024));
+            if (BN == 256) tmem_cp_32x128b_warpx4_pair(sfb_t + 4, sf_atom_desc(s0 + 1024));
           } else {
             tmem_cp_32x128b_warpx4(sfa_t, sf_atom_desc(s0));
             tmem_cp_32x128b_warpx4(sfb_t, sf_atom_desc(s0 + 512));

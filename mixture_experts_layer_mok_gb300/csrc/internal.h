@@ -46,11 +46,18 @@ cudaError_t launch_mx_quantize_t(const uint16_t* src, long long ld, int batch, i
                                  uint8_t* rscales = nullptr, int rtiled = 0);
 // One matrix of row-major E8M0 scales [rows][K/32] to rearrange into the
 // tensor-core scale layout at dst (rows and K multiples of 128; rows 0 = skip).
+// gate_up = 1 or 2 writes the gate (1) or up (2) rows of a SwiGLU weight into
+// the interleaved gate|up layout the CTA-pair SwiGLU GEMM with 128-wide tiles
+// reads: with `group` rows per expert, row n of expert e lands on combined row
+// e*2*group + (n/64)*128 + (gate_up == 2 ? 64 : 0) + n%64, so one 512-byte
+// atom holds the scales of 64 gate rows and the 64 up rows of the same columns.
 struct MxTileScaleJob {
   const uint8_t* src;
   long long rows;
   int K;
   uint8_t* dst;
+  int gate_up = 0;
+  int group = 0;
 };
 constexpr int kMaxScaleJobs = 6;
 // All jobs (at most kMaxScaleJobs that are not skipped) in one launch.

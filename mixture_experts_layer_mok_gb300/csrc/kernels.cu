@@ -547,6 +547,8 @@ struct TileScaleJobs {
   const uint8_t* src[kMaxScaleJobs];
   uint8_t* dst[kMaxScaleJobs];
   int K[kMaxScaleJobs];
+  int gate_up[kMaxScaleJobs];   // 0: row r -> row r; 1 / 2: gate / up rows into the interleaved layout
+  int group[kMaxScaleJobs];     // rows per expert of an interleaved job
   int rb0[kMaxScaleJobs + 1];   // job j owns blocks [rb0[j], rb0[j+1]) of grid.x
   int n;
 };
@@ -569,11 +571,26 @@ __global__ void __launch_bounds__(256) mx_tile_scales_kernel(const __grid_consta
     if (g < ng) tile[row][g] = __ldg(s + (rb * 128 + row) * cg + g0 + g);
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < 128 * 16; i += 256) {
-    const int g = i >> 7, w = i & 127;       // atom g, word w = (row % 32) * 4 + row / 32
-    if (g >= ng) continue;
-    const int row = (w >> 2) + 32 * (w & 3);
-    reinterpret_cast<uint32_t*>(dst + ((rb * cg) + g0 + g) * 512)[w] = tile[row][g];
+  if (J.gate_up[j] == 0) {
+    for (int i = threadIdx.x; i < 128 * 16; i += 256) {
+      const int g = i >> 7, w = i & 127;       // atom g, word w = (row % 32) * 4 + row / 32
+      if (g >= ng) continue;
+      const int row = (w >> 2) + 32 * (w & 3);
+      reinterpret_cast<uint32_t*>(dst + ((rb * cg) + g0 + g) * 512)[w] = tile[row][g];
+    }
+  } else {
+    // interleaved gate|up rows: each 64-row half of this block goes to half of
+    // a combined 128-row atom (gate rows first, up rows second)
+    const long long grp = J.group[j];
+    for (int i = threadIdx.x; i < 128 * 16; i += 256) {
+      const int g = i >> 7, row = i & 127;
+      if (g >= ng) continue;
+      const long long src_row = rb * 128 + row;
+      const long long e = src_row / grp, nr = src_row - e * grp;
+      const long long comb = e * 2 * grp + (nr >> 6) * 128 + (J.gate_up[j] == 2 ? 64 : 0) + (nr & 63);
+      const int r = static_cast<int>(comb & 127);
+      reinterpret_cast<uint32_t*>(dst + (((comb >> 7) * cg) + g0 + g) * 512)[(r & 31) * 4 + (r >> 5)] = tile[row][g];
+    }
   }
 }
 
@@ -584,9 +601,13 @@ cudaError_t launch_mx_tile_scales(const MxTileScaleJob* jobs, int n, cudaStream_
   for (int i = 0; i < n; ++i) {
     if (jobs[i].rows <= 0) continue;
     if (m == kMaxScaleJobs || jobs[i].rows % 128 || jobs[i].K <= 0 || jobs[i].K % 128) return cudaErrorInvalidValue;
+    if (jobs[i].gate_up != 0 && (jobs[i].group <= 0 || jobs[i].group % 128 || jobs[i].rows % jobs[i].group))
+      return cudaErrorInvalidValue;
     J.src[m] = jobs[i].src;
     J.dst[m] = jobs[i].dst;
     J.K[m] = jobs[i].K;
+    J.gate_up[m] = jobs[i].gate_up;
+    J.group[m] = jobs[i].group;
     J.rb0[m] = static_cast<int>(total);
     total += jobs[i].rows / 128;
     if (total > 0x7fffffffll) return cudaErrorInvalidValue;

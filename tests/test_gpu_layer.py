@@ -240,24 +240,27 @@ def test_dispatch_paths_agree_bitwise(name, mode):
 def test_cta_pairs_match_single_ctas_bitwise(name, mode):
     """CTA pairs (M = 256 over two SMs, each holding half of B) and single CTAs
     run every output element's K loop in the same order, so forward and
-    backward must be bit-identical between the two (bf16 GEMMs: pairs by
-    default, 4 = MOK_DEBUG_NO_CTA_PAIR; block-scaled GEMMs: single CTAs by
-    default, 8 = MOK_DEBUG_MX_CTA_PAIR)."""
+    backward must be bit-identical between them (bf16 GEMMs: pairs by
+    default, 4 = MOK_DEBUG_NO_CTA_PAIR; block-scaled forward GEMMs: single
+    CTAs with 256-wide tiles, 8 = MOK_DEBUG_MX_CTA_PAIR (pairs, 256-wide
+    tiles), 16 = MOK_DEBUG_MX_PAIR128 (pairs, 128-wide tiles, interleaved
+    gate|up weight scales))."""
     m = mok()
     inp = _inputs(name, seed=9)
     g = inp.to("cuda")
     sched = m.schedule(g.top_experts, inp.meta["E"], 0.5)
     w = weights_of(g, mode)
     outs = []
-    for flags in ((0, 4) if mode == "bf16" else (0, 8)):
+    for flags in ((0, 4) if mode == "bf16" else (0, 8, 16)):
         y, ctx = m.forward(g.x, g.router_w, sched, w, mode=mode, debug=flags)
         grads = m.backward(g.dy, g.x, g.router_w, sched, ctx, w, debug=flags)
         torch.cuda.synchronize()
         assert ctx.status() == 0
         outs.append((y.clone(), {kk: v.clone() for kk, v in grads.items()}))
-    assert torch.equal(outs[0][0], outs[1][0])
-    for key in outs[0][1]:
-        assert torch.equal(outs[0][1][key], outs[1][1][key]), key
+    for other in outs[1:]:
+        assert torch.equal(outs[0][0], other[0])
+        for key in outs[0][1]:
+            assert torch.equal(outs[0][1][key], other[1][key]), key
 
 
 def test_fused_forward_permuted_backward_mix():
