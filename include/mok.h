@@ -92,7 +92,14 @@ typedef int mok_status_t;
                                         tile waits for both CTAs' epilogues) */
 #define MOK_DEBUG_MX_PAIR128     16  /* run the block-scaled MXFP8 forward GEMMs as
                                         CTA pairs with 128-wide tiles and a
-                                        double-buffered accumulator (same results) */
+                                        double-buffered accumulator (same results;
+                                        measured slower on one GB300) */
+#define MOK_DEBUG_PLAIN_ORDER    32  /* visit each GEMM's output tiles row unit by
+                                        row unit, all column tiles of one before
+                                        the next (same results; for comparison with
+                                        the default, which walks a group of row
+                                        units inside each column tile so that the
+                                        larger operand streams through L2 once) */
 
 /* Stages of the layer, for optional per-stage timing events. */
 #define MOK_STAGE_FWD_PREP                 0  /* status hand-over; MXFP8: weight scales into the tensor-core layout */
@@ -230,7 +237,9 @@ typedef struct {
   uint8_t*  xq;       /* [T][H] x codes in token order, MXFP8 mode (scratch) */
   uint8_t*  xq_sc;    /* their scales, tensor-core scale layout (rows padded to 128) */
   int32_t*  status;   /* device status word: MOK_OK or the first device error */
-  uint16_t* x_perm;   /* [max_tiles*128][H] token rows of x in schedule order (MOK_DISPATCH_PERMUTE) */
+  uint16_t* x_perm;   /* [max_tiles*128][H] token rows of x in schedule order: the bf16 forward's
+                         GEMM operand (MOK_DISPATCH_PERMUTE), or, in MOK_MODE_MXFP8_FWD, the bf16
+                         backward's (written on the library's side stream during the forward) */
   int dispatch;       /* the dispatch the forward used */
   uint8_t*  xq_perm;  /* [max_tiles*128][H] x codes in schedule order, MXFP8 mode (scratch) */
   uint8_t*  xq_perm_sc; /* their scales, tensor-core scale layout */

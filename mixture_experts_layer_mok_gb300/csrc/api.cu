@@ -274,6 +274,9 @@ size_t carve_ctx(void* buf, int T, int k, int E, int H, int I, int Is, int mode,
     ctx->x_perm = c.take<uint16_t>(mr * H);
     ctx->h = c.take<uint16_t>(mr * I);
   } else {
+    // the bf16 token rows in schedule order for the bf16 backward's gate/up
+    // weight gradient, written during the forward (MXFP8 forward mode only)
+    if (mode == MOK_MODE_MXFP8_FWD) ctx->x_perm = c.take<uint16_t>(mr * H);
     ctx->xq = c.take<uint8_t>(static_cast<long long>(T) * H);
     ctx->xq_sc = c.take<uint8_t>(tiled_scale_bytes(T, H));
     ctx->xq_perm = c.take<uint8_t>(mr * H);
@@ -351,7 +354,8 @@ size_t carve_bwd(void* buf, int T, int k, int E, int H, int I, int Is, int mode,
   L->dx_slots = c.take<uint16_t>(mr * H);
   if (!mx) {
     L->dy_perm = c.take<uint16_t>(mr * H);
-    L->xb_perm = c.take<uint16_t>(mr * H);
+    // x's rows in schedule order: after an MXFP8 forward the context holds them
+    if (mode == MOK_MODE_BF16) L->xb_perm = c.take<uint16_t>(mr * H);
   }
   if (Is > 0) {
     if (!mx) {
@@ -407,9 +411,14 @@ mok_status_t check_shapes(int T, int k, int E, int H, int I, int Is) {
   return MOK_OK;
 }
 
-GemmParams base_params(const mok_schedule_t* s, int* status, int debug) {
+// Work-item order: -1 lets the launch pick the L2-friendly order (see
+// resolve_item_order), -2 keeps the plain order (MOK_DEBUG_PLAIN_ORDER).
+GemmParams base_params(const mok_config_t* cfg, const mok_schedule_t* s, int* status, int debug) {
   GemmParams p;
   memset(&p, 0, sizeof(p));
+  const int order = (cfg && (cfg->debug_flags & MOK_DEBUG_PLAIN_ORDER)) ? -2 : -1;
+  p.group = order;
+  p.wg_col_outer = order;
   p.topk = s ? s->k : 1;
   if (s) {
     p.header = s->header;
@@ -592,7 +601,7 @@ mok_status_t forward_bf16(const mok_config_t* cfg, const uint16_t* x, const floa
         (st = make_map(&m.b1, w->ws_up, H, Is, 128, kTileBK)))
       return st;
     if ((st = make_map_out(&m.o0, ctx->gu_s, 2ull * Is, T)) || (st = make_map_out(&m.o1, ctx->h_s, Is, T))) return st;
-    GemmParams p = base_params(nullptr, ctx->status, 0);
+    GemmParams p = base_params(cfg, nullptr, ctx->status, 0);
     p.rows = T; p.K = H; p.N = Is; p.n_tiles = Is / 128; p.b_rows_per_expert = 0;
     p.out0 = ctx->gu_s; p.out1 = ctx->h_s;
     p.swiglu_limit = cfg->swiglu_limit;
@@ -609,7 +618,7 @@ mok_status_t forward_bf16(const mok_config_t* cfg, const uint16_t* x, const floa
         (st = make_map_out(&m2.o0, ctx->shared_out, H, T)))
       return st;
     m2.b1 = m2.b0;
-    GemmParams q = base_params(nullptr, ctx->status, 0);
+    GemmParams q = base_params(cfg, nullptr, ctx->status, 0);
     q.rows = T; q.K = Is; q.N = H; q.n_tiles = H / bn; q.out0 = ctx->shared_out; q.ld = H;
     const long long items2 = ((T + 127) / 128) * static_cast<long long>(q.n_tiles);
     if (bn == 256)
@@ -633,7 +642,7 @@ mok_status_t forward_bf16(const mok_config_t* cfg, const uint16_t* x, const floa
       (st = make_map(&m.b1, w->w_up, H, static_cast<uint64_t>(E) * I, 128, bk)) ||
       (st = make_map_out(&m.o0, ctx->gu, 2ull * I, mr)) || (st = make_map_out(&m.o1, ctx->h, I, mr)))
     return st;
-  GemmParams p = base_params(s, ctx->status, cfg->debug_flags);
+  GemmParams p = base_params(cfg, s, ctx->status, cfg->debug_flags);
   p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / 128; p.b_rows_per_expert = I;
   p.out0 = ctx->gu; p.out1 = ctx->h; p.ga = x; p.ga_ld = H;
   p.swiglu_limit = cfg->swiglu_limit;
@@ -655,7 +664,7 @@ mok_status_t forward_bf16(const mok_config_t* cfg, const uint16_t* x, const floa
       (st = make_map_out(&m2.o0, ctx->slots, H, mr)))
     return st;
   m2.b1 = m2.b0;
-  GemmParams q = base_params(s, ctx->status, 0);
+  GemmParams q = base_params(cfg, s, ctx->status, 0);
   q.grouped = 1; q.K = I; q.N = H; q.n_tiles = H / bn; q.b_rows_per_expert = H;
   q.out0 = ctx->slots; q.ld = H; q.rw = router_w;
   const long long items2 = static_cast<long long>(s->max_tiles) * q.n_tiles;
@@ -702,6 +711,14 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
   }
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_PREP, 1, side->s));
   MOK_CUDA(cudaEventRecord(side->join, side->s));
+  // MXFP8 forward / bf16 backward: the backward's gate/up weight gradient
+  // reads x's bf16 token rows in schedule order.  Writing them here, on the
+  // side stream under the compute-bound block-scaled GEMMs, keeps that HBM
+  // traffic out of the backward (handed back at `join2`, end of the forward).
+  if (cfg->mode == MOK_MODE_MXFP8_FWD) {
+    MOK_CUDA(launch_permute_rows(x, H, k, s->row_src, s->header, mr, ctx->x_perm, sms, side->s));
+    MOK_CUDA(cudaEventRecord(side->join2, side->s));
+  }
   ctx->dispatch = MOK_DISPATCH_PERMUTE;
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 0, cs));
   MOK_CUDA(launch_mx_dispatch(x, T, H, k, s->slot_row, s->row_src, s->header, mr, ctx->xq, ctx->xq_sc, ctx->xq_perm,
@@ -757,7 +774,7 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
         (st = make_map_u8(&m.b1, w->mxs_up, H, Is, gu_box)) ||
         (st = make_map_sf(&m.sfa, ctx->xq_sc, t_atoms * (H / 128))) || (st = gu_sf_maps(m, X.wsg_sc, X.wsu_sc, Is)))
       return st;
-    GemmParams p = base_params(nullptr, ctx->status, 0);
+    GemmParams p = base_params(cfg, nullptr, ctx->status, 0);
     p.rows = T; p.K = H; p.N = Is; p.n_tiles = Is / gu_cols; p.b_rows_per_expert = 0;
     p.out0 = ctx->gu_s; p.out1 = ctx->hq_s; p.sf_out = ctx->hq_s_sc;
     p.swiglu_limit = cfg->swiglu_limit;
@@ -773,7 +790,7 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
       return st;
     m2.b1 = m2.b0;
     m2.sfb1 = m2.sfb0;
-    GemmParams q = base_params(nullptr, ctx->status, 0);
+    GemmParams q = base_params(cfg, nullptr, ctx->status, 0);
     q.rows = T; q.K = Is; q.N = H; q.n_tiles = H / dn_bn; q.out0 = ctx->shared_out; q.ld = H;
     q.sfa = ctx->hq_s_sc; q.sfb0 = X.wsd_sc;
     const long long items2 = ((T + 127) / 128) * static_cast<long long>(q.n_tiles);
@@ -793,7 +810,7 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
       (st = make_map_sf(&m.sfa, ctx->xq_perm_sc, r_atoms * (H / 128))) ||
       (st = gu_sf_maps(m, X.wg_sc, X.wu_sc, static_cast<long long>(E) * I)))
     return st;
-  GemmParams p = base_params(s, ctx->status, cfg->debug_flags);
+  GemmParams p = base_params(cfg, s, ctx->status, cfg->debug_flags);
   p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / gu_cols; p.b_rows_per_expert = I;
   p.out0 = ctx->gu; p.out1 = ctx->hq; p.sf_out = ctx->hq_sc;
   p.swiglu_limit = cfg->swiglu_limit;
@@ -810,13 +827,14 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
     return st;
   m2.b1 = m2.b0;
   m2.sfb1 = m2.sfb0;
-  GemmParams q = base_params(s, ctx->status, 0);
+  GemmParams q = base_params(cfg, s, ctx->status, 0);
   q.grouped = 1; q.K = I; q.N = H; q.n_tiles = H / dn_bn; q.b_rows_per_expert = H;
   q.out0 = ctx->slots; q.ld = H; q.rw = router_w;
   q.sfa = ctx->hq_sc; q.sfb0 = X.wd_sc;
   const long long items2 = static_cast<long long>(s->max_tiles) * q.n_tiles;
   MOK_CUDA(launch_dn(EPI_SCALE_ROWS, m2, q, items2, items2));
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DOWN, 1, cs));
+  if (cfg->mode == MOK_MODE_MXFP8_FWD) MOK_CUDA(cudaStreamWaitEvent(cs, side->join2, 0));
   return MOK_OK;
 }
 
@@ -894,7 +912,7 @@ mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const u
           (st = make_map_codes_out(&m.o1, L.dgusT, Tp, 2ull * Is)) || (st = make_map_codes_out(&m.o2, L.hsT, Tp, Is)))
         return st;
       m.b1 = m.b0;
-      GemmParams p = base_params(nullptr, ctx->status, 0);
+      GemmParams p = base_params(cfg, nullptr, ctx->status, 0);
       p.rows = T; p.K = H; p.N = Is; p.n_tiles = Is / 128; p.b_rows_per_expert = 0;
       p.aux0 = ctx->gu_s; p.swiglu_limit = ctx->swiglu_limit;
       p.sf_out = L.dgusq_sc; p.out2 = L.dgusT_sc; p.sf_out2 = L.hsT_sc; p.ld = Tp;   // codes: maps o0..o2
@@ -909,7 +927,7 @@ mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const u
       if ((st = make_map_u8(&m.a, L.dyT_tok, Tp, H, 128)) || (st = make_map_u8(&m.b0, L.hsT, Tp, Is, bnS)))
         return st;
       m.b1 = m.b0;
-      GemmParams p = base_params(nullptr, ctx->status, 0);
+      GemmParams p = base_params(cfg, nullptr, ctx->status, 0);
       p.wgrad = 1; p.rows = T; p.K = Tp; p.E = 1; p.m_tiles = H / 128; p.n_tiles = Is / bnS;
       p.out0 = g->d_ws_down; p.out1 = g->d_ws_down; p.ld = Is; p.split = H;
       p.sfa = L.dyT_tok_sc; p.sfb0 = L.hsT_sc;
@@ -923,7 +941,7 @@ mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const u
       if ((st = make_map_u8(&m.a, L.dgusT, Tp, 2ull * Is, 128)) || (st = make_map_u8(&m.b0, L.xT_tok, Tp, H, bnH)))
         return st;
       m.b1 = m.b0;
-      GemmParams p = base_params(nullptr, ctx->status, 0);
+      GemmParams p = base_params(cfg, nullptr, ctx->status, 0);
       p.wgrad = 1; p.rows = T; p.K = Tp; p.E = 1; p.m_tiles = 2 * Is / 128; p.n_tiles = H / bnH;
       p.out0 = g->d_ws_gate; p.out1 = g->d_ws_up; p.ld = H; p.split = Is;
       p.sfa = L.dgusT_sc; p.sfb0 = L.xT_tok_sc;
@@ -936,7 +954,7 @@ mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const u
       if ((st = make_map_u8(&m.a, L.dgusq, 2ull * Is, T, 128)) || (st = make_map_u8(&m.b0, w->mxts_gate, Is, H, bnH)) ||
           (st = make_map_u8(&m.b1, w->mxts_up, Is, H, bnH)))
         return st;
-      GemmParams p = base_params(nullptr, ctx->status, 0);
+      GemmParams p = base_params(cfg, nullptr, ctx->status, 0);
       p.rows = T; p.K = 2 * Is; p.N = H; p.n_tiles = H / bnH; p.b_rows_per_expert = 0; p.b_split = Is;
       p.out0 = L.dx_s; p.ld = H;
       p.sfa = L.dgusq_sc; p.sfb0 = L.wtsg_sc; p.sfb1 = L.wtsu_sc; p.sf_kgb = Is / 128;
@@ -961,7 +979,7 @@ mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const u
         (st = make_map_codes_out(&m.o2, L.hwT, mr, I)))
       return st;
     m.b1 = m.b0;
-    GemmParams p = base_params(s, ctx->status, 0);
+    GemmParams p = base_params(cfg, s, ctx->status, 0);
     p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / 128; p.b_rows_per_expert = I;
     p.aux0 = ctx->gu; p.rw = router_w; p.dw_part = L.dw_part; p.swiglu_limit = ctx->swiglu_limit;
     p.sf_out = L.dguq_sc; p.out2 = L.dguT_sc; p.sf_out2 = L.hwT_sc; p.ld = mr;   // codes: maps o0..o2
@@ -976,7 +994,7 @@ mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const u
     MxMaps m;
     if ((st = make_map_u8(&m.a, L.dyT, mr, H, 128)) || (st = make_map_u8(&m.b0, L.hwT, mr, I, bn))) return st;
     m.b1 = m.b0;
-    GemmParams p = base_params(s, ctx->status, 0);
+    GemmParams p = base_params(cfg, s, ctx->status, 0);
     p.wgrad = 1; p.grouped = 1; p.K = mri; p.E = E; p.m_tiles = H / 128; p.n_tiles = I / bn;
     p.out0 = g->d_w_down; p.out1 = g->d_w_down; p.ld = I; p.split = H;
     p.sfa = L.dyT_sc; p.sfb0 = L.hwT_sc;
@@ -989,7 +1007,7 @@ mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const u
     if ((st = make_map_u8(&m.a, L.dguT, mr, 2ull * I, 128)) || (st = make_map_u8(&m.b0, L.xT, mr, H, bnH)))
       return st;
     m.b1 = m.b0;
-    GemmParams p = base_params(s, ctx->status, 0);
+    GemmParams p = base_params(cfg, s, ctx->status, 0);
     p.wgrad = 1; p.grouped = 1; p.K = mri; p.E = E; p.m_tiles = 2 * I / 128; p.n_tiles = H / bnH;
     p.out0 = g->d_w_gate; p.out1 = g->d_w_up; p.ld = H; p.split = I;
     p.sfa = L.dguT_sc; p.sfb0 = L.xT_sc;
@@ -1003,7 +1021,7 @@ mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const u
         (st = make_map_u8(&m.b0, w->mxt_gate, I, static_cast<uint64_t>(E) * H, bnH)) ||
         (st = make_map_u8(&m.b1, w->mxt_up, I, static_cast<uint64_t>(E) * H, bnH)))
       return st;
-    GemmParams p = base_params(s, ctx->status, 0);
+    GemmParams p = base_params(cfg, s, ctx->status, 0);
     p.grouped = 1; p.K = 2 * I; p.N = H; p.n_tiles = H / bnH; p.b_rows_per_expert = H; p.b_split = I;
     p.out0 = L.dx_slots; p.ld = H;
     p.sfa = L.dguq_sc; p.sfb0 = L.wtg_sc; p.sfb1 = L.wtu_sc; p.sf_kgb = I / 128;
@@ -1272,9 +1290,11 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
     MOK_CUDA(cudaEventRecord(side->fork, cs));
     MOK_CUDA(cudaStreamWaitEvent(side->s, side->fork, 0));
     MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 0, side->s));
-    if (ctx->dispatch == MOK_DISPATCH_PERMUTE && ctx->mode == MOK_MODE_BF16 && ctx->x_perm) {
+    if (ctx->dispatch == MOK_DISPATCH_PERMUTE && (ctx->mode == MOK_MODE_BF16 || ctx->mode == MOK_MODE_MXFP8_FWD) &&
+        ctx->x_perm) {
       x_rows = ctx->x_perm;
     } else {
+      if (!L.xb_perm) return fail(MOK_ERR_INVALID_ARG, "context holds no schedule-order copy of x");
       MOK_CUDA(launch_permute_rows(x, H, k, s->row_src, s->header, mr, L.xb_perm, sms, side->s));
       x_rows = L.xb_perm;
     }
@@ -1297,7 +1317,7 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
           (st = make_map_out(&m.o0, L.dgu_s, 2ull * Is, T)) || (st = make_map_out(&m.o1, L.hs, Is, T)))
         return st;
       m.b1 = m.b0;
-      GemmParams p = base_params(nullptr, ctx->status, 0);
+      GemmParams p = base_params(cfg, nullptr, ctx->status, 0);
       p.rows = T; p.K = H; p.N = Is; p.n_tiles = Is / bns; p.b_rows_per_expert = 0;
       p.aux0 = ctx->gu_s; p.out0 = L.dgu_s; p.out1 = L.hs;
       p.swiglu_limit = ctx->swiglu_limit;
@@ -1319,7 +1339,7 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
         return st;
       m.o1 = m.o0;
       m.b1 = m.b0;
-      GemmParams p = base_params(nullptr, ctx->status, 0);
+      GemmParams p = base_params(cfg, nullptr, ctx->status, 0);
       p.wgrad = 1; p.rows = T; p.E = 1; p.m_tiles = H / 128; p.n_tiles = Is / bns;
       p.out0 = g->d_ws_down; p.out1 = g->d_ws_down; p.ld = Is; p.split = H; p.estride = 0;
       const long long items = static_cast<long long>(p.m_tiles) * p.n_tiles;
@@ -1340,7 +1360,7 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
           (st = make_map_out(&m.o0, g->d_ws_gate, H, Is)) || (st = make_map_out(&m.o1, g->d_ws_up, H, Is)))
         return st;
       m.b1 = m.b0;
-      GemmParams p = base_params(nullptr, ctx->status, 0);
+      GemmParams p = base_params(cfg, nullptr, ctx->status, 0);
       p.wgrad = 1; p.rows = T; p.E = 1; p.m_tiles = 2 * Is / 128; p.n_tiles = H / bn;
       p.out0 = g->d_ws_gate; p.out1 = g->d_ws_up; p.ld = H; p.split = Is; p.estride = 0;
       const long long items = static_cast<long long>(p.m_tiles) * p.n_tiles;
@@ -1361,7 +1381,7 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
           (st = make_map_mn(&m.b1, w->ws_up, H, Is, pr ? bn / 2 : bn, kTileBK)) ||
           (st = make_map_out(&m.o0, L.dx_s, H, T)))
         return st;
-      GemmParams p = base_params(nullptr, ctx->status, 0);
+      GemmParams p = base_params(cfg, nullptr, ctx->status, 0);
       p.rows = T; p.K = 2 * Is; p.N = H; p.n_tiles = H / bn; p.b_rows_per_expert = 0; p.b_split = Is;
       p.out0 = L.dx_s; p.ld = H;
       const long long items = ((T + 127) / 128) * static_cast<long long>(p.n_tiles);
@@ -1390,7 +1410,7 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
         (st = make_map_out(&m.o0, L.dgu, 2ull * I, mr)) || (st = make_map_out(&m.o1, L.hw, I, mr)))
       return st;
     m.b1 = m.b0;
-    GemmParams p = base_params(s, ctx->status, 0);
+    GemmParams p = base_params(cfg, s, ctx->status, 0);
     p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / bn1; p.b_rows_per_expert = H;
     p.aux0 = ctx->gu; p.out0 = L.dgu; p.out1 = L.hw; p.rw = router_w; p.dw_part = L.dw_part;
     p.swiglu_limit = ctx->swiglu_limit;
@@ -1424,7 +1444,7 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
       return st;
     m.o1 = m.o0;
     m.b1 = m.b0;
-    GemmParams p = base_params(s, ctx->status, 0);
+    GemmParams p = base_params(cfg, s, ctx->status, 0);
     p.wgrad = 1; p.grouped = 1; p.E = E; p.m_tiles = H / 128; p.n_tiles = I / bn;
     p.out0 = g->d_w_down; p.out1 = g->d_w_down; p.ld = I; p.split = H;
     p.estride = static_cast<long long>(H) * I;
@@ -1459,7 +1479,7 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
         (st = make_map_out(&m.o1, g->d_w_up, H, static_cast<uint64_t>(E) * I)))
       return st;
     m.b1 = m.b0;
-    GemmParams p = base_params(s, ctx->status, 0);
+    GemmParams p = base_params(cfg, s, ctx->status, 0);
     p.wgrad = 1; p.grouped = 1; p.E = E; p.m_tiles = 2 * I / 128; p.n_tiles = H / bn;
     p.out0 = g->d_w_gate; p.out1 = g->d_w_up; p.ld = H; p.split = I;
     p.estride = static_cast<long long>(I) * H;
@@ -1493,7 +1513,7 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
         (st = make_map_mn(&m.b1, w->w_up, H, static_cast<uint64_t>(E) * I, bw, kTileBK)) ||
         (st = make_map_out(&m.o0, L.dx_slots, H, mr)))
       return st;
-    GemmParams p = base_params(s, ctx->status, 0);
+    GemmParams p = base_params(cfg, s, ctx->status, 0);
     p.grouped = 1; p.K = 2 * I; p.N = H; p.n_tiles = H / bn; p.b_rows_per_expert = I; p.b_split = I;
     p.out0 = L.dx_slots; p.ld = H;
     const long long items = static_cast<long long>(s->max_tiles) * p.n_tiles;

@@ -120,7 +120,44 @@ struct GemmParams {
   uint8_t* sf_out2;  // EPI_DOWN_BWD_MX: scales of the transposed w h
   int sf_kga;        // 128-column groups of A's / B's scale layout (0 = K / 128); a weight
   int sf_kgb;        // gradient's operands span the whole row range, not one item's K
+  // ---- order of the work items (never changes a result: each output tile has
+  // one owner and a fixed K order)
+  int group;         // row GEMMs: 0 = column tiles inside each row unit (tile or pair);
+                     // g > 0 = row units in groups of g, the group's units inside
+                     // each column tile (B's columns stream once per group while
+                     // the group's A rows stay in L2)
+  int wg_col_outer;  // weight gradients: 1 = an expert's row units inside each
+                     // column tile (B streams once, A stays in L2), 0 = the reverse
 };
+
+// Default work-item order, chosen at launch where p.group / p.wg_col_outer
+// are -1 (-2: the plain order).  Row GEMMs take their row units (tiles, or
+// pairs of tiles) in groups of 16 row tiles inside each column tile: while
+// the group's A rows stay in L2, each B column slice (an expert's weights, a
+// few MB) is read once for the whole group instead of once per row unit.
+// Weight gradients walk an expert's row units inside each column tile when A
+// (M rows per expert) is the smaller operand, so that B streams through once.
+inline void resolve_item_order(GemmParams& p, bool pair) {
+  if (p.group < 0) p.group = (p.group == -2) ? 0 : (pair ? 8 : 16);
+  if (p.wg_col_outer < 0)
+    p.wg_col_outer = (p.wg_col_outer == -2) ? 0 : (p.wgrad && static_cast<long long>(p.m_tiles) * kBM < p.ld ? 1 : 0);
+}
+
+// Work item idx of a grid of `units` row units x n_tiles column tiles -> (row
+// unit u, column tile nt), in the order GemmParams::group describes.
+__device__ __forceinline__ void unit_and_col(int idx, int units, int n_tiles, int group, int& u, int& nt) {
+  if (group <= 0) {
+    u = idx / n_tiles;
+    nt = idx - u * n_tiles;
+    return;
+  }
+  const int span = group * n_tiles;
+  const int g = idx / span;
+  const int r = idx - g * span;
+  const int gs = min(group, units - g * group);   // the last group may be short
+  nt = r / gs;
+  u = g * group + (r - nt * gs);
+}
 
 struct Item {
   int e, p0, rows, m0, nt, kbeg, nk;
@@ -140,8 +177,8 @@ __device__ __forceinline__ Item get_item(const GemmParams& p, int idx, int bk) {
   Item it;
   it.empty = false;
   if (!p.wgrad) {
-    const int mt = idx / p.n_tiles;
-    it.nt = idx - mt * p.n_tiles;
+    int mt;
+    unit_and_col(idx, p.grouped ? p.header[0] : (p.rows + kBM - 1) / kBM, p.n_tiles, p.group, mt, it.nt);
     if (p.grouped) {
       it.e = __ldg(p.tile_expert + mt);
       it.p0 = __ldg(p.tile_row0 + mt);
@@ -158,8 +195,8 @@ __device__ __forceinline__ Item get_item(const GemmParams& p, int idx, int bk) {
     const int per_e = p.m_tiles * p.n_tiles;
     it.e = idx / per_e;
     const int r = idx - it.e * per_e;
-    const int mt = r / p.n_tiles;
-    it.nt = r - mt * p.n_tiles;
+    int mt;
+    unit_and_col(r, p.m_tiles, p.n_tiles, p.wg_col_outer ? p.m_tiles : 0, mt, it.nt);
     it.m0 = mt * kBM;
     it.p0 = 0;
     it.rows = 0;
@@ -191,8 +228,8 @@ __device__ __forceinline__ Item get_item_pair(const GemmParams& p, int idx, int 
   Item it;
   it.empty = false;
   if (!p.wgrad) {
-    const int pr = idx / p.n_tiles;
-    it.nt = idx - pr * p.n_tiles;
+    int pr;
+    unit_and_col(idx, p.grouped ? p.header[4] : ((p.rows + kBM - 1) / kBM + 1) / 2, p.n_tiles, p.group, pr, it.nt);
     if (p.grouped) {
       const int t0 = __ldg(p.pair_tile + 2 * pr);
       const int t1 = __ldg(p.pair_tile + 2 * pr + 1);
@@ -215,8 +252,8 @@ __device__ __forceinline__ Item get_item_pair(const GemmParams& p, int idx, int 
     const int per_e = mp_n * p.n_tiles;
     it.e = idx / per_e;
     const int r = idx - it.e * per_e;
-    const int mp = r / p.n_tiles;
-    it.nt = r - mp * p.n_tiles;
+    int mp;
+    unit_and_col(r, mp_n, p.n_tiles, p.wg_col_outer ? mp_n : 0, mp, it.nt);
     const int mt = 2 * mp + rank;
     it.empty = mt >= p.m_tiles;
     it.m0 = (it.empty ? 2 * mp : mt) * kBM;

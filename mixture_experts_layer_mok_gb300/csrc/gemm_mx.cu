@@ -24,7 +24,9 @@ cudaError_t launch_gemm_mx(const MxMaps& maps, const GemmParams& p, int grid, cu
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, kern, maps, p);
+  GemmParams q = p;
+  resolve_item_order(q, false);
+  err = cudaLaunchKernelEx(&cfg, kern, maps, q);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
@@ -69,7 +71,9 @@ cudaError_t launch_gemm_mx_pair(const MxMaps& maps, const GemmParams& p, long lo
   const long long clusters = max_items < resident[dev] ? max_items : resident[dev];
   cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
   cfg.numAttrs = 2;
-  err = cudaLaunchKernelEx(&cfg, kern, maps, p);
+  GemmParams q = p;
+  resolve_item_order(q, true);
+  err = cudaLaunchKernelEx(&cfg, kern, maps, q);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
