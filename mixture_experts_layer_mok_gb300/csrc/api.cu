@@ -515,6 +515,7 @@ struct SideStream {
   cudaEvent_t fork = nullptr;
   cudaEvent_t join = nullptr;
   cudaEvent_t join2 = nullptr;   // a second hand-back point within one call
+  cudaEvent_t mid = nullptr;     // a later start point on the caller's stream
 };
 thread_local SideStream g_side[64];
 
@@ -528,6 +529,7 @@ mok_status_t side_stream(SideStream** out) {
     MOK_CUDA(cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming));
     MOK_CUDA(cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming));
     MOK_CUDA(cudaEventCreateWithFlags(&sd.join2, cudaEventDisableTiming));
+    MOK_CUDA(cudaEventCreateWithFlags(&sd.mid, cudaEventDisableTiming));
   }
   *out = &sd;
   return MOK_OK;
@@ -711,14 +713,6 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
   }
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_PREP, 1, side->s));
   MOK_CUDA(cudaEventRecord(side->join, side->s));
-  // MXFP8 forward / bf16 backward: the backward's gate/up weight gradient
-  // reads x's bf16 token rows in schedule order.  Writing them here, on the
-  // side stream under the compute-bound block-scaled GEMMs, keeps that HBM
-  // traffic out of the backward (handed back at `join2`, end of the forward).
-  if (cfg->mode == MOK_MODE_MXFP8_FWD) {
-    MOK_CUDA(launch_permute_rows(x, H, k, s->row_src, s->header, mr, ctx->x_perm, sms, side->s));
-    MOK_CUDA(cudaEventRecord(side->join2, side->s));
-  }
   ctx->dispatch = MOK_DISPATCH_PERMUTE;
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 0, cs));
   MOK_CUDA(launch_mx_dispatch(x, T, H, k, s->slot_row, s->row_src, s->header, mr, ctx->xq, ctx->xq_sc, ctx->xq_perm,
@@ -801,6 +795,17 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
   }
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_DOWN, 1, cs));
 
+  // MXFP8 forward / bf16 backward: the backward's gate/up weight gradient
+  // reads x's bf16 token rows in schedule order.  The side stream writes them
+  // from here on, under the long, compute-bound routed gate/up GEMM (which
+  // uses a fraction of HBM bandwidth), instead of in the backward; handed back
+  // at `join2`, at the end of the forward.
+  if (cfg->mode == MOK_MODE_MXFP8_FWD) {
+    MOK_CUDA(cudaEventRecord(side->mid, cs));
+    MOK_CUDA(cudaStreamWaitEvent(side->s, side->mid, 0));
+    MOK_CUDA(launch_permute_rows(x, H, k, s->row_src, s->header, mr, ctx->x_perm, sms, side->s));
+    MOK_CUDA(cudaEventRecord(side->join2, side->s));
+  }
   // ---- routed experts
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_GATEUP, 0, cs));
   MxMaps m;
@@ -1305,7 +1310,11 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
     MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 0, cs));
     MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 1, cs));
   }
-  // ---- shared expert backward (dense rows, w = 1)
+  // ---- shared expert backward, first part (dense rows, w = 1): the SwiGLU
+  // backward and the dgrad, which read dy in token order.  They run while the
+  // side stream writes dy's rows in schedule order; the shared weight
+  // gradients, whose deep contractions over all T tokens suffer most from
+  // sharing HBM with that copy, run after the routed GEMMs.
   if (Is > 0) {
     const int bns = tile_n(Is);
     {
@@ -1329,48 +1338,6 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
         MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_MN_TILE, 128, EPI_DOWN_BWD>(m, p, items, 0, false, sms, cs)));
       MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DOWN, 1, cs));
     }
-    {  // dW_s_down = dy^T h_s
-      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_DOWN, 0, cs));
-      GemmMaps m;
-      const bool pr = pair_on(cfg, bns);
-      if ((st = make_map_mn(&m.a, dy, H, T, 128, kTileBK)) ||
-          (st = make_map_mn(&m.b0, L.hs, Is, T, pr ? bns / 2 : bns, kTileBK)) ||
-          (st = make_map_out(&m.o0, g->d_ws_down, Is, H)))
-        return st;
-      m.o1 = m.o0;
-      m.b1 = m.b0;
-      GemmParams p = base_params(cfg, nullptr, ctx->status, 0);
-      p.wgrad = 1; p.rows = T; p.E = 1; p.m_tiles = H / 128; p.n_tiles = Is / bns;
-      p.out0 = g->d_ws_down; p.out1 = g->d_ws_down; p.ld = Is; p.split = H; p.estride = 0;
-      const long long items = static_cast<long long>(p.m_tiles) * p.n_tiles;
-      const long long pitems = static_cast<long long>((p.m_tiles + 1) / 2) * p.n_tiles;
-      if (bns == 256)
-        MOK_CUDA((launch_tiles<SRC_MN_TILE, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, items, pitems, pr, sms, cs)));
-      else
-        MOK_CUDA((launch_tiles<SRC_MN_TILE, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, items, 0, false, sms, cs)));
-      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_DOWN, 1, cs));
-    }
-    {  // dW_s_gate|up = (dG_s|dU_s)^T x
-      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_GATEUP, 0, cs));
-      GemmMaps m;
-      const int bn = tile_n(H);
-      const bool pr = pair_on(cfg, bn);
-      if ((st = make_map_mn(&m.a, L.dgu_s, 2 * Is, T, 128, kTileBK)) ||
-          (st = make_map_mn(&m.b0, x, H, T, pr ? bn / 2 : bn, kTileBK)) ||
-          (st = make_map_out(&m.o0, g->d_ws_gate, H, Is)) || (st = make_map_out(&m.o1, g->d_ws_up, H, Is)))
-        return st;
-      m.b1 = m.b0;
-      GemmParams p = base_params(cfg, nullptr, ctx->status, 0);
-      p.wgrad = 1; p.rows = T; p.E = 1; p.m_tiles = 2 * Is / 128; p.n_tiles = H / bn;
-      p.out0 = g->d_ws_gate; p.out1 = g->d_ws_up; p.ld = H; p.split = Is; p.estride = 0;
-      const long long items = static_cast<long long>(p.m_tiles) * p.n_tiles;
-      const long long pitems = static_cast<long long>((p.m_tiles + 1) / 2) * p.n_tiles;
-      if (bn == 256)
-        MOK_CUDA((launch_tiles<SRC_MN_TILE, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, items, pitems, pr, sms, cs)));
-      else
-        MOK_CUDA((launch_tiles<SRC_MN_TILE, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, items, 0, false, sms, cs)));
-      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_GATEUP, 1, cs));
-    }
     {  // dx_s = dG_s W_s_gate + dU_s W_s_up
       MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DGRAD, 0, cs));
       GemmMaps m;
@@ -1393,7 +1360,7 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
       MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DGRAD, 1, cs));
     }
   } else {
-    for (int sg = MOK_STAGE_BWD_SHARED_DOWN; sg <= MOK_STAGE_BWD_SHARED_DGRAD; ++sg) {
+    for (int sg : {MOK_STAGE_BWD_SHARED_DOWN, MOK_STAGE_BWD_SHARED_DGRAD}) {
       MOK_CUDA(mark(cfg, sg, 0, cs));
       MOK_CUDA(mark(cfg, sg, 1, cs));
     }
@@ -1522,6 +1489,57 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
     else
       MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_MN_TILE, 128, EPI_STORE_ROWS>(m, p, items, 0, false, sms, cs)));
     MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DGRAD_GATEUP, 1, cs));
+  }
+  // ---- shared expert backward, second part: the weight gradients
+  if (Is > 0) {
+    const int bns = tile_n(Is);
+    {  // dW_s_down = dy^T h_s
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_DOWN, 0, cs));
+      GemmMaps m;
+      const bool pr = pair_on(cfg, bns);
+      if ((st = make_map_mn(&m.a, dy, H, T, 128, kTileBK)) ||
+          (st = make_map_mn(&m.b0, L.hs, Is, T, pr ? bns / 2 : bns, kTileBK)) ||
+          (st = make_map_out(&m.o0, g->d_ws_down, Is, H)))
+        return st;
+      m.o1 = m.o0;
+      m.b1 = m.b0;
+      GemmParams p = base_params(cfg, nullptr, ctx->status, 0);
+      p.wgrad = 1; p.rows = T; p.E = 1; p.m_tiles = H / 128; p.n_tiles = Is / bns;
+      p.out0 = g->d_ws_down; p.out1 = g->d_ws_down; p.ld = Is; p.split = H; p.estride = 0;
+      const long long items = static_cast<long long>(p.m_tiles) * p.n_tiles;
+      const long long pitems = static_cast<long long>((p.m_tiles + 1) / 2) * p.n_tiles;
+      if (bns == 256)
+        MOK_CUDA((launch_tiles<SRC_MN_TILE, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, items, pitems, pr, sms, cs)));
+      else
+        MOK_CUDA((launch_tiles<SRC_MN_TILE, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, items, 0, false, sms, cs)));
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_DOWN, 1, cs));
+    }
+    {  // dW_s_gate|up = (dG_s|dU_s)^T x
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_GATEUP, 0, cs));
+      GemmMaps m;
+      const int bn = tile_n(H);
+      const bool pr = pair_on(cfg, bn);
+      if ((st = make_map_mn(&m.a, L.dgu_s, 2 * Is, T, 128, kTileBK)) ||
+          (st = make_map_mn(&m.b0, x, H, T, pr ? bn / 2 : bn, kTileBK)) ||
+          (st = make_map_out(&m.o0, g->d_ws_gate, H, Is)) || (st = make_map_out(&m.o1, g->d_ws_up, H, Is)))
+        return st;
+      m.b1 = m.b0;
+      GemmParams p = base_params(cfg, nullptr, ctx->status, 0);
+      p.wgrad = 1; p.rows = T; p.E = 1; p.m_tiles = 2 * Is / 128; p.n_tiles = H / bn;
+      p.out0 = g->d_ws_gate; p.out1 = g->d_ws_up; p.ld = H; p.split = Is; p.estride = 0;
+      const long long items = static_cast<long long>(p.m_tiles) * p.n_tiles;
+      const long long pitems = static_cast<long long>((p.m_tiles + 1) / 2) * p.n_tiles;
+      if (bn == 256)
+        MOK_CUDA((launch_tiles<SRC_MN_TILE, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, items, pitems, pr, sms, cs)));
+      else
+        MOK_CUDA((launch_tiles<SRC_MN_TILE, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, items, 0, false, sms, cs)));
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_GATEUP, 1, cs));
+    }
+  } else {
+    for (int sg : {MOK_STAGE_BWD_SHARED_WGRAD_DOWN, MOK_STAGE_BWD_SHARED_WGRAD_GATEUP}) {
+      MOK_CUDA(mark(cfg, sg, 0, cs));
+      MOK_CUDA(mark(cfg, sg, 1, cs));
+    }
   }
   // ---- fixed-order reductions: dx and the router-weight gradient
   MOK_CUDA(mark(cfg, MOK_STAGE_BWD_REDUCE, 0, cs));

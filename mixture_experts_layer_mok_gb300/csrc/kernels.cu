@@ -290,13 +290,17 @@ cudaError_t launch_mx_quantize(const uint16_t* x, long long nblocks, uint8_t* co
 // unit scales; so do the scales of the token-order copy's last partial
 // 128-row block.  One warp per job: tokens, then schedule rows, then the tail.
 // ===========================================================================
-__global__ void __launch_bounds__(256) mx_dispatch_kernel(
+__global__ void __launch_bounds__(256, 3) mx_dispatch_kernel(
     const uint16_t* __restrict__ x, int T, int H, int topk, const int* __restrict__ slot_row,
     const int* __restrict__ row_src, const int* __restrict__ header, long long max_rows, uint8_t* __restrict__ xq,
     uint8_t* __restrict__ xq_sc, uint8_t* __restrict__ xp, uint8_t* __restrict__ xp_sc) {
   griddep_wait();
   griddep_launch_dependents();
   if (header[2] != 0) return;
+  // per warp: the codes of one 32-block chunk of a row (1 KB), so that every
+  // store instruction of the k + 1 copies writes 512 contiguous bytes
+  __shared__ __align__(16) uint8_t stage[8][1024];
+  uint8_t* wst = stage[threadIdx.x >> 5];
   const long long P = header[1];
   const int lane = threadIdx.x & 31;
   const int nb = H / 32;             // blocks per row (a multiple of 4)
@@ -310,37 +314,51 @@ __global__ void __launch_bounds__(256) mx_dispatch_kernel(
       // schedule rows of this token's k copies, spread over the lanes
       const int p_lo = lane < topk ? __ldg(slot_row + t * topk + lane) : -1;
       const int p_hi = lane + 32 < topk ? __ldg(slot_row + t * topk + lane + 32) : -1;
+      const uint16_t* xrow = x + t * H;
+      // raw bf16 of this lane's block in the current chunk, the next chunk's
+      // loaded while this one is quantised and stored
+      uint4 raw[4];
+      if (lane < nb) load_raw64(xrow + lane * 32, raw);
       for (int b0 = 0; b0 < nb; b0 += 32) {
         const int b = b0 + lane;
         const bool act = b < nb;       // whole aligned groups of 4 lanes share this
         float v[32];
+        if (act) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = bf16_at(raw, i);
+        }
+        if (b0 + 32 + lane < nb) load_raw64(xrow + (b0 + 32 + lane) * 32, raw);
         uint8_t codes[32];
         uint32_t sc = 127;
-        if (act) {
-          load_bf16x32(x + t * H + static_cast<long long>(b) * 32, v);
-          sc = mx_quantize32(v, codes);
-        }
+        if (act) sc = mx_quantize32(v, codes);
         // the 4 scales of an aligned group of blocks form one 32-bit word
         const uint32_t s1 = __shfl_down_sync(0xffffffffu, sc, 1);
         const uint32_t s2 = __shfl_down_sync(0xffffffffu, sc, 2);
         const uint32_t s3 = __shfl_down_sync(0xffffffffu, sc, 3);
         const uint32_t word = sc | (s1 << 8) | (s2 << 16) | (s3 << 24);
-        uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0;
         if (act) {
-          c0 = reinterpret_cast<const uint4*>(codes)[0];
-          c1 = reinterpret_cast<const uint4*>(codes)[1];
-          uint4* d = reinterpret_cast<uint4*>(xq + t * H + static_cast<long long>(b) * 32);
-          d[0] = c0;
-          d[1] = c1;
-          if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(xq_sc + mx_tiled_scale_offset(t, b, cg)) = word;
+          uint4* sw = reinterpret_cast<uint4*>(wst + lane * 32);
+          sw[0] = reinterpret_cast<const uint4*>(codes)[0];
+          sw[1] = reinterpret_cast<const uint4*>(codes)[1];
         }
+        __syncwarp();
+        // this chunk's bytes [32 * b0, 32 * min(nb, b0 + 32)) of each copy's row:
+        // lane l stores the 16-byte pieces l and l + 32
+        const int bytes = 32 * (min(nb, b0 + 32) - b0);
+        const uint4 q0 = 16 * lane < bytes ? reinterpret_cast<const uint4*>(wst)[lane] : make_uint4(0, 0, 0, 0);
+        const uint4 q1 = 16 * (lane + 32) < bytes ? reinterpret_cast<const uint4*>(wst)[lane + 32] : q0;
+        __syncwarp();
+        const long long off = static_cast<long long>(b0) * 32;
+        uint4* d = reinterpret_cast<uint4*>(xq + t * H + off);
+        if (16 * lane < bytes) d[lane] = q0;
+        if (16 * (lane + 32) < bytes) d[lane + 32] = q1;
+        if (act && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(xq_sc + mx_tiled_scale_offset(t, b, cg)) = word;
         for (int jj = 0; jj < topk; ++jj) {   // all lanes take part in the shuffle
           const int pr = __shfl_sync(0xffffffffu, jj < 32 ? p_lo : p_hi, jj & 31);
-          if (!act) continue;
-          uint4* dp = reinterpret_cast<uint4*>(xp + static_cast<long long>(pr) * H + static_cast<long long>(b) * 32);
-          dp[0] = c0;
-          dp[1] = c1;
-          if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(xp_sc + mx_tiled_scale_offset(pr, b, cg)) = word;
+          uint4* dp = reinterpret_cast<uint4*>(xp + static_cast<long long>(pr) * H + off);
+          if (16 * lane < bytes) dp[lane] = q0;
+          if (16 * (lane + 32) < bytes) dp[lane + 32] = q1;
+          if (act && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(xp_sc + mx_tiled_scale_offset(pr, b, cg)) = word;
         }
       }
     } else if (j < T + max_rows) {
