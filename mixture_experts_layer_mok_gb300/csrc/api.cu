@@ -715,8 +715,11 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
   MOK_CUDA(cudaEventRecord(side->join, side->s));
   ctx->dispatch = MOK_DISPATCH_PERMUTE;
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 0, cs));
+  // MXFP8 forward / bf16 backward: the same pass also writes x's bf16 rows
+  // in schedule order, which the backward's gate/up weight gradient reads (a
+  // separate copy would contend for HBM with whichever GEMM it overlapped)
   MOK_CUDA(launch_mx_dispatch(x, T, H, k, s->slot_row, s->row_src, s->header, mr, ctx->xq, ctx->xq_sc, ctx->xq_perm,
-                              ctx->xq_perm_sc, sms, cs));
+                              ctx->xq_perm_sc, cfg->mode == MOK_MODE_MXFP8_FWD ? ctx->x_perm : nullptr, sms, cs));
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 1, cs));
   MOK_CUDA(cudaStreamWaitEvent(cs, side->join, 0));
 
@@ -795,17 +798,6 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
   }
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_DOWN, 1, cs));
 
-  // MXFP8 forward / bf16 backward: the backward's gate/up weight gradient
-  // reads x's bf16 token rows in schedule order.  The side stream writes them
-  // from here on, under the long, compute-bound routed gate/up GEMM (which
-  // uses a fraction of HBM bandwidth), instead of in the backward; handed back
-  // at `join2`, at the end of the forward.
-  if (cfg->mode == MOK_MODE_MXFP8_FWD) {
-    MOK_CUDA(cudaEventRecord(side->mid, cs));
-    MOK_CUDA(cudaStreamWaitEvent(side->s, side->mid, 0));
-    MOK_CUDA(launch_permute_rows(x, H, k, s->row_src, s->header, mr, ctx->x_perm, sms, side->s));
-    MOK_CUDA(cudaEventRecord(side->join2, side->s));
-  }
   // ---- routed experts
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_GATEUP, 0, cs));
   MxMaps m;
@@ -839,7 +831,6 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
   const long long items2 = static_cast<long long>(s->max_tiles) * q.n_tiles;
   MOK_CUDA(launch_dn(EPI_SCALE_ROWS, m2, q, items2, items2));
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DOWN, 1, cs));
-  if (cfg->mode == MOK_MODE_MXFP8_FWD) MOK_CUDA(cudaStreamWaitEvent(cs, side->join2, 0));
   return MOK_OK;
 }
 
@@ -1311,10 +1302,10 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
     MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 1, cs));
   }
   // ---- shared expert backward, first part (dense rows, w = 1): the SwiGLU
-  // backward and the dgrad, which read dy in token order.  They run while the
-  // side stream writes dy's rows in schedule order; the shared weight
-  // gradients, whose deep contractions over all T tokens suffer most from
-  // sharing HBM with that copy, run after the routed GEMMs.
+  // backward, which reads dy in token order while the side stream writes dy's
+  // rows in schedule order, and the dgrad.  A GEMM that shares HBM with that
+  // copy slows by more than the copy takes alone, so only this first GEMM
+  // overlaps it; the shared weight gradients run after the routed GEMMs.
   if (Is > 0) {
     const int bns = tile_n(Is);
     {
@@ -1338,6 +1329,7 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
         MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_MN_TILE, 128, EPI_DOWN_BWD>(m, p, items, 0, false, sms, cs)));
       MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DOWN, 1, cs));
     }
+    if (side) MOK_CUDA(cudaStreamWaitEvent(cs, side->join, 0));   // dy's schedule-order rows are written
     {  // dx_s = dG_s W_s_gate + dU_s W_s_up
       MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DGRAD, 0, cs));
       GemmMaps m;

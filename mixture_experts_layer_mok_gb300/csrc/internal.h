@@ -37,9 +37,10 @@ cudaError_t launch_schedule(const int64_t* te, int T, int k, int E, int cap_tile
                             cudaStream_t st);
 cudaError_t launch_mx_quantize(const uint16_t* x, long long nblocks, uint8_t* codes, uint8_t* scales,
                                int num_sms, cudaStream_t st);
+// xb (may be NULL): also write x's bf16 rows in schedule order (padding rows zero).
 cudaError_t launch_mx_dispatch(const uint16_t* x, int T, int H, int topk, const int* slot_row, const int* row_src,
                                const int* header, long long max_rows, uint8_t* xq, uint8_t* xq_sc, uint8_t* xp,
-                               uint8_t* xp_sc, int num_sms, cudaStream_t st);
+                               uint8_t* xp_sc, uint16_t* xb, int num_sms, cudaStream_t st);
 cudaError_t launch_mx_quantize_t(const uint16_t* src, long long ld, int batch, int R, int C, int valid_rows,
                                  const int* row_src, int topk, const int* header, uint8_t* codes, uint8_t* scales,
                                  int tiled, int num_sms, cudaStream_t st, uint8_t* rcodes = nullptr,

@@ -293,14 +293,17 @@ cudaError_t launch_mx_quantize(const uint16_t* x, long long nblocks, uint8_t* co
 __global__ void __launch_bounds__(256, 3) mx_dispatch_kernel(
     const uint16_t* __restrict__ x, int T, int H, int topk, const int* __restrict__ slot_row,
     const int* __restrict__ row_src, const int* __restrict__ header, long long max_rows, uint8_t* __restrict__ xq,
-    uint8_t* __restrict__ xq_sc, uint8_t* __restrict__ xp, uint8_t* __restrict__ xp_sc) {
+    uint8_t* __restrict__ xq_sc, uint8_t* __restrict__ xp, uint8_t* __restrict__ xp_sc, uint16_t* __restrict__ xb) {
   griddep_wait();
   griddep_launch_dependents();
   if (header[2] != 0) return;
-  // per warp: the codes of one 32-block chunk of a row (1 KB), so that every
-  // store instruction of the k + 1 copies writes 512 contiguous bytes
+  // per warp: the codes of one 32-block chunk of a row (1 KB) and, when the
+  // bf16 rows are wanted too, its bf16 values (2 KB), so that every store
+  // instruction of the copies writes 512 contiguous bytes
   __shared__ __align__(16) uint8_t stage[8][1024];
+  __shared__ __align__(16) uint8_t stage_b[8][2048];
   uint8_t* wst = stage[threadIdx.x >> 5];
+  uint4* wsb = reinterpret_cast<uint4*>(stage_b[threadIdx.x >> 5]);
   const long long P = header[1];
   const int lane = threadIdx.x & 31;
   const int nb = H / 32;             // blocks per row (a multiple of 4)
@@ -323,9 +326,10 @@ __global__ void __launch_bounds__(256, 3) mx_dispatch_kernel(
         const int b = b0 + lane;
         const bool act = b < nb;       // whole aligned groups of 4 lanes share this
         float v[32];
+        uint4 vraw[4] = {raw[0], raw[1], raw[2], raw[3]};
         if (act) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = bf16_at(raw, i);
+          for (int i = 0; i < 32; ++i) v[i] = bf16_at(vraw, i);
         }
         if (b0 + 32 + lane < nb) load_raw64(xrow + (b0 + 32 + lane) * 32, raw);
         uint8_t codes[32];
@@ -340,6 +344,10 @@ __global__ void __launch_bounds__(256, 3) mx_dispatch_kernel(
           uint4* sw = reinterpret_cast<uint4*>(wst + lane * 32);
           sw[0] = reinterpret_cast<const uint4*>(codes)[0];
           sw[1] = reinterpret_cast<const uint4*>(codes)[1];
+          if (xb) {   // this lane's 64 bf16 bytes, pieces swizzled against bank conflicts
+#pragma unroll
+            for (int q = 0; q < 4; ++q) wsb[lane * 4 + (q ^ (lane & 3))] = vraw[q];
+          }
         }
         __syncwarp();
         // this chunk's bytes [32 * b0, 32 * min(nb, b0 + 32)) of each copy's row:
@@ -359,13 +367,27 @@ __global__ void __launch_bounds__(256, 3) mx_dispatch_kernel(
           if (16 * lane < bytes) dp[lane] = q0;
           if (16 * (lane + 32) < bytes) dp[lane + 32] = q1;
           if (act && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(xp_sc + mx_tiled_scale_offset(pr, b, cg)) = word;
+          if (xb) {   // the chunk's bf16 bytes: its piece i (16 bytes) is piece
+                      // (i % 4) ^ ((i / 4) % 4) of block i / 4 in the staging layout
+            uint4* db = reinterpret_cast<uint4*>(xb + static_cast<long long>(pr) * H + off);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int i = lane + 32 * q, blk = i >> 2;
+              if (16 * i < 2 * bytes) db[i] = wsb[blk * 4 + ((i & 3) ^ (blk & 3))];
+            }
+          }
         }
+        __syncwarp();   // the staging is read before the next chunk overwrites it
       }
     } else if (j < T + max_rows) {
       const long long pr = j - T;
       if (pr >= P || __ldg(row_src + pr) >= 0) continue;
       uint4* d = reinterpret_cast<uint4*>(xp + pr * H);
       for (int i = lane; i < H / 16; i += 32) d[i] = make_uint4(0, 0, 0, 0);
+      if (xb) {
+        uint4* db = reinterpret_cast<uint4*>(xb + pr * H);
+        for (int i = lane; i < H / 8; i += 32) db[i] = make_uint4(0, 0, 0, 0);
+      }
       for (int g = lane; g < cg; g += 32)
         *reinterpret_cast<uint32_t*>(xp_sc + mx_tiled_scale_offset(pr, 4 * g, cg)) = 0x7F7F7F7Fu;
     } else {
@@ -378,10 +400,10 @@ __global__ void __launch_bounds__(256, 3) mx_dispatch_kernel(
 
 cudaError_t launch_mx_dispatch(const uint16_t* x, int T, int H, int topk, const int* slot_row, const int* row_src,
                                const int* header, long long max_rows, uint8_t* xq, uint8_t* xq_sc, uint8_t* xp,
-                               uint8_t* xp_sc, int num_sms, cudaStream_t st) {
+                               uint8_t* xp_sc, uint16_t* xb, int num_sms, cudaStream_t st) {
   const long long jobs = T + max_rows + ((static_cast<long long>(T) + 127) / 128 * 128 - T);
   cudaError_t err = launch_dependent(mx_dispatch_kernel, dim3(grid_for(jobs * 32, 256, num_sms)), dim3(256), 0, st, x,
-                                     T, H, topk, slot_row, row_src, header, max_rows, xq, xq_sc, xp, xp_sc);
+                                     T, H, topk, slot_row, row_src, header, max_rows, xq, xq_sc, xp, xp_sc, xb);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }

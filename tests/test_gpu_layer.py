@@ -327,7 +327,8 @@ def _untile_scales(tiled, rows, K):
 def test_mxfp8_dispatch_codes_and_scales_bit_exact(name):
     """The MXFP8 forward's quantise-and-dispatch step: x's E4M3 codes and E8M0
     scales in token order and in schedule order equal the oracle's quantiser,
-    row for row; padding rows hold zero codes and unit scales."""
+    row for row; padding rows hold zero codes and unit scales.  The bf16 rows
+    it copies into schedule order are x's rows, bit for bit."""
     m = mok()
     inp = _inputs(name, seed=3)
     T, H, k = inp.meta["T"], inp.meta["H"], inp.meta["k"]
@@ -354,6 +355,11 @@ def test_mxfp8_dispatch_codes_and_scales_bit_exact(name):
     assert np.array_equal(xp[valid], codes[tok[valid]])
     assert np.array_equal(xps[valid], scales[tok[valid]])
     assert np.all(xp[~valid] == 0) and np.all(xps[~valid] == 127)
+    # the same pass writes x's bf16 rows in schedule order for the bf16 backward
+    xb = _ctx_bytes(ctx, "x_perm", P * H * 2).view(np.uint16).reshape(P, H)
+    x16 = inp.x.view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(xb[valid], x16[tok[valid]])
+    assert np.all(xb[~valid] == 0)
 
 
 @pytest.mark.parametrize("name,mode", [("ragged_shared", "bf16"), ("wide", "bf16"), ("skewed", "bf16"),
