@@ -935,6 +935,13 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI, PAIR>::kThreads
         if (v_bwd) {
           const uint16_t* gu = static_cast<const uint16_t*>(p.aux0) + static_cast<long long>(prow) * 2 * p.N + n0 +
                                epi_c0 * 32;
+          // the rest of this row's gate|up for the tile (128-byte lines of two
+          // 32-column chunks; the first line is loaded just below) into L2
+          // while the accumulator fills, so that each chunk's loads hit L2
+          for (int c = 2; c < epi_c1 - epi_c0; c += 2) {
+            prefetch_l2(gu + c * 32);
+            prefetch_l2(gu + p.N + c * 32);
+          }
           load_raw64(gu, ng);
           load_raw64(gu + p.N, nu);
         }

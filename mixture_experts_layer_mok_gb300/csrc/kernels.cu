@@ -746,7 +746,17 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(const uint16_t* __res
       for (int i = lane; i < per_row; i += 32) d[i] = make_uint4(0, 0, 0, 0);
     } else {
       const uint4* s = reinterpret_cast<const uint4*>(src + static_cast<long long>(f / topk) * H);
-      for (int i = lane; i < per_row; i += 32) d[i] = __ldg(s + i);
+      // four 16-byte loads per lane in flight before their stores (a row of
+      // H = 7168 bf16 values is 28 pieces per lane)
+      int i = lane;
+      for (; i + 96 < per_row; i += 128) {
+        const uint4 a = __ldg(s + i), b = __ldg(s + i + 32), c = __ldg(s + i + 64), e = __ldg(s + i + 96);
+        d[i] = a;
+        d[i + 32] = b;
+        d[i + 64] = c;
+        d[i + 96] = e;
+      }
+      for (; i < per_row; i += 32) d[i] = __ldg(s + i);
     }
   }
 }

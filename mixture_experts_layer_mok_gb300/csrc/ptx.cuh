@@ -145,6 +145,11 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// Hint: bring the 128-byte line holding p into L2 (no register, no wait).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
 // ---------------------------------------------------------------- cp.async
 // 16-byte global -> shared copy through L2 (generic proxy); src_bytes = 0
 // writes zeros.
