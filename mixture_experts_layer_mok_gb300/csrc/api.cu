@@ -587,7 +587,7 @@ mok_status_t forward_bf16(const mok_config_t* cfg, const uint16_t* x, const floa
     MOK_CUDA(cudaEventRecord(side->fork, cs));
     MOK_CUDA(cudaStreamWaitEvent(side->s, side->fork, 0));
     MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 0, side->s));
-    MOK_CUDA(launch_permute_rows(x, H, k, s->row_src, s->header, mr, ctx->x_perm, sms, side->s));
+    MOK_CUDA(launch_permute_rows(x, T, H, k, s->slot_row, s->row_src, s->header, mr, ctx->x_perm, sms, side->s));
     MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 1, side->s));
     MOK_CUDA(cudaEventRecord(side->join, side->s));
   } else {
@@ -1291,10 +1291,10 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
       x_rows = ctx->x_perm;
     } else {
       if (!L.xb_perm) return fail(MOK_ERR_INVALID_ARG, "context holds no schedule-order copy of x");
-      MOK_CUDA(launch_permute_rows(x, H, k, s->row_src, s->header, mr, L.xb_perm, sms, side->s));
+      MOK_CUDA(launch_permute_rows(x, T, H, k, s->slot_row, s->row_src, s->header, mr, L.xb_perm, sms, side->s));
       x_rows = L.xb_perm;
     }
-    MOK_CUDA(launch_permute_rows(dy, H, k, s->row_src, s->header, mr, L.dy_perm, sms, side->s));
+    MOK_CUDA(launch_permute_rows(dy, T, H, k, s->slot_row, s->row_src, s->header, mr, L.dy_perm, sms, side->s));
     MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 1, side->s));
     MOK_CUDA(cudaEventRecord(side->join, side->s));
   } else {

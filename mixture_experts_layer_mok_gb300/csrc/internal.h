@@ -65,8 +65,8 @@ constexpr int kMaxScaleJobs = 6;
 cudaError_t launch_mx_tile_scales(const MxTileScaleJob* jobs, int n, cudaStream_t st);
 cudaError_t launch_combine(const uint16_t* rows, const int* slot_row, const int* header, long long max_rows,
                            const uint16_t* base, int T, int k, int H, uint16_t* out, int num_sms, cudaStream_t st);
-cudaError_t launch_permute_rows(const uint16_t* src, int H, int topk, const int* row_src, const int* header,
-                                long long max_rows, uint16_t* out, int num_sms, cudaStream_t st);
+cudaError_t launch_permute_rows(const uint16_t* src, int T, int H, int topk, const int* slot_row, const int* row_src,
+                                const int* header, long long max_rows, uint16_t* out, int num_sms, cudaStream_t st);
 cudaError_t launch_dw_reduce(const float* part, int nf, int ntiles, float* dw, cudaStream_t st);
 
 // Grouped GEMM launch: instantiated for the operand sources / tile widths /

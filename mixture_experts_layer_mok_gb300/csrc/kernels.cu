@@ -725,10 +725,15 @@ cudaError_t launch_combine(const uint16_t* rows, const int* slot_row, const int*
 // ===========================================================================
 // Dispatch permutation: out[p] = src[row_src[p] / k] for every schedule row
 // p < P (zeros for padding rows), so the routed GEMMs read their gathered
-// operand as dense TMA tiles.  One warp per row, 16-byte accesses; bandwidth
-// bound (reads x or dy from L2, writes P rows).
+// operand as dense TMA tiles.  Token-major: one warp per token reads its row
+// once and writes it to the token's k schedule rows (slot_row), four 16-byte
+// pieces per lane in flight, each store instruction 512 contiguous bytes; then
+// one warp per padding row writes zeros.  Bandwidth bound: T*H*2 bytes read,
+// P*H*2 written (a row-major walk over schedule rows would read each token row
+// k times).
 // ===========================================================================
-__global__ void __launch_bounds__(256) permute_rows_kernel(const uint16_t* __restrict__ src, int H, int topk,
+__global__ void __launch_bounds__(256) permute_rows_kernel(const uint16_t* __restrict__ src, int T, int H, int topk,
+                                                           const int* __restrict__ slot_row,
                                                            const int* __restrict__ row_src,
                                                            const int* __restrict__ header, long long max_rows,
                                                            uint16_t* __restrict__ out) {
@@ -737,35 +742,41 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(const uint16_t* __res
   if (header[2] != 0) return;
   const long long P = header[1];
   const int lane = threadIdx.x & 31;
-  const int per_row = H / 8;  // 16-byte words per row
-  for (long long q = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5; q < P && q < max_rows;
-       q += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
-    const int f = __ldg(row_src + q);
-    uint4* d = reinterpret_cast<uint4*>(out + q * H);
-    if (f < 0) {
-      for (int i = lane; i < per_row; i += 32) d[i] = make_uint4(0, 0, 0, 0);
-    } else {
-      const uint4* s = reinterpret_cast<const uint4*>(src + static_cast<long long>(f / topk) * H);
-      // four 16-byte loads per lane in flight before their stores (a row of
-      // H = 7168 bf16 values is 28 pieces per lane)
-      int i = lane;
-      for (; i + 96 < per_row; i += 128) {
-        const uint4 a = __ldg(s + i), b = __ldg(s + i + 32), c = __ldg(s + i + 64), e = __ldg(s + i + 96);
-        d[i] = a;
-        d[i + 32] = b;
-        d[i + 64] = c;
-        d[i + 96] = e;
+  const int per_row = H / 8;  // 16-byte pieces per row
+  const long long jobs = T + max_rows;
+  for (long long j = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5; j < jobs;
+       j += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
+    if (j < T) {
+      const int p_lo = lane < topk ? __ldg(slot_row + j * topk + lane) : -1;
+      const int p_hi = lane + 32 < topk ? __ldg(slot_row + j * topk + lane + 32) : -1;
+      const uint4* s = reinterpret_cast<const uint4*>(src + j * H);
+      for (int i0 = 0; i0 < per_row; i0 += 128) {
+        uint4 v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (i0 + lane + 32 * q < per_row) v[q] = __ldg(s + i0 + lane + 32 * q);
+        for (int jj = 0; jj < topk; ++jj) {   // all lanes take part in the shuffle
+          const long long pr = __shfl_sync(0xffffffffu, jj < 32 ? p_lo : p_hi, jj & 31);
+          uint4* d = reinterpret_cast<uint4*>(out + pr * H);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (i0 + lane + 32 * q < per_row) d[i0 + lane + 32 * q] = v[q];
+        }
       }
-      for (; i < per_row; i += 32) d[i] = __ldg(s + i);
+    } else {
+      const long long pr = j - T;
+      if (pr >= P || __ldg(row_src + pr) >= 0) continue;
+      uint4* d = reinterpret_cast<uint4*>(out + pr * H);
+      for (int i = lane; i < per_row; i += 32) d[i] = make_uint4(0, 0, 0, 0);
     }
   }
 }
 
-cudaError_t launch_permute_rows(const uint16_t* src, int H, int topk, const int* row_src, const int* header,
-                                long long max_rows, uint16_t* out, int num_sms, cudaStream_t st) {
+cudaError_t launch_permute_rows(const uint16_t* src, int T, int H, int topk, const int* slot_row, const int* row_src,
+                                const int* header, long long max_rows, uint16_t* out, int num_sms, cudaStream_t st) {
   if (max_rows == 0) return cudaSuccess;
-  cudaError_t err = launch_dependent(permute_rows_kernel, dim3(grid_for(max_rows * 32, 256, num_sms)), dim3(256), 0, st,
-                                     src, H, topk, row_src, header, max_rows, out);
+  cudaError_t err = launch_dependent(permute_rows_kernel, dim3(grid_for((T + max_rows) * 32, 256, num_sms)), dim3(256),
+                                     0, st, src, T, H, topk, slot_row, row_src, header, max_rows, out);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
