@@ -769,7 +769,8 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
     MxMaps m;
     if ((st = make_map_u8(&m.a, ctx->xq, H, T, 128)) || (st = make_map_u8(&m.b0, w->mxs_gate, H, Is, gu_box)) ||
         (st = make_map_u8(&m.b1, w->mxs_up, H, Is, gu_box)) ||
-        (st = make_map_sf(&m.sfa, ctx->xq_sc, t_atoms * (H / 128))) || (st = gu_sf_maps(m, X.wsg_sc, X.wsu_sc, Is)))
+        (st = make_map_sf(&m.sfa, ctx->xq_sc, t_atoms * (H / 128))) || (st = gu_sf_maps(m, X.wsg_sc, X.wsu_sc, Is)) ||
+        (st = make_map_out(&m.o0, ctx->gu_s, 2ull * Is, T)) || (st = make_map_codes_out(&m.o1, ctx->hq_s, Is, T)))
       return st;
     GemmParams p = base_params(cfg, nullptr, ctx->status, 0);
     p.rows = T; p.K = H; p.N = Is; p.n_tiles = Is / gu_cols; p.b_rows_per_expert = 0;
@@ -783,7 +784,8 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
     MxMaps m2;
     if ((st = make_map_u8(&m2.a, ctx->hq_s, Is, T, 128)) || (st = make_map_u8(&m2.b0, w->mxs_down, Is, H, dn_box)) ||
         (st = make_map_sf(&m2.sfa, ctx->hq_s_sc, t_atoms * (Is / 128))) ||
-        (st = make_map_sf(&m2.sfb0, X.wsd_sc, (H / 128) * (Is / 128))))
+        (st = make_map_sf(&m2.sfb0, X.wsd_sc, (H / 128) * (Is / 128))) ||
+        (st = make_map_out(&m2.o0, ctx->shared_out, H, T)))
       return st;
     m2.b1 = m2.b0;
     m2.sfb1 = m2.sfb0;
@@ -805,7 +807,8 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
       (st = make_map_u8(&m.b0, w->mx_gate, H, static_cast<uint64_t>(E) * I, gu_box)) ||
       (st = make_map_u8(&m.b1, w->mx_up, H, static_cast<uint64_t>(E) * I, gu_box)) ||
       (st = make_map_sf(&m.sfa, ctx->xq_perm_sc, r_atoms * (H / 128))) ||
-      (st = gu_sf_maps(m, X.wg_sc, X.wu_sc, static_cast<long long>(E) * I)))
+      (st = gu_sf_maps(m, X.wg_sc, X.wu_sc, static_cast<long long>(E) * I)) ||
+      (st = make_map_out(&m.o0, ctx->gu, 2ull * I, mr)) || (st = make_map_codes_out(&m.o1, ctx->hq, I, mr)))
     return st;
   GemmParams p = base_params(cfg, s, ctx->status, cfg->debug_flags);
   p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / gu_cols; p.b_rows_per_expert = I;
@@ -820,7 +823,8 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
   if ((st = make_map_u8(&m2.a, ctx->hq, I, mr, 128)) ||
       (st = make_map_u8(&m2.b0, w->mx_down, I, static_cast<uint64_t>(E) * H, dn_box)) ||
       (st = make_map_sf(&m2.sfa, ctx->hq_sc, r_atoms * (I / 128))) ||
-      (st = make_map_sf(&m2.sfb0, X.wd_sc, (static_cast<long long>(E) * H / 128) * (I / 128))))
+      (st = make_map_sf(&m2.sfb0, X.wd_sc, (static_cast<long long>(E) * H / 128) * (I / 128))) ||
+      (st = make_map_out(&m2.o0, ctx->slots, H, mr)))
     return st;
   m2.b1 = m2.b0;
   m2.sfb1 = m2.sfb0;
@@ -948,7 +952,7 @@ mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const u
       MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DGRAD, 0, cs));
       MxMaps m;
       if ((st = make_map_u8(&m.a, L.dgusq, 2ull * Is, T, 128)) || (st = make_map_u8(&m.b0, w->mxts_gate, Is, H, bnH)) ||
-          (st = make_map_u8(&m.b1, w->mxts_up, Is, H, bnH)))
+          (st = make_map_u8(&m.b1, w->mxts_up, Is, H, bnH)) || (st = make_map_out(&m.o0, L.dx_s, H, T)))
         return st;
       GemmParams p = base_params(cfg, nullptr, ctx->status, 0);
       p.rows = T; p.K = 2 * Is; p.N = H; p.n_tiles = H / bnH; p.b_rows_per_expert = 0; p.b_split = Is;
@@ -1015,7 +1019,8 @@ mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const u
     MxMaps m;
     if ((st = make_map_u8(&m.a, L.dguq, 2ull * I, mr, 128)) ||
         (st = make_map_u8(&m.b0, w->mxt_gate, I, static_cast<uint64_t>(E) * H, bnH)) ||
-        (st = make_map_u8(&m.b1, w->mxt_up, I, static_cast<uint64_t>(E) * H, bnH)))
+        (st = make_map_u8(&m.b1, w->mxt_up, I, static_cast<uint64_t>(E) * H, bnH)) ||
+        (st = make_map_out(&m.o0, L.dx_slots, H, mr)))
       return st;
     GemmParams p = base_params(cfg, s, ctx->status, 0);
     p.grouped = 1; p.K = 2 * I; p.N = H; p.n_tiles = H / bnH; p.b_rows_per_expert = H; p.b_split = I;

@@ -57,7 +57,11 @@ struct MxCfg {
   static constexpr int kBarBytes = 512;
   // per epilogue warp: one 32-row staging block (2 KB); the MXFP8 SwiGLU
   // backward stages its three 32 x 32 output blocks (dG, dU, w h)
-  static constexpr int kEpiStageBytes = EPI == EPI_DOWN_BWD_MX ? 3 * 2048 : 2048;
+  // per epilogue warp: the staging of its TMA stores (a 32 x 32 bf16 block;
+  // the SwiGLU adds a 32 x 32 block of E4M3 codes; the MXFP8 SwiGLU backward
+  // stages its three 32 x 32 output blocks)
+  static constexpr int kEpiStageBytes =
+      EPI == EPI_DOWN_BWD_MX ? 3 * 2048 : (EPI == EPI_SWIGLU_MX ? 2048 + 1024 : 2048);
   static constexpr int kStagesFit =
       (227 * 1024 - 1024 - kBarBytes - kEpiWarps * kEpiStageBytes) / (kStageBytes + kSfStride);
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
@@ -121,6 +125,44 @@ __device__ __forceinline__ uint32_t mx_col_from_stage(const uint32_t* blk, int l
     v[i] = __uint_as_float((lane & 1) ? (x & 0xFFFF0000u) : (x << 16));
   }
   return mx_store_codes(v, dst);
+}
+
+// Warp-cooperative TMA store of a 32-row x 32-column bf16 block at {col, row}
+// through one 2 KB staging block (the 64-byte-swizzled layout of the output's
+// tensor map): each lane hands in 16 packed words of its row.  The staging is
+// reused once the previous bulk copy of lane 0 has read it.
+__device__ __forceinline__ void warp_store_tma1(const uint32_t* w, const CUtensorMap* map, int col, int row,
+                                                uint8_t* stage, int lane) {
+  if (lane == 0) bulk_wait_read<0>();
+  __syncwarp();
+  uint4* s = reinterpret_cast<uint4*>(stage);
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    s[lane * 4 + (j ^ sw)] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+  fence_proxy_async_smem();   // generic-proxy writes, then the async-proxy read
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(map, stage, col, row);
+    bulk_commit();
+  }
+}
+
+// The same for a 32-row x 32-byte block of E4M3 codes (unswizzled 1 KB
+// staging, row r at byte 32 r): each lane hands in its row's 32 codes.
+__device__ __forceinline__ void warp_store_codes_tma(const uint8_t* codes, const CUtensorMap* map, int col, int row,
+                                                     uint8_t* stage, int lane) {
+  if (lane == 0) bulk_wait_read<0>();
+  __syncwarp();
+  uint4* s = reinterpret_cast<uint4*>(stage + lane * 32);
+  s[0] = reinterpret_cast<const uint4*>(codes)[0];
+  s[1] = reinterpret_cast<const uint4*>(codes)[1];
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(map, stage, col, row);
+    bulk_commit();
+  }
 }
 
 // Shared-memory descriptor of a 512-byte scale atom as the tcgen05.cp source:
@@ -450,10 +492,12 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
       }
 
       uint32_t wv[16];
+      const int orow = it.p0 + q * 32;     // first row of this warp's 32 rows
       if constexpr (EPI == EPI_SWIGLU_MX) {
-        // out0 = gu [rows][2N] (bf16), out1 = h codes [rows][N], sf_out = h scales
+        // map o0 = G|U [rows][2N] (bf16), o1 = h codes [rows][N], sf_out = h
+        // scales; both stored by TMA in 32-row blocks (rows past a dense
+        // layer's end are clipped; a grouped tile's padding rows are zeros)
         constexpr int kH = kCols / 2;        // h columns of this thread
-        const bool inb = (p.grouped ? true : valid) && live;
         const int col0 = n0 + half * kH;
         float* g = v;
         float* u = v + kH;
@@ -461,13 +505,12 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
 #pragma unroll
           for (int i = 0; i < kCols; ++i) v[i] = 0.f;
         }
-        uint16_t* gu = inb ? static_cast<uint16_t*>(p.out0) + static_cast<long long>(prow) * 2 * p.N + col0 : nullptr;
 #pragma unroll
         for (int c = 0; c < kH / 32; ++c) {
           pack_bf16x32(g + c * 32, wv);
-          warp_store_row64(wv, gu ? gu + c * 32 : nullptr, wstage, lane);
+          if (live) warp_store_tma1(wv, &maps.o0, col0 + c * 32, orow, wstage, lane);
           pack_bf16x32(u + c * 32, wv);
-          warp_store_row64(wv, gu ? gu + p.N + c * 32 : nullptr, wstage, lane);
+          if (live) warp_store_tma1(wv, &maps.o0, p.N + col0 + c * 32, orow, wstage, lane);
         }
         uint32_t sc = 0;
 #pragma unroll
@@ -487,12 +530,7 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
           uint8_t codes[32];
           const uint32_t s8 = mx_quantize32(hv, codes);
           sc |= s8 << (8 * c);
-          if (inb) {
-            uint4* d = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out1) + static_cast<long long>(prow) * p.N +
-                                                col0 + c * 32);
-            d[0] = reinterpret_cast<const uint4*>(codes)[0];
-            d[1] = reinterpret_cast<const uint4*>(codes)[1];
-          }
+          if (live) warp_store_codes_tma(codes, &maps.o1, col0 + c * 32, orow, wstage + 2048, lane);
         }
         // the scales of this thread's blocks are adjacent bytes of its row's word
         // (rows past the end of a dense layer get the unit scales of zeros)
@@ -646,10 +684,9 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
         }
         if (p.grouped && v_ok) p.dw_part[(static_cast<long long>(f) * p.n_tiles + it.nt) * 2 + half] = dpart;
       } else {
-        // rows in schedule order (router-weighted: the combine reads them
-        // back per (token, k) through slot_row), or dense rows
-        uint16_t* dst = nullptr;
-        if (valid) dst = static_cast<uint16_t*>(p.out0) + static_cast<long long>(prow) * p.ld + n0 + half * kCols;
+        // map o0 = rows in schedule order (router-weighted: the combine reads
+        // them back per (token, k) through slot_row; a tile's padding rows get
+        // zeros), or dense rows (clipped past the layer's end), by TMA
 #pragma unroll
         for (int c = 0; c < kCols / 32; ++c) {
           if (EPI == EPI_SCALE_ROWS) {
@@ -657,13 +694,11 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
             for (int i = 0; i < 32; ++i) v[c * 32 + i] *= wt;
           }
           pack_bf16x32(v + c * 32, wv);
-          warp_store_row64(wv, dst ? dst + c * 32 : nullptr, wstage, lane);
+          if (live) warp_store_tma1(wv, &maps.o0, n0 + half * kCols + c * 32, orow, wstage, lane);
         }
       }
     }
-    if constexpr (EPI == EPI_DOWN_BWD_MX) {
-      if (lane == 0) bulk_wait<0>();   // this warp's TMA stores are complete before the CTA ends
-    }
+    if (lane == 0) bulk_wait<0>();   // this warp's TMA stores are complete before the CTA ends
   }
 
   tc_fence_before();
