@@ -90,28 +90,55 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int n, int E, int nchu
     }
     return;
   }
-  int c = 0;
-  if (e < E) {
-    // each chunk's count becomes its exclusive offset within expert e; eight
-    // chunks per round so the loads overlap
+  // each chunk's count becomes its exclusive offset within its expert.  The
+  // chunks are split over `tpe` threads per expert (all 1024 threads when E
+  // is small): each sums its run of chunks, the runs' sums are scanned in
+  // shared memory, and each thread rewrites its run from its base, sixteen
+  // loads in flight per round.
+  __shared__ int part[1024];
+  int tpe = 1;
+  while (tpe * 2 * E <= 1024) tpe *= 2;
+  const int ee = threadIdx.x / tpe, sub = threadIdx.x % tpe;
+  const int per = (nchunks + tpe - 1) / tpe;
+  const int k0 = min(nchunks, sub * per), k1 = min(nchunks, k0 + per);
+  int sum = 0;
+  if (ee < E) {
+    int k = k0;
+    for (; k + 16 <= k1; k += 16) {
+      int v[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) v[q] = hist[(k + q) * E + ee];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) sum += v[q];
+    }
+    for (; k < k1; ++k) sum += hist[k * E + ee];
+  }
+  part[threadIdx.x] = sum;
+  __syncthreads();
+  if (ee < E) {
     int run = 0;
-    int k = 0;
-    for (; k + 8 <= nchunks; k += 8) {
-      int v[8];
+    for (int q = 0; q < sub; ++q) run += part[ee * tpe + q];
+    int k = k0;
+    for (; k + 16 <= k1; k += 16) {
+      int v[16];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) v[q] = hist[(k + q) * E + e];
+      for (int q = 0; q < 16; ++q) v[q] = hist[(k + q) * E + ee];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        hist[(k + q) * E + e] = run;
+      for (int q = 0; q < 16; ++q) {
+        hist[(k + q) * E + ee] = run;
         run += v[q];
       }
     }
-    for (; k < nchunks; ++k) {
-      const int v = hist[k * E + e];
-      hist[k * E + e] = run;
+    for (; k < k1; ++k) {
+      const int v = hist[k * E + ee];
+      hist[k * E + ee] = run;
       run += v;
     }
-    c = run;
+  }
+  __syncthreads();
+  int c = 0;
+  if (e < E) {
+    for (int q = 0; q < tpe; ++q) c += part[e * tpe + q];
     cnt[e] = c;
   }
   int total_rows;
