@@ -55,7 +55,8 @@ typedef int mok_status_t;
 #define MOK_OK               0
 #define MOK_ERR_INVALID_ARG  1  /* bad size, NULL or misaligned pointer, short buffer */
 #define MOK_ERR_INDEX        2  /* an expert id outside [0, E) */
-#define MOK_ERR_CAPACITY     3  /* reserved: the capacity split never drops rows */
+#define MOK_ERR_CAPACITY     3  /* one expert's rows do not fit the macrobatch ring (the
+                                   capacity split itself never drops rows) */
 #define MOK_ERR_UNSUPPORTED  4  /* not an sm_103a device, or a shape outside the kernels' contract */
 #define MOK_ERR_TIMEOUT      5  /* a bounded device-side wait gave up */
 #define MOK_ERR_CUDA         6  /* a CUDA runtime call failed */
@@ -163,6 +164,34 @@ typedef struct {
                           the clamp (gate gradient where G <= L, up gradient
                           where |U| <= L).  Negative or non-finite:
                           MOK_ERR_INVALID_ARG. */
+  int64_t macrobatch_size; /* rows of the token ring ([MoKEd] "Tuning the five
+                          hyperparameters before production": macrobatch_size
+                          is the token ring buffer size; a value that holds
+                          every row means the ring is used once).  A routed
+                          row is one token's copy for one expert.  0, or a
+                          size of at least max_tiles * 128 rows, runs the
+                          routed experts in one pass over buffers for the
+                          whole schedule.  A smaller size, rounded up to a
+                          multiple of 128, bounds every schedule-order scratch
+                          buffer of the call (the token rows, h, dG|dU, w*h
+                          and their MXFP8 codes): the routed experts then run
+                          window by window, each window a run of whole
+                          experts in expert order whose padded rows fit the
+                          ring (mok_macrobatch_plan), so no contraction is
+                          split and every result bit equals the single pass.
+                          The saved gate|up pre-activations and the per-row
+                          outputs the fixed-order combines read (y's and dx's
+                          schedule-order rows) stay full size.  Such a call
+                          reads the expert counts back to the host once
+                          (it synchronises `stream`, so it cannot be captured
+                          in a CUDA graph), and fails with MOK_ERR_CAPACITY,
+                          enqueueing no layer work, when one expert's padded
+                          rows exceed the ring.  Size the buffers with
+                          mok_ctx_bytes_ring / mok_bwd_workspace_bytes_ring.
+                          With a ring, per-stage events of the routed stages
+                          bracket all windows (from the stage's start in the
+                          first window to its end in the last), so their
+                          intervals overlap.  Negative: MOK_ERR_INVALID_ARG. */
 } mok_config_t;
 
 /* The dispatch/combine schedule ([MoKEd] "The two API layers and the
@@ -180,7 +209,8 @@ typedef struct {
   int32_t* tile_expert;   /* [max_tiles] expert of each 128-row tile, or -1 */
   int32_t* tile_row0;     /* [max_tiles] first schedule row of the tile, or -1 */
   int32_t* tile_rows;     /* [max_tiles] valid rows in the tile (1..128), or -1 */
-  int32_t* header;        /* [8] num_tiles, P, status, num_primary, num_pairs, 0... */
+  int32_t* header;        /* [8] num_tiles, P, status, num_primary, num_pairs, cap_tiles
+                             (the per-expert budget of the primary list), 0, 0 */
   int32_t* scratch;       /* internal: per-chunk histograms */
   int32_t* pair_tile;     /* [max_tiles][2] tile pairs for CTA-pair GEMMs: two consecutive
                              tiles of one expert (within the primary list, then within the
@@ -228,7 +258,8 @@ typedef struct {
   uint8_t*  hq;       /* [max_tiles*128][I]  SwiGLU output E4M3 codes, MXFP8 mode (scratch) */
   uint8_t*  hq_sc;    /* its E8M0 scales, tensor-core scale layout (below) */
   uint16_t* slots;    /* [max_tiles*128][H] router-weighted expert outputs in schedule order
-                         (scratch; the combine reads row slot_row[t*k + j] for (t, j)) */
+                         (scratch; the combine reads row slot_row[t*k + j] for (t, j)).
+                         The backward reuses it for its dx rows in schedule order. */
   uint16_t* gu_s;     /* [T][2 I_s] shared gate | up (saved) */
   uint16_t* h_s;      /* [T][I_s] shared SwiGLU output, bf16 mode (scratch) */
   uint8_t*  hq_s;     /* [T][I_s] shared SwiGLU output codes, MXFP8 mode */
@@ -244,6 +275,11 @@ typedef struct {
   uint8_t*  xq_perm;  /* [max_tiles*128][H] x codes in schedule order, MXFP8 mode (scratch) */
   uint8_t*  xq_perm_sc; /* their scales, tensor-core scale layout */
   float swiglu_limit; /* the forward's mok_config_t.swiglu_limit */
+  int64_t ring_rows;  /* 0: the forward ran in one pass and its schedule-order
+                         scratch (x_perm, h, hq, xq_perm) spans the whole
+                         schedule; else the rows of its macrobatch ring: that
+                         scratch holds one window, and x_perm is NULL in
+                         MOK_MODE_MXFP8_FWD */
 } mok_ctx_t;
 /* Tensor-core scale layout (MXFP8 context scratch): the E8M0 scales of a
  * [R][K] code tensor as 512-byte atoms, one per (128-row block rb, 128-column
@@ -354,6 +390,8 @@ mok_status_t mok_mxfp8_quantize_dual(const uint16_t* x, int64_t batch, int rows,
  * x bf16 [T][H]; router_w fp32 [T][k]; y bf16 [T][H].  The context buffer
  * (mok_ctx_bytes) must stay alive and unmodified until mok_backward. */
 size_t mok_ctx_bytes(int T, int k, int E, int H, int I, int I_s, int mode);
+/* The context bytes for mok_config_t.macrobatch_size (0: mok_ctx_bytes). */
+size_t mok_ctx_bytes_ring(int T, int k, int E, int H, int I, int I_s, int mode, int64_t macrobatch_size);
 mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x,
                          const float* router_w, const mok_schedule_t* sched,
                          const mok_weights_t* w, uint16_t* y, void* ctx_buf,
@@ -375,8 +413,30 @@ mok_status_t mok_ctx_status(const mok_ctx_t* ctx, int* status);
  * roundings of dG, dU and w*h.  x and router_w are the forward's inputs.  Outputs:
  * dx bf16 [T][H], d_router_w fp32 [T][k] (= <dy[t], F_e(x[t])>), the six
  * weight gradients.  Scratch comes from `ws` (mok_bwd_workspace_bytes with
- * the context's mode).  Device errors land in ctx->status. */
+ * the context's mode) and from the context's slots, the forward's scratch,
+ * which receive the dx rows in schedule order; the saved activations are only
+ * read, so the backward may run again on the same context.  Device errors
+ * land in ctx->status. */
 size_t mok_bwd_workspace_bytes(int T, int k, int E, int H, int I, int I_s, int mode);
+/* The workspace bytes for mok_config_t.macrobatch_size (0:
+ * mok_bwd_workspace_bytes).  The backward's ring is its own: it need not
+ * match the forward's. */
+size_t mok_bwd_workspace_bytes_ring(int T, int k, int E, int H, int I, int I_s, int mode,
+                                    int64_t macrobatch_size);
+
+/* ---- macrobatch windows ([MoKEd] "Tuning the five hyperparameters before
+ * production": macrobatch_size) ----------------------------------------
+ * The windows a ring of macrobatch_size rows (rounded up to a multiple of
+ * 128) runs the routed experts in, from the per-expert row counts cnt (a
+ * HOST array of E counts, as the schedule's cnt): experts in order, each
+ * padded to a multiple of 128 rows; a window takes the next expert while its
+ * padded rows still fit the ring, else the next window starts there.
+ * first_expert (HOST, E + 1 entries) receives each window's first expert and
+ * then E; *num_windows their number (>= 1).  macrobatch_size 0 gives one
+ * window.  An expert whose padded rows exceed the ring: MOK_ERR_CAPACITY.
+ * Host only: needs no GPU. */
+mok_status_t mok_macrobatch_plan(const int32_t* cnt, int E, int64_t macrobatch_size, int32_t* first_expert,
+                                 int* num_windows);
 mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy,
                           const uint16_t* x, const float* router_w,
                           const mok_schedule_t* sched, const mok_ctx_t* ctx,

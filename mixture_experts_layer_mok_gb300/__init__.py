@@ -17,8 +17,8 @@ import torch
 from . import _lib
 from ._lib import MokError  # noqa: F401
 
-__all__ = ["schedule", "schedule_noalloc", "mxfp8_quantize", "mxfp8_quantize_t", "mxfp8_quantize_dual", "forward", "backward", "Schedule",
-           "Weights", "Context", "MokError", "quantize_weights", "MODES"]
+__all__ = ["schedule", "schedule_noalloc", "mxfp8_quantize", "mxfp8_quantize_t", "mxfp8_quantize_dual", "forward",
+           "backward", "Schedule", "Weights", "Context", "MokError", "quantize_weights", "macrobatch_plan", "MODES"]
 
 # forward/backward precision: "bf16"; "mxfp8" (MXFP8 forward GEMMs, bf16
 # backward); "mxfp8_full" (MXFP8 forward and backward GEMMs)
@@ -276,9 +276,24 @@ def quantize_weights(w: Weights, stream=None, backward: bool = False) -> Weights
     return Weights(w.w_gate, w.w_up, w.w_down, w.ws_gate, w.ws_up, w.ws_down, mx)
 
 
-def _config(mode, minibatch, debug, events=None, dispatch="auto", swiglu_limit=0.0):
+def macrobatch_plan(cnt, macrobatch: int):
+    """The windows a macrobatch ring of ``macrobatch`` rows runs the routed
+    experts in, for per-expert row counts ``cnt`` (a sequence of ints, e.g. the
+    schedule's ``cnt`` read back): a list of (first expert, end expert).  Host
+    only; raises MokError(MOK_ERR_CAPACITY) when one expert does not fit."""
+    lib = _lib.load()
+    E = len(cnt)
+    arr = (C.c_int32 * E)(*[int(c) for c in cnt])
+    first = (C.c_int32 * (E + 1))()
+    nw = C.c_int()
+    _lib.check(lib.mok_macrobatch_plan(arr, E, int(macrobatch), first, C.byref(nw)), "mok_macrobatch_plan")
+    return [(first[i], first[i + 1]) for i in range(nw.value)]
+
+
+def _config(mode, minibatch, debug, events=None, dispatch="auto", swiglu_limit=0.0, macrobatch=0):
     cfg = _lib.MokConfig(mode=mode, minibatch_size=minibatch, debug_flags=debug, dispatch=_lib.DISPATCH[dispatch],
-                         num_events=0, events=None, swiglu_limit=float(swiglu_limit))
+                         num_events=0, events=None, swiglu_limit=float(swiglu_limit),
+                         macrobatch_size=int(macrobatch))
     if events is not None:
         if len(events) != 2 * _lib.MOK_NUM_STAGES:
             raise ValueError("events must hold 2 * MOK_NUM_STAGES torch.cuda.Event objects (or None)")
@@ -294,12 +309,15 @@ def _config(mode, minibatch, debug, events=None, dispatch="auto", swiglu_limit=0
 
 def forward(x, router_w, sched: Schedule, weights: Weights, mode: str = "bf16", minibatch: int = 0,
             debug: int = 0, out=None, ctx_buf=None, stream=None, events=None, dispatch="auto",
-            swiglu_limit: float = 0.0):
+            swiglu_limit: float = 0.0, macrobatch: int = 0):
     """y = layer(x); returns (y, Context).  ``mode`` is "bf16", "mxfp8" or
     "mxfp8_full" (see ``MODES``; the backward follows the forward's mode);
     ``dispatch`` is "auto", "permute" or "fused" (same results, different kernels).
     ``swiglu_limit`` > 0 clamps the SwiGLU pre-activations (gate to <= L, up
     to [-L, L]); the backward follows the forward's value.
+    ``macrobatch`` > 0: rows of the token ring (mok_config_t.macrobatch_size):
+    the routed experts run in windows of whole experts over scratch of that
+    many rows, with the same result bits (reads the expert counts back once).
     ``events``: optional list of 2 * MOK_NUM_STAGES torch.cuda.Event (timing); a
     None entry records nothing (each record costs a few microseconds on the
     device, so a timing run can watch one stage alone)."""
@@ -312,22 +330,24 @@ def forward(x, router_w, sched: Schedule, weights: Weights, mode: str = "bf16", 
     _need(x, torch.bfloat16, (T, H), "x")
     _need(router_w, torch.float32, (T, k), "router_w")
     ws = weights.struct()
-    nbytes = lib.mok_ctx_bytes(T, k, E, H, I, I_s, m)
+    nbytes = lib.mok_ctx_bytes_ring(T, k, E, H, I, I_s, m, int(macrobatch))
     if nbytes == 0:
         raise ValueError("shape outside the kernels' contract")
     if ctx_buf is None or ctx_buf.numel() < nbytes:
         ctx_buf = torch.empty(nbytes, dtype=torch.uint8, device=x.device)
     y = out if out is not None else torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
     c = _lib.MokCtx()
-    cfg = _config(m, minibatch, debug, events, dispatch, swiglu_limit)
+    cfg = _config(m, minibatch, debug, events, dispatch, swiglu_limit, macrobatch)
     _lib.check(lib.mok_forward(C.byref(cfg), _ptr(x), _ptr(router_w), C.byref(sched.c), C.byref(ws), _ptr(y),
                                _ptr(ctx_buf), ctx_buf.numel(), C.byref(c), _stream(stream)), "mok_forward")
     return y, Context(ctx_buf, c, m)
 
 
 def backward(dy, x, router_w, sched: Schedule, ctx: Context, weights: Weights, minibatch: int = 0,
-             grads: dict | None = None, ws_buf=None, stream=None, events=None, dispatch="auto", debug: int = 0):
-    """Returns dict dx, d_router_w, d_w_gate, d_w_up, d_w_down (+ d_ws_* with a shared expert)."""
+             grads: dict | None = None, ws_buf=None, stream=None, events=None, dispatch="auto", debug: int = 0,
+             macrobatch: int = 0):
+    """Returns dict dx, d_router_w, d_w_gate, d_w_up, d_w_down (+ d_ws_* with a shared expert).
+    ``macrobatch``: the backward's own token ring (see ``forward``)."""
     lib = _lib.load()
     E, H, I, I_s = weights.dims
     T, k = sched.T, sched.k
@@ -347,10 +367,12 @@ def backward(dy, x, router_w, sched: Schedule, ctx: Context, weights: Weights, m
     for name in ("d_w_gate", "d_w_up", "d_w_down", "d_ws_gate", "d_ws_up", "d_ws_down"):
         if name in grads:
             setattr(g, name, grads[name].data_ptr())
-    nbytes = lib.mok_bwd_workspace_bytes(T, k, E, H, I, I_s, ctx.mode)
+    nbytes = lib.mok_bwd_workspace_bytes_ring(T, k, E, H, I, I_s, ctx.mode, int(macrobatch))
+    if nbytes == 0:
+        raise ValueError("shape outside the kernels' contract")
     if ws_buf is None or ws_buf.numel() < nbytes:
         ws_buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-    cfg = _config(ctx.mode, minibatch, debug, events, dispatch)
+    cfg = _config(ctx.mode, minibatch, debug, events, dispatch, macrobatch=macrobatch)
     wsd = weights.struct()
     _lib.check(lib.mok_backward(C.byref(cfg), _ptr(dy), _ptr(x), _ptr(router_w), C.byref(sched.c),
                                 C.byref(ctx.c), C.byref(wsd), _ptr(grads["dx"]), _ptr(grads["d_router_w"]),

@@ -42,7 +42,7 @@ STAGE_NAMES = ["fwd_prep", "fwd_shared_gateup", "fwd_shared_down", "fwd_gateup",
 class MokConfig(C.Structure):
     _fields_ = [("mode", C.c_int), ("minibatch_size", C.c_int), ("debug_flags", C.c_int),
                 ("dispatch", C.c_int), ("num_events", C.c_int), ("events", C.POINTER(C.c_void_p)),
-                ("swiglu_limit", C.c_float)]
+                ("swiglu_limit", C.c_float), ("macrobatch_size", C.c_int64)]
 
 
 class MokSchedule(C.Structure):
@@ -68,7 +68,7 @@ class MokCtx(C.Structure):
                 ("gu", P), ("h", P), ("hq", P), ("hq_sc", P), ("slots", P), ("gu_s", P), ("h_s", P),
                 ("hq_s", P), ("hq_s_sc", P), ("shared_out", P), ("xq", P), ("xq_sc", P), ("status", P),
                 ("x_perm", P), ("dispatch", C.c_int), ("xq_perm", P), ("xq_perm_sc", P),
-                ("swiglu_limit", C.c_float)]
+                ("swiglu_limit", C.c_float), ("ring_rows", C.c_int64)]
 
 
 class MokWeightGrads(C.Structure):
@@ -90,10 +90,13 @@ SIGNATURES = {
     "mok_mxfp8_quantize_t": (C.c_int, [P, C.c_int64, C.c_int, C.c_int, P, P, P]),
     "mok_mxfp8_quantize_dual": (C.c_int, [P, C.c_int64, C.c_int, C.c_int, P, P, P, P, P]),
     "mok_ctx_bytes": (C.c_size_t, [C.c_int] * 7),
+    "mok_ctx_bytes_ring": (C.c_size_t, [C.c_int] * 7 + [C.c_int64]),
     "mok_forward": (C.c_int, [C.POINTER(MokConfig), P, P, C.POINTER(MokSchedule),
                               C.POINTER(MokWeights), P, P, C.c_size_t, C.POINTER(MokCtx), P]),
     "mok_ctx_status": (C.c_int, [C.POINTER(MokCtx), I32P]),
     "mok_bwd_workspace_bytes": (C.c_size_t, [C.c_int] * 7),
+    "mok_bwd_workspace_bytes_ring": (C.c_size_t, [C.c_int] * 7 + [C.c_int64]),
+    "mok_macrobatch_plan": (C.c_int, [I32P, C.c_int, C.c_int64, I32P, C.POINTER(C.c_int)]),
     "mok_backward": (C.c_int, [C.POINTER(MokConfig), P, P, P, C.POINTER(MokSchedule), C.POINTER(MokCtx),
                                C.POINTER(MokWeights), P, P, C.POINTER(MokWeightGrads), P, C.c_size_t, P]),
 }

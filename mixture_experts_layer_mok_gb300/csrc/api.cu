@@ -11,6 +11,7 @@
 
 #include <cmath>
 #include <mutex>
+#include <vector>
 
 #include "../../include/mok.h"
 #include "gemm.cuh"
@@ -251,38 +252,59 @@ size_t carve_schedule(void* buf, int T, int k, int E, SchedLayout* L) {
 struct CtxExtra {  // forward scratch beyond the public context fields
   // MXFP8 mode: weight scales in the tensor-core scale layout
   uint8_t *wg_sc, *wu_sc, *wd_sc, *wsg_sc, *wsu_sc, *wsd_sc;
+  int32_t* view;   // macrobatch ring: the windows' schedule views
 };
+
+// ---------------------------------------------------------------- macrobatch ring
+// Rows of the ring for a macrobatch size: 0 (no ring: every schedule-order
+// buffer spans all max_rows rows) for 0 or a size that holds every row, else
+// the size rounded up to whole 128-row tiles.
+long long ring_rows_of(long long macrobatch, long long max_rows) {
+  if (macrobatch <= 0) return 0;
+  const long long r = (macrobatch + kTileRows - 1) / kTileRows * kTileRows;
+  return r >= max_rows ? 0 : r;
+}
+
+// Ints of the windows' schedule views: the tiles and the pairs of all windows
+// (max_tiles at most), ne + 1 row offsets and an 8-int header per window (at
+// most E windows).
+long long view_ints(long long max_tiles, int E) { return 5 * max_tiles + 10ll * E; }
 
 // Bytes of E8M0 scales of a [rows][K] tensor in the tensor-core scale layout
 // (rows padded to whole 128-row blocks).
 long long tiled_scale_bytes(long long rows, long long K) { return (rows + 127) / 128 * 128 * (K / 32); }
 
-size_t carve_ctx(void* buf, int T, int k, int E, int H, int I, int Is, int mode, mok_ctx_t* ctx,
+// The context: gu (saved) and slots (read by the combine) span every schedule
+// row; the rest of the schedule-order scratch spans `ring` rows (0: every row).
+size_t carve_ctx(void* buf, int T, int k, int E, int H, int I, int Is, int mode, long long ring, mok_ctx_t* ctx,
                  CtxExtra* X) {
-  const long long mr = max_tiles_of(T, k, E) * kTileRows;
-  const long long n = static_cast<long long>(T) * k;
+  const long long mt = max_tiles_of(T, k, E);
+  const long long mr = mt * kTileRows;
+  const long long rr = ring ? ring : mr;
   const bool mx = (mode == MOK_MODE_MXFP8_FWD || mode == MOK_MODE_MXFP8);
   Carver c(buf);
   memset(ctx, 0, sizeof(*ctx));
   memset(X, 0, sizeof(*X));
   ctx->T = T; ctx->k = k; ctx->E = E; ctx->H = H; ctx->I = I; ctx->I_s = Is; ctx->mode = mode;
-  ctx->max_tiles = static_cast<int>(max_tiles_of(T, k, E));
+  ctx->max_tiles = static_cast<int>(mt);
+  ctx->ring_rows = ring;
   ctx->status = c.take<int32_t>(8);
   ctx->gu = c.take<uint16_t>(mr * 2 * I);
   ctx->slots = c.take<uint16_t>(mr * H);
   if (!mx) {
-    ctx->x_perm = c.take<uint16_t>(mr * H);
-    ctx->h = c.take<uint16_t>(mr * I);
+    ctx->x_perm = c.take<uint16_t>(rr * H);
+    ctx->h = c.take<uint16_t>(rr * I);
   } else {
     // the bf16 token rows in schedule order for the bf16 backward's gate/up
-    // weight gradient, written during the forward (MXFP8 forward mode only)
-    if (mode == MOK_MODE_MXFP8_FWD) ctx->x_perm = c.take<uint16_t>(mr * H);
+    // weight gradient, written during a one-pass forward (MXFP8 forward mode
+    // only; a backward after a ring forward makes its own)
+    if (mode == MOK_MODE_MXFP8_FWD && !ring) ctx->x_perm = c.take<uint16_t>(mr * H);
     ctx->xq = c.take<uint8_t>(static_cast<long long>(T) * H);
     ctx->xq_sc = c.take<uint8_t>(tiled_scale_bytes(T, H));
-    ctx->xq_perm = c.take<uint8_t>(mr * H);
-    ctx->xq_perm_sc = c.take<uint8_t>(tiled_scale_bytes(mr, H));
-    ctx->hq = c.take<uint8_t>(mr * I);
-    ctx->hq_sc = c.take<uint8_t>(tiled_scale_bytes(mr, I));
+    ctx->xq_perm = c.take<uint8_t>(rr * H);
+    ctx->xq_perm_sc = c.take<uint8_t>(tiled_scale_bytes(rr, H));
+    ctx->hq = c.take<uint8_t>(rr * I);
+    ctx->hq_sc = c.take<uint8_t>(tiled_scale_bytes(rr, I));
     // gate and up scales back to back: the CTA-pair 128-wide SwiGLU GEMM reads
     // the same bytes as one interleaved gate|up tensor of 2 E I rows
     X->wg_sc = c.take<uint8_t>(2 * tiled_scale_bytes(static_cast<long long>(E) * I, H));
@@ -302,11 +324,12 @@ size_t carve_ctx(void* buf, int T, int k, int E, int H, int I, int Is, int mode,
       X->wsd_sc = c.take<uint8_t>(tiled_scale_bytes(H, Is));
     }
   }
+  if (ring) X->view = c.take<int32_t>(view_ints(mt, E));
   return c.off + 256;
 }
 
 struct BwdLayout {
-  uint16_t *dgu, *hw, *dx_slots, *dgu_s, *hs, *dx_s, *dy_perm, *xb_perm;
+  uint16_t *dgu, *hw, *dgu_s, *hs, *dx_s, *dy_perm, *xb_perm;
   float* dw_part;
   // MOK_MODE_MXFP8: E4M3 operands of the backward GEMMs and their E8M0 scales
   // (tensor-core scale layout).  Row-quantised: dy (schedule and token order),
@@ -316,6 +339,7 @@ struct BwdLayout {
   uint8_t *xT, *xT_sc, *xT_tok, *xT_tok_sc, *dguq, *dguq_sc, *dguT, *dguT_sc, *hwT, *hwT_sc;
   uint8_t *dgusq, *dgusq_sc, *dgusT, *dgusT_sc, *hsT, *hsT_sc;
   uint8_t *wtg_sc, *wtu_sc, *wtd_sc, *wtsg_sc, *wtsu_sc, *wtsd_sc;
+  int32_t* view;   // macrobatch ring: the windows' schedule views
 };
 
 int tile_n(int N) { return (N % 256 == 0) ? 256 : 128; }
@@ -338,24 +362,30 @@ cudaError_t launch_tiles(const GemmMaps& m, const GemmParams& p, long long items
 // Pair work items: row tiles taken two at a time.
 long long row_pairs(long long rows) { return ((rows + 127) / 128 + 1) / 2; }
 
-size_t carve_bwd(void* buf, int T, int k, int E, int H, int I, int Is, int mode, BwdLayout* L) {
-  const long long mr = max_tiles_of(T, k, E) * kTileRows;
+// The backward workspace: dw_part (read by the fixed-order reduction) spans
+// every routed row; the schedule-order scratch spans `ring` rows (0: every
+// row).  The dx rows in schedule order go to the context's slots, the
+// forward's scratch, which its combine has consumed.
+size_t carve_bwd(void* buf, int T, int k, int E, int H, int I, int Is, int mode, long long ring, BwdLayout* L) {
+  const long long mt = max_tiles_of(T, k, E);
+  const long long mr = mt * kTileRows;
+  const long long rr = ring ? ring : mr;
   const long long n = static_cast<long long>(T) * k;
   const long long Tl = T, Tp = (Tl + 127) / 128 * 128;
   const bool mx = (mode == MOK_MODE_MXFP8);
   Carver c(buf);
   memset(L, 0, sizeof(*L));
   if (!mx) {   // the MXFP8 backward keeps these only as E4M3 codes
-    L->dgu = c.take<uint16_t>(mr * 2 * I);
-    L->hw = c.take<uint16_t>(mr * I);
+    L->dgu = c.take<uint16_t>(rr * 2 * I);
+    L->hw = c.take<uint16_t>(rr * I);
   }
   // two column halves per N tile (128-wide tiles in the MXFP8 backward)
   L->dw_part = c.take<float>(n * 2 * (I / (mx ? 128 : tile_n(I))));
-  L->dx_slots = c.take<uint16_t>(mr * H);
   if (!mx) {
-    L->dy_perm = c.take<uint16_t>(mr * H);
-    // x's rows in schedule order: after an MXFP8 forward the context holds them
-    if (mode == MOK_MODE_BF16) L->xb_perm = c.take<uint16_t>(mr * H);
+    L->dy_perm = c.take<uint16_t>(rr * H);
+    // x's rows in schedule order: a one-pass MXFP8 forward leaves them in the
+    // context; with a ring they are made window by window
+    if (mode == MOK_MODE_BF16 || ring) L->xb_perm = c.take<uint16_t>(rr * H);
   }
   if (Is > 0) {
     if (!mx) {
@@ -365,20 +395,20 @@ size_t carve_bwd(void* buf, int T, int k, int E, int H, int I, int Is, int mode,
     L->dx_s = c.take<uint16_t>(Tl * H);
   }
   if (mx) {
-    L->dyq = c.take<uint8_t>(mr * H);
-    L->dyq_sc = c.take<uint8_t>(tiled_scale_bytes(mr, H));
+    L->dyq = c.take<uint8_t>(rr * H);
+    L->dyq_sc = c.take<uint8_t>(tiled_scale_bytes(rr, H));
     L->dyq_tok = c.take<uint8_t>(Tp * H);   // rows up to the 128-row boundary (zeros past T)
     L->dyq_tok_sc = c.take<uint8_t>(tiled_scale_bytes(Tl, H));
-    L->dyT = c.take<uint8_t>(mr * H);
-    L->dyT_sc = c.take<uint8_t>(tiled_scale_bytes(H, mr));
-    L->xT = c.take<uint8_t>(mr * H);
-    L->xT_sc = c.take<uint8_t>(tiled_scale_bytes(H, mr));
-    L->dguq = c.take<uint8_t>(mr * 2 * I);
-    L->dguq_sc = c.take<uint8_t>(tiled_scale_bytes(mr, 2 * I));
-    L->dguT = c.take<uint8_t>(mr * 2 * I);
-    L->dguT_sc = c.take<uint8_t>(tiled_scale_bytes(2 * I, mr));
-    L->hwT = c.take<uint8_t>(mr * I);
-    L->hwT_sc = c.take<uint8_t>(tiled_scale_bytes(I, mr));
+    L->dyT = c.take<uint8_t>(rr * H);
+    L->dyT_sc = c.take<uint8_t>(tiled_scale_bytes(H, rr));
+    L->xT = c.take<uint8_t>(rr * H);
+    L->xT_sc = c.take<uint8_t>(tiled_scale_bytes(H, rr));
+    L->dguq = c.take<uint8_t>(rr * 2 * I);
+    L->dguq_sc = c.take<uint8_t>(tiled_scale_bytes(rr, 2 * I));
+    L->dguT = c.take<uint8_t>(rr * 2 * I);
+    L->dguT_sc = c.take<uint8_t>(tiled_scale_bytes(2 * I, rr));
+    L->hwT = c.take<uint8_t>(rr * I);
+    L->hwT_sc = c.take<uint8_t>(tiled_scale_bytes(I, rr));
     L->wtg_sc = c.take<uint8_t>(tiled_scale_bytes(static_cast<long long>(E) * H, I));
     L->wtu_sc = c.take<uint8_t>(tiled_scale_bytes(static_cast<long long>(E) * H, I));
     L->wtd_sc = c.take<uint8_t>(tiled_scale_bytes(static_cast<long long>(E) * I, H));
@@ -398,6 +428,7 @@ size_t carve_bwd(void* buf, int T, int k, int E, int H, int I, int Is, int mode,
       L->wtsd_sc = c.take<uint8_t>(tiled_scale_bytes(Is, H));
     }
   }
+  if (ring) L->view = c.take<int32_t>(view_ints(mt, E));
   return c.off + 256;
 }
 
@@ -436,6 +467,104 @@ GemmParams base_params(const mok_config_t* cfg, const mok_schedule_t* s, int* st
   return p;
 }
 
+// Windows of whole experts for a ring of `ring` rows ("Mixture-of-Kittens: a
+// deterministic MoE megakernel for NVL72 racks", "Tuning the five
+// hyperparameters before production": macrobatch_size): in expert order, each
+// expert padded to whole 128-row tiles, a window takes the next expert while
+// its rows fit the ring.  first[w] = window w's first expert, first.back() =
+// E; ring 0: one window.  An expert larger than the ring: MOK_ERR_CAPACITY.
+mok_status_t plan_windows(const int32_t* cnt, int E, long long ring, std::vector<int>* first) {
+  first->assign(1, 0);
+  long long used = 0;
+  for (int e = 0; e < E; ++e) {
+    if (cnt[e] < 0) return fail(MOK_ERR_INVALID_ARG, "expert %d has a negative row count", e);
+    const long long padded = (static_cast<long long>(cnt[e]) + kTileRows - 1) / kTileRows * kTileRows;
+    if (ring > 0 && padded > ring)
+      return fail(MOK_ERR_CAPACITY, "expert %d has %lld padded rows; the macrobatch ring holds %lld", e, padded,
+                  ring);
+    if (ring > 0 && used + padded > ring) {
+      first->push_back(e);
+      used = 0;
+    }
+    used += padded;
+  }
+  first->push_back(E);
+  return MOK_OK;
+}
+
+// One window of the routed experts: experts [e0, e0 + ne) and their schedule
+// rows [r0, r0 + rows).  `s` is the schedule itself when one window covers it,
+// else the window's view (launch_window_view): its own tile list, pairs and
+// header, tile rows and row0 counted from r0, cnt and row_src offset to the
+// window; s.max_tiles is the window's tile count.  Tile experts stay absolute.
+struct Win {
+  mok_schedule_t s;
+  int e0, ne;
+  long long r0, rows;
+};
+
+// The windows of a call.  Without a ring: one window over the whole schedule
+// (nothing is read back).  With one: the expert counts and the header are
+// read back (synchronising cs), the windows planned, and each window's view
+// built on cs into `view`.  A failed schedule gives no window: the routed
+// kernels would do nothing, and the status travels on in the header.
+mok_status_t make_windows(const mok_schedule_t* s, long long ring, int32_t* view, cudaStream_t cs,
+                          std::vector<Win>* out) {
+  out->clear();
+  const long long mt = s->max_tiles;
+  if (ring == 0) {
+    out->push_back(Win{*s, 0, s->E, 0, mt * kTileRows});
+    return MOK_OK;
+  }
+  const int E = s->E;
+  std::vector<int32_t> cnt(E), hdr(8);
+  MOK_CUDA(cudaMemcpyAsync(hdr.data(), s->header, 8 * sizeof(int32_t), cudaMemcpyDeviceToHost, cs));
+  MOK_CUDA(cudaMemcpyAsync(cnt.data(), s->cnt, E * sizeof(int32_t), cudaMemcpyDeviceToHost, cs));
+  MOK_CUDA(cudaStreamSynchronize(cs));
+  if (hdr[2] != 0) return MOK_OK;
+  std::vector<int> first;
+  mok_status_t st = plan_windows(cnt.data(), E, ring, &first);
+  if (st) return st;
+  const int nw = static_cast<int>(first.size()) - 1;
+  const int cap = hdr[5];
+  long long r0 = 0, tile_off = 0, pair_off = 0;
+  for (int w = 0; w < nw; ++w) {
+    Win v;
+    v.s = *s;
+    v.e0 = first[w];
+    v.ne = first[w + 1] - first[w];
+    v.r0 = r0;
+    long long tiles = 0, pairs = 0;
+    for (int e = v.e0; e < v.e0 + v.ne; ++e) {
+      const long long nt = (cnt[e] + kTileRows - 1) / kTileRows, prim = nt < cap ? nt : cap;
+      tiles += nt;
+      pairs += (prim + 1) / 2 + (nt - prim + 1) / 2;
+    }
+    v.rows = tiles * kTileRows;
+    v.s.max_tiles = static_cast<int>(tiles);
+    if (nw > 1) {
+      int32_t* rows0 = view + 5 * mt + v.e0 + w;
+      int32_t* header = view + 5 * mt + 2ll * E + 8ll * w;
+      v.s.tile_expert = view + tile_off;
+      v.s.tile_row0 = view + mt + tile_off;
+      v.s.tile_rows = view + 2 * mt + tile_off;
+      v.s.pair_tile = view + 3 * mt + 2 * pair_off;
+      v.s.row0 = rows0;
+      v.s.header = header;
+      v.s.cnt = s->cnt + v.e0;
+      v.s.row_src = s->row_src + r0;
+      v.s.scratch = nullptr;
+      MOK_CUDA(launch_window_view(s->cnt, s->row0, s->header, v.e0, v.ne, v.s.tile_expert, v.s.tile_row0,
+                                  v.s.tile_rows, v.s.pair_tile, rows0, header, cs));
+    }
+    out->push_back(v);
+    r0 += v.rows;
+    tile_off += tiles;
+    pair_off += pairs;
+  }
+  return MOK_OK;
+}
+
 // NVTX ranges (host timeline; they cost nothing unless a tool is attached):
 // one per C-ABI call and one per stage inside it, so that a profiler can pick
 // a call's or a stage's kernels (e.g. ncu --nvtx --nvtx-include "mok_backward/").
@@ -463,8 +592,11 @@ struct NvtxCall {
 };
 
 // Records the caller's timing event for the start (end = 0) or end of a stage
-// (a NULL entry: nothing), and opens or closes the stage's NVTX range.
-cudaError_t mark(const mok_config_t* cfg, int stage, int end, cudaStream_t st) {
+// (a NULL entry, or event = false: nothing), and opens or closes the stage's
+// NVTX range.  With a macrobatch ring a routed stage runs once per window: its
+// NVTX range opens and closes each time, its events are recorded at the start
+// in the first window and the end in the last.
+cudaError_t mark(const mok_config_t* cfg, int stage, int end, cudaStream_t st, bool event = true) {
   if (!end) {
     nvtxRangePushA(kStageNames[stage]);
     ++g_nvtx_depth;
@@ -472,7 +604,7 @@ cudaError_t mark(const mok_config_t* cfg, int stage, int end, cudaStream_t st) {
     nvtxRangePop();
     --g_nvtx_depth;
   }
-  if (cfg->events && cfg->num_events >= 2 * MOK_NUM_STAGES && cfg->events[2 * stage + end])
+  if (event && cfg->events && cfg->num_events >= 2 * MOK_NUM_STAGES && cfg->events[2 * stage + end])
     return cudaEventRecord(static_cast<cudaEvent_t>(cfg->events[2 * stage + end]), st);
   return cudaSuccess;
 }
@@ -483,6 +615,7 @@ mok_status_t check_config(const mok_config_t* cfg) {
   if (cfg->events && cfg->num_events != 2 * MOK_NUM_STAGES)
     return fail(MOK_ERR_INVALID_ARG, "events needs 2 * MOK_NUM_STAGES entries");
   if (cfg->minibatch_size < 0) return fail(MOK_ERR_INVALID_ARG, "minibatch_size < 0");
+  if (cfg->macrobatch_size < 0) return fail(MOK_ERR_INVALID_ARG, "macrobatch_size < 0");
   if (cfg->dispatch < MOK_DISPATCH_AUTO || cfg->dispatch > MOK_DISPATCH_FUSED)
     return fail(MOK_ERR_INVALID_ARG, "unknown dispatch %d", cfg->dispatch);
   if (!std::isfinite(cfg->swiglu_limit) || cfg->swiglu_limit < 0.f)
@@ -515,7 +648,6 @@ struct SideStream {
   cudaEvent_t fork = nullptr;
   cudaEvent_t join = nullptr;
   cudaEvent_t join2 = nullptr;   // a second hand-back point within one call
-  cudaEvent_t mid = nullptr;     // a later start point on the caller's stream
 };
 thread_local SideStream g_side[64];
 
@@ -529,7 +661,6 @@ mok_status_t side_stream(SideStream** out) {
     MOK_CUDA(cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming));
     MOK_CUDA(cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming));
     MOK_CUDA(cudaEventCreateWithFlags(&sd.join2, cudaEventDisableTiming));
-    MOK_CUDA(cudaEventCreateWithFlags(&sd.mid, cudaEventDisableTiming));
   }
   *out = &sd;
   return MOK_OK;
@@ -569,30 +700,46 @@ mok_status_t static_sched_scratch(int32_t** out) {
 
 namespace {
 
-// BF16 forward: shared expert, then the routed experts (token rows of x
-// permuted into schedule order, or gathered inside the GEMM).
+// Events for the routed stages of a forward or backward that found no window
+// (a failed schedule under a ring): each recorded back to back.
+cudaError_t mark_skipped(const mok_config_t* cfg, std::initializer_list<int> stages, cudaStream_t cs) {
+  for (int sg : stages) {
+    cudaError_t e = mark(cfg, sg, 0, cs);
+    if (e == cudaSuccess) e = mark(cfg, sg, 1, cs);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+// BF16 forward: shared expert, then the routed experts window by window (token
+// rows of x permuted into schedule order, or gathered inside the GEMM).
 mok_status_t forward_bf16(const mok_config_t* cfg, const uint16_t* x, const float* router_w, const mok_schedule_t* s,
-                          const mok_weights_t* w, mok_ctx_t* ctx, long long mr, int sms, bool g4, cudaStream_t cs) {
+                          const std::vector<Win>& wins, const mok_weights_t* w, mok_ctx_t* ctx, int sms, bool g4,
+                          cudaStream_t cs) {
   const int T = s->T, k = s->k, E = s->E, H = w->H, I = w->I, Is = w->I_s;
+  const size_t nw = wins.size();
   mok_status_t st;
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_PREP, 1, cs));
   const int disp = resolve_dispatch(cfg);
   ctx->dispatch = disp;
   const bool perm = disp == MOK_DISPATCH_PERMUTE;
+  auto permute = [&](const Win& v, cudaStream_t st2) {
+    return launch_permute_rows(x, T, H, k, s->slot_row, s->row_src, s->header, v.r0, v.rows, ctx->x_perm, sms, st2);
+  };
   // token rows of x in schedule order (read by the routed gate/up GEMM as
-  // dense tiles), written on a side stream while the shared expert runs
+  // dense tiles); the first window's are written on a side stream while the
+  // shared expert runs
   SideStream* side = nullptr;
-  if (perm) {
+  if (perm && nw > 0) {
     if ((st = side_stream(&side))) return st;
     MOK_CUDA(cudaEventRecord(side->fork, cs));
     MOK_CUDA(cudaStreamWaitEvent(side->s, side->fork, 0));
     MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 0, side->s));
-    MOK_CUDA(launch_permute_rows(x, T, H, k, s->slot_row, s->row_src, s->header, mr, ctx->x_perm, sms, side->s));
-    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 1, side->s));
+    MOK_CUDA(permute(wins[0], side->s));
+    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 1, side->s, nw == 1));
     MOK_CUDA(cudaEventRecord(side->join, side->s));
   } else {
-    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 0, cs));
-    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 1, cs));
+    MOK_CUDA(mark_skipped(cfg, {MOK_STAGE_FWD_DISPATCH}, cs));
   }
 
   // ---- shared expert: gate/up + SwiGLU over all T tokens, then down
@@ -634,59 +781,73 @@ mok_status_t forward_bf16(const mok_config_t* cfg, const uint16_t* x, const floa
   }
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_DOWN, 1, cs));
 
-  // ---- routed experts: gate/up + SwiGLU, then down + scale + scatter
+  // ---- routed experts, window by window: gate/up + SwiGLU, then down +
+  // scale + scatter (h and the token rows span the window; gu and the slots
+  // every row)
   if (side) MOK_CUDA(cudaStreamWaitEvent(cs, side->join, 0));
-  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_GATEUP, 0, cs));
-  GemmMaps m;
-  const int bk = perm ? kTileBK : kGatherBK;
-  if ((st = perm ? make_map(&m.a, ctx->x_perm, H, mr, 128, bk) : make_map(&m.a, x, H, T, 1, bk)) ||
-      (st = make_map(&m.b0, w->w_gate, H, static_cast<uint64_t>(E) * I, 128, bk)) ||
-      (st = make_map(&m.b1, w->w_up, H, static_cast<uint64_t>(E) * I, 128, bk)) ||
-      (st = make_map_out(&m.o0, ctx->gu, 2ull * I, mr)) || (st = make_map_out(&m.o1, ctx->h, I, mr)))
-    return st;
-  GemmParams p = base_params(cfg, s, ctx->status, cfg->debug_flags);
-  p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / 128; p.b_rows_per_expert = I;
-  p.out0 = ctx->gu; p.out1 = ctx->h; p.ga = x; p.ga_ld = H;
-  p.swiglu_limit = cfg->swiglu_limit;
-  const long long items = static_cast<long long>(s->max_tiles) * p.n_tiles;
-  const int grid = items < sms ? static_cast<int>(items) : sms;
-  if (perm)
-    MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_K_TILE, 256, EPI_SWIGLU>(m, p, items, items, pair_on(cfg, 256), sms, cs)));
-  else if (g4)
-    MOK_CUDA((launch_gemm<SRC_K_GATHER, SRC_K_TILE, 256, EPI_SWIGLU>(m, p, grid, cs)));
-  else
-    MOK_CUDA((launch_gemm<SRC_K_GATHER_LSU, SRC_K_TILE, 256, EPI_SWIGLU>(m, p, grid, cs)));
-  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_GATEUP, 1, cs));
-  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DOWN, 0, cs));
-  GemmMaps m2;
-  const int bn = tile_n(H);
-  const bool pr = pair_on(cfg, bn);
-  if ((st = make_map(&m2.a, ctx->h, I, mr, 128, kTileBK)) ||
-      (st = make_map(&m2.b0, w->w_down, I, static_cast<uint64_t>(E) * H, pr ? bn / 2 : bn, kTileBK)) ||
-      (st = make_map_out(&m2.o0, ctx->slots, H, mr)))
-    return st;
-  m2.b1 = m2.b0;
-  GemmParams q = base_params(cfg, s, ctx->status, 0);
-  q.grouped = 1; q.K = I; q.N = H; q.n_tiles = H / bn; q.b_rows_per_expert = H;
-  q.out0 = ctx->slots; q.ld = H; q.rw = router_w;
-  const long long items2 = static_cast<long long>(s->max_tiles) * q.n_tiles;
-  if (bn == 256)
-    MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_K_TILE, 256, EPI_SCALE_ROWS>(m2, q, items2, items2, pr, sms, cs)));
-  else
-    MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_K_TILE, 128, EPI_SCALE_ROWS>(m2, q, items2, 0, false, sms, cs)));
-  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DOWN, 1, cs));
+  if (nw == 0) MOK_CUDA(mark_skipped(cfg, {MOK_STAGE_FWD_GATEUP, MOK_STAGE_FWD_DOWN}, cs));
+  for (size_t i = 0; i < nw; ++i) {
+    const Win& v = wins[i];
+    const bool first = i == 0, last = i + 1 == nw;
+    if (perm && !first) {
+      MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 0, cs, false));
+      MOK_CUDA(permute(v, cs));
+      MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 1, cs, last));
+    }
+    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_GATEUP, 0, cs, first));
+    uint16_t* gu = ctx->gu + v.r0 * 2 * I;
+    GemmMaps m;
+    const int bk = perm ? kTileBK : kGatherBK;
+    if ((st = perm ? make_map(&m.a, ctx->x_perm, H, v.rows, 128, bk) : make_map(&m.a, x, H, T, 1, bk)) ||
+        (st = make_map(&m.b0, w->w_gate, H, static_cast<uint64_t>(E) * I, 128, bk)) ||
+        (st = make_map(&m.b1, w->w_up, H, static_cast<uint64_t>(E) * I, 128, bk)) ||
+        (st = make_map_out(&m.o0, gu, 2ull * I, v.rows)) || (st = make_map_out(&m.o1, ctx->h, I, v.rows)))
+      return st;
+    GemmParams p = base_params(cfg, &v.s, ctx->status, cfg->debug_flags);
+    p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / 128; p.b_rows_per_expert = I;
+    p.out0 = gu; p.out1 = ctx->h; p.ga = x; p.ga_ld = H;
+    p.swiglu_limit = cfg->swiglu_limit;
+    const long long items = static_cast<long long>(v.s.max_tiles) * p.n_tiles;
+    const int grid = items < sms ? static_cast<int>(items) : sms;
+    if (perm)
+      MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_K_TILE, 256, EPI_SWIGLU>(m, p, items, items, pair_on(cfg, 256), sms, cs)));
+    else if (g4)
+      MOK_CUDA((launch_gemm<SRC_K_GATHER, SRC_K_TILE, 256, EPI_SWIGLU>(m, p, grid, cs)));
+    else
+      MOK_CUDA((launch_gemm<SRC_K_GATHER_LSU, SRC_K_TILE, 256, EPI_SWIGLU>(m, p, grid, cs)));
+    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_GATEUP, 1, cs, last));
+    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DOWN, 0, cs, first));
+    uint16_t* slots = ctx->slots + v.r0 * H;
+    GemmMaps m2;
+    const int bn = tile_n(H);
+    const bool pr = pair_on(cfg, bn);
+    if ((st = make_map(&m2.a, ctx->h, I, v.rows, 128, kTileBK)) ||
+        (st = make_map(&m2.b0, w->w_down, I, static_cast<uint64_t>(E) * H, pr ? bn / 2 : bn, kTileBK)) ||
+        (st = make_map_out(&m2.o0, slots, H, v.rows)))
+      return st;
+    m2.b1 = m2.b0;
+    GemmParams q = base_params(cfg, &v.s, ctx->status, 0);
+    q.grouped = 1; q.K = I; q.N = H; q.n_tiles = H / bn; q.b_rows_per_expert = H;
+    q.out0 = slots; q.ld = H; q.rw = router_w;
+    const long long items2 = static_cast<long long>(v.s.max_tiles) * q.n_tiles;
+    if (bn == 256)
+      MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_K_TILE, 256, EPI_SCALE_ROWS>(m2, q, items2, items2, pr, sms, cs)));
+    else
+      MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_K_TILE, 128, EPI_SCALE_ROWS>(m2, q, items2, 0, false, sms, cs)));
+    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DOWN, 1, cs, last));
+  }
   return MOK_OK;
 }
 
 // MXFP8 forward: x quantised straight into token order (shared expert) and
-// schedule order (routed experts), weight scales rearranged for the tensor
-// core, then the same four GEMMs on the block-scaled MMA; h is requantised in
-// the SwiGLU epilogue.
+// schedule order (routed experts, one window at a time), weight scales
+// rearranged for the tensor core, then the same four GEMMs on the
+// block-scaled MMA; h is requantised in the SwiGLU epilogue.
 mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const float* router_w,
-                           const mok_schedule_t* s, const mok_weights_t* w, mok_ctx_t* ctx, const CtxExtra& X,
-                           int sms, cudaStream_t cs) {
+                           const mok_schedule_t* s, const std::vector<Win>& wins, const mok_weights_t* w,
+                           mok_ctx_t* ctx, const CtxExtra& X, int sms, cudaStream_t cs) {
   const int T = s->T, k = s->k, E = s->E, H = w->H, I = w->I, Is = w->I_s;
-  const long long mr = static_cast<long long>(s->max_tiles) * kTileRows;
+  const size_t nw = wins.size();
   mok_status_t st;
   // Tiling of the block-scaled GEMMs: single CTAs with 256-wide tiles (the
   // accumulator single-buffered beside the scale ring), or CTA pairs (M = 256)
@@ -714,13 +875,18 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_PREP, 1, side->s));
   MOK_CUDA(cudaEventRecord(side->join, side->s));
   ctx->dispatch = MOK_DISPATCH_PERMUTE;
+  // MXFP8 forward / bf16 backward without a ring: the same pass also writes
+  // x's bf16 rows in schedule order, which the backward's gate/up weight
+  // gradient reads (a separate copy would contend for HBM with whichever GEMM
+  // it overlapped).  Later windows skip the token-order copy.
+  auto dispatch = [&](const Win& v, bool tokens) {
+    return launch_mx_dispatch(x, T, H, k, s->slot_row, s->row_src, s->header, v.r0, v.rows,
+                              tokens ? ctx->xq : nullptr, ctx->xq_sc, ctx->xq_perm, ctx->xq_perm_sc, ctx->x_perm, sms,
+                              cs);
+  };
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 0, cs));
-  // MXFP8 forward / bf16 backward: the same pass also writes x's bf16 rows
-  // in schedule order, which the backward's gate/up weight gradient reads (a
-  // separate copy would contend for HBM with whichever GEMM it overlapped)
-  MOK_CUDA(launch_mx_dispatch(x, T, H, k, s->slot_row, s->row_src, s->header, mr, ctx->xq, ctx->xq_sc, ctx->xq_perm,
-                              ctx->xq_perm_sc, cfg->mode == MOK_MODE_MXFP8_FWD ? ctx->x_perm : nullptr, sms, cs));
-  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 1, cs));
+  if (nw > 0) MOK_CUDA(dispatch(wins[0], true));
+  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 1, cs, nw <= 1));
   MOK_CUDA(cudaStreamWaitEvent(cs, side->join, 0));
 
   const int bn = tile_n(H);
@@ -732,7 +898,7 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
   const int dn_bn = tiling == 2 ? 128 : bn;
   const bool dn_pair = tiling == 2 || (tiling == 1 && bn == 256);
   const int dn_box = dn_pair ? dn_bn / 2 : dn_bn;
-  const long long t_atoms = (T + 127) / 128, r_atoms = mr / 128;   // 128-row blocks
+  const long long t_atoms = (T + 127) / 128;   // 128-row blocks
   // gate|up scale maps: two tensors, or one interleaved tensor of 2 * rows
   auto gu_sf_maps = [&](MxMaps& m, const uint8_t* g_sc, const uint8_t* u_sc, long long rows) -> mok_status_t {
     mok_status_t r;
@@ -800,41 +966,55 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
   }
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_SHARED_DOWN, 1, cs));
 
-  // ---- routed experts
-  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_GATEUP, 0, cs));
-  MxMaps m;
-  if ((st = make_map_u8(&m.a, ctx->xq_perm, H, mr, 128)) ||
-      (st = make_map_u8(&m.b0, w->mx_gate, H, static_cast<uint64_t>(E) * I, gu_box)) ||
-      (st = make_map_u8(&m.b1, w->mx_up, H, static_cast<uint64_t>(E) * I, gu_box)) ||
-      (st = make_map_sf(&m.sfa, ctx->xq_perm_sc, r_atoms * (H / 128))) ||
-      (st = gu_sf_maps(m, X.wg_sc, X.wu_sc, static_cast<long long>(E) * I)) ||
-      (st = make_map_out(&m.o0, ctx->gu, 2ull * I, mr)) || (st = make_map_codes_out(&m.o1, ctx->hq, I, mr)))
-    return st;
-  GemmParams p = base_params(cfg, s, ctx->status, cfg->debug_flags);
-  p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / gu_cols; p.b_rows_per_expert = I;
-  p.out0 = ctx->gu; p.out1 = ctx->hq; p.sf_out = ctx->hq_sc;
-  p.swiglu_limit = cfg->swiglu_limit;
-  p.sfa = ctx->xq_perm_sc; p.sfb0 = X.wg_sc; p.sfb1 = X.wu_sc;
-  const long long items = static_cast<long long>(s->max_tiles) * p.n_tiles;
-  MOK_CUDA(launch_gu(m, p, items, items));
-  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_GATEUP, 1, cs));
-  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DOWN, 0, cs));
-  MxMaps m2;
-  if ((st = make_map_u8(&m2.a, ctx->hq, I, mr, 128)) ||
-      (st = make_map_u8(&m2.b0, w->mx_down, I, static_cast<uint64_t>(E) * H, dn_box)) ||
-      (st = make_map_sf(&m2.sfa, ctx->hq_sc, r_atoms * (I / 128))) ||
-      (st = make_map_sf(&m2.sfb0, X.wd_sc, (static_cast<long long>(E) * H / 128) * (I / 128))) ||
-      (st = make_map_out(&m2.o0, ctx->slots, H, mr)))
-    return st;
-  m2.b1 = m2.b0;
-  m2.sfb1 = m2.sfb0;
-  GemmParams q = base_params(cfg, s, ctx->status, 0);
-  q.grouped = 1; q.K = I; q.N = H; q.n_tiles = H / dn_bn; q.b_rows_per_expert = H;
-  q.out0 = ctx->slots; q.ld = H; q.rw = router_w;
-  q.sfa = ctx->hq_sc; q.sfb0 = X.wd_sc;
-  const long long items2 = static_cast<long long>(s->max_tiles) * q.n_tiles;
-  MOK_CUDA(launch_dn(EPI_SCALE_ROWS, m2, q, items2, items2));
-  MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DOWN, 1, cs));
+  // ---- routed experts, window by window (the codes of x and h span the
+  // window; gu and the slots every row)
+  if (nw == 0) MOK_CUDA(mark_skipped(cfg, {MOK_STAGE_FWD_GATEUP, MOK_STAGE_FWD_DOWN}, cs));
+  for (size_t i = 0; i < nw; ++i) {
+    const Win& v = wins[i];
+    const bool first = i == 0, last = i + 1 == nw;
+    const long long r_atoms = v.rows / 128;
+    if (!first) {
+      MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 0, cs, false));
+      MOK_CUDA(dispatch(v, false));
+      MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 1, cs, last));
+    }
+    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_GATEUP, 0, cs, first));
+    uint16_t* gu = ctx->gu + v.r0 * 2 * I;
+    MxMaps m;
+    if ((st = make_map_u8(&m.a, ctx->xq_perm, H, v.rows, 128)) ||
+        (st = make_map_u8(&m.b0, w->mx_gate, H, static_cast<uint64_t>(E) * I, gu_box)) ||
+        (st = make_map_u8(&m.b1, w->mx_up, H, static_cast<uint64_t>(E) * I, gu_box)) ||
+        (st = make_map_sf(&m.sfa, ctx->xq_perm_sc, r_atoms * (H / 128))) ||
+        (st = gu_sf_maps(m, X.wg_sc, X.wu_sc, static_cast<long long>(E) * I)) ||
+        (st = make_map_out(&m.o0, gu, 2ull * I, v.rows)) || (st = make_map_codes_out(&m.o1, ctx->hq, I, v.rows)))
+      return st;
+    GemmParams p = base_params(cfg, &v.s, ctx->status, cfg->debug_flags);
+    p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / gu_cols; p.b_rows_per_expert = I;
+    p.out0 = gu; p.out1 = ctx->hq; p.sf_out = ctx->hq_sc;
+    p.swiglu_limit = cfg->swiglu_limit;
+    p.sfa = ctx->xq_perm_sc; p.sfb0 = X.wg_sc; p.sfb1 = X.wu_sc;
+    const long long items = static_cast<long long>(v.s.max_tiles) * p.n_tiles;
+    MOK_CUDA(launch_gu(m, p, items, items));
+    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_GATEUP, 1, cs, last));
+    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DOWN, 0, cs, first));
+    uint16_t* slots = ctx->slots + v.r0 * H;
+    MxMaps m2;
+    if ((st = make_map_u8(&m2.a, ctx->hq, I, v.rows, 128)) ||
+        (st = make_map_u8(&m2.b0, w->mx_down, I, static_cast<uint64_t>(E) * H, dn_box)) ||
+        (st = make_map_sf(&m2.sfa, ctx->hq_sc, r_atoms * (I / 128))) ||
+        (st = make_map_sf(&m2.sfb0, X.wd_sc, (static_cast<long long>(E) * H / 128) * (I / 128))) ||
+        (st = make_map_out(&m2.o0, slots, H, v.rows)))
+      return st;
+    m2.b1 = m2.b0;
+    m2.sfb1 = m2.sfb0;
+    GemmParams q = base_params(cfg, &v.s, ctx->status, 0);
+    q.grouped = 1; q.K = I; q.N = H; q.n_tiles = H / dn_bn; q.b_rows_per_expert = H;
+    q.out0 = slots; q.ld = H; q.rw = router_w;
+    q.sfa = ctx->hq_sc; q.sfb0 = X.wd_sc;
+    const long long items2 = static_cast<long long>(v.s.max_tiles) * q.n_tiles;
+    MOK_CUDA(launch_dn(EPI_SCALE_ROWS, m2, q, items2, items2));
+    MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DOWN, 1, cs, last));
+  }
   return MOK_OK;
 }
 
@@ -856,14 +1036,25 @@ cudaError_t launch_mx_tiles(const MxMaps& m, const GemmParams& p, int bn, long l
 // the SwiGLU backward's epilogue writes dG|dU (rows and transposed) and w h
 // (transposed) straight as E4M3 codes, quantised from their bf16 values.
 mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const uint16_t* x, const float* router_w,
-                            const mok_schedule_t* s, const mok_ctx_t* ctx, const mok_weights_t* w,
-                            uint16_t* dx, float* d_router_w, const mok_weight_grads_t* g, const BwdLayout& L,
-                            int sms, cudaStream_t cs) {
+                            const mok_schedule_t* s, const std::vector<Win>& wins, const mok_ctx_t* ctx,
+                            const mok_weights_t* w, uint16_t* dx, float* d_router_w, const mok_weight_grads_t* g,
+                            const BwdLayout& L, int sms, cudaStream_t cs) {
   const int T = s->T, k = s->k, E = s->E, H = w->H, I = w->I, Is = w->I_s;
   const long long mr = static_cast<long long>(s->max_tiles) * kTileRows;
   const int Tp = (T + 127) / 128 * 128;
-  const int mri = static_cast<int>(mr);
+  const size_t nw = wins.size();
   mok_status_t st;
+  // a window's x (transposed) and dy (rows and transposed), through the
+  // schedule: its rows from 0 of the workspace's codes
+  auto quant_x = [&](const Win& v, cudaStream_t st2) {
+    const int rows = static_cast<int>(v.rows);
+    return launch_mx_quantize_t(x, H, 1, rows, H, rows, v.s.row_src, k, s->header, L.xT, L.xT_sc, 1, sms, st2);
+  };
+  auto quant_dy = [&](const Win& v) {
+    const int rows = static_cast<int>(v.rows);
+    return launch_mx_quantize_t(dy, H, 1, rows, H, rows, v.s.row_src, k, s->header, L.dyT, L.dyT_sc, 1, sms, cs,
+                                L.dyq, L.dyq_sc, 1);
+  };
   // ---- on the side stream: weight scales into the tensor-core layout (one
   // launch, handed back at `join`), then the transposed x,
   // which only the gate/up weight gradients read (handed back at `join2`)
@@ -885,17 +1076,16 @@ mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const u
   MOK_CUDA(cudaEventRecord(side->join, side->s));
   if (Is > 0)
     MOK_CUDA(launch_mx_quantize_t(x, H, 1, Tp, H, T, nullptr, 1, nullptr, L.xT_tok, L.xT_tok_sc, 1, sms, side->s));
-  MOK_CUDA(launch_mx_quantize_t(x, H, 1, mri, H, mri, s->row_src, k, s->header, L.xT, L.xT_sc, 1, sms, side->s));
+  if (nw > 0) MOK_CUDA(quant_x(wins[0], side->s));
   MOK_CUDA(cudaEventRecord(side->join2, side->s));
-  // ---- dy, rows and transposed from one read: in schedule order (routed) and
-  // in token order (shared expert)
+  // ---- dy, rows and transposed from one read: in schedule order (routed,
+  // the first window) and in token order (shared expert)
   MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 0, cs));
-  MOK_CUDA(launch_mx_quantize_t(dy, H, 1, mri, H, mri, s->row_src, k, s->header, L.dyT, L.dyT_sc, 1, sms, cs, L.dyq,
-                                L.dyq_sc, 1));
+  if (nw > 0) MOK_CUDA(quant_dy(wins[0]));
   if (Is > 0)
     MOK_CUDA(launch_mx_quantize_t(dy, H, 1, Tp, H, T, nullptr, 1, nullptr, L.dyT_tok, L.dyT_tok_sc, 1, sms, cs,
                                   L.dyq_tok, L.dyq_tok_sc, 1));
-  MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 1, cs));
+  MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 1, cs, nw <= 1));
   MOK_CUDA(cudaStreamWaitEvent(cs, side->join, 0));
   const int bnH = tile_n(H);
 
@@ -969,70 +1159,386 @@ mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const u
     MOK_CUDA(cudaStreamWaitEvent(cs, side->join2, 0));   // the transposed x is ready
   }
 
-  // ---- routed: dgrad through down + SwiGLU backward + router-weight partials
-  {
-    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DOWN, 0, cs));
-    MxMaps m;
-    if ((st = make_map_u8(&m.a, L.dyq, H, mr, 128)) ||
-        (st = make_map_u8(&m.b0, w->mxt_down, H, static_cast<uint64_t>(E) * I, 128)) ||
-        (st = make_map_codes_out(&m.o0, L.dguq, 2ull * I, mr)) || (st = make_map_codes_out(&m.o1, L.dguT, mr, 2ull * I)) ||
-        (st = make_map_codes_out(&m.o2, L.hwT, mr, I)))
-      return st;
-    m.b1 = m.b0;
-    GemmParams p = base_params(cfg, s, ctx->status, 0);
-    p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / 128; p.b_rows_per_expert = I;
-    p.aux0 = ctx->gu; p.rw = router_w; p.dw_part = L.dw_part; p.swiglu_limit = ctx->swiglu_limit;
-    p.sf_out = L.dguq_sc; p.out2 = L.dguT_sc; p.sf_out2 = L.hwT_sc; p.ld = mr;   // codes: maps o0..o2
-    p.sfa = L.dyq_sc; p.sfb0 = L.wtd_sc;
-    const long long items = static_cast<long long>(s->max_tiles) * p.n_tiles;
-    MOK_CUDA((launch_gemm_mx<128, EPI_DOWN_BWD_MX>(m, p, items < sms ? static_cast<int>(items) : sms, cs)));
-    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DOWN, 1, cs));
-  }
-  {  // dW_down[e] = sum over e's rows of dy[t(r)]^T (w h)[r]
-    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_DOWN, 0, cs));
-    const int bn = tile_n(I);
-    MxMaps m;
-    if ((st = make_map_u8(&m.a, L.dyT, mr, H, 128)) || (st = make_map_u8(&m.b0, L.hwT, mr, I, bn))) return st;
-    m.b1 = m.b0;
-    GemmParams p = base_params(cfg, s, ctx->status, 0);
-    p.wgrad = 1; p.grouped = 1; p.K = mri; p.E = E; p.m_tiles = H / 128; p.n_tiles = I / bn;
-    p.out0 = g->d_w_down; p.out1 = g->d_w_down; p.ld = I; p.split = H;
-    p.sfa = L.dyT_sc; p.sfb0 = L.hwT_sc;
-    MOK_CUDA(launch_mx_tiles<EPI_WGRAD>(m, p, bn, static_cast<long long>(E) * p.m_tiles * p.n_tiles, sms, cs));
-    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_DOWN, 1, cs));
-  }
-  {  // dW_gate|up[e] = sum over e's rows of (dG|dU)[r]^T x[t(r)]
-    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_GATEUP, 0, cs));
-    MxMaps m;
-    if ((st = make_map_u8(&m.a, L.dguT, mr, 2ull * I, 128)) || (st = make_map_u8(&m.b0, L.xT, mr, H, bnH)))
-      return st;
-    m.b1 = m.b0;
-    GemmParams p = base_params(cfg, s, ctx->status, 0);
-    p.wgrad = 1; p.grouped = 1; p.K = mri; p.E = E; p.m_tiles = 2 * I / 128; p.n_tiles = H / bnH;
-    p.out0 = g->d_w_gate; p.out1 = g->d_w_up; p.ld = H; p.split = I;
-    p.sfa = L.dguT_sc; p.sfb0 = L.xT_sc;
-    MOK_CUDA(launch_mx_tiles<EPI_WGRAD>(m, p, bnH, static_cast<long long>(E) * p.m_tiles * p.n_tiles, sms, cs));
-    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_GATEUP, 1, cs));
-  }
-  {  // dx rows = dG W_gate[e] + dU W_up[e], in schedule order
-    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DGRAD_GATEUP, 0, cs));
-    MxMaps m;
-    if ((st = make_map_u8(&m.a, L.dguq, 2ull * I, mr, 128)) ||
-        (st = make_map_u8(&m.b0, w->mxt_gate, I, static_cast<uint64_t>(E) * H, bnH)) ||
-        (st = make_map_u8(&m.b1, w->mxt_up, I, static_cast<uint64_t>(E) * H, bnH)) ||
-        (st = make_map_out(&m.o0, L.dx_slots, H, mr)))
-      return st;
-    GemmParams p = base_params(cfg, s, ctx->status, 0);
-    p.grouped = 1; p.K = 2 * I; p.N = H; p.n_tiles = H / bnH; p.b_rows_per_expert = H; p.b_split = I;
-    p.out0 = L.dx_slots; p.ld = H;
-    p.sfa = L.dguq_sc; p.sfb0 = L.wtg_sc; p.sfb1 = L.wtu_sc; p.sf_kgb = I / 128;
-    MOK_CUDA(launch_mx_tiles<EPI_STORE_ROWS>(m, p, bnH, static_cast<long long>(s->max_tiles) * p.n_tiles, sms, cs));
-    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DGRAD_GATEUP, 1, cs));
+  // ---- routed, window by window (the codes span the window; the dx rows
+  // and the router-weight partials every row)
+  if (nw == 0)
+    MOK_CUDA(mark_skipped(cfg, {MOK_STAGE_BWD_DOWN, MOK_STAGE_BWD_WGRAD_DOWN, MOK_STAGE_BWD_WGRAD_GATEUP,
+                                MOK_STAGE_BWD_DGRAD_GATEUP}, cs));
+  for (size_t i = 0; i < nw; ++i) {
+    const Win& v = wins[i];
+    const bool first = i == 0, last = i + 1 == nw;
+    const int rows = static_cast<int>(v.rows);
+    if (!first) {
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 0, cs, false));
+      MOK_CUDA(quant_dy(v));
+      MOK_CUDA(quant_x(v, cs));
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 1, cs, last));
+    }
+    {  // dgrad through down + SwiGLU backward + router-weight partials
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DOWN, 0, cs, first));
+      MxMaps m;
+      if ((st = make_map_u8(&m.a, L.dyq, H, v.rows, 128)) ||
+          (st = make_map_u8(&m.b0, w->mxt_down, H, static_cast<uint64_t>(E) * I, 128)) ||
+          (st = make_map_codes_out(&m.o0, L.dguq, 2ull * I, v.rows)) ||
+          (st = make_map_codes_out(&m.o1, L.dguT, v.rows, 2ull * I)) ||
+          (st = make_map_codes_out(&m.o2, L.hwT, v.rows, I)))
+        return st;
+      m.b1 = m.b0;
+      GemmParams p = base_params(cfg, &v.s, ctx->status, 0);
+      p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / 128; p.b_rows_per_expert = I;
+      p.aux0 = ctx->gu + v.r0 * 2 * I; p.rw = router_w; p.dw_part = L.dw_part; p.swiglu_limit = ctx->swiglu_limit;
+      p.sf_out = L.dguq_sc; p.out2 = L.dguT_sc; p.sf_out2 = L.hwT_sc; p.ld = v.rows;   // codes: maps o0..o2
+      p.sfa = L.dyq_sc; p.sfb0 = L.wtd_sc;
+      const long long items = static_cast<long long>(v.s.max_tiles) * p.n_tiles;
+      MOK_CUDA((launch_gemm_mx<128, EPI_DOWN_BWD_MX>(m, p, items < sms ? static_cast<int>(items) : sms, cs)));
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DOWN, 1, cs, last));
+    }
+    {  // dW_down[e] = sum over e's rows of dy[t(r)]^T (w h)[r]
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_DOWN, 0, cs, first));
+      const int bn = tile_n(I);
+      uint16_t* out = g->d_w_down + static_cast<long long>(v.e0) * H * I;
+      MxMaps m;
+      if ((st = make_map_u8(&m.a, L.dyT, v.rows, H, 128)) || (st = make_map_u8(&m.b0, L.hwT, v.rows, I, bn)))
+        return st;
+      m.b1 = m.b0;
+      GemmParams p = base_params(cfg, &v.s, ctx->status, 0);
+      p.wgrad = 1; p.grouped = 1; p.K = rows; p.E = v.ne; p.m_tiles = H / 128; p.n_tiles = I / bn;
+      p.out0 = out; p.out1 = out; p.ld = I; p.split = H;
+      p.sfa = L.dyT_sc; p.sfb0 = L.hwT_sc;
+      MOK_CUDA(launch_mx_tiles<EPI_WGRAD>(m, p, bn, static_cast<long long>(v.ne) * p.m_tiles * p.n_tiles, sms, cs));
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_DOWN, 1, cs, last));
+    }
+    {  // dW_gate|up[e] = sum over e's rows of (dG|dU)[r]^T x[t(r)]
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_GATEUP, 0, cs, first));
+      MxMaps m;
+      if ((st = make_map_u8(&m.a, L.dguT, v.rows, 2ull * I, 128)) || (st = make_map_u8(&m.b0, L.xT, v.rows, H, bnH)))
+        return st;
+      m.b1 = m.b0;
+      GemmParams p = base_params(cfg, &v.s, ctx->status, 0);
+      p.wgrad = 1; p.grouped = 1; p.K = rows; p.E = v.ne; p.m_tiles = 2 * I / 128; p.n_tiles = H / bnH;
+      p.out0 = g->d_w_gate + static_cast<long long>(v.e0) * I * H;
+      p.out1 = g->d_w_up + static_cast<long long>(v.e0) * I * H;
+      p.ld = H; p.split = I;
+      p.sfa = L.dguT_sc; p.sfb0 = L.xT_sc;
+      MOK_CUDA(launch_mx_tiles<EPI_WGRAD>(m, p, bnH, static_cast<long long>(v.ne) * p.m_tiles * p.n_tiles, sms, cs));
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_GATEUP, 1, cs, last));
+    }
+    {  // dx rows = dG W_gate[e] + dU W_up[e], in schedule order
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DGRAD_GATEUP, 0, cs, first));
+      uint16_t* out = ctx->slots + v.r0 * H;
+      MxMaps m;
+      if ((st = make_map_u8(&m.a, L.dguq, 2ull * I, v.rows, 128)) ||
+          (st = make_map_u8(&m.b0, w->mxt_gate, I, static_cast<uint64_t>(E) * H, bnH)) ||
+          (st = make_map_u8(&m.b1, w->mxt_up, I, static_cast<uint64_t>(E) * H, bnH)) ||
+          (st = make_map_out(&m.o0, out, H, v.rows)))
+        return st;
+      GemmParams p = base_params(cfg, &v.s, ctx->status, 0);
+      p.grouped = 1; p.K = 2 * I; p.N = H; p.n_tiles = H / bnH; p.b_rows_per_expert = H; p.b_split = I;
+      p.out0 = out; p.ld = H;
+      p.sfa = L.dguq_sc; p.sfb0 = L.wtg_sc; p.sfb1 = L.wtu_sc; p.sf_kgb = I / 128;
+      MOK_CUDA(launch_mx_tiles<EPI_STORE_ROWS>(m, p, bnH, static_cast<long long>(v.s.max_tiles) * p.n_tiles, sms, cs));
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DGRAD_GATEUP, 1, cs, last));
+    }
   }
   // ---- fixed-order reductions: dx and the router-weight gradient
   MOK_CUDA(mark(cfg, MOK_STAGE_BWD_REDUCE, 0, cs));
-  MOK_CUDA(launch_combine(L.dx_slots, s->slot_row, s->header, mr, Is > 0 ? L.dx_s : nullptr, T, k, H, dx, sms, cs));
+  MOK_CUDA(launch_combine(ctx->slots, s->slot_row, s->header, mr, Is > 0 ? L.dx_s : nullptr, T, k, H, dx, sms, cs));
   MOK_CUDA(launch_dw_reduce(L.dw_part, T * k, 2 * (I / 128), d_router_w, cs));
+  MOK_CUDA(mark(cfg, MOK_STAGE_BWD_REDUCE, 1, cs));
+  return MOK_OK;
+}
+
+// BF16 backward (after MOK_MODE_BF16 and MOK_MODE_MXFP8_FWD forwards): the
+// shared expert's SwiGLU backward and dgrad, the routed experts window by
+// window, the shared weight gradients, then the fixed-order reductions.
+mok_status_t backward_bf16(const mok_config_t* cfg, const uint16_t* dy, const uint16_t* x, const float* router_w,
+                           const mok_schedule_t* s, const std::vector<Win>& wins, const mok_ctx_t* ctx, const mok_weights_t* w, uint16_t* dx, float* d_router_w,
+                           const mok_weight_grads_t* g, const BwdLayout& L, int sms, bool g4, cudaStream_t cs) {
+  const int T = s->T, k = s->k, E = s->E, H = w->H, I = w->I, Is = w->I_s;
+  const long long mr = static_cast<long long>(s->max_tiles) * kTileRows;
+  const size_t nw = wins.size();
+  mok_status_t st;
+  const int bn1 = tile_n(I);
+  const bool perm = resolve_dispatch(cfg) == MOK_DISPATCH_PERMUTE;
+  // ---- permuted dispatch: token rows of dy, and of x (unquantised, for the
+  // gate/up weight gradient), in schedule order.  x's rows: the forward's copy
+  // where it spans the whole schedule (a one-pass forward with the permuted
+  // dispatch), else permuted here window by window, else (a one-pass MXFP8
+  // forward workspace after a forward with a ring) gathered by that GEMM.  The
+  // first window's permutes run on a side stream, overlapping the shared
+  // expert's backward, which reads token-order rows only.
+  const bool reuse_x = perm && ctx->ring_rows == 0 && ctx->dispatch == MOK_DISPATCH_PERMUTE && ctx->x_perm &&
+                       (ctx->mode == MOK_MODE_BF16 || ctx->mode == MOK_MODE_MXFP8_FWD);
+  uint16_t* x_ws = (perm && !reuse_x) ? L.xb_perm : nullptr;
+  auto x_rows = [&](const Win& v) -> const uint16_t* {
+    if (reuse_x) return ctx->x_perm + v.r0 * H;
+    return x_ws;   // NULL: gathered
+  };
+  auto dispatch = [&](const Win& v, cudaStream_t st2) -> cudaError_t {
+    cudaError_t e = cudaSuccess;
+    if (x_ws) e = launch_permute_rows(x, T, H, k, s->slot_row, s->row_src, s->header, v.r0, v.rows, x_ws, sms, st2);
+    if (e == cudaSuccess)
+      e = launch_permute_rows(dy, T, H, k, s->slot_row, s->row_src, s->header, v.r0, v.rows, L.dy_perm, sms, st2);
+    return e;
+  };
+  SideStream* side = nullptr;
+  if (perm && nw > 0) {
+    if ((st = side_stream(&side))) return st;
+    MOK_CUDA(cudaEventRecord(side->fork, cs));
+    MOK_CUDA(cudaStreamWaitEvent(side->s, side->fork, 0));
+    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 0, side->s));
+    MOK_CUDA(dispatch(wins[0], side->s));
+    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 1, side->s, nw == 1));
+    MOK_CUDA(cudaEventRecord(side->join, side->s));
+  } else {
+    MOK_CUDA(mark_skipped(cfg, {MOK_STAGE_BWD_DISPATCH}, cs));
+  }
+  // ---- shared expert backward, first part (dense rows, w = 1): the SwiGLU
+  // backward, which reads dy in token order while the side stream writes dy's
+  // rows in schedule order, and the dgrad.  A GEMM that shares HBM with that
+  // copy slows by more than the copy takes alone, so only this first GEMM
+  // overlaps it; the shared weight gradients run after the routed GEMMs.
+  if (Is > 0) {
+    const int bns = tile_n(Is);
+    {
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DOWN, 0, cs));
+      GemmMaps m;
+      const bool pr = pair_on(cfg, bns);
+      if ((st = make_map(&m.a, dy, H, T, 128, kTileBK)) ||
+          (st = make_map_mn(&m.b0, w->ws_down, Is, H, pr ? bns / 2 : bns, kTileBK)) ||
+          (st = make_map_out(&m.o0, L.dgu_s, 2ull * Is, T)) || (st = make_map_out(&m.o1, L.hs, Is, T)))
+        return st;
+      m.b1 = m.b0;
+      GemmParams p = base_params(cfg, nullptr, ctx->status, 0);
+      p.rows = T; p.K = H; p.N = Is; p.n_tiles = Is / bns; p.b_rows_per_expert = 0;
+      p.aux0 = ctx->gu_s; p.out0 = L.dgu_s; p.out1 = L.hs;
+      p.swiglu_limit = ctx->swiglu_limit;
+      const long long items = ((T + 127) / 128) * static_cast<long long>(p.n_tiles);
+      if (bns == 256)
+        MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_MN_TILE, 256, EPI_DOWN_BWD>(m, p, items, row_pairs(T) * p.n_tiles, pr,
+                                                                           sms, cs)));
+      else
+        MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_MN_TILE, 128, EPI_DOWN_BWD>(m, p, items, 0, false, sms, cs)));
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DOWN, 1, cs));
+    }
+    if (side) MOK_CUDA(cudaStreamWaitEvent(cs, side->join, 0));   // dy's schedule-order rows are written
+    {  // dx_s = dG_s W_s_gate + dU_s W_s_up
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DGRAD, 0, cs));
+      GemmMaps m;
+      const int bn = tile_n(H);
+      const bool pr = pair_on(cfg, bn);
+      if ((st = make_map(&m.a, L.dgu_s, 2 * Is, T, 128, kTileBK)) ||
+          (st = make_map_mn(&m.b0, w->ws_gate, H, Is, pr ? bn / 2 : bn, kTileBK)) ||
+          (st = make_map_mn(&m.b1, w->ws_up, H, Is, pr ? bn / 2 : bn, kTileBK)) ||
+          (st = make_map_out(&m.o0, L.dx_s, H, T)))
+        return st;
+      GemmParams p = base_params(cfg, nullptr, ctx->status, 0);
+      p.rows = T; p.K = 2 * Is; p.N = H; p.n_tiles = H / bn; p.b_rows_per_expert = 0; p.b_split = Is;
+      p.out0 = L.dx_s; p.ld = H;
+      const long long items = ((T + 127) / 128) * static_cast<long long>(p.n_tiles);
+      if (bn == 256)
+        MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_MN_TILE, 256, EPI_STORE_ROWS>(m, p, items, row_pairs(T) * p.n_tiles, pr,
+                                                                             sms, cs)));
+      else
+        MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_MN_TILE, 128, EPI_STORE_ROWS>(m, p, items, 0, false, sms, cs)));
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DGRAD, 1, cs));
+    }
+  } else {
+    MOK_CUDA(mark_skipped(cfg, {MOK_STAGE_BWD_SHARED_DOWN, MOK_STAGE_BWD_SHARED_DGRAD}, cs));
+  }
+  if (side) MOK_CUDA(cudaStreamWaitEvent(cs, side->join, 0));
+  // ---- routed experts, window by window (the token rows, dG|dU and w h span
+  // the window; the dx rows and the router-weight partials every row)
+  if (nw == 0)
+    MOK_CUDA(mark_skipped(cfg, {MOK_STAGE_BWD_DOWN, MOK_STAGE_BWD_WGRAD_DOWN, MOK_STAGE_BWD_WGRAD_GATEUP,
+                                MOK_STAGE_BWD_DGRAD_GATEUP}, cs));
+  for (size_t i = 0; i < nw; ++i) {
+    const Win& v = wins[i];
+    const bool first = i == 0, last = i + 1 == nw;
+    if (perm && !first) {
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 0, cs, false));
+      MOK_CUDA(dispatch(v, cs));
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 1, cs, last));
+    }
+    {  // down dgrad + SwiGLU backward + router-weight partials
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DOWN, 0, cs, first));
+      GemmMaps m;
+      const int bk = perm ? kTileBK : kGatherBK;
+      const bool pr = perm && pair_on(cfg, bn1);
+      if ((st = perm ? make_map(&m.a, L.dy_perm, H, v.rows, 128, bk) : make_map(&m.a, dy, H, T, 1, bk)) ||
+          (st = make_map_mn(&m.b0, w->w_down, I, static_cast<uint64_t>(E) * H, pr ? bn1 / 2 : bn1, bk)) ||
+          (st = make_map_out(&m.o0, L.dgu, 2ull * I, v.rows)) || (st = make_map_out(&m.o1, L.hw, I, v.rows)))
+        return st;
+      m.b1 = m.b0;
+      GemmParams p = base_params(cfg, &v.s, ctx->status, 0);
+      p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / bn1; p.b_rows_per_expert = H;
+      p.aux0 = ctx->gu + v.r0 * 2 * I; p.out0 = L.dgu; p.out1 = L.hw; p.rw = router_w; p.dw_part = L.dw_part;
+      p.swiglu_limit = ctx->swiglu_limit;
+      p.ga = dy; p.ga_ld = H;
+      const long long items = static_cast<long long>(v.s.max_tiles) * p.n_tiles;
+      const int grid = items < sms ? static_cast<int>(items) : sms;
+      if (perm && bn1 == 256)
+        MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_MN_TILE, 256, EPI_DOWN_BWD>(m, p, items, items, pr, sms, cs)));
+      else if (perm)
+        MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_MN_TILE, 128, EPI_DOWN_BWD>(m, p, grid, cs)));
+      else if (g4 && bn1 == 256)
+        MOK_CUDA((launch_gemm<SRC_K_GATHER, SRC_MN_TILE, 256, EPI_DOWN_BWD>(m, p, grid, cs)));
+      else if (g4)
+        MOK_CUDA((launch_gemm<SRC_K_GATHER, SRC_MN_TILE, 128, EPI_DOWN_BWD>(m, p, grid, cs)));
+      else if (bn1 == 256)
+        MOK_CUDA((launch_gemm<SRC_K_GATHER_LSU, SRC_MN_TILE, 256, EPI_DOWN_BWD>(m, p, grid, cs)));
+      else
+        MOK_CUDA((launch_gemm<SRC_K_GATHER_LSU, SRC_MN_TILE, 128, EPI_DOWN_BWD>(m, p, grid, cs)));
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DOWN, 1, cs, last));
+    }
+    {  // dW_down[e] = sum over e's rows of dy[t(r)]^T (w h)[r]
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_DOWN, 0, cs, first));
+      uint16_t* out = g->d_w_down + static_cast<long long>(v.e0) * H * I;
+      GemmMaps m;
+      const int bk = perm ? kTileBK : kGatherBK;
+      const int bn = tile_n(I);
+      const bool pr = perm && pair_on(cfg, bn);
+      if ((st = perm ? make_map_mn(&m.a, L.dy_perm, H, v.rows, 128, bk) : make_map(&m.a, dy, H, T, 1, bk)) ||
+          (st = make_map_mn(&m.b0, L.hw, I, v.rows, pr ? bn / 2 : bn, bk)) ||
+          (st = make_map_out(&m.o0, out, I, static_cast<uint64_t>(v.ne) * H)))
+        return st;
+      m.o1 = m.o0;
+      m.b1 = m.b0;
+      GemmParams p = base_params(cfg, &v.s, ctx->status, 0);
+      p.wgrad = 1; p.grouped = 1; p.E = v.ne; p.m_tiles = H / 128; p.n_tiles = I / bn;
+      p.out0 = out; p.out1 = out; p.ld = I; p.split = H;
+      p.estride = static_cast<long long>(H) * I;
+      p.ga = dy; p.ga_ld = H;
+      const long long items = static_cast<long long>(v.ne) * p.m_tiles * p.n_tiles;
+      const long long pitems = static_cast<long long>(v.ne) * ((p.m_tiles + 1) / 2) * p.n_tiles;
+      const int grid = items < sms ? static_cast<int>(items) : sms;
+      if (perm && bn == 256)
+        MOK_CUDA((launch_tiles<SRC_MN_TILE, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, items, pitems, pr, sms, cs)));
+      else if (perm)
+        MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, grid, cs)));
+      else if (g4 && bn == 256)
+        MOK_CUDA((launch_gemm<SRC_MN_GATHER, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, grid, cs)));
+      else if (g4)
+        MOK_CUDA((launch_gemm<SRC_MN_GATHER, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, grid, cs)));
+      else if (bn == 256)
+        MOK_CUDA((launch_gemm<SRC_MN_GATHER_LSU, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, grid, cs)));
+      else
+        MOK_CUDA((launch_gemm<SRC_MN_GATHER_LSU, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, grid, cs)));
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_DOWN, 1, cs, last));
+    }
+    {  // dW_gate|up[e] = sum over e's rows of (dG|dU)[r]^T x[t(r)]
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_GATEUP, 0, cs, first));
+      uint16_t* out_g = g->d_w_gate + static_cast<long long>(v.e0) * I * H;
+      uint16_t* out_u = g->d_w_up + static_cast<long long>(v.e0) * I * H;
+      const uint16_t* xr = x_rows(v);
+      GemmMaps m;
+      const int bk = xr ? kTileBK : kGatherBK;
+      const int bn = tile_n(H);
+      const bool pr = xr && pair_on(cfg, bn);
+      if ((st = make_map_mn(&m.a, L.dgu, 2 * I, v.rows, 128, bk)) ||
+          (st = xr ? make_map_mn(&m.b0, xr, H, v.rows, pr ? bn / 2 : bn, bk) : make_map(&m.b0, x, H, T, 1, bk)) ||
+          (st = make_map_out(&m.o0, out_g, H, static_cast<uint64_t>(v.ne) * I)) ||
+          (st = make_map_out(&m.o1, out_u, H, static_cast<uint64_t>(v.ne) * I)))
+        return st;
+      m.b1 = m.b0;
+      GemmParams p = base_params(cfg, &v.s, ctx->status, 0);
+      p.wgrad = 1; p.grouped = 1; p.E = v.ne; p.m_tiles = 2 * I / 128; p.n_tiles = H / bn;
+      p.out0 = out_g; p.out1 = out_u; p.ld = H; p.split = I;
+      p.estride = static_cast<long long>(I) * H;
+      p.gb = x; p.gb_ld = H;
+      const long long items = static_cast<long long>(v.ne) * p.m_tiles * p.n_tiles;
+      const long long pitems = static_cast<long long>(v.ne) * ((p.m_tiles + 1) / 2) * p.n_tiles;
+      const int grid = items < sms ? static_cast<int>(items) : sms;
+      if (xr && bn == 256)
+        MOK_CUDA((launch_tiles<SRC_MN_TILE, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, items, pitems, pr, sms, cs)));
+      else if (xr)
+        MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, grid, cs)));
+      else if (g4 && bn == 256)
+        MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_GATHER, 256, EPI_WGRAD>(m, p, grid, cs)));
+      else if (g4)
+        MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_GATHER, 128, EPI_WGRAD>(m, p, grid, cs)));
+      else if (bn == 256)
+        MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_GATHER_LSU, 256, EPI_WGRAD>(m, p, grid, cs)));
+      else
+        MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_GATHER_LSU, 128, EPI_WGRAD>(m, p, grid, cs)));
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_GATEUP, 1, cs, last));
+    }
+    {  // dx rows = dG W_gate[e] + dU W_up[e], in schedule order
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DGRAD_GATEUP, 0, cs, first));
+      uint16_t* out = ctx->slots + v.r0 * H;
+      GemmMaps m;
+      const int bn = tile_n(H);
+      const bool pr = pair_on(cfg, bn);
+      const int bw = pr ? bn / 2 : bn;
+      if ((st = make_map(&m.a, L.dgu, 2 * I, v.rows, 128, kTileBK)) ||
+          (st = make_map_mn(&m.b0, w->w_gate, H, static_cast<uint64_t>(E) * I, bw, kTileBK)) ||
+          (st = make_map_mn(&m.b1, w->w_up, H, static_cast<uint64_t>(E) * I, bw, kTileBK)) ||
+          (st = make_map_out(&m.o0, out, H, v.rows)))
+        return st;
+      GemmParams p = base_params(cfg, &v.s, ctx->status, 0);
+      p.grouped = 1; p.K = 2 * I; p.N = H; p.n_tiles = H / bn; p.b_rows_per_expert = I; p.b_split = I;
+      p.out0 = out; p.ld = H;
+      const long long items = static_cast<long long>(v.s.max_tiles) * p.n_tiles;
+      if (bn == 256)
+        MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_MN_TILE, 256, EPI_STORE_ROWS>(m, p, items, items, pr, sms, cs)));
+      else
+        MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_MN_TILE, 128, EPI_STORE_ROWS>(m, p, items, 0, false, sms, cs)));
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DGRAD_GATEUP, 1, cs, last));
+    }
+  }
+  // ---- shared expert backward, second part: the weight gradients
+  if (Is > 0) {
+    const int bns = tile_n(Is);
+    {  // dW_s_down = dy^T h_s
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_DOWN, 0, cs));
+      GemmMaps m;
+      const bool pr = pair_on(cfg, bns);
+      if ((st = make_map_mn(&m.a, dy, H, T, 128, kTileBK)) ||
+          (st = make_map_mn(&m.b0, L.hs, Is, T, pr ? bns / 2 : bns, kTileBK)) ||
+          (st = make_map_out(&m.o0, g->d_ws_down, Is, H)))
+        return st;
+      m.o1 = m.o0;
+      m.b1 = m.b0;
+      GemmParams p = base_params(cfg, nullptr, ctx->status, 0);
+      p.wgrad = 1; p.rows = T; p.E = 1; p.m_tiles = H / 128; p.n_tiles = Is / bns;
+      p.out0 = g->d_ws_down; p.out1 = g->d_ws_down; p.ld = Is; p.split = H; p.estride = 0;
+      const long long items = static_cast<long long>(p.m_tiles) * p.n_tiles;
+      const long long pitems = static_cast<long long>((p.m_tiles + 1) / 2) * p.n_tiles;
+      if (bns == 256)
+        MOK_CUDA((launch_tiles<SRC_MN_TILE, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, items, pitems, pr, sms, cs)));
+      else
+        MOK_CUDA((launch_tiles<SRC_MN_TILE, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, items, 0, false, sms, cs)));
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_DOWN, 1, cs));
+    }
+    {  // dW_s_gate|up = (dG_s|dU_s)^T x
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_GATEUP, 0, cs));
+      GemmMaps m;
+      const int bn = tile_n(H);
+      const bool pr = pair_on(cfg, bn);
+      if ((st = make_map_mn(&m.a, L.dgu_s, 2 * Is, T, 128, kTileBK)) ||
+          (st = make_map_mn(&m.b0, x, H, T, pr ? bn / 2 : bn, kTileBK)) ||
+          (st = make_map_out(&m.o0, g->d_ws_gate, H, Is)) || (st = make_map_out(&m.o1, g->d_ws_up, H, Is)))
+        return st;
+      m.b1 = m.b0;
+      GemmParams p = base_params(cfg, nullptr, ctx->status, 0);
+      p.wgrad = 1; p.rows = T; p.E = 1; p.m_tiles = 2 * Is / 128; p.n_tiles = H / bn;
+      p.out0 = g->d_ws_gate; p.out1 = g->d_ws_up; p.ld = H; p.split = Is; p.estride = 0;
+      const long long items = static_cast<long long>(p.m_tiles) * p.n_tiles;
+      const long long pitems = static_cast<long long>((p.m_tiles + 1) / 2) * p.n_tiles;
+      if (bn == 256)
+        MOK_CUDA((launch_tiles<SRC_MN_TILE, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, items, pitems, pr, sms, cs)));
+      else
+        MOK_CUDA((launch_tiles<SRC_MN_TILE, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, items, 0, false, sms, cs)));
+      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_GATEUP, 1, cs));
+    }
+  } else {
+    MOK_CUDA(mark_skipped(cfg, {MOK_STAGE_BWD_SHARED_WGRAD_DOWN, MOK_STAGE_BWD_SHARED_WGRAD_GATEUP}, cs));
+  }
+  // ---- fixed-order reductions: dx and the router-weight gradient
+  MOK_CUDA(mark(cfg, MOK_STAGE_BWD_REDUCE, 0, cs));
+  MOK_CUDA(launch_combine(ctx->slots, s->slot_row, s->header, mr, Is > 0 ? L.dx_s : nullptr, T, k, H, dx, sms,
+                          cs));
+  MOK_CUDA(launch_dw_reduce(L.dw_part, T * k, 2 * (I / bn1), d_router_w, cs));
   MOK_CUDA(mark(cfg, MOK_STAGE_BWD_REDUCE, 1, cs));
   return MOK_OK;
 }
@@ -1145,10 +1651,29 @@ mok_status_t mok_mxfp8_quantize_dual(const uint16_t* x, int64_t batch, int rows,
 }
 
 size_t mok_ctx_bytes(int T, int k, int E, int H, int I, int I_s, int mode) {
-  if (check_shapes(T, k, E, H, I, I_s) != MOK_OK) return 0;
+  return mok_ctx_bytes_ring(T, k, E, H, I, I_s, mode, 0);
+}
+
+size_t mok_ctx_bytes_ring(int T, int k, int E, int H, int I, int I_s, int mode, int64_t macrobatch_size) {
+  if (check_shapes(T, k, E, H, I, I_s) != MOK_OK || macrobatch_size < 0) return 0;
   mok_ctx_t c;
   CtxExtra X;
-  return carve_ctx(nullptr, T, k, E, H, I, I_s, mode, &c, &X);
+  return carve_ctx(nullptr, T, k, E, H, I, I_s, mode,
+                   ring_rows_of(macrobatch_size, max_tiles_of(T, k, E) * kTileRows), &c, &X);
+}
+
+mok_status_t mok_macrobatch_plan(const int32_t* cnt, int E, int64_t macrobatch_size, int32_t* first_expert,
+                                 int* num_windows) {
+  if (!cnt || !first_expert || !num_windows) return fail(MOK_ERR_INVALID_ARG, "NULL argument");
+  if (E < 1 || E > 1024) return fail(MOK_ERR_INVALID_ARG, "need 1 <= E <= 1024 (E=%d)", E);
+  if (macrobatch_size < 0) return fail(MOK_ERR_INVALID_ARG, "macrobatch_size < 0");
+  const long long ring = macrobatch_size == 0 ? 0 : (macrobatch_size + kTileRows - 1) / kTileRows * kTileRows;
+  std::vector<int> first;
+  const mok_status_t st = plan_windows(cnt, E, ring, &first);
+  if (st) return st;
+  for (size_t i = 0; i < first.size(); ++i) first_expert[i] = first[i];
+  *num_windows = static_cast<int>(first.size()) - 1;
+  return MOK_OK;
 }
 
 mok_status_t mok_ctx_status(const mok_ctx_t* ctx, int* status) {
@@ -1189,27 +1714,34 @@ mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x, const float
     if (!aligned16(q)) return fail(MOK_ERR_INVALID_ARG, "misaligned pointer");
   if (Is > 0 && (!aligned16(w->ws_gate) || !aligned16(w->ws_up) || !aligned16(w->ws_down)))
     return fail(MOK_ERR_INVALID_ARG, "misaligned shared weight pointer");
-  if (ctx_bytes < mok_ctx_bytes(T, k, E, H, I, Is, cfg->mode))
+  if (ctx_bytes < mok_ctx_bytes_ring(T, k, E, H, I, Is, cfg->mode, cfg->macrobatch_size))
     return fail(MOK_ERR_INVALID_ARG, "context buffer too small");
   int sms = 0;
   st = device_info(&sms);
   if (st) return st;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const bool g4 = (cfg->debug_flags & MOK_DEBUG_TMA_GATHER4) != 0;
+  const long long mr = static_cast<long long>(s->max_tiles) * kTileRows;
+  const long long ring = ring_rows_of(cfg->macrobatch_size, mr);
   CtxExtra X;
-  carve_ctx(ctx_buf, T, k, E, H, I, Is, cfg->mode, ctx, &X);
+  mok_ctx_t c;
+  carve_ctx(ctx_buf, T, k, E, H, I, Is, cfg->mode, ring, &c, &X);
+  // the windows are planned (a ring reads the expert counts back) before any
+  // layer work is enqueued
+  std::vector<Win> wins;
+  if ((st = make_windows(s, ring, X.view, cs, &wins))) return st;
+  *ctx = c;
   ctx->swiglu_limit = cfg->swiglu_limit;
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_PREP, 0, cs));
   MOK_CUDA(cudaMemsetAsync(ctx->status, 0, 8 * sizeof(int), cs));
   MOK_CUDA(launch_dependent(propagate_status_kernel, dim3(1), dim3(1), 0, cs, static_cast<const int*>(s->header),
                             ctx->status));
 
-  const long long mr = static_cast<long long>(s->max_tiles) * kTileRows;
   if (mx) {
-    st = forward_mxfp8(cfg, x, router_w, s, w, ctx, X, sms, cs);
+    st = forward_mxfp8(cfg, x, router_w, s, wins, w, ctx, X, sms, cs);
     if (st) return st;
   } else {
-    st = forward_bf16(cfg, x, router_w, s, w, ctx, mr, sms, g4, cs);
+    st = forward_bf16(cfg, x, router_w, s, wins, w, ctx, sms, g4, cs);
     if (st) return st;
   }
 
@@ -1222,10 +1754,15 @@ mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x, const float
 }
 
 size_t mok_bwd_workspace_bytes(int T, int k, int E, int H, int I, int I_s, int mode) {
-  if (check_shapes(T, k, E, H, I, I_s) != MOK_OK) return 0;
+  return mok_bwd_workspace_bytes_ring(T, k, E, H, I, I_s, mode, 0);
+}
+
+size_t mok_bwd_workspace_bytes_ring(int T, int k, int E, int H, int I, int I_s, int mode, int64_t macrobatch_size) {
+  if (check_shapes(T, k, E, H, I, I_s) != MOK_OK || macrobatch_size < 0) return 0;
   if (mode != MOK_MODE_BF16 && mode != MOK_MODE_MXFP8_FWD && mode != MOK_MODE_MXFP8) return 0;
   BwdLayout L;
-  return carve_bwd(nullptr, T, k, E, H, I, I_s, mode, &L);
+  return carve_bwd(nullptr, T, k, E, H, I, I_s, mode,
+                   ring_rows_of(macrobatch_size, max_tiles_of(T, k, E) * kTileRows), &L);
 }
 
 mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uint16_t* x,
@@ -1266,285 +1803,20 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
       if (Is > 0 && (!q || !aligned16(q)))
         return fail(MOK_ERR_INVALID_ARG, "MXFP8 backward needs the transposed shared weight copies");
   }
-  if (ws_bytes < mok_bwd_workspace_bytes(T, k, E, H, I, Is, ctx->mode))
+  if (ws_bytes < mok_bwd_workspace_bytes_ring(T, k, E, H, I, Is, ctx->mode, cfg->macrobatch_size))
     return fail(MOK_ERR_INVALID_ARG, "backward workspace too small");
   int sms = 0;
   st = device_info(&sms);
   if (st) return st;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const bool g4 = (cfg->debug_flags & MOK_DEBUG_TMA_GATHER4) != 0;
+  const long long ring = ring_rows_of(cfg->macrobatch_size, max_tiles_of(T, k, E) * kTileRows);
   BwdLayout L;
-  carve_bwd(ws, T, k, E, H, I, Is, ctx->mode, &L);
-  if (mxb) return backward_mxfp8(cfg, dy, x, router_w, s, ctx, w, dx, d_router_w, g, L, sms, cs);
-  const long long mr = static_cast<long long>(s->max_tiles) * kTileRows;
-
-  const int bn1 = tile_n(I);
-  const bool perm = resolve_dispatch(cfg) == MOK_DISPATCH_PERMUTE;
-  // ---- permuted dispatch: token rows of dy, and of x (unquantised, for the
-  // weight gradient), in schedule order; the forward's copy of x serves when it
-  // holds exactly that.  The permutes run on a side stream, overlapping the
-  // shared expert's backward, which reads token-order rows only.
-  const uint16_t* x_rows = nullptr;
-  SideStream* side = nullptr;
-  if (perm) {
-    if ((st = side_stream(&side))) return st;
-    MOK_CUDA(cudaEventRecord(side->fork, cs));
-    MOK_CUDA(cudaStreamWaitEvent(side->s, side->fork, 0));
-    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 0, side->s));
-    if (ctx->dispatch == MOK_DISPATCH_PERMUTE && (ctx->mode == MOK_MODE_BF16 || ctx->mode == MOK_MODE_MXFP8_FWD) &&
-        ctx->x_perm) {
-      x_rows = ctx->x_perm;
-    } else {
-      if (!L.xb_perm) return fail(MOK_ERR_INVALID_ARG, "context holds no schedule-order copy of x");
-      MOK_CUDA(launch_permute_rows(x, T, H, k, s->slot_row, s->row_src, s->header, mr, L.xb_perm, sms, side->s));
-      x_rows = L.xb_perm;
-    }
-    MOK_CUDA(launch_permute_rows(dy, T, H, k, s->slot_row, s->row_src, s->header, mr, L.dy_perm, sms, side->s));
-    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 1, side->s));
-    MOK_CUDA(cudaEventRecord(side->join, side->s));
-  } else {
-    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 0, cs));
-    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DISPATCH, 1, cs));
-  }
-  // ---- shared expert backward, first part (dense rows, w = 1): the SwiGLU
-  // backward, which reads dy in token order while the side stream writes dy's
-  // rows in schedule order, and the dgrad.  A GEMM that shares HBM with that
-  // copy slows by more than the copy takes alone, so only this first GEMM
-  // overlaps it; the shared weight gradients run after the routed GEMMs.
-  if (Is > 0) {
-    const int bns = tile_n(Is);
-    {
-      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DOWN, 0, cs));
-      GemmMaps m;
-      const bool pr = pair_on(cfg, bns);
-      if ((st = make_map(&m.a, dy, H, T, 128, kTileBK)) ||
-          (st = make_map_mn(&m.b0, w->ws_down, Is, H, pr ? bns / 2 : bns, kTileBK)) ||
-          (st = make_map_out(&m.o0, L.dgu_s, 2ull * Is, T)) || (st = make_map_out(&m.o1, L.hs, Is, T)))
-        return st;
-      m.b1 = m.b0;
-      GemmParams p = base_params(cfg, nullptr, ctx->status, 0);
-      p.rows = T; p.K = H; p.N = Is; p.n_tiles = Is / bns; p.b_rows_per_expert = 0;
-      p.aux0 = ctx->gu_s; p.out0 = L.dgu_s; p.out1 = L.hs;
-      p.swiglu_limit = ctx->swiglu_limit;
-      const long long items = ((T + 127) / 128) * static_cast<long long>(p.n_tiles);
-      if (bns == 256)
-        MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_MN_TILE, 256, EPI_DOWN_BWD>(m, p, items, row_pairs(T) * p.n_tiles, pr,
-                                                                           sms, cs)));
-      else
-        MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_MN_TILE, 128, EPI_DOWN_BWD>(m, p, items, 0, false, sms, cs)));
-      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DOWN, 1, cs));
-    }
-    if (side) MOK_CUDA(cudaStreamWaitEvent(cs, side->join, 0));   // dy's schedule-order rows are written
-    {  // dx_s = dG_s W_s_gate + dU_s W_s_up
-      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DGRAD, 0, cs));
-      GemmMaps m;
-      const int bn = tile_n(H);
-      const bool pr = pair_on(cfg, bn);
-      if ((st = make_map(&m.a, L.dgu_s, 2 * Is, T, 128, kTileBK)) ||
-          (st = make_map_mn(&m.b0, w->ws_gate, H, Is, pr ? bn / 2 : bn, kTileBK)) ||
-          (st = make_map_mn(&m.b1, w->ws_up, H, Is, pr ? bn / 2 : bn, kTileBK)) ||
-          (st = make_map_out(&m.o0, L.dx_s, H, T)))
-        return st;
-      GemmParams p = base_params(cfg, nullptr, ctx->status, 0);
-      p.rows = T; p.K = 2 * Is; p.N = H; p.n_tiles = H / bn; p.b_rows_per_expert = 0; p.b_split = Is;
-      p.out0 = L.dx_s; p.ld = H;
-      const long long items = ((T + 127) / 128) * static_cast<long long>(p.n_tiles);
-      if (bn == 256)
-        MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_MN_TILE, 256, EPI_STORE_ROWS>(m, p, items, row_pairs(T) * p.n_tiles, pr,
-                                                                             sms, cs)));
-      else
-        MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_MN_TILE, 128, EPI_STORE_ROWS>(m, p, items, 0, false, sms, cs)));
-      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_DGRAD, 1, cs));
-    }
-  } else {
-    for (int sg : {MOK_STAGE_BWD_SHARED_DOWN, MOK_STAGE_BWD_SHARED_DGRAD}) {
-      MOK_CUDA(mark(cfg, sg, 0, cs));
-      MOK_CUDA(mark(cfg, sg, 1, cs));
-    }
-  }
-  // ---- routed: down dgrad + SwiGLU backward + router-weight partials
-  if (side) MOK_CUDA(cudaStreamWaitEvent(cs, side->join, 0));
-  {
-    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DOWN, 0, cs));
-    GemmMaps m;
-    const int bk = perm ? kTileBK : kGatherBK;
-    const bool pr = perm && pair_on(cfg, bn1);
-    if ((st = perm ? make_map(&m.a, L.dy_perm, H, mr, 128, bk) : make_map(&m.a, dy, H, T, 1, bk)) ||
-        (st = make_map_mn(&m.b0, w->w_down, I, static_cast<uint64_t>(E) * H, pr ? bn1 / 2 : bn1, bk)) ||
-        (st = make_map_out(&m.o0, L.dgu, 2ull * I, mr)) || (st = make_map_out(&m.o1, L.hw, I, mr)))
-      return st;
-    m.b1 = m.b0;
-    GemmParams p = base_params(cfg, s, ctx->status, 0);
-    p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / bn1; p.b_rows_per_expert = H;
-    p.aux0 = ctx->gu; p.out0 = L.dgu; p.out1 = L.hw; p.rw = router_w; p.dw_part = L.dw_part;
-    p.swiglu_limit = ctx->swiglu_limit;
-    p.ga = dy; p.ga_ld = H;
-    const long long items = static_cast<long long>(s->max_tiles) * p.n_tiles;
-    const int grid = items < sms ? static_cast<int>(items) : sms;
-    if (perm && bn1 == 256)
-      MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_MN_TILE, 256, EPI_DOWN_BWD>(m, p, items, items, pr, sms, cs)));
-    else if (perm)
-      MOK_CUDA((launch_gemm<SRC_K_TILE, SRC_MN_TILE, 128, EPI_DOWN_BWD>(m, p, grid, cs)));
-    else if (g4 && bn1 == 256)
-      MOK_CUDA((launch_gemm<SRC_K_GATHER, SRC_MN_TILE, 256, EPI_DOWN_BWD>(m, p, grid, cs)));
-    else if (g4)
-      MOK_CUDA((launch_gemm<SRC_K_GATHER, SRC_MN_TILE, 128, EPI_DOWN_BWD>(m, p, grid, cs)));
-    else if (bn1 == 256)
-      MOK_CUDA((launch_gemm<SRC_K_GATHER_LSU, SRC_MN_TILE, 256, EPI_DOWN_BWD>(m, p, grid, cs)));
-    else
-      MOK_CUDA((launch_gemm<SRC_K_GATHER_LSU, SRC_MN_TILE, 128, EPI_DOWN_BWD>(m, p, grid, cs)));
-    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DOWN, 1, cs));
-  }
-  // ---- routed: dW_down[e] = sum over e's rows of dy[t(r)]^T (w h)[r]
-  {
-    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_DOWN, 0, cs));
-    GemmMaps m;
-    const int bk = perm ? kTileBK : kGatherBK;
-    const int bn = tile_n(I);
-    const bool pr = perm && pair_on(cfg, bn);
-    if ((st = perm ? make_map_mn(&m.a, L.dy_perm, H, mr, 128, bk) : make_map(&m.a, dy, H, T, 1, bk)) ||
-        (st = make_map_mn(&m.b0, L.hw, I, mr, pr ? bn / 2 : bn, bk)) ||
-        (st = make_map_out(&m.o0, g->d_w_down, I, static_cast<uint64_t>(E) * H)))
-      return st;
-    m.o1 = m.o0;
-    m.b1 = m.b0;
-    GemmParams p = base_params(cfg, s, ctx->status, 0);
-    p.wgrad = 1; p.grouped = 1; p.E = E; p.m_tiles = H / 128; p.n_tiles = I / bn;
-    p.out0 = g->d_w_down; p.out1 = g->d_w_down; p.ld = I; p.split = H;
-    p.estride = static_cast<long long>(H) * I;
-    p.ga = dy; p.ga_ld = H;
-    const long long items = static_cast<long long>(E) * p.m_tiles * p.n_tiles;
-    const long long pitems = static_cast<long long>(E) * ((p.m_tiles + 1) / 2) * p.n_tiles;
-    const int grid = items < sms ? static_cast<int>(items) : sms;
-    if (perm && bn == 256)
-      MOK_CUDA((launch_tiles<SRC_MN_TILE, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, items, pitems, pr, sms, cs)));
-    else if (perm)
-      MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, grid, cs)));
-    else if (g4 && bn == 256)
-      MOK_CUDA((launch_gemm<SRC_MN_GATHER, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, grid, cs)));
-    else if (g4)
-      MOK_CUDA((launch_gemm<SRC_MN_GATHER, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, grid, cs)));
-    else if (bn == 256)
-      MOK_CUDA((launch_gemm<SRC_MN_GATHER_LSU, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, grid, cs)));
-    else
-      MOK_CUDA((launch_gemm<SRC_MN_GATHER_LSU, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, grid, cs)));
-    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_DOWN, 1, cs));
-  }
-  // ---- routed: dW_gate|up[e] = sum over e's rows of (dG|dU)[r]^T x[t(r)]
-  {
-    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_GATEUP, 0, cs));
-    GemmMaps m;
-    const int bk = perm ? kTileBK : kGatherBK;
-    const int bn = tile_n(H);
-    const bool pr = perm && pair_on(cfg, bn);
-    if ((st = make_map_mn(&m.a, L.dgu, 2 * I, mr, 128, bk)) ||
-        (st = perm ? make_map_mn(&m.b0, x_rows, H, mr, pr ? bn / 2 : bn, bk) : make_map(&m.b0, x, H, T, 1, bk)) ||
-        (st = make_map_out(&m.o0, g->d_w_gate, H, static_cast<uint64_t>(E) * I)) ||
-        (st = make_map_out(&m.o1, g->d_w_up, H, static_cast<uint64_t>(E) * I)))
-      return st;
-    m.b1 = m.b0;
-    GemmParams p = base_params(cfg, s, ctx->status, 0);
-    p.wgrad = 1; p.grouped = 1; p.E = E; p.m_tiles = 2 * I / 128; p.n_tiles = H / bn;
-    p.out0 = g->d_w_gate; p.out1 = g->d_w_up; p.ld = H; p.split = I;
-    p.estride = static_cast<long long>(I) * H;
-    p.gb = x; p.gb_ld = H;
-    const long long items = static_cast<long long>(E) * p.m_tiles * p.n_tiles;
-    const long long pitems = static_cast<long long>(E) * ((p.m_tiles + 1) / 2) * p.n_tiles;
-    const int grid = items < sms ? static_cast<int>(items) : sms;
-    if (perm && bn == 256)
-      MOK_CUDA((launch_tiles<SRC_MN_TILE, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, items, pitems, pr, sms, cs)));
-    else if (perm)
-      MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, grid, cs)));
-    else if (g4 && bn == 256)
-      MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_GATHER, 256, EPI_WGRAD>(m, p, grid, cs)));
-    else if (g4)
-      MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_GATHER, 128, EPI_WGRAD>(m, p, grid, cs)));
-    else if (bn == 256)
-      MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_GATHER_LSU, 256, EPI_WGRAD>(m, p, grid, cs)));
-    else
-      MOK_CUDA((launch_gemm<SRC_MN_TILE, SRC_MN_GATHER_LSU, 128, EPI_WGRAD>(m, p, grid, cs)));
-    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_WGRAD_GATEUP, 1, cs));
-  }
-  // ---- routed: dx slots = dG W_gate[e] + dU W_up[e]
-  {
-    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DGRAD_GATEUP, 0, cs));
-    GemmMaps m;
-    const int bn = tile_n(H);
-    const bool pr = pair_on(cfg, bn);
-    const int bw = pr ? bn / 2 : bn;
-    if ((st = make_map(&m.a, L.dgu, 2 * I, mr, 128, kTileBK)) ||
-        (st = make_map_mn(&m.b0, w->w_gate, H, static_cast<uint64_t>(E) * I, bw, kTileBK)) ||
-        (st = make_map_mn(&m.b1, w->w_up, H, static_cast<uint64_t>(E) * I, bw, kTileBK)) ||
-        (st = make_map_out(&m.o0, L.dx_slots, H, mr)))
-      return st;
-    GemmParams p = base_params(cfg, s, ctx->status, 0);
-    p.grouped = 1; p.K = 2 * I; p.N = H; p.n_tiles = H / bn; p.b_rows_per_expert = I; p.b_split = I;
-    p.out0 = L.dx_slots; p.ld = H;
-    const long long items = static_cast<long long>(s->max_tiles) * p.n_tiles;
-    if (bn == 256)
-      MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_MN_TILE, 256, EPI_STORE_ROWS>(m, p, items, items, pr, sms, cs)));
-    else
-      MOK_CUDA((launch_tiles<SRC_K_TILE, SRC_MN_TILE, 128, EPI_STORE_ROWS>(m, p, items, 0, false, sms, cs)));
-    MOK_CUDA(mark(cfg, MOK_STAGE_BWD_DGRAD_GATEUP, 1, cs));
-  }
-  // ---- shared expert backward, second part: the weight gradients
-  if (Is > 0) {
-    const int bns = tile_n(Is);
-    {  // dW_s_down = dy^T h_s
-      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_DOWN, 0, cs));
-      GemmMaps m;
-      const bool pr = pair_on(cfg, bns);
-      if ((st = make_map_mn(&m.a, dy, H, T, 128, kTileBK)) ||
-          (st = make_map_mn(&m.b0, L.hs, Is, T, pr ? bns / 2 : bns, kTileBK)) ||
-          (st = make_map_out(&m.o0, g->d_ws_down, Is, H)))
-        return st;
-      m.o1 = m.o0;
-      m.b1 = m.b0;
-      GemmParams p = base_params(cfg, nullptr, ctx->status, 0);
-      p.wgrad = 1; p.rows = T; p.E = 1; p.m_tiles = H / 128; p.n_tiles = Is / bns;
-      p.out0 = g->d_ws_down; p.out1 = g->d_ws_down; p.ld = Is; p.split = H; p.estride = 0;
-      const long long items = static_cast<long long>(p.m_tiles) * p.n_tiles;
-      const long long pitems = static_cast<long long>((p.m_tiles + 1) / 2) * p.n_tiles;
-      if (bns == 256)
-        MOK_CUDA((launch_tiles<SRC_MN_TILE, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, items, pitems, pr, sms, cs)));
-      else
-        MOK_CUDA((launch_tiles<SRC_MN_TILE, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, items, 0, false, sms, cs)));
-      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_DOWN, 1, cs));
-    }
-    {  // dW_s_gate|up = (dG_s|dU_s)^T x
-      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_GATEUP, 0, cs));
-      GemmMaps m;
-      const int bn = tile_n(H);
-      const bool pr = pair_on(cfg, bn);
-      if ((st = make_map_mn(&m.a, L.dgu_s, 2 * Is, T, 128, kTileBK)) ||
-          (st = make_map_mn(&m.b0, x, H, T, pr ? bn / 2 : bn, kTileBK)) ||
-          (st = make_map_out(&m.o0, g->d_ws_gate, H, Is)) || (st = make_map_out(&m.o1, g->d_ws_up, H, Is)))
-        return st;
-      m.b1 = m.b0;
-      GemmParams p = base_params(cfg, nullptr, ctx->status, 0);
-      p.wgrad = 1; p.rows = T; p.E = 1; p.m_tiles = 2 * Is / 128; p.n_tiles = H / bn;
-      p.out0 = g->d_ws_gate; p.out1 = g->d_ws_up; p.ld = H; p.split = Is; p.estride = 0;
-      const long long items = static_cast<long long>(p.m_tiles) * p.n_tiles;
-      const long long pitems = static_cast<long long>((p.m_tiles + 1) / 2) * p.n_tiles;
-      if (bn == 256)
-        MOK_CUDA((launch_tiles<SRC_MN_TILE, SRC_MN_TILE, 256, EPI_WGRAD>(m, p, items, pitems, pr, sms, cs)));
-      else
-        MOK_CUDA((launch_tiles<SRC_MN_TILE, SRC_MN_TILE, 128, EPI_WGRAD>(m, p, items, 0, false, sms, cs)));
-      MOK_CUDA(mark(cfg, MOK_STAGE_BWD_SHARED_WGRAD_GATEUP, 1, cs));
-    }
-  } else {
-    for (int sg : {MOK_STAGE_BWD_SHARED_WGRAD_DOWN, MOK_STAGE_BWD_SHARED_WGRAD_GATEUP}) {
-      MOK_CUDA(mark(cfg, sg, 0, cs));
-      MOK_CUDA(mark(cfg, sg, 1, cs));
-    }
-  }
-  // ---- fixed-order reductions: dx and the router-weight gradient
-  MOK_CUDA(mark(cfg, MOK_STAGE_BWD_REDUCE, 0, cs));
-  MOK_CUDA(launch_combine(L.dx_slots, s->slot_row, s->header, mr, Is > 0 ? L.dx_s : nullptr, T, k, H, dx, sms,
-                          cs));
-  MOK_CUDA(launch_dw_reduce(L.dw_part, T * k, 2 * (I / bn1), d_router_w, cs));
-  MOK_CUDA(mark(cfg, MOK_STAGE_BWD_REDUCE, 1, cs));
-  return MOK_OK;
+  carve_bwd(ws, T, k, E, H, I, Is, ctx->mode, ring, &L);
+  std::vector<Win> wins;
+  if ((st = make_windows(s, ring, L.view, cs, &wins))) return st;
+  if (mxb) return backward_mxfp8(cfg, dy, x, router_w, s, wins, ctx, w, dx, d_router_w, g, L, sms, cs);
+  return backward_bf16(cfg, dy, x, router_w, s, wins, ctx, w, dx, d_router_w, g, L, sms, g4, cs);
 }
 
 mok_status_t mok_schedule_noalloc(const int64_t* top_experts, int T, int k, int E,

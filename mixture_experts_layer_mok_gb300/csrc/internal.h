@@ -37,10 +37,12 @@ cudaError_t launch_schedule(const int64_t* te, int T, int k, int E, int cap_tile
                             cudaStream_t st);
 cudaError_t launch_mx_quantize(const uint16_t* x, long long nblocks, uint8_t* codes, uint8_t* scales,
                                int num_sms, cudaStream_t st);
-// xb (may be NULL): also write x's bf16 rows in schedule order (padding rows zero).
+// Schedule rows [w0, w0 + wrows) go to rows from 0 of xp / xp_sc (and xb);
+// xq (may be NULL, then xq_sc is unused): the token-order copy; xb (may be
+// NULL): also x's bf16 rows in schedule order (padding rows zero).
 cudaError_t launch_mx_dispatch(const uint16_t* x, int T, int H, int topk, const int* slot_row, const int* row_src,
-                               const int* header, long long max_rows, uint8_t* xq, uint8_t* xq_sc, uint8_t* xp,
-                               uint8_t* xp_sc, uint16_t* xb, int num_sms, cudaStream_t st);
+                               const int* header, long long w0, long long wrows, uint8_t* xq, uint8_t* xq_sc,
+                               uint8_t* xp, uint8_t* xp_sc, uint16_t* xb, int num_sms, cudaStream_t st);
 cudaError_t launch_mx_quantize_t(const uint16_t* src, long long ld, int batch, int R, int C, int valid_rows,
                                  const int* row_src, int topk, const int* header, uint8_t* codes, uint8_t* scales,
                                  int tiled, int num_sms, cudaStream_t st, uint8_t* rcodes = nullptr,
@@ -65,8 +67,17 @@ constexpr int kMaxScaleJobs = 6;
 cudaError_t launch_mx_tile_scales(const MxTileScaleJob* jobs, int n, cudaStream_t st);
 cudaError_t launch_combine(const uint16_t* rows, const int* slot_row, const int* header, long long max_rows,
                            const uint16_t* base, int T, int k, int H, uint16_t* out, int num_sms, cudaStream_t st);
+// Token rows of src into schedule order: schedule rows [w0, w0 + wrows) go to
+// rows from 0 of out.
 cudaError_t launch_permute_rows(const uint16_t* src, int T, int H, int topk, const int* slot_row, const int* row_src,
-                                const int* header, long long max_rows, uint16_t* out, int num_sms, cudaStream_t st);
+                                const int* header, long long w0, long long wrows, uint16_t* out, int num_sms,
+                                cudaStream_t st);
+// The schedule restricted to experts [e0, e0 + ne) (a macrobatch window):
+// its tile list, pairs, row offsets (ne + 1) and header, rows counted from
+// row0[e0].
+cudaError_t launch_window_view(const int* cnt, const int* row0, const int* header, int e0, int ne, int* tile_expert,
+                               int* tile_row0, int* tile_rows, int* pair_tile, int* wrow0, int* wheader,
+                               cudaStream_t st);
 cudaError_t launch_dw_reduce(const float* part, int nf, int ntiles, float* dw, cudaStream_t st);
 
 // Grouped GEMM launch: instantiated for the operand sources / tile widths /

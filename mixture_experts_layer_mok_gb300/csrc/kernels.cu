@@ -87,6 +87,7 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int n, int E, int nchu
       header[1] = 0;
       header[3] = 0;
       header[4] = 0;
+      header[5] = cap_tiles;
     }
     return;
   }
@@ -194,6 +195,7 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int n, int E, int nchu
     header[1] = total_rows;
     header[3] = total_prim;
     header[4] = num_pairs;
+    header[5] = cap_tiles;
   }
 }
 
@@ -272,6 +274,83 @@ cudaError_t launch_schedule(const int64_t* te, int T, int k, int E, int cap_tile
 }
 
 // ===========================================================================
+// Macrobatch window view ("Mixture-of-Kittens: a deterministic MoE megakernel
+// for NVL72 racks", "Tuning the five hyperparameters before production":
+// macrobatch_size is the size of the token ring buffer).  The schedule
+// restricted to experts [e0, e0 + ne), with rows counted from the window's
+// first schedule row row0[e0]: its tile list in the schedule's own order
+// (primary tiles, at most cap_tiles of each expert, then the overflow list),
+// tile pairs, per-expert row offsets (ne + 1 entries) and header.  Tile
+// experts stay absolute (they index the weights).  One 1024-thread block, one
+// thread per expert of the window.
+// ===========================================================================
+__global__ void __launch_bounds__(1024) window_view_kernel(const int* __restrict__ cnt, const int* __restrict__ row0,
+                                                           const int* __restrict__ header, int e0, int ne,
+                                                           int* __restrict__ tile_expert, int* __restrict__ tile_row0,
+                                                           int* __restrict__ tile_rows, int* __restrict__ pair_tile,
+                                                           int* __restrict__ wrow0, int* __restrict__ wheader) {
+  griddep_wait();
+  griddep_launch_dependents();
+  __shared__ int tmp[32];
+  if (header[2] != 0) {   // no schedule: an empty view that carries the status
+    if (threadIdx.x < 8) wheader[threadIdx.x] = threadIdx.x == 2 ? header[2] : 0;
+    return;
+  }
+  const int i = threadIdx.x, e = e0 + i;
+  const int cap = header[5];
+  const int base = row0[e0];
+  const int c = i < ne ? cnt[e] : 0;
+  const int ntile = (c + kTileRows - 1) / kTileRows;
+  const int prim = min(ntile, cap);
+  int total_prim, total_ovf, total_pp, total_po;
+  const int prim_off = block_exclusive_scan(prim, tmp, &total_prim);
+  const int ovf_off = block_exclusive_scan(ntile - prim, tmp, &total_ovf);
+  const int pp = (prim + 1) / 2, po = (ntile - prim + 1) / 2;
+  const int pp_off = block_exclusive_scan(pp, tmp, &total_pp);
+  const int po_off = block_exclusive_scan(po, tmp, &total_po);
+  if (i < ne) {
+    const int r = row0[e] - base;
+    wrow0[i] = r;
+    for (int t = 0; t < ntile; ++t) {
+      const int idx = (t < prim) ? prim_off + t : total_prim + ovf_off + (t - prim);
+      tile_expert[idx] = e;
+      tile_row0[idx] = r + t * kTileRows;
+      tile_rows[idx] = min(kTileRows, c - t * kTileRows);
+    }
+    for (int j = 0; j < pp; ++j) {
+      pair_tile[2 * (pp_off + j)] = prim_off + 2 * j;
+      pair_tile[2 * (pp_off + j) + 1] = (2 * j + 1 < prim) ? prim_off + 2 * j + 1 : -1;
+    }
+    const int no = ntile - prim;
+    for (int j = 0; j < po; ++j) {
+      pair_tile[2 * (total_pp + po_off + j)] = total_prim + ovf_off + 2 * j;
+      pair_tile[2 * (total_pp + po_off + j) + 1] = (2 * j + 1 < no) ? total_prim + ovf_off + 2 * j + 1 : -1;
+    }
+  }
+  if (i == 0) {
+    const int rows = row0[e0 + ne] - base;
+    wrow0[ne] = rows;
+    wheader[0] = total_prim + total_ovf;
+    wheader[1] = rows;
+    wheader[2] = 0;
+    wheader[3] = total_prim;
+    wheader[4] = total_pp + total_po;
+    wheader[5] = cap;
+    wheader[6] = 0;
+    wheader[7] = 0;
+  }
+}
+
+cudaError_t launch_window_view(const int* cnt, const int* row0, const int* header, int e0, int ne, int* tile_expert,
+                               int* tile_row0, int* tile_rows, int* pair_tile, int* wrow0, int* wheader,
+                               cudaStream_t st) {
+  cudaError_t err = launch_dependent(window_view_kernel, dim3(1), dim3(1024), 0, st, cnt, row0, header, e0, ne,
+                                     tile_expert, tile_row0, tile_rows, pair_tile, wrow0, wheader);
+  if (err != cudaSuccess) return err;
+  return cudaGetLastError();
+}
+
+// ===========================================================================
 // MXFP8 quantiser ("Mixture-of-Kittens: a deterministic MoE megakernel for
 // NVL72 racks", "Tuning the five hyperparameters before production": MXFP8
 // weights are prequantised by a separate mxfp8_quantize).  One thread per
@@ -315,12 +394,17 @@ cudaError_t launch_mx_quantize(const uint16_t* x, long long nblocks, uint8_t* co
 // one GPU as a write into schedule order).  Scales go straight into the
 // tensor-core scale layout.  Padding rows of the schedule get zero codes and
 // unit scales; so do the scales of the token-order copy's last partial
-// 128-row block.  One warp per job: tokens, then schedule rows, then the tail.
+// 128-row block.  Only the schedule rows of the window [w0, w0 + wrows) are
+// written, at row p - w0 (the whole schedule is the window [0, max_rows); a
+// macrobatch ring passes one window of experts at a time), and the
+// token-order copy only when xq is not NULL.  One warp per job: tokens, then
+// the window's schedule rows, then the tail.
 // ===========================================================================
 __global__ void __launch_bounds__(256, 3) mx_dispatch_kernel(
     const uint16_t* __restrict__ x, int T, int H, int topk, const int* __restrict__ slot_row,
-    const int* __restrict__ row_src, const int* __restrict__ header, long long max_rows, uint8_t* __restrict__ xq,
-    uint8_t* __restrict__ xq_sc, uint8_t* __restrict__ xp, uint8_t* __restrict__ xp_sc, uint16_t* __restrict__ xb) {
+    const int* __restrict__ row_src, const int* __restrict__ header, long long w0, long long wrows,
+    uint8_t* __restrict__ xq, uint8_t* __restrict__ xq_sc, uint8_t* __restrict__ xp, uint8_t* __restrict__ xp_sc,
+    uint16_t* __restrict__ xb) {
   griddep_wait();
   griddep_launch_dependents();
   if (header[2] != 0) return;
@@ -336,7 +420,7 @@ __global__ void __launch_bounds__(256, 3) mx_dispatch_kernel(
   const int nb = H / 32;             // blocks per row (a multiple of 4)
   const int cg = H / 128;            // column groups of the scale layout
   const long long t_pad = (static_cast<long long>(T) + 127) / 128 * 128;
-  const long long jobs = T + max_rows + (t_pad - T);
+  const long long jobs = T + wrows + (xq ? t_pad - T : 0);
   for (long long j = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5; j < jobs;
        j += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
     if (j < T) {
@@ -344,6 +428,10 @@ __global__ void __launch_bounds__(256, 3) mx_dispatch_kernel(
       // schedule rows of this token's k copies, spread over the lanes
       const int p_lo = lane < topk ? __ldg(slot_row + t * topk + lane) : -1;
       const int p_hi = lane + 32 < topk ? __ldg(slot_row + t * topk + lane + 32) : -1;
+      // without the token-order copy, a token none of whose rows falls in the
+      // window is not read at all
+      if (!xq && !__any_sync(0xffffffffu, (p_lo >= w0 && p_lo - w0 < wrows) || (p_hi >= w0 && p_hi - w0 < wrows)))
+        continue;
       const uint16_t* xrow = x + t * H;
       // raw bf16 of this lane's block in the current chunk, the next chunk's
       // loaded while this one is quantised and stored
@@ -384,12 +472,15 @@ __global__ void __launch_bounds__(256, 3) mx_dispatch_kernel(
         const uint4 q1 = 16 * (lane + 32) < bytes ? reinterpret_cast<const uint4*>(wst)[lane + 32] : q0;
         __syncwarp();
         const long long off = static_cast<long long>(b0) * 32;
-        uint4* d = reinterpret_cast<uint4*>(xq + t * H + off);
-        if (16 * lane < bytes) d[lane] = q0;
-        if (16 * (lane + 32) < bytes) d[lane + 32] = q1;
-        if (act && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(xq_sc + mx_tiled_scale_offset(t, b, cg)) = word;
+        if (xq) {
+          uint4* d = reinterpret_cast<uint4*>(xq + t * H + off);
+          if (16 * lane < bytes) d[lane] = q0;
+          if (16 * (lane + 32) < bytes) d[lane + 32] = q1;
+          if (act && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(xq_sc + mx_tiled_scale_offset(t, b, cg)) = word;
+        }
         for (int jj = 0; jj < topk; ++jj) {   // all lanes take part in the shuffle
-          const int pr = __shfl_sync(0xffffffffu, jj < 32 ? p_lo : p_hi, jj & 31);
+          const long long pr = __shfl_sync(0xffffffffu, jj < 32 ? p_lo : p_hi, jj & 31) - w0;
+          if (pr < 0 || pr >= wrows) continue;   // the same for every lane
           uint4* dp = reinterpret_cast<uint4*>(xp + static_cast<long long>(pr) * H + off);
           if (16 * lane < bytes) dp[lane] = q0;
           if (16 * (lane + 32) < bytes) dp[lane + 32] = q1;
@@ -406,9 +497,9 @@ __global__ void __launch_bounds__(256, 3) mx_dispatch_kernel(
         }
         __syncwarp();   // the staging is read before the next chunk overwrites it
       }
-    } else if (j < T + max_rows) {
+    } else if (j < T + wrows) {
       const long long pr = j - T;
-      if (pr >= P || __ldg(row_src + pr) >= 0) continue;
+      if (w0 + pr >= P || __ldg(row_src + w0 + pr) >= 0) continue;
       uint4* d = reinterpret_cast<uint4*>(xp + pr * H);
       for (int i = lane; i < H / 16; i += 32) d[i] = make_uint4(0, 0, 0, 0);
       if (xb) {
@@ -418,7 +509,7 @@ __global__ void __launch_bounds__(256, 3) mx_dispatch_kernel(
       for (int g = lane; g < cg; g += 32)
         *reinterpret_cast<uint32_t*>(xp_sc + mx_tiled_scale_offset(pr, 4 * g, cg)) = 0x7F7F7F7Fu;
     } else {
-      const long long tr = T + (j - T - max_rows);
+      const long long tr = T + (j - T - wrows);
       for (int g = lane; g < cg; g += 32)
         *reinterpret_cast<uint32_t*>(xq_sc + mx_tiled_scale_offset(tr, 4 * g, cg)) = 0x7F7F7F7Fu;
     }
@@ -426,11 +517,11 @@ __global__ void __launch_bounds__(256, 3) mx_dispatch_kernel(
 }
 
 cudaError_t launch_mx_dispatch(const uint16_t* x, int T, int H, int topk, const int* slot_row, const int* row_src,
-                               const int* header, long long max_rows, uint8_t* xq, uint8_t* xq_sc, uint8_t* xp,
-                               uint8_t* xp_sc, uint16_t* xb, int num_sms, cudaStream_t st) {
-  const long long jobs = T + max_rows + ((static_cast<long long>(T) + 127) / 128 * 128 - T);
+                               const int* header, long long w0, long long wrows, uint8_t* xq, uint8_t* xq_sc,
+                               uint8_t* xp, uint8_t* xp_sc, uint16_t* xb, int num_sms, cudaStream_t st) {
+  const long long jobs = T + wrows + (xq ? (static_cast<long long>(T) + 127) / 128 * 128 - T : 0);
   cudaError_t err = launch_dependent(mx_dispatch_kernel, dim3(grid_for(jobs * 32, 256, num_sms)), dim3(256), 0, st, x,
-                                     T, H, topk, slot_row, row_src, header, max_rows, xq, xq_sc, xp, xp_sc, xb);
+                                     T, H, topk, slot_row, row_src, header, w0, wrows, xq, xq_sc, xp, xp_sc, xb);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
@@ -750,32 +841,37 @@ cudaError_t launch_combine(const uint16_t* rows, const int* slot_row, const int*
 }
 
 // ===========================================================================
-// Dispatch permutation: out[p] = src[row_src[p] / k] for every schedule row
-// p < P (zeros for padding rows), so the routed GEMMs read their gathered
-// operand as dense TMA tiles.  Token-major: one warp per token reads its row
-// once and writes it to the token's k schedule rows (slot_row), four 16-byte
-// pieces per lane in flight, each store instruction 512 contiguous bytes; then
-// one warp per padding row writes zeros.  Bandwidth bound: T*H*2 bytes read,
-// P*H*2 written (a row-major walk over schedule rows would read each token row
+// Dispatch permutation: out[p - w0] = src[row_src[p] / k] for every schedule
+// row p of the window [w0, w0 + wrows) below P (zeros for padding rows), so
+// the routed GEMMs read their gathered operand as dense TMA tiles.  The whole
+// schedule is the window [0, max_rows); a macrobatch ring passes the rows of
+// one window of experts.  Token-major: one warp per token reads its row once
+// and writes it to those of the token's k schedule rows (slot_row) that fall
+// in the window, four 16-byte pieces per lane in flight, each store
+// instruction 512 contiguous bytes; then one warp per padding row of the
+// window writes zeros.  Bandwidth bound: T*H*2 bytes read, the window's rows
+// *H*2 written (a row-major walk over schedule rows would read each token row
 // k times).
 // ===========================================================================
 __global__ void __launch_bounds__(256) permute_rows_kernel(const uint16_t* __restrict__ src, int T, int H, int topk,
                                                            const int* __restrict__ slot_row,
                                                            const int* __restrict__ row_src,
-                                                           const int* __restrict__ header, long long max_rows,
-                                                           uint16_t* __restrict__ out) {
+                                                           const int* __restrict__ header, long long w0,
+                                                           long long wrows, uint16_t* __restrict__ out) {
   griddep_wait();
   griddep_launch_dependents();
   if (header[2] != 0) return;
   const long long P = header[1];
   const int lane = threadIdx.x & 31;
   const int per_row = H / 8;  // 16-byte pieces per row
-  const long long jobs = T + max_rows;
+  const long long jobs = T + wrows;
   for (long long j = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5; j < jobs;
        j += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
     if (j < T) {
       const int p_lo = lane < topk ? __ldg(slot_row + j * topk + lane) : -1;
       const int p_hi = lane + 32 < topk ? __ldg(slot_row + j * topk + lane + 32) : -1;
+      // a token none of whose rows falls in the window is not read at all
+      if (!__any_sync(0xffffffffu, (p_lo >= w0 && p_lo - w0 < wrows) || (p_hi >= w0 && p_hi - w0 < wrows))) continue;
       const uint4* s = reinterpret_cast<const uint4*>(src + j * H);
       for (int i0 = 0; i0 < per_row; i0 += 128) {
         uint4 v[4];
@@ -783,7 +879,8 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(const uint16_t* __res
         for (int q = 0; q < 4; ++q)
           if (i0 + lane + 32 * q < per_row) v[q] = __ldg(s + i0 + lane + 32 * q);
         for (int jj = 0; jj < topk; ++jj) {   // all lanes take part in the shuffle
-          const long long pr = __shfl_sync(0xffffffffu, jj < 32 ? p_lo : p_hi, jj & 31);
+          const long long pr = __shfl_sync(0xffffffffu, jj < 32 ? p_lo : p_hi, jj & 31) - w0;
+          if (pr < 0 || pr >= wrows) continue;   // the same for every lane
           uint4* d = reinterpret_cast<uint4*>(out + pr * H);
 #pragma unroll
           for (int q = 0; q < 4; ++q)
@@ -792,7 +889,7 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(const uint16_t* __res
       }
     } else {
       const long long pr = j - T;
-      if (pr >= P || __ldg(row_src + pr) >= 0) continue;
+      if (w0 + pr >= P || __ldg(row_src + w0 + pr) >= 0) continue;
       uint4* d = reinterpret_cast<uint4*>(out + pr * H);
       for (int i = lane; i < per_row; i += 32) d[i] = make_uint4(0, 0, 0, 0);
     }
@@ -800,10 +897,11 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(const uint16_t* __res
 }
 
 cudaError_t launch_permute_rows(const uint16_t* src, int T, int H, int topk, const int* slot_row, const int* row_src,
-                                const int* header, long long max_rows, uint16_t* out, int num_sms, cudaStream_t st) {
-  if (max_rows == 0) return cudaSuccess;
-  cudaError_t err = launch_dependent(permute_rows_kernel, dim3(grid_for((T + max_rows) * 32, 256, num_sms)), dim3(256),
-                                     0, st, src, T, H, topk, slot_row, row_src, header, max_rows, out);
+                                const int* header, long long w0, long long wrows, uint16_t* out, int num_sms,
+                                cudaStream_t st) {
+  if (wrows == 0) return cudaSuccess;
+  cudaError_t err = launch_dependent(permute_rows_kernel, dim3(grid_for((T + wrows) * 32, 256, num_sms)), dim3(256),
+                                     0, st, src, T, H, topk, slot_row, row_src, header, w0, wrows, out);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }

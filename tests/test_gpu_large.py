@@ -132,3 +132,37 @@ def test_large_T65536_full_size_mxfp8_full():
     """The large layer with MXFP8 forward and backward: 12 tokens, slices of the
     hottest and coldest experts' and the shared expert's weight gradients."""
     _large("mxfp8_full", 12, 3)
+
+
+def test_large_T65536_ring_matches_single_pass_bitwise():
+    """The large layer (MXFP8 forward / BF16 backward, the benchmark's default)
+    with a 131072-row macrobatch ring in the forward and the backward: every
+    bit of y, dx, the router-weight gradient and the six weight gradients
+    equals the single pass (whose parity the tests above check), while the
+    ring bounds the schedule-order scratch."""
+    from tests.gpu_util import mok, weights_of
+
+    _need_bytes(150 << 30)
+    m = mok()
+    inp = gen.make_workload("large_T65536", seed=0, device="cuda")
+    w = weights_of(inp, "mxfp8")
+    E, mb = inp.meta["E"], 131072
+    sched = m.schedule(inp.top_experts, E, 0.5)
+    out = []
+    for ring in (0, mb):
+        y, ctx = m.forward(inp.x, inp.router_w, sched, w, mode="mxfp8", minibatch=4096, macrobatch=ring)
+        grads = m.backward(inp.dy, inp.x, inp.router_w, sched, ctx, w, minibatch=4096, macrobatch=ring)
+        torch.cuda.synchronize()
+        assert ctx.status() == 0
+        out.append((y, grads))
+        del ctx
+        torch.cuda.empty_cache()
+    for key in out[0][1]:
+        assert torch.equal(out[0][1][key], out[1][1][key]), key
+    assert torch.equal(out[0][0], out[1][0])
+    assert len(m.macrobatch_plan(sched.arrays()["cnt"].cpu().tolist(), mb)) >= 4
+    dims = (inp.meta["T"], inp.meta["k"], E, inp.meta["H"], inp.meta["I"], inp.meta["I_s"], 1)
+    lib = m._lib.load()
+    full = lib.mok_ctx_bytes(*dims) + lib.mok_bwd_workspace_bytes(*dims)
+    ringed = lib.mok_ctx_bytes_ring(*dims, mb) + lib.mok_bwd_workspace_bytes_ring(*dims, mb)
+    assert ringed < 0.6 * full

@@ -5,6 +5,7 @@ import ctypes as C
 import os
 import re
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -57,12 +58,14 @@ def test_buffer_sizes(lib):
     assert mb >= 2 * (mt * 128 * 2 * I + T * k * H + T * 2 * Is + T * H) + codes + codes // 32
     wb = lib.mok_bwd_workspace_bytes(T, k, E, H, I, Is, 0)
     assert wb >= 2 * (mt * 128 * 3 * I + T * k * H)
-    assert lib.mok_bwd_workspace_bytes(T, k, E, H, I, Is, 1) == wb
-    # MXFP8 backward: the bf16 dx rows, and E4M3 codes of dy (rows and
-    # transposed), x (transposed), dG|dU (rows and transposed) and w h
-    # (transposed) in place of the bf16 permuted copies and SwiGLU-backward rows
+    # after an MXFP8 forward the context holds x's schedule-order rows: no copy
+    assert 0 <= wb - lib.mok_bwd_workspace_bytes(T, k, E, H, I, Is, 1) - 2 * mt * 128 * H < 256
+    # MXFP8 backward: E4M3 codes of dy (rows and transposed), x (transposed),
+    # dG|dU (rows and transposed) and w h (transposed) in place of the bf16
+    # permuted copies and SwiGLU-backward rows (the dx rows in schedule order
+    # go to the context's slots)
     wm = lib.mok_bwd_workspace_bytes(T, k, E, H, I, Is, 2)
-    assert wm >= 2 * mt * 128 * H + mt * 128 * (3 * H + 5 * I)
+    assert wm >= mt * 128 * (3 * H + 5 * I)
     assert wm < wb
     assert lib.mok_bwd_workspace_bytes(T, k, E, H, I, Is, 3) == 0
     # shapes outside the contract report 0
@@ -266,3 +269,70 @@ def test_schedule_calls_take_the_multiplier_as_double(tmp_path):
                     str(tmp_path / "sig.o")], check=True, capture_output=True)
     for name in ("mok_schedule", "mok_schedule_noalloc"):
         assert _lib.SIGNATURES[name][1][4] is C.c_double, name
+
+
+def _plan(lib, cnt, mb):
+    import ctypes as C
+
+    E = len(cnt)
+    first = (C.c_int32 * (E + 1))()
+    nw = C.c_int()
+    rc = lib.mok_macrobatch_plan((C.c_int32 * E)(*cnt), E, mb, first, C.byref(nw))
+    return rc, [first[i] for i in range(nw.value + 1)] if rc == 0 else None
+
+
+def test_macrobatch_plan_is_the_greedy_split_of_whole_experts(lib):
+    """The windows of a ring of mb rows: consecutive runs of whole experts
+    covering 0..E in order, each run's 128-padded rows within the ring, and
+    each run maximal (the next expert would not fit); an expert that alone
+    exceeds the ring is MOK_ERR_CAPACITY.  Together these fix the split."""
+    rng = np.random.default_rng(0)
+    for trial in range(300):
+        E = int(rng.integers(1, 40))
+        cnt = rng.integers(0, 700, E) * (rng.random(E) < 0.8)
+        mb = int(rng.integers(1, 3000))
+        ring = -(-mb // 128) * 128
+        padded = -(-cnt // 128) * 128
+        rc, first = _plan(lib, [int(c) for c in cnt], mb)
+        if padded.max() > ring:
+            assert rc == 3, (cnt, mb)
+            continue
+        assert rc == 0
+        assert first[0] == 0 and first[-1] == E and all(a < b for a, b in zip(first, first[1:]))
+        for w in range(len(first) - 1):
+            rows = padded[first[w]:first[w + 1]].sum()
+            assert rows <= ring
+            if first[w + 1] < E:
+                assert rows + padded[first[w + 1]] > ring
+    # no ring: one window; a ring that holds everything: one window
+    assert _plan(lib, [5, 0, 300], 0)[1] == [0, 3]
+    assert _plan(lib, [5, 0, 300], 10 ** 9)[1] == [0, 3]
+    # one tile per window: every expert with rows starts a window, empty
+    # experts ride along
+    assert _plan(lib, [0, 3, 0, 128, 1, 0], 1)[1] == [0, 3, 4, 6]
+    assert _plan(lib, [129], 128)[0] == 3
+    assert _plan(lib, [-1], 128)[0] == 1
+    assert _plan(lib, [1], -1)[0] == 1
+
+
+def test_ring_buffer_sizes(lib):
+    """The schedule-order scratch shrinks with the ring; 0, or a ring that holds
+    every row, is the one-pass size; what stays full size (the saved gate|up
+    rows, the slots, the router-weight partials) bounds it from below."""
+    T, k, E, H, I, Is = 4096, 8, 64, 2048, 1024, 2048
+    mt = (T * k + 127 * E) // 128
+    for mode in (0, 1, 2):
+        dims = (T, k, E, H, I, Is, mode)
+        c0, w0 = lib.mok_ctx_bytes(*dims), lib.mok_bwd_workspace_bytes(*dims)
+        assert lib.mok_ctx_bytes_ring(*dims, 0) == c0 and lib.mok_bwd_workspace_bytes_ring(*dims, 0) == w0
+        assert lib.mok_ctx_bytes_ring(*dims, mt * 128) == c0
+        assert lib.mok_bwd_workspace_bytes_ring(*dims, mt * 128 + 5) == w0
+        prev = None
+        for mb in (128, 1024, 4096, 16384):
+            c, w = lib.mok_ctx_bytes_ring(*dims, mb), lib.mok_bwd_workspace_bytes_ring(*dims, mb)
+            assert c < c0 and (w < w0 or mode == 1 and mb >= 16384)
+            assert c >= 2 * mt * 128 * (2 * I + H)      # gate|up and the slots stay full size
+            if prev:
+                assert c >= prev[0] and w >= prev[1]
+            prev = (c, w)
+        assert lib.mok_ctx_bytes_ring(*dims, -1) == 0 and lib.mok_bwd_workspace_bytes_ring(*dims, -1) == 0
