@@ -95,6 +95,7 @@ def launches_per_step(c, windows=1, ring=False):
     shared = c["I_s"] > 0
     W = windows
     n = 3                                   # schedule: count, scan, scatter
+    n += 1 if -(-c["T"] * c["k"] // 1024) > 64 else 0   # and per-expert chunk offsets (large schedules)
     n += 2 * W if W > 1 else 0              # window views, forward and backward
     n += 1 + 2 * W + 1                      # status hand-over, routed gate/up + down, combine
     if shared:

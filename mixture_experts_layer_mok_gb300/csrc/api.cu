@@ -503,6 +503,14 @@ struct Win {
   long long r0, rows;
 };
 
+// GEMM parameters over a window's schedule view: its row0 and cnt start at the
+// window's first expert.
+GemmParams win_params(const mok_config_t* cfg, const Win& v, int* status, int debug) {
+  GemmParams p = base_params(cfg, &v.s, status, debug);
+  p.e_base = v.e0;
+  return p;
+}
+
 // The windows of a call.  Without a ring: one window over the whole schedule
 // (nothing is read back).  With one: the expert counts and the header are
 // read back (synchronising cs), the windows planned, and each window's view
@@ -803,7 +811,7 @@ mok_status_t forward_bf16(const mok_config_t* cfg, const uint16_t* x, const floa
         (st = make_map(&m.b1, w->w_up, H, static_cast<uint64_t>(E) * I, 128, bk)) ||
         (st = make_map_out(&m.o0, gu, 2ull * I, v.rows)) || (st = make_map_out(&m.o1, ctx->h, I, v.rows)))
       return st;
-    GemmParams p = base_params(cfg, &v.s, ctx->status, cfg->debug_flags);
+    GemmParams p = win_params(cfg, v, ctx->status, cfg->debug_flags);
     p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / 128; p.b_rows_per_expert = I;
     p.out0 = gu; p.out1 = ctx->h; p.ga = x; p.ga_ld = H;
     p.swiglu_limit = cfg->swiglu_limit;
@@ -826,7 +834,7 @@ mok_status_t forward_bf16(const mok_config_t* cfg, const uint16_t* x, const floa
         (st = make_map_out(&m2.o0, slots, H, v.rows)))
       return st;
     m2.b1 = m2.b0;
-    GemmParams q = base_params(cfg, &v.s, ctx->status, 0);
+    GemmParams q = win_params(cfg, v, ctx->status, 0);
     q.grouped = 1; q.K = I; q.N = H; q.n_tiles = H / bn; q.b_rows_per_expert = H;
     q.out0 = slots; q.ld = H; q.rw = router_w;
     const long long items2 = static_cast<long long>(v.s.max_tiles) * q.n_tiles;
@@ -988,7 +996,7 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
         (st = gu_sf_maps(m, X.wg_sc, X.wu_sc, static_cast<long long>(E) * I)) ||
         (st = make_map_out(&m.o0, gu, 2ull * I, v.rows)) || (st = make_map_codes_out(&m.o1, ctx->hq, I, v.rows)))
       return st;
-    GemmParams p = base_params(cfg, &v.s, ctx->status, cfg->debug_flags);
+    GemmParams p = win_params(cfg, v, ctx->status, cfg->debug_flags);
     p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / gu_cols; p.b_rows_per_expert = I;
     p.out0 = gu; p.out1 = ctx->hq; p.sf_out = ctx->hq_sc;
     p.swiglu_limit = cfg->swiglu_limit;
@@ -1007,7 +1015,7 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
       return st;
     m2.b1 = m2.b0;
     m2.sfb1 = m2.sfb0;
-    GemmParams q = base_params(cfg, &v.s, ctx->status, 0);
+    GemmParams q = win_params(cfg, v, ctx->status, 0);
     q.grouped = 1; q.K = I; q.N = H; q.n_tiles = H / dn_bn; q.b_rows_per_expert = H;
     q.out0 = slots; q.ld = H; q.rw = router_w;
     q.sfa = ctx->hq_sc; q.sfb0 = X.wd_sc;
@@ -1184,7 +1192,7 @@ mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const u
           (st = make_map_codes_out(&m.o2, L.hwT, v.rows, I)))
         return st;
       m.b1 = m.b0;
-      GemmParams p = base_params(cfg, &v.s, ctx->status, 0);
+      GemmParams p = win_params(cfg, v, ctx->status, 0);
       p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / 128; p.b_rows_per_expert = I;
       p.aux0 = ctx->gu + v.r0 * 2 * I; p.rw = router_w; p.dw_part = L.dw_part; p.swiglu_limit = ctx->swiglu_limit;
       p.sf_out = L.dguq_sc; p.out2 = L.dguT_sc; p.sf_out2 = L.hwT_sc; p.ld = v.rows;   // codes: maps o0..o2
@@ -1201,7 +1209,7 @@ mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const u
       if ((st = make_map_u8(&m.a, L.dyT, v.rows, H, 128)) || (st = make_map_u8(&m.b0, L.hwT, v.rows, I, bn)))
         return st;
       m.b1 = m.b0;
-      GemmParams p = base_params(cfg, &v.s, ctx->status, 0);
+      GemmParams p = win_params(cfg, v, ctx->status, 0);
       p.wgrad = 1; p.grouped = 1; p.K = rows; p.E = v.ne; p.m_tiles = H / 128; p.n_tiles = I / bn;
       p.out0 = out; p.out1 = out; p.ld = I; p.split = H;
       p.sfa = L.dyT_sc; p.sfb0 = L.hwT_sc;
@@ -1214,7 +1222,7 @@ mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const u
       if ((st = make_map_u8(&m.a, L.dguT, v.rows, 2ull * I, 128)) || (st = make_map_u8(&m.b0, L.xT, v.rows, H, bnH)))
         return st;
       m.b1 = m.b0;
-      GemmParams p = base_params(cfg, &v.s, ctx->status, 0);
+      GemmParams p = win_params(cfg, v, ctx->status, 0);
       p.wgrad = 1; p.grouped = 1; p.K = rows; p.E = v.ne; p.m_tiles = 2 * I / 128; p.n_tiles = H / bnH;
       p.out0 = g->d_w_gate + static_cast<long long>(v.e0) * I * H;
       p.out1 = g->d_w_up + static_cast<long long>(v.e0) * I * H;
@@ -1232,7 +1240,7 @@ mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const u
           (st = make_map_u8(&m.b1, w->mxt_up, I, static_cast<uint64_t>(E) * H, bnH)) ||
           (st = make_map_out(&m.o0, out, H, v.rows)))
         return st;
-      GemmParams p = base_params(cfg, &v.s, ctx->status, 0);
+      GemmParams p = win_params(cfg, v, ctx->status, 0);
       p.grouped = 1; p.K = 2 * I; p.N = H; p.n_tiles = H / bnH; p.b_rows_per_expert = H; p.b_split = I;
       p.out0 = out; p.ld = H;
       p.sfa = L.dguq_sc; p.sfb0 = L.wtg_sc; p.sfb1 = L.wtu_sc; p.sf_kgb = I / 128;
@@ -1370,7 +1378,7 @@ mok_status_t backward_bf16(const mok_config_t* cfg, const uint16_t* dy, const ui
           (st = make_map_out(&m.o0, L.dgu, 2ull * I, v.rows)) || (st = make_map_out(&m.o1, L.hw, I, v.rows)))
         return st;
       m.b1 = m.b0;
-      GemmParams p = base_params(cfg, &v.s, ctx->status, 0);
+      GemmParams p = win_params(cfg, v, ctx->status, 0);
       p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / bn1; p.b_rows_per_expert = H;
       p.aux0 = ctx->gu + v.r0 * 2 * I; p.out0 = L.dgu; p.out1 = L.hw; p.rw = router_w; p.dw_part = L.dw_part;
       p.swiglu_limit = ctx->swiglu_limit;
@@ -1404,7 +1412,7 @@ mok_status_t backward_bf16(const mok_config_t* cfg, const uint16_t* dy, const ui
         return st;
       m.o1 = m.o0;
       m.b1 = m.b0;
-      GemmParams p = base_params(cfg, &v.s, ctx->status, 0);
+      GemmParams p = win_params(cfg, v, ctx->status, 0);
       p.wgrad = 1; p.grouped = 1; p.E = v.ne; p.m_tiles = H / 128; p.n_tiles = I / bn;
       p.out0 = out; p.out1 = out; p.ld = I; p.split = H;
       p.estride = static_cast<long long>(H) * I;
@@ -1441,7 +1449,7 @@ mok_status_t backward_bf16(const mok_config_t* cfg, const uint16_t* dy, const ui
           (st = make_map_out(&m.o1, out_u, H, static_cast<uint64_t>(v.ne) * I)))
         return st;
       m.b1 = m.b0;
-      GemmParams p = base_params(cfg, &v.s, ctx->status, 0);
+      GemmParams p = win_params(cfg, v, ctx->status, 0);
       p.wgrad = 1; p.grouped = 1; p.E = v.ne; p.m_tiles = 2 * I / 128; p.n_tiles = H / bn;
       p.out0 = out_g; p.out1 = out_u; p.ld = H; p.split = I;
       p.estride = static_cast<long long>(I) * H;
@@ -1475,7 +1483,7 @@ mok_status_t backward_bf16(const mok_config_t* cfg, const uint16_t* dy, const ui
           (st = make_map_mn(&m.b1, w->w_up, H, static_cast<uint64_t>(E) * I, bw, kTileBK)) ||
           (st = make_map_out(&m.o0, out, H, v.rows)))
         return st;
-      GemmParams p = base_params(cfg, &v.s, ctx->status, 0);
+      GemmParams p = win_params(cfg, v, ctx->status, 0);
       p.grouped = 1; p.K = 2 * I; p.N = H; p.n_tiles = H / bn; p.b_rows_per_expert = I; p.b_split = I;
       p.out0 = out; p.ld = H;
       const long long items = static_cast<long long>(v.s.max_tiles) * p.n_tiles;

@@ -123,22 +123,26 @@ struct GemmParams {
   // ---- order of the work items (never changes a result: each output tile has
   // one owner and a fixed K order)
   int group;         // row GEMMs: 0 = column tiles inside each row unit (tile or pair);
-                     // g > 0 = row units in groups of g, the group's units inside
-                     // each column tile (B's columns stream once per group while
-                     // the group's A rows stay in L2)
+                     // g > 0 = row units in groups of at most g, the group's units
+                     // inside each column tile (B's columns stream once per group
+                     // while the group's A rows stay in L2); a grouped GEMM whose
+                     // tiles are all primary cuts its groups at expert boundaries
+  int e_base;        // grouped: first expert of row0 / cnt (a macrobatch window's view)
   int wg_col_outer;  // weight gradients: 1 = an expert's row units inside each
                      // column tile (B streams once, A stays in L2), 0 = the reverse
 };
 
 // Default work-item order, chosen at launch where p.group / p.wg_col_outer
 // are -1 (-2: the plain order).  Row GEMMs take their row units (tiles, or
-// pairs of tiles) in groups of 16 row tiles inside each column tile: while
-// the group's A rows stay in L2, each B column slice (an expert's weights, a
-// few MB) is read once for the whole group instead of once per row unit.
-// Weight gradients walk an expert's row units inside each column tile when A
-// (M rows per expert) is the smaller operand, so that B streams through once.
+// pairs of tiles) in groups inside each column tile: while the group's A rows
+// stay in L2, each B column slice (an expert's weights, a few MB) is read once
+// for the whole group instead of once per row unit.  Dense GEMMs group 16 row
+// tiles; grouped ones up to 32 tiles of one expert (an expert of more is split
+// into even groups), so that no group holds two experts' weights.  Weight
+// gradients walk an expert's row units inside each column tile when A (M rows
+// per expert) is the smaller operand, so that B streams through once.
 inline void resolve_item_order(GemmParams& p, bool pair) {
-  if (p.group < 0) p.group = (p.group == -2) ? 0 : (pair ? 8 : 16);
+  if (p.group < 0) p.group = (p.group == -2) ? 0 : (p.grouped ? (pair ? 16 : 32) : (pair ? 8 : 16));
   if (p.wg_col_outer < 0)
     p.wg_col_outer = (p.wg_col_outer == -2) ? 0 : (p.wgrad && static_cast<long long>(p.m_tiles) * kBM < p.ld ? 1 : 0);
 }
@@ -157,6 +161,29 @@ __device__ __forceinline__ void unit_and_col(int idx, int units, int n_tiles, in
   const int gs = min(group, units - g * group);   // the last group may be short
   nt = r / gs;
   u = g * group + (r - nt * gs);
+}
+
+// The same for a grouped GEMM whose tiles are all in the primary list (each
+// expert's row units consecutive, in expert order, unit j of expert e covering
+// its rows [j U, (j + 1) U) with U = 128 for tiles, 256 for pairs): the groups
+// are an expert's units, split evenly into ceil(units / cap) groups when it
+// has more than cap.  The items of a group of units [s, s + L) are [s n, (s +
+// L) n), so the unit idx / n lies in idx's group.
+__device__ __forceinline__ void expert_unit_and_col(const GemmParams& p, int idx, bool pairs, int& u, int& nt) {
+  const int n = p.n_tiles;
+  const int u0 = idx / n;
+  const int t0 = pairs ? __ldg(p.pair_tile + 2 * u0) : u0;
+  const int e = __ldg(p.tile_expert + t0) - p.e_base;
+  const int shift = pairs ? 8 : 7;
+  const int j = (__ldg(p.tile_row0 + t0) - __ldg(p.row0 + e)) >> shift;
+  const int nu = (__ldg(p.cnt + e) + (1 << shift) - 1) >> shift;
+  const int ng = (nu + p.group - 1) / p.group;
+  const int gsz = (nu + ng - 1) / ng;
+  const int gj = j / gsz * gsz;
+  const int gl = min(gsz, nu - gj);
+  const int r = idx - (u0 - j + gj) * n;
+  nt = r / gl;
+  u = u0 - j + gj + (r - nt * gl);
 }
 
 struct Item {
@@ -178,7 +205,10 @@ __device__ __forceinline__ Item get_item(const GemmParams& p, int idx, int bk) {
   it.empty = false;
   if (!p.wgrad) {
     int mt;
-    unit_and_col(idx, p.grouped ? p.header[0] : (p.rows + kBM - 1) / kBM, p.n_tiles, p.group, mt, it.nt);
+    if (p.grouped && p.group > 0 && p.header[3] == p.header[0])
+      expert_unit_and_col(p, idx, false, mt, it.nt);
+    else
+      unit_and_col(idx, p.grouped ? p.header[0] : (p.rows + kBM - 1) / kBM, p.n_tiles, p.group, mt, it.nt);
     if (p.grouped) {
       it.e = __ldg(p.tile_expert + mt);
       it.p0 = __ldg(p.tile_row0 + mt);
@@ -229,7 +259,10 @@ __device__ __forceinline__ Item get_item_pair(const GemmParams& p, int idx, int 
   it.empty = false;
   if (!p.wgrad) {
     int pr;
-    unit_and_col(idx, p.grouped ? p.header[4] : ((p.rows + kBM - 1) / kBM + 1) / 2, p.n_tiles, p.group, pr, it.nt);
+    if (p.grouped && p.group > 0 && p.header[3] == p.header[0])
+      expert_unit_and_col(p, idx, true, pr, it.nt);
+    else
+      unit_and_col(idx, p.grouped ? p.header[4] : ((p.rows + kBM - 1) / kBM + 1) / 2, p.n_tiles, p.group, pr, it.nt);
     if (p.grouped) {
       const int t0 = __ldg(p.pair_tile + 2 * pr);
       const int t1 = __ldg(p.pair_tile + 2 * pr + 1);

@@ -16,6 +16,8 @@ namespace mok {
 // materialised into a dispatch/combine plan before any compute kernel runs).
 // Three launches: per-chunk histograms; one block scans them into per-expert
 // counts, padded row offsets and the tile list; per-chunk stable scatter.
+// Above kPrefixChunks chunks a fourth launch, one block per expert, turns the
+// histograms into per-expert chunk offsets first.
 // ===========================================================================
 
 __global__ void sched_count_kernel(const int64_t* __restrict__ te, int n, int E,
@@ -67,6 +69,34 @@ __device__ int block_exclusive_scan(int v, int* tmp /* >= 32 ints */, int* total
   return before + x - v;
 }
 
+// Large schedules: the per-expert chunk offsets, one block per expert.  Column
+// e of hist [nchunks][E] becomes each chunk's exclusive offset within expert
+// e, and cnt[e] its total; each thread takes a run of consecutive chunks.
+__global__ void __launch_bounds__(256) sched_prefix_kernel(int E, int nchunks, int* __restrict__ hist,
+                                                           int* __restrict__ cnt, const int* __restrict__ header) {
+  griddep_wait();
+  griddep_launch_dependents();
+  __shared__ int tmp[32];
+  if (header[2] != 0) return;
+  const int e = blockIdx.x;
+  const int per = (nchunks + blockDim.x - 1) / blockDim.x;
+  const int k0 = min(nchunks, static_cast<int>(threadIdx.x) * per), k1 = min(nchunks, k0 + per);
+  int sum = 0;
+  for (int k = k0; k < k1; ++k) sum += hist[static_cast<long long>(k) * E + e];
+  int total;
+  int run = block_exclusive_scan(sum, tmp, &total);
+  for (int k = k0; k < k1; ++k) {
+    const long long i = static_cast<long long>(k) * E + e;
+    const int v = hist[i];
+    hist[i] = run;
+    run += v;
+  }
+  if (threadIdx.x == 0) cnt[e] = total;
+}
+
+// Chunk counts above which the per-expert offsets get their own launch.
+constexpr int kPrefixChunks = 64;
+
 __global__ void __launch_bounds__(1024) sched_scan_kernel(int n, int E, int nchunks, int cap_tiles,
                                                           int max_tiles, int* __restrict__ hist,
                                                           int* __restrict__ cnt, int* __restrict__ row0,
@@ -91,11 +121,13 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int n, int E, int nchu
     }
     return;
   }
-  // each chunk's count becomes its exclusive offset within its expert.  The
+  // each chunk's count becomes its exclusive offset within its expert (done
+  // already by sched_prefix_kernel for more than kPrefixChunks chunks).  The
   // chunks are split over `tpe` threads per expert (all 1024 threads when E
   // is small): each sums its run of chunks, the runs' sums are scanned in
   // shared memory, and each thread rewrites its run from its base, sixteen
   // loads in flight per round.
+  const bool prefixed = nchunks > kPrefixChunks;
   __shared__ int part[1024];
   int tpe = 1;
   while (tpe * 2 * E <= 1024) tpe *= 2;
@@ -103,7 +135,7 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int n, int E, int nchu
   const int per = (nchunks + tpe - 1) / tpe;
   const int k0 = min(nchunks, sub * per), k1 = min(nchunks, k0 + per);
   int sum = 0;
-  if (ee < E) {
+  if (ee < E && !prefixed) {
     int k = k0;
     for (; k + 16 <= k1; k += 16) {
       int v[16];
@@ -116,7 +148,7 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int n, int E, int nchu
   }
   part[threadIdx.x] = sum;
   __syncthreads();
-  if (ee < E) {
+  if (ee < E && !prefixed) {
     int run = 0;
     for (int q = 0; q < sub; ++q) run += part[ee * tpe + q];
     int k = k0;
@@ -138,7 +170,9 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int n, int E, int nchu
   }
   __syncthreads();
   int c = 0;
-  if (e < E) {
+  if (e < E && prefixed) {
+    c = cnt[e];
+  } else if (e < E) {
     for (int q = 0; q < tpe; ++q) c += part[e * tpe + q];
     cnt[e] = c;
   }
@@ -257,6 +291,11 @@ cudaError_t launch_schedule(const int64_t* te, int T, int k, int E, int cap_tile
   if (err != cudaSuccess) return err;
   err = launch_dependent(sched_count_kernel, dim3(nchunks), dim3(256), E * sizeof(int), st, te, n, E, hist, header);
   if (err != cudaSuccess) return err;
+  if (nchunks > kPrefixChunks) {
+    err = launch_dependent(sched_prefix_kernel, dim3(E), dim3(256), 0, st, E, nchunks, hist, cnt,
+                           static_cast<const int*>(header));
+    if (err != cudaSuccess) return err;
+  }
   err = launch_dependent(sched_scan_kernel, dim3(1), dim3(1024), 0, st, n, E, nchunks, cap_tiles, max_tiles, hist, cnt,
                          row0, row_src, tile_expert, tile_row0, tile_rows, pair_tile, header);
   if (err != cudaSuccess) return err;
