@@ -215,6 +215,12 @@ typedef struct {
   int32_t* pair_tile;     /* [max_tiles][2] tile pairs for CTA-pair GEMMs: two consecutive
                              tiles of one expert (within the primary list, then within the
                              overflow list), second -1 for an odd tile; unused pairs -1 */
+  int32_t* unit_group;    /* [2][max_tiles] the GEMMs' work groups: entry t of the first
+                             half for tile t, entry p of the second for pair p.  Each run of
+                             one expert's tiles (pairs) in the primary list, and in the
+                             overflow list, is cut evenly into groups of at most 32 tiles
+                             (16 pairs); an entry holds the unit's position in its group in
+                             bits 0..7 and the group's length in bits 8..15.  Unused -1 */
 } mok_schedule_t;
 
 /* Layer weights, [MoKDoc] _MoKRuntime.forward layouts.  The shared expert is

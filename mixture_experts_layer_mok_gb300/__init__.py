@@ -112,7 +112,8 @@ class Schedule:
         view = {}
         for name, n in (("cnt", self.E), ("row0", self.E + 1), ("row_src", mt * 128),
                         ("slot_row", self.T * self.k), ("tile_expert", mt), ("tile_row0", mt),
-                        ("tile_rows", mt), ("header", 8), ("pair_tile", 2 * mt)):
+                        ("tile_rows", mt), ("header", 8), ("pair_tile", 2 * mt),
+                        ("unit_group", 2 * mt)):
             off = getattr(self.c, name) - base
             view[name] = self.buf[off: off + 4 * n].view(torch.int32)
         return view

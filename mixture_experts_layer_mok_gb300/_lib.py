@@ -48,7 +48,8 @@ class MokConfig(C.Structure):
 class MokSchedule(C.Structure):
     _fields_ = [("T", C.c_int), ("k", C.c_int), ("E", C.c_int), ("max_tiles", C.c_int),
                 ("cnt", P), ("row0", P), ("row_src", P), ("slot_row", P), ("tile_expert", P),
-                ("tile_row0", P), ("tile_rows", P), ("header", P), ("scratch", P), ("pair_tile", P)]
+                ("tile_row0", P), ("tile_rows", P), ("header", P), ("scratch", P), ("pair_tile", P),
+                ("unit_group", P)]
 
 
 class MokWeights(C.Structure):

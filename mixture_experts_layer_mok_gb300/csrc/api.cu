@@ -228,7 +228,8 @@ long long max_tiles_of(int T, int k, int E) {
 }
 
 struct SchedLayout {
-  int32_t *cnt, *row0, *row_src, *slot_row, *tile_expert, *tile_row0, *tile_rows, *header, *hist, *pair_tile;
+  int32_t *cnt, *row0, *row_src, *slot_row, *tile_expert, *tile_row0, *tile_rows, *header, *hist, *pair_tile,
+      *unit_group;
 };
 
 size_t carve_schedule(void* buf, int T, int k, int E, SchedLayout* L) {
@@ -245,6 +246,7 @@ size_t carve_schedule(void* buf, int T, int k, int E, SchedLayout* L) {
   L->tile_rows = c.take<int32_t>(mt);
   L->header = c.take<int32_t>(8);
   L->pair_tile = c.take<int32_t>(2 * mt);
+  L->unit_group = c.take<int32_t>(2 * mt);
   L->hist = c.take<int32_t>(nchunks * E);
   return c.off + 256;
 }
@@ -265,10 +267,10 @@ long long ring_rows_of(long long macrobatch, long long max_rows) {
   return r >= max_rows ? 0 : r;
 }
 
-// Ints of the windows' schedule views: the tiles and the pairs of all windows
-// (max_tiles at most), ne + 1 row offsets and an 8-int header per window (at
-// most E windows).
-long long view_ints(long long max_tiles, int E) { return 5 * max_tiles + 10ll * E; }
+// Ints of the windows' schedule views: the tiles, pairs and work groups of all
+// windows (max_tiles tiles at most), ne + 1 row offsets and an 8-int header
+// per window (at most E windows).
+long long view_ints(long long max_tiles, int E) { return 7 * max_tiles + 10ll * E; }
 
 // Bytes of E8M0 scales of a [rows][K] tensor in the tensor-core scale layout
 // (rows padded to whole 128-row blocks).
@@ -460,6 +462,8 @@ GemmParams base_params(const mok_config_t* cfg, const mok_schedule_t* s, int* st
     p.row0 = s->row0;
     p.cnt = s->cnt;
     p.pair_tile = s->pair_tile;
+    p.tile_group = s->unit_group;
+    p.pair_group = s->unit_group ? s->unit_group + s->max_tiles : nullptr;
   }
   p.status = status;
   p.debug = debug;
@@ -494,22 +498,15 @@ mok_status_t plan_windows(const int32_t* cnt, int E, long long ring, std::vector
 
 // One window of the routed experts: experts [e0, e0 + ne) and their schedule
 // rows [r0, r0 + rows).  `s` is the schedule itself when one window covers it,
-// else the window's view (launch_window_view): its own tile list, pairs and
-// header, tile rows and row0 counted from r0, cnt and row_src offset to the
-// window; s.max_tiles is the window's tile count.  Tile experts stay absolute.
+// else the window's view (launch_window_view): its own tile list, pairs, work
+// groups and header, tile rows and row0 counted from r0, cnt and row_src
+// offset to the window; s.max_tiles is then the window's tile count.  Tile
+// experts stay absolute.
 struct Win {
   mok_schedule_t s;
   int e0, ne;
   long long r0, rows;
 };
-
-// GEMM parameters over a window's schedule view: its row0 and cnt start at the
-// window's first expert.
-GemmParams win_params(const mok_config_t* cfg, const Win& v, int* status, int debug) {
-  GemmParams p = base_params(cfg, &v.s, status, debug);
-  p.e_base = v.e0;
-  return p;
-}
 
 // The windows of a call.  Without a ring: one window over the whole schedule
 // (nothing is read back).  With one: the expert counts and the header are
@@ -549,21 +546,22 @@ mok_status_t make_windows(const mok_schedule_t* s, long long ring, int32_t* view
       pairs += (prim + 1) / 2 + (nt - prim + 1) / 2;
     }
     v.rows = tiles * kTileRows;
-    v.s.max_tiles = static_cast<int>(tiles);
     if (nw > 1) {
-      int32_t* rows0 = view + 5 * mt + v.e0 + w;
-      int32_t* header = view + 5 * mt + 2ll * E + 8ll * w;
+      int32_t* rows0 = view + 7 * mt + v.e0 + w;
+      int32_t* header = view + 7 * mt + 2ll * E + 8ll * w;
+      v.s.max_tiles = static_cast<int>(tiles);
       v.s.tile_expert = view + tile_off;
       v.s.tile_row0 = view + mt + tile_off;
       v.s.tile_rows = view + 2 * mt + tile_off;
       v.s.pair_tile = view + 3 * mt + 2 * pair_off;
+      v.s.unit_group = view + 5 * mt + 2 * tile_off;   // the window's tile groups, then its pair groups
       v.s.row0 = rows0;
       v.s.header = header;
       v.s.cnt = s->cnt + v.e0;
       v.s.row_src = s->row_src + r0;
       v.s.scratch = nullptr;
       MOK_CUDA(launch_window_view(s->cnt, s->row0, s->header, v.e0, v.ne, v.s.tile_expert, v.s.tile_row0,
-                                  v.s.tile_rows, v.s.pair_tile, rows0, header, cs));
+                                  v.s.tile_rows, v.s.pair_tile, v.s.unit_group, rows0, header, cs));
     }
     out->push_back(v);
     r0 += v.rows;
@@ -811,7 +809,7 @@ mok_status_t forward_bf16(const mok_config_t* cfg, const uint16_t* x, const floa
         (st = make_map(&m.b1, w->w_up, H, static_cast<uint64_t>(E) * I, 128, bk)) ||
         (st = make_map_out(&m.o0, gu, 2ull * I, v.rows)) || (st = make_map_out(&m.o1, ctx->h, I, v.rows)))
       return st;
-    GemmParams p = win_params(cfg, v, ctx->status, cfg->debug_flags);
+    GemmParams p = base_params(cfg, &v.s, ctx->status, cfg->debug_flags);
     p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / 128; p.b_rows_per_expert = I;
     p.out0 = gu; p.out1 = ctx->h; p.ga = x; p.ga_ld = H;
     p.swiglu_limit = cfg->swiglu_limit;
@@ -834,7 +832,7 @@ mok_status_t forward_bf16(const mok_config_t* cfg, const uint16_t* x, const floa
         (st = make_map_out(&m2.o0, slots, H, v.rows)))
       return st;
     m2.b1 = m2.b0;
-    GemmParams q = win_params(cfg, v, ctx->status, 0);
+    GemmParams q = base_params(cfg, &v.s, ctx->status, 0);
     q.grouped = 1; q.K = I; q.N = H; q.n_tiles = H / bn; q.b_rows_per_expert = H;
     q.out0 = slots; q.ld = H; q.rw = router_w;
     const long long items2 = static_cast<long long>(v.s.max_tiles) * q.n_tiles;
@@ -996,7 +994,7 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
         (st = gu_sf_maps(m, X.wg_sc, X.wu_sc, static_cast<long long>(E) * I)) ||
         (st = make_map_out(&m.o0, gu, 2ull * I, v.rows)) || (st = make_map_codes_out(&m.o1, ctx->hq, I, v.rows)))
       return st;
-    GemmParams p = win_params(cfg, v, ctx->status, cfg->debug_flags);
+    GemmParams p = base_params(cfg, &v.s, ctx->status, cfg->debug_flags);
     p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / gu_cols; p.b_rows_per_expert = I;
     p.out0 = gu; p.out1 = ctx->hq; p.sf_out = ctx->hq_sc;
     p.swiglu_limit = cfg->swiglu_limit;
@@ -1015,7 +1013,7 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
       return st;
     m2.b1 = m2.b0;
     m2.sfb1 = m2.sfb0;
-    GemmParams q = win_params(cfg, v, ctx->status, 0);
+    GemmParams q = base_params(cfg, &v.s, ctx->status, 0);
     q.grouped = 1; q.K = I; q.N = H; q.n_tiles = H / dn_bn; q.b_rows_per_expert = H;
     q.out0 = slots; q.ld = H; q.rw = router_w;
     q.sfa = ctx->hq_sc; q.sfb0 = X.wd_sc;
@@ -1192,7 +1190,7 @@ mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const u
           (st = make_map_codes_out(&m.o2, L.hwT, v.rows, I)))
         return st;
       m.b1 = m.b0;
-      GemmParams p = win_params(cfg, v, ctx->status, 0);
+      GemmParams p = base_params(cfg, &v.s, ctx->status, 0);
       p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / 128; p.b_rows_per_expert = I;
       p.aux0 = ctx->gu + v.r0 * 2 * I; p.rw = router_w; p.dw_part = L.dw_part; p.swiglu_limit = ctx->swiglu_limit;
       p.sf_out = L.dguq_sc; p.out2 = L.dguT_sc; p.sf_out2 = L.hwT_sc; p.ld = v.rows;   // codes: maps o0..o2
@@ -1209,7 +1207,7 @@ mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const u
       if ((st = make_map_u8(&m.a, L.dyT, v.rows, H, 128)) || (st = make_map_u8(&m.b0, L.hwT, v.rows, I, bn)))
         return st;
       m.b1 = m.b0;
-      GemmParams p = win_params(cfg, v, ctx->status, 0);
+      GemmParams p = base_params(cfg, &v.s, ctx->status, 0);
       p.wgrad = 1; p.grouped = 1; p.K = rows; p.E = v.ne; p.m_tiles = H / 128; p.n_tiles = I / bn;
       p.out0 = out; p.out1 = out; p.ld = I; p.split = H;
       p.sfa = L.dyT_sc; p.sfb0 = L.hwT_sc;
@@ -1222,7 +1220,7 @@ mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const u
       if ((st = make_map_u8(&m.a, L.dguT, v.rows, 2ull * I, 128)) || (st = make_map_u8(&m.b0, L.xT, v.rows, H, bnH)))
         return st;
       m.b1 = m.b0;
-      GemmParams p = win_params(cfg, v, ctx->status, 0);
+      GemmParams p = base_params(cfg, &v.s, ctx->status, 0);
       p.wgrad = 1; p.grouped = 1; p.K = rows; p.E = v.ne; p.m_tiles = 2 * I / 128; p.n_tiles = H / bnH;
       p.out0 = g->d_w_gate + static_cast<long long>(v.e0) * I * H;
       p.out1 = g->d_w_up + static_cast<long long>(v.e0) * I * H;
@@ -1240,7 +1238,7 @@ mok_status_t backward_mxfp8(const mok_config_t* cfg, const uint16_t* dy, const u
           (st = make_map_u8(&m.b1, w->mxt_up, I, static_cast<uint64_t>(E) * H, bnH)) ||
           (st = make_map_out(&m.o0, out, H, v.rows)))
         return st;
-      GemmParams p = win_params(cfg, v, ctx->status, 0);
+      GemmParams p = base_params(cfg, &v.s, ctx->status, 0);
       p.grouped = 1; p.K = 2 * I; p.N = H; p.n_tiles = H / bnH; p.b_rows_per_expert = H; p.b_split = I;
       p.out0 = out; p.ld = H;
       p.sfa = L.dguq_sc; p.sfb0 = L.wtg_sc; p.sfb1 = L.wtu_sc; p.sf_kgb = I / 128;
@@ -1378,7 +1376,7 @@ mok_status_t backward_bf16(const mok_config_t* cfg, const uint16_t* dy, const ui
           (st = make_map_out(&m.o0, L.dgu, 2ull * I, v.rows)) || (st = make_map_out(&m.o1, L.hw, I, v.rows)))
         return st;
       m.b1 = m.b0;
-      GemmParams p = win_params(cfg, v, ctx->status, 0);
+      GemmParams p = base_params(cfg, &v.s, ctx->status, 0);
       p.grouped = 1; p.K = H; p.N = I; p.n_tiles = I / bn1; p.b_rows_per_expert = H;
       p.aux0 = ctx->gu + v.r0 * 2 * I; p.out0 = L.dgu; p.out1 = L.hw; p.rw = router_w; p.dw_part = L.dw_part;
       p.swiglu_limit = ctx->swiglu_limit;
@@ -1412,7 +1410,7 @@ mok_status_t backward_bf16(const mok_config_t* cfg, const uint16_t* dy, const ui
         return st;
       m.o1 = m.o0;
       m.b1 = m.b0;
-      GemmParams p = win_params(cfg, v, ctx->status, 0);
+      GemmParams p = base_params(cfg, &v.s, ctx->status, 0);
       p.wgrad = 1; p.grouped = 1; p.E = v.ne; p.m_tiles = H / 128; p.n_tiles = I / bn;
       p.out0 = out; p.out1 = out; p.ld = I; p.split = H;
       p.estride = static_cast<long long>(H) * I;
@@ -1449,7 +1447,7 @@ mok_status_t backward_bf16(const mok_config_t* cfg, const uint16_t* dy, const ui
           (st = make_map_out(&m.o1, out_u, H, static_cast<uint64_t>(v.ne) * I)))
         return st;
       m.b1 = m.b0;
-      GemmParams p = win_params(cfg, v, ctx->status, 0);
+      GemmParams p = base_params(cfg, &v.s, ctx->status, 0);
       p.wgrad = 1; p.grouped = 1; p.E = v.ne; p.m_tiles = 2 * I / 128; p.n_tiles = H / bn;
       p.out0 = out_g; p.out1 = out_u; p.ld = H; p.split = I;
       p.estride = static_cast<long long>(I) * H;
@@ -1483,7 +1481,7 @@ mok_status_t backward_bf16(const mok_config_t* cfg, const uint16_t* dy, const ui
           (st = make_map_mn(&m.b1, w->w_up, H, static_cast<uint64_t>(E) * I, bw, kTileBK)) ||
           (st = make_map_out(&m.o0, out, H, v.rows)))
         return st;
-      GemmParams p = win_params(cfg, v, ctx->status, 0);
+      GemmParams p = base_params(cfg, &v.s, ctx->status, 0);
       p.grouped = 1; p.K = 2 * I; p.N = H; p.n_tiles = H / bn; p.b_rows_per_expert = I; p.b_split = I;
       p.out0 = out; p.ld = H;
       const long long items = static_cast<long long>(v.s.max_tiles) * p.n_tiles;
@@ -1591,11 +1589,11 @@ mok_status_t mok_schedule(const int64_t* top_experts, int T, int k, int E, doubl
   const int cap = static_cast<int>(capd);
   MOK_CUDA(launch_schedule(top_experts, T, k, E, cap, static_cast<int>(mt), L.hist, L.cnt, L.row0,
                            L.row_src, L.slot_row, L.tile_expert, L.tile_row0, L.tile_rows, L.pair_tile,
-                           L.header, static_cast<cudaStream_t>(stream)));
+                           L.unit_group, L.header, static_cast<cudaStream_t>(stream)));
   out->T = T; out->k = k; out->E = E; out->max_tiles = static_cast<int>(mt);
   out->cnt = L.cnt; out->row0 = L.row0; out->row_src = L.row_src; out->slot_row = L.slot_row;
   out->tile_expert = L.tile_expert; out->tile_row0 = L.tile_row0; out->tile_rows = L.tile_rows;
-  out->header = L.header; out->scratch = L.hist; out->pair_tile = L.pair_tile;
+  out->header = L.header; out->scratch = L.hist; out->pair_tile = L.pair_tile; out->unit_group = L.unit_group;
   return MOK_OK;
 }
 
@@ -1862,11 +1860,11 @@ mok_status_t mok_schedule_noalloc(const int64_t* top_experts, int T, int k, int 
   // array needs no clearing between calls
   MOK_CUDA(launch_schedule(top_experts, T, k, E, static_cast<int>(capd), static_cast<int>(mt), scratch, L.cnt,
                            L.row0, L.row_src, L.slot_row, L.tile_expert, L.tile_row0, L.tile_rows, L.pair_tile,
-                           L.header, static_cast<cudaStream_t>(stream)));
+                           L.unit_group, L.header, static_cast<cudaStream_t>(stream)));
   out->T = T; out->k = k; out->E = E; out->max_tiles = static_cast<int>(mt);
   out->cnt = L.cnt; out->row0 = L.row0; out->row_src = L.row_src; out->slot_row = L.slot_row;
   out->tile_expert = L.tile_expert; out->tile_row0 = L.tile_row0; out->tile_rows = L.tile_rows;
-  out->header = L.header; out->scratch = scratch; out->pair_tile = L.pair_tile;
+  out->header = L.header; out->scratch = scratch; out->pair_tile = L.pair_tile; out->unit_group = L.unit_group;
   return MOK_OK;
 }
 

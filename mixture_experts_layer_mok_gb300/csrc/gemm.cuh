@@ -89,6 +89,8 @@ struct GemmParams {
   const int* row0;
   const int* cnt;
   const int* pair_tile;  // CTA-pair GEMMs: [pairs][2] tile indices (second -1 = none)
+  const int* tile_group; // work groups of the tiles and of the pairs (the schedule's unit_group):
+  const int* pair_group; // position in the group (bits 0..7), group length (bits 8..15)
   // ---- operand coordinates
   int b_rows_per_expert;  // weight rows (K-major B) or K-rows (MN-major B) per expert
   int b_split;            // MN-major B: K index where map b1 takes over (0 = never)
@@ -123,11 +125,10 @@ struct GemmParams {
   // ---- order of the work items (never changes a result: each output tile has
   // one owner and a fixed K order)
   int group;         // row GEMMs: 0 = column tiles inside each row unit (tile or pair);
-                     // g > 0 = row units in groups of at most g, the group's units
-                     // inside each column tile (B's columns stream once per group
-                     // while the group's A rows stay in L2); a grouped GEMM whose
-                     // tiles are all primary cuts its groups at expert boundaries
-  int e_base;        // grouped: first expert of row0 / cnt (a macrobatch window's view)
+                     // g > 0 = row units in groups, the group's units inside each
+                     // column tile (B's columns stream once per group while the
+                     // group's A rows stay in L2): a grouped GEMM takes the
+                     // schedule's groups (one expert each), a dense one groups of g
   int wg_col_outer;  // weight gradients: 1 = an expert's row units inside each
                      // column tile (B streams once, A stays in L2), 0 = the reverse
 };
@@ -136,13 +137,13 @@ struct GemmParams {
 // are -1 (-2: the plain order).  Row GEMMs take their row units (tiles, or
 // pairs of tiles) in groups inside each column tile: while the group's A rows
 // stay in L2, each B column slice (an expert's weights, a few MB) is read once
-// for the whole group instead of once per row unit.  Dense GEMMs group 16 row
-// tiles; grouped ones up to 32 tiles of one expert (an expert of more is split
-// into even groups), so that no group holds two experts' weights.  Weight
+// for the whole group instead of once per row unit.  Grouped GEMMs take the
+// schedule's groups, at most 32 tiles (16 pairs) of one expert, so that no
+// group holds two experts' weights; dense ones group 16 row tiles.  Weight
 // gradients walk an expert's row units inside each column tile when A (M rows
 // per expert) is the smaller operand, so that B streams through once.
 inline void resolve_item_order(GemmParams& p, bool pair) {
-  if (p.group < 0) p.group = (p.group == -2) ? 0 : (p.grouped ? (pair ? 16 : 32) : (pair ? 8 : 16));
+  if (p.group < 0) p.group = (p.group == -2) ? 0 : (pair ? 8 : 16);
   if (p.wg_col_outer < 0)
     p.wg_col_outer = (p.wg_col_outer == -2) ? 0 : (p.wgrad && static_cast<long long>(p.m_tiles) * kBM < p.ld ? 1 : 0);
 }
@@ -163,27 +164,17 @@ __device__ __forceinline__ void unit_and_col(int idx, int units, int n_tiles, in
   u = g * group + (r - nt * gs);
 }
 
-// The same for a grouped GEMM whose tiles are all in the primary list (each
-// expert's row units consecutive, in expert order, unit j of expert e covering
-// its rows [j U, (j + 1) U) with U = 128 for tiles, 256 for pairs): the groups
-// are an expert's units, split evenly into ceil(units / cap) groups when it
-// has more than cap.  The items of a group of units [s, s + L) are [s n, (s +
-// L) n), so the unit idx / n lies in idx's group.
-__device__ __forceinline__ void expert_unit_and_col(const GemmParams& p, int idx, bool pairs, int& u, int& nt) {
-  const int n = p.n_tiles;
+// The same for a grouped GEMM, whose groups the schedule lists (each group a
+// run of consecutive units of one expert): the items of a group of units [s,
+// s + L) are [s n, (s + L) n), so the unit idx / n lies in idx's group, and its
+// entry gives s and L.
+__device__ __forceinline__ void listed_unit_and_col(const int* groups, int idx, int n, int& u, int& nt) {
   const int u0 = idx / n;
-  const int t0 = pairs ? __ldg(p.pair_tile + 2 * u0) : u0;
-  const int e = __ldg(p.tile_expert + t0) - p.e_base;
-  const int shift = pairs ? 8 : 7;
-  const int j = (__ldg(p.tile_row0 + t0) - __ldg(p.row0 + e)) >> shift;
-  const int nu = (__ldg(p.cnt + e) + (1 << shift) - 1) >> shift;
-  const int ng = (nu + p.group - 1) / p.group;
-  const int gsz = (nu + ng - 1) / ng;
-  const int gj = j / gsz * gsz;
-  const int gl = min(gsz, nu - gj);
-  const int r = idx - (u0 - j + gj) * n;
-  nt = r / gl;
-  u = u0 - j + gj + (r - nt * gl);
+  const int g = __ldg(groups + u0);
+  const int s = u0 - (g & 0xFF), len = g >> 8;
+  const int r = idx - s * n;
+  nt = r / len;
+  u = s + (r - nt * len);
 }
 
 struct Item {
@@ -205,8 +196,8 @@ __device__ __forceinline__ Item get_item(const GemmParams& p, int idx, int bk) {
   it.empty = false;
   if (!p.wgrad) {
     int mt;
-    if (p.grouped && p.group > 0 && p.header[3] == p.header[0])
-      expert_unit_and_col(p, idx, false, mt, it.nt);
+    if (p.grouped && p.group > 0)
+      listed_unit_and_col(p.tile_group, idx, p.n_tiles, mt, it.nt);
     else
       unit_and_col(idx, p.grouped ? p.header[0] : (p.rows + kBM - 1) / kBM, p.n_tiles, p.group, mt, it.nt);
     if (p.grouped) {
@@ -259,8 +250,8 @@ __device__ __forceinline__ Item get_item_pair(const GemmParams& p, int idx, int 
   it.empty = false;
   if (!p.wgrad) {
     int pr;
-    if (p.grouped && p.group > 0 && p.header[3] == p.header[0])
-      expert_unit_and_col(p, idx, true, pr, it.nt);
+    if (p.grouped && p.group > 0)
+      listed_unit_and_col(p.pair_group, idx, p.n_tiles, pr, it.nt);
     else
       unit_and_col(idx, p.grouped ? p.header[4] : ((p.rows + kBM - 1) / kBM + 1) / 2, p.n_tiles, p.group, pr, it.nt);
     if (p.grouped) {
@@ -302,6 +293,17 @@ __device__ __forceinline__ Item get_item_pair(const GemmParams& p, int idx, int 
     }
   }
   return it;
+}
+
+// The K-block count of work item idx, which is all the MMA issuer needs:
+// constant for row GEMMs, an expert's row count for weight gradients (the same
+// value get_item / get_item_pair give, without their row-unit lookups).
+__device__ __forceinline__ int item_nk(const GemmParams& p, int idx, int bk, bool pair) {
+  if (!p.wgrad) return p.K / bk;
+  if (!p.grouped) return (p.rows + bk - 1) / bk;
+  const int per_e = (pair ? (p.m_tiles + 1) / 2 : p.m_tiles) * p.n_tiles;
+  const int c = __ldg(p.cnt + idx / per_e);
+  return (c + kBM - 1) / kBM * (kBM / bk);
 }
 
 // Token row of schedule row q (padding rows read token 0; their partner
@@ -754,13 +756,13 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI, PAIR>::kThreads
       uint32_t aphase = 0;
       bool first = true;
       for (int idx = item0; idx < nitems; idx += istep) {
-        const Item it = item_at(idx, C::kBK);
-        if (it.nk == 0) continue;
+        const int nk = item_nk(p, idx, C::kBK, PAIR);
+        if (nk == 0) continue;
         if (!mbar_wait(&tempty[abuf], aphase ^ 1, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t acc = tmem_base + static_cast<uint32_t>(abuf * BN);
         bool ok = true;
-        for (int kb = 0; kb < it.nk; ++kb) {
+        for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
             ok = false;
             break;

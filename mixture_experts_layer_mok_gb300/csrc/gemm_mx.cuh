@@ -345,13 +345,13 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
       uint32_t aphase = 0;
       bool first = true;
       for (int idx = item0; idx < nitems; idx += istep) {
-        const Item it = item_at(idx);
-        if (it.nk == 0) continue;
+        const int nk = item_nk(p, idx, C::kBK, PAIR);
+        if (nk == 0) continue;
         if (!mbar_wait(&tempty[abuf], aphase ^ 1, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t acc = tmem_base + static_cast<uint32_t>(abuf * BN);
         bool ok = true;
-        for (int kb = 0; kb < it.nk; ++kb) {
+        for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
             ok = false;
             break;

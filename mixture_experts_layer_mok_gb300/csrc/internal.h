@@ -8,6 +8,8 @@
 namespace mok {
 
 constexpr int kTileRows = 128;     // rows per expert tile
+constexpr int kGroupTiles = 32;    // work group of the grouped GEMMs: at most this many tiles
+constexpr int kGroupPairs = 16;    // ... or tile pairs, of one expert
 constexpr int kSchedChunk = 1024;  // routed rows per schedule block
 
 struct GemmMaps;
@@ -33,8 +35,8 @@ cudaError_t launch_dependent(void (*kern)(P...), dim3 grid, dim3 block, size_t s
 
 cudaError_t launch_schedule(const int64_t* te, int T, int k, int E, int cap_tiles, int max_tiles,
                             int* hist, int* cnt, int* row0, int* row_src, int* slot_row,
-                            int* tile_expert, int* tile_row0, int* tile_rows, int* pair_tile, int* header,
-                            cudaStream_t st);
+                            int* tile_expert, int* tile_row0, int* tile_rows, int* pair_tile, int* unit_group,
+                            int* header, cudaStream_t st);
 cudaError_t launch_mx_quantize(const uint16_t* x, long long nblocks, uint8_t* codes, uint8_t* scales,
                                int num_sms, cudaStream_t st);
 // Schedule rows [w0, w0 + wrows) go to rows from 0 of xp / xp_sc (and xb);
@@ -73,11 +75,11 @@ cudaError_t launch_permute_rows(const uint16_t* src, int T, int H, int topk, con
                                 const int* header, long long w0, long long wrows, uint16_t* out, int num_sms,
                                 cudaStream_t st);
 // The schedule restricted to experts [e0, e0 + ne) (a macrobatch window):
-// its tile list, pairs, row offsets (ne + 1) and header, rows counted from
-// row0[e0].
+// its tile list, pairs, work groups ([2][tiles of the window]), row offsets
+// (ne + 1) and header, rows counted from row0[e0].
 cudaError_t launch_window_view(const int* cnt, const int* row0, const int* header, int e0, int ne, int* tile_expert,
-                               int* tile_row0, int* tile_rows, int* pair_tile, int* wrow0, int* wheader,
-                               cudaStream_t st);
+                               int* tile_row0, int* tile_rows, int* pair_tile, int* unit_group, int* wrow0,
+                               int* wheader, cudaStream_t st);
 cudaError_t launch_dw_reduce(const float* part, int nf, int ntiles, float* dw, cudaStream_t st);
 
 // Grouped GEMM launch: instantiated for the operand sources / tile widths /

@@ -69,6 +69,19 @@ __device__ int block_exclusive_scan(int v, int* tmp /* >= 32 ints */, int* total
   return before + x - v;
 }
 
+// Work-group entries of a run of `len` units (tiles or pairs) of one expert
+// from unit `first`: groups of at most `cap` consecutive units, the run cut
+// evenly; an entry packs the unit's position in its group (bits 0..7) and the
+// group's length (bits 8..15).
+__device__ void write_groups(int* g, int first, int len, int cap) {
+  if (len <= 0) return;
+  const int ng = (len + cap - 1) / cap, gsz = (len + ng - 1) / ng;
+  for (int i = 0; i < len; ++i) {
+    const int gj = i / gsz * gsz;
+    g[first + i] = (i - gj) | (min(gsz, len - gj) << 8);
+  }
+}
+
 // Large schedules: the per-expert chunk offsets, one block per expert.  Column
 // e of hist [nchunks][E] becomes each chunk's exclusive offset within expert
 // e, and cnt[e] its total; each thread takes a run of consecutive chunks.
@@ -105,6 +118,7 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int n, int E, int nchu
                                                           int* __restrict__ tile_row0,
                                                           int* __restrict__ tile_rows,
                                                           int* __restrict__ pair_tile,
+                                                          int* __restrict__ unit_group,
                                                           int* __restrict__ header) {
   griddep_wait();
   griddep_launch_dependents();
@@ -212,16 +226,22 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int n, int E, int nchu
       pair_tile[2 * (total_pp + po_off + j)] = total_prim + ovf_off + 2 * j;
       pair_tile[2 * (total_pp + po_off + j) + 1] = (2 * j + 1 < no) ? total_prim + ovf_off + 2 * j + 1 : -1;
     }
+    write_groups(unit_group, prim_off, prim, kGroupTiles);
+    write_groups(unit_group, total_prim + ovf_off, no, kGroupTiles);
+    write_groups(unit_group + max_tiles, pp_off, pp, kGroupPairs);
+    write_groups(unit_group + max_tiles, total_pp + po_off, po, kGroupPairs);
   }
   const int num_pairs = total_pp + total_po;
   for (int i = num_pairs + threadIdx.x; i < max_tiles; i += blockDim.x) {
     pair_tile[2 * i] = -1;
     pair_tile[2 * i + 1] = -1;
+    unit_group[max_tiles + i] = -1;
   }
   for (int i = num_tiles + threadIdx.x; i < max_tiles; i += blockDim.x) {
     tile_expert[i] = -1;
     tile_row0[i] = -1;
     tile_rows[i] = -1;
+    unit_group[i] = -1;
   }
   for (long long q = total_rows + threadIdx.x; q < max_rows; q += blockDim.x) row_src[q] = -1;
   if (threadIdx.x == 0) {
@@ -283,8 +303,8 @@ __global__ void __launch_bounds__(256) sched_scatter_kernel(const int64_t* __res
 
 cudaError_t launch_schedule(const int64_t* te, int T, int k, int E, int cap_tiles, int max_tiles,
                             int* hist, int* cnt, int* row0, int* row_src, int* slot_row,
-                            int* tile_expert, int* tile_row0, int* tile_rows, int* pair_tile, int* header,
-                            cudaStream_t st) {
+                            int* tile_expert, int* tile_row0, int* tile_rows, int* pair_tile, int* unit_group,
+                            int* header, cudaStream_t st) {
   const int n = T * k;
   const int nchunks = (n + kSchedChunk - 1) / kSchedChunk;
   cudaError_t err = cudaMemsetAsync(header, 0, 8 * sizeof(int), st);
@@ -297,7 +317,7 @@ cudaError_t launch_schedule(const int64_t* te, int T, int k, int E, int cap_tile
     if (err != cudaSuccess) return err;
   }
   err = launch_dependent(sched_scan_kernel, dim3(1), dim3(1024), 0, st, n, E, nchunks, cap_tiles, max_tiles, hist, cnt,
-                         row0, row_src, tile_expert, tile_row0, tile_rows, pair_tile, header);
+                         row0, row_src, tile_expert, tile_row0, tile_rows, pair_tile, unit_group, header);
   if (err != cudaSuccess) return err;
   const size_t smem = 9 * E * sizeof(int);
   if (smem > 48 * 1024) {
@@ -319,7 +339,8 @@ cudaError_t launch_schedule(const int64_t* te, int T, int k, int E, int cap_tile
 // restricted to experts [e0, e0 + ne), with rows counted from the window's
 // first schedule row row0[e0]: its tile list in the schedule's own order
 // (primary tiles, at most cap_tiles of each expert, then the overflow list),
-// tile pairs, per-expert row offsets (ne + 1 entries) and header.  Tile
+// tile pairs, work groups (those of the tiles, then of the pairs),
+// per-expert row offsets (ne + 1 entries) and header.  Tile
 // experts stay absolute (they index the weights).  One 1024-thread block, one
 // thread per expert of the window.
 // ===========================================================================
@@ -327,7 +348,8 @@ __global__ void __launch_bounds__(1024) window_view_kernel(const int* __restrict
                                                            const int* __restrict__ header, int e0, int ne,
                                                            int* __restrict__ tile_expert, int* __restrict__ tile_row0,
                                                            int* __restrict__ tile_rows, int* __restrict__ pair_tile,
-                                                           int* __restrict__ wrow0, int* __restrict__ wheader) {
+                                                           int* __restrict__ unit_group, int* __restrict__ wrow0,
+                                                           int* __restrict__ wheader) {
   griddep_wait();
   griddep_launch_dependents();
   __shared__ int tmp[32];
@@ -365,6 +387,11 @@ __global__ void __launch_bounds__(1024) window_view_kernel(const int* __restrict
       pair_tile[2 * (total_pp + po_off + j)] = total_prim + ovf_off + 2 * j;
       pair_tile[2 * (total_pp + po_off + j) + 1] = (2 * j + 1 < no) ? total_prim + ovf_off + 2 * j + 1 : -1;
     }
+    const int tiles = total_prim + total_ovf;   // the window's pair groups follow its tile groups
+    write_groups(unit_group, prim_off, prim, kGroupTiles);
+    write_groups(unit_group, total_prim + ovf_off, no, kGroupTiles);
+    write_groups(unit_group + tiles, pp_off, pp, kGroupPairs);
+    write_groups(unit_group + tiles, total_pp + po_off, po, kGroupPairs);
   }
   if (i == 0) {
     const int rows = row0[e0 + ne] - base;
@@ -381,10 +408,10 @@ __global__ void __launch_bounds__(1024) window_view_kernel(const int* __restrict
 }
 
 cudaError_t launch_window_view(const int* cnt, const int* row0, const int* header, int e0, int ne, int* tile_expert,
-                               int* tile_row0, int* tile_rows, int* pair_tile, int* wrow0, int* wheader,
-                               cudaStream_t st) {
+                               int* tile_row0, int* tile_rows, int* pair_tile, int* unit_group, int* wrow0,
+                               int* wheader, cudaStream_t st) {
   cudaError_t err = launch_dependent(window_view_kernel, dim3(1), dim3(1024), 0, st, cnt, row0, header, e0, ne,
-                                     tile_expert, tile_row0, tile_rows, pair_tile, wrow0, wheader);
+                                     tile_expert, tile_row0, tile_rows, pair_tile, unit_group, wrow0, wheader);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }

@@ -23,6 +23,7 @@ def _check_schedule(te, E, c):
         assert np.array_equal(arr[key], ref[key]), key
     assert arr["header"][3] == ref["num_primary"]
     _check_pairs(arr, ref)
+    _check_groups(arr, ref)
 
 
 def _check_pairs(arr, ref):
@@ -42,6 +43,43 @@ def _check_pairs(arr, ref):
     assert arr["header"][4] == len(want)
     assert [tuple(int(v) for v in p) for p in pairs[:len(want)]] == want
     assert np.all(pairs[len(want):] == -1)
+
+
+def _run_groups(experts, lo, hi, cap):
+    """Work-group entries of units [lo, hi): each run of one expert cut evenly
+    into groups of at most cap units; entry = position | length << 8."""
+    want, i = {}, lo
+    while i < hi:
+        j = i
+        while j < hi and experts[j] == experts[i]:
+            j += 1
+        n = j - i
+        ng = -(-n // cap)
+        size = -(-n // ng)
+        for q in range(n):
+            start = q // size * size
+            want[i + q] = (q - start) | (min(size, n - start) << 8)
+        i = j
+    return want
+
+
+def _check_groups(arr, ref):
+    """The GEMMs' work groups (unit_group): runs of one expert's tiles within
+    the primary and the overflow list, and of its pairs, cut evenly into groups
+    of at most 32 tiles or 16 pairs; unused entries -1."""
+    nt, npr, mt = ref["num_tiles"], ref["num_primary"], len(ref["tile_expert"])
+    te = ref["tile_expert"]
+    g = arr["unit_group"]
+    want = {**_run_groups(te, 0, npr, 32), **_run_groups(te, npr, nt, 32)}
+    assert [int(g[t]) for t in range(nt)] == [want[t] for t in range(nt)]
+    assert np.all(g[nt:mt] == -1)
+    pairs = arr["pair_tile"].reshape(-1, 2)
+    npairs = int(arr["header"][4])
+    pe = [te[pairs[p][0]] for p in range(npairs)]
+    prim_pairs = sum(1 for p in range(npairs) if pairs[p][0] < npr)
+    want = {**_run_groups(pe, 0, prim_pairs, 16), **_run_groups(pe, prim_pairs, npairs, 16)}
+    assert [int(g[mt + p]) for p in range(npairs)] == [want[p] for p in range(npairs)]
+    assert np.all(g[mt + npairs:] == -1)
 
 
 @pytest.mark.parametrize("T,k,E,skew,c", [

@@ -20,14 +20,15 @@ from tests.gpu_util import mok
 
 pytestmark = pytest.mark.gpu
 
-ARRAYS = ("cnt", "row0", "row_src", "slot_row", "tile_expert", "tile_row0", "tile_rows", "header")
+ARRAYS = ("cnt", "row0", "row_src", "slot_row", "tile_expert", "tile_row0", "tile_rows", "header", "pair_tile",
+          "unit_group")
 
 
 def _views(sc, buf, T, k, E):
     base = buf.data_ptr()
     mt = sc.max_tiles
     sizes = {"cnt": E, "row0": E + 1, "row_src": mt * 128, "slot_row": T * k, "tile_expert": mt,
-             "tile_row0": mt, "tile_rows": mt, "header": 8}
+             "tile_row0": mt, "tile_rows": mt, "header": 8, "pair_tile": 2 * mt, "unit_group": 2 * mt}
     out = {}
     for name in ARRAYS:
         off = getattr(sc, name) - base
