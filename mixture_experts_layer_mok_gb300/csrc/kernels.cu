@@ -635,18 +635,23 @@ __global__ void __launch_bounds__(256) mx_quantize_t_kernel(const uint16_t* __re
   __shared__ __align__(16) uint8_t out[64 * kOutStride];
   __shared__ uint32_t osc[64];
   const int rtiles = (R + 127) / 128, ctiles = C / 64;
-  const long long ntiles = static_cast<long long>(batch) * rtiles * ctiles;
+  const int ntiles = batch * rtiles * ctiles;   // below 2^31 (the launch checks)
   const int c = threadIdx.x & 63, rb = threadIdx.x >> 6;
-  auto coords = [&](long long t, int& b, int& r0, int& c0) {
-    const int ct = static_cast<int>(t % ctiles);
-    const long long rest = t / ctiles;
-    r0 = static_cast<int>(rest % rtiles) * 128;
-    b = static_cast<int>(rest / rtiles);
-    c0 = ct * 64;
-  };
-  auto issue = [&](long long t, int buf) {   // cp.async of tile t's rows (zeros past the valid rows)
+  // tile t -> (batch b, first row r0, first column c0), in 32-bit arithmetic
+  // and once per tile (the next tile's coordinates are kept for its turn)
+  struct Coord {
     int b, r0, c0;
-    coords(t, b, r0, c0);
+  };
+  auto coords = [&](int t) {
+    const int rest = t / ctiles;
+    Coord x;
+    x.c0 = (t - rest * ctiles) * 64;
+    x.b = rest / rtiles;
+    x.r0 = (rest - x.b * rtiles) * 128;
+    return x;
+  };
+  auto issue = [&](const Coord& tc, int buf) {   // cp.async of the tile's rows (zeros past the valid rows)
+    const int b = tc.b, r0 = tc.r0, c0 = tc.c0;
     // this thread copies piece (tid & 7) of rows (tid >> 3) + 32 j, j < 4: their
     // source rows first (independent index loads), then the four copies
     const int piece = threadIdx.x & 7;
@@ -669,12 +674,18 @@ __global__ void __launch_bounds__(256) mx_quantize_t_kernel(const uint16_t* __re
     }
   };
   int buf = 0;
-  if (blockIdx.x < ntiles) issue(blockIdx.x, 0);
+  Coord cur = {0, 0, 0};
+  if (static_cast<int>(blockIdx.x) < ntiles) {
+    cur = coords(blockIdx.x);
+    issue(cur, 0);
+  }
   cp_async_commit();
-  for (long long t = blockIdx.x; t < ntiles; t += gridDim.x) {
-    int b, r0, c0;
-    coords(t, b, r0, c0);
-    if (t + gridDim.x < ntiles) issue(t + gridDim.x, buf ^ 1);
+  for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const int b = cur.b, r0 = cur.r0, c0 = cur.c0;
+    if (t + static_cast<int>(gridDim.x) < ntiles) {
+      cur = coords(t + gridDim.x);
+      issue(cur, buf ^ 1);
+    }
     cp_async_commit();
     cp_async_wait<1>();   // this tile's copies have landed (the next tile's may still fly)
     __syncthreads();
@@ -750,6 +761,7 @@ cudaError_t launch_mx_quantize_t(const uint16_t* src, long long ld, int batch, i
                                  int rtiled) {
   const long long tiles = static_cast<long long>(batch) * ((R + 127) / 128) * (C / 64);
   if (tiles == 0) return cudaSuccess;
+  if (tiles >= (1ll << 31)) return cudaErrorInvalidValue;   // the kernel indexes tiles in 32 bits
   // up to 32 blocks per SM, far more than are resident at once (5): blocks
   // that start as others finish keep more tiles' copies in flight than a
   // single resident wave walking its tiles does (measured on one GB300: 8, 16,
