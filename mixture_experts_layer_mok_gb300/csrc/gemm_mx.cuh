@@ -478,16 +478,16 @@ __global__ void __launch_bounds__(MxCfg<BN, EPI, PAIR>::kThreads, 1)
       // (the SwiGLU backward reads its chunks as it goes, from a second buffer)
       float v[EPI == EPI_DOWN_BWD_MX ? 1 : kCols];
       if constexpr (EPI != EPI_DOWN_BWD_MX) {
-        if (kSwiGLU) {   // gate columns [half*BN/4, +BN/4), up columns BN/2 later
+        // all loads in flight at once, one wait: the MMA waits for this drain
+        uint32_t ta[kCols / 32];
 #pragma unroll
-          for (int c = 0; c < kCols / 64; ++c) {
-            tmem_ld32(tb + half * (BN / 4) + c * 32, v + c * 32);
-            tmem_ld32(tb + BN / 2 + half * (BN / 4) + c * 32, v + kCols / 2 + c * 32);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < kCols / 32; ++c) tmem_ld32(tb + half * kCols + c * 32, v + c * 32);
+        for (int c = 0; c < kCols / 32; ++c) {
+          if (kSwiGLU)   // gate columns [half*BN/4, +BN/4) to v[0, kCols/2), up columns BN/2 later
+            ta[c] = tb + (c < kCols / 64 ? half * (BN / 4) + c * 32 : BN / 2 + half * (BN / 4) + (c - kCols / 64) * 32);
+          else
+            ta[c] = tb + half * kCols + c * 32;
         }
+        tmem_ld32_multi<kCols / 32>(ta, v);
         release_acc();
       }
 

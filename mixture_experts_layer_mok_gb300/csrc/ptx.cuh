@@ -347,6 +347,31 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// N loads of 32 consecutive fp32 columns of this thread's TMEM lane (32x32b
+// shape) at taddr[0..N), then one wait for all of them: v[32 i + j] = column j
+// of load i.  The registers pass through an empty asm after the wait, so that
+// no use can be scheduled before it.
+template <int N>
+__device__ __forceinline__ void tmem_ld32_multi(const uint32_t (&taddr)[N], float* v) {
+  uint32_t r[N][32];
+#pragma unroll
+  for (int i = 0; i < N; ++i)
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[i][0]), "=r"(r[i][1]), "=r"(r[i][2]), "=r"(r[i][3]), "=r"(r[i][4]), "=r"(r[i][5]), "=r"(r[i][6]), "=r"(r[i][7]), "=r"(r[i][8]), "=r"(r[i][9]), "=r"(r[i][10]), "=r"(r[i][11]), "=r"(r[i][12]), "=r"(r[i][13]), "=r"(r[i][14]), "=r"(r[i][15]), "=r"(r[i][16]), "=r"(r[i][17]), "=r"(r[i][18]), "=r"(r[i][19]), "=r"(r[i][20]), "=r"(r[i][21]), "=r"(r[i][22]), "=r"(r[i][23]), "=r"(r[i][24]), "=r"(r[i][25]), "=r"(r[i][26]), "=r"(r[i][27]), "=r"(r[i][28]), "=r"(r[i][29]), "=r"(r[i][30]), "=r"(r[i][31])
+        : "r"(taddr[i])
+        : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < N; ++i)
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      asm volatile("" : "+r"(r[i][j]));
+      v[32 * i + j] = __uint_as_float(r[i][j]);
+    }
+}
+
 // 16 consecutive fp32 columns of this thread's TMEM lane (32x32b shape), waited on.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   uint32_t r[16];
