@@ -108,6 +108,34 @@ def test_skewed_T16384_full_size(capacity):
         assert grads["d_w_down"][int(e)].abs().max().item() == 0.0
 
 
+def test_skewed_T16384_ring_matches_single_pass_bitwise():
+    """The skewed layer with a ring of 16384 rows (the hot experts alone in
+    their windows, the cold ones many to a window): bitwise equal to the single
+    pass."""
+    from tests.gpu_util import mok, weights_of
+
+    _need_bytes(40 << 30)
+    m = mok()
+    inp = gen.make_workload("skewed_T16384", seed=0, device="cuda")
+    w = weights_of(inp, "bf16")
+    E = inp.meta["E"]
+    sched = m.schedule(inp.top_experts, E, 0.5)
+    cnt = sched.arrays()["cnt"].cpu().numpy()
+    ring = max(16384, int(((cnt + 127) // 128 * 128).max()))
+    out = []
+    for mb in (0, ring):
+        y, ctx = m.forward(inp.x, inp.router_w, sched, w, minibatch=4096, macrobatch=mb)
+        grads = m.backward(inp.dy, inp.x, inp.router_w, sched, ctx, w, minibatch=4096, macrobatch=mb)
+        torch.cuda.synchronize()
+        assert ctx.status() == 0
+        out.append((y, grads))
+        del ctx
+    assert torch.equal(out[0][0], out[1][0])
+    for key in out[0][1]:
+        assert torch.equal(out[0][1][key], out[1][1][key]), key
+    assert len(m.macrobatch_plan(cnt.tolist(), ring)) > 2
+
+
 def _large(mode, ntok, seed):
     """T=65536, H=7168, I=2048, E=256, k=8, one shared expert (I_s=2048)."""
     _need_bytes(150 << 30)

@@ -216,3 +216,24 @@ def test_ring_under_autograd_matches_single_pass():
     for a, b in zip(*out):
         assert torch.equal(a, b)
     assert np.isfinite(out[0][1].float().cpu().numpy()).all()
+
+
+@pytest.mark.parametrize("mode", ["bf16", "mxfp8_full"])
+def test_ring_edge_layers_match_single_pass(mode):
+    """A one-expert layer (its only expert fills the one window), and a layer
+    where most experts are empty (the windows fold them in): bitwise equal to
+    the single pass, the latter with a ring of one tile."""
+    for (T, H, I, E, k, I_s, skew), mb in (((300, 384, 128, 1, 1, 128, None), None),
+                                           ((96, 128, 128, 64, 1, 128, 2.0), 1)):
+        inp = gen.make_layer_inputs(T, H, I, E, k, I_s, skew=skew, seed=12)
+        g = inp.to("cuda")
+        w = weights_of(g, mode)
+        ref = _run(g, E, w, mode)
+        ring = mb or _largest_padded(ref[2])
+        if mb:
+            cnt = ref[2].arrays()["cnt"].cpu().numpy()
+            if ((cnt + 127) // 128 * 128).max() > 128:
+                ring = _largest_padded(ref[2])
+            assert (cnt == 0).sum() > E // 2          # the routing leaves most experts empty
+        got = _run(g, E, w, mode, fwd_mb=ring, bwd_mb=ring)
+        _assert_same(got, ref)
