@@ -324,14 +324,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-__device__ __forceinline__ void store_bf16x32(void* dst, const float* v) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    d[q] = make_uint4(pack_bf16(v[8 * q + 0], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
-                      pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
-}
-
 __device__ __forceinline__ void pack_bf16x32(const float* v, uint32_t* w) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) w[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
@@ -396,12 +388,6 @@ __device__ __forceinline__ void load_raw64(const uint16_t* src, uint4* raw) {
   const uint4* s = reinterpret_cast<const uint4*>(src);
 #pragma unroll
   for (int q = 0; q < 4; ++q) raw[q] = __ldg(s + q);
-}
-
-__device__ __forceinline__ void zero_bytes64(void* dst) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) d[q] = make_uint4(0, 0, 0, 0);
 }
 
 __device__ __forceinline__ void load_bf16x32(const void* src, float* v) {
