@@ -101,6 +101,16 @@ typedef int mok_status_t;
                                         the default, which walks a group of row
                                         units inside each column tile so that the
                                         larger operand streams through L2 once) */
+#define MOK_DEBUG_STATIC_ORDER   64  /* give each CTA of the bf16 GEMMs the work
+                                        items idx, idx + grid, ... (same results).
+                                        By default the row GEMMs of long launches
+                                        (at least 200 work items per SM) hand out
+                                        the next item in line as a CTA starts one,
+                                        which keeps every CTA on neighbouring items
+                                        so that shared operands stay in L2 */
+#define MOK_DEBUG_TICKET_ORDER  128  /* hand out every TMA-fed bf16 GEMM's items
+                                        in line, whatever the launch's size (same
+                                        results; tests and comparison) */
 
 /* Stages of the layer, for optional per-stage timing events. */
 #define MOK_STAGE_FWD_PREP                 0  /* status hand-over; MXFP8: weight scales into the tensor-core layout */

@@ -20,6 +20,8 @@ MOK_MODE_MXFP8_FWD = 1
 MOK_MODE_MXFP8 = 2
 MOK_DEBUG_DROP_ACC_SIGNAL = 1
 MOK_DEBUG_TMA_GATHER4 = 2
+MOK_DEBUG_STATIC_ORDER = 64
+MOK_DEBUG_TICKET_ORDER = 128
 MOK_DISPATCH_AUTO = 0
 MOK_DISPATCH_PERMUTE = 1
 MOK_DISPATCH_FUSED = 2

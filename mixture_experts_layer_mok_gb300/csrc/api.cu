@@ -254,8 +254,15 @@ size_t carve_schedule(void* buf, int T, int k, int E, SchedLayout* L) {
 struct CtxExtra {  // forward scratch beyond the public context fields
   // MXFP8 mode: weight scales in the tensor-core scale layout
   uint8_t *wg_sc, *wu_sc, *wd_sc, *wsg_sc, *wsu_sc, *wsd_sc;
-  int32_t* view;   // macrobatch ring: the windows' schedule views
+  int32_t* view;      // macrobatch ring: the windows' schedule views
+  int32_t* tickets;   // work-item counters of the GEMM launches
 };
+
+// Work-item counters a call needs: one per TMA-fed GEMM launch, at most two
+// (forward) or four (backward) routed GEMMs per window, windows at most E,
+// plus the shared expert's.
+int fwd_tickets(int E) { return 8 + 2 * E; }
+int bwd_tickets(int E) { return 8 + 4 * E; }
 
 // ---------------------------------------------------------------- macrobatch ring
 // Rows of the ring for a macrobatch size: 0 (no ring: every schedule-order
@@ -327,6 +334,7 @@ size_t carve_ctx(void* buf, int T, int k, int E, int H, int I, int Is, int mode,
     }
   }
   if (ring) X->view = c.take<int32_t>(view_ints(mt, E));
+  X->tickets = c.take<int32_t>(fwd_tickets(E));
   return c.off + 256;
 }
 
@@ -341,7 +349,8 @@ struct BwdLayout {
   uint8_t *xT, *xT_sc, *xT_tok, *xT_tok_sc, *dguq, *dguq_sc, *dguT, *dguT_sc, *hwT, *hwT_sc;
   uint8_t *dgusq, *dgusq_sc, *dgusT, *dgusT_sc, *hsT, *hsT_sc;
   uint8_t *wtg_sc, *wtu_sc, *wtd_sc, *wtsg_sc, *wtsu_sc, *wtsd_sc;
-  int32_t* view;   // macrobatch ring: the windows' schedule views
+  int32_t* view;      // macrobatch ring: the windows' schedule views
+  int32_t* tickets;   // work-item counters of the GEMM launches
 };
 
 int tile_n(int N) { return (N % 256 == 0) ? 256 : 128; }
@@ -350,15 +359,28 @@ int tile_n(int N) { return (N % 256 == 0) ? 256 : 128; }
 // TMA-fed GEMMs, unless the caller turns them off.
 bool pair_on(const mok_config_t* cfg, int bn) { return bn == 256 && !(cfg->debug_flags & MOK_DEBUG_NO_CTA_PAIR); }
 
+// Work items per SM from which a row GEMM takes its items in ticket order.
+// Over a long launch the CTAs of the static order drift apart and the
+// operands they share fall out of L2 (at T=65536 the dgrad through gate/up
+// read 58 GB per launch that way, 19.5 GB in ticket order, and ran 3%
+// faster); on a short launch the hand-over of each item through the queue
+// costs more than that (T=4096: 5-10% slower).  The weight gradients keep
+// the static order at every size (in ticket order they read less but did
+// not run faster).
+constexpr long long kTicketItemsPerSm = 200;
+
 // One TMA-fed GEMM as CTA pairs or as single CTAs; items / pair_items bound
 // the work items of each form.
 template <int A, int B, int BN, int EPI>
 cudaError_t launch_tiles(const GemmMaps& m, const GemmParams& p, long long items, long long pair_items, bool pair,
                          int sms, cudaStream_t st) {
+  GemmParams q = p;
+  if (q.ticket_mode == 2 || (q.ticket_mode == 0 && !q.wgrad && items >= kTicketItemsPerSm * sms))
+    q.ticket = next_ticket();
   if constexpr (BN == 256) {
-    if (pair) return launch_gemm_pair<A, B, BN, EPI>(m, p, pair_items, st);
+    if (pair) return launch_gemm_pair<A, B, BN, EPI>(m, q, pair_items, st);
   }
-  return launch_gemm<A, B, BN, EPI>(m, p, items < sms ? static_cast<int>(items) : sms, st);
+  return launch_gemm<A, B, BN, EPI>(m, q, items < sms ? static_cast<int>(items) : sms, st);
 }
 
 // Pair work items: row tiles taken two at a time.
@@ -431,6 +453,7 @@ size_t carve_bwd(void* buf, int T, int k, int E, int H, int I, int Is, int mode,
     }
   }
   if (ring) L->view = c.take<int32_t>(view_ints(mt, E));
+  L->tickets = c.take<int32_t>(bwd_tickets(E));
   return c.off + 256;
 }
 
@@ -445,13 +468,19 @@ mok_status_t check_shapes(int T, int k, int E, int H, int I, int Is) {
 }
 
 // Work-item order: -1 lets the launch pick the L2-friendly order (see
-// resolve_item_order), -2 keeps the plain order (MOK_DEBUG_PLAIN_ORDER).
+// resolve_item_order), -2 keeps the plain order (MOK_DEBUG_PLAIN_ORDER);
+// MOK_DEBUG_STATIC_ORDER / MOK_DEBUG_TICKET_ORDER keep every launch off the
+// ticket counters / put every one on them.
 GemmParams base_params(const mok_config_t* cfg, const mok_schedule_t* s, int* status, int debug) {
   GemmParams p;
   memset(&p, 0, sizeof(p));
   const int order = (cfg && (cfg->debug_flags & MOK_DEBUG_PLAIN_ORDER)) ? -2 : -1;
   p.group = order;
   p.wg_col_outer = order;
+  p.ticket_mode = !cfg ? 0
+                  : (cfg->debug_flags & MOK_DEBUG_STATIC_ORDER) ? 1
+                  : (cfg->debug_flags & MOK_DEBUG_TICKET_ORDER) ? 2
+                                                                 : 0;
   p.topk = s ? s->k : 1;
   if (s) {
     p.header = s->header;
@@ -657,6 +686,20 @@ struct SideStream {
 };
 thread_local SideStream g_side[64];
 
+// The work-item counters of the calling thread's current forward or backward
+// call (zeroed at its start), handed out one per TMA-fed GEMM launch in
+// launch order; the scope ends with the call.
+struct TicketPool {
+  int32_t* base = nullptr;
+  int n = 0;
+  int used = 0;
+};
+thread_local TicketPool g_tickets;
+struct TicketScope {
+  TicketScope(int32_t* base, int n) { g_tickets = TicketPool{base, n, 0}; }
+  ~TicketScope() { g_tickets = TicketPool{}; }
+};
+
 mok_status_t side_stream(SideStream** out) {
   int dev = 0;
   MOK_CUDA(cudaGetDevice(&dev));
@@ -673,6 +716,12 @@ mok_status_t side_stream(SideStream** out) {
 }
 
 }  // namespace
+
+int* mok::next_ticket() {
+  if (!g_tickets.base || g_tickets.used >= g_tickets.n) return nullptr;
+  return g_tickets.base + g_tickets.used++;
+}
+
 
 // ---------------------------------------------------------------------------
 // Scratch for mok_schedule_noalloc: per-chunk expert histograms live in this
@@ -1738,6 +1787,8 @@ mok_status_t mok_forward(const mok_config_t* cfg, const uint16_t* x, const float
   if ((st = make_windows(s, ring, X.view, cs, &wins))) return st;
   *ctx = c;
   ctx->swiglu_limit = cfg->swiglu_limit;
+  MOK_CUDA(cudaMemsetAsync(X.tickets, 0, fwd_tickets(E) * sizeof(int32_t), cs));
+  TicketScope tickets(X.tickets, fwd_tickets(E));
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_PREP, 0, cs));
   MOK_CUDA(cudaMemsetAsync(ctx->status, 0, 8 * sizeof(int), cs));
   MOK_CUDA(launch_dependent(propagate_status_kernel, dim3(1), dim3(1), 0, cs, static_cast<const int*>(s->header),
@@ -1821,6 +1872,8 @@ mok_status_t mok_backward(const mok_config_t* cfg, const uint16_t* dy, const uin
   carve_bwd(ws, T, k, E, H, I, Is, ctx->mode, ring, &L);
   std::vector<Win> wins;
   if ((st = make_windows(s, ring, L.view, cs, &wins))) return st;
+  MOK_CUDA(cudaMemsetAsync(L.tickets, 0, bwd_tickets(E) * sizeof(int32_t), cs));
+  TicketScope tickets(L.tickets, bwd_tickets(E));
   if (mxb) return backward_mxfp8(cfg, dy, x, router_w, s, wins, ctx, w, dx, d_router_w, g, L, sms, cs);
   return backward_bf16(cfg, dy, x, router_w, s, wins, ctx, w, dx, d_router_w, g, L, sms, g4, cs);
 }

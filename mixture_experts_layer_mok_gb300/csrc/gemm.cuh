@@ -107,6 +107,9 @@ struct GemmParams {
   int split;         // EPI_WGRAD: first output row that goes to out1
   long long estride; // EPI_WGRAD: elements per expert in out0 / out1
   int* status;       // device status word
+  int* ticket;       // TMA-fed GEMMs: this launch's work-item counter (zeroed), NULL = the static order
+  int ticket_mode;   // 0: ticket order for long row GEMMs; 1: never (MOK_DEBUG_STATIC_ORDER);
+                     // 2: always (MOK_DEBUG_TICKET_ORDER)
   int debug;         // MOK_DEBUG_* flags
   float swiglu_limit;  // SwiGLU epilogues: 0 = plain; L > 0 clamps gate to <= L, up to [-L, L]
   // ---- gathered operands (gather warps): token-row tensors [T][ld]
@@ -483,6 +486,9 @@ struct GemmCfg {
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kBarBytes = 512;
   static constexpr int kEpiStageBytes = 4096;  // per epilogue warp: two 32-row x 64-byte blocks
+  // work items in ticket order (TMA-fed GEMMs): a ring of kQ item slots
+  static constexpr bool kDyn = !kHasLsu;
+  static constexpr int kQ = 8;
   static constexpr int kStagesFit = (227 * 1024 - 1024 - kBarBytes - kEpiWarps * kEpiStageBytes) / kStageBytes;
   static constexpr int kStages = kStagesFit > 16 ? 16 : kStagesFit;
   static constexpr int kTmemCols = 2 * BN;  // two accumulator buffers
@@ -561,6 +567,10 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI, PAIR>::kThreads
   uint64_t* done = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint64_t* qfull = done + 2;            // item queue: one arrival, the producer's
+  uint64_t* qempty = qfull + C::kQ;      // one arrival per consumer (the leader's counts both CTAs')
+  int* qslot = reinterpret_cast<int*>(qempty + C::kQ);
+  static_assert((2 * C::kStages + 7 + 2 * C::kQ) * 8 + 4 * C::kQ <= C::kBarBytes, "barrier region");
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -569,6 +579,37 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI, PAIR>::kThreads
   const int item0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   const int istep = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   auto item_at = [&](int idx, int bk) { return PAIR ? get_item_pair(p, idx, bk, rank) : get_item(p, idx, bk); };
+  // Work items come in a static order (item0, item0 + istep, ...), or, with a
+  // ticket counter, in ticket order: the leader's producer takes the next
+  // ticket as it starts an item, so that all CTAs work on neighbouring items
+  // and the operands they share stay in L2 (a static order lets the CTAs
+  // drift apart over a long launch).  It hands each item to the other roles
+  // (and the peer CTA) through the queue; -1 ends the sequence, -2 reports an
+  // aborted wait.  The debug signal drop keeps the static order.
+  const bool dyn = C::kDyn && p.ticket != nullptr && !(p.debug & 1);
+  auto queue_put = [&](int k, int idx) -> bool {   // the leader's producer, one lane
+    const int s = k % C::kQ;
+    if (!mbar_wait<PAIR>(&qempty[s], ((k / C::kQ) & 1) ^ 1, abort_flag, p.status)) return false;
+    qslot[s] = idx;
+    if (PAIR) st_shared_cluster(cluster_addr(&qslot[s], 1), idx);
+    mbar_arrive(&qfull[s]);
+    if (PAIR) mbar_arrive_cluster(cluster_addr(&qfull[s], 1));
+    return true;
+  };
+  auto queue_take = [&](int k) -> int {   // every other role, one lane
+    const int s = k % C::kQ;
+    // acquire at cluster scope only where the slot was written by the other
+    // CTA (the leader's own roles read what their producer wrote)
+    const bool ok = (PAIR && rank != 0) ? mbar_wait<true>(&qfull[s], (k / C::kQ) & 1, abort_flag, p.status)
+                                        : mbar_wait<false>(&qfull[s], (k / C::kQ) & 1, abort_flag, p.status);
+    if (!ok) return -2;
+    const int idx = *reinterpret_cast<volatile int*>(&qslot[s]);
+    if (PAIR && rank != 0)
+      mbar_arrive_cluster(cluster_addr(&qempty[s], 0));
+    else
+      mbar_arrive(&qempty[s]);
+    return idx;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -578,6 +619,12 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI, PAIR>::kThreads
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], (PAIR ? 2 : 1) * C::kEpiWarps);   // the leader's counts both CTAs' warps
+    }
+    for (int s = 0; s < C::kQ; ++s) {
+      mbar_init(&qfull[s], 1);
+      // the MMA issuer and the epilogue warps; a pair's leader also counts the
+      // peer's producer and epilogue warps
+      mbar_init(&qempty[s], PAIR ? 2 + 2 * C::kEpiWarps : 1 + C::kEpiWarps);
     }
     mbar_init(done, 1);
     *abort_flag = 0;
@@ -614,7 +661,43 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI, PAIR>::kThreads
     uint32_t phase = 0;
     long long fills = 0;
     bool ok = true;
-    for (int idx = item0; idx < nitems && ok; idx += istep) {
+    const bool lead = !PAIR || rank == 0;
+    // the leader publishes items kAhead ahead of the one it loads, so that the
+    // other roles (and the peer's producer) find the next item waiting; its
+    // next ticket is taken as soon as one is published
+    constexpr int kAhead = 2;
+    static_assert(kAhead < C::kQ, "a published slot is read back before it is reused");
+    int ticket = 0, pub = 0;
+    bool pub_end = false;
+    if (dyn && lane == 0 && lead) ticket = atomicAdd(p.ticket, 1);
+    for (int k = 0, sidx = item0;; ++k, sidx += istep) {
+      int idx = sidx;
+      if (dyn) {
+        int v = 0;
+        if (lane == 0) {
+          if (lead) {
+            bool put = true;
+            while (put && !pub_end && pub <= k + kAhead) {
+              const int pv = ticket < nitems ? ticket : -1;
+              put = queue_put(pub, pv);
+              if (!put) break;
+              if (pv >= 0)
+                ticket = atomicAdd(p.ticket, 1);
+              else
+                pub_end = true;
+              ++pub;
+            }
+            v = put ? *reinterpret_cast<volatile int*>(&qslot[k % C::kQ]) : -2;
+          } else {
+            v = queue_take(k);
+          }
+        }
+        idx = __shfl_sync(0xffffffffu, v, 0);
+        if (idx == -2) ok = false;
+        if (idx < 0) break;
+      } else if (idx >= nitems) {
+        break;
+      }
       const Item it = item_at(idx, C::kBK);
       const int bn_out = (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_MX) ? BN / 2 : BN;
       const int n0 = it.nt * bn_out;
@@ -718,6 +801,7 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI, PAIR>::kThreads
             ktok[i] = token_of(p, it.kbeg + (kb + 1) * kBK + 4 * (lane & 15) + i);
         }
       }
+      if (!ok) break;
     }
     if (!ok && lane == 0 && (!PAIR || rank == 0)) {
       // drain: wait until every load issued into a stage has landed (a CTA
@@ -741,7 +825,14 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI, PAIR>::kThreads
       int abuf = 0;
       uint32_t aphase = 0;
       bool first = true;
-      for (int idx = item0; idx < nitems; idx += istep) {
+      for (int k = 0, sidx = item0;; ++k, sidx += istep) {
+        int idx = sidx;
+        if (dyn) {
+          idx = queue_take(k);
+          if (idx < 0) break;
+        } else if (idx >= nitems) {
+          break;
+        }
         const int nk = item_nk(p, idx, C::kBK, PAIR);
         if (nk == 0) continue;
         if (!mbar_wait(&tempty[abuf], aphase ^ 1, abort_flag, p.status)) break;
@@ -914,7 +1005,16 @@ __global__ void __launch_bounds__(GemmCfg<A_SRC, B_SRC, BN, EPI, PAIR>::kThreads
         row = t.e * (p.m_tiles * kBM - p.split) + (mblock - p.split);
       }
     };
-    for (int idx = item0; idx < nitems; idx += istep) {
+    for (int k = 0, sidx = item0;; ++k, sidx += istep) {
+      int idx = sidx;
+      if (dyn) {
+        int v = 0;
+        if (lane == 0) v = queue_take(k);
+        idx = __shfl_sync(0xffffffffu, v, 0);
+        if (idx < 0) break;
+      } else if (idx >= nitems) {
+        break;
+      }
       const Item it = item_at(idx, C::kBK);
       const int bn_out = (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_MX) ? BN / 2 : BN;
       const int n0 = it.nt * bn_out;

@@ -34,6 +34,7 @@ cudaError_t launch_gemm(const GemmMaps& maps, const GemmParams& p, int grid, cud
   cfg.numAttrs = 1;
   GemmParams q = p;
   resolve_item_order(q, false);
+  if (!C::kDyn) q.ticket = nullptr;
   err = cudaLaunchKernelEx(&cfg, kern, maps, q);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
@@ -82,6 +83,7 @@ cudaError_t launch_gemm_pair(const GemmMaps& maps, const GemmParams& p, long lon
   cfg.numAttrs = 2;
   GemmParams q = p;
   resolve_item_order(q, true);
+  if (!C::kDyn) q.ticket = nullptr;
   err = cudaLaunchKernelEx(&cfg, kern, maps, q);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();

@@ -82,6 +82,12 @@ cudaError_t launch_window_view(const int* cnt, const int* row0, const int* heade
                                int* wheader, cudaStream_t st);
 cudaError_t launch_dw_reduce(const float* part, int nf, int ntiles, float* dw, cudaStream_t st);
 
+// The next work-item counter (one int, zeroed) of the calling thread's current
+// forward or backward call, or NULL outside one or once the call's counters
+// are used up: a TMA-fed GEMM launch given one takes its work items in
+// ticket order, else in the static order.
+int* next_ticket();
+
 // Grouped GEMM launch: instantiated for the operand sources / tile widths /
 // epilogues the layer uses (gemm_fwd.cu, gemm_bwd.cu).
 template <int A_SRC, int B_SRC, int BN, int EPI>

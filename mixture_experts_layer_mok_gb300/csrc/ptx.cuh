@@ -59,17 +59,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same with acquire semantics at cluster scope: for a phase completed by
+// arrivals of the other CTA of a pair that release data written into this
+// CTA's shared memory (or read from it) across the cluster.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity.  Returns false when the
 // CTA's abort flag is raised or the wait limit expires (which raises it and
 // records MOK_ERR_TIMEOUT in the device status word).
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           volatile int* abort_flag, int* status) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto ready = [&]() { return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+  if (ready()) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+      if (ready()) return true;
     if (*abort_flag) return false;
     if (global_timer_ns() - t0 > kWaitLimitNs) {
       *abort_flag = 1;
@@ -219,6 +236,10 @@ __device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
 // Arrive once on an mbarrier given by its cluster address.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+// Store a 32-bit word at a cluster shared-memory address (another CTA's).
+__device__ __forceinline__ void st_shared_cluster(uint32_t addr, int v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),

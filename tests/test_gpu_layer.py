@@ -267,23 +267,26 @@ def test_cta_pairs_match_single_ctas_bitwise(name, mode):
                                        ("ragged_shared", "mxfp8_full")])
 def test_item_order_changes_no_bit(name, mode):
     """Each GEMM output tile has one owner and a fixed K order, so the order in
-    which the persistent CTAs visit the tiles (the default grouped order, or
-    32 = MOK_DEBUG_PLAIN_ORDER) changes no output bit."""
+    which the persistent CTAs visit the tiles changes no output bit: the
+    default grouped order, 32 = MOK_DEBUG_PLAIN_ORDER, 64 =
+    MOK_DEBUG_STATIC_ORDER, 128 = MOK_DEBUG_TICKET_ORDER (every CTA takes the
+    next item in line through the work-item queue), and combinations."""
     m = mok()
     inp = _inputs(name, seed=13)
     g = inp.to("cuda")
     sched = m.schedule(g.top_experts, inp.meta["E"], 0.5)
     w = weights_of(g, mode)
     outs = []
-    for flags in (0, 32):
+    for flags in (0, 32, 64, 128, 160):
         y, ctx = m.forward(g.x, g.router_w, sched, w, mode=mode, debug=flags)
         grads = m.backward(g.dy, g.x, g.router_w, sched, ctx, w, debug=flags)
         torch.cuda.synchronize()
         assert ctx.status() == 0
         outs.append((y.clone(), {kk: v.clone() for kk, v in grads.items()}))
-    assert torch.equal(outs[0][0], outs[1][0])
-    for key in outs[0][1]:
-        assert torch.equal(outs[0][1][key], outs[1][1][key]), key
+    for other in outs[1:]:
+        assert torch.equal(outs[0][0], other[0])
+        for key in outs[0][1]:
+            assert torch.equal(outs[0][1][key], other[1][key]), key
 
 
 def test_fused_forward_permuted_backward_mix():
