@@ -104,6 +104,8 @@ def launches_per_step(c, windows=1, ring=False):
         n += 3 + (3 if shared else 0)       # weight prequantisation (every step)
         n += 1                              # weight scales into the tensor-core layout (one launch)
     n += W                                  # x into schedule order (MXFP8: quantised, token order too)
+    if mx:
+        n += W                              # and its scales into the tensor-core layout
     if full:                                # (the prequantisation above writes both weight copies)
         n += 1                              # transposed weights' scales into the tensor-core layout
         n += 2 * W + (2 if shared else 0)   # x transposed; dy rows + transposed (schedule, token order)

@@ -256,6 +256,7 @@ struct CtxExtra {  // forward scratch beyond the public context fields
   uint8_t *wg_sc, *wu_sc, *wd_sc, *wsg_sc, *wsu_sc, *wsd_sc;
   int32_t* view;      // macrobatch ring: the windows' schedule views
   int32_t* tickets;   // work-item counters of the GEMM launches
+  uint8_t* xs;        // MXFP8 modes: the dispatch's scales of x, row-major [T][H/32]
 };
 
 // Work-item counters a call needs: one per TMA-fed GEMM launch, at most two
@@ -310,6 +311,7 @@ size_t carve_ctx(void* buf, int T, int k, int E, int H, int I, int Is, int mode,
     if (mode == MOK_MODE_MXFP8_FWD && !ring) ctx->x_perm = c.take<uint16_t>(mr * H);
     ctx->xq = c.take<uint8_t>(static_cast<long long>(T) * H);
     ctx->xq_sc = c.take<uint8_t>(tiled_scale_bytes(T, H));
+    X->xs = c.take<uint8_t>(static_cast<long long>(T) * (H / 32));
     ctx->xq_perm = c.take<uint8_t>(rr * H);
     ctx->xq_perm_sc = c.take<uint8_t>(tiled_scale_bytes(rr, H));
     ctx->hq = c.take<uint8_t>(rr * I);
@@ -935,9 +937,11 @@ mok_status_t forward_mxfp8(const mok_config_t* cfg, const uint16_t* x, const flo
   // gradient reads (a separate copy would contend for HBM with whichever GEMM
   // it overlapped).  Later windows skip the token-order copy.
   auto dispatch = [&](const Win& v, bool tokens) {
-    return launch_mx_dispatch(x, T, H, k, s->slot_row, s->row_src, s->header, v.r0, v.rows,
-                              tokens ? ctx->xq : nullptr, ctx->xq_sc, ctx->xq_perm, ctx->xq_perm_sc, ctx->x_perm, sms,
-                              cs);
+    cudaError_t e = launch_mx_dispatch(x, T, H, k, s->slot_row, s->row_src, s->header, v.r0, v.rows,
+                                       tokens ? ctx->xq : nullptr, X.xs, ctx->xq_perm, ctx->x_perm, sms, cs);
+    if (e != cudaSuccess) return e;
+    return launch_mx_scale_gather(X.xs, T, H, k, s->row_src, s->header, v.r0, v.rows, ctx->xq_perm_sc,
+                                  tokens ? ctx->xq_sc : nullptr, cs);
   };
   MOK_CUDA(mark(cfg, MOK_STAGE_FWD_DISPATCH, 0, cs));
   if (nw > 0) MOK_CUDA(dispatch(wins[0], true));

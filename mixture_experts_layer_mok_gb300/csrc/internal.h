@@ -39,12 +39,16 @@ cudaError_t launch_schedule(const int64_t* te, int T, int k, int E, int cap_tile
                             int* header, cudaStream_t st);
 cudaError_t launch_mx_quantize(const uint16_t* x, long long nblocks, uint8_t* codes, uint8_t* scales,
                                int num_sms, cudaStream_t st);
-// Schedule rows [w0, w0 + wrows) go to rows from 0 of xp / xp_sc (and xb);
-// xq (may be NULL, then xq_sc is unused): the token-order copy; xb (may be
-// NULL): also x's bf16 rows in schedule order (padding rows zero).
+// Schedule rows [w0, w0 + wrows) go to rows from 0 of xp (and xb); xq (may be
+// NULL): the token-order copy, with the scales row-major in xs ([T][H/32]);
+// xb (may be NULL): also x's bf16 rows in schedule order (padding rows zero).
 cudaError_t launch_mx_dispatch(const uint16_t* x, int T, int H, int topk, const int* slot_row, const int* row_src,
-                               const int* header, long long w0, long long wrows, uint8_t* xq, uint8_t* xq_sc,
-                               uint8_t* xp, uint8_t* xp_sc, uint16_t* xb, int num_sms, cudaStream_t st);
+                               const int* header, long long w0, long long wrows, uint8_t* xq, uint8_t* xs,
+                               uint8_t* xp, uint16_t* xb, int num_sms, cudaStream_t st);
+// The dispatch's scales xs into the tensor-core scale layout: the window's
+// schedule rows into xp_sc, and token order into xq_sc (may be NULL).
+cudaError_t launch_mx_scale_gather(const uint8_t* xs, int T, int H, int topk, const int* row_src, const int* header,
+                                   long long w0, long long wrows, uint8_t* xp_sc, uint8_t* xq_sc, cudaStream_t st);
 cudaError_t launch_mx_quantize_t(const uint16_t* src, long long ld, int batch, int R, int C, int valid_rows,
                                  const int* row_src, int topk, const int* header, uint8_t* codes, uint8_t* scales,
                                  int tiled, int num_sms, cudaStream_t st, uint8_t* rcodes = nullptr,

@@ -457,20 +457,22 @@ cudaError_t launch_mx_quantize(const uint16_t* x, long long nblocks, uint8_t* co
 // scales, OCP MX v1.0 blocks of 32) and written to its own row of the
 // token-order copy (the shared expert's operand) and to the k schedule rows
 // that route it (the routed experts' operand: MoK's dispatch exchange, done on
-// one GPU as a write into schedule order).  Scales go straight into the
-// tensor-core scale layout.  Padding rows of the schedule get zero codes and
-// unit scales; so do the scales of the token-order copy's last partial
-// 128-row block.  Only the schedule rows of the window [w0, w0 + wrows) are
+// one GPU as a write into schedule order).  Padding rows of the schedule get
+// zero codes.  Only the schedule rows of the window [w0, w0 + wrows) are
 // written, at row p - w0 (the whole schedule is the window [0, max_rows); a
 // macrobatch ring passes one window of experts at a time), and the
-// token-order copy only when xq is not NULL.  One warp per job: tokens, then
-// the window's schedule rows, then the tail.
+// token-order copy only when xq is not NULL.  The scales go, with the
+// token-order copy, to xs: row-major [T][H/32], every store a whole 32-byte
+// sector; mx_scale_gather_kernel lays them out for the GEMMs.  (Stored from
+// here into the tensor-core layout, each 4-byte scale word would share its
+// sector with seven rows of other tokens written at other times, and every
+// partly written sector that L2 evicts costs a read-modify-write.)  One warp
+// per job: tokens, then the window's schedule rows.
 // ===========================================================================
 __global__ void __launch_bounds__(256, 3) mx_dispatch_kernel(
     const uint16_t* __restrict__ x, int T, int H, int topk, const int* __restrict__ slot_row,
     const int* __restrict__ row_src, const int* __restrict__ header, long long w0, long long wrows,
-    uint8_t* __restrict__ xq, uint8_t* __restrict__ xq_sc, uint8_t* __restrict__ xp, uint8_t* __restrict__ xp_sc,
-    uint16_t* __restrict__ xb) {
+    uint8_t* __restrict__ xq, uint8_t* __restrict__ xs, uint8_t* __restrict__ xp, uint16_t* __restrict__ xb) {
   griddep_wait();
   griddep_launch_dependents();
   if (header[2] != 0) return;
@@ -484,9 +486,7 @@ __global__ void __launch_bounds__(256, 3) mx_dispatch_kernel(
   const long long P = header[1];
   const int lane = threadIdx.x & 31;
   const int nb = H / 32;             // blocks per row (a multiple of 4)
-  const int cg = H / 128;            // column groups of the scale layout
-  const long long t_pad = (static_cast<long long>(T) + 127) / 128 * 128;
-  const long long jobs = T + wrows + (xq ? t_pad - T : 0);
+  const long long jobs = T + wrows;
   for (long long j = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5; j < jobs;
        j += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
     if (j < T) {
@@ -516,11 +516,6 @@ __global__ void __launch_bounds__(256, 3) mx_dispatch_kernel(
         uint8_t codes[32];
         uint32_t sc = 127;
         if (act) sc = mx_quantize32(v, codes);
-        // the 4 scales of an aligned group of blocks form one 32-bit word
-        const uint32_t s1 = __shfl_down_sync(0xffffffffu, sc, 1);
-        const uint32_t s2 = __shfl_down_sync(0xffffffffu, sc, 2);
-        const uint32_t s3 = __shfl_down_sync(0xffffffffu, sc, 3);
-        const uint32_t word = sc | (s1 << 8) | (s2 << 16) | (s3 << 24);
         if (act) {
           uint4* sw = reinterpret_cast<uint4*>(wst + lane * 32);
           sw[0] = reinterpret_cast<const uint4*>(codes)[0];
@@ -542,7 +537,13 @@ __global__ void __launch_bounds__(256, 3) mx_dispatch_kernel(
           uint4* d = reinterpret_cast<uint4*>(xq + t * H + off);
           if (16 * lane < bytes) d[lane] = q0;
           if (16 * (lane + 32) < bytes) d[lane + 32] = q1;
-          if (act && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(xq_sc + mx_tiled_scale_offset(t, b, cg)) = word;
+          // the chunk's scale bytes, 4 per word from every fourth lane: one
+          // store of up to 32 contiguous bytes
+          const uint32_t s1 = __shfl_down_sync(0xffffffffu, sc, 1);
+          const uint32_t s2 = __shfl_down_sync(0xffffffffu, sc, 2);
+          const uint32_t s3 = __shfl_down_sync(0xffffffffu, sc, 3);
+          if (act && (lane & 3) == 0)
+            *reinterpret_cast<uint32_t*>(xs + t * nb + b) = sc | (s1 << 8) | (s2 << 16) | (s3 << 24);
         }
         for (int jj = 0; jj < topk; ++jj) {   // all lanes take part in the shuffle
           const long long pr = __shfl_sync(0xffffffffu, jj < 32 ? p_lo : p_hi, jj & 31) - w0;
@@ -550,7 +551,6 @@ __global__ void __launch_bounds__(256, 3) mx_dispatch_kernel(
           uint4* dp = reinterpret_cast<uint4*>(xp + static_cast<long long>(pr) * H + off);
           if (16 * lane < bytes) dp[lane] = q0;
           if (16 * (lane + 32) < bytes) dp[lane + 32] = q1;
-          if (act && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(xp_sc + mx_tiled_scale_offset(pr, b, cg)) = word;
           if (xb) {   // the chunk's bf16 bytes: its piece i (16 bytes) is piece
                       // (i % 4) ^ ((i / 4) % 4) of block i / 4 in the staging layout
             uint4* db = reinterpret_cast<uint4*>(xb + static_cast<long long>(pr) * H + off);
@@ -563,7 +563,7 @@ __global__ void __launch_bounds__(256, 3) mx_dispatch_kernel(
         }
         __syncwarp();   // the staging is read before the next chunk overwrites it
       }
-    } else if (j < T + wrows) {
+    } else {
       const long long pr = j - T;
       if (w0 + pr >= P || __ldg(row_src + w0 + pr) >= 0) continue;
       uint4* d = reinterpret_cast<uint4*>(xp + pr * H);
@@ -572,22 +572,87 @@ __global__ void __launch_bounds__(256, 3) mx_dispatch_kernel(
         uint4* db = reinterpret_cast<uint4*>(xb + pr * H);
         for (int i = lane; i < H / 8; i += 32) db[i] = make_uint4(0, 0, 0, 0);
       }
-      for (int g = lane; g < cg; g += 32)
-        *reinterpret_cast<uint32_t*>(xp_sc + mx_tiled_scale_offset(pr, 4 * g, cg)) = 0x7F7F7F7Fu;
-    } else {
-      const long long tr = T + (j - T - wrows);
-      for (int g = lane; g < cg; g += 32)
-        *reinterpret_cast<uint32_t*>(xq_sc + mx_tiled_scale_offset(tr, 4 * g, cg)) = 0x7F7F7F7Fu;
     }
   }
 }
 
 cudaError_t launch_mx_dispatch(const uint16_t* x, int T, int H, int topk, const int* slot_row, const int* row_src,
-                               const int* header, long long w0, long long wrows, uint8_t* xq, uint8_t* xq_sc,
-                               uint8_t* xp, uint8_t* xp_sc, uint16_t* xb, int num_sms, cudaStream_t st) {
-  const long long jobs = T + wrows + (xq ? (static_cast<long long>(T) + 127) / 128 * 128 - T : 0);
+                               const int* header, long long w0, long long wrows, uint8_t* xq, uint8_t* xs,
+                               uint8_t* xp, uint16_t* xb, int num_sms, cudaStream_t st) {
+  const long long jobs = T + wrows;
   cudaError_t err = launch_dependent(mx_dispatch_kernel, dim3(grid_for(jobs * 32, 256, num_sms)), dim3(256), 0, st, x,
-                                     T, H, topk, slot_row, row_src, header, w0, wrows, xq, xq_sc, xp, xp_sc, xb);
+                                     T, H, topk, slot_row, row_src, header, w0, wrows, xq, xs, xp, xb);
+  if (err != cudaSuccess) return err;
+  return cudaGetLastError();
+}
+
+// ===========================================================================
+// The dispatch's scales, row-major by token (xs [T][H/32]), into the
+// tensor-core scale layout (mx_tiled_scale_offset): for the window's schedule
+// rows [w0, w0 + wrows) at rows from 0 of xp_sc (a row takes its token's
+// scales; padding rows and rows from P on unit scales), and, when xq_sc is not
+// NULL, for token order (rows from T on: unit scales).  One block of 128
+// threads per 128-row block, 32 column groups (one 128-byte piece of each
+// source row) per pass: warp w reads rows 32 w .. 32 w + 31, one whole piece
+// per load, into a shared-memory tile of the pass's 512-byte atoms (stride
+// 129 words: no bank conflicts), and the block then stores the atoms whole.
+// ===========================================================================
+__global__ void __launch_bounds__(128) mx_scale_gather_kernel(const uint8_t* __restrict__ xs, int T, int nb, int topk,
+                                                              const int* __restrict__ row_src,
+                                                              const int* __restrict__ header, long long w0,
+                                                              long long wrows, uint8_t* __restrict__ xp_sc,
+                                                              uint8_t* __restrict__ xq_sc) {
+  griddep_wait();
+  griddep_launch_dependents();
+  if (header[2] != 0) return;
+  constexpr int kChunk = 32;                    // column groups (scale words of a row) per pass
+  constexpr int kStride = 129;                  // words per atom in shared memory
+  __shared__ uint32_t sw[kChunk * kStride];
+  const long long P = header[1];
+  const int cg = nb / 4;
+  const long long sgroups = wrows / 128;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  long long g = blockIdx.x;
+  long long src = -1;                           // the token of row 32 warp + lane
+  uint32_t* out;
+  if (g < sgroups) {
+    const long long p = w0 + 128 * g + 32 * warp + lane;
+    const int rs = p < P ? __ldg(row_src + p) : -1;
+    if (rs >= 0) src = rs / topk;
+    out = reinterpret_cast<uint32_t*>(xp_sc);
+  } else {
+    g -= sgroups;
+    const long long t = 128 * g + 32 * warp + lane;
+    if (t < T) src = t;
+    out = reinterpret_cast<uint32_t*>(xq_sc);
+  }
+  out += g * cg * 128;
+  const uint32_t* xw = reinterpret_cast<const uint32_t*>(xs);
+  const int words = nb / 4;                     // scale words per source row
+  for (int c0 = 0; c0 < cg; c0 += kChunk) {
+    const int nc = min(kChunk, cg - c0);
+    uint32_t v[32];
+#pragma unroll
+    for (int l = 0; l < 32; ++l) {              // row 32 warp + l: lane c loads its word c0 + c
+      const long long sl = __shfl_sync(0xffffffffu, src, l);
+      v[l] = (sl >= 0 && lane < nc) ? __ldg(xw + sl * words + c0 + lane) : 0x7F7F7F7Fu;
+    }
+    // row r sits at word (r % 32) * 4 + r / 32 of its atom
+#pragma unroll
+    for (int l = 0; l < 32; ++l)
+      if (lane < nc) sw[lane * kStride + l * 4 + warp] = v[l];
+    __syncthreads();
+    for (int c = 0; c < nc; ++c) out[static_cast<long long>(c0 + c) * 128 + threadIdx.x] = sw[c * kStride + threadIdx.x];
+    __syncthreads();
+  }
+}
+
+cudaError_t launch_mx_scale_gather(const uint8_t* xs, int T, int H, int topk, const int* row_src, const int* header,
+                                   long long w0, long long wrows, uint8_t* xp_sc, uint8_t* xq_sc, cudaStream_t st) {
+  const long long blocks = wrows / 128 + (xq_sc ? (static_cast<long long>(T) + 127) / 128 : 0);
+  if (blocks == 0) return cudaSuccess;
+  cudaError_t err = launch_dependent(mx_scale_gather_kernel, dim3(static_cast<unsigned>(blocks)), dim3(128), 0, st, xs,
+                                     T, H / 32, topk, row_src, header, w0, wrows, xp_sc, xq_sc);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
