@@ -21,10 +21,13 @@ SHAPES = {
     "one_expert": (300, 384, 128, 1, 1, 128, None),
     "wide": (520, 512, 256, 12, 6, 384, 1.2),
 }
+# a deep H for the MXFP8 dispatch's scales only: 132 blocks of 32 a row (not a
+# whole number of 32-block chunks) in 33 column groups of the scale layout
+EXTRA_SHAPES = {"deep_h": (300, 4224, 128, 4, 2, 128, None)}
 
 
 def _inputs(name, seed=0):
-    T, H, I, E, k, I_s, skew = SHAPES[name]
+    T, H, I, E, k, I_s, skew = SHAPES[name] if name in SHAPES else EXTRA_SHAPES[name]
     inp = gen.make_layer_inputs(T, H, I, E, k, I_s, skew=skew, seed=seed)
     inp.meta.update(name=name)
     return inp
@@ -326,7 +329,7 @@ def _untile_scales(tiled, rows, K):
     return out
 
 
-@pytest.mark.parametrize("name", ["ragged_shared", "skewed"])
+@pytest.mark.parametrize("name", ["ragged_shared", "skewed", "deep_h"])
 def test_mxfp8_dispatch_codes_and_scales_bit_exact(name):
     """The MXFP8 forward's quantise-and-dispatch step: x's E4M3 codes and E8M0
     scales in token order and in schedule order equal the oracle's quantiser,
