@@ -843,33 +843,47 @@ cudaError_t launch_mx_quantize_t(const uint16_t* src, long long ld, int batch, i
 // to kMaxScaleJobs matrices in one launch (a forward or a backward needs six;
 // separate launches would each wait for the last).  One block per (128-row
 // block of one job, 16 column groups): coalesced row reads into shared memory,
-// coalesced atom writes out of it.
+// coalesced atom writes out of it.  The blocks of one 128-row block are
+// neighbours in the grid, so that the pieces of a row they read share its
+// L2 lines while those are resident (in row-block order the lines came from
+// DRAM once per block).
 struct TileScaleJobs {
   const uint8_t* src[kMaxScaleJobs];
   uint8_t* dst[kMaxScaleJobs];
   int K[kMaxScaleJobs];
   int gate_up[kMaxScaleJobs];   // 0: row r -> row r; 1 / 2: gate / up rows into the interleaved layout
   int group[kMaxScaleJobs];     // rows per expert of an interleaved job
-  int rb0[kMaxScaleJobs + 1];   // job j owns blocks [rb0[j], rb0[j+1]) of grid.x
+  int rb0[kMaxScaleJobs + 1];   // job j owns 128-row blocks [rb0[j], rb0[j+1])
   int n;
+  int ny;                       // blocks per 128-row block (16 column groups each)
 };
 
 __global__ void __launch_bounds__(256) mx_tile_scales_kernel(const __grid_constant__ TileScaleJobs J) {
   griddep_wait();
   griddep_launch_dependents();
   __shared__ uint32_t tile[128][17];
+  const int xb = static_cast<int>(blockIdx.x / J.ny);   // 128-row block over all jobs
   int j = 0;
-  while (j + 1 < J.n && static_cast<int>(blockIdx.x) >= J.rb0[j + 1]) ++j;
+  while (j + 1 < J.n && xb >= J.rb0[j + 1]) ++j;
   const int cg = J.K[j] / 128;
-  const int g0 = blockIdx.y * 16;
-  if (g0 >= cg) return;   // this job has fewer column groups than the grid's y extent
-  const long long rb = static_cast<long long>(blockIdx.x) - J.rb0[j];
+  const int g0 = static_cast<int>(blockIdx.x % J.ny) * 16;
+  if (g0 >= cg) return;   // this job has fewer column groups than the widest one
+  const long long rb = xb - J.rb0[j];
   const int ng = min(16, cg - g0);
   const uint32_t* s = reinterpret_cast<const uint32_t*>(J.src[j]);  // one word = one column group of a row
   uint8_t* dst = J.dst[j];
-  for (int i = threadIdx.x; i < 128 * 16; i += 256) {
-    const int row = i >> 4, g = i & 15;
-    if (g < ng) tile[row][g] = __ldg(s + (rb * 128 + row) * cg + g0 + g);
+  // all eight loads of a thread in flight before any of them is stored (one
+  // at a time, the block's 8 KB took several memory latencies)
+  uint32_t v[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int i = threadIdx.x + 256 * q, row = i >> 4, g = i & 15;
+    v[q] = g < ng ? __ldg(s + (rb * 128 + row) * cg + g0 + g) : 0u;
+  }
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int i = threadIdx.x + 256 * q;
+    tile[i >> 4][i & 15] = v[q];
   }
   __syncthreads();
   if (J.gate_up[j] == 0) {
@@ -916,10 +930,12 @@ cudaError_t launch_mx_tile_scales(const MxTileScaleJob* jobs, int n, cudaStream_
     ++m;
   }
   if (m == 0) return cudaSuccess;
+  if (total * ymax > 0x7fffffffll) return cudaErrorInvalidValue;
   J.rb0[m] = static_cast<int>(total);
   J.n = m;
-  cudaError_t err = launch_dependent(mx_tile_scales_kernel, dim3(static_cast<unsigned>(total),
-                                     static_cast<unsigned>(ymax)), dim3(256), 0, st, J);
+  J.ny = ymax;
+  cudaError_t err = launch_dependent(mx_tile_scales_kernel, dim3(static_cast<unsigned>(total * ymax)), dim3(256), 0,
+                                     st, J);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
