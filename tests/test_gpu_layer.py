@@ -21,8 +21,9 @@ SHAPES = {
     "one_expert": (300, 384, 128, 1, 1, 128, None),
     "wide": (520, 512, 256, 12, 6, 384, 1.2),
 }
-# a deep H for the MXFP8 dispatch's scales only: 132 blocks of 32 a row (not a
-# whole number of 32-block chunks) in 33 column groups of the scale layout
+# a deep H for the MXFP8 paths: 132 blocks of 32 a row (not a whole number of
+# 32-block chunks) in 33 column groups of the scale layout (more than one pass
+# of the scale layouts' 16- and 32-group loops)
 EXTRA_SHAPES = {"deep_h": (300, 4224, 128, 4, 2, 128, None)}
 
 
@@ -43,7 +44,7 @@ def test_bf16_forward_backward_matches_oracle(name):
     assert not bad, errs
 
 
-@pytest.mark.parametrize("name", list(SHAPES))
+@pytest.mark.parametrize("name", list(SHAPES) + ["deep_h"])
 def test_mxfp8_forward_matches_same_quantisation_oracle(name):
     inp = _inputs(name, seed=1)
     y, grads, sched, ctx = run_layer(inp, "mxfp8")
@@ -60,7 +61,7 @@ def test_mxfp8_forward_matches_same_quantisation_oracle(name):
     assert rel_l2(y, y_unq) <= max(MX_UNQ_TOL, intrinsic + BF16_TOL), (rel_l2(y, y_unq), intrinsic)
 
 
-@pytest.mark.parametrize("name", list(SHAPES))
+@pytest.mark.parametrize("name", list(SHAPES) + ["deep_h"])
 def test_mxfp8_full_backward_matches_same_quantisation_oracle(name):
     """MXFP8 forward and backward: every backward GEMM on block-scaled E4M3
     operands, against the oracle that quantises the same operands along the
